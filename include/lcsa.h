@@ -1,0 +1,222 @@
+/*
+ * lcsa.h -- C ABI of the hybrid compressed attention library (CSA / HCA), sm_103a.
+ *
+ * The operations follow the description of DeepSeek-V4's hybrid attention on the page
+ * m.x-techcon.com/article/133366, section "2. 核心技术创新：混合压缩注意力":
+ *   CSA step 1  compress every m raw KV rows into one entry (learned per-token score plus a
+ *               positional bias, softmax-normalised weights, weighted sum; adjacent blocks
+ *               overlap)                                          -> csa_compress
+ *   CSA step 2  a low-rank lightning indexer scores every entry; each query keeps its top-k
+ *                                                                 -> csa_index_topk
+ *   CSA step 3  shared-KV multi-query attention over the selected entries together with the
+ *               most recent 128 uncompressed tokens               -> csa_attend
+ *   HCA         m' = 128 compression, no selection, dense attention over every entry plus the
+ *               same window                                      -> hca_compress, hca_attend
+ * and, on the same page, the efficiency paragraph (RoPE dims BF16, the rest FP8; indexer QK
+ * path FP4) and section 4 (state cache for the window and the uncompressed tail; compressed
+ * cache allocated in blocks of LCM(4,128) = 128 raw tokens).
+ *
+ * Conventions for every entry point
+ *  - Pointers marked "device" are CUDA device pointers; "host" are host pointers.  Every
+ *    buffer is owned by the caller.  The library allocates nothing, frees nothing, never
+ *    synchronises and keeps no pointer after a call returns.  It is stateless and reentrant.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).  Calls
+ *    enqueue kernels and return; results are ready once the stream reaches them.
+ *  - Argument errors are reported synchronously by the return value (nothing is launched).
+ *    Errors found on the device (a block id or an index outside its buffer) are written to
+ *    `*dev_status` (device int32, may be NULL) with atomicCAS(status, 0, code): the first code
+ *    wins, the offending row is skipped, the kernel never traps.  Read it after the stream.
+ *  - Launch failures return LCS_ERR_CUDA.
+ *  - Results are deterministic: identical inputs give identical bits, independent of the
+ *    other sequences in the batch.
+ *
+ * Row format.  A KV row has D dims in the order [rope(64) | nope(D-64)].
+ *  LCS_ROW_FP8_SPLIT: rope dims BF16 (64 x 2 bytes), nope dims FP8 E4M3 (D-64 bytes) with one
+ *    fp32 scale per row: value = code * scale; scale = fp32(amax)/448 over the nope dims (1 for
+ *    an all-zero row); codes round to nearest even and saturate at +-448.  580 bytes at D=512.
+ *  LCS_ROW_BF16: all D dims BF16.
+ *  A row set (lcs_rows) stores row i at nope + i*(D-64) (FP8) or nope + i*D*2 (BF16),
+ *  rope + i*128, scale + i.
+ */
+#ifndef LCSA_H_
+#define LCSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define LCSA_ABI_VERSION 1
+#define LCSA_WINDOW 128      /* sliding-window rows (x-techcon section 2, CSA step 3)      */
+#define LCSA_ROPE_DIMS 64    /* BF16 RoPE slice (chenxutan.com/d/4230, section 4.5)         */
+#define LCSA_BLOCK_TOKENS 128 /* raw tokens per cache block, LCM(4,128) (x-techcon sec. 4) */
+
+typedef enum {
+  LCS_OK = 0,
+  LCS_ERR_INVALID_ARG = 1,  /* NULL where a buffer is required, negative size, bad flag    */
+  LCS_ERR_SHAPE = 2,        /* inconsistent sizes                                         */
+  LCS_ERR_ALIGNMENT = 3,    /* a buffer is not 16-byte aligned                             */
+  LCS_ERR_UNSUPPORTED = 4,  /* a size outside the supported set (see each call)            */
+  LCS_ERR_CUDA = 5,         /* a CUDA launch or device query failed                        */
+  LCS_ERR_DEVICE_GUARD = 6, /* (device status) a block id / index / row outside its buffer */
+  LCS_ERR_TIMEOUT = 7,      /* (device status) a bounded wait gave up                      */
+  LCS_ERR_WORKSPACE = 8     /* workspace NULL or smaller than the *_workspace() size       */
+} lcs_status;
+
+enum { LCS_ROW_BF16 = 0, LCS_ROW_FP8_SPLIT = 1 };
+enum { LCS_INDEX_RELU = 1 }; /* flags of csa_index_topk: phi = ReLU instead of identity     */
+
+/* A batch: num_seqs sequences that each receive new tokens in this call (a prefill chunk,
+ * one decode token, or several speculative tokens).  Sequence b holds seq_len[b] raw tokens
+ * after the call; its new tokens are the last q_b = cu_new[b+1]-cu_new[b] of them, at
+ * absolute positions seq_len[b]-q_b .. seq_len[b]-1, and they are also the queries.  Global
+ * token / query index of new token i of sequence b: cu_new[b] + i.
+ * The host fields are used for grid sizing and validation and must be upper bounds. */
+typedef struct {
+  int32_t num_seqs;          /* host                                                        */
+  const int32_t* cu_new;     /* device int32[num_seqs+1], cu_new[0] = 0, non-decreasing      */
+  const int32_t* seq_len;    /* device int32[num_seqs], seq_len[b] >= q_b                     */
+  int32_t total_new;         /* host: cu_new[num_seqs]                                        */
+  int32_t max_new;           /* host: >= every q_b                                            */
+  int32_t max_seq_len;       /* host: >= every seq_len[b]                                     */
+} lcs_batch;
+
+/* A set of rows in the row format (see the file comment). */
+typedef struct {
+  int32_t format;            /* LCS_ROW_BF16 | LCS_ROW_FP8_SPLIT                             */
+  int32_t dim;               /* D: 128 or 512                                                */
+  int64_t num_rows;          /* rows the arrays hold (device-side bounds check)             */
+  void* nope;                /* device; FP8: uint8[num_rows][D-64]; BF16: bf16[num_rows][D]  */
+  void* rope;                /* device; FP8: bf16[num_rows][64]; BF16: NULL                  */
+  float* scale;              /* device; FP8: f32[num_rows]; BF16: NULL                        */
+} lcs_rows;
+
+/* Paging of a per-sequence array of entries: entry j of sequence b lives in physical block
+ * block_table[b*max_blocks_per_seq + j/entries_per_block], slot j % entries_per_block, i.e. at
+ * row block*entries_per_block + slot.  entries_per_block = 128/m (32 for CSA, 1 for HCA). */
+typedef struct {
+  int32_t entries_per_block;
+  int32_t max_blocks_per_seq;
+  const int32_t* block_table;  /* device int32[num_seqs][max_blocks_per_seq]; < 0 = unmapped */
+} lcs_paging;
+
+/* Per-sequence state cache (x-techcon section 4: window rows and the uncompressed tail).
+ *  window:   ring of the last 128 raw rows in the row format; token p of sequence b is row
+ *            b*128 + p%128.  num_rows >= num_seqs*128.
+ *  pending:  ring of raw BF16 rows not yet folded into a complete entry, plus (overlapping
+ *            compressors) the previous block: token p of sequence b is row
+ *            b*pending_slots + p%pending_slots of a bf16[num_seqs][pending_slots][D] array.
+ *            pending_slots = 2m (overlap) or m.
+ *  new_rows: rows of this call's new tokens in the row format (row = global token index), so
+ *            that attention can read window rows of a multi-token chunk before they enter
+ *            the ring.  If new_rows.nope is NULL, compress writes the ring itself (use when
+ *            the call is not followed by attention over the same tokens). */
+typedef struct {
+  lcs_rows window;
+  void* pending;
+  int32_t pending_slots;
+  lcs_rows new_rows;
+} lcs_state;
+
+/* Compressor parameters: z_t = w . k_t + bias[o], o = offset of token t in the entry's window
+ * (0 .. 2m-1 with overlap, 0 .. m-1 without).  Entry j uses tokens [(j-1)m, (j+1)m) with
+ * overlap, [jm, (j+1)m) without; tokens before 0 are left out of the softmax. */
+typedef struct {
+  const float* w;            /* device f32[D]                                                */
+  const float* bias;         /* device f32[2m] (overlap) or f32[m]                            */
+  int32_t m;                 /* ratio; a power of two dividing 128                            */
+  int32_t overlap;           /* 1: overlapping windows of 2m rows                             */
+} lcs_compressor;
+
+/* Indexer keys: one per compressed entry, paged like the entries. */
+typedef struct {
+  const uint8_t* fp4;        /* device uint8[num_rows][rank/2]: E2M1 codes, element 2i in the low nibble */
+  const uint8_t* scale;      /* device uint8[num_rows][rank/32]: UE8M0 per-32 block scales    */
+  int32_t rank;              /* r: 64 or 128                                                  */
+  int64_t num_rows;
+} lcs_index_keys;
+
+/* --- compression (x-techcon section 2, CSA step 1 and the HCA paragraph) ---------------------
+ * Consumes the new raw rows raw[cu_new[b]+i] (device bf16[total_new][D], tokens at positions
+ * seq_len[b]-q_b+i) and, for every sequence, writes the entries completed by them:
+ * j in [floor(n0/m), floor(n1/m)) with n0 = seq_len-q_b, n1 = seq_len, quantised into
+ * `entries` through `paging`.  Updates state->pending and writes state->new_rows (or, when
+ * new_rows.nope is NULL, the window ring).  csa_compress accepts any ratio with overlap = 1 or 0;
+ * hca_compress requires overlap = 0.  Supported: D in {128, 512}, m a power of two <= 128. */
+lcs_status csa_compress(const lcs_batch* batch, const void* raw, const lcs_compressor* comp,
+                        const lcs_state* state, const lcs_rows* entries, const lcs_paging* paging,
+                        int32_t* dev_status, void* stream);
+lcs_status hca_compress(const lcs_batch* batch, const void* raw, const lcs_compressor* comp,
+                        const lcs_state* state, const lcs_rows* entries, const lcs_paging* paging,
+                        int32_t* dev_status, void* stream);
+
+/* Moves the window rows of this call's new tokens from state->new_rows into the window ring
+ * (the last min(q_b, 128) of each sequence).  Call it after the attention of the same tokens. */
+lcs_status lcs_window_commit(const lcs_batch* batch, const lcs_state* state, int32_t* dev_status,
+                             void* stream);
+
+/* --- lightning indexer + top-k (x-techcon section 2, CSA step 2; section 4, FP4 QK path) -----
+ * For query i at position t and every visible entry j < N(t) = floor((t+1)/m):
+ *   score(i,j) = sum_h w[i,h] * phi( sum_c qhat[i,h,c] * khat[j,c] ),
+ * qhat/khat = E2M1 value * 2^(ue8m0-127) of its 32-element block, phi = identity or ReLU
+ * (flags & LCS_INDEX_RELU).  Scores are computed exactly (fp32, every partial sum exact) when
+ * block exponents of q and k stay within [-8, 8] of 0 and head weights are powers of two times
+ * at most 2 significant bits; outside that range they round like fp32 sums.
+ * out_idx[i][0..k) receives the min(k, N(t)) entries with the largest scores (ties: lower j),
+ * in ascending j, padded with -1; out_cnt[i] = min(k, N(t)).
+ *   q_fp4   device uint8[total_new][heads][rank/2]    q_scale device uint8[total_new][heads][rank/32]
+ *   head_w  device f32[total_new][heads] or NULL (all 1)
+ *   heads in {1, 2, 4, 8}; rank in {64, 128}; 1 <= k <= 4096.
+ * Workspace: device, >= lcs_index_topk_workspace(batch, m, k) bytes, 256-byte aligned. */
+size_t lcs_index_topk_workspace(const lcs_batch* batch, int32_t m, int32_t k);
+lcs_status csa_index_topk(const lcs_batch* batch, const uint8_t* q_fp4, const uint8_t* q_scale,
+                          const float* head_w, int32_t heads, const lcs_index_keys* keys,
+                          const lcs_paging* paging, int32_t m, int32_t k, int32_t flags,
+                          int32_t* out_idx, int32_t* out_cnt, void* workspace,
+                          size_t workspace_bytes, int32_t* dev_status, void* stream);
+/* The exact fp32 scores themselves: out_scores[i*ld + j] for j < N(t); other slots untouched.
+ * ld >= floor(max_seq_len/m).  For verification and analysis. */
+lcs_status csa_index_scores(const lcs_batch* batch, const uint8_t* q_fp4, const uint8_t* q_scale,
+                            const float* head_w, int32_t heads, const lcs_index_keys* keys,
+                            const lcs_paging* paging, int32_t m, int32_t flags, float* out_scores,
+                            int64_t ld, int32_t* dev_status, void* stream);
+
+/* --- attention (x-techcon section 2, CSA step 3 and the HCA paragraph) -----------------------
+ * For query i (position t of sequence b) and every head h: one softmax over the rows
+ *   CSA: the entries topk_idx[i][0..cnt) (cnt = topk_cnt[i], or the count of non-negative
+ *        values when topk_cnt is NULL; every index must be below N(t) = floor((t+1)/m)),
+ *        then window tokens max(0,t-127) .. t;
+ *   HCA: the entries 0 .. N(t)-1, N(t) = floor((t+1)/m), then the same window tokens;
+ * logits = softmax_scale * q[i,h,:] . row, o[i,h,:] = sum p * row (shared KV: the row is key
+ * and value).  Window token p is read from state->new_rows when p is one of this call's new
+ * tokens (p >= seq_len-q_b) and from the window ring otherwise.
+ *   q       device bf16[total_new][heads][D]    out device bf16[total_new][heads][D]
+ *   out_lse device f32[total_new][heads] (natural log of the softmax denominator) or NULL
+ *   heads in {8, 16, 64, 128} (multiples of 16 up to 128, or 8); D in {128, 512}.
+ * FP8-split rows: query values of the FP8 dims must lie within the f16 range, and row scales
+ * must stay below 256 (|x| < 114688 before quantisation).
+ * Workspace: device, >= lcs_attend_workspace(batch, heads, D, max_rows) bytes, where max_rows
+ * bounds the rows of one query (CSA: k + 128; HCA: floor(max_seq_len/m) + 128). */
+size_t lcs_attend_workspace(const lcs_batch* batch, int32_t heads, int32_t dim, int32_t max_rows);
+lcs_status csa_attend(const lcs_batch* batch, const void* q, int32_t heads, const int32_t* topk_idx,
+                      const int32_t* topk_cnt, int32_t k, int32_t m, const lcs_rows* entries,
+                      const lcs_paging* paging, const lcs_state* state, float softmax_scale,
+                      void* out, float* out_lse, void* workspace, size_t workspace_bytes,
+                      int32_t* dev_status, void* stream);
+lcs_status hca_attend(const lcs_batch* batch, const void* q, int32_t heads, int32_t m,
+                      const lcs_rows* entries, const lcs_paging* paging, const lcs_state* state,
+                      float softmax_scale, void* out, float* out_lse, void* workspace,
+                      size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/* --- library information -------------------------------------------------------------------- */
+int32_t lcs_abi_version(void);
+const char* lcs_status_string(int32_t status);
+/* LCS_OK when the current device can run the library's kernels (compute capability 10.3). */
+lcs_status lcs_device_check(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LCSA_H_ */

@@ -1,0 +1,347 @@
+// C ABI entry points: argument validation, workspace layout and kernel launches.
+#include <cstring>
+
+#include "kernels.cuh"
+
+using namespace lcsa;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+lcs_status check_batch(const lcs_batch* b) {
+  if (b == nullptr || b->cu_new == nullptr || b->seq_len == nullptr) return LCS_ERR_INVALID_ARG;
+  if (b->num_seqs <= 0 || b->num_seqs > 65535) return LCS_ERR_UNSUPPORTED;
+  if (b->total_new < 0 || b->max_new < 0 || b->max_seq_len < 0) return LCS_ERR_INVALID_ARG;
+  if (b->max_new > b->max_seq_len) return LCS_ERR_SHAPE;
+  return LCS_OK;
+}
+
+lcs_status check_rows(const lcs_rows* r, bool need_data = true) {
+  if (r == nullptr) return LCS_ERR_INVALID_ARG;
+  if (r->dim != 128 && r->dim != 512) return LCS_ERR_UNSUPPORTED;
+  if (r->format == LCS_ROW_BF16) {
+    if (need_data && r->nope == nullptr) return LCS_ERR_INVALID_ARG;
+    if (!aligned16(r->nope)) return LCS_ERR_ALIGNMENT;
+  } else if (r->format == LCS_ROW_FP8_SPLIT) {
+    if (need_data && (r->nope == nullptr || r->rope == nullptr || r->scale == nullptr)) return LCS_ERR_INVALID_ARG;
+    if (!aligned16(r->nope) || !aligned16(r->rope) || (reinterpret_cast<uintptr_t>(r->scale) & 3u))
+      return LCS_ERR_ALIGNMENT;
+  } else {
+    return LCS_ERR_UNSUPPORTED;
+  }
+  if (r->num_rows < 0) return LCS_ERR_INVALID_ARG;
+  return LCS_OK;
+}
+
+bool same_layout(const lcs_rows& a, const lcs_rows& b) { return a.format == b.format && a.dim == b.dim; }
+
+lcs_status check_paging(const lcs_paging* p) {
+  if (p == nullptr || p->block_table == nullptr) return LCS_ERR_INVALID_ARG;
+  if (p->entries_per_block <= 0 || p->max_blocks_per_seq <= 0) return LCS_ERR_INVALID_ARG;
+  return LCS_OK;
+}
+
+lcs_status from_cuda(cudaError_t e) { return e == cudaSuccess ? LCS_OK : LCS_ERR_CUDA; }
+
+int num_sms() {
+  int dev = 0, n = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 148;
+}
+
+long long index_ld(const lcs_batch* b, int m) {
+  long long n = b->max_seq_len / m;
+  return (n + 3) / 4 * 4;
+}
+
+struct SplitPlan {
+  int splits;
+  int rows_per_split;
+};
+
+SplitPlan plan_splits(const lcs_batch* b, int heads, int max_rows) {
+  const int hg = heads <= 16 ? 1 : (heads + 63) / 64;
+  const long long base = (long long)b->total_new * hg;
+  SplitPlan s{1, max_rows > 0 ? max_rows : 1};
+  const int sms = num_sms();
+  if (base <= 0 || base >= sms || max_rows <= 64) return s;
+  int want = (int)(sms / base);
+  const int cap = (max_rows + 63) / 64;
+  if (want > cap) want = cap;
+  if (want <= 1) return s;
+  int rps = (max_rows + want - 1) / want;
+  rps = (rps + 31) / 32 * 32;
+  s.rows_per_split = rps;
+  s.splits = (max_rows + rps - 1) / rps;
+  return s;
+}
+
+size_t attend_ws_bytes(const lcs_batch* b, int heads, int dim, const SplitPlan& s) {
+  if (s.splits <= 1) return 0;
+  const size_t per = (size_t)b->total_new * heads * s.splits;
+  return per * dim * 4 + per * 2 * 4 + 256;
+}
+
+lcs_status compress_common(const lcs_batch* batch, const void* raw, const lcs_compressor* comp,
+                           const lcs_state* state, const lcs_rows* entries, const lcs_paging* paging,
+                           int32_t* dev_status, void* stream, bool hca) {
+  lcs_status s = check_batch(batch);
+  if (s != LCS_OK) return s;
+  if (comp == nullptr || state == nullptr || comp->w == nullptr || comp->bias == nullptr) return LCS_ERR_INVALID_ARG;
+  if (raw == nullptr && batch->total_new > 0) return LCS_ERR_INVALID_ARG;
+  if (!aligned16(raw) || !aligned16(state->pending)) return LCS_ERR_ALIGNMENT;
+  const int m = comp->m;
+  if (m <= 0 || m > 128 || (m & (m - 1)) != 0) return LCS_ERR_UNSUPPORTED;
+  if (hca && comp->overlap) return LCS_ERR_UNSUPPORTED;
+  const int slots = comp->overlap ? 2 * m : m;
+  if (state->pending == nullptr || state->pending_slots != slots) return LCS_ERR_SHAPE;
+  if ((s = check_rows(entries)) != LCS_OK) return s;
+  if ((s = check_paging(paging)) != LCS_OK) return s;
+  const bool have_new = state->new_rows.nope != nullptr;
+  if (have_new) {
+    if ((s = check_rows(&state->new_rows)) != LCS_OK) return s;
+    if (!same_layout(state->new_rows, *entries)) return LCS_ERR_SHAPE;
+    if (state->new_rows.num_rows < batch->total_new) return LCS_ERR_SHAPE;
+  } else {
+    if ((s = check_rows(&state->window)) != LCS_OK) return s;
+    if (!same_layout(state->window, *entries)) return LCS_ERR_SHAPE;
+    if (state->window.num_rows < (int64_t)batch->num_seqs * LCSA_WINDOW) return LCS_ERR_SHAPE;
+  }
+  CompressParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.cu_new = batch->cu_new;
+  p.seq_len = batch->seq_len;
+  p.num_seqs = batch->num_seqs;
+  p.raw = static_cast<const __nv_bfloat16*>(raw);
+  p.w = comp->w;
+  p.bias = comp->bias;
+  p.m = m;
+  p.overlap = comp->overlap ? 1 : 0;
+  p.pending = static_cast<const __nv_bfloat16*>(state->pending);
+  p.pending_out = static_cast<__nv_bfloat16*>(state->pending);
+  p.pending_slots = slots;
+  p.entries = make_rows(*entries);
+  p.paging = make_paging(*paging);
+  p.new_rows = make_rows(state->new_rows);
+  if (!have_new) p.new_rows.nope = nullptr;
+  p.window = make_rows(state->window);
+  p.status = dev_status;
+  return from_cuda(launch_compress(p, entries->dim, batch->max_new, static_cast<cudaStream_t>(stream)));
+}
+
+lcs_status index_common(const lcs_batch* batch, const uint8_t* q_fp4, const uint8_t* q_scale, int32_t heads,
+                        const lcs_index_keys* keys, const lcs_paging* paging, int32_t m, IndexParams& p) {
+  lcs_status s = check_batch(batch);
+  if (s != LCS_OK) return s;
+  if (q_fp4 == nullptr || q_scale == nullptr || keys == nullptr || keys->fp4 == nullptr || keys->scale == nullptr)
+    return LCS_ERR_INVALID_ARG;
+  if (heads != 1 && heads != 2 && heads != 4 && heads != 8) return LCS_ERR_UNSUPPORTED;
+  if (keys->rank != 64 && keys->rank != 128) return LCS_ERR_UNSUPPORTED;
+  if (m <= 0 || m > 128 || (m & (m - 1)) != 0) return LCS_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(q_fp4) & 3u) || (reinterpret_cast<uintptr_t>(keys->fp4) & 3u) ||
+      (reinterpret_cast<uintptr_t>(keys->scale) & 3u) || (reinterpret_cast<uintptr_t>(q_scale) & 1u))
+    return LCS_ERR_ALIGNMENT;
+  if ((s = check_paging(paging)) != LCS_OK) return s;
+  std::memset(&p, 0, sizeof(p));
+  p.cu_new = batch->cu_new;
+  p.seq_len = batch->seq_len;
+  p.num_seqs = batch->num_seqs;
+  p.q_fp4 = q_fp4;
+  p.q_scale = q_scale;
+  p.heads = heads;
+  p.k_fp4 = keys->fp4;
+  p.k_scale = keys->scale;
+  p.k_rows = keys->num_rows;
+  p.paging = make_paging(*paging);
+  p.m = m;
+  return LCS_OK;
+}
+
+lcs_status attend_common(const lcs_batch* batch, const void* q, int32_t heads, const lcs_rows* entries,
+                         const lcs_paging* paging, const lcs_state* state, void* out, void* workspace,
+                         size_t workspace_bytes, int max_rows, AttendParams& p) {
+  lcs_status s = check_batch(batch);
+  if (s != LCS_OK) return s;
+  if (q == nullptr || out == nullptr || state == nullptr) return LCS_ERR_INVALID_ARG;
+  if (!(heads == 8 || (heads % 16 == 0 && heads >= 16 && heads <= 128))) return LCS_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(out)) return LCS_ERR_ALIGNMENT;
+  if ((s = check_rows(entries)) != LCS_OK) return s;
+  if ((s = check_paging(paging)) != LCS_OK) return s;
+  if ((s = check_rows(&state->window)) != LCS_OK) return s;
+  if (!same_layout(state->window, *entries)) return LCS_ERR_SHAPE;
+  if (state->window.num_rows < (int64_t)batch->num_seqs * LCSA_WINDOW) return LCS_ERR_SHAPE;
+  // every query's own token is one of this call's new tokens: its window row comes from new_rows
+  if ((s = check_rows(&state->new_rows)) != LCS_OK) return s;
+  if (!same_layout(state->new_rows, *entries)) return LCS_ERR_SHAPE;
+  if (state->new_rows.num_rows < batch->total_new) return LCS_ERR_SHAPE;
+  if (entries->num_rows < 1) return LCS_ERR_SHAPE;
+  if (entries->format == LCS_ROW_BF16 && entries->dim == 512) return LCS_ERR_UNSUPPORTED;
+  const SplitPlan plan = plan_splits(batch, heads, max_rows);
+  const size_t need = attend_ws_bytes(batch, heads, entries->dim, plan);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return LCS_ERR_WORKSPACE;
+  if (need > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return LCS_ERR_ALIGNMENT;
+  std::memset(&p, 0, sizeof(p));
+  p.cu_new = batch->cu_new;
+  p.seq_len = batch->seq_len;
+  p.num_seqs = batch->num_seqs;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.heads = heads;
+  p.entries = make_rows(*entries);
+  p.paging = make_paging(*paging);
+  p.window = make_rows(state->window);
+  p.new_rows = make_rows(state->new_rows);
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.splits = plan.splits;
+  p.rows_per_split = plan.rows_per_split;
+  if (plan.splits > 1) {
+    const size_t per = (size_t)batch->total_new * heads * plan.splits;
+    p.ws_o = static_cast<float*>(workspace);
+    p.ws_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + per * entries->dim * 4);
+  }
+  return LCS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t lcs_abi_version(void) { return LCSA_ABI_VERSION; }
+
+const char* lcs_status_string(int32_t s) {
+  switch (s) {
+    case LCS_OK: return "ok";
+    case LCS_ERR_INVALID_ARG: return "invalid argument";
+    case LCS_ERR_SHAPE: return "inconsistent shapes";
+    case LCS_ERR_ALIGNMENT: return "misaligned buffer";
+    case LCS_ERR_UNSUPPORTED: return "unsupported size";
+    case LCS_ERR_CUDA: return "CUDA error";
+    case LCS_ERR_DEVICE_GUARD: return "device-side index or block id out of range";
+    case LCS_ERR_TIMEOUT: return "bounded device wait timed out";
+    case LCS_ERR_WORKSPACE: return "workspace missing or too small";
+    default: return "unknown status";
+  }
+}
+
+lcs_status lcs_device_check(void) {
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return LCS_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return LCS_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return LCS_ERR_CUDA;
+  return (major == 10 && minor == 3) ? LCS_OK : LCS_ERR_UNSUPPORTED;
+}
+
+lcs_status csa_compress(const lcs_batch* batch, const void* raw, const lcs_compressor* comp, const lcs_state* state,
+                        const lcs_rows* entries, const lcs_paging* paging, int32_t* dev_status, void* stream) {
+  return compress_common(batch, raw, comp, state, entries, paging, dev_status, stream, false);
+}
+
+lcs_status hca_compress(const lcs_batch* batch, const void* raw, const lcs_compressor* comp, const lcs_state* state,
+                        const lcs_rows* entries, const lcs_paging* paging, int32_t* dev_status, void* stream) {
+  return compress_common(batch, raw, comp, state, entries, paging, dev_status, stream, true);
+}
+
+lcs_status lcs_window_commit(const lcs_batch* batch, const lcs_state* state, int32_t* dev_status, void* stream) {
+  lcs_status s = check_batch(batch);
+  if (s != LCS_OK) return s;
+  if (state == nullptr) return LCS_ERR_INVALID_ARG;
+  if ((s = check_rows(&state->window)) != LCS_OK) return s;
+  if ((s = check_rows(&state->new_rows)) != LCS_OK) return s;
+  if (!same_layout(state->window, state->new_rows)) return LCS_ERR_SHAPE;
+  if (state->window.num_rows < (int64_t)batch->num_seqs * LCSA_WINDOW) return LCS_ERR_SHAPE;
+  return from_cuda(launch_window_commit(batch->cu_new, batch->seq_len, batch->num_seqs, batch->max_new,
+                                        make_rows(state->new_rows), make_rows(state->window), dev_status,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+size_t lcs_index_topk_workspace(const lcs_batch* batch, int32_t m, int32_t k) {
+  (void)k;
+  if (batch == nullptr || m <= 0) return 0;
+  return (size_t)batch->total_new * (size_t)index_ld(batch, m) * 4 + 256;
+}
+
+lcs_status csa_index_topk(const lcs_batch* batch, const uint8_t* q_fp4, const uint8_t* q_scale, const float* head_w,
+                          int32_t heads, const lcs_index_keys* keys, const lcs_paging* paging, int32_t m, int32_t k,
+                          int32_t flags, int32_t* out_idx, int32_t* out_cnt, void* workspace, size_t workspace_bytes,
+                          int32_t* dev_status, void* stream) {
+  IndexParams p;
+  lcs_status s = index_common(batch, q_fp4, q_scale, heads, keys, paging, m, p);
+  if (s != LCS_OK) return s;
+  if (k < 1 || k > 4096) return LCS_ERR_UNSUPPORTED;
+  if ((flags & ~LCS_INDEX_RELU) != 0) return LCS_ERR_INVALID_ARG;
+  if (out_idx == nullptr || out_cnt == nullptr) return LCS_ERR_INVALID_ARG;
+  const size_t need = lcs_index_topk_workspace(batch, m, k);
+  if (workspace == nullptr || workspace_bytes < need) return LCS_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return LCS_ERR_ALIGNMENT;
+  p.head_w = head_w;
+  p.relu = (flags & LCS_INDEX_RELU) ? 1 : 0;
+  p.ld = index_ld(batch, m);
+  p.keys_out = static_cast<uint32_t*>(workspace);
+  p.status = dev_status;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int max_entries = batch->max_seq_len / m;
+  cudaError_t e = launch_index_scores(p, keys->rank, batch->max_new, max_entries, st);
+  if (e != cudaSuccess) return LCS_ERR_CUDA;
+  e = launch_topk_select(p.keys_out, p.ld, batch->cu_new, batch->seq_len, batch->num_seqs, batch->max_new, m, k,
+                         max_entries, out_idx, out_cnt, st);
+  return from_cuda(e);
+}
+
+lcs_status csa_index_scores(const lcs_batch* batch, const uint8_t* q_fp4, const uint8_t* q_scale, const float* head_w,
+                            int32_t heads, const lcs_index_keys* keys, const lcs_paging* paging, int32_t m,
+                            int32_t flags, float* out_scores, int64_t ld, int32_t* dev_status, void* stream) {
+  IndexParams p;
+  lcs_status s = index_common(batch, q_fp4, q_scale, heads, keys, paging, m, p);
+  if (s != LCS_OK) return s;
+  if ((flags & ~LCS_INDEX_RELU) != 0 || out_scores == nullptr) return LCS_ERR_INVALID_ARG;
+  if (ld < batch->max_seq_len / m) return LCS_ERR_SHAPE;
+  p.head_w = head_w;
+  p.relu = (flags & LCS_INDEX_RELU) ? 1 : 0;
+  p.ld = ld;
+  p.scores_out = out_scores;
+  p.status = dev_status;
+  return from_cuda(launch_index_scores(p, keys->rank, batch->max_new, batch->max_seq_len / m,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+size_t lcs_attend_workspace(const lcs_batch* batch, int32_t heads, int32_t dim, int32_t max_rows) {
+  if (batch == nullptr) return 0;
+  return attend_ws_bytes(batch, heads, dim, plan_splits(batch, heads, max_rows));
+}
+
+lcs_status csa_attend(const lcs_batch* batch, const void* q, int32_t heads, const int32_t* topk_idx,
+                      const int32_t* topk_cnt, int32_t k, int32_t m, const lcs_rows* entries, const lcs_paging* paging,
+                      const lcs_state* state, float softmax_scale, void* out, float* out_lse, void* workspace,
+                      size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  if (topk_idx == nullptr) return LCS_ERR_INVALID_ARG;
+  if (k < 1 || k > 4096 || m <= 0 || m > 128) return LCS_ERR_UNSUPPORTED;
+  AttendParams p;
+  lcs_status s = attend_common(batch, q, heads, entries, paging, state, out, workspace, workspace_bytes,
+                               k + LCSA_WINDOW, p);
+  if (s != LCS_OK) return s;
+  p.topk_idx = topk_idx;
+  p.topk_cnt = topk_cnt;
+  p.k = k;
+  p.m = m;
+  p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  p.out_lse = out_lse;
+  p.status = dev_status;
+  return from_cuda(launch_attend(p, entries->dim, entries->format, batch->total_new, static_cast<cudaStream_t>(stream)));
+}
+
+lcs_status hca_attend(const lcs_batch* batch, const void* q, int32_t heads, int32_t m, const lcs_rows* entries,
+                      const lcs_paging* paging, const lcs_state* state, float softmax_scale, void* out, float* out_lse,
+                      void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  if (m <= 0 || m > 128) return LCS_ERR_UNSUPPORTED;
+  AttendParams p;
+  lcs_status s = attend_common(batch, q, heads, entries, paging, state, out, workspace, workspace_bytes,
+                               batch ? batch->max_seq_len / m + LCSA_WINDOW : 0, p);
+  if (s != LCS_OK) return s;
+  p.m = m;
+  p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  p.out_lse = out_lse;
+  p.status = dev_status;
+  return from_cuda(launch_attend(p, entries->dim, entries->format, batch->total_new, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

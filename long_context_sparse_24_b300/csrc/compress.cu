@@ -1,0 +1,329 @@
+// KV compression (CSA m=4 with overlapping windows, HCA m'=128) and the state-cache update.
+//
+// Defined by: m.x-techcon.com/article/133366, section 2 "核心技术创新：混合压缩注意力", CSA step 1
+// (each raw token gets a learned weight plus a positional bias, the weights are softmax-
+// normalised and the rows summed with them; adjacent blocks overlap) and the HCA paragraph
+// (ratio 128); section 4 "专门为混合注意力设计的KV缓存管理" (state cache holds the window rows and
+// the uncompressed tail; the compressed cache is allocated in blocks).  Storage format from the
+// same page's efficiency paragraph (RoPE dims BF16, the rest FP8).
+//
+// Work split: one warp per entry for windows of up to 16 rows (CSA), one CTA of 8 warps per
+// entry for longer windows (HCA).  Every raw row is read with 16-byte vector loads; lane l of a
+// warp owns the 16-byte chunks l, l+32, ... of a row, so a warp-wide load is one contiguous
+// 512-byte segment.  The arithmetic of one entry does not depend on how many entries the call
+// completes, so decode-time (one token) and prefill-time (many tokens) compression give the
+// same bits.
+#include "kernels.cuh"
+
+namespace lcsa {
+
+
+
+template <int D>
+struct RowChunks {
+  static constexpr int kChunks = D / 8;                 // 16-byte chunks of a bf16 row
+  static constexpr int kPerLane = (kChunks + 31) / 32;  // chunks owned by one lane
+};
+
+// Load lane-owned chunks of a bf16 row as fp32.
+template <int D>
+__device__ __forceinline__ void load_row(const __nv_bfloat16* row, int lane, float (&v)[RowChunks<D>::kPerLane][8]) {
+#pragma unroll
+  for (int i = 0; i < RowChunks<D>::kPerLane; ++i) {
+    int c = lane + 32 * i;
+    if (c < RowChunks<D>::kChunks) {
+      uint4 u = *reinterpret_cast<const uint4*>(row + c * 8);
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        float2 f = __bfloat1622float2(h[k]);
+        v[i][2 * k] = f.x;
+        v[i][2 * k + 1] = f.y;
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) v[i][k] = 0.0f;
+    }
+  }
+}
+
+// Quantise one row held by a warp (lane-owned chunks) and store it as row `r` of `dst`.
+template <int D>
+__device__ __forceinline__ void store_row(const Rows& dst, long long r, int lane,
+                                          const float (&v)[RowChunks<D>::kPerLane][8]) {
+  constexpr int C = RowChunks<D>::kChunks;
+  if (dst.format == LCS_ROW_BF16) {
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(dst.nope) + r * D;
+#pragma unroll
+    for (int i = 0; i < RowChunks<D>::kPerLane; ++i) {
+      int c = lane + 32 * i;
+      if (c < C) {
+        uint4 u;
+        __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) h[k] = __floats2bfloat162_rn(v[i][2 * k], v[i][2 * k + 1]);
+        *reinterpret_cast<uint4*>(out + c * 8) = u;
+      }
+    }
+    return;
+  }
+  // FP8 split: chunks 0..7 are the RoPE dims (BF16), chunks 8.. the E4M3 dims.
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < RowChunks<D>::kPerLane; ++i) {
+    int c = lane + 32 * i;
+    if (c >= kRope / 8 && c < C) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(v[i][k]));
+    }
+  }
+  amax = warp_max(amax);
+  const float s = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+#pragma unroll
+  for (int i = 0; i < RowChunks<D>::kPerLane; ++i) {
+    int c = lane + 32 * i;
+    if (c < kRope / 8) {
+      uint4 u;
+      __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) h[k] = __floats2bfloat162_rn(v[i][2 * k], v[i][2 * k + 1]);
+      *reinterpret_cast<uint4*>(dst.rope + r * kRope + c * 8) = u;
+    } else if (c < C) {
+      uint2 u;
+      uint16_t* q = reinterpret_cast<uint16_t*>(&u);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        q[k] = f32x2_to_e4m3x2(__fdiv_rn(v[i][2 * k], s), __fdiv_rn(v[i][2 * k + 1], s));
+      *reinterpret_cast<uint2*>(dst.nope + r * (D - kRope) + (c - kRope / 8) * 8) = u;
+    }
+  }
+  if (lane == 0) dst.scale[r] = s;
+}
+
+// Pointer to raw token t of sequence span sp (t < n0: the pending ring; t >= n0: this call's rows).
+__device__ __forceinline__ const __nv_bfloat16* token_row(const CompressParams& p, int b, const SeqSpan& sp,
+                                                          int t, int D) {
+  if (t >= sp.n0()) return p.raw + (long long)(sp.q0 + t - sp.n0()) * D;
+  return p.pending + ((long long)b * p.pending_slots + (t % p.pending_slots)) * D;
+}
+
+// grid: (ceil(max_entries_per_call / EPC), num_seqs), block 256.  WPE warps per entry.
+template <int D, int WPE>
+__global__ void __launch_bounds__(256) compress_entries_kernel(CompressParams p) {
+  constexpr int EPC = 8 / WPE;
+  constexpr int PL = RowChunks<D>::kPerLane;
+  constexpr int kMaxRows = 256;
+  __shared__ float zbuf[EPC][kMaxRows];
+  __shared__ float red[WPE > 1 ? 8 : 1][WPE > 1 ? D : 1];
+
+  const int b = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e_local = warp / WPE, wi = warp % WPE;
+  const SeqSpan sp = seq_span(p.cu_new, p.seq_len, b);
+  const int m = p.m;
+  const int j_first = sp.n0() / m, j_end = sp.n1 / m;
+  const int j = j_first + blockIdx.x * EPC + e_local;
+  const bool active = j < j_end;  // warp-uniform; whole entry group shares it
+  const int R = p.overlap ? 2 * m : m;
+  const int lo = p.overlap ? (j - 1) * m : j * m;
+
+  // phase 1: scores z_t = w . k_t + b[offset]
+  float wv[PL][8];
+#pragma unroll
+  for (int i = 0; i < PL; ++i) {
+    int c = lane + 32 * i;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) wv[i][k] = c < RowChunks<D>::kChunks ? p.w[c * 8 + k] : 0.0f;
+  }
+  if (active) {
+    for (int rr = wi; rr < R; rr += WPE) {
+      const int t = lo + rr;
+      float z = -INFINITY;
+      if (t >= 0) {
+        float v[PL][8];
+        load_row<D>(token_row(p, b, sp, t, D), lane, v);
+        float acc = 0.0f;
+#pragma unroll
+        for (int i = 0; i < PL; ++i)
+#pragma unroll
+          for (int k = 0; k < 8; ++k) acc = fmaf(wv[i][k], v[i][k], acc);
+        z = warp_sum(acc) + p.bias[rr];
+      }
+      if (lane == 0) zbuf[e_local][rr] = z;
+    }
+  }
+  __syncthreads();
+  if (!active) return;  // entry groups are whole: no later block-wide barrier is skipped unevenly
+
+  // phase 2: softmax weights over the rows that exist, weighted sum
+  float zmax = -INFINITY;
+  for (int rr = lane; rr < R; rr += 32) zmax = fmaxf(zmax, zbuf[e_local][rr]);
+  zmax = warp_max(zmax);
+  float zsum = 0.0f;
+  for (int rr = lane; rr < R; rr += 32) {
+    float z = zbuf[e_local][rr];
+    zsum += (z == -INFINITY) ? 0.0f : expf(z - zmax);
+  }
+  zsum = warp_sum(zsum);
+  const float inv = 1.0f / zsum;
+
+  float acc[PL][8];
+#pragma unroll
+  for (int i = 0; i < PL; ++i)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) acc[i][k] = 0.0f;
+  for (int rr = wi; rr < R; rr += WPE) {
+    const int t = lo + rr;
+    if (t < 0) continue;
+    const float a = expf(zbuf[e_local][rr] - zmax) * inv;
+    float v[PL][8];
+    load_row<D>(token_row(p, b, sp, t, D), lane, v);
+#pragma unroll
+    for (int i = 0; i < PL; ++i)
+#pragma unroll
+      for (int k = 0; k < 8; ++k) acc[i][k] = fmaf(a, v[i][k], acc[i][k]);
+  }
+
+  if constexpr (WPE > 1) {
+    // cross-warp sum in a fixed order (deterministic)
+#pragma unroll
+    for (int i = 0; i < PL; ++i) {
+      int c = lane + 32 * i;
+      if (c < RowChunks<D>::kChunks)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) red[warp][c * 8 + k] = acc[i][k];
+    }
+    __syncthreads();
+    if (wi != 0) return;
+#pragma unroll
+    for (int i = 0; i < PL; ++i) {
+      int c = lane + 32 * i;
+      if (c < RowChunks<D>::kChunks)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          float s = 0.0f;
+          for (int wq = 0; wq < WPE; ++wq) s += red[e_local * WPE + wq][c * 8 + k];
+          acc[i][k] = s;
+        }
+    }
+  }
+
+  const long long row = entry_row(p.paging, b, j, p.entries.num_rows);
+  if (row < 0) {
+    if (lane == 0) report(p.status, LCS_ERR_DEVICE_GUARD);
+    return;
+  }
+  store_row<D>(p.entries, row, lane, acc);
+}
+
+// One warp per new token: keep it in the pending ring if a future entry needs it, and write
+// its quantised row to new_rows (or to the window ring when new_rows is absent).
+// grid: (ceil(max_new / 8), num_seqs), block 256.
+template <int D>
+__global__ void __launch_bounds__(256) compress_state_kernel(CompressParams p) {
+  constexpr int PL = RowChunks<D>::kPerLane;
+  const int b = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const SeqSpan sp = seq_span(p.cu_new, p.seq_len, b);
+  const int i = blockIdx.x * 8 + warp;
+  if (i >= sp.qn) return;
+  const int t = sp.n0() + i;
+  const int m = p.m;
+  const int full = sp.n1 / m;
+  const int keep_lo = p.overlap ? (full - 1) * m : full * m;
+  const __nv_bfloat16* src = p.raw + (long long)(sp.q0 + i) * D;
+  float v[PL][8];
+  load_row<D>(src, lane, v);
+  if (t >= keep_lo) {
+    __nv_bfloat16* dst = p.pending_out + ((long long)b * p.pending_slots + (t % p.pending_slots)) * D;
+#pragma unroll
+    for (int k = 0; k < PL; ++k) {
+      int c = lane + 32 * k;
+      if (c < RowChunks<D>::kChunks)
+        *reinterpret_cast<uint4*>(dst + c * 8) = *reinterpret_cast<const uint4*>(src + c * 8);
+    }
+  }
+  if (p.new_rows.nope != nullptr) {
+    long long r = (long long)sp.q0 + i;
+    if (r >= p.new_rows.num_rows) {
+      if (lane == 0) report(p.status, LCS_ERR_DEVICE_GUARD);
+      return;
+    }
+    store_row<D>(p.new_rows, r, lane, v);
+  } else if (t >= sp.n1 - kWindow) {
+    long long r = (long long)b * kWindow + (t % kWindow);
+    if (r >= p.window.num_rows) {
+      if (lane == 0) report(p.status, LCS_ERR_DEVICE_GUARD);
+      return;
+    }
+    store_row<D>(p.window, r, lane, v);
+  }
+}
+
+// Copy this call's new rows into the window ring.  grid: (ceil(min(max_new,128)/8), num_seqs).
+__global__ void __launch_bounds__(256) window_commit_kernel(const int32_t* cu_new, const int32_t* seq_len,
+                                                           Rows src, Rows ring, int32_t* status) {
+  const int b = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const SeqSpan sp = seq_span(cu_new, seq_len, b);
+  const int ncopy = min(sp.qn, kWindow);
+  const int i = blockIdx.x * 8 + warp;  // 0 .. ncopy-1, the last ncopy new tokens
+  if (i >= ncopy) return;
+  const int t = sp.n1 - ncopy + i;
+  const long long s = (long long)sp.q0 + (t - sp.n0());
+  const long long d = (long long)b * kWindow + (t % kWindow);
+  if (s >= src.num_rows || d >= ring.num_rows) {
+    if (lane == 0) report(status, LCS_ERR_DEVICE_GUARD);
+    return;
+  }
+  const int D = src.dim;
+  if (src.format == LCS_ROW_BF16) {
+    const uint4* a = reinterpret_cast<const uint4*>(src.nope + s * D * 2);
+    uint4* o = reinterpret_cast<uint4*>(ring.nope + d * D * 2);
+    for (int c = lane; c < D / 8; c += 32) o[c] = a[c];
+    return;
+  }
+  const uint4* a = reinterpret_cast<const uint4*>(src.nope + s * (D - kRope));
+  uint4* o = reinterpret_cast<uint4*>(ring.nope + d * (D - kRope));
+  for (int c = lane; c < (D - kRope) / 16; c += 32) o[c] = a[c];
+  const uint4* ra = reinterpret_cast<const uint4*>(src.rope + s * kRope);
+  uint4* ro = reinterpret_cast<uint4*>(ring.rope + d * kRope);
+  if (lane < kRope / 8) ro[lane] = ra[lane];
+  if (lane == 0) ring.scale[d] = src.scale[s];
+}
+
+// ----------------------------------------------------------------------------------------------
+// launchers
+// ----------------------------------------------------------------------------------------------
+
+cudaError_t launch_compress(const CompressParams& p, int D, int max_new, cudaStream_t st) {
+  const int R = p.overlap ? 2 * p.m : p.m;
+  const int max_entries = max_new / p.m + 1;
+  const bool cta_per_entry = R > 16;
+  const int epc = cta_per_entry ? 1 : 8;
+  dim3 grid((max_entries + epc - 1) / epc, p.num_seqs);
+  if (D == 512) {
+    if (cta_per_entry) compress_entries_kernel<512, 8><<<grid, 256, 0, st>>>(p);
+    else compress_entries_kernel<512, 1><<<grid, 256, 0, st>>>(p);
+  } else {
+    if (cta_per_entry) compress_entries_kernel<128, 8><<<grid, 256, 0, st>>>(p);
+    else compress_entries_kernel<128, 1><<<grid, 256, 0, st>>>(p);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || max_new == 0) return e;
+  dim3 g2((max_new + 7) / 8, p.num_seqs);
+  if (D == 512) compress_state_kernel<512><<<g2, 256, 0, st>>>(p);
+  else compress_state_kernel<128><<<g2, 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_window_commit(const int32_t* cu_new, const int32_t* seq_len, int num_seqs, int max_new,
+                                 const Rows& src, const Rows& ring, int32_t* status, cudaStream_t st) {
+  int n = max_new < kWindow ? max_new : kWindow;
+  if (n <= 0) return cudaSuccess;
+  dim3 grid((n + 7) / 8, num_seqs);
+  window_commit_kernel<<<grid, 256, 0, st>>>(cu_new, seq_len, src, ring, status);
+  return cudaGetLastError();
+}
+
+}  // namespace lcsa

@@ -1,0 +1,80 @@
+// Kernel parameter blocks and launchers shared by the C ABI layer and the kernel files.
+#pragma once
+
+#include "common.cuh"
+
+namespace lcsa {
+
+struct CompressParams {
+  const int32_t* cu_new;
+  const int32_t* seq_len;
+  int num_seqs;
+  const __nv_bfloat16* raw;
+  const float* w;
+  const float* bias;
+  int m;
+  int overlap;
+  const __nv_bfloat16* pending;
+  __nv_bfloat16* pending_out;
+  int pending_slots;
+  Rows entries;
+  Paging paging;
+  Rows new_rows;   // nope == nullptr: write the window ring instead
+  Rows window;
+  int32_t* status;
+};
+
+struct IndexParams {
+  const int32_t* cu_new;
+  const int32_t* seq_len;
+  int num_seqs;
+  const uint8_t* q_fp4;     // [T][Hi][r/2]
+  const uint8_t* q_scale;   // [T][Hi][r/32]
+  const float* head_w;      // [T][Hi] or null
+  int heads;
+  const uint8_t* k_fp4;     // [rows][r/2]
+  const uint8_t* k_scale;   // [rows][r/32]
+  long long k_rows;
+  Paging paging;
+  int m;
+  int relu;
+  uint32_t* keys_out;       // [T][ld] order-preserving keys, or
+  float* scores_out;        // [T][ld] fp32 scores
+  long long ld;
+  int32_t* status;
+};
+
+struct AttendParams {
+  const int32_t* cu_new;
+  const int32_t* seq_len;
+  int num_seqs;
+  const __nv_bfloat16* q;
+  int heads;
+  const int32_t* topk_idx;   // CSA; null -> HCA
+  const int32_t* topk_cnt;
+  int k;
+  int m;
+  Rows entries;
+  Paging paging;
+  Rows window;
+  Rows new_rows;
+  float scale_log2;
+  __nv_bfloat16* out;
+  float* out_lse;
+  float* ws_o;               // [T][H][splits][D]
+  float* ws_ml;              // [T][H][splits][2]
+  int splits;
+  int rows_per_split;
+  int32_t* status;
+};
+
+cudaError_t launch_compress(const CompressParams& p, int D, int max_new, cudaStream_t st);
+cudaError_t launch_window_commit(const int32_t* cu_new, const int32_t* seq_len, int num_seqs, int max_new,
+                                 const Rows& src, const Rows& ring, int32_t* status, cudaStream_t st);
+cudaError_t launch_index_scores(const IndexParams& p, int rank, int max_new, int max_entries, cudaStream_t st);
+cudaError_t launch_topk_select(const uint32_t* keys, long long ld, const int32_t* cu_new, const int32_t* seq_len,
+                               int num_seqs, int max_new, int m, int k, int max_entries, int32_t* out_idx,
+                               int32_t* out_cnt, cudaStream_t st);
+cudaError_t launch_attend(const AttendParams& p, int D, int fmt, int total_new, cudaStream_t st);
+
+}  // namespace lcsa

@@ -1,0 +1,88 @@
+"""The C ABI library: loads, exports every entry point the header declares, validates arguments
+on the host (no GPU needed for any call here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "lcsa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:lcs_status|size_t|int32_t|const char\*)\s+(\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_five_operations():
+    names = header_functions()
+    for n in ("csa_compress", "hca_compress", "csa_index_topk", "csa_attend", "hca_attend"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    import long_context_sparse_24_b300 as lcsa
+    lib = ctypes.CDLL(lcsa.LIB_PATH)
+    for n in header_functions():
+        assert hasattr(lib, n), n
+    assert set(header_functions()) == set(lcsa.EXPORTED)
+
+
+def test_abi_version_and_status_strings():
+    import long_context_sparse_24_b300 as lcsa
+    assert lcsa.lcs_abi_version() == 1
+    assert lcsa.lcs_status_string(0) == "ok"
+    assert "workspace" in lcsa.lcs_status_string(8)
+
+
+def _batch(lcsa, **kw):
+    b = lcsa.lcs_batch(1, 0x1000, 0x2000, 1, 1, 10)
+    for k, v in kw.items():
+        setattr(b, k, v)
+    return b
+
+
+def test_host_validation_without_gpu():
+    import long_context_sparse_24_b300 as lcsa
+    L = lcsa._lib
+    rows = lcsa.lcs_rows(lcsa.LCS_ROW_FP8_SPLIT, 512, 10, 0x1000, 0x2000, 0x3000)
+    pag = lcsa.lcs_paging(32, 4, 0x4000)
+    st = lcsa.lcs_state(rows, 0x5000, 8, rows)
+    comp = lcsa.lcs_compressor(0x6000, 0x7000, 4, 1)
+    by = ctypes.byref
+    # null batch
+    assert L.csa_compress(None, 0x1000, by(comp), by(st), by(rows), by(pag), None, None) == 1
+    # ratio not a power of two
+    bad = lcsa.lcs_compressor(0x6000, 0x7000, 3, 1)
+    assert L.csa_compress(by(_batch(lcsa)), 0x1000, by(bad), by(st), by(rows), by(pag), None, None) == 4
+    # HCA rejects overlapping windows
+    assert L.hca_compress(by(_batch(lcsa)), 0x1000, by(comp), by(st), by(rows), by(pag), None, None) == 4
+    # pending slots must be 2m for an overlapping compressor
+    st_bad = lcsa.lcs_state(rows, 0x5000, 4, rows)
+    assert L.csa_compress(by(_batch(lcsa)), 0x1000, by(comp), by(st_bad), by(rows), by(pag), None, None) == 2
+    # misaligned raw rows
+    assert L.csa_compress(by(_batch(lcsa)), 0x1001, by(comp), by(st), by(rows), by(pag), None, None) == 3
+    # unsupported head dim
+    rows_bad = lcsa.lcs_rows(lcsa.LCS_ROW_FP8_SPLIT, 256, 10, 0x1000, 0x2000, 0x3000)
+    assert L.csa_compress(by(_batch(lcsa)), 0x1000, by(comp), by(st), by(rows_bad), by(pag), None, None) == 4
+    keys = lcsa.lcs_index_keys(0x1000, 0x2000, 128, 10)
+    # indexer: 3 heads unsupported, k = 0 unsupported, missing workspace
+    args = lambda heads, k, ws, wsb: (by(_batch(lcsa)), 0x1000, 0x2000, None, heads, by(keys), by(pag), 4, k, 0,
+                                      0x3000, 0x4000, ws, wsb, None, None)
+    assert L.csa_index_topk(*args(3, 16, 0x8000, 1 << 20)) == 4
+    assert L.csa_index_topk(*args(4, 0, 0x8000, 1 << 20)) == 4
+    assert L.csa_index_topk(*args(4, 16, None, 0)) == 8
+    assert L.csa_index_topk(*args(4, 16, 0x8000, 1)) == 8
+    # attention: heads 24 unsupported; topk list missing
+    assert L.csa_attend(by(_batch(lcsa)), 0x1000, 24, 0x2000, None, 16, 4, by(rows), by(pag), by(st), 1.0,
+                        0x3000, None, None, 0, None, None) == 4
+    assert L.csa_attend(by(_batch(lcsa)), 0x1000, 64, None, None, 16, 4, by(rows), by(pag), by(st), 1.0,
+                        0x3000, None, None, 0, None, None) == 1
+
+
+def test_workspace_sizes():
+    import long_context_sparse_24_b300 as lcsa
+    b = lcsa.lcs_batch(32, 0x1000, 0x2000, 32, 1, 131072)
+    n = lcsa._lib.lcs_index_topk_workspace(ctypes.byref(b), 4, 512)
+    assert n >= 32 * (131072 // 4) * 4

@@ -1,0 +1,308 @@
+"""Stage-level parity of the CUDA path with the oracle (compression, indexer + top-k, attention).
+
+Each stage is fed seeded inputs; attention is fed the oracle's own quantised rows so that its
+comparison isolates the attention arithmetic.  Top-k index sets and counts are compared
+bit-exactly, indexer scores bit-exactly, stored rows to within one storage ulp, attention
+outputs within max-abs 3e-2 / rel-L2 1e-2.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from harness import *  # noqa: F401,F403
+from harness import DEV
+
+lcsa = pytest.importorskip("long_context_sparse_24_b300")
+from long_context_sparse_24_b300 import buffers  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+# ---------------------------------------------------------------------------------------- generator
+
+def test_gpu_generator_matches_numpy():
+    import synth.gpu as sg
+    sg.build()
+    out = torch.empty(70001, dtype=torch.bfloat16, device=DEV)
+    sg.normal_bf16(out, 5, 77, 12345)
+    ref = synth.normal_bf16(5, 77, 12345, 70001)
+    assert np.array_equal(out.view(torch.int16).cpu().numpy().view(np.uint16), ref)
+    pk = torch.empty(4099, dtype=torch.uint8, device=DEV)
+    sg.e2m1_packed(pk, 6, 78, 1000)
+    assert np.array_equal(pk.cpu().numpy(), synth.pack_e2m1(synth.e2m1_codes(6, 78, 1000, 8198)))
+    sc = torch.empty(5000, dtype=torch.uint8, device=DEV)
+    sg.ue8m0(sc, 7, 79, 3)
+    assert np.array_equal(sc.cpu().numpy(), synth.ue8m0_scales(7, 79, 3, 5000))
+
+
+# ---------------------------------------------------------------------------------------- compression
+
+def _compress_run(lengths, chunk_plan, m, overlap, dim, fmt, seed=21, block_order_seed=None):
+    """Compress len(lengths) sequences fed in calls: chunk_plan[c][b] new tokens of seq b in call c."""
+    S = len(lengths)
+    fmtc = buffers.row_format_code(fmt)
+    cap = max(lengths) + 256
+    bps = math.ceil(cap / 128)
+    order = None
+    if block_order_seed is not None:
+        order = np.random.default_rng(block_order_seed).permutation(S * bps).tolist()
+    new_cap = max(sum(c) for c in chunk_plan)
+    cache = buffers.alloc_layer(S, cap, dim, fmtc, m, overlap, new_cap, DEV, block_order=order)
+    w, bias = compressor_params(seed, 0, dim, m, overlap)
+    comp = lcsa.Compressor(to_dev_f32(w), to_dev_f32(bias), m, overlap)
+    raws = [raw_rows_gpu(seed, 0, b, lengths[b], dim) for b in range(S)]
+    st = dev_status()
+    pos = [0] * S
+    for call in chunk_plan:
+        after = [pos[b] + call[b] for b in range(S)]
+        batch = buffers.make_batch(after, call, DEV, max_seq_len=cap)
+        parts = [raws[b][pos[b]:after[b]] for b in range(S)]
+        raw = torch.cat(parts).contiguous() if batch.total_new else torch.empty((1, dim), dtype=torch.bfloat16, device=DEV)
+        fn = lcsa.csa_compress if overlap or m < 128 else lcsa.hca_compress
+        fn(batch, raw, comp, cache.state, cache.entries, cache.paging, st)
+        lcsa.lcs_window_commit(batch, cache.state, st)
+        pos = after
+    torch.cuda.synchronize()
+    assert_status_ok(st)
+    assert pos == list(lengths)
+    return cache, w, bias
+
+
+@pytest.mark.parametrize("m,overlap,dim,fmt", [(4, True, 512, "fp8_split"), (4, True, 128, "bf16"),
+                                               (128, False, 512, "fp8_split"), (1, False, 128, "fp8_split"),
+                                               (8, True, 128, "fp8_split"), (2, False, 512, "fp8_split")])
+def test_compress_matches_oracle(m, overlap, dim, fmt):
+    lengths = [1, 3, 300, 517] if m < 128 else [100, 300, 1100]
+    cache, w, bias = _compress_run(lengths, [lengths], m, overlap, dim, fmt, block_order_seed=3)
+    for b, L in enumerate(lengths):
+        raw = bits_to_f64(raw_rows_np(21, 0, b, L, dim))
+        nf = L // m
+        if nf:
+            orc = oracle.quantize_rows(oracle.compress_blocked(raw, w, bias, m, overlap), fmt)
+            gpu = read_rows(cache.entries, entry_rows_of(cache, b, range(nf)))
+            compare_quantized(gpu, orc, f"entries seq {b}")
+        # window ring: the last min(L,128) raw rows, quantised bit-exactly like the oracle
+        ps = np.arange(max(0, L - 128), L)
+        gw = read_rows(cache.state.window, b * 128 + ps % 128)
+        ow = oracle.quantize_rows(raw[ps], fmt)
+        for key in ("bf16", "nope", "rope", "scale"):
+            if key in ow:
+                assert np.array_equal(gw[key], ow[key]), f"window {key} seq {b}"
+        # pending ring holds the rows a future entry still needs
+        slots = cache.state.pending_slots
+        full = L // m
+        keep_lo = max(0, (full - 1) * m if overlap else full * m)
+        pend = cache.state.pending[b].view(torch.int16).cpu().numpy().view(np.uint16)
+        rb = raw_rows_np(21, 0, b, L, dim)
+        for p in range(keep_lo, L):
+            assert np.array_equal(pend[p % slots], rb[p])
+
+
+@pytest.mark.parametrize("m,overlap", [(4, True), (128, False)])
+def test_compress_incremental_equals_one_shot(m, overlap):
+    # decode-time appends (one token per call, ragged chunks) give the same bits as one prefill call
+    lengths = [263, 517, 130] if m == 4 else [300, 520, 129]
+    rng = np.random.default_rng(5)
+    plan, left = [], list(lengths)
+    while any(left):
+        call = []
+        for b in range(3):
+            c = min(left[b], int(rng.choice([0, 1, 1, 1, 3, 17, 64])))
+            call.append(c)
+            left[b] -= c
+        plan.append(call)
+    dim = 512
+    one, _, _ = _compress_run(lengths, [lengths], m, overlap, dim, "fp8_split")
+    inc, _, _ = _compress_run(lengths, plan, m, overlap, dim, "fp8_split")
+    for b, L in enumerate(lengths):
+        rows = entry_rows_of(one, b, range(L // m))
+        a, c = read_rows(one.entries, rows), read_rows(inc.entries, rows)
+        for key in ("nope", "rope", "scale"):
+            assert np.array_equal(a[key], c[key]), (b, key)
+    for key in ("nope", "rope", "scale"):
+        assert torch.equal(getattr(one.state.window, key), getattr(inc.state.window, key))
+
+
+# ---------------------------------------------------------------------------------------- indexer
+
+def _index_case(lengths, new, m, k, heads, rank, relu, scaled, seed=31, ties=False):
+    S = len(lengths)
+    cap = max(lengths) + 128
+    order = np.random.default_rng(seed).permutation(S * math.ceil(cap / 128)).tolist()
+    cache = buffers.alloc_layer(S, cap, 512, lcsa.LCS_ROW_FP8_SPLIT, m, True, 0, DEV, index_rank=rank,
+                                block_order=order)
+    batch = buffers.make_batch(lengths, new, DEV, max_seq_len=cap)
+    kcs, kss, qcs, qss, hws = [], [], [], [], []
+    for b in range(S):
+        ne = lengths[b] // m
+        kc, ks = index_inputs(seed, 0, b, ne, rank, scaled)
+        if ties:
+            kc[:] = kc[:1]
+            ks[:] = ks[:1]
+        rows = entry_rows_of(cache, b, range(ne))
+        if ne:
+            cache.keys.fp4[torch.as_tensor(rows, device=DEV)] = u8(synth.pack_e2m1(kc))
+            cache.keys.scale[torch.as_tensor(rows, device=DEV)] = u8(ks)
+        qc, qs, hw = query_index_inputs(seed, 0, b, lengths[b] - new[b], new[b], heads, rank, scaled)
+        kcs.append(kc); kss.append(ks); qcs.append(qc); qss.append(qs); hws.append(hw)
+    qc_all = np.concatenate(qcs)
+    q_fp4 = u8(synth.pack_e2m1(qc_all))
+    q_sc = u8(np.concatenate(qss))
+    hw_all = to_dev_f32(np.concatenate(hws))
+    return cache, batch, kcs, kss, qcs, qss, hws, q_fp4, q_sc, hw_all
+
+
+@pytest.mark.parametrize("heads,rank,relu,scaled,new", [
+    (4, 128, False, True, [1, 1, 1]),
+    (4, 128, False, True, [1, 5, 40]),
+    (1, 64, False, False, [1, 7, 33]),
+    (2, 128, True, True, [2, 1, 9]),
+    (8, 64, False, True, [1, 3, 17]),
+    (4, 128, True, True, [1, 1, 1]),
+])
+def test_index_scores_exact_and_topk_sets(heads, rank, relu, scaled, new):
+    m, k = 4, 24
+    lengths = [37, 600, 2100]
+    cache, batch, kcs, kss, qcs, qss, hws, q_fp4, q_sc, hw = _index_case(lengths, new, m, k, heads, rank, relu, scaled)
+    flags = lcsa.LCS_INDEX_RELU if relu else 0
+    T = batch.total_new
+    ld = (max(lengths) + 128) // m
+    scores = torch.full((T, ld), float("nan"), device=DEV)
+    st = dev_status()
+    lcsa.csa_index_scores(batch, q_fp4, q_sc, hw, heads, cache.keys, cache.paging, m, flags, scores, ld, st)
+    out_idx = torch.full((T, k), -7, dtype=torch.int32, device=DEV)
+    out_cnt = torch.full((T,), -7, dtype=torch.int32, device=DEV)
+    wsb = lcsa.lcs_index_topk_workspace(batch, m, k)
+    ws = workspace(wsb)
+    lcsa.csa_index_topk(batch, q_fp4, q_sc, hw, heads, cache.keys, cache.paging, m, k, flags, out_idx, out_cnt,
+                        ws, wsb, st)
+    torch.cuda.synchronize()
+    assert_status_ok(st)
+    sc = scores.cpu().numpy(); oi = out_idx.cpu().numpy(); oc = out_cnt.cpu().numpy()
+    qi = 0
+    for b in range(len(lengths)):
+        ref = oracle.index_scores(qcs[b], qss[b], hws[b], kcs[b], kss[b], relu)
+        for i in range(new[b]):
+            t = lengths[b] - new[b] + i
+            n = oracle.visible_entries(t, m)
+            assert np.array_equal(sc[qi, :n].astype(np.float64), ref[i, :n]), f"scores seq {b} query {i}"
+            sel = oracle.topk_select(ref[i, :n], k)
+            assert oc[qi] == len(sel)
+            assert np.array_equal(oi[qi, :len(sel)], sel), f"top-k seq {b} query {i}"
+            assert np.all(oi[qi, len(sel):] == -1)
+            qi += 1
+
+
+def test_topk_ties_take_lowest_index():
+    m, k = 4, 24
+    lengths, new = [400, 1000], [1, 2]
+    cache, batch, *_, q_fp4, q_sc, hw = _index_case(lengths, new, m, k, 4, 128, False, True, ties=True)
+    out_idx = torch.empty((batch.total_new, k), dtype=torch.int32, device=DEV)
+    out_cnt = torch.empty((batch.total_new,), dtype=torch.int32, device=DEV)
+    wsb = lcsa.lcs_index_topk_workspace(batch, m, k)
+    lcsa.csa_index_topk(batch, q_fp4, q_sc, hw, 4, cache.keys, cache.paging, m, k, 0, out_idx, out_cnt,
+                        workspace(wsb), wsb)
+    torch.cuda.synchronize()
+    assert np.array_equal(out_idx.cpu().numpy(), np.tile(np.arange(k), (batch.total_new, 1)))
+
+
+# ---------------------------------------------------------------------------------------- attention
+
+def _attend_case(kind, lengths, new, heads, dim, fmt, m, k, seed=41, scale=None):
+    """Fill an entry cache / window ring / new rows with oracle-quantised rows and run one call."""
+    S = len(lengths)
+    fmtc = buffers.row_format_code(fmt)
+    cap = max(lengths) + 128
+    order = np.random.default_rng(seed).permutation(S * math.ceil(cap / 128)).tolist()
+    T = sum(new)
+    cache = buffers.alloc_layer(S, cap, dim, fmtc, m, kind == "csa", T, DEV, block_order=order)
+    batch = buffers.make_batch(lengths, new, DEV, max_seq_len=cap)
+    rng = np.random.default_rng(seed)
+    ent_deq, win_deq, sels, qs = [], [], [], []
+    for b in range(S):
+        L, q_n = lengths[b], new[b]
+        n0 = L - q_n
+        ne = L // m
+        ent = oracle.quantize_rows(rng.standard_normal((max(ne, 1), dim)), fmt)
+        if ne:
+            sub = {kk: v[:ne] for kk, v in ent.items() if kk != "format"}
+            sub["format"] = ent["format"]
+            write_rows(cache.entries, entry_rows_of(cache, b, range(ne)), sub)
+        ent_deq.append(ent["deq"][:ne])
+        # raw rows of the last 128 + new positions
+        p_lo = max(0, n0 - 128)
+        raw = bits_to_f64(raw_rows_np(seed, 0, b, L - p_lo, dim, start=p_lo))
+        wq = oracle.quantize_rows(raw, fmt)
+        wd = np.zeros((L, dim)); wd[p_lo:L] = wq["deq"]
+        win_deq.append(wd)
+        ring_pos = np.arange(p_lo, n0)
+        if ring_pos.size:
+            sub = {kk: v[:n0 - p_lo] for kk, v in wq.items() if kk not in ("format", "deq")}
+            sub["format"] = wq["format"]
+            write_rows(cache.state.window, b * 128 + ring_pos % 128, sub)
+        sub = {kk: v[n0 - p_lo:] for kk, v in wq.items() if kk not in ("format", "deq")}
+        sub["format"] = wq["format"]
+        q0 = sum(new[:b])
+        if q_n:
+            write_rows(cache.state.new_rows, np.arange(q0, q0 + q_n), sub)
+        for i in range(q_n):
+            t = n0 + i
+            n = oracle.visible_entries(t, m)
+            if kind == "csa":
+                s = np.sort(rng.choice(n, size=min(k, n), replace=False)) if n else np.zeros(0, np.int64)
+                sels.append(s)
+        qs.append(queries_np(seed, 0, b, n0, q_n, heads, dim))
+    q_bits = np.concatenate(qs)
+    q = to_dev_bf16_bits(q_bits)
+    out = torch.empty((T, heads, dim), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((T, heads), dtype=torch.float32, device=DEV)
+    scale = scale if scale is not None else 1 / math.sqrt(dim)
+    st = dev_status()
+    if kind == "csa":
+        idx = np.full((T, k), -1, np.int32)
+        for i, s in enumerate(sels):
+            idx[i, :len(s)] = s
+        idx_t = torch.from_numpy(idx).to(DEV)
+        cnt_t = torch.tensor([len(s) for s in sels], dtype=torch.int32, device=DEV)
+        wsb = lcsa.lcs_attend_workspace(batch, heads, dim, k + 128)
+        lcsa.csa_attend(batch, q, heads, idx_t, cnt_t, k, m, cache.entries, cache.paging, cache.state, scale, out,
+                        lse, workspace(wsb), wsb, st)
+    else:
+        wsb = lcsa.lcs_attend_workspace(batch, heads, dim, cap // m + 128)
+        lcsa.hca_attend(batch, q, heads, m, cache.entries, cache.paging, cache.state, scale, out, lse,
+                        workspace(wsb), wsb, st)
+    torch.cuda.synchronize()
+    assert_status_ok(st)
+    o = bf16_tensor_to_f64(out); l = lse.cpu().numpy()
+    qf = bits_to_f64(q_bits)
+    qi = 0
+    for b in range(S):
+        n0 = lengths[b] - new[b]
+        for i in range(new[b]):
+            t = n0 + i
+            if kind == "csa":
+                rows = oracle.csa_query_rows(t, sels[qi], ent_deq[b], win_deq[b])
+            else:
+                rows = oracle.hca_query_rows(t, m, ent_deq[b], win_deq[b])
+            ro, rl = oracle.attend(qf[qi], rows, scale)
+            check_outputs(o[qi], ro, f"{kind} seq {b} query {i}")
+            assert np.allclose(l[qi], rl, atol=2e-3, rtol=1e-4), f"lse seq {b} query {i}"
+            qi += 1
+
+
+@pytest.mark.parametrize("kind,lengths,new,heads,dim,fmt,m,k", [
+    ("csa", [2000, 4100, 300], [1, 1, 1], 64, 512, "fp8_split", 4, 512),       # decode, split-KV
+    ("csa", [900, 2200], [40, 9], 64, 512, "fp8_split", 4, 64),                # prefill chunk
+    ("csa", [3000], [3], 128, 512, "fp8_split", 4, 256),                       # 128 heads = 2 groups
+    ("csa", [50, 700], [50, 20], 8, 128, "bf16", 4, 64),                       # small-model rows
+    ("csa", [600], [5], 8, 128, "fp8_split", 4, 64),
+    ("csa", [130, 7], [1, 7], 16, 512, "fp8_split", 4, 32),                    # N(t) < k, short seqs
+    ("hca", [20000, 1500, 128], [1, 1, 1], 64, 512, "fp8_split", 128, 0),      # HCA decode
+    ("hca", [3000], [17], 64, 512, "fp8_split", 128, 0),
+])
+def test_attend_matches_oracle(kind, lengths, new, heads, dim, fmt, m, k):
+    _attend_case(kind, lengths, new, heads, dim, fmt, m, k)
