@@ -1,0 +1,445 @@
+"""Throughput of the CSA decode hot path (compress -> lightning indexer top-k -> attention -> window
+commit) on the 32-sequence x 131072-token workload: 64 query heads, shared KV dim 512 (448 FP8 +
+64 BF16 RoPE dims), m=4 overlapped compression (32768 entries per sequence), indexer rank 128 with
+4 heads in FP4 E2M1 with per-32 UE8M0 scales, top-k 512, window 128.
+
+One step = one decode token for every sequence through the whole path.  Inputs are seeded
+synthetic tensors already resident in HBM; L2 is flushed (a 256 MB write) between timed steps.
+Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+WL = synth.CONFIGS["csa_decode"]
+METRIC = "CSA/HCA attention queries/s at 128K-1M ctx"
+UNIT = "queries/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def workload_config(extra=None):
+    cfg = {"workload": WL.name, "num_seqs": WL.num_seqs, "ctx_len": WL.ctx_len, "new_tokens_per_seq": 1,
+           "heads": WL.heads, "kv_dim": WL.dim, "row_format": "fp8_e4m3(448)+bf16_rope(64)+f32_scale",
+           "m": WL.m, "overlap": True, "index_heads": WL.index_heads, "index_rank": WL.index_rank,
+           "index_format": "fp4_e2m1+ue8m0/32", "top_k": WL.top_k, "window": WL.window, "seed": WL.seed,
+           "l2": "flushed between timed steps (256 MB write)", "data": "synthetic"}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+# ---------------------------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out" if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else "",
+                                 f".clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1])); mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d.get("hbm_gbs", 6400.0), "measured"
+    return 6400.0, "fallback"
+
+
+# ---------------------------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------------------------
+
+def run_gpu(args, rank, world, local):
+    import torch
+    import synth.gpu as sg
+    import long_context_sparse_24_b300 as lcsa
+    from long_context_sparse_24_b300.layer import Layer
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if lcsa.lcs_device_check() != 0:
+        raise SystemExit("liblcsa needs a compute-capability 10.3 GPU")
+    S, L, H, D = WL.num_seqs, WL.ctx_len, WL.heads, WL.dim
+    Hi, r, k, m = WL.index_heads, WL.index_rank, WL.top_k, WL.m
+    steps_total = args.warmup + args.steps
+    cap = L + 128 * math.ceil((steps_total + 1) / 128) + 128
+    seed = WL.seed + 1000 * rank            # each rank serves its own sequences
+    layer = Layer("csa", S, cap, H, D, lcsa.LCS_ROW_FP8_SPLIT, m, top_k=k, index_heads=Hi, index_rank=r,
+                  max_new=1, device=dev)
+    # compressor parameters (w ~ N(0,1)/16, bias ~ N(0,1)/2)
+    w = synth.bf16_bits_to_f32(synth.normal_bf16(seed, synth.tensor_id(synth.COMP_W), 0, D)) / 16
+    bias = synth.bf16_bits_to_f32(synth.normal_bf16(seed, synth.tensor_id(synth.COMP_B), 0, 2 * m)) / 2
+    layer.set_compressor(torch.from_numpy(w.astype(np.float32)).to(dev),
+                         torch.from_numpy(bias.astype(np.float32)).to(dev))
+    # ---- build the cached context: L raw tokens per sequence, compressed by the library
+    chunk = 16384
+    raw_chunk = torch.empty((S * chunk, D), dtype=torch.bfloat16, device=dev)
+    for c0 in range(0, L, chunk):
+        n = min(chunk, L - c0)
+        for b in range(S):
+            sg.normal_bf16(raw_chunk[b * n:(b + 1) * n], seed, synth.tensor_id(synth.RAW, 0, b), c0 * D)
+        layer.fill(layer.batch([c0 + n] * S, [n] * S), raw_chunk[:S * n])
+    del raw_chunk
+    # ---- indexer keys of every entry the run will create (identity paging: contiguous per sequence)
+    bps = layer.cache.paging.max_blocks_per_seq
+    n_ent = cap // m
+    for b in range(S):
+        r0 = b * bps * 32
+        sg.e2m1_packed(layer.cache.keys.fp4[r0:r0 + n_ent], seed, synth.tensor_id(synth.IDX_K, 0, b), 0)
+        sg.ue8m0(layer.cache.keys.scale[r0:r0 + n_ent], seed, synth.tensor_id(synth.IDX_KS, 0, b), 0)
+    # ---- per-step inputs (decode token L+s of every sequence)
+    raw_steps = torch.empty((steps_total, S, D), dtype=torch.bfloat16, device=dev)
+    q_steps = torch.empty((steps_total, S, H, D), dtype=torch.bfloat16, device=dev)
+    iq_steps = torch.empty((steps_total, S, Hi, r // 2), dtype=torch.uint8, device=dev)
+    iqs_steps = torch.empty((steps_total, S, Hi, r // 32), dtype=torch.uint8, device=dev)
+    hw_np = np.stack([synth.head_weights(seed, synth.tensor_id(synth.HEAD_W, 0, b), L * Hi, steps_total * Hi)
+                      .reshape(steps_total, Hi) for b in range(S)], axis=1)
+    hw_steps = torch.from_numpy(np.ascontiguousarray(hw_np)).to(dev)
+    for s in range(steps_total):
+        t = L + s
+        for b in range(S):
+            sg.normal_bf16(raw_steps[s, b], seed, synth.tensor_id(synth.RAW, 0, b), t * D)
+            sg.normal_bf16(q_steps[s, b], seed, synth.tensor_id(synth.QUERY, 0, b), t * H * D)
+            sg.e2m1_packed(iq_steps[s, b], seed, synth.tensor_id(synth.IDX_Q, 0, b), t * Hi * r)
+            sg.ue8m0(iqs_steps[s, b], seed, synth.tensor_id(synth.IDX_QS, 0, b), t * Hi * r // 32)
+    # ---- static step buffers + CUDA graph of one step
+    raw_in = torch.empty((S, D), dtype=torch.bfloat16, device=dev)
+    q_in = torch.empty((S, H, D), dtype=torch.bfloat16, device=dev)
+    iq_in = torch.empty((S, Hi, r // 2), dtype=torch.uint8, device=dev)
+    iqs_in = torch.empty((S, Hi, r // 32), dtype=torch.uint8, device=dev)
+    hw_in = torch.empty((S, Hi), dtype=torch.float32, device=dev)
+    out = torch.empty((S, H, D), dtype=torch.bfloat16, device=dev)
+    cu_new = torch.arange(S + 1, dtype=torch.int32, device=dev)
+    seq_len = torch.full((S,), L + 1, dtype=torch.int32, device=dev)
+    batch = layer.batch([cap] * S, [1] * S, cu_new=cu_new, seq_len=seq_len)
+
+    def load_step(s):
+        raw_in.copy_(raw_steps[s]); q_in.copy_(q_steps[s]); iq_in.copy_(iq_steps[s])
+        iqs_in.copy_(iqs_steps[s]); hw_in.copy_(hw_steps[s]); seq_len.fill_(L + s + 1)
+
+    try:
+        evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(5)]
+    except TypeError:  # torch without event-record nodes in graphs: stage times from separate graphs
+        evs = None
+
+    def step_body(with_events=True):
+        if with_events and evs:
+            evs[0].record()
+        layer.compress(batch, raw_in)
+        if with_events and evs:
+            evs[1].record()
+        layer.select(batch, iq_in, iqs_in, hw_in)
+        if with_events and evs:
+            evs[2].record()
+        layer.attend(batch, q_in, out)
+        if with_events and evs:
+            evs[3].record()
+        layer.commit(batch)
+        if with_events and evs:
+            evs[4].record()
+
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    # warm-up step 0 runs eagerly (first launches set the kernels' shared-memory attributes);
+    # the step is then captured once and replayed for every later decode position
+    load_step(0)
+    step_body(with_events=False)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step_body()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps_total)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps_total)]
+    stage_ms = []
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for s in range(1, steps_total):
+            load_step(s)
+            flush.zero_()
+            starts[s].record()
+            graph.replay()
+            ends[s].record()
+            if s >= args.warmup and evs:
+                torch.cuda.synchronize()
+                stage_ms.append([evs[i].elapsed_time(evs[i + 1]) for i in range(4)])
+        torch.cuda.synchronize()
+    status_ok = True
+    if int(layer.status.item()) != 0:
+        status_ok = False
+    per_step = [starts[s].elapsed_time(ends[s]) for s in range(args.warmup, steps_total)]
+    ms = statistics.mean(per_step)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    stages = [statistics.mean(x[i] for x in stage_ms) for i in range(4)] if stage_ms else [float("nan")] * 4
+    splits_used = layer.attend_ws_bytes > 0
+    launches_per_step = 2 + 2 + (2 if splits_used else 1) + 1
+    # ---- roofline of the dominant call (lightning indexer: score scan + top-k select)
+    hbm, peak_kind = measured_peaks()
+    n_vis = [(L + s + 1) // m for s in range(args.warmup, steps_total)]
+    key_bytes = r // 2 + r // 32
+    alg_bytes = statistics.mean(S * (n * key_bytes + Hi * key_bytes + Hi * 4 + k * 4 + 4) for n in n_vis)
+    idx_ms = stages[1]
+    achieved = alg_bytes / (idx_ms * 1e-3) / 1e9
+    roofline = {"kernel": "csa_index_topk (index_score_kernel + topk_select_kernel)", "bound": "hbm",
+                "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
+                "algorithmic_bytes_per_launch": int(alg_bytes), "traffic": None}
+    # ---- end to end through the public API with host buffers (pinned), copies in the timed region
+    e2e = run_e2e(torch, layer, batch, graph, raw_in, q_in, iq_in, iqs_in, hw_in, out, seq_len, raw_steps,
+                  q_steps, iq_steps, iqs_steps, hw_steps, args, L, S, flush)
+    return {"ms": ms, "stages": stages, "clocks": clk.summary(), "roofline": roofline, "e2e": e2e,
+            "launches": launches_per_step * args.steps, "status_ok": status_ok,
+            "per_rank_queries": S}
+
+
+def run_e2e(torch, layer, batch, graph, raw_in, q_in, iq_in, iqs_in, hw_in, out, seq_len, raw_steps, q_steps,
+            iq_steps, iqs_steps, hw_steps, args, L, S, flush):
+    """Same step with its inputs coming from pinned host memory and the output read back."""
+    n = min(args.steps, 8)
+    host_in = [t[:n].cpu().pin_memory() for t in (raw_steps, q_steps, iq_steps, iqs_steps, hw_steps)]
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t[0].numel() * t.element_size() for t in host_in) + seq_len.numel() * 4
+    d2h = out.numel() * out.element_size()
+    seq_host = torch.empty(seq_len.shape, dtype=torch.int32).pin_memory()
+    # rewind the state positions: re-run decode positions L+warmup+steps .. (new tokens, same shapes)
+    base = L + args.warmup + args.steps
+    times = []
+    st = torch.cuda.current_stream()
+    for s in range(n):
+        seq_host.fill_(base + s + 1)
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True); e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        raw_in.copy_(host_in[0][s], non_blocking=True)
+        q_in.copy_(host_in[1][s], non_blocking=True)
+        iq_in.copy_(host_in[2][s], non_blocking=True)
+        iqs_in.copy_(host_in[3][s], non_blocking=True)
+        hw_in.copy_(host_in[4][s], non_blocking=True)
+        seq_len.copy_(seq_host, non_blocking=True)
+        graph.replay()
+        host_out.copy_(out, non_blocking=True)
+        e1.record()
+        st.synchronize()
+        times.append(e0.elapsed_time(e1))
+    ms = statistics.mean(times)
+    return {"value": round(S / (ms * 1e-3), 1), "unit": UNIT, "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": n,
+            "api": "layer.step body (csa_compress, csa_index_topk, csa_attend, lcs_window_commit) as one CUDA graph"}
+
+
+# ---------------------------------------------------------------------------------------------
+# oracle (CPU) arm
+# ---------------------------------------------------------------------------------------------
+
+class OracleDecode:
+    """The fp64 oracle serving decode steps of a few workload sequences."""
+
+    def __init__(self, n_seqs: int, seed: int):
+        import oracle
+        self.o = oracle
+        D, m, r, Hi = WL.dim, WL.m, WL.index_rank, WL.index_heads
+        self.w = (synth.bf16_bits_to_f32(synth.normal_bf16(seed, synth.tensor_id(synth.COMP_W), 0, D)) / 16).astype(np.float64)
+        self.bias = (synth.bf16_bits_to_f32(synth.normal_bf16(seed, synth.tensor_id(synth.COMP_B), 0, 2 * m)) / 2).astype(np.float64)
+        self.seed = seed
+        self.seqs = []
+        L = WL.ctx_len
+        for b in range(n_seqs):
+            raw = synth.bf16_bits_to_f32(synth.normal_bf16(seed, synth.tensor_id(synth.RAW, 0, b), 0, (L + 64) * D))
+            raw = raw.reshape(L + 64, D).astype(np.float64)
+            ent = oracle.quantize_rows(oracle.compress_blocked(raw[:L], self.w, self.bias, m, True), "fp8_split")["deq"]
+            win = oracle.quantize_rows(raw[L - 128:L], "fp8_split")["deq"]
+            n_ent = (L + 64) // m
+            kc = synth.e2m1_codes(seed, synth.tensor_id(synth.IDX_K, 0, b), 0, n_ent * r).reshape(n_ent, r)
+            ks = synth.ue8m0_scales(seed, synth.tensor_id(synth.IDX_KS, 0, b), 0, n_ent * r // 32).reshape(n_ent, r // 32)
+            self.seqs.append({"raw": raw, "ent": list(ent), "win": list(win), "t": L, "kc": kc, "ks": ks})
+
+    def step(self, b: int):
+        """Decode the next token of sequence b: compress, index + top-k, attend."""
+        o, s = self.o, self.seqs[b]
+        D, H, m, r, Hi, k = WL.dim, WL.heads, WL.m, WL.index_rank, WL.index_heads, WL.top_k
+        t = s["t"]
+        if (t + 1) % m == 0:
+            e = o.compress(s["raw"][:t + 1], self.w, self.bias, m, True, (t + 1) // m - 1, 1)
+            s["ent"].append(o.quantize_rows(e, "fp8_split")["deq"][0])
+        s["win"].append(o.quantize_rows(s["raw"][t:t + 1], "fp8_split")["deq"][0])
+        s["win"] = s["win"][-128:]
+        qc = synth.e2m1_codes(self.seed, synth.tensor_id(synth.IDX_Q, 0, b), t * Hi * r, Hi * r).reshape(1, Hi, r)
+        qs = synth.ue8m0_scales(self.seed, synth.tensor_id(synth.IDX_QS, 0, b), t * Hi * r // 32, Hi * r // 32)
+        hw = synth.head_weights(self.seed, synth.tensor_id(synth.HEAD_W, 0, b), t * Hi, Hi).reshape(1, Hi)
+        n = o.visible_entries(t, m)
+        sc = o.index_scores(qc, qs.reshape(1, Hi, r // 32), hw, s["kc"][:n], s["ks"][:n])
+        sel = o.topk_select(sc[0], k)
+        q = synth.bf16_bits_to_f32(synth.normal_bf16(self.seed, synth.tensor_id(synth.QUERY, 0, b), t * H * D, H * D))
+        rows = np.concatenate([np.asarray(s["ent"])[sel], np.asarray(s["win"])])
+        out, _ = o.attend(q.reshape(H, D).astype(np.float64), rows, 1 / math.sqrt(D))
+        s["t"] = t + 1
+        return out
+
+
+def oracle_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(budget_s: float = 12.0, n_seqs: int = 2):
+    od = OracleDecode(n_seqs, WL.seed)
+    done, t0 = 0, time.perf_counter()
+    while True:
+        od.step(done % n_seqs)
+        done += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or done >= 400:
+            break
+    return {"value": round(done / el, 3), "unit": UNIT, "cores": oracle_cores(), "kind": "oracle",
+            "sample": f"{done} decode queries of {n_seqs} workload sequences (131072-token contexts; cache "
+                      f"built untimed), fp64 numpy oracle, {el:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    od = OracleDecode(2, WL.seed)
+    for i in range(args.warmup):
+        od.step(i % 2)
+    times = []
+    per_step = 2                     # bounded sample: 2 decode queries per step
+    for s in range(args.steps):
+        t0 = time.perf_counter()
+        for b in range(per_step):
+            od.step(b)
+        times.append(time.perf_counter() - t0)
+    ms = statistics.mean(times) * 1e3
+    val = per_step / (ms * 1e-3)
+    cores = oracle_cores()
+    return {"metric": METRIC, "value": round(val, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": workload_config({"sample_per_step": f"{per_step} decode queries"}),
+            "cpu_baseline": {"value": round(val, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"{per_step} decode queries per step of 2 workload sequences"},
+            "e2e": {"value": round(val, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line))
+        return
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+    res = run_gpu(args, rank, world, local)
+    if rank == 0:
+        S_all = res["per_rank_queries"] * world
+        value = S_all / (res["ms"] * 1e-3)
+        line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": round(res["ms"], 5), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "fp8/fp4 storage, bf16/f16 MMA, fp32 accumulate",
+                "data": "synthetic",
+                "config": workload_config({"parallelism": f"replicas x{world} (independent sequences per GPU)",
+                                           "stage_ms": {k: round(v, 5) for k, v in zip(
+                                               ["compress", "index_topk", "attend", "window_commit"],
+                                               res["stages"])}}),
+                "roofline": res["roofline"], "clocks": res["clocks"], "e2e": res["e2e"],
+                "gpu_launches": res["launches"], "device_status_ok": res["status_ok"]}
+        if not args.no_cpu_baseline and world == 1:
+            line["cpu_baseline"] = cpu_baseline()
+        print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()
