@@ -183,6 +183,23 @@ lcs_status csa_index_scores(const lcs_batch* batch, const uint8_t* q_fp4, const 
                             const lcs_paging* paging, int32_t m, int32_t flags, float* out_scores,
                             int64_t ld, int32_t* dev_status, void* stream);
 
+/* Same as csa_index_topk for callers that cannot allocate device memory (for example code
+ * running while another framework captures a CUDA graph, or a runtime that hands out all device
+ * memory from its own pool at start-up): no workspace argument; the scratch is a fixed array of
+ * LCSA_NOALLOC_SCRATCH_BYTES in the library's device image, reserved on every GPU that loads the
+ * library until the process exits.  Not a step of the method: the pages have no counterpart.
+ *  - Requests needing more scratch than that (lcs_index_topk_workspace(batch, m, k) >
+ *    LCSA_NOALLOC_SCRATCH_BYTES) return LCS_ERR_WORKSPACE and launch nothing.
+ *  - Runs on the current device.  Its first call on a device looks up the array's device
+ *    address (cudaGetSymbolAddress); make that first call before any stream capture.
+ *  - Calls no allocator.  All calls share the array: calls whose kernels overlap on the GPU
+ *    race and must be ordered by the caller. */
+#define LCSA_NOALLOC_SCRATCH_BYTES (8u << 20)
+lcs_status csa_index_topk_noalloc(const lcs_batch* batch, const uint8_t* q_fp4, const uint8_t* q_scale,
+                                  const float* head_w, int32_t heads, const lcs_index_keys* keys,
+                                  const lcs_paging* paging, int32_t m, int32_t k, int32_t flags,
+                                  int32_t* out_idx, int32_t* out_cnt, int32_t* dev_status, void* stream);
+
 /* --- attention (x-techcon section 2, CSA step 3 and the HCA paragraph) -----------------------
  * For query i (position t of sequence b) and every head h: one softmax over the rows
  *   CSA: the entries topk_idx[i][0..cnt) (cnt = topk_cnt[i], or the count of non-negative

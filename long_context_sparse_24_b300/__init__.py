@@ -82,6 +82,8 @@ _SIGS = {
                                c_i32, c_i32, c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
     "csa_index_scores": (c_i32, [P(lcs_batch), c_vp, c_vp, c_vp, c_i32, P(lcs_index_keys), P(lcs_paging), c_i32,
                                  c_i32, c_vp, c_i64, c_vp, c_vp]),
+    "csa_index_topk_noalloc": (c_i32, [P(lcs_batch), c_vp, c_vp, c_vp, c_i32, P(lcs_index_keys), P(lcs_paging),
+                                       c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp]),
     "lcs_attend_workspace": (c_sz, [P(lcs_batch), c_i32, c_i32, c_i32]),
     "csa_attend": (c_i32, [P(lcs_batch), c_vp, c_i32, c_vp, c_vp, c_i32, c_i32, P(lcs_rows), P(lcs_paging),
                            P(lcs_state), ctypes.c_float, c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
@@ -248,6 +250,19 @@ def csa_index_scores(batch: Batch, q_fp4, q_scale, head_w, heads: int, keys: Ind
     _check(_lib.csa_index_scores(ctypes.byref(b), _ptr(q_fp4), _ptr(q_scale), _ptr(head_w), heads,
                                  ctypes.byref(kk), ctypes.byref(p), m, flags, _ptr(out_scores), ld,
                                  _ptr(dev_status), _stream(stream)), "csa_index_scores")
+
+
+NOALLOC_SCRATCH_BYTES = 8 << 20
+
+
+def csa_index_topk_noalloc(batch: Batch, q_fp4, q_scale, head_w, heads: int, keys: IndexKeys, paging: Paging,
+                           m: int, k: int, flags: int, out_idx, out_cnt, dev_status=None, stream=None) -> None:
+    """csa_index_topk without a workspace argument, for callers that cannot allocate: the scratch
+    is the library's fixed device array (NOALLOC_SCRATCH_BYTES).  Calls must not overlap on the GPU."""
+    b, kk, p = batch.c(), keys.c(), paging.c()
+    _check(_lib.csa_index_topk_noalloc(ctypes.byref(b), _ptr(q_fp4), _ptr(q_scale), _ptr(head_w), heads,
+                                       ctypes.byref(kk), ctypes.byref(p), m, k, flags, _ptr(out_idx), _ptr(out_cnt),
+                                       _ptr(dev_status), _stream(stream)), "csa_index_topk_noalloc")
 
 
 def lcs_attend_workspace(batch: Batch, heads: int, dim: int, max_rows: int) -> int:
