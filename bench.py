@@ -144,8 +144,9 @@ def run_gpu(args, rank, world, local):
         raise SystemExit("liblcsa needs a compute-capability 10.3 GPU")
     S, L, H, D = WL.num_seqs, WL.ctx_len, WL.heads, WL.dim
     Hi, r, k, m = WL.index_heads, WL.index_rank, WL.top_k, WL.m
-    steps_total = args.warmup + args.steps
-    cap = L + 128 * math.ceil((steps_total + 1) / 128) + 128
+    n_stage = 5                              # extra replays of an instrumented graph (stage times)
+    steps_total = args.warmup + args.steps + n_stage
+    cap = L + 128 * math.ceil((steps_total + 1) / 128) + 256
     seed = WL.seed + 1000 * rank            # each rank serves its own sequences
     layer = Layer("csa", S, cap, H, D, lcsa.LCS_ROW_FP8_SPLIT, m, top_k=k, index_heads=Hi, index_rank=r,
                   max_new=1, device=dev)
@@ -227,9 +228,13 @@ def run_gpu(args, rank, world, local):
     load_step(0)
     step_body(with_events=False)
     torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
+    graph = torch.cuda.CUDAGraph()             # the timed step: kernels only
     with torch.cuda.graph(graph):
-        step_body()
+        step_body(with_events=False)
+    graph_ev = torch.cuda.CUDAGraph()          # the same step with event nodes between the calls
+    with torch.cuda.graph(graph_ev):
+        step_body(with_events=True)
+    timed_end = args.warmup + args.steps
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps_total)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps_total)]
     stage_ms = []
@@ -238,20 +243,24 @@ def run_gpu(args, rank, world, local):
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
-        for s in range(1, steps_total):
+        for s in range(1, timed_end):
             load_step(s)
             flush.zero_()
             starts[s].record()
             graph.replay()
             ends[s].record()
-            if s >= args.warmup and evs:
-                torch.cuda.synchronize()
-                stage_ms.append([evs[i].elapsed_time(evs[i + 1]) for i in range(4)])
         torch.cuda.synchronize()
+    for s in range(timed_end, steps_total):      # stage breakdown (not part of the timed steps)
+        load_step(s)
+        flush.zero_()
+        graph_ev.replay()
+        torch.cuda.synchronize()
+        if evs:
+            stage_ms.append([evs[i].elapsed_time(evs[i + 1]) for i in range(4)])
     status_ok = True
     if int(layer.status.item()) != 0:
         status_ok = False
-    per_step = [starts[s].elapsed_time(ends[s]) for s in range(args.warmup, steps_total)]
+    per_step = [starts[s].elapsed_time(ends[s]) for s in range(args.warmup, timed_end)]
     ms = statistics.mean(per_step)
     if world > 1:
         import torch.distributed as dist
@@ -263,7 +272,7 @@ def run_gpu(args, rank, world, local):
     launches_per_step = 2 + 2 + (2 if splits_used else 1) + 1
     # ---- roofline of the dominant call (lightning indexer: score scan + top-k select)
     hbm, peak_kind = measured_peaks()
-    n_vis = [(L + s + 1) // m for s in range(args.warmup, steps_total)]
+    n_vis = [(L + s + 1) // m for s in range(timed_end, steps_total)]
     key_bytes = r // 2 + r // 32
     alg_bytes = statistics.mean(S * (n * key_bytes + Hi * key_bytes + Hi * 4 + k * 4 + 4) for n in n_vis)
     idx_ms = stages[1]
@@ -290,7 +299,7 @@ def run_e2e(torch, layer, batch, graph, raw_in, q_in, iq_in, iqs_in, hw_in, out,
     d2h = out.numel() * out.element_size()
     seq_host = torch.empty(seq_len.shape, dtype=torch.int32).pin_memory()
     # rewind the state positions: re-run decode positions L+warmup+steps .. (new tokens, same shapes)
-    base = L + args.warmup + args.steps
+    base = L + args.warmup + args.steps + 5
     times = []
     st = torch.cuda.current_stream()
     for s in range(n):
@@ -431,6 +440,7 @@ def main():
                 "scaling": "weak", "vs_baseline": None, "dtype": "fp8/fp4 storage, bf16/f16 MMA, fp32 accumulate",
                 "data": "synthetic",
                 "config": workload_config({"parallelism": f"replicas x{world} (independent sequences per GPU)",
+                                           "stage_ms_source": "separate replays of the step graph with event nodes between calls",
                                            "stage_ms": {k: round(v, 5) for k, v in zip(
                                                ["compress", "index_topk", "attend", "window_commit"],
                                                res["stages"])}}),

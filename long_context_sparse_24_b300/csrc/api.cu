@@ -257,7 +257,7 @@ lcs_status lcs_window_commit(const lcs_batch* batch, const lcs_state* state, int
 size_t lcs_index_topk_workspace(const lcs_batch* batch, int32_t m, int32_t k) {
   (void)k;
   if (batch == nullptr || m <= 0) return 0;
-  return (size_t)batch->total_new * (size_t)index_ld(batch, m) * 4 + 256;
+  return (size_t)batch->total_new * (size_t)index_ld(batch, m) * 4 + (size_t)batch->total_new * kTopkHistBins * 4 + 256;
 }
 
 lcs_status csa_index_topk(const lcs_batch* batch, const uint8_t* q_fp4, const uint8_t* q_scale, const float* head_w,
@@ -277,13 +277,17 @@ lcs_status csa_index_topk(const lcs_batch* batch, const uint8_t* q_fp4, const ui
   p.relu = (flags & LCS_INDEX_RELU) ? 1 : 0;
   p.ld = index_ld(batch, m);
   p.keys_out = static_cast<uint32_t*>(workspace);
+  p.hist = p.keys_out + (size_t)batch->total_new * p.ld;
   p.status = dev_status;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int max_entries = batch->max_seq_len / m;
-  cudaError_t e = launch_index_scores(p, keys->rank, batch->max_new, max_entries, st);
+  // the per-query histograms accumulate with atomics: clear them first
+  cudaError_t e = cudaMemsetAsync(p.hist, 0, (size_t)batch->total_new * kTopkHistBins * 4, st);
   if (e != cudaSuccess) return LCS_ERR_CUDA;
-  e = launch_topk_select(p.keys_out, p.ld, batch->cu_new, batch->seq_len, batch->num_seqs, batch->max_new, m, k,
-                         max_entries, out_idx, out_cnt, st);
+  e = launch_index_scores(p, keys->rank, batch->max_new, max_entries, st);
+  if (e != cudaSuccess) return LCS_ERR_CUDA;
+  e = launch_topk_select(p.keys_out, p.hist, p.ld, batch->cu_new, batch->seq_len, batch->num_seqs, batch->max_new,
+                         m, k, out_idx, out_cnt, st);
   return from_cuda(e);
 }
 

@@ -23,6 +23,8 @@
 namespace lcsa {
 
 constexpr int kRT = 32;           // rows per tile
+constexpr int kStages = 3;        // cp.async gather stages in flight
+constexpr int kDescRows = 256;    // row descriptors resolved per refill (8 tiles)
 constexpr float kP2Scale = 256.f; // power-of-two pre-scale of P*scale_row for the f16 operand
 
 
@@ -62,7 +64,7 @@ struct AttendSmem {
   static constexpr int kQ = 0;
   static constexpr int kR = kQ + HG * D * 2;
   static constexpr int kStage = kR + kRT * D * 2;
-  static constexpr int kS = kStage + 2 * StageLayout<D, FMT>::kBytes;
+  static constexpr int kS = kStage + kStages * StageLayout<D, FMT>::kBytes;
   static constexpr int kSStride = kRT + 1;
   static constexpr int kP = kS + HG * kSStride * 4;
   static constexpr int kP2 = kP + HG * kRT * 2;
@@ -70,7 +72,8 @@ struct AttendSmem {
   static constexpr int kM = kRowScale + kRT * 4;
   static constexpr int kL = kM + HG * 4;
   static constexpr int kAlpha = kL + HG * 4;
-  static constexpr int kBytes = kAlpha + HG * 4;
+  static constexpr int kDesc = kAlpha + HG * 4;              // long long [kDescRows]
+  static constexpr int kBytes = kDesc + kDescRows * 8;
 };
 
 // Locate sequence of global query q (cu_new non-decreasing).
@@ -136,46 +139,50 @@ __global__ void __launch_bounds__(256, 1) attend_kernel(AttendParams p) {
     return;
   }
 
+  // ---- row descriptors: source set (bits 60..61: 0 entries, 1 new rows, 2 window ring; -1 =
+  //      invalid) and physical row, resolved for kDescRows rows at a time so that the gather of a
+  //      tile issues its copies without waiting on index loads
+  long long* desc = reinterpret_cast<long long*>(smem + L::kDesc);
+  auto fill_descs = [&](int seg_begin) {
+    const int r = seg_begin + tid;
+    long long d = -1;
+    if (r < r_end) {
+      if (r < cnt) {
+        const int j = sel ? sel[r] : r;
+        long long row = -1;
+        if (j >= 0 && j < nvis) row = entry_row(p.paging, b, j, p.entries.num_rows);
+        if (row < 0) report(p.status, LCS_ERR_DEVICE_GUARD);
+        d = row;
+      } else {
+        const int pos = t - W + 1 + (r - cnt);
+        long long row;
+        if (pos >= n0) {
+          row = (long long)sp.q0 + (pos - n0);
+          d = row < p.new_rows.num_rows ? (row | (1ll << 60)) : -1;
+        } else {
+          row = (long long)b * kWindow + (pos % kWindow);
+          d = row < p.window.num_rows ? (row | (2ll << 60)) : -1;
+        }
+        if (d < 0) report(p.status, LCS_ERR_DEVICE_GUARD);
+      }
+    }
+    if (tid < kDescRows) desc[tid] = d;
+  };
+
   // ---- gather issue: thread -> (row rr = tid/8, sub u = tid%8)
   auto issue_tile = [&](int tile_begin, int stage) {
     uint8_t* st = smem + L::kStage + stage * SL::kBytes;
     const int rr = tid >> 3, u = tid & 7;
     const int r = tile_begin + rr;
-    const uint8_t* src_nope = p.entries.nope;
-    const uint8_t* src_rope = reinterpret_cast<const uint8_t*>(p.entries.rope);
-    const float* src_scale = p.entries.scale;
-    long long row = -1;
-    if (r < r_end) {
-      if (r < cnt) {
-        const int j = sel ? sel[r] : r;
-        if (j >= 0 && j < nvis) row = entry_row(p.paging, b, j, p.entries.num_rows);
-        if (row < 0 && u == 0) report(p.status, LCS_ERR_DEVICE_GUARD);
-      } else {
-        const int pos = t - W + 1 + (r - cnt);
-        if (pos >= n0) {
-          row = (long long)sp.q0 + (pos - n0);
-          if (row >= p.new_rows.num_rows) row = -1;
-          src_nope = p.new_rows.nope;
-          src_rope = reinterpret_cast<const uint8_t*>(p.new_rows.rope);
-          src_scale = p.new_rows.scale;
-        } else {
-          row = (long long)b * kWindow + (pos % kWindow);
-          if (row >= p.window.num_rows) row = -1;
-          src_nope = p.window.nope;
-          src_rope = reinterpret_cast<const uint8_t*>(p.window.rope);
-          src_scale = p.window.scale;
-        }
-        if (row < 0 && u == 0) report(p.status, LCS_ERR_DEVICE_GUARD);
-      }
-    }
-    const bool ok = row >= 0;
-    if (!ok) {  // zero-fill from a base that always holds at least one row
-      src_nope = p.entries.nope;
-      src_rope = reinterpret_cast<const uint8_t*>(p.entries.rope);
-      src_scale = p.entries.scale;
-    }
-    const long long rw = ok ? row : 0;
-    const int nb = ok ? 16 : 0;
+    const long long d = r < r_end ? desc[(r - r_begin) % kDescRows] : -1;
+    const bool ok = d >= 0;
+    const int kind = ok ? (int)(d >> 60) : 0;
+    const long long rw = ok ? (d & ((1ll << 60) - 1)) : 0;
+    const uint8_t* src_nope = kind == 1 ? p.new_rows.nope : (kind == 2 ? p.window.nope : p.entries.nope);
+    const uint8_t* src_rope = reinterpret_cast<const uint8_t*>(kind == 1 ? p.new_rows.rope
+                                                               : (kind == 2 ? p.window.rope : p.entries.rope));
+    const float* src_scale = kind == 1 ? p.new_rows.scale : (kind == 2 ? p.window.scale : p.entries.scale);
+    const int nb = ok ? 16 : 0;   // invalid rows are zero-filled from row 0 of a set that has one
     for (int c = u; c < SL::kNopeBytes / 16; c += 8)
       cp_async16_zfill(st + rr * SL::kNopeBytes + c * 16, src_nope + rw * SL::kNopeBytes + c * 16, nb);
     if (kSplitFmt) {
@@ -186,33 +193,30 @@ __global__ void __launch_bounds__(256, 1) attend_kernel(AttendParams p) {
   };
 
   const int ntiles = (r_end - r_begin + kRT - 1) / kRT;
-  issue_tile(r_begin, 0);
-  cp_async_commit();
+  constexpr int kTilesPerSeg = kDescRows / kRT;
+  fill_descs(r_begin);
+  __syncthreads();
 
-  // ---- Q tile -> shared (RoPE dims bf16; FP8-split rows: other dims converted to f16)
+  // ---- Q tile -> shared with cp.async (one batch of 16-byte copies); FP8-split rows: the
+  //      non-RoPE dims are converted to f16 in place once the copies have landed (tile 0)
   {
     uint8_t* Qs = smem + L::kQ;
     for (int idx = tid; idx < HG * kChunks; idx += 256) {
       const int h = idx / kChunks, c = idx % kChunks;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (h0 + h < H) {
-        v = *reinterpret_cast<const uint4*>(p.q + ((long long)q * H + h0 + h) * D + c * 8);
-        if (kSplitFmt && c >= kRope / 8) {
-          uint32_t* w = reinterpret_cast<uint32_t*>(&v);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            float2 f = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w[k]));
-            __half2 hh = __float22half2_rn(f);
-            w[k] = *reinterpret_cast<uint32_t*>(&hh);
-          }
-        }
-      }
-      *reinterpret_cast<uint4*>(Qs + tile_off<D>(h, c)) = v;
+      uint8_t* dst = Qs + tile_off<D>(h, c);
+      if (h0 + h < H) cp_async16(dst, p.q + ((long long)q * H + h0 + h) * D + c * 8);
+      else *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
     }
+    cp_async_commit();
     for (int h = tid; h < HG; h += 256) {
       mrow[h] = -INFINITY;
       lrow[h] = 0.0f;
     }
+  }
+
+  for (int pre = 0; pre < kStages - 1; ++pre) {
+    if (pre < ntiles) issue_tile(r_begin + pre * kRT, pre);
+    cp_async_commit();
   }
 
   // ---- output accumulators: warp owns columns [warp*D/8, (warp+1)*D/8)
@@ -236,13 +240,38 @@ __global__ void __launch_bounds__(256, 1) attend_kernel(AttendParams p) {
 
   for (int ti = 0; ti < ntiles; ++ti) {
     const int tile_begin = r_begin + ti * kRT;
-    if (ti + 1 < ntiles) issue_tile(tile_begin + kRT, (ti + 1) & 1);
-    cp_async_commit();
-    cp_async_wait<1>();
+    {
+      const int nx = ti + kStages - 1;            // tile to issue now
+      if (nx < ntiles && nx % kTilesPerSeg == 0) {  // its rows start a new descriptor segment
+        __syncthreads();                          // every earlier issue has read the old ones
+        fill_descs(r_begin + nx * kRT);
+        __syncthreads();
+      }
+      if (nx < ntiles) issue_tile(r_begin + nx * kRT, nx % kStages);
+      cp_async_commit();
+    }
+    cp_async_wait<kStages - 1>();
     __syncthreads();
 
+    if (kSplitFmt && ti == 0) {
+      uint8_t* Qs = smem + L::kQ;
+      constexpr int kNopeChunks = kChunks - kRope / 8;
+      for (int idx = tid; idx < HG * kNopeChunks; idx += 256) {
+        const int h = idx / kNopeChunks, c = kRope / 8 + idx % kNopeChunks;
+        uint32_t* w = reinterpret_cast<uint32_t*>(Qs + tile_off<D>(h, c));
+        uint4 v = *reinterpret_cast<uint4*>(w);
+        uint32_t* x = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          float2 f = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&x[k]));
+          __half2 hh = __float22half2_rn(f);
+          x[k] = *reinterpret_cast<uint32_t*>(&hh);
+        }
+        *reinterpret_cast<uint4*>(w) = v;
+      }
+    }
     // ---- widen the staged rows into the [RT][D] tile
-    const uint8_t* st = smem + L::kStage + (ti & 1) * SL::kBytes;
+    const uint8_t* st = smem + L::kStage + (ti % kStages) * SL::kBytes;
     for (int idx = tid; idx < kRT * kChunks; idx += 256) {
       const int r = idx / kChunks, c = idx % kChunks;
       uint4 v;

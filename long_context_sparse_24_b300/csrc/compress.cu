@@ -47,6 +47,31 @@ __device__ __forceinline__ void load_row(const __nv_bfloat16* row, int lane, flo
   }
 }
 
+// Lane-owned 16-byte chunks of a bf16 row, raw (issue all loads first, convert later).
+template <int D>
+__device__ __forceinline__ void load_row_raw(const __nv_bfloat16* row, int lane, uint4 (&r)[RowChunks<D>::kPerLane]) {
+#pragma unroll
+  for (int i = 0; i < RowChunks<D>::kPerLane; ++i) {
+    const int c = lane + 32 * i;
+    r[i] = c < RowChunks<D>::kChunks ? *reinterpret_cast<const uint4*>(row + c * 8) : make_uint4(0, 0, 0, 0);
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void unpack_row(const uint4 (&r)[RowChunks<D>::kPerLane], int lane,
+                                           float (&v)[RowChunks<D>::kPerLane][8]) {
+#pragma unroll
+  for (int i = 0; i < RowChunks<D>::kPerLane; ++i) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&r[i]);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 f = __bfloat1622float2(h[k]);
+      v[i][2 * k] = f.x;
+      v[i][2 * k + 1] = f.y;
+    }
+  }
+}
+
 // Quantise one row held by a warp (lane-owned chunks) and store it as row `r` of `dst`.
 template <int D>
 __device__ __forceinline__ void store_row(const Rows& dst, long long r, int lane,
@@ -136,20 +161,31 @@ __global__ void __launch_bounds__(256) compress_entries_kernel(CompressParams p)
     for (int k = 0; k < 8; ++k) wv[i][k] = c < RowChunks<D>::kChunks ? p.w[c * 8 + k] : 0.0f;
   }
   if (active) {
-    for (int rr = wi; rr < R; rr += WPE) {
-      const int t = lo + rr;
-      float z = -INFINITY;
-      if (t >= 0) {
-        float v[PL][8];
-        load_row<D>(token_row(p, b, sp, t, D), lane, v);
-        float acc = 0.0f;
+    // rows in batches of 4 so that four row loads are in flight per warp
+    for (int rb = wi; rb < R; rb += 4 * WPE) {
+      uint4 raw[4][PL];
 #pragma unroll
-        for (int i = 0; i < PL; ++i)
-#pragma unroll
-          for (int k = 0; k < 8; ++k) acc = fmaf(wv[i][k], v[i][k], acc);
-        z = warp_sum(acc) + p.bias[rr];
+      for (int u = 0; u < 4; ++u) {
+        const int rr = rb + u * WPE, t = lo + rr;
+        if (rr < R && t >= 0) load_row_raw<D>(token_row(p, b, sp, t, D), lane, raw[u]);
       }
-      if (lane == 0) zbuf[e_local][rr] = z;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int rr = rb + u * WPE, t = lo + rr;
+        if (rr >= R) break;
+        float z = -INFINITY;
+        if (t >= 0) {
+          float v[PL][8];
+          unpack_row<D>(raw[u], lane, v);
+          float acc = 0.0f;
+#pragma unroll
+          for (int i = 0; i < PL; ++i)
+#pragma unroll
+            for (int k = 0; k < 8; ++k) acc = fmaf(wv[i][k], v[i][k], acc);
+          z = warp_sum(acc) + p.bias[rr];
+        }
+        if (lane == 0) zbuf[e_local][rr] = z;
+      }
     }
   }
   __syncthreads();
@@ -172,16 +208,26 @@ __global__ void __launch_bounds__(256) compress_entries_kernel(CompressParams p)
   for (int i = 0; i < PL; ++i)
 #pragma unroll
     for (int k = 0; k < 8; ++k) acc[i][k] = 0.0f;
-  for (int rr = wi; rr < R; rr += WPE) {
-    const int t = lo + rr;
-    if (t < 0) continue;
-    const float a = expf(zbuf[e_local][rr] - zmax) * inv;
-    float v[PL][8];
-    load_row<D>(token_row(p, b, sp, t, D), lane, v);
+  for (int rb = wi; rb < R; rb += 4 * WPE) {
+    uint4 raw[4][PL];
 #pragma unroll
-    for (int i = 0; i < PL; ++i)
+    for (int u = 0; u < 4; ++u) {
+      const int rr = rb + u * WPE, t = lo + rr;
+      if (rr < R && t >= 0) load_row_raw<D>(token_row(p, b, sp, t, D), lane, raw[u]);
+    }
 #pragma unroll
-      for (int k = 0; k < 8; ++k) acc[i][k] = fmaf(a, v[i][k], acc[i][k]);
+    for (int u = 0; u < 4; ++u) {
+      const int rr = rb + u * WPE, t = lo + rr;
+      if (rr >= R) break;
+      if (t < 0) continue;
+      const float a = expf(zbuf[e_local][rr] - zmax) * inv;
+      float v[PL][8];
+      unpack_row<D>(raw[u], lane, v);
+#pragma unroll
+      for (int i = 0; i < PL; ++i)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) acc[i][k] = fmaf(a, v[i][k], acc[i][k]);
+    }
   }
 
   if constexpr (WPE > 1) {

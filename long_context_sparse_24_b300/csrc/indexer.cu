@@ -57,6 +57,7 @@ template <int NT, int RB>
 __global__ void __launch_bounds__(256) index_score_kernel(IndexParams p) {
   constexpr int TPW = 8;                       // 16-entry tiles per warp
   constexpr int CHUNK = 8 * TPW * 16;          // entries per CTA
+  extern __shared__ uint32_t hist_s[];         // [QG][kTopkHistBins] when p.hist != null
   const int b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t4 = lane & 3;
@@ -72,6 +73,11 @@ __global__ void __launch_bounds__(256) index_score_kernel(IndexParams p) {
   const int chunk0 = blockIdx.x * CHUNK;
   if (chunk0 >= nmax) return;
   constexpr int rh = RB * 16;                  // bytes per FP4 row (r/2)
+  const bool with_hist = p.hist != nullptr;
+  if (with_hist) {
+    for (int i = threadIdx.x; i < QG * kTopkHistBins; i += blockDim.x) hist_s[i] = 0;
+    __syncthreads();
+  }
 
   // ---- query operands (B) and per-column scales / weights
   uint32_t bq[NT][RB][2];
@@ -161,8 +167,13 @@ __global__ void __launch_bounds__(256) index_score_kernel(IndexParams p) {
             const float s = c == 0 ? s0 : s1;
             if (qi >= 0 && j < (n0 + qbase + qi + 1) / p.m) {
               const long long o = (long long)(sp.q0 + qbase + qi) * p.ld + j;
-              if (p.scores_out) p.scores_out[o] = s;
-              else p.keys_out[o] = score_key(s);
+              if (p.scores_out) {
+                p.scores_out[o] = s;
+              } else {
+                const uint32_t key = score_key(s);
+                p.keys_out[o] = key;
+                if (with_hist) atomicAdd(&hist_s[qi * kTopkHistBins + (key >> 21)], 1u);
+              }
             }
           }
         } else {
@@ -173,11 +184,23 @@ __global__ void __launch_bounds__(256) index_score_kernel(IndexParams p) {
           const int qi = colq[nt][0];
           if ((t4 % lead) == 0 && qi >= 0 && j < (n0 + qbase + qi + 1) / p.m) {
             const long long o = (long long)(sp.q0 + qbase + qi) * p.ld + j;
-            if (p.scores_out) p.scores_out[o] = s;
-            else p.keys_out[o] = score_key(s);
+            if (p.scores_out) {
+              p.scores_out[o] = s;
+            } else {
+              const uint32_t key = score_key(s);
+              p.keys_out[o] = key;
+              if (with_hist) atomicAdd(&hist_s[qi * kTopkHistBins + (key >> 21)], 1u);
+            }
           }
         }
       }
+    }
+  }
+  if (with_hist) {
+    __syncthreads();
+    for (int i = threadIdx.x; i < qcount * kTopkHistBins; i += blockDim.x) {
+      const uint32_t c = hist_s[i];
+      if (c) atomicAdd(&p.hist[(long long)(sp.q0 + qbase + i / kTopkHistBins) * kTopkHistBins + i % kTopkHistBins], c);
     }
   }
 }
@@ -188,14 +211,18 @@ __global__ void __launch_bounds__(256) index_score_kernel(IndexParams p) {
 
 constexpr int kSelThreads = 512;
 constexpr int kSelWarps = kSelThreads / 32;
-constexpr int kHistBins = 2048;
-constexpr int kSelCacheKeys = 40960;   // keys kept in shared memory when N fits (160 KB)
+constexpr int kHistBins = kTopkHistBins;
+constexpr int kKPT = 16;                          // keys per thread per chunk
+constexpr int kChunkKeys = kSelThreads * kKPT;    // 8192
+constexpr int kCandCap = 8192;                    // (key, j) pairs kept in shared memory
 
 struct SelectShared {
   uint32_t hist[kHistBins];
   int warp_tot[2][kSelWarps];
   int found_bin;
   int found_above;
+  uint32_t cand_key[kCandCap];
+  int32_t cand_j[kCandCap];
 };
 
 // Block-wide exclusive scan of one int per thread; returns the exclusive prefix, total in *tot.
@@ -221,14 +248,85 @@ __device__ __forceinline__ int block_excl_scan(int v, int* warp_tot, int* tot) {
   return before + x - v;
 }
 
-// grid: (max_new, num_seqs); block kSelThreads; dynamic smem: SelectShared + cache.
-__global__ void __launch_bounds__(kSelThreads) topk_select_kernel(const uint32_t* keys, long long ld,
-                                                                 const int32_t* cu_new, const int32_t* seq_len,
-                                                                 int m, int k, int32_t* out_idx, int32_t* out_cnt,
-                                                                 int use_cache) {
+// Highest bin d with (count of bins above d) < remaining <= (count of bins >= d).  Thread tid
+// owns bins 2047-4*tid .. 2044-4*tid.  Result in sh.found_bin / sh.found_above.
+__device__ __forceinline__ void find_bin(SelectShared& sh, int remaining) {
+  const int tid = threadIdx.x;
+  int cnt[4];
+  int local = 0;
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    cnt[r] = (int)sh.hist[kHistBins - 1 - 4 * tid - r];
+    local += cnt[r];
+  }
+  int tot;
+  int running = block_excl_scan(local, sh.warp_tot[0], &tot);
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    if (running < remaining && running + cnt[r] >= remaining) {
+      sh.found_bin = kHistBins - 1 - 4 * tid - r;
+      sh.found_above = running;
+    }
+    running += cnt[r];
+  }
+  __syncthreads();
+}
+
+// Exact radix select over `n` keys read through `key_at`; bits above `start_shift + width` of
+// every counted key must equal `prefix`.  Returns the k-th key; *need_eq = ties to take.
+template <typename KeyAt>
+__device__ uint32_t radix_select(SelectShared& sh, int n, KeyAt key_at, uint32_t prefix, int remaining, int npass,
+                                 const int* shifts, const int* widths, int* need_eq) {
+  for (int pass = 0; pass < npass; ++pass) {
+    const int sh_ = shifts[pass];
+    const uint32_t dmask = (1u << widths[pass]) - 1u;
+    const int hi_shift = sh_ + widths[pass];
+    for (int d = threadIdx.x; d < kHistBins; d += kSelThreads) sh.hist[d] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += kSelThreads) {
+      const uint32_t u = key_at(i);
+      const bool match = hi_shift >= 32 ? true : ((u >> hi_shift) == (prefix >> hi_shift));
+      if (match) atomicAdd(&sh.hist[(u >> sh_) & dmask], 1u);
+    }
+    __syncthreads();
+    find_bin(sh, remaining);
+    prefix |= (uint32_t)sh.found_bin << sh_;
+    remaining -= sh.found_above;
+    __syncthreads();
+  }
+  *need_eq = remaining;
+  return prefix;
+}
+
+// Ordered emission: out[pos] = j for every selected key, j ascending.
+template <typename KeyAt, typename IdxAt>
+__device__ void emit_selected(SelectShared& sh, int n, KeyAt key_at, IdxAt idx_at, uint32_t T, int need_eq,
+                              int32_t* out, int k) {
+  int base = 0, eq_seen = 0;
+  for (int i0 = 0; i0 < n; i0 += kSelThreads) {
+    const int i = i0 + threadIdx.x;
+    const uint32_t u = i < n ? key_at(i) : 0u;
+    const bool gt = i < n && u > T;
+    const bool eq = i < n && u == T;
+    int eq_tot;
+    const int eq_rank = eq_seen + block_excl_scan(eq ? 1 : 0, sh.warp_tot[0], &eq_tot);
+    const bool sel = gt || (eq && eq_rank < need_eq);
+    int sel_tot;
+    const int pos = base + block_excl_scan(sel ? 1 : 0, sh.warp_tot[1], &sel_tot);
+    if (sel && pos < k) out[pos] = idx_at(i);
+    base += sel_tot;
+    eq_seen += eq_tot;
+  }
+}
+
+// grid: (max_new, num_seqs); block kSelThreads; dynamic smem sizeof(SelectShared).
+// hist: the per-query histogram of key >> 21 built by the score kernel.
+__global__ void __launch_bounds__(kSelThreads) topk_select_kernel(const uint32_t* keys, const uint32_t* hist,
+                                                                 long long ld, const int32_t* cu_new,
+                                                                 const int32_t* seq_len, int m, int k,
+                                                                 int32_t* out_idx, int32_t* out_cnt) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   SelectShared& sh = *reinterpret_cast<SelectShared*>(smem_raw);
-  uint32_t* cache = reinterpret_cast<uint32_t*>(smem_raw + sizeof(SelectShared));
   const int b = blockIdx.y, i = blockIdx.x, tid = threadIdx.x;
   const SeqSpan sp = seq_span(cu_new, seq_len, b);
   if (i >= sp.qn) return;
@@ -242,71 +340,69 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(const uint32_t
     return;
   }
   const uint32_t* src = keys + q * ld;
-  if (use_cache && N <= kSelCacheKeys) {
-    for (int j = tid; j < N; j += kSelThreads) cache[j] = src[j];
-    src = cache;
+
+  // 1. bin of the k-th largest key from the score kernel's histogram
+  for (int d = tid; d < kHistBins; d += kSelThreads) sh.hist[d] = hist[q * kHistBins + d];
+  __syncthreads();
+  find_bin(sh, k);
+  const uint32_t b1 = (uint32_t)sh.found_bin;
+  const int above1 = sh.found_above;
+  __syncthreads();
+
+  // 2. one ordered pass: keep (key, j) of every key in bin b1 or above, j ascending
+  int ncand = 0;
+  bool overflow = false;
+  for (int c0 = 0; c0 < N; c0 += kChunkKeys) {
+    const int j0 = c0 + tid * kKPT;
+    uint32_t u[kKPT];
+    if (j0 + kKPT <= N) {
+      const uint4* v = reinterpret_cast<const uint4*>(src + j0);
+#pragma unroll
+      for (int w = 0; w < kKPT / 4; ++w) {
+        const uint4 x = v[w];
+        u[4 * w] = x.x; u[4 * w + 1] = x.y; u[4 * w + 2] = x.z; u[4 * w + 3] = x.w;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < kKPT; ++e) u[e] = (j0 + e < N) ? src[j0 + e] : 0u;
+    }
+    int cnt = 0;
+#pragma unroll
+    for (int e = 0; e < kKPT; ++e) cnt += (j0 + e < N && (u[e] >> 21) >= b1) ? 1 : 0;
+    int tot;
+    int pos = ncand + block_excl_scan(cnt, sh.warp_tot[0], &tot);
+    if (ncand + tot > kCandCap) {   // uniform: tot is the block total
+      overflow = true;
+      break;
+    }
+#pragma unroll
+    for (int e = 0; e < kKPT; ++e) {
+      if (j0 + e < N && (u[e] >> 21) >= b1) {
+        sh.cand_key[pos] = u[e];
+        sh.cand_j[pos] = j0 + e;
+        ++pos;
+      }
+    }
+    ncand += tot;
   }
   __syncthreads();
 
-  uint32_t prefix = 0;
-  int remaining = k;
-  const int shifts[3] = {21, 10, 0};
-  const int widths[3] = {11, 11, 10};
-#pragma unroll 1
-  for (int pass = 0; pass < 3; ++pass) {
-    const int sh_ = shifts[pass];
-    const uint32_t dmask = (1u << widths[pass]) - 1u;
-    const int hi_shift = sh_ + widths[pass];   // bits at and above this must match the prefix
-    for (int d = tid; d < kHistBins; d += kSelThreads) sh.hist[d] = 0;
-    __syncthreads();
-    for (int j = tid; j < N; j += kSelThreads) {
-      const uint32_t u = src[j];
-      const bool match = hi_shift >= 32 ? true : ((u >> hi_shift) == (prefix >> hi_shift));
-      if (match) atomicAdd(&sh.hist[(u >> sh_) & dmask], 1u);
-    }
-    __syncthreads();
-    // thread `tid` owns bins top-down: d = 2047 - 4*tid - r
-    int cnt[4];
-    int local = 0;
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      cnt[r] = (int)sh.hist[kHistBins - 1 - 4 * tid - r];
-      local += cnt[r];
-    }
-    int tot;
-    int running = block_excl_scan(local, sh.warp_tot[0], &tot);
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      if (running < remaining && running + cnt[r] >= remaining) {
-        sh.found_bin = kHistBins - 1 - 4 * tid - r;
-        sh.found_above = running;
-      }
-      running += cnt[r];
-    }
-    __syncthreads();
-    prefix |= (uint32_t)sh.found_bin << sh_;
-    remaining -= sh.found_above;
-    __syncthreads();
-  }
-  const uint32_t T = prefix;
-  const int need_eq = remaining;   // keys equal to T to take, lowest j first
-
-  int base = 0, eq_seen = 0;
-  const unsigned lt_mask = (1u << (tid & 31)) - 1u;
-  for (int j0 = 0; j0 < N; j0 += kSelThreads) {
-    const int j = j0 + tid;
-    const uint32_t u = j < N ? src[j] : 0u;
-    const bool gt = j < N && u > T;
-    const bool eq = j < N && u == T;
-    int eq_tot;
-    const int eq_rank = eq_seen + block_excl_scan(eq ? 1 : 0, sh.warp_tot[0], &eq_tot);
-    const bool sel = gt || (eq && eq_rank < need_eq);
-    int sel_tot;
-    const int pos = base + block_excl_scan(sel ? 1 : 0, sh.warp_tot[1], &sel_tot);
-    if (sel && pos < k) out[pos] = j;
-    base += sel_tot;
-    eq_seen += eq_tot;
-    (void)lt_mask;
+  int need_eq;
+  if (!overflow) {
+    // 3. resolve the k-th key inside bin b1 (low 21 bits) among the kept keys
+    const int shifts[2] = {10, 0};
+    const int widths[2] = {11, 10};
+    const uint32_t T = radix_select(sh, ncand, [&](int x) { return sh.cand_key[x]; }, b1 << 21, k - above1, 2,
+                                    shifts, widths, &need_eq);
+    // 4. ordered emission from the kept keys
+    emit_selected(sh, ncand, [&](int x) { return sh.cand_key[x]; }, [&](int x) { return sh.cand_j[x]; }, T,
+                  need_eq, out, k);
+  } else {
+    // degenerate distributions (very many keys near the k-th): full radix select over all keys
+    const int shifts[3] = {21, 10, 0};
+    const int widths[3] = {11, 11, 10};
+    const uint32_t T = radix_select(sh, N, [&](int x) { return src[x]; }, 0u, k, 3, shifts, widths, &need_eq);
+    emit_selected(sh, N, [&](int x) { return src[x]; }, [&](int x) { return x; }, T, need_eq, out, k);
   }
   if (tid == 0) out_cnt[q] = k;
 }
@@ -316,42 +412,51 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(const uint32_t
 // ----------------------------------------------------------------------------------------------
 
 cudaError_t launch_index_scores(const IndexParams& p, int rank, int max_new, int max_entries, cudaStream_t st) {
+  // queries per CTA = (8 / heads) * NT, kept at 8 or fewer so the CTA's histogram fits in 64 KB
   const bool prefill = max_new > 2;
-  const int NT = prefill ? 4 : 1;
+  const int NT = prefill ? (p.heads >= 4 ? 4 : p.heads) : 1;
   const int QG = (8 / p.heads) * NT;
   constexpr int CHUNK = 8 * 8 * 16;
   dim3 grid((max_entries + CHUNK - 1) / CHUNK, (max_new + QG - 1) / QG, p.num_seqs);
   if (grid.x == 0 || grid.y == 0) return cudaSuccess;
+  const size_t smem = p.hist ? (size_t)QG * kTopkHistBins * 4 : 0;
+  static bool attr = false;
+  if (!attr) {
+    const int mx = 8 * kTopkHistBins * 4;
+    cudaFuncSetAttribute(index_score_kernel<4, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+    cudaFuncSetAttribute(index_score_kernel<2, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+    cudaFuncSetAttribute(index_score_kernel<1, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+    cudaFuncSetAttribute(index_score_kernel<4, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+    cudaFuncSetAttribute(index_score_kernel<2, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+    cudaError_t e = cudaFuncSetAttribute(index_score_kernel<1, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
   if (rank == 128) {
-    if (prefill) index_score_kernel<4, 4><<<grid, 256, 0, st>>>(p);
-    else index_score_kernel<1, 4><<<grid, 256, 0, st>>>(p);
+    if (NT == 4) index_score_kernel<4, 4><<<grid, 256, smem, st>>>(p);
+    else if (NT == 2) index_score_kernel<2, 4><<<grid, 256, smem, st>>>(p);
+    else index_score_kernel<1, 4><<<grid, 256, smem, st>>>(p);
   } else {
-    if (prefill) index_score_kernel<4, 2><<<grid, 256, 0, st>>>(p);
-    else index_score_kernel<1, 2><<<grid, 256, 0, st>>>(p);
+    if (NT == 4) index_score_kernel<4, 2><<<grid, 256, smem, st>>>(p);
+    else if (NT == 2) index_score_kernel<2, 2><<<grid, 256, smem, st>>>(p);
+    else index_score_kernel<1, 2><<<grid, 256, smem, st>>>(p);
   }
   return cudaGetLastError();
 }
 
-size_t select_smem_bytes(bool cache) {
-  return sizeof(SelectShared) + (cache ? (size_t)kSelCacheKeys * 4 : 0);
-}
-
-cudaError_t launch_topk_select(const uint32_t* keys, long long ld, const int32_t* cu_new, const int32_t* seq_len,
-                               int num_seqs, int max_new, int m, int k, int max_entries, int32_t* out_idx,
+cudaError_t launch_topk_select(const uint32_t* keys, const uint32_t* hist, long long ld, const int32_t* cu_new,
+                               const int32_t* seq_len, int num_seqs, int max_new, int m, int k, int32_t* out_idx,
                                int32_t* out_cnt, cudaStream_t st) {
-  const bool cache = max_entries <= kSelCacheKeys;
-  const size_t smem = select_smem_bytes(cache);
+  const size_t smem = sizeof(SelectShared);
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)select_smem_bytes(true));
+    cudaError_t e = cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   dim3 grid(max_new, num_seqs);
   if (grid.x == 0) return cudaSuccess;
-  topk_select_kernel<<<grid, kSelThreads, smem, st>>>(keys, ld, cu_new, seq_len, m, k, out_idx, out_cnt,
-                                                       cache ? 1 : 0);
+  topk_select_kernel<<<grid, kSelThreads, smem, st>>>(keys, hist, ld, cu_new, seq_len, m, k, out_idx, out_cnt);
   return cudaGetLastError();
 }
 

@@ -1,0 +1,131 @@
+"""End-to-end parity on the five synthetic workloads, through the layer driver (compress ->
+indexer top-k -> attention -> window commit) against the fp64 oracle.
+
+Small workload: every query is checked.  Large workloads run at their full sizes on the GPU
+and are checked on sampled sequences / queries that the oracle computes one by one (the
+entries they need are compressed by the oracle from the raw rows of their own spans).
+Top-k index sets and counts: bit-exact.  Outputs: max-abs 3e-2 / rel-L2 1e-2.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import synth.gpu as sg
+from harness import DEV, OUT_MAX_ABS, OUT_REL_L2, bits_to_f64, check_outputs, to_dev_bf16_bits
+
+lcsa = pytest.importorskip("long_context_sparse_24_b300")
+from long_context_sparse_24_b300.layer import Layer  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+def _comp_params(seed, layer, dim, m, overlap):
+    wscale = np.float32(1 / 16 if dim >= 512 else 1 / 8)
+    w = synth.bf16_bits_to_f32(synth.normal_bf16(seed, synth.tensor_id(synth.COMP_W, layer), 0, dim)) * wscale
+    nb = 2 * m if overlap else m
+    b = synth.bf16_bits_to_f32(synth.normal_bf16(seed, synth.tensor_id(synth.COMP_B, layer), 0, nb)) * np.float32(0.5)
+    return w.astype(np.float32), b.astype(np.float32)
+
+
+def _raw_f64(seed, layer, seq, t0, n, dim):
+    return bits_to_f64(synth.normal_bf16(seed, synth.tensor_id(synth.RAW, layer, seq), t0 * dim, n * dim)).reshape(n, dim)
+
+
+def _fill_keys(layer_obj, seed, lay, seq, n_ent, rank, scaled=True):
+    """Indexer keys of entries 0..n_ent-1 of one sequence (identity paging) on the device."""
+    if n_ent <= 0:
+        return
+    bps = layer_obj.cache.paging.max_blocks_per_seq
+    epb = layer_obj.cache.paging.entries_per_block
+    table = layer_obj.cache.paging.block_table[seq].cpu().numpy()
+    assert np.array_equal(table, np.arange(seq * bps, (seq + 1) * bps))
+    r0 = seq * bps * epb
+    sg.e2m1_packed(layer_obj.cache.keys.fp4[r0:r0 + n_ent], seed, synth.tensor_id(synth.IDX_K, lay, seq), 0)
+    if scaled:
+        sg.ue8m0(layer_obj.cache.keys.scale[r0:r0 + n_ent], seed, synth.tensor_id(synth.IDX_KS, lay, seq), 0)
+
+
+def _keys_np(seed, lay, seq, n_ent, rank, scaled=True):
+    kc = synth.e2m1_codes(seed, synth.tensor_id(synth.IDX_K, lay, seq), 0, n_ent * rank).reshape(n_ent, rank)
+    if scaled:
+        ks = synth.ue8m0_scales(seed, synth.tensor_id(synth.IDX_KS, lay, seq), 0, n_ent * rank // 32)
+        ks = ks.reshape(n_ent, rank // 32)
+    else:
+        ks = np.full((n_ent, rank // 32), 127, np.uint8)
+    return kc, ks
+
+
+def _query_inputs(seed, lay, seq, t0, n, heads, dim, hi, rank, scaled=True, q_scale_bits=None):
+    q = synth.normal_bf16(seed, synth.tensor_id(synth.QUERY, lay, seq), t0 * heads * dim, n * heads * dim, q_scale_bits)
+    q = q.reshape(n, heads, dim)
+    qc = synth.e2m1_codes(seed, synth.tensor_id(synth.IDX_Q, lay, seq), t0 * hi * rank, n * hi * rank)
+    qc = qc.reshape(n, hi, rank)
+    if scaled:
+        qs = synth.ue8m0_scales(seed, synth.tensor_id(synth.IDX_QS, lay, seq), t0 * hi * rank // 32,
+                                n * hi * rank // 32).reshape(n, hi, rank // 32)
+        hw = synth.head_weights(seed, synth.tensor_id(synth.HEAD_W, lay, seq), t0 * hi, n * hi).reshape(n, hi)
+    else:
+        qs = np.full((n, hi, rank // 32), 127, np.uint8)
+        hw = np.ones((n, hi), np.float32)
+    return q, qc, qs, hw
+
+
+def _dev_u8(x):
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.uint8)).to(DEV)
+
+
+# ------------------------------------------------------------------------------------------ small
+
+@pytest.mark.parametrize("fmt", ["bf16", "fp8_split"])
+def test_csa_tiny_prefill_then_decode(fmt):
+    """4096-token sequence, 8 heads, D=128, indexer rank 64 (1 head, unscaled), k=64: prefill of
+    all 4096 tokens (every query checked), then 64 decode steps (every step checked)."""
+    wl = synth.CONFIGS["csa_tiny"]
+    seed, D, H, m, k, r, hi = wl.seed, wl.dim, wl.heads, wl.m, wl.top_k, wl.index_rank, wl.index_heads
+    n, steps = wl.new_tokens, 64
+    fmtc = lcsa.LCS_ROW_BF16 if fmt == "bf16" else lcsa.LCS_ROW_FP8_SPLIT
+    lay = Layer("csa", 1, n + steps + 128, H, D, fmtc, m, top_k=k, index_heads=hi, index_rank=r, max_new=n,
+                softmax_scale=1.0, device=DEV)
+    w, b = _comp_params(seed, 0, D, m, True)
+    lay.set_compressor(torch.from_numpy(w).to(DEV), torch.from_numpy(b).to(DEV))
+    total = n + steps
+    raw = _raw_f64(seed, 0, 0, 0, total, D)
+    raw_dev = to_dev_bf16_bits(synth.normal_bf16(seed, synth.tensor_id(synth.RAW, 0, 0), 0, total * D).reshape(total, D))
+    _fill_keys(lay, seed, 0, 0, total // m, r, scaled=False)
+    kc, ks = _keys_np(seed, 0, 0, total // m, r, scaled=False)
+    q, qc, qs, hw = _query_inputs(seed, 0, 0, 0, total, H, D, hi, r, scaled=False,
+                                  q_scale_bits=synth.INV_SQRT128_BITS)
+    ref = oracle.csa_layer(raw, w.astype(np.float64), b.astype(np.float64), m, True, fmt,
+                           bits_to_f64(q), np.arange(total), qc, qs, hw, kc, ks, k, 1.0)
+    # prefill: all n tokens in one call
+    out = torch.empty((n, H, D), dtype=torch.bfloat16, device=DEV)
+    batch = lay.batch([n], [n])
+    lay.step(batch, raw_dev[:n], to_dev_bf16_bits(q[:n]), out, idx_q_fp4=_dev_u8(synth.pack_e2m1(qc[:n])),
+             idx_q_scale=_dev_u8(qs[:n]), head_w=torch.from_numpy(hw[:n]).to(DEV))
+    torch.cuda.synchronize()
+    assert int(lay.status.item()) == 0
+    got_idx = lay.topk_idx[:n].cpu().numpy()
+    got_cnt = lay.topk_cnt[:n].cpu().numpy()
+    o = out.float().cpu().numpy().astype(np.float64)
+    for t in range(n):
+        sel = ref["topk"][t]
+        assert got_cnt[t] == len(sel), t
+        assert np.array_equal(got_idx[t, :len(sel)], sel), t
+    check_outputs(o, ref["o"][:n], "prefill")
+    # decode: one token per call
+    out1 = torch.empty((1, H, D), dtype=torch.bfloat16, device=DEV)
+    for s in range(steps):
+        t = n + s
+        batch = lay.batch([t + 1], [1])
+        lay.step(batch, raw_dev[t:t + 1], to_dev_bf16_bits(q[t:t + 1]), out1,
+                 idx_q_fp4=_dev_u8(synth.pack_e2m1(qc[t:t + 1])), idx_q_scale=_dev_u8(qs[t:t + 1]),
+                 head_w=torch.from_numpy(hw[t:t + 1]).to(DEV))
+        torch.cuda.synchronize()
+        sel = ref["topk"][t]
+        assert np.array_equal(lay.topk_idx[0, :len(sel)].cpu().numpy(), sel), t
+        check_outputs(out1.float().cpu().numpy()[0].astype(np.float64), ref["o"][t], f"decode step {s}")
+    assert int(lay.status.item()) == 0
