@@ -34,7 +34,7 @@ class LcsError(RuntimeError):
 
 
 if not os.path.exists(LIB_PATH):
-    raise ImportError(f"{LIB_PATH} is missing: build it with `python -m long_context_sparse_24_b300.build` "
+    raise ImportError(f"{LIB_PATH} is missing: build it with `python long_context_sparse_24_b300/build.py` "
                       "(nvcc, sm_103a); there is no fallback implementation")
 _lib = ctypes.CDLL(LIB_PATH)
 
