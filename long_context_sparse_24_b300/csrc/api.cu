@@ -284,7 +284,8 @@ lcs_status csa_index_topk(const lcs_batch* batch, const uint8_t* q_fp4, const ui
   // the per-query histograms accumulate with atomics: clear them first
   cudaError_t e = cudaMemsetAsync(p.hist, 0, (size_t)batch->total_new * kTopkHistBins * 4, st);
   if (e != cudaSuccess) return LCS_ERR_CUDA;
-  e = launch_index_scores(p, keys->rank, batch->max_new, max_entries, st);
+  e = index_tc_qh(p, keys->rank, batch->max_new) > 0 ? launch_index_tc(p, keys->rank, batch->max_new, max_entries, num_sms(), st)
+                                                     : launch_index_scores(p, keys->rank, batch->max_new, max_entries, st);
   if (e != cudaSuccess) return LCS_ERR_CUDA;
   e = launch_topk_select(p.keys_out, p.hist, p.ld, batch->cu_new, batch->seq_len, batch->num_seqs, batch->max_new,
                          m, k, out_idx, out_cnt, st);
@@ -304,8 +305,11 @@ lcs_status csa_index_scores(const lcs_batch* batch, const uint8_t* q_fp4, const 
   p.ld = ld;
   p.scores_out = out_scores;
   p.status = dev_status;
-  return from_cuda(launch_index_scores(p, keys->rank, batch->max_new, batch->max_seq_len / m,
-                                       static_cast<cudaStream_t>(stream)));
+  const int max_entries = batch->max_seq_len / m;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return from_cuda(index_tc_qh(p, keys->rank, batch->max_new) > 0
+                       ? launch_index_tc(p, keys->rank, batch->max_new, max_entries, num_sms(), st)
+                       : launch_index_scores(p, keys->rank, batch->max_new, max_entries, st));
 }
 
 size_t lcs_attend_workspace(const lcs_batch* batch, int32_t heads, int32_t dim, int32_t max_rows) {

@@ -156,17 +156,24 @@ def _index_case(lengths, new, m, k, heads, rank, relu, scaled, seed=31, ties=Fal
     return cache, batch, kcs, kss, qcs, qss, hws, q_fp4, q_sc, hw_all
 
 
-@pytest.mark.parametrize("heads,rank,relu,scaled,new", [
-    (4, 128, False, True, [1, 1, 1]),
-    (4, 128, False, True, [1, 5, 40]),
-    (1, 64, False, False, [1, 7, 33]),
-    (2, 128, True, True, [2, 1, 9]),
-    (8, 64, False, True, [1, 3, 17]),
-    (4, 128, True, True, [1, 1, 1]),
+@pytest.mark.parametrize("heads,rank,relu,scaled,new,lengths", [
+    # up to 4 queries per sequence at rank 128: tensor-core (tcgen05) scorer
+    (4, 128, False, True, [1, 1, 1], [37, 600, 2100]),
+    (4, 128, True, True, [1, 1, 1], [37, 600, 2100]),
+    (4, 128, False, True, [1, 1, 1], [5, 9000, 4100]),
+    (4, 128, False, True, [2, 1, 4], [37, 600, 2100]),
+    (1, 128, False, True, [4, 1, 3], [37, 600, 2100]),
+    (2, 128, True, True, [3, 4, 1], [37, 600, 2100]),
+    (8, 128, False, True, [1, 1, 1], [37, 600, 2100]),
+    (8, 128, False, True, [2, 1, 2], [300, 4600, 2100]),
+    # longer runs of queries, or rank 64: warp-MMA scorer
+    (4, 128, False, True, [1, 5, 40], [37, 600, 2100]),
+    (1, 64, False, False, [1, 7, 33], [37, 600, 2100]),
+    (2, 128, True, True, [2, 1, 9], [37, 600, 2100]),
+    (8, 64, False, True, [1, 3, 17], [37, 600, 2100]),
 ])
-def test_index_scores_exact_and_topk_sets(heads, rank, relu, scaled, new):
+def test_index_scores_exact_and_topk_sets(heads, rank, relu, scaled, new, lengths):
     m, k = 4, 24
-    lengths = [37, 600, 2100]
     cache, batch, kcs, kss, qcs, qss, hws, q_fp4, q_sc, hw = _index_case(lengths, new, m, k, heads, rank, relu, scaled)
     flags = lcsa.LCS_INDEX_RELU if relu else 0
     T = batch.total_new
