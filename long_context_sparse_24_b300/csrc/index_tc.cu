@@ -1,4 +1,4 @@
-// Lightning-indexer scores on the tcgen05 tensor cores, fed by TMA, for batches with a few
+// Lightning-indexer scores on the tcgen05 tensor cores for batches with a few
 // queries per sequence (decode, short speculative runs).
 //
 // Defined by: m.x-techcon.com/article/133366, section 2, CSA step 2 (a low-rank indexer scores
@@ -9,16 +9,17 @@
 // Layout of the work.  A persistent, warp-specialised CTA scans a contiguous run of 128-entry
 // tiles of one sequence for all of that sequence's queries (QPS <= 4), through a ring of
 // shared-memory stages:
-//   warp 8 (producer)  looks the run's pages up in the block table once, then streams tiles:
-//                      the key codes of each page arrive by TMA in the tensor map's "16 x U4 in
-//                      16 bytes" form with the 128-byte swizzle -- each entry's 128 E2M1 codes
-//                      occupy one 128-byte shared-memory row, the K-major operand form of the
-//                      kind::f8f6f4 MMA with E2M1 inputs -- and its block scales by a bulk copy;
-//   warp 9 (MMA)       issues four K = 32 MMAs per tile into one of kAcc tensor-memory
+//   warps 8-9 (producers, alternating tiles) look the run's pages up in the block table once, then streams tiles:
+//                      one lane per page issues a TMA copy of the page's codes in the tensor
+//                      map's "16 x U4 in 16 bytes" form with the 128-byte swizzle -- each
+//                      entry's 128 E2M1 codes occupy one 128-byte shared-memory row, the K-major
+//                      operand form of the kind::f8f6f4 MMA with E2M1 inputs -- and every lane
+//                      copies 16 bytes of block scales with cp.async (tiny bulk copies issue too
+//                      slowly from one thread to keep a paged scan at memory speed);
+//   warp 10 (MMA)       issues four K = 32 MMAs per tile into one of kAcc tensor-memory
 //                      accumulators and commits them to that accumulator's barrier;
 //   warps 0-7          (one thread per entry = per TMEM lane, two warps per lane quadrant
-//                      taking alternate tiles) read the accumulator, release it
-//                      and the stage, form the scores, write the order-preserving keys and
+//                      taking alternate tiles) read the accumulator and release it, form the scores, write the order-preserving keys and
 //                      count them into the per-query key histogram used by the top-k selection.
 // The grid is one wave: about (SMs x resident CTAs) / sequences CTAs per sequence.
 //
@@ -36,23 +37,28 @@ namespace lcsa {
 namespace {
 
 constexpr int kTile = 128;          // entries per MMA tile (M)
-constexpr int kStages = 5;          // shared-memory ring depth (tiles in flight per CTA)
+#ifndef LCSA_INDEX_STAGES
+#define LCSA_INDEX_STAGES 5
+#endif
+constexpr int kStages = LCSA_INDEX_STAGES;  // shared-memory ring depth (tiles in flight per CTA)
 constexpr int kAcc = 4;             // tensor-memory accumulators
 constexpr int kMaxPages = 256;      // block-table entries a CTA's run may span
 constexpr int kRowBytes = 128;      // shared-memory bytes of one entry's 128 codes (16U4 in 16 B)
-constexpr int kPackedRowBytes = 64; // global bytes of the same codes; a 16U4 TMA copy counts these
+constexpr int kPackedRowBytes = 64; // global bytes of the same codes
 constexpr int kATileBytes = kTile * kRowBytes;
 constexpr int kEpiWarps = 8;        // two per TMEM lane quadrant, alternating tiles
 constexpr int kEpiThreads = kEpiWarps * 32;
-constexpr int kThreads = kEpiThreads + 64;
+constexpr int kProdWarps = 2;       // producer warps, alternating tiles
+constexpr int kScaleSlots = 2 * kStages;  // block-scale ring (read by the epilogue, outlives a stage)
+constexpr int kThreads = kEpiThreads + 32 * kProdWarps + 32;
 
 template <int QH, int QPS>
 struct TcSmem {
   static constexpr int N = 4 * QH;                            // MMA N: (block, query-head) columns
   static constexpr int kA = 0;                                // kStages x 16 KB, 1024-aligned
   static constexpr int kB = kA + kStages * kATileBytes;       // N x 128 B
-  static constexpr int kScale = kB + N * kRowBytes;           // kStages x 128 x 4 B
-  static constexpr int kQs = kScale + kStages * kTile * 4;    // f32 [QH][4] q block scales
+  static constexpr int kScale = kB + N * kRowBytes;           // kScaleSlots x 128 x 4 B
+  static constexpr int kQs = kScale + kScaleSlots * kTile * 4;  // f32 [QH][4] q block scales
   static constexpr int kHw = kQs + QH * 4 * 4;                // f32 [QH] head weights
   static constexpr int kPages = kHw + QH * 4;                 // int [kMaxPages]
   static constexpr int kBar = kPages + kMaxPages * 4;         // u64 full/empty[kStages], accf/acce[kAcc]
@@ -112,8 +118,8 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
 
   if (tid == kEpiThreads) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(bar_full + 8 * i, 1);
-      mbar_init(bar_empty + 8 * i, 4);
+      mbar_init(bar_full + 8 * i, 33);   // the expect-tx arrival + one per producer lane
+      mbar_init(bar_empty + 8 * i, 1);   // the MMA commit
     }
     for (int i = 0; i < kAcc; ++i) {
       mbar_init(bar_accf + 8 * i, 1);
@@ -170,32 +176,35 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == kEpiWarps) {
-    if (lane == 0) {
-      // ---- producer: stage i % kStages receives tile t_begin + i
-      for (int i = 0; i < nt; ++i) {
-        const int s = i % kStages;
-        if (!mbar_wait(bar_empty + 8 * s, ((i / kStages) & 1) ^ 1, p.status, abort_flag)) break;
-        const int e0 = (t_begin + i) * kTile;
-        const int e1 = min(nmax, e0 + kTile);
-        uint32_t bytes = 0;
-        for (int j = e0; j < e1; j += epb)
-          if (pages_s[(j >> eshift) - page0] >= 0) bytes += epb * (kPackedRowBytes + 4);
-        const uint32_t bar = bar_full + 8 * s;
-        mbar_arrive_expect_tx(bar, bytes);
-        const uint32_t a_dst = sbase + L::kA + s * kATileBytes;
-        const uint32_t s_dst = sbase + L::kScale + s * kTile * 4;
-        for (int j = e0; j < e1; j += epb) {
-          const int phys = pages_s[(j >> eshift) - page0];
-          if (phys < 0) continue;
-          const int r0 = j - e0;   // first tile row of the page
-          tma_load_2d(a_dst + r0 * kRowBytes, &tmap_k, 0, phys * epb, bar);
-          bulk_load(s_dst + r0 * 4, p.k_scale + (long long)phys * epb * 4, epb * 4, bar);
-        }
-      }
+  if (warp >= kEpiWarps && warp < kEpiWarps + kProdWarps) {
+    // ---- producer warps (tile i by producer warp i % kProdWarps): stage i % kStages receives
+    //      tile t_begin + i.  Lane p issues page p's
+    //      tensor copy of the codes (the TMA unpacks them into the MMA operand form); every lane
+    //      copies 16 bytes of block scales with cp.async.  The stage's barrier expects the code
+    //      bytes from the copies plus one arrival per lane when its scale copy lands.
+    for (int i = warp - kEpiWarps; i < nt; i += kProdWarps) {
+      const int s = i % kStages;
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait(bar_empty + 8 * s, ((i / kStages) & 1) ^ 1, p.status, abort_flag);
+      if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) == 0) break;
+      const int e0 = (t_begin + i) * kTile;
+      const int rows = min(kTile, ((min(nmax, e0 + kTile) - e0 + epb - 1) >> eshift) << eshift);  // whole pages
+      const uint32_t bar = bar_full + 8 * s;
+      const uint32_t a_dst = sbase + L::kA + s * kATileBytes;
+      const uint32_t s_dst = sbase + L::kScale + (i % kScaleSlots) * kTile * 4;
+      const int npg = rows >> eshift;
+      const int phys = lane < npg ? pages_s[((e0 >> eshift) - page0) + lane] : -1;
+      const uint32_t valid = __ballot_sync(0xffffffffu, phys >= 0);
+      if (lane == 0) mbar_arrive_expect_tx(bar, __popc(valid) * epb * kPackedRowBytes);
+      __syncwarp();
+      if (phys >= 0) tma_load_2d(a_dst + (lane << eshift) * kRowBytes, &tmap_k, 0, phys * epb, bar);
+      const int r = lane * 4;   // this lane's four scale words
+      const int ph = __shfl_sync(0xffffffffu, phys, (r >> eshift) & 31);
+      if (r < rows && ph >= 0) cp_async16_s(s_dst + r * 4, p.k_scale + ((long long)ph * epb + (r & (epb - 1))) * 4);
+      cp_async_arrive_noinc(bar);
     }
-    __syncwarp();
-  } else if (warp == kEpiWarps + 1) {
+    cp_async_wait<0>();
+  } else if (warp == kEpiWarps + kProdWarps) {
     if (lane == 0) {
       // ---- MMA issuer: tile i -> accumulator i % kAcc
       const uint64_t bdesc = smem_desc_sw128(sbase + L::kB);
@@ -209,6 +218,7 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
         for (int kb = 0; kb < 4; ++kb)   // K = 32 codes per MMA: 32 shared-memory bytes per step
           tc_mma_f8f6f4(tmem + a * N, adesc + 2 * kb, bdesc + 2 * kb, kIdesc, kb > 0 ? 1u : 0u);
         tc_commit(bar_accf + 8 * a);
+        tc_commit(bar_empty + 8 * s);   // the stage is free once these MMAs have read it
       }
     }
     __syncwarp();
@@ -230,7 +240,7 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
     for (int qi = 0; qi < QPS; ++qi) nq[qi] = qi < qn ? (n0 + qi + 1) >> mshift : 0;
     const int row = quad * 32 + lane;
     for (int i = par; i < nt; i += 2) {
-      const int s = i % kStages, a = i % kAcc;
+      const int a = i % kAcc;
       bool ok = mbar_wait(bar_accf + 8 * a, (i / kAcc) & 1, p.status, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
@@ -241,13 +251,10 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
         tmem_ld16(tmem + ((uint32_t)(quad * 32) << 16) + a * N + c16 * 16,
                   *reinterpret_cast<uint32_t(*)[16]>(&d[c16 * 16]));
       tmem_ld_wait();
-      const uint32_t sc = *reinterpret_cast<const uint32_t*>(smem + L::kScale + (s * kTile + row) * 4);
+      const uint32_t sc = *reinterpret_cast<const uint32_t*>(smem + L::kScale + ((i % kScaleSlots) * kTile + row) * 4);
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(bar_acce + 8 * a);
-        mbar_arrive(bar_empty + 8 * s);
-      }
+      if (lane == 0) mbar_arrive(bar_acce + 8 * a);
       // 2^(e-127) for the four UE8M0 bytes (e = 0 gives the subnormal 2^-127)
       float ksc[4];
       ksc[0] = __uint_as_float(max((sc << 23) & 0x7F800000u, 0x00400000u));
@@ -338,7 +345,7 @@ cudaError_t launch_tc_t(const CUtensorMap& tmap, const IndexParams& p, int max_e
   int runs = (sms * occ) / p.num_seqs;             // one wave of CTAs
   if (runs < 1) runs = 1;
   int tpc = (tiles + runs - 1) / runs;
-  const int tpc_cap = kMaxPages * p.paging.epb / kTile - 1;   // a run spans at most kMaxPages pages
+  const int tpc_cap = kMaxPages * p.paging.epb / kTile;   // a run spans at most kMaxPages pages
   if (tpc > tpc_cap) tpc = tpc_cap;
   dim3 grid((tiles + tpc - 1) / tpc, p.num_seqs);
   index_tc_kernel<HI, QH><<<grid, kThreads, L::kBytes, st>>>(tmap, p, tpc);
@@ -349,7 +356,7 @@ cudaError_t launch_tc_t(const CUtensorMap& tmap, const IndexParams& p, int max_e
 
 // Columns (query-heads) per 32-code block the tensor-core scorer needs, or 0 when it does not
 // apply (rank other than 128, pages outside 8..128 entries, more than 4 queries per sequence,
-// key codes not 32-byte aligned).
+// key codes not 32-byte or scales not 16-byte aligned).
 int index_tc_qh(const IndexParams& p, int rank, int max_new) {
   if (rank != 128 || p.paging.epb < 8 || p.paging.epb > 128 || (p.paging.epb & (p.paging.epb - 1))) return 0;
   if ((reinterpret_cast<uintptr_t>(p.k_fp4) & 31u) || (reinterpret_cast<uintptr_t>(p.k_scale) & 15u)) return 0;
@@ -366,6 +373,7 @@ cudaError_t launch_index_tc(const IndexParams& p, int rank, int max_new, int max
   if (qh == 0) return cudaErrorInvalidValue;
   auto enc = tensor_map_encoder();
   if (enc == nullptr) return cudaErrorNotSupported;
+  // codes as [rows][128] 4-bit values; a box of one page is unpacked to 16 codes per 16 bytes
   CUtensorMap tmap;
   const cuuint64_t gdim[2] = {(cuuint64_t)rank, (cuuint64_t)p.k_rows};
   const cuuint64_t gstride[1] = {(cuuint64_t)(rank / 2)};

@@ -11,6 +11,10 @@
 
 #include "common.cuh"
 
+#ifndef LCSA_WAIT_HINT_NS
+#define LCSA_WAIT_HINT_NS 1000u
+#endif
+
 namespace lcsa {
 
 // ---------------------------------------------------------------------------------------------
@@ -41,7 +45,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(1000u)
+      : "r"(bar), "r"(parity), "r"(LCSA_WAIT_HINT_NS)
       : "memory");
   return ok != 0;
 }
@@ -82,6 +86,21 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                "l"(src), "r"(bytes), "r"(bar)
                : "memory");
+}
+
+// cp.async (LDGSTS) into shared memory at a 32-bit shared address: 8 bytes (L1-allocating form,
+// the only one that takes 8) and 16 bytes (L2 only).
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async16_s(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// Arrival on the barrier once every cp.async this thread issued so far has landed (the barrier's
+// expected count includes it).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
 // Orders this thread's generic-proxy shared-memory writes before later async-proxy reads
