@@ -111,8 +111,11 @@ typedef struct {
  *            pending_slots = 2m (overlap) or m.
  *  new_rows: rows of this call's new tokens in the row format (row = global token index), so
  *            that attention can read window rows of a multi-token chunk before they enter
- *            the ring.  If new_rows.nope is NULL, compress writes the ring itself (use when
- *            the call is not followed by attention over the same tokens). */
+ *            the ring.  If new_rows.nope is NULL, compress writes the ring itself: use it when
+ *            the call is not followed by attention over the same tokens, or when every sequence
+ *            has at most one new token (decode).  Token p then replaces token p-128, which is
+ *            outside p's window, so attention can read the whole window from the ring and no
+ *            lcs_window_commit is needed. */
 typedef struct {
   lcs_rows window;
   void* pending;
@@ -208,7 +211,8 @@ lcs_status csa_index_topk_noalloc(const lcs_batch* batch, const uint8_t* q_fp4, 
  *   HCA: the entries 0 .. N(t)-1, N(t) = floor((t+1)/m), then the same window tokens;
  * logits = softmax_scale * q[i,h,:] . row, o[i,h,:] = sum p * row (shared KV: the row is key
  * and value).  Window token p is read from state->new_rows when p is one of this call's new
- * tokens (p >= seq_len-q_b) and from the window ring otherwise.
+ * tokens (p >= seq_len-q_b) and from the window ring otherwise; with new_rows.nope NULL every
+ * window row comes from the ring, which requires batch->max_new <= 1 (LCS_ERR_SHAPE otherwise).
  *   q       device bf16[total_new][heads][D]    out device bf16[total_new][heads][D]
  *   out_lse device f32[total_new][heads] (natural log of the softmax denominator) or NULL
  *   heads in {8, 16, 64, 128} (multiples of 16 up to 128, or 8); D in {128, 512}.

@@ -83,6 +83,20 @@ size_t attend_ws_bytes(const lcs_batch* b, int heads, int dim, const SplitPlan& 
   return per * dim * 4 + per * 2 * 4 + 256;
 }
 
+// Workspace of csa_index_topk, in order: keys u32[T][ld], histograms u32[T][2048].
+struct TopkWs {
+  size_t keys, hist, total;
+};
+
+TopkWs topk_ws_layout(const lcs_batch* b, int m) {
+  const size_t T = (size_t)b->total_new, ld = (size_t)index_ld(b, m);
+  TopkWs w;
+  w.keys = 0;
+  w.hist = w.keys + T * ld * 4;
+  w.total = w.hist + T * kTopkHistBins * 4 + 256;
+  return w;
+}
+
 lcs_status compress_common(const lcs_batch* batch, const void* raw, const lcs_compressor* comp,
                            const lcs_state* state, const lcs_rows* entries, const lcs_paging* paging,
                            int32_t* dev_status, void* stream, bool hca) {
@@ -171,10 +185,16 @@ lcs_status attend_common(const lcs_batch* batch, const void* q, int32_t heads, c
   if ((s = check_rows(&state->window)) != LCS_OK) return s;
   if (!same_layout(state->window, *entries)) return LCS_ERR_SHAPE;
   if (state->window.num_rows < (int64_t)batch->num_seqs * LCSA_WINDOW) return LCS_ERR_SHAPE;
-  // every query's own token is one of this call's new tokens: its window row comes from new_rows
-  if ((s = check_rows(&state->new_rows)) != LCS_OK) return s;
-  if (!same_layout(state->new_rows, *entries)) return LCS_ERR_SHAPE;
-  if (state->new_rows.num_rows < batch->total_new) return LCS_ERR_SHAPE;
+  // every query's own token is one of this call's new tokens: its window row comes from new_rows,
+  // or, when new_rows is absent, from the ring (one new token per sequence, already in the ring)
+  const bool have_new = state->new_rows.nope != nullptr;
+  if (have_new) {
+    if ((s = check_rows(&state->new_rows)) != LCS_OK) return s;
+    if (!same_layout(state->new_rows, *entries)) return LCS_ERR_SHAPE;
+    if (state->new_rows.num_rows < batch->total_new) return LCS_ERR_SHAPE;
+  } else if (batch->max_new > 1) {
+    return LCS_ERR_SHAPE;
+  }
   if (entries->num_rows < 1) return LCS_ERR_SHAPE;
   if (entries->format == LCS_ROW_BF16 && entries->dim == 512) return LCS_ERR_UNSUPPORTED;
   const SplitPlan plan = plan_splits(batch, heads, max_rows);
@@ -191,6 +211,10 @@ lcs_status attend_common(const lcs_batch* batch, const void* q, int32_t heads, c
   p.paging = make_paging(*paging);
   p.window = make_rows(state->window);
   p.new_rows = make_rows(state->new_rows);
+  if (!have_new) {
+    p.new_rows.nope = nullptr;
+    p.new_rows.num_rows = 0;
+  }
   p.out = static_cast<__nv_bfloat16*>(out);
   p.splits = plan.splits;
   p.rows_per_split = plan.rows_per_split;
@@ -205,6 +229,12 @@ lcs_status attend_common(const lcs_batch* batch, const void* q, int32_t heads, c
 }  // namespace
 
 extern "C" {
+
+size_t lcs_index_topk_workspace(const lcs_batch* batch, int32_t m, int32_t k) {
+  (void)k;
+  if (batch == nullptr || m <= 0) return 0;
+  return topk_ws_layout(batch, m).total;
+}
 
 int32_t lcs_abi_version(void) { return LCSA_ABI_VERSION; }
 
@@ -254,11 +284,7 @@ lcs_status lcs_window_commit(const lcs_batch* batch, const lcs_state* state, int
                                         static_cast<cudaStream_t>(stream)));
 }
 
-size_t lcs_index_topk_workspace(const lcs_batch* batch, int32_t m, int32_t k) {
-  (void)k;
-  if (batch == nullptr || m <= 0) return 0;
-  return (size_t)batch->total_new * (size_t)index_ld(batch, m) * 4 + (size_t)batch->total_new * kTopkHistBins * 4 + 256;
-}
+
 
 lcs_status csa_index_topk(const lcs_batch* batch, const uint8_t* q_fp4, const uint8_t* q_scale, const float* head_w,
                           int32_t heads, const lcs_index_keys* keys, const lcs_paging* paging, int32_t m, int32_t k,
@@ -276,13 +302,15 @@ lcs_status csa_index_topk(const lcs_batch* batch, const uint8_t* q_fp4, const ui
   p.head_w = head_w;
   p.relu = (flags & LCS_INDEX_RELU) ? 1 : 0;
   p.ld = index_ld(batch, m);
-  p.keys_out = static_cast<uint32_t*>(workspace);
-  p.hist = p.keys_out + (size_t)batch->total_new * p.ld;
+  const TopkWs w = topk_ws_layout(batch, m);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.keys_out = reinterpret_cast<uint32_t*>(ws + w.keys);
+  p.hist = reinterpret_cast<uint32_t*>(ws + w.hist);
   p.status = dev_status;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int max_entries = batch->max_seq_len / m;
   // the per-query histograms accumulate with atomics: clear them first
-  cudaError_t e = cudaMemsetAsync(p.hist, 0, (size_t)batch->total_new * kTopkHistBins * 4, st);
+  cudaError_t e = cudaMemsetAsync(ws + w.hist, 0, w.total - 256 - w.hist, st);
   if (e != cudaSuccess) return LCS_ERR_CUDA;
   e = index_tc_qh(p, keys->rank, batch->max_new) > 0 ? launch_index_tc(p, keys->rank, batch->max_new, max_entries, num_sms(), st)
                                                      : launch_index_scores(p, keys->rank, batch->max_new, max_entries, st);

@@ -156,7 +156,7 @@ __global__ void __launch_bounds__(256, 1) attend_kernel(AttendParams p) {
       } else {
         const int pos = t - W + 1 + (r - cnt);
         long long row;
-        if (pos >= n0) {
+        if (pos >= n0 && p.new_rows.nope != nullptr) {
           row = (long long)sp.q0 + (pos - n0);
           d = row < p.new_rows.num_rows ? (row | (1ll << 60)) : -1;
         } else {

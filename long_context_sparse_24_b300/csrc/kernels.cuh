@@ -73,10 +73,10 @@ cudaError_t launch_compress(const CompressParams& p, int D, int max_new, cudaStr
 cudaError_t launch_window_commit(const int32_t* cu_new, const int32_t* seq_len, int num_seqs, int max_new,
                                  const Rows& src, const Rows& ring, int32_t* status, cudaStream_t st);
 cudaError_t launch_index_scores(const IndexParams& p, int rank, int max_new, int max_entries, cudaStream_t st);
+constexpr int kTopkHistBins = 2048;   // bins of the per-query score-key histogram (key >> 21)
 cudaError_t launch_topk_select(const uint32_t* keys, const uint32_t* hist, long long ld, const int32_t* cu_new,
                                const int32_t* seq_len, int num_seqs, int max_new, int m, int k, int32_t* out_idx,
                                int32_t* out_cnt, cudaStream_t st);
-constexpr int kTopkHistBins = 2048;   // bins of the per-query score-key histogram (key >> 21)
 // tcgen05 scorer for a few queries per sequence: query-head columns it would use (0 = not applicable)
 int index_tc_qh(const IndexParams& p, int rank, int max_new);
 cudaError_t launch_index_tc(const IndexParams& p, int rank, int max_new, int max_entries, int sms, cudaStream_t st);

@@ -2,8 +2,9 @@
 
 Owns the caller-side buffers (entry cache, indexer keys, state cache, workspaces) and issues the
 library calls of one step in order:
-  CSA: csa_compress -> csa_index_topk -> csa_attend -> lcs_window_commit
-  HCA: hca_compress -> hca_attend -> lcs_window_commit
+  CSA: csa_compress || csa_index_topk -> csa_attend [-> lcs_window_commit]
+  HCA: hca_compress -> hca_attend [-> lcs_window_commit]
+(lcs_window_commit only for multi-token steps; single-token steps keep the window in the ring.)
 No arithmetic of the method happens here.
 """
 from __future__ import annotations
@@ -33,9 +34,15 @@ class Layer:
         self.num_seqs, self.capacity, self.max_new = num_seqs, capacity, max_new
         self.scale = softmax_scale if softmax_scale is not None else 1.0 / math.sqrt(dim)
         self.device = device
-        self.cache = buffers.alloc_layer(num_seqs, capacity, dim, fmt, self.m, self.overlap, num_seqs * max_new,
+        # one new token per sequence: the window ring takes every token directly (token p replaces
+        # p-128, outside p's window), so there are no separate new-token rows and no commit step
+        self.ring_only = max_new <= 1
+        self.cache = buffers.alloc_layer(num_seqs, capacity, dim, fmt, self.m, self.overlap,
+                                         0 if self.ring_only else num_seqs * max_new,
                                          device, index_rank=index_rank if kind == "csa" else 0,
                                          block_order=block_order)
+        # compression does not feed the indexer: it runs on a side stream next to it
+        self.side = torch.cuda.Stream(device=device) if kind == "csa" else None
         self.comp: Optional[Compressor] = None
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
         # workspaces sized for the largest step this layer will run
@@ -87,13 +94,20 @@ class Layer:
                        self.scale, out, lse, self.attend_ws, self.attend_ws_bytes, self.status, stream)
 
     def commit(self, batch: Batch, stream=None) -> None:
-        lcs_window_commit(batch, self.cache.state, self.status, stream)
+        if not self.ring_only:
+            lcs_window_commit(batch, self.cache.state, self.status, stream)
 
     def step(self, batch: Batch, raw_new: torch.Tensor, q: torch.Tensor, out: torch.Tensor,
              lse: Optional[torch.Tensor] = None, idx_q_fp4=None, idx_q_scale=None, head_w=None, stream=None) -> None:
-        """One pass of the hot path for the batch's new tokens."""
-        self.compress(batch, raw_new, stream)
+        """One pass of the hot path for the batch's new tokens.  CSA: compression (side stream) and
+        the indexer top-k run concurrently; attention waits for both."""
+        main = stream if stream is not None else torch.cuda.current_stream()
         if self.kind == "csa":
-            self.select(batch, idx_q_fp4, idx_q_scale, head_w, stream)
-        self.attend(batch, q, out, lse, stream)
-        self.commit(batch, stream)
+            self.side.wait_stream(main)
+            self.compress(batch, raw_new, self.side)
+            self.select(batch, idx_q_fp4, idx_q_scale, head_w, main)
+            main.wait_stream(self.side)
+        else:
+            self.compress(batch, raw_new, main)
+        self.attend(batch, q, out, lse, main)
+        self.commit(batch, main)
