@@ -58,12 +58,20 @@ long long index_ld(const lcs_batch* b, int m) {
 struct SplitPlan {
   int splits;
   int rows_per_split;
+  int tc;
 };
 
-SplitPlan plan_splits(const lcs_batch* b, int heads, int max_rows) {
+// The tensor-core attention takes FP8-split rows of D = 512 (the only D = 512 format), up to 64
+// heads and up to kAttendTcMaxRows rows per query, one 128-row tile per CTA.
+bool attend_tc_applies(int heads, int dim, int max_rows) {
+  return dim == 512 && heads <= 64 && max_rows <= kAttendTcMaxRows;
+}
+
+SplitPlan plan_splits(const lcs_batch* b, int heads, int dim, int max_rows) {
+  if (attend_tc_applies(heads, dim, max_rows)) return SplitPlan{(max_rows + 127) / 128, 128, 1};
   const int hg = heads <= 16 ? 1 : (heads + 63) / 64;
   const long long base = (long long)b->total_new * hg;
-  SplitPlan s{1, max_rows > 0 ? max_rows : 1};
+  SplitPlan s{1, max_rows > 0 ? max_rows : 1, 0};
   const int sms = num_sms();
   if (base <= 0 || base >= sms || max_rows <= 64) return s;
   int want = (int)(sms / base);
@@ -197,7 +205,7 @@ lcs_status attend_common(const lcs_batch* batch, const void* q, int32_t heads, c
   }
   if (entries->num_rows < 1) return LCS_ERR_SHAPE;
   if (entries->format == LCS_ROW_BF16 && entries->dim == 512) return LCS_ERR_UNSUPPORTED;
-  const SplitPlan plan = plan_splits(batch, heads, max_rows);
+  const SplitPlan plan = plan_splits(batch, heads, entries->dim, max_rows);
   const size_t need = attend_ws_bytes(batch, heads, entries->dim, plan);
   if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return LCS_ERR_WORKSPACE;
   if (need > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return LCS_ERR_ALIGNMENT;
@@ -218,6 +226,7 @@ lcs_status attend_common(const lcs_batch* batch, const void* q, int32_t heads, c
   p.out = static_cast<__nv_bfloat16*>(out);
   p.splits = plan.splits;
   p.rows_per_split = plan.rows_per_split;
+  p.tc = plan.tc;
   if (plan.splits > 1) {
     const size_t per = (size_t)batch->total_new * heads * plan.splits;
     p.ws_o = static_cast<float*>(workspace);
@@ -342,7 +351,7 @@ lcs_status csa_index_scores(const lcs_batch* batch, const uint8_t* q_fp4, const 
 
 size_t lcs_attend_workspace(const lcs_batch* batch, int32_t heads, int32_t dim, int32_t max_rows) {
   if (batch == nullptr) return 0;
-  return attend_ws_bytes(batch, heads, dim, plan_splits(batch, heads, max_rows));
+  return attend_ws_bytes(batch, heads, dim, plan_splits(batch, heads, dim, max_rows));
 }
 
 lcs_status csa_attend(const lcs_batch* batch, const void* q, int32_t heads, const int32_t* topk_idx,

@@ -537,6 +537,12 @@ static cudaError_t launch_attend_t(const AttendParams& p, int total_new, cudaStr
   return cudaGetLastError();
 }
 
+cudaError_t launch_attend_combine(const AttendParams& p, int total_new, int D, cudaStream_t st) {
+  if (D == 512) attend_combine_kernel<512><<<dim3(total_new, p.heads), 512 / 4, 0, st>>>(p);
+  else attend_combine_kernel<128><<<dim3(total_new, p.heads), 128 / 4, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
 size_t attend_smem_bytes(int D, int fmt, int heads) {
   const bool small = heads <= 16;
   if (D == 512) return small ? AttendSmem<512, LCS_ROW_FP8_SPLIT, 1>::kBytes : AttendSmem<512, LCS_ROW_FP8_SPLIT, 4>::kBytes;
@@ -546,6 +552,7 @@ size_t attend_smem_bytes(int D, int fmt, int heads) {
 
 cudaError_t launch_attend(const AttendParams& p, int D, int fmt, int total_new, cudaStream_t st) {
   if (total_new == 0) return cudaSuccess;
+  if (p.tc) return launch_attend_tc(p, total_new, st);
   const bool small = p.heads <= 16;
   if (D == 512) {
     if (small) return launch_attend_t<512, LCS_ROW_FP8_SPLIT, 1>(p, total_new, st);

@@ -66,6 +66,7 @@ struct AttendParams {
   float* ws_ml;              // [T][H][splits][2]
   int splits;
   int rows_per_split;
+  int tc;                    // 1: tensor-core kernel (128-row tiles, rows_per_split == 128)
   int32_t* status;
 };
 
@@ -81,5 +82,9 @@ cudaError_t launch_topk_select(const uint32_t* keys, const uint32_t* hist, long 
 int index_tc_qh(const IndexParams& p, int rank, int max_new);
 cudaError_t launch_index_tc(const IndexParams& p, int rank, int max_new, int max_entries, int sms, cudaStream_t st);
 cudaError_t launch_attend(const AttendParams& p, int D, int fmt, int total_new, cudaStream_t st);
+cudaError_t launch_attend_tc(const AttendParams& p, int total_new, cudaStream_t st);
+cudaError_t launch_attend_combine(const AttendParams& p, int total_new, int D, cudaStream_t st);
+// rows of one query the tensor-core attention takes at most (per 64-head group)
+constexpr int kAttendTcMaxRows = 1024;
 
 }  // namespace lcsa
