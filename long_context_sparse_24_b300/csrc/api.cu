@@ -85,10 +85,12 @@ SplitPlan plan_splits(const lcs_batch* b, int heads, int dim, int max_rows) {
   return s;
 }
 
+// Split partials: O [T][H][splits][D] (fp32, or BF16 for the tensor-core kernel), then the
+// (max, sum) pairs [T][H][splits][2] fp32.
 size_t attend_ws_bytes(const lcs_batch* b, int heads, int dim, const SplitPlan& s) {
   if (s.splits <= 1) return 0;
   const size_t per = (size_t)b->total_new * heads * s.splits;
-  return per * dim * 4 + per * 2 * 4 + 256;
+  return per * dim * (s.tc ? 2 : 4) + per * 2 * 4 + 256;
 }
 
 // Workspace of csa_index_topk, in order: keys u32[T][ld], histograms u32[T][2048].
@@ -229,8 +231,10 @@ lcs_status attend_common(const lcs_batch* batch, const void* q, int32_t heads, c
   p.tc = plan.tc;
   if (plan.splits > 1) {
     const size_t per = (size_t)batch->total_new * heads * plan.splits;
-    p.ws_o = static_cast<float*>(workspace);
-    p.ws_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + per * entries->dim * 4);
+    const size_t ob = per * entries->dim * (plan.tc ? 2 : 4);
+    if (plan.tc) p.ws_ob = static_cast<__nv_bfloat16*>(workspace);
+    else p.ws_o = static_cast<float*>(workspace);
+    p.ws_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + ob);
   }
   return LCS_OK;
 }

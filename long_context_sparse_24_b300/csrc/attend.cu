@@ -501,7 +501,16 @@ __global__ void __launch_bounds__(D / 4) attend_combine_kernel(AttendParams p) {
     if (!(l > 0.0f)) continue;
     const float wgt = exp2f(ml[2 * s] - M);
     Lsum += l * wgt;
-    const float4 v = *reinterpret_cast<const float4*>(p.ws_o + (((long long)q * H + h) * S + s) * D + tid * 4);
+    float4 v;
+    const long long off = (((long long)q * H + h) * S + s) * D + tid * 4;
+    if (p.ws_ob != nullptr) {
+      const uint2 raw = *reinterpret_cast<const uint2*>(p.ws_ob + off);
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
+      const float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
+      v = make_float4(a.x, a.y, c.x, c.y);
+    } else {
+      v = *reinterpret_cast<const float4*>(p.ws_o + off);
+    }
     acc.x = fmaf(v.x, wgt, acc.x);
     acc.y = fmaf(v.y, wgt, acc.y);
     acc.z = fmaf(v.z, wgt, acc.z);

@@ -11,8 +11,8 @@
 // Work of a CTA (query q, 64-head group, tile of rows).  Everything runs in F16 on the rows
 // rescaled by their own FP8 scale s_r: R'_r = [rope_r / s_r | codes_r] (the E4M3 codes are exact
 // in F16), so that q . row_r = s_r * (q . R'_r) and sum_r p_r row_r = sum_r (p_r s_r) R'_r.
-//   gather   row descriptors and scales (top-k entries, window rows); every thread then loads
-//            its 8-byte pieces of FP8 codes and 16-byte pieces of RoPE dims straight into
+//   gather   row descriptors (top-k entries, window rows); every thread then loads the row
+//            scales, its 8-byte pieces of FP8 codes and 16-byte pieces of RoPE dims straight into
 //            registers and writes them widened to F16 into the tile: eight K-major chunks of
 //            [128 rows][64 dims] (chunk 0 the RoPE dims times 1/s_r); the query arrives by
 //            cp.async into eight K-major chunks of [64 heads][64 dims] and becomes F16 in place;
@@ -26,7 +26,7 @@
 //            heads, K = 16 rows;
 //   epilogue O^T is read from tensor memory (lane = dim, column = head), transposed per warp
 //            through shared memory and written in 16-byte pieces, normalised by 2^8 * sum p (one
-//            split) or as a partial with its (max, sum) for the combine kernel.
+//            split) or as a BF16 partial with its (max, sum) for the combine kernel.
 // Operand chunks use the 128-byte swizzle (16-byte piece j of row r at position j ^ (r % 8)).
 // Range: query values within F16 range and row scales below 256 (|x| < 114688), as for the
 // warp-MMA kernel.
@@ -195,14 +195,6 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
       }
     }
     desc[tid] = d;
-    float sc = 0.0f;
-    if (d >= 0) {
-      const int kind = (int)(d >> 60);
-      const long long rw = d & ((1ll << 60) - 1);
-      sc = (kind == 1 ? p.new_rows.scale : (kind == 2 ? p.window.scale : p.entries.scale))[rw];
-    }
-    sscale[tid] = sc;
-    rinv[tid] = sc > 0.0f ? __frcp_rn(sc) : 0.0f;
   }
   if (tid == 0) {
     mbar_init(bar_s, 1);
@@ -219,6 +211,13 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
     constexpr int kRP = kTileRows * 8 / kThreads;      // 4 RoPE pieces per thread
     uint2 cv[kNP];
     uint4 rv[kRP];
+    float sc = 0.0f;                                   // threads 0-127: the scale of row tid
+    if (tid < kTileRows && desc[tid] >= 0) {
+      const long long d = desc[tid];
+      const int kind = (int)(d >> 60);
+      const long long rw = d & ((1ll << 60) - 1);
+      sc = __ldg((kind == 1 ? p.new_rows.scale : (kind == 2 ? p.window.scale : p.entries.scale)) + rw);
+    }
 #pragma unroll
     for (int it = 0; it < kNP; ++it) {
       const int idx = it * kThreads + tid, r = idx / 56, u = idx % 56;
@@ -243,6 +242,11 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
         rv[it] = __ldg(reinterpret_cast<const uint4*>(src + rw * kRope + j * 8));
       }
     }
+    if (tid < kTileRows) {
+      sscale[tid] = sc;
+      rinv[tid] = sc > 0.0f ? __frcp_rn(sc) : 0.0f;
+    }
+    __syncthreads();
 #pragma unroll
     for (int it = 0; it < kNP; ++it) {
       const int idx = it * kThreads + tid, r = idx / 56, u = idx % 56;
@@ -383,7 +387,9 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
             uint2 pk = make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
             *reinterpret_cast<uint2*>(p.out + ((long long)q * H + h0 + h) * kD + dim0 + d4) = pk;
           } else {
-            *reinterpret_cast<float4*>(p.ws_o + (((long long)q * H + h0 + h) * p.splits + split) * kD + dim0 + d4) = o;
+            __nv_bfloat162 lo = __floats2bfloat162_rn(o.x, o.y), hi = __floats2bfloat162_rn(o.z, o.w);
+            uint2 pk = make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+            *reinterpret_cast<uint2*>(p.ws_ob + (((long long)q * H + h0 + h) * p.splits + split) * kD + dim0 + d4) = pk;
           }
         }
       }

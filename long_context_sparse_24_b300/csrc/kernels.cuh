@@ -62,7 +62,8 @@ struct AttendParams {
   float scale_log2;
   __nv_bfloat16* out;
   float* out_lse;
-  float* ws_o;               // [T][H][splits][D]
+  float* ws_o;               // [T][H][splits][D] fp32 partials (warp-MMA kernel), or
+  __nv_bfloat16* ws_ob;      // [T][H][splits][D] BF16 partials (tensor-core kernel)
   float* ws_ml;              // [T][H][splits][2]
   int splits;
   int rows_per_split;
