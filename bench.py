@@ -273,8 +273,11 @@ def run_gpu(args, rank, world, local):
         ms = float(t.item())
     stages = [statistics.mean(x[i] for x in stage_ms) for i in range(4)] if stage_ms else [float("nan")] * 4
     splits_used = layer.attend_ws_bytes > 0
-    # compress (entries + state) + indexer (score + select) + attention (+ combine) + commit
-    launches_per_step = 2 + 2 + (2 if splits_used else 1) + (0 if layer.ring_only else 1)
+    # compress (entries + state) + indexer (score + select) + attention (tensor-core plan: window part,
+    # top-k part, merge; otherwise one kernel, plus a merge when split) + window commit
+    tc_plan = D == 512 and H <= 64 and k + 128 <= 1024
+    attend_launches = 3 if tc_plan else (2 if splits_used else 1)
+    launches_per_step = 2 + 2 + attend_launches + (0 if layer.ring_only else 1)
     # ---- roofline of the dominant call (lightning indexer: score scan + top-k select)
     hbm, peak_kind = measured_peaks()
     n_vis = [(L + s + 1) // m for s in range(timed_end, steps_total)]

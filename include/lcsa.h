@@ -226,6 +226,27 @@ lcs_status csa_attend(const lcs_batch* batch, const void* q, int32_t heads, cons
                       const lcs_paging* paging, const lcs_state* state, float softmax_scale,
                       void* out, float* out_lse, void* workspace, size_t workspace_bytes,
                       int32_t* dev_status, void* stream);
+/* csa_attend in two calls, so that the sliding-window part, which does not depend on the top-k
+ * selection, can run while the indexer does (CSA step 3 of x-techcon section 2 attends the window
+ * rows and the selected entries in one softmax; splitting the rows and merging the per-part
+ * (max, sum, weighted sum) partials is exact up to rounding).
+ *  csa_attend_window: the window rows of every query into the workspace (no output yet).
+ *  csa_attend_topk:   the selected entries, then the merge with the window part into out/out_lse.
+ * Arguments as for csa_attend (the window call needs no top-k list).  Both calls must get the same
+ * batch, heads, k, m, row sets and workspace, and the window call must complete before the top-k
+ * call's merge starts (same stream, or an event).  csa_attend_window + csa_attend_topk give
+ * exactly the bits of csa_attend.  When the library does not compute the window part apart (see
+ * lcs_attend_workspace: shapes outside the tensor-core plan), csa_attend_window launches nothing
+ * and csa_attend_topk computes everything. */
+lcs_status csa_attend_window(const lcs_batch* batch, const void* q, int32_t heads, int32_t k, int32_t m,
+                             const lcs_rows* entries, const lcs_paging* paging, const lcs_state* state,
+                             float softmax_scale, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                             void* stream);
+lcs_status csa_attend_topk(const lcs_batch* batch, const void* q, int32_t heads, const int32_t* topk_idx,
+                           const int32_t* topk_cnt, int32_t k, int32_t m, const lcs_rows* entries,
+                           const lcs_paging* paging, const lcs_state* state, float softmax_scale, void* out,
+                           float* out_lse, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                           void* stream);
 lcs_status hca_attend(const lcs_batch* batch, const void* q, int32_t heads, int32_t m,
                       const lcs_rows* entries, const lcs_paging* paging, const lcs_state* state,
                       float softmax_scale, void* out, float* out_lse, void* workspace,

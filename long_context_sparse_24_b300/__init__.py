@@ -87,6 +87,10 @@ _SIGS = {
     "lcs_attend_workspace": (c_sz, [P(lcs_batch), c_i32, c_i32, c_i32]),
     "csa_attend": (c_i32, [P(lcs_batch), c_vp, c_i32, c_vp, c_vp, c_i32, c_i32, P(lcs_rows), P(lcs_paging),
                            P(lcs_state), ctypes.c_float, c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
+    "csa_attend_window": (c_i32, [P(lcs_batch), c_vp, c_i32, c_i32, c_i32, P(lcs_rows), P(lcs_paging), P(lcs_state),
+                                  ctypes.c_float, c_vp, c_sz, c_vp, c_vp]),
+    "csa_attend_topk": (c_i32, [P(lcs_batch), c_vp, c_i32, c_vp, c_vp, c_i32, c_i32, P(lcs_rows), P(lcs_paging),
+                                P(lcs_state), ctypes.c_float, c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
     "hca_attend": (c_i32, [P(lcs_batch), c_vp, c_i32, c_i32, P(lcs_rows), P(lcs_paging), P(lcs_state),
                            ctypes.c_float, c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
 }
@@ -277,6 +281,24 @@ def csa_attend(batch: Batch, q, heads: int, topk_idx, topk_cnt, k: int, m: int, 
     _check(_lib.csa_attend(ctypes.byref(b), _ptr(q), heads, _ptr(topk_idx), _ptr(topk_cnt), k, m, ctypes.byref(e),
                            ctypes.byref(p), ctypes.byref(s), softmax_scale, _ptr(out), _ptr(out_lse),
                            _ptr(workspace), workspace_bytes, _ptr(dev_status), _stream(stream)), "csa_attend")
+
+
+def csa_attend_window(batch: Batch, q, heads: int, k: int, m: int, entries: RowSet, paging: Paging, state: State,
+                      softmax_scale: float, workspace, workspace_bytes: int, dev_status=None, stream=None) -> None:
+    b, e, p, s = batch.c(), entries.c(), paging.c(), state.c()
+    _check(_lib.csa_attend_window(ctypes.byref(b), _ptr(q), heads, k, m, ctypes.byref(e), ctypes.byref(p),
+                                  ctypes.byref(s), softmax_scale, _ptr(workspace), workspace_bytes, _ptr(dev_status),
+                                  _stream(stream)), "csa_attend_window")
+
+
+def csa_attend_topk(batch: Batch, q, heads: int, topk_idx, topk_cnt, k: int, m: int, entries: RowSet, paging: Paging,
+                    state: State, softmax_scale: float, out, out_lse, workspace, workspace_bytes: int,
+                    dev_status=None, stream=None) -> None:
+    b, e, p, s = batch.c(), entries.c(), paging.c(), state.c()
+    _check(_lib.csa_attend_topk(ctypes.byref(b), _ptr(q), heads, _ptr(topk_idx), _ptr(topk_cnt), k, m,
+                                ctypes.byref(e), ctypes.byref(p), ctypes.byref(s), softmax_scale, _ptr(out),
+                                _ptr(out_lse), _ptr(workspace), workspace_bytes, _ptr(dev_status), _stream(stream)),
+           "csa_attend_topk")
 
 
 def hca_attend(batch: Batch, q, heads: int, m: int, entries: RowSet, paging: Paging, state: State,

@@ -1,4 +1,5 @@
 // C ABI entry points: argument validation, workspace layout and kernel launches.
+#include <algorithm>
 #include <cstring>
 
 #include "kernels.cuh"
@@ -59,6 +60,7 @@ struct SplitPlan {
   int splits;
   int rows_per_split;
   int tc;
+  int entry_splits;   // tensor-core plan: 128-row tiles of entries; one more split for the window
 };
 
 // The tensor-core attention takes FP8-split rows of D = 512 (the only D = 512 format), up to 64
@@ -68,10 +70,13 @@ bool attend_tc_applies(int heads, int dim, int max_rows) {
 }
 
 SplitPlan plan_splits(const lcs_batch* b, int heads, int dim, int max_rows) {
-  if (attend_tc_applies(heads, dim, max_rows)) return SplitPlan{(max_rows + 127) / 128, 128, 1};
+  if (attend_tc_applies(heads, dim, max_rows)) {
+    const int es = std::max(1, (max_rows - LCSA_WINDOW + 127) / 128);
+    return SplitPlan{es + 1, 128, 1, es};
+  }
   const int hg = heads <= 16 ? 1 : (heads + 63) / 64;
   const long long base = (long long)b->total_new * hg;
-  SplitPlan s{1, max_rows > 0 ? max_rows : 1, 0};
+  SplitPlan s{1, max_rows > 0 ? max_rows : 1, 0, 0};
   const int sms = num_sms();
   if (base <= 0 || base >= sms || max_rows <= 64) return s;
   int want = (int)(sms / base);
@@ -184,10 +189,10 @@ lcs_status index_common(const lcs_batch* batch, const uint8_t* q_fp4, const uint
 
 lcs_status attend_common(const lcs_batch* batch, const void* q, int32_t heads, const lcs_rows* entries,
                          const lcs_paging* paging, const lcs_state* state, void* out, void* workspace,
-                         size_t workspace_bytes, int max_rows, AttendParams& p) {
+                         size_t workspace_bytes, int max_rows, AttendParams& p, bool no_out = false) {
   lcs_status s = check_batch(batch);
   if (s != LCS_OK) return s;
-  if (q == nullptr || out == nullptr || state == nullptr) return LCS_ERR_INVALID_ARG;
+  if (q == nullptr || (out == nullptr && !no_out) || state == nullptr) return LCS_ERR_INVALID_ARG;
   if (!(heads == 8 || (heads % 16 == 0 && heads >= 16 && heads <= 128))) return LCS_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(out)) return LCS_ERR_ALIGNMENT;
   if ((s = check_rows(entries)) != LCS_OK) return s;
@@ -229,6 +234,7 @@ lcs_status attend_common(const lcs_batch* batch, const void* q, int32_t heads, c
   p.splits = plan.splits;
   p.rows_per_split = plan.rows_per_split;
   p.tc = plan.tc;
+  p.entry_splits = plan.entry_splits;
   if (plan.splits > 1) {
     const size_t per = (size_t)batch->total_new * heads * plan.splits;
     const size_t ob = per * entries->dim * (plan.tc ? 2 : 4);
@@ -237,6 +243,34 @@ lcs_status attend_common(const lcs_batch* batch, const void* q, int32_t heads, c
     p.ws_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + ob);
   }
   return LCS_OK;
+}
+
+lcs_status csa_attend_part(const lcs_batch* batch, const void* q, int32_t heads, const int32_t* topk_idx,
+                           const int32_t* topk_cnt, int32_t k, int32_t m, const lcs_rows* entries,
+                           const lcs_paging* paging, const lcs_state* state, float softmax_scale, void* out,
+                           float* out_lse, void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream,
+                           int part) {
+  if (topk_idx == nullptr && part != 1) return LCS_ERR_INVALID_ARG;
+  if (k < 1 || k > 4096 || m <= 0 || m > 128) return LCS_ERR_UNSUPPORTED;
+  AttendParams p;
+  lcs_status s = attend_common(batch, q, heads, entries, paging, state, part == 1 ? nullptr : out, workspace,
+                               workspace_bytes, k + LCSA_WINDOW, p, part == 1);
+  if (s != LCS_OK) return s;
+  if (part != 0 && !p.tc) {
+    // only the tensor-core plan computes the window split apart: here the window call does
+    // nothing and the top-k call computes everything
+    if (part == 1) return LCS_OK;
+    part = 0;
+  }
+  p.part = part;
+  p.topk_idx = topk_idx;
+  p.topk_cnt = topk_cnt;
+  p.k = k;
+  p.m = m;
+  p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  p.out_lse = out_lse;
+  p.status = dev_status;
+  return from_cuda(launch_attend(p, entries->dim, entries->format, batch->total_new, static_cast<cudaStream_t>(stream)));
 }
 
 }  // namespace
@@ -362,20 +396,25 @@ lcs_status csa_attend(const lcs_batch* batch, const void* q, int32_t heads, cons
                       const int32_t* topk_cnt, int32_t k, int32_t m, const lcs_rows* entries, const lcs_paging* paging,
                       const lcs_state* state, float softmax_scale, void* out, float* out_lse, void* workspace,
                       size_t workspace_bytes, int32_t* dev_status, void* stream) {
-  if (topk_idx == nullptr) return LCS_ERR_INVALID_ARG;
-  if (k < 1 || k > 4096 || m <= 0 || m > 128) return LCS_ERR_UNSUPPORTED;
-  AttendParams p;
-  lcs_status s = attend_common(batch, q, heads, entries, paging, state, out, workspace, workspace_bytes,
-                               k + LCSA_WINDOW, p);
-  if (s != LCS_OK) return s;
-  p.topk_idx = topk_idx;
-  p.topk_cnt = topk_cnt;
-  p.k = k;
-  p.m = m;
-  p.scale_log2 = softmax_scale * 1.4426950408889634f;
-  p.out_lse = out_lse;
-  p.status = dev_status;
-  return from_cuda(launch_attend(p, entries->dim, entries->format, batch->total_new, static_cast<cudaStream_t>(stream)));
+  return csa_attend_part(batch, q, heads, topk_idx, topk_cnt, k, m, entries, paging, state, softmax_scale, out,
+                         out_lse, workspace, workspace_bytes, dev_status, stream, 0);
+}
+
+lcs_status csa_attend_window(const lcs_batch* batch, const void* q, int32_t heads, int32_t k, int32_t m,
+                             const lcs_rows* entries, const lcs_paging* paging, const lcs_state* state,
+                             float softmax_scale, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                             void* stream) {
+  return csa_attend_part(batch, q, heads, nullptr, nullptr, k, m, entries, paging, state, softmax_scale, nullptr,
+                         nullptr, workspace, workspace_bytes, dev_status, stream, 1);
+}
+
+lcs_status csa_attend_topk(const lcs_batch* batch, const void* q, int32_t heads, const int32_t* topk_idx,
+                           const int32_t* topk_cnt, int32_t k, int32_t m, const lcs_rows* entries,
+                           const lcs_paging* paging, const lcs_state* state, float softmax_scale, void* out,
+                           float* out_lse, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                           void* stream) {
+  return csa_attend_part(batch, q, heads, topk_idx, topk_cnt, k, m, entries, paging, state, softmax_scale, out,
+                         out_lse, workspace, workspace_bytes, dev_status, stream, 2);
 }
 
 lcs_status hca_attend(const lcs_batch* batch, const void* q, int32_t heads, int32_t m, const lcs_rows* entries,

@@ -100,14 +100,15 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v, float m) {
 
 }  // namespace
 
-// grid: (total_new, head groups, splits); rows_per_split == 128.
+// grid: (total_new, head groups, splits); splits 0 .. entry_splits-1 take 128-row tiles of the
+// entries, split entry_splits the window rows (part 1: that split alone, part 2: the entry splits).
 __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) {
   using L = TcAttSmem;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int q = blockIdx.x, hg = blockIdx.y, split = blockIdx.z;
+  const int q = blockIdx.x, hg = blockIdx.y;
   const int H = p.heads;
   const int h0 = hg * kHeads;
   // sequence of query q (cu_new non-decreasing)
@@ -125,7 +126,9 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
   const int t = n0 + (q - sp.q0);
   const int32_t* sel = p.topk_idx != nullptr ? p.topk_idx + (long long)q * p.k : nullptr;
   int cnt;
-  if (sel == nullptr) {
+  if (p.part == 1) {
+    cnt = 0;                         // window split alone: the entry list is not needed
+  } else if (sel == nullptr) {
     cnt = (t + 1) / p.m;             // HCA: every visible entry
   } else if (p.topk_cnt != nullptr) {
     cnt = min(p.topk_cnt[q], p.k);
@@ -136,8 +139,10 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
   const int nvis = (t + 1) / p.m;
   const int W = min(t + 1, kWindow);
   const int R = cnt + W;
-  const int r_begin = split * kTileRows;
-  const int r_end = min(R, r_begin + kTileRows);
+  // splits 0 .. entry_splits-1 cover the entries in 128-row tiles, split entry_splits the window
+  const int split = p.part == 1 ? p.entry_splits : blockIdx.z;
+  const int r_begin = split < p.entry_splits ? split * kTileRows : cnt;
+  const int r_end = split < p.entry_splits ? min(cnt, r_begin + kTileRows) : R;
   if (r_begin >= r_end) {
     if (p.splits > 1)
       for (int h = tid; h < kHeads; h += kThreads)
@@ -423,10 +428,11 @@ cudaError_t launch_attend_tc(const AttendParams& p, int total_new, cudaStream_t 
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  dim3 grid(total_new, (p.heads + kHeads - 1) / kHeads, p.splits);
+  const int z = p.part == 1 ? 1 : (p.part == 2 ? p.entry_splits : p.splits);
+  dim3 grid(total_new, (p.heads + kHeads - 1) / kHeads, z);
   attend_tc_kernel<<<grid, kThreads, TcAttSmem::kBytes, st>>>(p);
   cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || p.splits == 1) return e;
+  if (e != cudaSuccess || p.splits == 1 || p.part == 1) return e;
   return launch_attend_combine(p, total_new, kD, st);
 }
 

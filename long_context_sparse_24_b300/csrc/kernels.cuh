@@ -68,6 +68,8 @@ struct AttendParams {
   int splits;
   int rows_per_split;
   int tc;                    // 1: tensor-core kernel (128-row tiles, rows_per_split == 128)
+  int entry_splits;          // tensor-core kernel: splits over the entries; split entry_splits = window
+  int part;                  // tensor-core kernel: 0 every split, 1 the window split only, 2 the entry splits
   int32_t* status;
 };
 

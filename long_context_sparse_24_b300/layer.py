@@ -2,7 +2,7 @@
 
 Owns the caller-side buffers (entry cache, indexer keys, state cache, workspaces) and issues the
 library calls of one step in order:
-  CSA: csa_compress || csa_index_topk -> csa_attend [-> lcs_window_commit]
+  CSA: (csa_compress -> csa_attend_window) || csa_index_topk -> csa_attend_topk [-> lcs_window_commit]
   HCA: hca_compress -> hca_attend [-> lcs_window_commit]
 (lcs_window_commit only for multi-token steps; single-token steps keep the window in the ring.)
 No arithmetic of the method happens here.
@@ -14,7 +14,8 @@ from typing import Optional, Sequence
 
 import torch
 
-from . import (LCS_INDEX_RELU, WINDOW, Batch, Compressor, csa_attend, csa_compress, csa_index_topk, hca_attend,
+from . import (LCS_INDEX_RELU, WINDOW, Batch, Compressor, csa_attend, csa_attend_topk, csa_attend_window,
+               csa_compress, csa_index_topk, hca_attend,
                hca_compress, lcs_attend_workspace, lcs_index_topk_workspace, lcs_window_commit)
 from . import buffers
 
@@ -99,15 +100,22 @@ class Layer:
 
     def step(self, batch: Batch, raw_new: torch.Tensor, q: torch.Tensor, out: torch.Tensor,
              lse: Optional[torch.Tensor] = None, idx_q_fp4=None, idx_q_scale=None, head_w=None, stream=None) -> None:
-        """One pass of the hot path for the batch's new tokens.  CSA: compression (side stream) and
-        the indexer top-k run concurrently; attention waits for both."""
+        """One pass of the hot path for the batch's new tokens.  CSA: compression and then the
+        window part of attention (side stream) run next to the indexer top-k; the top-k part of
+        attention, with the merge, waits for both."""
         main = stream if stream is not None else torch.cuda.current_stream()
         if self.kind == "csa":
             self.side.wait_stream(main)
             self.compress(batch, raw_new, self.side)
+            csa_attend_window(batch, q, self.heads, self.top_k, self.m, self.cache.entries, self.cache.paging,
+                              self.cache.state, self.scale, self.attend_ws, self.attend_ws_bytes, self.status,
+                              self.side)
             self.select(batch, idx_q_fp4, idx_q_scale, head_w, main)
             main.wait_stream(self.side)
+            csa_attend_topk(batch, q, self.heads, self.topk_idx, self.topk_cnt, self.top_k, self.m, self.cache.entries,
+                            self.cache.paging, self.cache.state, self.scale, out, lse, self.attend_ws,
+                            self.attend_ws_bytes, self.status, main)
         else:
             self.compress(batch, raw_new, main)
-        self.attend(batch, q, out, lse, main)
+            self.attend(batch, q, out, lse, main)
         self.commit(batch, main)

@@ -219,7 +219,7 @@ def test_topk_ties_take_lowest_index():
 
 # ---------------------------------------------------------------------------------------- attention
 
-def _attend_case(kind, lengths, new, heads, dim, fmt, m, k, seed=41, scale=None):
+def _attend_case(kind, lengths, new, heads, dim, fmt, m, k, seed=41, scale=None, split=False):
     """Fill an entry cache / window ring / new rows with oracle-quantised rows and run one call."""
     S = len(lengths)
     fmtc = buffers.row_format_code(fmt)
@@ -276,8 +276,26 @@ def _attend_case(kind, lengths, new, heads, dim, fmt, m, k, seed=41, scale=None)
         idx_t = torch.from_numpy(idx).to(DEV)
         cnt_t = torch.tensor([len(s) for s in sels], dtype=torch.int32, device=DEV)
         wsb = lcsa.lcs_attend_workspace(batch, heads, dim, k + 128)
-        lcsa.csa_attend(batch, q, heads, idx_t, cnt_t, k, m, cache.entries, cache.paging, cache.state, scale, out,
-                        lse, workspace(wsb), wsb, st)
+        if split:
+            # window part on a second stream, then the top-k part with the merge
+            ws = workspace(wsb)
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            lcsa.csa_attend_window(batch, q, heads, k, m, cache.entries, cache.paging, cache.state, scale, ws, wsb,
+                                   st, stream=side)
+            torch.cuda.current_stream().wait_stream(side)
+            lcsa.csa_attend_topk(batch, q, heads, idx_t, cnt_t, k, m, cache.entries, cache.paging, cache.state,
+                                 scale, out, lse, ws, wsb, st)
+            one_out = torch.empty_like(out)
+            one_lse = torch.empty_like(lse)
+            lcsa.csa_attend(batch, q, heads, idx_t, cnt_t, k, m, cache.entries, cache.paging, cache.state, scale,
+                            one_out, one_lse, workspace(wsb), wsb, st)
+            torch.cuda.synchronize()
+            assert torch.equal(out.view(torch.int16), one_out.view(torch.int16)), "split != one call (outputs)"
+            assert torch.equal(lse, one_lse), "split != one call (lse)"
+        else:
+            lcsa.csa_attend(batch, q, heads, idx_t, cnt_t, k, m, cache.entries, cache.paging, cache.state, scale, out,
+                            lse, workspace(wsb), wsb, st)
     else:
         wsb = lcsa.lcs_attend_workspace(batch, heads, dim, cap // m + 128)
         lcsa.hca_attend(batch, q, heads, m, cache.entries, cache.paging, cache.state, scale, out, lse,
@@ -313,3 +331,13 @@ def _attend_case(kind, lengths, new, heads, dim, fmt, m, k, seed=41, scale=None)
 ])
 def test_attend_matches_oracle(kind, lengths, new, heads, dim, fmt, m, k):
     _attend_case(kind, lengths, new, heads, dim, fmt, m, k)
+
+
+@pytest.mark.parametrize("lengths,new,heads,dim,fmt,k", [
+    ([2000, 4100, 300], [1, 1, 1], 64, 512, "fp8_split", 512),     # decode: window part computed apart
+    ([900, 2200], [40, 9], 64, 512, "fp8_split", 64),              # multi-token chunk, window from new rows
+    ([130, 7], [1, 7], 16, 512, "fp8_split", 32),                  # short sequences, N(t) < k
+    ([50, 700], [50, 20], 8, 128, "bf16", 64),                     # no separate window part: all in the top-k call
+])
+def test_attend_window_then_topk_equals_one_call(lengths, new, heads, dim, fmt, k):
+    _attend_case("csa", lengths, new, heads, dim, fmt, 4, k, split=True)
