@@ -29,6 +29,11 @@ import synth  # noqa: E402
 
 WL = synth.CONFIGS["csa_decode"]
 METRIC = "CSA/HCA attention queries/s at 128K-1M ctx"
+# DRAM bytes (read + write) per step of the two attention launches and of the indexer (scorer +
+# select), from one ncu capture of this workload (dram__bytes_read.sum + dram__bytes_write.sum) on
+# the current kernels; set to None whenever those kernels change until they are measured again.
+ATTEND_DRAM_BYTES = int(14.503e6 + 0.000256e6 + 4.550e6)
+INDEX_DRAM_BYTES = int(71.510e6 + 1.821e6 + 4.500e6)
 UNIT = "queries/s"
 
 
@@ -201,30 +206,35 @@ def run_gpu(args, rank, world, local):
         raw_in.copy_(raw_steps[s]); q_in.copy_(q_steps[s]); iq_in.copy_(iq_steps[s])
         iqs_in.copy_(iqs_steps[s]); hw_in.copy_(hw_steps[s]); seq_len.fill_(L + s + 1)
 
+    STAGES = ["compress", "attend_window", "index_topk", "attend_topk", "window_commit"]
     try:
-        evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(5)]
-    except TypeError:  # torch without event-record nodes in graphs: stage times from separate graphs
+        evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(STAGES) + 1)]
+    except TypeError:  # torch without event-record nodes in graphs: no stage breakdown
         evs = None
+    from long_context_sparse_24_b300 import csa_attend_topk, csa_attend_window
 
     def step_body(with_events=True):
         if not with_events:
-            # the timed step: compression next to the indexer (side stream), then attention
+            # the timed step: compression and the window part of attention next to the indexer
+            # (side stream), then the top-k part of attention with the merge
             layer.step(batch, raw_in, q_in, out, idx_q_fp4=iq_in, idx_q_scale=iqs_in, head_w=hw_in)
             return
+        # the same calls, serialised on one stream with an event node after each
+        c = layer.cache
+        calls = [lambda: layer.compress(batch, raw_in),
+                 lambda: csa_attend_window(batch, q_in, H, k, m, c.entries, c.paging, c.state, layer.scale,
+                                           layer.attend_ws, layer.attend_ws_bytes, layer.status),
+                 lambda: layer.select(batch, iq_in, iqs_in, hw_in),
+                 lambda: csa_attend_topk(batch, q_in, H, layer.topk_idx, layer.topk_cnt, k, m, c.entries, c.paging,
+                                         c.state, layer.scale, out, None, layer.attend_ws, layer.attend_ws_bytes,
+                                         layer.status),
+                 lambda: layer.commit(batch)]
         if evs:
             evs[0].record()
-        layer.compress(batch, raw_in)
-        if with_events and evs:
-            evs[1].record()
-        layer.select(batch, iq_in, iqs_in, hw_in)
-        if with_events and evs:
-            evs[2].record()
-        layer.attend(batch, q_in, out)
-        if with_events and evs:
-            evs[3].record()
-        layer.commit(batch)
-        if with_events and evs:
-            evs[4].record()
+        for i, fn in enumerate(calls):
+            fn()
+            if evs:
+                evs[i + 1].record()
 
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     # warm-up step 0 runs eagerly (first launches set the kernels' shared-memory attributes);
@@ -260,7 +270,7 @@ def run_gpu(args, rank, world, local):
         graph_ev.replay()
         torch.cuda.synchronize()
         if evs:
-            stage_ms.append([evs[i].elapsed_time(evs[i + 1]) for i in range(4)])
+            stage_ms.append([evs[i].elapsed_time(evs[i + 1]) for i in range(len(STAGES))])
     status_ok = True
     if int(layer.status.item()) != 0:
         status_ok = False
@@ -271,28 +281,45 @@ def run_gpu(args, rank, world, local):
         t = torch.tensor([ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
-    stages = [statistics.mean(x[i] for x in stage_ms) for i in range(4)] if stage_ms else [float("nan")] * 4
+    stages = ([statistics.mean(x[i] for x in stage_ms) for i in range(len(STAGES))] if stage_ms
+              else [float("nan")] * len(STAGES))
+    stage = dict(zip(STAGES, stages))
     splits_used = layer.attend_ws_bytes > 0
     # compress (entries + state) + indexer (score + select) + attention (tensor-core plan: window part,
     # top-k part, merge; otherwise one kernel, plus a merge when split) + window commit
     tc_plan = D == 512 and H <= 64 and k + 128 <= 1024
     attend_launches = 3 if tc_plan else (2 if splits_used else 1)
     launches_per_step = 2 + 2 + attend_launches + (0 if layer.ring_only else 1)
-    # ---- roofline of the dominant call (lightning indexer: score scan + top-k select)
     hbm, peak_kind = measured_peaks()
+    peak_src = f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback"
     n_vis = [(L + s + 1) // m for s in range(timed_end, steps_total)]
+    # ---- roofline of the dominant kernel: attend_tc_kernel (window launch + top-k launch + merge).
+    #      Algorithmic bytes per query: (k + window) rows of 580 B, the query and the output (H x D
+    #      BF16 each); 4*H*D FLOP per row, i.e. about 167 FLOP/B, below the BF16/F16 tensor balance
+    #      point (~270 FLOP/B on this part), so HBM is the roof.
+    att_bytes = S * ((k + 128) * (D - 64 + 128 + 4) + 2 * H * D * 2)
+    att_ms = stage["attend_window"] + stage["attend_topk"]
+    att_achieved = att_bytes / (att_ms * 1e-3) / 1e9
+    roofline = {"kernel": "attend_tc_kernel (csa_attend_window + csa_attend_topk incl. attend_combine_kernel)",
+                "bound": "hbm", "achieved": round(att_achieved, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(att_achieved / hbm, 4), "peak_source": peak_src,
+                "algorithmic_bytes_per_launch": int(att_bytes), "flop_per_step": int(S * 4 * H * D * (k + 128)),
+                "traffic": ATTEND_DRAM_BYTES,
+                "timing": "CUDA events around the two calls in the serialised copy of the step"}
+    # ---- the indexer (score scan + top-k select): 68 B per visible entry per query, plus queries and
+    #      the selection
     key_bytes = r // 2 + r // 32
-    alg_bytes = statistics.mean(S * (n * key_bytes + Hi * key_bytes + Hi * 4 + k * 4 + 4) for n in n_vis)
-    idx_ms = stages[1]
-    achieved = alg_bytes / (idx_ms * 1e-3) / 1e9
-    roofline = {"kernel": "csa_index_topk (index_score_kernel + topk_select_kernel)", "bound": "hbm",
-                "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
-                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
-                "algorithmic_bytes_per_launch": int(alg_bytes), "traffic": None}
+    idx_bytes = statistics.mean(S * (n * key_bytes + Hi * key_bytes + Hi * 4 + k * 4 + 4) for n in n_vis)
+    idx_achieved = idx_bytes / (stage["index_topk"] * 1e-3) / 1e9
+    roofline_index = {"kernel": "csa_index_topk (index_tc_kernel + topk_select_kernel)", "bound": "hbm",
+                      "achieved": round(idx_achieved, 1), "peak": hbm, "unit": "GB/s",
+                      "frac": round(idx_achieved / hbm, 4), "peak_source": peak_src,
+                      "algorithmic_bytes_per_launch": int(idx_bytes), "traffic": INDEX_DRAM_BYTES}
     # ---- end to end through the public API with host buffers (pinned), copies in the timed region
     e2e = run_e2e(torch, layer, batch, graph, raw_in, q_in, iq_in, iqs_in, hw_in, out, seq_len, raw_steps,
                   q_steps, iq_steps, iqs_steps, hw_steps, args, L, S, flush)
-    return {"ms": ms, "stages": stages, "clocks": clk.summary(), "roofline": roofline, "e2e": e2e,
+    return {"ms": ms, "stages": stage, "clocks": clk.summary(), "roofline": roofline,
+            "roofline_index": roofline_index, "e2e": e2e,
             "launches": launches_per_step * args.steps, "status_ok": status_ok,
             "per_rank_queries": S}
 
@@ -448,11 +475,10 @@ def main():
                 "scaling": "weak", "vs_baseline": None, "dtype": "fp8/fp4 storage, bf16/f16 MMA, fp32 accumulate",
                 "data": "synthetic",
                 "config": workload_config({"parallelism": f"replicas x{world} (independent sequences per GPU)",
-                                           "stage_ms_source": "separate replays of a serialised copy of the step with event nodes between calls (the timed step overlaps compress with index_topk)",
-                                           "stage_ms": {k: round(v, 5) for k, v in zip(
-                                               ["compress", "index_topk", "attend", "window_commit"],
-                                               res["stages"])}}),
-                "roofline": res["roofline"], "clocks": res["clocks"], "e2e": res["e2e"],
+                                           "stage_ms_source": "separate replays of a serialised copy of the step with event nodes between calls (the timed step runs compress and attend_window next to index_topk)",
+                                           "stage_ms": {k_: round(v, 5) for k_, v in res["stages"].items()}}),
+                "roofline": res["roofline"], "roofline_index": res["roofline_index"], "clocks": res["clocks"],
+                "e2e": res["e2e"],
                 "gpu_launches": res["launches"], "device_status_ok": res["status_ok"]}
         if not args.no_cpu_baseline and world == 1:
             line["cpu_baseline"] = cpu_baseline()
