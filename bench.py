@@ -44,6 +44,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="csa_decode", choices=["csa_decode", "hca_decode", "mixed_decode"],
+                    help="csa_decode is the headline line; the others measure the HCA decode and the mixed "
+                         "ragged multi-layer workloads with the same timing rules")
     return ap.parse_args()
 
 
@@ -287,7 +290,7 @@ def run_gpu(args, rank, world, local):
     splits_used = layer.attend_ws_bytes > 0
     # compress (entries + state) + indexer (score + select) + attention (tensor-core plan: window part,
     # top-k part, merge; otherwise one kernel, plus a merge when split) + window commit
-    tc_plan = D == 512 and H <= 64 and k + 128 <= 1024
+    tc_plan = D == 512 and H <= 64 and k <= 2048
     attend_launches = 3 if tc_plan else (2 if splits_used else 1)
     launches_per_step = 2 + 2 + attend_launches + (0 if layer.ring_only else 1)
     hbm, peak_kind = measured_peaks()
@@ -322,6 +325,160 @@ def run_gpu(args, rank, world, local):
             "roofline_index": roofline_index, "e2e": e2e,
             "launches": launches_per_step * args.steps, "status_ok": status_ok,
             "per_rank_queries": S}
+
+
+# ---------------------------------------------------------------------------------------------
+# GPU arm, other workloads: HCA decode (one HCA layer) and the mixed ragged stack (CSA/HCA x 4)
+# ---------------------------------------------------------------------------------------------
+
+def run_gpu_stack(args, rank, world, local, wl):
+    import torch
+    import synth.gpu as sg
+    import long_context_sparse_24_b300 as lcsa
+    from long_context_sparse_24_b300.model import HybridStack
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if lcsa.lcs_device_check() != 0:
+        raise SystemExit("liblcsa needs a compute-capability 10.3 GPU")
+    S, H, D = wl.num_seqs, wl.heads, wl.dim
+    Hi, r, k = wl.index_heads, wl.index_rank, wl.top_k
+    seed = wl.seed + 1000 * rank
+    if wl.kind == "mixed":
+        lengths = [int(x) for x in synth.mixed_lengths(seed, S)]
+        n_layers, first = wl.layers, "csa"
+    else:
+        lengths = [wl.ctx_len] * S
+        n_layers, first = 1, "hca"
+    steps_total = args.warmup + args.steps
+    cap = max(lengths) + 128 * math.ceil((steps_total + 1) / 128) + 256
+    stack = HybridStack(n_layers, S, cap, H, D, lcsa.LCS_ROW_FP8_SPLIT, csa_m=4, hca_m=128, top_k=k,
+                        index_heads=Hi, index_rank=r, max_new=1, first=first, device=dev)
+    # ---- per layer: compressor parameters, the cached context (ragged), indexer keys
+    chunk = 16384 if S <= 32 else 8192
+    raw_chunk = torch.empty((S * chunk, D), dtype=torch.bfloat16, device=dev)
+    for li, layer in enumerate(stack.layers):
+        m = layer.m
+        nb = 2 * m if layer.overlap else m
+        w = synth.bf16_bits_to_f32(synth.normal_bf16(seed, synth.tensor_id(synth.COMP_W, li), 0, D)) / 16
+        bias = synth.bf16_bits_to_f32(synth.normal_bf16(seed, synth.tensor_id(synth.COMP_B, li), 0, nb)) / 2
+        layer.set_compressor(torch.from_numpy(w.astype(np.float32)).to(dev),
+                             torch.from_numpy(bias.astype(np.float32)).to(dev))
+        for c0 in range(0, max(lengths), chunk):
+            ns = [max(0, min(chunk, L - c0)) for L in lengths]
+            off = 0
+            for b, n in enumerate(ns):
+                if n:
+                    sg.normal_bf16(raw_chunk[off:off + n], seed, synth.tensor_id(synth.RAW, li, b), c0 * D)
+                    off += n
+            layer.fill(layer.batch([min(L, c0 + n) if n else L for L, n in zip(lengths, ns)], ns), raw_chunk[:off])
+        if layer.kind == "csa":
+            bps = layer.cache.paging.max_blocks_per_seq
+            n_ent = cap // m
+            for b in range(S):
+                r0 = b * bps * (128 // m)
+                sg.e2m1_packed(layer.cache.keys.fp4[r0:r0 + n_ent], seed, synth.tensor_id(synth.IDX_K, li, b), 0)
+                sg.ue8m0(layer.cache.keys.scale[r0:r0 + n_ent], seed, synth.tensor_id(synth.IDX_KS, li, b), 0)
+    del raw_chunk
+    # ---- per-step inputs of every layer (decode token L_b + s of every sequence)
+    def gen(shape, dtype, fn, tid_kind, li, per_tok):
+        t = torch.empty((steps_total, S) + shape, dtype=dtype, device=dev)
+        for st in range(steps_total):
+            for b in range(S):
+                fn(t[st, b], seed, synth.tensor_id(tid_kind, li, b), (lengths[b] + st) * per_tok)
+        return t
+    raw_s, q_s, iq_s, iqs_s = [], [], [], []
+    for li, layer in enumerate(stack.layers):
+        raw_s.append(gen((D,), torch.bfloat16, sg.normal_bf16, synth.RAW, li, D))
+        q_s.append(gen((H, D), torch.bfloat16, sg.normal_bf16, synth.QUERY, li, H * D))
+        if layer.kind == "csa":
+            iq_s.append(gen((Hi, r // 2), torch.uint8, sg.e2m1_packed, synth.IDX_Q, li, Hi * r))
+            iqs_s.append(gen((Hi, r // 32), torch.uint8, sg.ue8m0, synth.IDX_QS, li, Hi * r // 32))
+        else:
+            iq_s.append(None)
+            iqs_s.append(None)
+    raw_in = [torch.empty((S, D), dtype=torch.bfloat16, device=dev) for _ in stack.layers]
+    q_in = [torch.empty((S, H, D), dtype=torch.bfloat16, device=dev) for _ in stack.layers]
+    iq_in = [torch.empty((S, Hi, r // 2), dtype=torch.uint8, device=dev) if x is not None else None for x in iq_s]
+    iqs_in = [torch.empty((S, Hi, r // 32), dtype=torch.uint8, device=dev) if x is not None else None for x in iqs_s]
+    hw_in = [torch.ones((S, Hi), dtype=torch.float32, device=dev) if x is not None else None for x in iq_s]
+    outs = [torch.empty((S, H, D), dtype=torch.bfloat16, device=dev) for _ in stack.layers]
+    cu_new = torch.arange(S + 1, dtype=torch.int32, device=dev)
+    seq_len = torch.tensor([L + 1 for L in lengths], dtype=torch.int32, device=dev)
+    batch = stack.layers[0].batch([cap] * S, [1] * S, cu_new=cu_new, seq_len=seq_len)
+    base_len = torch.tensor(lengths, dtype=torch.int32, device=dev)
+
+    def load_step(st):
+        for li in range(n_layers):
+            raw_in[li].copy_(raw_s[li][st]); q_in[li].copy_(q_s[li][st])
+            if iq_in[li] is not None:
+                iq_in[li].copy_(iq_s[li][st]); iqs_in[li].copy_(iqs_s[li][st])
+        torch.add(base_len, st + 1, out=seq_len)
+
+    def step_body():
+        stack.step(batch, raw_in, q_in, outs, iq_in, iqs_in, hw_in)
+
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    load_step(0)
+    step_body()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step_body()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps_total)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps_total)]
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for st in range(1, steps_total):
+            load_step(st)
+            flush.zero_()
+            starts[st].record()
+            graph.replay()
+            ends[st].record()
+        torch.cuda.synchronize()
+    status_ok = all(v == 0 for v in stack.status)
+    ms = statistics.mean(starts[st].elapsed_time(ends[st]) for st in range(args.warmup, steps_total))
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    # ---- whole-step algorithmic bytes (every layer is HBM-bound): CSA: 68 B per visible entry
+    #      (indexer) + (k + 128) rows of 580 B; HCA: (visible entries + 128) rows of 580 B; both:
+    #      query and output H x D BF16 per sequence
+    row_b, key_b, qo_b = D - 64 + 128 + 4, r // 2 + r // 32, 2 * H * D * 2
+    t_mid = args.warmup + args.steps // 2
+    alg = 0
+    for layer in stack.layers:
+        for L in lengths:
+            t = L + t_mid
+            n = (t + 1) // layer.m
+            if layer.kind == "csa":
+                alg += n * key_b + (min(k, n) + min(t + 1, 128)) * row_b + qo_b
+            else:
+                alg += (n + min(t + 1, 128)) * row_b + qo_b
+    hbm, peak_kind = measured_peaks()
+    achieved = alg / (ms * 1e-3) / 1e9
+    roofline = {"kernel": "whole step (every kernel of every layer)", "bound": "hbm", "achieved": round(achieved, 1),
+                "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
+                "algorithmic_bytes_per_launch": int(alg), "traffic": None}
+    n_csa = sum(1 for kd in stack.kinds if kd == "csa")
+    n_hca = n_layers - n_csa
+    hca_rows = max(lengths) // 128 + 128
+    hca_launch = 3 if hca_rows <= 2048 + 128 else 2
+    launches = n_csa * (2 + 2 + 3) + n_hca * (2 + hca_launch)
+    cfg = {"workload": wl.name, "num_seqs": S, "layers": n_layers, "layer_kinds": stack.kinds,
+           "ctx_len": lengths if wl.kind == "mixed" else wl.ctx_len, "new_tokens_per_seq": 1, "heads": H,
+           "kv_dim": D, "row_format": "fp8_e4m3(448)+bf16_rope(64)+f32_scale", "csa_m": 4, "hca_m": 128,
+           "top_k": k, "index_heads": Hi, "index_rank": r, "window": 128, "seed": wl.seed,
+           "l2": "flushed between timed steps (256 MB write)", "data": "synthetic",
+           "parallelism": f"replicas x{world} (independent sequences per GPU)"}
+    return {"ms": ms, "clocks": clk.summary(), "roofline": roofline, "launches": launches * args.steps,
+            "status_ok": status_ok, "per_rank_queries": S, "config": cfg}
 
 
 def run_e2e(torch, layer, batch, graph, raw_in, q_in, iq_in, iqs_in, hw_in, out, seq_len, raw_steps, q_steps,
@@ -466,6 +623,17 @@ def main():
             print(json.dumps(line))
         return
     assert args.warmup >= 3, "at least 3 warm-up steps"
+    if args.workload != "csa_decode":
+        res = run_gpu_stack(args, rank, world, local, synth.CONFIGS[args.workload])
+        if rank == 0:
+            value = res["per_rank_queries"] * world / (res["ms"] * 1e-3)
+            print(json.dumps({"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+                              "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(res["ms"], 5),
+                              "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                              "dtype": "fp8/fp4 storage, f16/bf16 MMA, fp32 accumulate", "data": "synthetic",
+                              "config": res["config"], "roofline": res["roofline"], "clocks": res["clocks"],
+                              "e2e": None, "gpu_launches": res["launches"], "device_status_ok": res["status_ok"]}))
+        return
     res = run_gpu(args, rank, world, local)
     if rank == 0:
         S_all = res["per_rank_queries"] * world

@@ -1,6 +1,6 @@
 // Shared-KV multi-query attention on the tcgen05 tensor cores: one 128-row tile of one query's
-// row list per CTA, for FP8-split rows of D = 512, up to 64 query heads and up to 1024 rows per
-// query (CSA decode and short HCA contexts).
+// row list per CTA, for FP8-split rows of D = 512, up to 64 query heads and up to 2048 entries
+// plus the window per query (CSA decode with top-k up to 2048, short HCA contexts).
 //
 // Defined by: m.x-techcon.com/article/133366, section 2, CSA step 3 (the selected compressed
 // entries and the most recent 128 uncompressed tokens are attended together, shared-KV

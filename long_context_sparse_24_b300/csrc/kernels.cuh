@@ -88,6 +88,6 @@ cudaError_t launch_attend(const AttendParams& p, int D, int fmt, int total_new, 
 cudaError_t launch_attend_tc(const AttendParams& p, int total_new, cudaStream_t st);
 cudaError_t launch_attend_combine(const AttendParams& p, int total_new, int D, cudaStream_t st);
 // rows of one query the tensor-core attention takes at most (per 64-head group)
-constexpr int kAttendTcMaxRows = 1024;
+constexpr int kAttendTcMaxRows = 2048 + 128;
 
 }  // namespace lcsa

@@ -129,3 +129,84 @@ def test_csa_tiny_prefill_then_decode(fmt):
         assert np.array_equal(lay.topk_idx[0, :len(sel)].cpu().numpy(), sel), t
         check_outputs(out1.float().cpu().numpy()[0].astype(np.float64), ref["o"][t], f"decode step {s}")
     assert int(lay.status.item()) == 0
+
+
+def test_hybrid_stack_ragged_decode_matches_oracle():
+    """A CSA layer and an HCA layer on one shared, permuted block table (blocks of 128 raw
+    tokens), ragged sequences, two decode steps through HybridStack; every sequence's output of
+    every layer against the oracle, top-k sets bit-exact."""
+    from long_context_sparse_24_b300 import buffers
+    from long_context_sparse_24_b300.model import HybridStack
+    seed, D, H, k, hi, r = 23, 512, 64, 64, 4, 128
+    lengths = [900, 2600, 259]
+    S, steps = len(lengths), 2
+    cap = max(lengths) + steps + 128
+    order = np.random.default_rng(seed).permutation(S * math.ceil(cap / 128)).tolist()
+    stack = HybridStack(2, S, cap, H, D, lcsa.LCS_ROW_FP8_SPLIT, top_k=k, index_heads=hi, index_rank=r,
+                        block_order=order, device=DEV)
+    assert stack.kinds == ["csa", "hca"]
+    params = []
+    for li, lay in enumerate(stack.layers):
+        w, b = _comp_params(seed, li, D, lay.m, lay.overlap)
+        lay.set_compressor(torch.from_numpy(w).to(DEV), torch.from_numpy(b).to(DEV))
+        params.append((w.astype(np.float64), b.astype(np.float64)))
+        raws = []
+        for s_, L in enumerate(lengths):
+            t = torch.empty((L, D), dtype=torch.bfloat16, device=DEV)
+            sg.normal_bf16(t, seed, synth.tensor_id(synth.RAW, li, s_), 0)
+            raws.append(t)
+        lay.fill(lay.batch(lengths, lengths), torch.cat(raws).contiguous())
+    # indexer keys of the CSA layer through the shared block table
+    csa = stack.layers[0]
+    table = csa.cache.paging.block_table.cpu().numpy()
+    keys = []
+    for s_, L in enumerate(lengths):
+        ne = (L + steps) // 4
+        kc, ks = _keys_np(seed, 0, s_, ne, r)
+        rows = table[s_, np.arange(ne) // 32].astype(np.int64) * 32 + np.arange(ne) % 32
+        ridx = torch.as_tensor(rows, device=DEV)
+        csa.cache.keys.fp4[ridx] = _dev_u8(synth.pack_e2m1(kc))
+        csa.cache.keys.scale[ridx] = _dev_u8(ks)
+        keys.append((kc, ks))
+    for st in range(steps):
+        pos = [L + st for L in lengths]
+        raw_new, q_in, outs, iq, iqs, ihw, qref = [], [], [], [], [], [], []
+        for li, lay in enumerate(stack.layers):
+            rn = torch.empty((S, D), dtype=torch.bfloat16, device=DEV)
+            for s_ in range(S):
+                sg.normal_bf16(rn[s_], seed, synth.tensor_id(synth.RAW, li, s_), pos[s_] * D)
+            raw_new.append(rn)
+            qs_, qcs, qss, hws = [], [], [], []
+            for s_ in range(S):
+                q, qc, qsc, hw = _query_inputs(seed, li, s_, pos[s_], 1, H, D, hi, r)
+                qs_.append(q); qcs.append(qc); qss.append(qsc); hws.append(hw)
+            qb = np.concatenate(qs_)
+            qref.append((qb, qcs, qss, hws))
+            q_in.append(to_dev_bf16_bits(qb))
+            outs.append(torch.empty((S, H, D), dtype=torch.bfloat16, device=DEV))
+            if lay.kind == "csa":
+                iq.append(_dev_u8(synth.pack_e2m1(np.concatenate(qcs))))
+                iqs.append(_dev_u8(np.concatenate(qss)))
+                ihw.append(torch.from_numpy(np.concatenate(hws)).to(DEV))
+            else:
+                iq.append(None); iqs.append(None); ihw.append(None)
+        batch = stack.batch([p + 1 for p in pos], [1] * S)
+        stack.step(batch, raw_new, q_in, outs, iq, iqs, ihw)
+        torch.cuda.synchronize()
+        assert stack.status == [0, 0]
+        for li, lay in enumerate(stack.layers):
+            o = outs[li].float().cpu().numpy().astype(np.float64)
+            w, b = params[li]
+            qb, qcs, qss, hws = qref[li]
+            for s_ in range(S):
+                raw = _raw_f64(seed, li, s_, 0, pos[s_] + 1, D)
+                qf = bits_to_f64(qb[s_:s_ + 1])
+                if lay.kind == "csa":
+                    kc, ks = keys[s_]
+                    ref = oracle.csa_layer(raw, w, b, 4, True, "fp8_split", qf, [pos[s_]], qcs[s_], qss[s_], hws[s_],
+                                           kc, ks, k, 1 / math.sqrt(D))
+                    n_sel = len(ref["topk"][0])
+                    assert np.array_equal(lay.topk_idx[s_, :n_sel].cpu().numpy(), ref["topk"][0]), (st, s_)
+                else:
+                    ref = oracle.hca_layer(raw, w, b, 128, "fp8_split", qf, [pos[s_]], 1 / math.sqrt(D))
+                check_outputs(o[s_], ref["o"][0], f"step {st} layer {li} seq {s_}")
