@@ -296,14 +296,14 @@ def run_gpu(args, rank, world, local):
     hbm, peak_kind = measured_peaks()
     peak_src = f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback"
     n_vis = [(L + s + 1) // m for s in range(timed_end, steps_total)]
-    # ---- roofline of the dominant kernel: attend_tc_kernel (window launch + top-k launch + merge).
+    # ---- roofline of the dominant kernel: attend_tc1_kernel (window launch + top-k launch + merge).
     #      Algorithmic bytes per query: (k + window) rows of 580 B, the query and the output (H x D
     #      BF16 each); 4*H*D FLOP per row, i.e. about 167 FLOP/B, below the BF16/F16 tensor balance
     #      point (~270 FLOP/B on this part), so HBM is the roof.
     att_bytes = S * ((k + 128) * (D - 64 + 128 + 4) + 2 * H * D * 2)
     att_ms = stage["attend_window"] + stage["attend_topk"]
     att_achieved = att_bytes / (att_ms * 1e-3) / 1e9
-    roofline = {"kernel": "attend_tc_kernel (csa_attend_window + csa_attend_topk incl. attend_combine_kernel)",
+    roofline = {"kernel": "attend_tc1_kernel (csa_attend_window + csa_attend_topk incl. attend_combine_kernel)",
                 "bound": "hbm", "achieved": round(att_achieved, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(att_achieved / hbm, 4), "peak_source": peak_src,
                 "algorithmic_bytes_per_launch": int(att_bytes), "flop_per_step": int(S * 4 * H * D * (k + 128)),
@@ -468,9 +468,9 @@ def run_gpu_stack(args, rank, world, local, wl):
                 "algorithmic_bytes_per_launch": int(alg), "traffic": None}
     n_csa = sum(1 for kd in stack.kinds if kd == "csa")
     n_hca = n_layers - n_csa
-    hca_rows = max(lengths) // 128 + 128
-    hca_launch = 3 if hca_rows <= 2048 + 128 else 2
-    launches = n_csa * (2 + 2 + 3) + n_hca * (2 + hca_launch)
+    # CSA layer: compress (2) + indexer (2) + attention window part, top-k part, merge (3);
+    # HCA layer: compress (2) + attention + merge (2)
+    launches = n_csa * (2 + 2 + 3) + n_hca * (2 + 2)
     cfg = {"workload": wl.name, "num_seqs": S, "layers": n_layers, "layer_kinds": stack.kinds,
            "ctx_len": lengths if wl.kind == "mixed" else wl.ctx_len, "new_tokens_per_seq": 1, "heads": H,
            "kv_dim": D, "row_format": "fp8_e4m3(448)+bf16_rope(64)+f32_scale", "csa_m": 4, "hca_m": 128,

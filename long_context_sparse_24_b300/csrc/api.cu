@@ -63,16 +63,29 @@ struct SplitPlan {
   int entry_splits;   // tensor-core plan: 128-row tiles of entries; one more split for the window
 };
 
-// The tensor-core attention takes FP8-split rows of D = 512 (the only D = 512 format), up to 64
-// heads and up to kAttendTcMaxRows rows per query, one 128-row tile per CTA.
-bool attend_tc_applies(int heads, int dim, int max_rows) {
-  return dim == 512 && heads <= 64 && max_rows <= kAttendTcMaxRows;
+// The tensor-core attention takes FP8-split rows of D = 512 (the only D = 512 format) and up to
+// 64 heads.  CSA (window apart, window_split): top-k lists up to 2048 entries, one split per
+// 128-row tile of entries while a wave has room, plus the window split.  HCA (one list): any
+// length, the list cut into about one wave of CTAs.
+bool attend_tc_applies(int heads, int dim, int max_rows, bool window_split) {
+  return dim == 512 && heads <= 64 && (!window_split || max_rows <= kAttendTcMaxRows);
 }
 
-SplitPlan plan_splits(const lcs_batch* b, int heads, int dim, int max_rows) {
-  if (attend_tc_applies(heads, dim, max_rows)) {
-    const int es = std::max(1, (max_rows - LCSA_WINDOW + 127) / 128);
-    return SplitPlan{es + 1, 128, 1, es};
+SplitPlan plan_splits(const lcs_batch* b, int heads, int dim, int max_rows, bool window_split) {
+  if (attend_tc_applies(heads, dim, max_rows, window_split)) {
+    const long long ctas = std::max<long long>(1, (long long)b->total_new * ((heads + 63) / 64));
+    const int per_query = (int)std::max<long long>(1, num_sms() / ctas);   // CTAs per (query, head group)
+    if (window_split) {
+      const int tiles = std::max(1, (max_rows - LCSA_WINDOW + 127) / 128);
+      const int es = std::min(tiles, per_query);
+      const int tps = (tiles + es - 1) / es;
+      return SplitPlan{(tiles + tps - 1) / tps + 1, 128 * tps, 1, (tiles + tps - 1) / tps};
+    }
+    const int tiles = std::max(1, (max_rows + 127) / 128);
+    const int sp = std::min(tiles, per_query);
+    const int tps = (tiles + sp - 1) / sp;
+    const int splits = (tiles + tps - 1) / tps;
+    return SplitPlan{splits, 128 * tps, 1, splits};
   }
   const int hg = heads <= 16 ? 1 : (heads + 63) / 64;
   const long long base = (long long)b->total_new * hg;
@@ -189,7 +202,8 @@ lcs_status index_common(const lcs_batch* batch, const uint8_t* q_fp4, const uint
 
 lcs_status attend_common(const lcs_batch* batch, const void* q, int32_t heads, const lcs_rows* entries,
                          const lcs_paging* paging, const lcs_state* state, void* out, void* workspace,
-                         size_t workspace_bytes, int max_rows, AttendParams& p, bool no_out = false) {
+                         size_t workspace_bytes, int max_rows, AttendParams& p, bool window_split,
+                         bool no_out = false) {
   lcs_status s = check_batch(batch);
   if (s != LCS_OK) return s;
   if (q == nullptr || (out == nullptr && !no_out) || state == nullptr) return LCS_ERR_INVALID_ARG;
@@ -212,7 +226,7 @@ lcs_status attend_common(const lcs_batch* batch, const void* q, int32_t heads, c
   }
   if (entries->num_rows < 1) return LCS_ERR_SHAPE;
   if (entries->format == LCS_ROW_BF16 && entries->dim == 512) return LCS_ERR_UNSUPPORTED;
-  const SplitPlan plan = plan_splits(batch, heads, entries->dim, max_rows);
+  const SplitPlan plan = plan_splits(batch, heads, entries->dim, max_rows, window_split);
   const size_t need = attend_ws_bytes(batch, heads, entries->dim, plan);
   if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return LCS_ERR_WORKSPACE;
   if (need > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return LCS_ERR_ALIGNMENT;
@@ -235,6 +249,7 @@ lcs_status attend_common(const lcs_batch* batch, const void* q, int32_t heads, c
   p.rows_per_split = plan.rows_per_split;
   p.tc = plan.tc;
   p.entry_splits = plan.entry_splits;
+  p.window_split = plan.tc && window_split ? 1 : 0;
   if (plan.splits > 1) {
     const size_t per = (size_t)batch->total_new * heads * plan.splits;
     const size_t ob = per * entries->dim * (plan.tc ? 2 : 4);
@@ -254,7 +269,7 @@ lcs_status csa_attend_part(const lcs_batch* batch, const void* q, int32_t heads,
   if (k < 1 || k > 4096 || m <= 0 || m > 128) return LCS_ERR_UNSUPPORTED;
   AttendParams p;
   lcs_status s = attend_common(batch, q, heads, entries, paging, state, part == 1 ? nullptr : out, workspace,
-                               workspace_bytes, k + LCSA_WINDOW, p, part == 1);
+                               workspace_bytes, k + LCSA_WINDOW, p, true, part == 1);
   if (s != LCS_OK) return s;
   if (part != 0 && !p.tc) {
     // only the tensor-core plan computes the window split apart: here the window call does
@@ -389,7 +404,9 @@ lcs_status csa_index_scores(const lcs_batch* batch, const uint8_t* q_fp4, const 
 
 size_t lcs_attend_workspace(const lcs_batch* batch, int32_t heads, int32_t dim, int32_t max_rows) {
   if (batch == nullptr) return 0;
-  return attend_ws_bytes(batch, heads, dim, plan_splits(batch, heads, dim, max_rows));
+  // the same size serves a CSA call (window apart) and an HCA call (one list)
+  return std::max(attend_ws_bytes(batch, heads, dim, plan_splits(batch, heads, dim, max_rows, true)),
+                  attend_ws_bytes(batch, heads, dim, plan_splits(batch, heads, dim, max_rows, false)));
 }
 
 lcs_status csa_attend(const lcs_batch* batch, const void* q, int32_t heads, const int32_t* topk_idx,
@@ -423,7 +440,7 @@ lcs_status hca_attend(const lcs_batch* batch, const void* q, int32_t heads, int3
   if (m <= 0 || m > 128) return LCS_ERR_UNSUPPORTED;
   AttendParams p;
   lcs_status s = attend_common(batch, q, heads, entries, paging, state, out, workspace, workspace_bytes,
-                               batch ? batch->max_seq_len / m + LCSA_WINDOW : 0, p);
+                               batch ? batch->max_seq_len / m + LCSA_WINDOW : 0, p, false);
   if (s != LCS_OK) return s;
   p.m = m;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;

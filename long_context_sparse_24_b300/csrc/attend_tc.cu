@@ -1,32 +1,35 @@
-// Shared-KV multi-query attention on the tcgen05 tensor cores: one 128-row tile of one query's
-// row list per CTA, for FP8-split rows of D = 512, up to 64 query heads and up to 2048 entries
-// plus the window per query (CSA decode with top-k up to 2048, short HCA contexts).
+// Shared-KV multi-query attention on the tcgen05 tensor cores for FP8-split rows of D = 512 and
+// up to 64 query heads: a CTA takes one query, one 64-head group and a run of 128-row tiles of its
+// row list (CSA: top-k entries, then the window; HCA: every visible entry, then the window).
+// Plans with one tile per CTA go to the single-tile kernel in attend_tc1.cu.
 //
 // Defined by: m.x-techcon.com/article/133366, section 2, CSA step 3 (the selected compressed
 // entries and the most recent 128 uncompressed tokens are attended together, shared-KV
-// multi-query attention); the efficiency paragraph fixes the row storage (RoPE dims BF16, the
-// rest FP8).  Same result as the warp-MMA kernel in attend.cu: one softmax per head over the
-// rows, o = sum p * row, with the row as key and value.
+// multi-query attention) and the HCA paragraph (dense attention over every entry plus the same
+// window); the efficiency paragraph fixes the row storage (RoPE dims BF16, the rest FP8).  Same
+// result as the warp-MMA kernel in attend.cu: one softmax per head over the rows, o = sum p * row,
+// with the row as key and value.
 //
-// Work of a CTA (query q, 64-head group, tile of rows).  Everything runs in F16 on the rows
-// rescaled by their own FP8 scale s_r: R'_r = [rope_r / s_r | codes_r] (the E4M3 codes are exact
-// in F16), so that q . row_r = s_r * (q . R'_r) and sum_r p_r row_r = sum_r (p_r s_r) R'_r.
-//   gather   row descriptors (top-k entries, window rows); every thread then loads the row
-//            scales, its 8-byte pieces of FP8 codes and 16-byte pieces of RoPE dims straight into
-//            registers and writes them widened to F16 into the tile: eight K-major chunks of
-//            [128 rows][64 dims] (chunk 0 the RoPE dims times 1/s_r); the query arrives by
-//            cp.async into eight K-major chunks of [64 heads][64 dims] and becomes F16 in place;
-//   S'^T     = R' . Q^T: 32 MMAs (M = 128 rows, N = 64 heads, K = 16), issued back to back;
-//   softmax  S'^T is read from tensor memory, scaled by s_r (logit = s_r * S'), transposed
-//            through shared memory (over the query buffer); four threads per head take the max
-//            and the exponentials (base 2, fp32) over the tile's rows; P' = p * s_r * 2^8 (F16)
+// Everything runs in F16 on the rows rescaled by their own FP8 scale s_r:
+// R'_r = [rope_r / s_r | codes_r] (the E4M3 codes are exact in F16), so that
+// q . row_r = s_r * (q . R'_r) and sum_r p_r row_r = sum_r (p_r s_r) R'_r.  Per tile:
+//   gather   row descriptors (warps 4-7, two tiles ahead) and the rows' scales, FP8 codes and
+//            RoPE dims loaded into registers one tile ahead (issued right after the current tile
+//            is widened, they fly while it computes), then widened to F16 into eight K-major
+//            chunks of [128 rows][64 dims]; the
+//            query arrives once by cp.async into eight K-major chunks and becomes F16 in place;
+//   S'^T     = R' . Q^T: 32 MMAs (M = 128 rows, N = 64 heads, K = 16);
+//   softmax  warps 0-3 read S'^T from tensor memory (lane = row), logit = s_r * S'; per-head max
+//            and sum over the tile's rows by warp-shuffle reduce-scatters (each lane ends with
+//            two heads) and a four-warp combine; exact online softmax: when a head's running max
+//            grows, warps 4-7 rescale its O^T columns in tensor memory; P' = p * s_r * 2^8 (F16)
 //            is written as the K-major [64 heads x 128 rows] operand;
-//   O^T      = R'^T . P'^T: 32 MMAs, M = 128 dims per block (the same tile chunks read as an
+//   O^T     += R'^T . P'^T: 32 MMAs, M = 128 dims per block (the same tile chunks read as an
 //            MN-major operand: two 64-dim chunks 16 KB apart, 8-row groups 1024 B apart), N = 64
-//            heads, K = 16 rows;
-//   epilogue O^T is read from tensor memory (lane = dim, column = head), transposed per warp
-//            through shared memory and written in 16-byte pieces, normalised by 2^8 * sum p (one
-//            split) or as a BF16 partial with its (max, sum) for the combine kernel.
+//            heads, K = 16 rows.
+// Epilogue: O^T read from tensor memory (lane = dim, column = head), transposed per warp through
+// shared memory, written in 16-byte pieces normalised by 2^8 * sum p (one split) or as a BF16
+// partial with its (max, sum) for the combine kernel.
 // Operand chunks use the 128-byte swizzle (16-byte piece j of row r at position j ^ (r % 8)).
 // Range: query values within F16 range and row scales below 256 (|x| < 114688), as for the
 // warp-MMA kernel.
@@ -46,23 +49,47 @@ constexpr int kQChunk = 8192;             // [64 heads][64 dims] BF16
 constexpr int kThreads = 256;
 
 struct TcAttSmem {
-  static constexpr int kQ = 0;                              // 8 x 8 KB; later the transposes
+  static constexpr int kQ = 0;                              // 8 x 8 KB; the epilogue transposes after the last tile
   static constexpr int kT = kQ + 8 * kQChunk;               // 8 x 16 KB row tile (chunk 0: RoPE)
   static constexpr int kP = kT + 8 * kChunk;                // 2 x 8 KB ([64 heads][64 rows])
-  static constexpr int kScale = kP + 2 * kQChunk;           // f32 [128]
-  static constexpr int kRinv = kScale + kTileRows * 4;      // f32 [128]  1 / s_r
-  static constexpr int kDesc = kRinv + kTileRows * 4;       // long long [128]
-  static constexpr int kM = kDesc + kTileRows * 8;          // f32 [64]
-  static constexpr int kL = kM + kHeads * 4;                // f32 [64]
-  static constexpr int kInv = kL + kHeads * 4;              // f32 [64] output factor per head
+  static constexpr int kScale = kP + 2 * kQChunk;           // f32 [2][128]   (tile parity)
+  static constexpr int kRinv = kScale + 2 * kTileRows * 4;  // f32 [2][128]   1 / s_r
+  static constexpr int kDesc = kRinv + 2 * kTileRows * 4;   // long long [3][128] (tiles t, t+1, t+2)
+  static constexpr int kRed = kDesc + 3 * kTileRows * 8;    // f32 [4 warps][64] per-head partials
+  static constexpr int kM = kRed + 4 * kHeads * 4;          // f32 [64] running max (base 2)
+  static constexpr int kL = kM + kHeads * 4;                // f32 [64] running sum
+  static constexpr int kMn = kL + kHeads * 4;               // f32 [64] the tile's new max
+  static constexpr int kAlpha = kMn + kHeads * 4;           // f32 [64] rescale factor of O and l
+  static constexpr int kInv = kAlpha + kHeads * 4;          // f32 [64] output factor per head
   static constexpr int kBar = kInv + kHeads * 4;            // u64 s, pv
-  static constexpr int kMisc = kBar + 16;                   // tmem base
+  static constexpr int kMisc = kBar + 16;                   // tmem base, rescale flag
   static constexpr int kBytes = kMisc + 16 + 1024;
 };
 static_assert(TcAttSmem::kBytes <= 227 * 1024, "shared memory");
 static_assert(TcAttSmem::kQ % 1024 == 0 && TcAttSmem::kT % 1024 == 0 && TcAttSmem::kP % 1024 == 0,
               "operand chunks on 1024-byte swizzle atoms");
-static_assert(kTileRows * 65 * 4 <= 8 * kQChunk, "softmax transpose fits the query buffer");
+
+// Reduce-scatter of 64 per-lane values over the 32 lanes of a warp: afterwards v[0], v[1] hold
+// the reduction of heads hb, hb + 1 with hb = 32 b4 + 16 b3 + 8 b2 + 4 b1 + 2 b0 (b = lane bits).
+template <bool kMax>
+__device__ __forceinline__ void reduce_scatter64(float (&v)[64], int lane) {
+#pragma unroll
+  for (int r = 0; r < 5; ++r) {
+    const int off = 16 >> r, n = 32 >> r;   // lanes apart, pairs kept
+    const bool hi = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < n; ++i) {
+      const float keep = hi ? v[n + i] : v[i];
+      const float give = hi ? v[i] : v[n + i];
+      const float o = __shfl_xor_sync(0xffffffffu, give, off);
+      v[i] = kMax ? fmaxf(keep, o) : keep + o;
+    }
+  }
+}
+
+__device__ __forceinline__ int scatter_head(int lane) {
+  return ((lane >> 4) & 1) * 32 + ((lane >> 3) & 1) * 16 + ((lane >> 2) & 1) * 8 + ((lane >> 1) & 1) * 4 + (lane & 1) * 2;
+}
 
 __device__ __forceinline__ uint64_t desc_mn_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   uint64_t d = 0;
@@ -139,10 +166,17 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
   const int nvis = (t + 1) / p.m;
   const int W = min(t + 1, kWindow);
   const int R = cnt + W;
-  // splits 0 .. entry_splits-1 cover the entries in 128-row tiles, split entry_splits the window
+  // this CTA's rows: CSA (window apart): splits 0 .. entry_splits-1 cover the entries, split
+  // entry_splits the window; HCA: one list of entries then window, rows_per_split each
   const int split = p.part == 1 ? p.entry_splits : blockIdx.z;
-  const int r_begin = split < p.entry_splits ? split * kTileRows : cnt;
-  const int r_end = split < p.entry_splits ? min(cnt, r_begin + kTileRows) : R;
+  int r_begin, r_end;
+  if (p.window_split) {
+    r_begin = split < p.entry_splits ? split * p.rows_per_split : cnt;
+    r_end = split < p.entry_splits ? min(cnt, r_begin + p.rows_per_split) : R;
+  } else {
+    r_begin = split * p.rows_per_split;
+    r_end = min(R, r_begin + p.rows_per_split);
+  }
   if (r_begin >= r_end) {
     if (p.splits > 1)
       for (int h = tid; h < kHeads; h += kThreads)
@@ -153,32 +187,36 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
         }
     return;
   }
-  const int nrows = r_end - r_begin;
+  const int ntiles = (r_end - r_begin + kTileRows - 1) / kTileRows;
 
   long long* desc = reinterpret_cast<long long*>(smem + L::kDesc);
   float* sscale = reinterpret_cast<float*>(smem + L::kScale);
   float* rinv = reinterpret_cast<float*>(smem + L::kRinv);
+  float* red = reinterpret_cast<float*>(smem + L::kRed);
   float* mrow = reinterpret_cast<float*>(smem + L::kM);
   float* lrow = reinterpret_cast<float*>(smem + L::kL);
+  float* mnew = reinterpret_cast<float*>(smem + L::kMn);
+  float* alpha_s = reinterpret_cast<float*>(smem + L::kAlpha);
   const uint32_t bar_s = sbase + L::kBar;
   const uint32_t bar_pv = bar_s + 8;
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + L::kMisc);
+  volatile int* rescale_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
 
   // ---- the query first (independent of the rows): cp.async into eight K-major chunks
   for (int idx = tid; idx < kHeads * 64; idx += kThreads) {
     const int h = idx >> 6, c = (idx >> 3) & 7, j = idx & 7;   // head, 64-dim chunk, 16-byte piece
-    const bool ok = h0 + h < H;
-    const __nv_bfloat16* g = p.q + ((long long)q * H + (ok ? h0 + h : 0)) * kD + c * 64 + j * 8;
+    const bool okq = h0 + h < H;
+    const __nv_bfloat16* g = p.q + ((long long)q * H + (okq ? h0 + h : 0)) * kD + c * 64 + j * 8;
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(sbase + L::kQ + c * kQChunk + h * 128 +
                                                                       ((j ^ (h & 7)) << 4)),
-                 "l"(g), "r"(ok ? 16 : 0) : "memory");
+                 "l"(g), "r"(okq ? 16 : 0) : "memory");
   }
   cp_async_commit();
 
-  // ---- row descriptors and scales: bits 60..61 select the row set (0 entries, 1 new rows,
-  //      2 ring), -1 = none
-  if (tid < kTileRows) {
-    const int r = r_begin + tid;
+  // row descriptor of tile row i of tile tt: bits 60..61 select the row set (0 entries, 1 new rows,
+  // 2 ring), -1 = none
+  auto make_desc = [&](int tt, int i) -> long long {
+    const int r = r_begin + tt * kTileRows + i;
     long long d = -1;
     if (r < r_end) {
       if (r < cnt) {
@@ -199,26 +237,20 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
         if (d < 0) report(p.status, LCS_ERR_DEVICE_GUARD);
       }
     }
-    desc[tid] = d;
-  }
-  if (tid == 0) {
-    mbar_init(bar_s, 1);
-    mbar_init(bar_pv, 1);
-    fence_mbar_init();
-  }
-  if (warp == 0) tmem_alloc(sbase + L::kMisc, 512);
-  __syncthreads();
+    return d;
+  };
 
-  // ---- rows: FP8 codes (8 bytes = 8 dims per piece, 56 pieces a row) and RoPE dims (8 per
-  //      piece, 8 pieces a row) into registers, then widened into the tile
-  {
-    constexpr int kNP = kTileRows * 56 / kThreads;     // 28 code pieces per thread
-    constexpr int kRP = kTileRows * 8 / kThreads;      // 4 RoPE pieces per thread
-    uint2 cv[kNP];
-    uint4 rv[kRP];
-    float sc = 0.0f;                                   // threads 0-127: the scale of row tid
-    if (tid < kTileRows && desc[tid] >= 0) {
-      const long long d = desc[tid];
+  constexpr int kNP = kTileRows * 56 / kThreads;     // 28 code pieces (8 FP8 codes) per thread
+  constexpr int kRP = kTileRows * 8 / kThreads;      // 4 RoPE pieces (8 BF16) per thread
+  uint2 cv[kNP];
+  uint4 rv[kRP];
+  float sc = 0.0f;                                   // threads 0-127: the scale of row tid
+  // issue the loads of tile tt (descriptors in desc[tt % 3]) into registers
+  auto load_tile = [&](int tt) {
+    const long long* dd = desc + (tt % 3) * kTileRows;
+    sc = 0.0f;
+    if (tid < kTileRows && dd[tid] >= 0) {
+      const long long d = dd[tid];
       const int kind = (int)(d >> 60);
       const long long rw = d & ((1ll << 60) - 1);
       sc = __ldg((kind == 1 ? p.new_rows.scale : (kind == 2 ? p.window.scale : p.entries.scale)) + rw);
@@ -226,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
 #pragma unroll
     for (int it = 0; it < kNP; ++it) {
       const int idx = it * kThreads + tid, r = idx / 56, u = idx % 56;
-      const long long d = desc[r];
+      const long long d = dd[r];
       cv[it] = make_uint2(0u, 0u);
       if (d >= 0) {
         const int kind = (int)(d >> 60);
@@ -238,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
 #pragma unroll
     for (int it = 0; it < kRP; ++it) {
       const int idx = it * kThreads + tid, r = idx >> 3, j = idx & 7;
-      const long long d = desc[r];
+      const long long d = dd[r];
       rv[it] = make_uint4(0u, 0u, 0u, 0u);
       if (d >= 0) {
         const int kind = (int)(d >> 60);
@@ -247,9 +279,44 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
         rv[it] = __ldg(reinterpret_cast<const uint4*>(src + rw * kRope + j * 8));
       }
     }
+  };
+
+  if (tid < kTileRows) desc[tid] = make_desc(0, tid);
+  else if (ntiles > 1) desc[tid] = make_desc(1, tid - kTileRows);   // tile 1 in desc[1]
+  if (tid < kHeads) {
+    mrow[tid] = -INFINITY;
+    lrow[tid] = 0.0f;
+  }
+  if (tid == 0) {
+    mbar_init(bar_s, 1);
+    mbar_init(bar_pv, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(sbase + L::kMisc, 512);
+  __syncthreads();
+  load_tile(0);
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tm_s = tmem;             // S'^T: columns 0..63
+  const uint32_t tm_o = tmem + 64;        // O^T block mb: columns 64 + 64*mb
+
+  constexpr uint32_t kIdS = idesc_f16(0, 128, kHeads);                 // F16, K-major A and B
+  constexpr uint32_t kIdO = idesc_f16(0, 128, kHeads) | (1u << 15);    // A (rows^T) MN-major
+  bool ok = true;
+
+  for (int tt = 0; tt < ntiles; ++tt) {
+    const int bp = tt & 1;
+    const int trows = min(kTileRows, r_end - r_begin - tt * kTileRows);
+    // ---- 1. the previous tile's PV MMAs have read the tile buffer and P
+    if (tt > 0) ok = mbar_wait(bar_pv, (tt - 1) & 1, p.status) && ok;
+    ok = __syncthreads_and(ok);
+    if (!ok) break;
+    // ---- 2. this tile's scales, then its rows widened into the tile buffer
     if (tid < kTileRows) {
-      sscale[tid] = sc;
-      rinv[tid] = sc > 0.0f ? __frcp_rn(sc) : 0.0f;
+      sscale[bp * kTileRows + tid] = sc;
+      rinv[bp * kTileRows + tid] = sc > 0.0f ? __frcp_rn(sc) : 0.0f;
     }
     __syncthreads();
 #pragma unroll
@@ -261,101 +328,140 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
 #pragma unroll
     for (int it = 0; it < kRP; ++it) {
       const int idx = it * kThreads + tid, r = idx >> 3, j = idx & 7;
-      *reinterpret_cast<uint4*>(smem + L::kT + r * 128 + ((j ^ (r & 7)) << 4)) = bf16x8_to_f16x8(rv[it], rinv[r]);
+      *reinterpret_cast<uint4*>(smem + L::kT + r * 128 + ((j ^ (r & 7)) << 4)) =
+          bf16x8_to_f16x8(rv[it], rinv[bp * kTileRows + r]);
     }
-  }
-  cp_async_wait<0>();
-  __syncthreads();
-  for (int idx = tid; idx < kHeads * 64; idx += kThreads) {   // query -> F16 in place
-    uint4* pc = reinterpret_cast<uint4*>(smem + L::kQ + idx * 16);
-    *pc = bf16x8_to_f16x8(*pc, 1.0f);
-  }
-  fence_proxy_async_smem();
-  tc_fence_before_sync();
-  __syncthreads();
-  tc_fence_after_sync();
-  const uint32_t tmem = *tmem_slot;
-  const uint32_t tm_s = tmem;             // S'^T: columns 0..63
-  const uint32_t tm_o = tmem + 64;        // O^T block mb: columns 64 + 64*mb
-
-  constexpr uint32_t kIdS = idesc_f16(0, 128, kHeads);                 // F16, K-major A and B
-  constexpr uint32_t kIdO = idesc_f16(0, 128, kHeads) | (1u << 15);    // A (rows^T) MN-major
-
-  // ---- S'^T = R' . Q^T: 8 chunks x 4 steps of 16 dims
-  if (tid == 0) {
-    tc_fence_after_sync();
-    for (int c = 0; c < 8; ++c)
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        tc_mma_f16(tm_s, smem_desc_sw128(sbase + L::kT + c * kChunk) + 2 * kk,
-                   smem_desc_sw128(sbase + L::kQ + c * kQChunk) + 2 * kk, kIdS, (c > 0 || kk > 0) ? 1u : 0u);
-    tc_commit(bar_s);
-  }
-  bool ok = mbar_wait(bar_s, 0, p.status);
-  ok = __syncthreads_and(ok);
-  tc_fence_after_sync();
-
-  // ---- softmax over the tile's rows, per head (transpose through the query buffer)
-  float* st = reinterpret_cast<float*>(smem + L::kQ);
-  if (ok && warp < 4) {
-    const int r = warp * 32 + lane;
-    const bool valid = r < nrows && desc[r] >= 0;
-    const float lsc = sscale[r] * p.scale_log2;   // logit = s_r * S', in base 2
-#pragma unroll
-    for (int c16 = 0; c16 < kHeads / 16; ++c16) {
-      uint32_t v[16];
-      tmem_ld16(tm_s + ((uint32_t)(warp * 32) << 16) + c16 * 16, v);
-      tmem_ld_wait();
-#pragma unroll
-      for (int j = 0; j < 16; ++j) st[r * 65 + c16 * 16 + j] = valid ? __uint_as_float(v[j]) * lsc : -INFINITY;
-    }
-  }
-  __syncthreads();
-  {
-    const int h = tid >> 2, u = tid & 3;     // four threads per head, 32 rows each
-    float mx = -INFINITY;
-    for (int i = 0; i < 32; ++i) mx = fmaxf(mx, st[(u * 32 + i) * 65 + h]);
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    float sum = 0.0f;
-#pragma unroll
-    for (int g8 = 0; g8 < 4; ++g8) {
-      uint4 pk;
-      uint32_t* w = &pk.x;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int r0 = u * 32 + g8 * 8 + 2 * e;
-        const float a0 = mx == -INFINITY ? 0.0f : exp2f(st[r0 * 65 + h] - mx);
-        const float a1 = mx == -INFINITY ? 0.0f : exp2f(st[(r0 + 1) * 65 + h] - mx);
-        sum += a0 + a1;
-        const __half2 pp = __floats2half2_rn(a0 * sscale[r0] * kP2Scale, a1 * sscale[r0 + 1] * kP2Scale);
-        w[e] = *reinterpret_cast<const uint32_t*>(&pp);
+    // the next tile's rows go out now and fly while this tile computes
+    if (tt + 1 < ntiles) load_tile(tt + 1);
+    if (tt == 0) {
+      cp_async_wait<0>();
+      __syncthreads();
+      for (int idx = tid; idx < kHeads * 64; idx += kThreads) {   // query -> F16 in place
+        uint4* pc = reinterpret_cast<uint4*>(smem + L::kQ + idx * 16);
+        *pc = bf16x8_to_f16x8(*pc, 1.0f);
       }
-      const int rr = u * 32 + g8 * 8;          // first row of this 8-row piece
-      const int pc = rr >> 6, j = (rr & 63) >> 3;
-      *reinterpret_cast<uint4*>(smem + L::kP + pc * kQChunk + h * 128 + ((j ^ (h & 7)) << 4)) = pk;
     }
-    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-    if (u == 0) {
-      mrow[h] = mx;
-      lrow[h] = sum;
-    }
-  }
-  fence_proxy_async_smem();
-  __syncthreads();
-
-  // ---- O^T = R'^T . P'^T: four 128-dim blocks x 8 steps of 16 rows
-  if (tid == 0 && ok) {
+    fence_proxy_async_smem();
+    tc_fence_before_sync();
+    __syncthreads();
     tc_fence_after_sync();
-    for (int mb = 0; mb < 4; ++mb)
+    // ---- 3. S'^T = R' . Q^T
+    if (tid == 0) {
+      for (int c = 0; c < 8; ++c)
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        tc_mma_f16(tm_o + 64 * mb, desc_mn_sw128(sbase + L::kT + 2 * mb * kChunk + kk * 2048, kChunk, 1024),
-                   smem_desc_sw128(sbase + L::kP + (kk >> 2) * kQChunk) + 2 * (kk & 3), kIdO, kk > 0 ? 1u : 0u);
-    tc_commit(bar_pv);
+        for (int kk = 0; kk < 4; ++kk)
+          tc_mma_f16(tm_s, smem_desc_sw128(sbase + L::kT + c * kChunk) + 2 * kk,
+                     smem_desc_sw128(sbase + L::kQ + c * kQChunk) + 2 * kk, kIdS, (c > 0 || kk > 0) ? 1u : 0u);
+      tc_commit(bar_s);
+    }
+    // ---- 4. warps 4-7: descriptors of tile tt + 2; warps 0-3: logits and the tile max per head
+    const int r = warp * 32 + lane;           // warps 0-3: tile row
+    const int hb = scatter_head(lane);
+    const bool rvalid = warp < 4 && r < trows && desc[(tt % 3) * kTileRows + (r & 127)] >= 0;
+    if (warp >= 4) {
+      if (tt + 2 < ntiles) desc[((tt + 2) % 3) * kTileRows + tid - 128] = make_desc(tt + 2, tid - 128);
+    } else {
+      ok = mbar_wait(bar_s, tt & 1, p.status) && ok;
+      ok = __all_sync(0xffffffffu, ok);
+      tc_fence_after_sync();
+      if (ok) {
+        const float lsc = sscale[bp * kTileRows + r] * p.scale_log2;   // logit = s_r * S', base 2
+        float w[64];
+#pragma unroll
+        for (int c16 = 0; c16 < kHeads / 16; ++c16) {
+          uint32_t u[16];
+          tmem_ld16(tm_s + ((uint32_t)(warp * 32) << 16) + c16 * 16, u);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) w[c16 * 16 + j] = rvalid ? __uint_as_float(u[j]) * lsc : -INFINITY;
+        }
+        reduce_scatter64<true>(w, lane);
+        red[warp * kHeads + hb] = w[0];
+        red[warp * kHeads + hb + 1] = w[1];
+      }
+    }
+    ok = __syncthreads_and(ok);
+    if (!ok) break;
+    // ---- 5. new running max and rescale factors per head
+    if (tid == 0) *rescale_flag = 0;
+    __syncthreads();
+    if (tid < kHeads) {
+      const float mt = fmaxf(fmaxf(red[tid], red[kHeads + tid]), fmaxf(red[2 * kHeads + tid], red[3 * kHeads + tid]));
+      const float mo = mrow[tid];
+      const float mn = fmaxf(mo, mt);
+      const float al = (mo == -INFINITY || mn == -INFINITY) ? 0.0f : exp2f(mo - mn);
+      mnew[tid] = mn;
+      alpha_s[tid] = al;
+      if (tt > 0 && al < 1.0f) *rescale_flag = 1;
+    }
+    __syncthreads();
+    // ---- 6. warps 0-3: P' and the tile sum per head; warps 4-7: rescale O^T where the max grew
+    if (warp < 4) {
+      float w[64];
+      const float srow = sscale[bp * kTileRows + r] * kP2Scale;
+      const float lsc = sscale[bp * kTileRows + r] * p.scale_log2;
+      tc_fence_after_sync();
+#pragma unroll
+      for (int c16 = 0; c16 < kHeads / 16; ++c16) {   // the logits again, from tensor memory
+        uint32_t u[16];
+        tmem_ld16(tm_s + ((uint32_t)(warp * 32) << 16) + c16 * 16, u);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) w[c16 * 16 + j] = rvalid ? __uint_as_float(u[j]) * lsc : -INFINITY;
+      }
+#pragma unroll
+      for (int h = 0; h < 64; h += 2) {
+        const float m0 = mnew[h], m1 = mnew[h + 1];
+        const float a0 = m0 == -INFINITY ? 0.0f : exp2f(w[h] - m0);
+        const float a1 = m1 == -INFINITY ? 0.0f : exp2f(w[h + 1] - m1);
+        w[h] = a0;
+        w[h + 1] = a1;
+        // P'[h][r], [h+1][r]: K-major, chunk r/64, piece (r%64)/8 of head row h, element r%8
+        const int pc = r >> 6, pj = (r & 63) >> 3, pe = r & 7;
+        *reinterpret_cast<__half*>(smem + L::kP + pc * kQChunk + h * 128 + ((pj ^ (h & 7)) << 4) + pe * 2) =
+            __float2half_rn(a0 * srow);
+        *reinterpret_cast<__half*>(smem + L::kP + pc * kQChunk + (h + 1) * 128 + ((pj ^ ((h + 1) & 7)) << 4) + pe * 2) =
+            __float2half_rn(a1 * srow);
+      }
+      reduce_scatter64<false>(w, lane);
+      red[warp * kHeads + hb] = w[0];
+      red[warp * kHeads + hb + 1] = w[1];
+    } else if (*rescale_flag) {
+      const int quad = warp & 3;
+#pragma unroll 1
+      for (int mb = 0; mb < 4; ++mb)
+#pragma unroll 1
+        for (int c16 = 0; c16 < kHeads / 16; ++c16) {
+          const uint32_t ta = tm_o + 64 * mb + ((uint32_t)(quad * 32) << 16) + c16 * 16;
+          uint32_t u[16];
+          tmem_ld16(ta, u);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) u[j] = __float_as_uint(__uint_as_float(u[j]) * alpha_s[c16 * 16 + j]);
+          tmem_st16(ta, u);
+        }
+      tmem_st_wait();
+    }
+    fence_proxy_async_smem();
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    // ---- 7. running statistics; O^T += R'^T . P'^T
+    if (tid < kHeads) {
+      lrow[tid] = lrow[tid] * alpha_s[tid] + (red[tid] + red[kHeads + tid]) + (red[2 * kHeads + tid] + red[3 * kHeads + tid]);
+      mrow[tid] = mnew[tid];
+    }
+    if (tid == 0) {
+      for (int mb = 0; mb < 4; ++mb)
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)   // 16 rows per step: two 8-row groups
+          tc_mma_f16(tm_o + 64 * mb, desc_mn_sw128(sbase + L::kT + 2 * mb * kChunk + kk * 2048, kChunk, 1024),
+                     smem_desc_sw128(sbase + L::kP + (kk >> 2) * kQChunk) + 2 * (kk & 3), kIdO,
+                     (tt > 0 || kk > 0) ? 1u : 0u);
+      tc_commit(bar_pv);
+    }
   }
-  if (ok) ok = mbar_wait(bar_pv, 0, p.status);
+  if (ok) ok = mbar_wait(bar_pv, (ntiles - 1) & 1, p.status);
   ok = __syncthreads_and(ok);
   tc_fence_after_sync();
 
@@ -422,6 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
 }
 
 cudaError_t launch_attend_tc(const AttendParams& p, int total_new, cudaStream_t st) {
+  if (p.rows_per_split == kTileRows) return launch_attend_tc1(p, total_new, st);   // one tile per CTA
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(attend_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TcAttSmem::kBytes);

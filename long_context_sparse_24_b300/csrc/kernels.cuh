@@ -70,6 +70,7 @@ struct AttendParams {
   int tc;                    // 1: tensor-core kernel (128-row tiles, rows_per_split == 128)
   int entry_splits;          // tensor-core kernel: splits over the entries; split entry_splits = window
   int part;                  // tensor-core kernel: 0 every split, 1 the window split only, 2 the entry splits
+  int window_split;          // tensor-core kernel: 1 the window rows form split entry_splits (CSA)
   int32_t* status;
 };
 
@@ -86,6 +87,7 @@ int index_tc_qh(const IndexParams& p, int rank, int max_new);
 cudaError_t launch_index_tc(const IndexParams& p, int rank, int max_new, int max_entries, int sms, cudaStream_t st);
 cudaError_t launch_attend(const AttendParams& p, int D, int fmt, int total_new, cudaStream_t st);
 cudaError_t launch_attend_tc(const AttendParams& p, int total_new, cudaStream_t st);
+cudaError_t launch_attend_tc1(const AttendParams& p, int total_new, cudaStream_t st);
 cudaError_t launch_attend_combine(const AttendParams& p, int total_new, int D, cudaStream_t st);
 // rows of one query the tensor-core attention takes at most (per 64-head group)
 constexpr int kAttendTcMaxRows = 2048 + 128;

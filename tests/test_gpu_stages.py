@@ -328,6 +328,9 @@ def _attend_case(kind, lengths, new, heads, dim, fmt, m, k, seed=41, scale=None,
     ("csa", [130, 7], [1, 7], 16, 512, "fp8_split", 4, 32),                    # N(t) < k, short seqs
     ("hca", [20000, 1500, 128], [1, 1, 1], 64, 512, "fp8_split", 128, 0),      # HCA decode
     ("hca", [3000], [17], 64, 512, "fp8_split", 128, 0),
+    # many queries: several 128-row tiles per CTA (online softmax across tiles, O rescaled)
+    ("hca", [40000 - 700 * i for i in range(40)], [1] * 40, 64, 512, "fp8_split", 128, 0),
+    ("csa", [3000 + 37 * i for i in range(120)], [1] * 120, 64, 512, "fp8_split", 4, 1024),
 ])
 def test_attend_matches_oracle(kind, lengths, new, heads, dim, fmt, m, k):
     _attend_case(kind, lengths, new, heads, dim, fmt, m, k)
