@@ -113,6 +113,12 @@ __device__ __forceinline__ uint4 widen8(uint2 codes) {
   return o;
 }
 
+// 16 FP8 codes -> two pieces of 8 F16, exact.
+__device__ __forceinline__ void widen16(uint4 codes, uint4& lo, uint4& hi) {
+  lo = widen8(make_uint2(codes.x, codes.y));
+  hi = widen8(make_uint2(codes.z, codes.w));
+}
+
 // 8 BF16 -> 8 F16, each multiplied by m (m = 1: exact conversion within the F16 range).
 __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v, float m) {
   uint32_t* w = &v.x;
@@ -240,9 +246,9 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
     return d;
   };
 
-  constexpr int kNP = kTileRows * 56 / kThreads;     // 28 code pieces (8 FP8 codes) per thread
+  constexpr int kNP = kTileRows * 28 / kThreads;     // 14 code pieces (16 FP8 codes) per thread
   constexpr int kRP = kTileRows * 8 / kThreads;      // 4 RoPE pieces (8 BF16) per thread
-  uint2 cv[kNP];
+  uint4 cv[kNP];
   uint4 rv[kRP];
   float sc = 0.0f;                                   // threads 0-127: the scale of row tid
   // issue the loads of tile tt (descriptors in desc[tt % 3]) into registers
@@ -257,14 +263,14 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
     }
 #pragma unroll
     for (int it = 0; it < kNP; ++it) {
-      const int idx = it * kThreads + tid, r = idx / 56, u = idx % 56;
+      const int idx = it * kThreads + tid, r = idx / 28, u = idx % 28;
       const long long d = dd[r];
-      cv[it] = make_uint2(0u, 0u);
+      cv[it] = make_uint4(0u, 0u, 0u, 0u);
       if (d >= 0) {
         const int kind = (int)(d >> 60);
         const long long rw = d & ((1ll << 60) - 1);
         const uint8_t* src = (kind == 1 ? p.new_rows.nope : (kind == 2 ? p.window.nope : p.entries.nope));
-        cv[it] = __ldg(reinterpret_cast<const uint2*>(src + rw * kNopeBytes + u * 8));
+        cv[it] = __ldg(reinterpret_cast<const uint4*>(src + rw * kNopeBytes + u * 16));
       }
     }
 #pragma unroll
@@ -321,9 +327,12 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
     __syncthreads();
 #pragma unroll
     for (int it = 0; it < kNP; ++it) {
-      const int idx = it * kThreads + tid, r = idx / 56, u = idx % 56;
-      const int c = 1 + (u >> 3), j = u & 7;
-      *reinterpret_cast<uint4*>(smem + L::kT + c * kChunk + r * 128 + ((j ^ (r & 7)) << 4)) = widen8(cv[it]);
+      const int idx = it * kThreads + tid, r = idx / 28, u = idx % 28;
+      const int c = 1 + (u >> 2), j = (u & 3) * 2;        // chunk, first 16-byte piece of 8 dims
+      uint4 lo, hi;
+      widen16(cv[it], lo, hi);
+      *reinterpret_cast<uint4*>(smem + L::kT + c * kChunk + r * 128 + ((j ^ (r & 7)) << 4)) = lo;
+      *reinterpret_cast<uint4*>(smem + L::kT + c * kChunk + r * 128 + (((j + 1) ^ (r & 7)) << 4)) = hi;
     }
 #pragma unroll
     for (int it = 0; it < kRP; ++it) {

@@ -13,7 +13,7 @@
 // rescaled by their own FP8 scale s_r: R'_r = [rope_r / s_r | codes_r] (the E4M3 codes are exact
 // in F16), so that q . row_r = s_r * (q . R'_r) and sum_r p_r row_r = sum_r (p_r s_r) R'_r.
 //   gather   row descriptors (top-k entries, window rows); every thread then loads the row
-//            scales, its 8-byte pieces of FP8 codes and 16-byte pieces of RoPE dims straight into
+//            scales, its 16-byte pieces of FP8 codes and RoPE dims straight into
 //            registers and writes them widened to F16 into the tile: eight K-major chunks of
 //            [128 rows][64 dims] (chunk 0 the RoPE dims times 1/s_r); the query arrives by
 //            cp.async into eight K-major chunks of [64 heads][64 dims] and becomes F16 in place;
@@ -85,6 +85,12 @@ __device__ __forceinline__ uint4 widen8(uint2 codes) {
   o.z = e4m3x2_to_f16x2((uint16_t)(codes.y & 0xFFFF));
   o.w = e4m3x2_to_f16x2((uint16_t)(codes.y >> 16));
   return o;
+}
+
+// 16 FP8 codes -> two pieces of 8 F16, exact.
+__device__ __forceinline__ void widen16(uint4 codes, uint4& lo, uint4& hi) {
+  lo = widen8(make_uint2(codes.x, codes.y));
+  hi = widen8(make_uint2(codes.z, codes.w));
 }
 
 // 8 BF16 -> 8 F16, each multiplied by m (m = 1: exact conversion within the F16 range).
@@ -220,9 +226,9 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc1_kernel(AttendParams p)
   // ---- rows: FP8 codes (8 bytes = 8 dims per piece, 56 pieces a row) and RoPE dims (8 per
   //      piece, 8 pieces a row) into registers, then widened into the tile
   {
-    constexpr int kNP = kTileRows * 56 / kThreads;     // 28 code pieces per thread
+    constexpr int kNP = kTileRows * 28 / kThreads;     // 14 code pieces (16 FP8 codes) per thread
     constexpr int kRP = kTileRows * 8 / kThreads;      // 4 RoPE pieces per thread
-    uint2 cv[kNP];
+    uint4 cv[kNP];
     uint4 rv[kRP];
     float sc = 0.0f;                                   // threads 0-127: the scale of row tid
     if (tid < kTileRows && desc[tid] >= 0) {
@@ -233,14 +239,14 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc1_kernel(AttendParams p)
     }
 #pragma unroll
     for (int it = 0; it < kNP; ++it) {
-      const int idx = it * kThreads + tid, r = idx / 56, u = idx % 56;
+      const int idx = it * kThreads + tid, r = idx / 28, u = idx % 28;
       const long long d = desc[r];
-      cv[it] = make_uint2(0u, 0u);
+      cv[it] = make_uint4(0u, 0u, 0u, 0u);
       if (d >= 0) {
         const int kind = (int)(d >> 60);
         const long long rw = d & ((1ll << 60) - 1);
         const uint8_t* src = (kind == 1 ? p.new_rows.nope : (kind == 2 ? p.window.nope : p.entries.nope));
-        cv[it] = __ldg(reinterpret_cast<const uint2*>(src + rw * kNopeBytes + u * 8));
+        cv[it] = __ldg(reinterpret_cast<const uint4*>(src + rw * kNopeBytes + u * 16));
       }
     }
 #pragma unroll
@@ -262,9 +268,12 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc1_kernel(AttendParams p)
     __syncthreads();
 #pragma unroll
     for (int it = 0; it < kNP; ++it) {
-      const int idx = it * kThreads + tid, r = idx / 56, u = idx % 56;
-      const int c = 1 + (u >> 3), j = u & 7;
-      *reinterpret_cast<uint4*>(smem + L::kT + c * kChunk + r * 128 + ((j ^ (r & 7)) << 4)) = widen8(cv[it]);
+      const int idx = it * kThreads + tid, r = idx / 28, u = idx % 28;
+      const int c = 1 + (u >> 2), j = (u & 3) * 2;        // chunk, first 16-byte piece of 8 dims
+      uint4 lo, hi;
+      widen16(cv[it], lo, hi);
+      *reinterpret_cast<uint4*>(smem + L::kT + c * kChunk + r * 128 + ((j ^ (r & 7)) << 4)) = lo;
+      *reinterpret_cast<uint4*>(smem + L::kT + c * kChunk + r * 128 + (((j + 1) ^ (r & 7)) << 4)) = hi;
     }
 #pragma unroll
     for (int it = 0; it < kRP; ++it) {
