@@ -44,7 +44,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", default="csa_decode", choices=["csa_decode", "hca_decode", "mixed_decode"],
+    ap.add_argument("--workload", default="csa_decode",
+                    choices=["csa_decode", "hca_decode", "mixed_decode", "csa_prefill"],
                     help="csa_decode is the headline line; the others measure the HCA decode and the mixed "
                          "ragged multi-layer workloads with the same timing rules")
     return ap.parse_args()
@@ -477,8 +478,130 @@ def run_gpu_stack(args, rank, world, local, wl):
            "top_k": k, "index_heads": Hi, "index_rank": r, "window": 128, "seed": wl.seed,
            "l2": "flushed between timed steps (256 MB write)", "data": "synthetic",
            "parallelism": f"replicas x{world} (independent sequences per GPU)"}
-    return {"ms": ms, "clocks": clk.summary(), "roofline": roofline, "launches": launches * args.steps,
+    return {"ms": ms, "clocks": clk.summary(), "roofline": roofline, "launches": launches,
             "status_ok": status_ok, "per_rank_queries": S, "config": cfg}
+
+
+# ---------------------------------------------------------------------------------------------
+# GPU arm, CSA prefill chunk: one sequence, 1M cached tokens + a chunk of new tokens (queries)
+# ---------------------------------------------------------------------------------------------
+
+def run_gpu_prefill(args, rank, world, local, wl):
+    import torch
+    import synth.gpu as sg
+    import long_context_sparse_24_b300 as lcsa
+    from long_context_sparse_24_b300.layer import Layer
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if lcsa.lcs_device_check() != 0:
+        raise SystemExit("liblcsa needs a compute-capability 10.3 GPU")
+    L, T, H, D = wl.ctx_len, wl.new_tokens, wl.heads, wl.dim
+    Hi, r, k, m = wl.index_heads, wl.index_rank, wl.top_k, wl.m
+    seed = wl.seed + 1000 * rank
+    cap = L + T + 256
+    layer = Layer("csa", 1, cap, H, D, lcsa.LCS_ROW_FP8_SPLIT, m, top_k=k, index_heads=Hi, index_rank=r,
+                  max_new=T, device=dev)
+    w = synth.bf16_bits_to_f32(synth.normal_bf16(seed, synth.tensor_id(synth.COMP_W), 0, D)) / 16
+    bias = synth.bf16_bits_to_f32(synth.normal_bf16(seed, synth.tensor_id(synth.COMP_B), 0, 2 * m)) / 2
+    layer.set_compressor(torch.from_numpy(w.astype(np.float32)).to(dev),
+                         torch.from_numpy(bias.astype(np.float32)).to(dev))
+    chunk = 65536
+    raw = torch.empty((chunk, D), dtype=torch.bfloat16, device=dev)
+    for c0 in range(0, L, chunk):
+        n = min(chunk, L - c0)
+        sg.normal_bf16(raw[:n], seed, synth.tensor_id(synth.RAW, 0, 0), c0 * D)
+        layer.fill(layer.batch([c0 + n], [n]), raw[:n])
+    n_ent = cap // m
+    sg.e2m1_packed(layer.cache.keys.fp4[:n_ent], seed, synth.tensor_id(synth.IDX_K, 0, 0), 0)
+    sg.ue8m0(layer.cache.keys.scale[:n_ent], seed, synth.tensor_id(synth.IDX_KS, 0, 0), 0)
+    # the chunk's inputs: tokens L .. L+T-1
+    raw_new = torch.empty((T, D), dtype=torch.bfloat16, device=dev)
+    sg.normal_bf16(raw_new, seed, synth.tensor_id(synth.RAW, 0, 0), L * D)
+    q = torch.empty((T, H, D), dtype=torch.bfloat16, device=dev)
+    sg.normal_bf16(q, seed, synth.tensor_id(synth.QUERY, 0, 0), L * H * D)
+    iq = torch.empty((T, Hi, r // 2), dtype=torch.uint8, device=dev)
+    sg.e2m1_packed(iq, seed, synth.tensor_id(synth.IDX_Q, 0, 0), L * Hi * r)
+    iqs = torch.empty((T, Hi, r // 32), dtype=torch.uint8, device=dev)
+    sg.ue8m0(iqs, seed, synth.tensor_id(synth.IDX_QS, 0, 0), L * Hi * r // 32)
+    hw = torch.from_numpy(synth.head_weights(seed, synth.tensor_id(synth.HEAD_W, 0, 0), L * Hi, T * Hi)
+                          .reshape(T, Hi).astype(np.float32)).to(dev)
+    out = torch.empty((T, H, D), dtype=torch.bfloat16, device=dev)
+    batch = layer.batch([L + T], [T])
+
+    def step_body():
+        layer.step(batch, raw_new, q, out, idx_q_fp4=iq, idx_q_scale=iqs, head_w=hw)
+
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    step_body()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step_body()
+    n_tot = args.warmup + args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(n_tot)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(n_tot)]
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for st in range(n_tot):
+            flush.zero_()
+            starts[st].record()
+            graph.replay()
+            ends[st].record()
+        torch.cuda.synchronize()
+    ms = statistics.mean(starts[st].elapsed_time(ends[st]) for st in range(args.warmup, n_tot))
+    if world > 1:
+        import torch.distributed as dist
+        t_ = torch.tensor([ms], device=dev)
+        dist.all_reduce(t_, op=dist.ReduceOp.MAX)
+        ms = float(t_.item())
+    # ---- per-stage device time: the step's calls one after another on one stream, untimed above
+    cur = torch.cuda.current_stream()
+    names = ["compress", "index_topk", "attend", "window_commit"]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
+    stage = {n_: 0.0 for n_ in names}
+    reps = 3
+    for _ in range(reps):
+        flush.zero_()
+        ev[0].record(cur)
+        layer.compress(batch, raw_new, cur); ev[1].record(cur)
+        layer.select(batch, iq, iqs, hw, cur); ev[2].record(cur)
+        layer.attend(batch, q, out, None, cur); ev[3].record(cur)
+        layer.commit(batch, cur); ev[4].record(cur)
+        torch.cuda.synchronize()
+        for i_, n_ in enumerate(names):
+            stage[n_] += ev[i_].elapsed_time(ev[i_ + 1]) / reps
+    # ---- roofline of the dominant stage, a contraction: the indexer takes 2 r Hi FLOP per
+    #      (query, visible entry) pair on FP8-class MMAs; the attention 4 H D FLOP per (query, row),
+    #      rows = min(k, N(t)) + 128, on BF16/F16 MMAs
+    pairs = sum((L + i + 1) // m for i in range(T))
+    idx_flop = pairs * 2 * r * Hi
+    att_flop = sum(4 * H * D * (min(k, (L + i + 1) // m) + 128) for i in range(T))
+    peak_bf16 = None
+    pth = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pth):
+        peak_bf16 = json.load(open(pth)).get("bf16_tflops")
+    peak_src = "of measured (MEASURED_PEAKS.json bf16_tflops)" if peak_bf16 else "of fallback"
+    peak_bf16 = peak_bf16 or 1800.0
+    if stage["index_topk"] >= stage["attend"]:
+        kern, flop, t_ms, peak = ("index_score_kernel + topk_select_kernel (csa_index_topk)", idx_flop,
+                                  stage["index_topk"], 2 * peak_bf16)
+        peak_src += " x 2 (nominal FP8/BF16 ratio)"
+    else:
+        kern, flop, t_ms, peak = ("attend_kernel + attend_combine_kernel (csa_attend)", att_flop, stage["attend"],
+                                  peak_bf16)
+    achieved = flop / (t_ms * 1e-3) / 1e12
+    roofline = {"kernel": kern, "bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1),
+                "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "peak_source": peak_src,
+                "flop_per_step": {"indexer": int(idx_flop), "attention": int(att_flop)},
+                "stage_ms": {n_: round(v, 4) for n_, v in stage.items()}, "traffic": None}
+    cfg = {"workload": wl.name, "num_seqs": 1, "ctx_len": L, "new_tokens_per_seq": T, "heads": H, "kv_dim": D,
+           "row_format": "fp8_e4m3(448)+bf16_rope(64)+f32_scale", "m": m, "overlap": True, "index_heads": Hi,
+           "index_rank": r, "index_format": "fp4_e2m1+ue8m0/32", "top_k": k, "window": 128, "seed": wl.seed,
+           "step": "the same chunk of new tokens re-run every step (identical work)",
+           "l2": "flushed between timed steps (256 MB write)", "data": "synthetic"}
+    return {"ms": ms, "clocks": clk.summary(), "roofline": roofline, "status_ok": int(layer.status.item()) == 0,
+            "per_rank_queries": T, "config": cfg, "launches": 2 + 2 + 1 + 1}
 
 
 def run_e2e(torch, layer, batch, graph, raw_in, q_in, iq_in, iqs_in, hw_in, out, seq_len, raw_steps, q_steps,
@@ -624,7 +747,8 @@ def main():
         return
     assert args.warmup >= 3, "at least 3 warm-up steps"
     if args.workload != "csa_decode":
-        res = run_gpu_stack(args, rank, world, local, synth.CONFIGS[args.workload])
+        runner = run_gpu_prefill if args.workload == "csa_prefill" else run_gpu_stack
+        res = runner(args, rank, world, local, synth.CONFIGS[args.workload])
         if rank == 0:
             value = res["per_rank_queries"] * world / (res["ms"] * 1e-3)
             print(json.dumps({"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
@@ -632,7 +756,8 @@ def main():
                               "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                               "dtype": "fp8/fp4 storage, f16/bf16 MMA, fp32 accumulate", "data": "synthetic",
                               "config": res["config"], "roofline": res["roofline"], "clocks": res["clocks"],
-                              "e2e": None, "gpu_launches": res["launches"], "device_status_ok": res["status_ok"]}))
+                              "e2e": None, "gpu_launches": res["launches"] * args.steps,
+                              "device_status_ok": res["status_ok"]}))
         return
     res = run_gpu(args, rank, world, local)
     if rank == 0:

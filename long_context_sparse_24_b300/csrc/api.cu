@@ -116,6 +116,14 @@ struct TopkWs {
   size_t keys, hist, total;
 };
 
+// Indexer scores: the tcgen05 scorer for a few queries per sequence, the tcgen05 prefill scorer
+// for query runs, the warp-MMA scorer for what neither takes (rank 64, other page sizes).
+cudaError_t launch_index(const IndexParams& p, int rank, int max_new, int max_entries, cudaStream_t st) {
+  if (index_tc_qh(p, rank, max_new) > 0) return launch_index_tc(p, rank, max_new, max_entries, num_sms(), st);
+  if (index_tc_pf_applies(p, rank, max_new)) return launch_index_tc_pf(p, rank, max_new, max_entries, st);
+  return launch_index_scores(p, rank, max_new, max_entries, st);
+}
+
 TopkWs topk_ws_layout(const lcs_batch* b, int m) {
   const size_t T = (size_t)b->total_new, ld = (size_t)index_ld(b, m);
   TopkWs w;
@@ -374,8 +382,7 @@ lcs_status csa_index_topk(const lcs_batch* batch, const uint8_t* q_fp4, const ui
   // the per-query histograms accumulate with atomics: clear them first
   cudaError_t e = cudaMemsetAsync(ws + w.hist, 0, w.total - 256 - w.hist, st);
   if (e != cudaSuccess) return LCS_ERR_CUDA;
-  e = index_tc_qh(p, keys->rank, batch->max_new) > 0 ? launch_index_tc(p, keys->rank, batch->max_new, max_entries, num_sms(), st)
-                                                     : launch_index_scores(p, keys->rank, batch->max_new, max_entries, st);
+  e = launch_index(p, keys->rank, batch->max_new, max_entries, st);
   if (e != cudaSuccess) return LCS_ERR_CUDA;
   e = launch_topk_select(p.keys_out, p.hist, p.ld, batch->cu_new, batch->seq_len, batch->num_seqs, batch->max_new,
                          m, k, out_idx, out_cnt, st);
@@ -397,9 +404,7 @@ lcs_status csa_index_scores(const lcs_batch* batch, const uint8_t* q_fp4, const 
   p.status = dev_status;
   const int max_entries = batch->max_seq_len / m;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  return from_cuda(index_tc_qh(p, keys->rank, batch->max_new) > 0
-                       ? launch_index_tc(p, keys->rank, batch->max_new, max_entries, num_sms(), st)
-                       : launch_index_scores(p, keys->rank, batch->max_new, max_entries, st));
+  return from_cuda(launch_index(p, keys->rank, batch->max_new, max_entries, st));
 }
 
 size_t lcs_attend_workspace(const lcs_batch* batch, int32_t heads, int32_t dim, int32_t max_rows) {

@@ -85,6 +85,9 @@ cudaError_t launch_topk_select(const uint32_t* keys, const uint32_t* hist, long 
 // tcgen05 scorer for a few queries per sequence: query-head columns it would use (0 = not applicable)
 int index_tc_qh(const IndexParams& p, int rank, int max_new);
 cudaError_t launch_index_tc(const IndexParams& p, int rank, int max_new, int max_entries, int sms, cudaStream_t st);
+// tcgen05 scorer for long runs of queries per sequence (prefill chunks)
+bool index_tc_pf_applies(const IndexParams& p, int rank, int max_new);
+cudaError_t launch_index_tc_pf(const IndexParams& p, int rank, int max_new, int max_entries, cudaStream_t st);
 cudaError_t launch_attend(const AttendParams& p, int D, int fmt, int total_new, cudaStream_t st);
 cudaError_t launch_attend_tc(const AttendParams& p, int total_new, cudaStream_t st);
 cudaError_t launch_attend_tc1(const AttendParams& p, int total_new, cudaStream_t st);

@@ -210,3 +210,167 @@ def test_hybrid_stack_ragged_decode_matches_oracle():
                 else:
                     ref = oracle.hca_layer(raw, w, b, 128, "fp8_split", qf, [pos[s_]], 1 / math.sqrt(D))
                 check_outputs(o[s_], ref["o"][0], f"step {st} layer {li} seq {s_}")
+
+
+# ------------------------------------------------------------------------------------------ large
+#
+# Full-size workloads, one step each in the layer driver's launch configuration.  The device
+# inputs come from the seeded generator's CUDA build (spot-checked against its numpy build);
+# the oracle recomputes the sampled queries from the numpy generator: their top-k over every
+# visible entry, the selected entries compressed from their own raw spans, the window rows.
+
+def _entries_from_spans(seed, lay, seq, js, m, overlap, w, b, dim):
+    """Oracle entries js (fp64, before quantisation), each compressed from its own raw span."""
+    out = np.empty((len(js), dim))
+    for i, j in enumerate(js):
+        j = int(j)
+        if overlap and j > 0:
+            raw = _raw_f64(seed, lay, seq, (j - 1) * m, 2 * m, dim)
+            out[i] = oracle.compress(raw, w, b, m, True, 1, 1)[0]
+        else:
+            raw = _raw_f64(seed, lay, seq, j * m, m, dim)
+            out[i] = oracle.compress(raw, w, b, m, overlap, 0, 1)[0]
+    return out
+
+
+def _fill_context(lay, seed, li, lengths, dim, chunk=16384):
+    raw_chunk = torch.empty((len(lengths) * chunk, dim), dtype=torch.bfloat16, device=DEV)
+    for c0 in range(0, max(lengths), chunk):
+        ns = [max(0, min(chunk, L - c0)) for L in lengths]
+        off = 0
+        for s_, n in enumerate(ns):
+            if n:
+                sg.normal_bf16(raw_chunk[off:off + n], seed, synth.tensor_id(synth.RAW, li, s_), c0 * dim)
+                off += n
+        lay.fill(lay.batch([min(L, c0 + n) if n else L for L, n in zip(lengths, ns)], ns), raw_chunk[:off])
+    del raw_chunk
+
+
+def _check_csa_query(lay, seed, s_, t, row, q_np, qc, qs, hw, w, b, out_row, label):
+    m, k, D = lay.m, lay.top_k, lay.dim
+    n = oracle.visible_entries(t, m)
+    kc, ks = _keys_np(seed, 0, s_, n, lay.index_rank)
+    sel = oracle.topk_select(oracle.index_scores(qc, qs, hw, kc, ks)[0, :n], k)
+    assert int(lay.topk_cnt[row].item()) == len(sel), label
+    assert np.array_equal(lay.topk_idx[row, :len(sel)].cpu().numpy(), sel), label
+    ent = oracle.quantize_rows(_entries_from_spans(seed, 0, s_, sel, m, True, w, b, D), "fp8_split")["deq"]
+    lo = max(0, t - 127)
+    win = oracle.quantize_rows(_raw_f64(seed, 0, s_, lo, t + 1 - lo, D), "fp8_split")["deq"]
+    o, _ = oracle.attend(bits_to_f64(q_np), np.concatenate([ent, win]), lay.scale)
+    check_outputs(out_row, o, label)
+
+
+def test_csa_decode_32x128k_full_size_sampled():
+    """32 sequences x 131,072 cached tokens, 64 heads, D=512, k=512: one decode step; sequences
+    0, 13 and 31 checked against the oracle (top-k bit-exact, outputs)."""
+    wl = synth.CONFIGS["csa_decode"]
+    seed, S, L, H, D, m, k, hi, r = wl.seed, wl.num_seqs, wl.ctx_len, wl.heads, wl.dim, wl.m, wl.top_k, \
+        wl.index_heads, wl.index_rank
+    lay = Layer("csa", S, L + 256, H, D, lcsa.LCS_ROW_FP8_SPLIT, m, top_k=k, index_heads=hi, index_rank=r,
+                max_new=1, device=DEV)
+    w, b = _comp_params(seed, 0, D, m, True)
+    lay.set_compressor(torch.from_numpy(w).to(DEV), torch.from_numpy(b).to(DEV))
+    _fill_context(lay, seed, 0, [L] * S, D)
+    for s_ in range(S):
+        _fill_keys(lay, seed, 0, s_, (L + 1) // m, r)
+    ins = [_query_inputs(seed, 0, s_, L, 1, H, D, hi, r) for s_ in range(S)]
+    raw_new = torch.empty((S, D), dtype=torch.bfloat16, device=DEV)
+    for s_ in range(S):
+        sg.normal_bf16(raw_new[s_], seed, synth.tensor_id(synth.RAW, 0, s_), L * D)
+    q_dev = to_dev_bf16_bits(np.concatenate([x[0] for x in ins]))
+    out = torch.empty((S, H, D), dtype=torch.bfloat16, device=DEV)
+    lay.step(lay.batch([L + 1] * S, [1] * S), raw_new, q_dev, out,
+             idx_q_fp4=_dev_u8(synth.pack_e2m1(np.concatenate([x[1] for x in ins]))),
+             idx_q_scale=_dev_u8(np.concatenate([x[2] for x in ins])),
+             head_w=torch.from_numpy(np.concatenate([x[3] for x in ins])).to(DEV))
+    torch.cuda.synchronize()
+    assert int(lay.status.item()) == 0
+    o = out.float().cpu().numpy().astype(np.float64)
+    w64, b64 = w.astype(np.float64), b.astype(np.float64)
+    for s_ in (0, 13, 31):
+        q, qc, qs, hw = ins[s_]
+        _check_csa_query(lay, seed, s_, L, s_, q[0], qc, qs, hw, w64, b64, o[s_], f"seq {s_}")
+    del lay, out
+    torch.cuda.empty_cache()
+
+
+def test_csa_prefill_1m_plus_16k_full_size_sampled():
+    """One sequence, 1,048,576 cached tokens + a 16,384-token chunk, 128 heads, D=512, k=1024:
+    one prefill step; queries 0, 1, 4099, 9000 and 16383 of the chunk checked against the
+    oracle (top-k over all visible entries bit-exact, outputs)."""
+    wl = synth.CONFIGS["csa_prefill"]
+    seed, L, T, H, D, m, k, hi, r = wl.seed, wl.ctx_len, wl.new_tokens, wl.heads, wl.dim, wl.m, wl.top_k, \
+        wl.index_heads, wl.index_rank
+    lay = Layer("csa", 1, L + T + 256, H, D, lcsa.LCS_ROW_FP8_SPLIT, m, top_k=k, index_heads=hi, index_rank=r,
+                max_new=T, device=DEV)
+    w, b = _comp_params(seed, 0, D, m, True)
+    lay.set_compressor(torch.from_numpy(w).to(DEV), torch.from_numpy(b).to(DEV))
+    _fill_context(lay, seed, 0, [L], D, chunk=65536)
+    _fill_keys(lay, seed, 0, 0, (L + T) // m, r)
+    raw_new = torch.empty((T, D), dtype=torch.bfloat16, device=DEV)
+    sg.normal_bf16(raw_new, seed, synth.tensor_id(synth.RAW, 0, 0), L * D)
+    q_dev = torch.empty((T, H, D), dtype=torch.bfloat16, device=DEV)
+    sg.normal_bf16(q_dev, seed, synth.tensor_id(synth.QUERY, 0, 0), L * H * D)
+    iq = torch.empty((T, hi, r // 2), dtype=torch.uint8, device=DEV)
+    sg.e2m1_packed(iq, seed, synth.tensor_id(synth.IDX_Q, 0, 0), L * hi * r)
+    iqs = torch.empty((T, hi, r // 32), dtype=torch.uint8, device=DEV)
+    sg.ue8m0(iqs, seed, synth.tensor_id(synth.IDX_QS, 0, 0), L * hi * r // 32)
+    hw = synth.head_weights(seed, synth.tensor_id(synth.HEAD_W, 0, 0), L * hi, T * hi).reshape(T, hi)
+    out = torch.empty((T, H, D), dtype=torch.bfloat16, device=DEV)
+    lay.step(lay.batch([L + T], [T]), raw_new, q_dev, out, idx_q_fp4=iq, idx_q_scale=iqs,
+             head_w=torch.from_numpy(np.ascontiguousarray(hw)).to(DEV))
+    torch.cuda.synchronize()
+    assert int(lay.status.item()) == 0
+    # the device-side generator agrees with the numpy one on the sampled queries' inputs
+    w64, b64 = w.astype(np.float64), b.astype(np.float64)
+    for i in (0, 1, 4099, 9000, T - 1):
+        q, qc, qs, hw_i = _query_inputs(seed, 0, 0, L + i, 1, H, D, hi, r)
+        assert np.array_equal(q_dev[i].view(torch.int16).cpu().numpy().view(np.uint16), q[0]), i
+        assert np.array_equal(iq[i].cpu().numpy(), synth.pack_e2m1(qc[0])), i
+        assert np.array_equal(hw[i], hw_i[0]), i
+        _check_csa_query(lay, seed, 0, L + i, i, q[0], qc, qs, hw_i, w64, b64,
+                         out[i].float().cpu().numpy().astype(np.float64), f"query {i}")
+    del lay, out, q_dev
+    torch.cuda.empty_cache()
+
+
+def test_hca_decode_64x1m_full_size_sampled():
+    """64 sequences x 1,048,576 cached tokens, 64 heads, D=512: one decode step; sequences 0
+    and 63 checked against dense oracle attention over all 8,192 entries + the window."""
+    wl = synth.CONFIGS["hca_decode"]
+    seed, S, L, H, D, m = wl.seed, wl.num_seqs, wl.ctx_len, wl.heads, wl.dim, wl.m
+    lay = Layer("hca", S, L + 256, H, D, lcsa.LCS_ROW_FP8_SPLIT, m, max_new=1, device=DEV)
+    w, b = _comp_params(seed, 0, D, m, False)
+    lay.set_compressor(torch.from_numpy(w).to(DEV), torch.from_numpy(b).to(DEV))
+    _fill_context(lay, seed, 0, [L] * S, D, chunk=8192)
+    raw_new = torch.empty((S, D), dtype=torch.bfloat16, device=DEV)
+    for s_ in range(S):
+        sg.normal_bf16(raw_new[s_], seed, synth.tensor_id(synth.RAW, 0, s_), L * D)
+    qs_np = [synth.normal_bf16(seed, synth.tensor_id(synth.QUERY, 0, s_), L * H * D, H * D).reshape(H, D)
+             for s_ in range(S)]
+    out = torch.empty((S, H, D), dtype=torch.bfloat16, device=DEV)
+    lay.step(lay.batch([L + 1] * S, [1] * S), raw_new, to_dev_bf16_bits(np.stack(qs_np)), out)
+    torch.cuda.synchronize()
+    assert int(lay.status.item()) == 0
+    o = out.float().cpu().numpy().astype(np.float64)
+    w64, b64 = w.astype(np.float64), b.astype(np.float64)
+    t = L
+    n = oracle.visible_entries(t, m)
+    chunk = 65536
+    raw_dev = torch.empty((chunk, D), dtype=torch.bfloat16, device=DEV)
+    for s_ in (0, S - 1):
+        # the sequence's raw rows from the device-side generator, spot-checked against numpy
+        ent = np.empty((n, D))
+        for c0 in range(0, n * m, chunk):
+            sg.normal_bf16(raw_dev, seed, synth.tensor_id(synth.RAW, 0, s_), c0 * D)
+            bits = raw_dev.view(torch.int16).cpu().numpy().view(np.uint16)
+            if c0 in (0, 7 * chunk):
+                ref_bits = synth.normal_bf16(seed, synth.tensor_id(synth.RAW, 0, s_), c0 * D, 4096).reshape(8, D)
+                assert np.array_equal(bits[:8], ref_bits)
+            ent[c0 // m:(c0 + chunk) // m] = oracle.compress_blocked(bits_to_f64(bits), w64, b64, m, False)
+        ent_q = oracle.quantize_rows(ent, "fp8_split")["deq"]
+        win = oracle.quantize_rows(_raw_f64(seed, 0, s_, t - 127, 128, D), "fp8_split")["deq"]
+        ref, _ = oracle.attend(bits_to_f64(qs_np[s_]), np.concatenate([ent_q, win]), lay.scale)
+        check_outputs(o[s_], ref, f"seq {s_}")
+    del lay, out, raw_dev
+    torch.cuda.empty_cache()
