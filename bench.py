@@ -584,12 +584,12 @@ def run_gpu_prefill(args, rank, world, local, wl):
     peak_src = "of measured (MEASURED_PEAKS.json bf16_tflops)" if peak_bf16 else "of fallback"
     peak_bf16 = peak_bf16 or 1800.0
     if stage["index_topk"] >= stage["attend"]:
-        kern, flop, t_ms, peak = ("index_score_kernel + topk_select_kernel (csa_index_topk)", idx_flop,
+        kern, flop, t_ms, peak = ("index_tc_pf_kernel + topk_select_kernel (csa_index_topk)", idx_flop,
                                   stage["index_topk"], 2 * peak_bf16)
         peak_src += " x 2 (nominal FP8/BF16 ratio)"
     else:
-        kern, flop, t_ms, peak = ("attend_kernel + attend_combine_kernel (csa_attend)", att_flop, stage["attend"],
-                                  peak_bf16)
+        kern, flop, t_ms, peak = ("attend_tc_kernel (csa_attend: one CTA per query and 64-head group)", att_flop,
+                                  stage["attend"], peak_bf16)
     achieved = flop / (t_ms * 1e-3) / 1e12
     roofline = {"kernel": kern, "bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1),
                 "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "peak_source": peak_src,

@@ -61,35 +61,36 @@ struct SplitPlan {
   int rows_per_split;
   int tc;
   int entry_splits;   // tensor-core plan: 128-row tiles of entries; one more split for the window
+  int window_apart;   // tensor-core plan: the window rows form their own split (CSA, few queries)
 };
 
-// The tensor-core attention takes FP8-split rows of D = 512 (the only D = 512 format) and up to
-// 64 heads.  CSA (window apart, window_split): top-k lists up to 2048 entries, one split per
-// 128-row tile of entries while a wave has room, plus the window split.  HCA (one list): any
-// length, the list cut into about one wave of CTAs.
-bool attend_tc_applies(int heads, int dim, int max_rows, bool window_split) {
-  return dim == 512 && heads <= 64 && (!window_split || max_rows <= kAttendTcMaxRows);
-}
+// The tensor-core attention takes FP8-split rows of D = 512 (the only D = 512 format), heads in
+// groups of 64 (one CTA per group).  CSA with few queries (window_split and less than a wave of
+// (query, head group) CTAs): top-k lists up to 2048 entries, one split per 128-row tile of
+// entries while a wave has room, plus the window split, so that the window part can run next to
+// the indexer.  Otherwise (HCA, or CSA prefill runs that fill the GPU by themselves): one list of
+// entries then window rows, cut into about one wave of CTAs.
+bool attend_tc_applies(int heads, int dim) { return dim == 512 && heads <= 128; }
 
 SplitPlan plan_splits(const lcs_batch* b, int heads, int dim, int max_rows, bool window_split) {
-  if (attend_tc_applies(heads, dim, max_rows, window_split)) {
+  if (attend_tc_applies(heads, dim)) {
     const long long ctas = std::max<long long>(1, (long long)b->total_new * ((heads + 63) / 64));
     const int per_query = (int)std::max<long long>(1, num_sms() / ctas);   // CTAs per (query, head group)
-    if (window_split) {
+    if (window_split && per_query > 1 && max_rows <= kAttendTcMaxRows) {
       const int tiles = std::max(1, (max_rows - LCSA_WINDOW + 127) / 128);
       const int es = std::min(tiles, per_query);
       const int tps = (tiles + es - 1) / es;
-      return SplitPlan{(tiles + tps - 1) / tps + 1, 128 * tps, 1, (tiles + tps - 1) / tps};
+      return SplitPlan{(tiles + tps - 1) / tps + 1, 128 * tps, 1, (tiles + tps - 1) / tps, 1};
     }
     const int tiles = std::max(1, (max_rows + 127) / 128);
     const int sp = std::min(tiles, per_query);
     const int tps = (tiles + sp - 1) / sp;
     const int splits = (tiles + tps - 1) / tps;
-    return SplitPlan{splits, 128 * tps, 1, splits};
+    return SplitPlan{splits, 128 * tps, 1, splits, 0};
   }
   const int hg = heads <= 16 ? 1 : (heads + 63) / 64;
   const long long base = (long long)b->total_new * hg;
-  SplitPlan s{1, max_rows > 0 ? max_rows : 1, 0, 0};
+  SplitPlan s{1, max_rows > 0 ? max_rows : 1, 0, 0, 0};
   const int sms = num_sms();
   if (base <= 0 || base >= sms || max_rows <= 64) return s;
   int want = (int)(sms / base);
@@ -257,7 +258,7 @@ lcs_status attend_common(const lcs_batch* batch, const void* q, int32_t heads, c
   p.rows_per_split = plan.rows_per_split;
   p.tc = plan.tc;
   p.entry_splits = plan.entry_splits;
-  p.window_split = plan.tc && window_split ? 1 : 0;
+  p.window_split = plan.window_apart;
   if (plan.splits > 1) {
     const size_t per = (size_t)batch->total_new * heads * plan.splits;
     const size_t ob = per * entries->dim * (plan.tc ? 2 : 4);
@@ -279,9 +280,9 @@ lcs_status csa_attend_part(const lcs_batch* batch, const void* q, int32_t heads,
   lcs_status s = attend_common(batch, q, heads, entries, paging, state, part == 1 ? nullptr : out, workspace,
                                workspace_bytes, k + LCSA_WINDOW, p, true, part == 1);
   if (s != LCS_OK) return s;
-  if (part != 0 && !p.tc) {
-    // only the tensor-core plan computes the window split apart: here the window call does
-    // nothing and the top-k call computes everything
+  if (part != 0 && !p.window_split) {
+    // only the tensor-core plan for few queries computes the window split apart: otherwise the
+    // window call does nothing and the top-k call computes everything
     if (part == 1) return LCS_OK;
     part = 0;
   }

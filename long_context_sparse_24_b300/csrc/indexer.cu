@@ -321,7 +321,7 @@ __device__ void emit_selected(SelectShared& sh, int n, KeyAt key_at, IdxAt idx_a
 
 // grid: (max_new, num_seqs); block kSelThreads; dynamic smem sizeof(SelectShared).
 // hist: the per-query histogram of key >> 21 built by the score kernel.
-__global__ void __launch_bounds__(kSelThreads) topk_select_kernel(const uint32_t* keys, const uint32_t* hist,
+__global__ void __launch_bounds__(kSelThreads, 2) topk_select_kernel(const uint32_t* keys, const uint32_t* hist,
                                                                  long long ld, const int32_t* cu_new,
                                                                  const int32_t* seq_len, int m, int k,
                                                                  int32_t* out_idx, int32_t* out_cnt) {
@@ -451,6 +451,9 @@ cudaError_t launch_topk_select(const uint32_t* keys, const uint32_t* hist, long 
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    // two CTAs per SM for long query runs (prefill): ask for the whole carveout as shared memory
+    e = cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }

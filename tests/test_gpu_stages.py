@@ -331,6 +331,9 @@ def _attend_case(kind, lengths, new, heads, dim, fmt, m, k, seed=41, scale=None,
     ("csa", [2000, 4100, 300], [1, 1, 1], 64, 512, "fp8_split", 4, 512),       # decode, split-KV
     ("csa", [900, 2200], [40, 9], 64, 512, "fp8_split", 4, 64),                # prefill chunk
     ("csa", [3000], [3], 128, 512, "fp8_split", 4, 256),                       # 128 heads = 2 groups
+    ("csa", [2000], [3], 96, 512, "fp8_split", 4, 256),                        # a partial head group
+    ("csa", [5000, 2600], [300, 200], 128, 512, "fp8_split", 4, 512),          # prefill: one list per CTA
+    ("hca", [3000], [200], 128, 512, "fp8_split", 128, 0),
     ("csa", [50, 700], [50, 20], 8, 128, "bf16", 4, 64),                       # small-model rows
     ("csa", [600], [5], 8, 128, "fp8_split", 4, 64),
     ("csa", [130, 7], [1, 7], 16, 512, "fp8_split", 4, 32),                    # N(t) < k, short seqs
