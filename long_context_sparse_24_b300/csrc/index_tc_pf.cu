@@ -10,15 +10,16 @@
 // tiles of that sequence (grid = runs x query groups x sequences).  The CTA is warp-specialised
 // like the decode scorer -- two producer warps stream the tiles' E2M1 codes through TMA (the
 // "16 x U4 in 16 bytes" form, 128-byte swizzle, i.e. the K-major E2M1 operand of kind::f8f6f4)
-// plus their block scales through cp.async, one thread issues the MMAs, eight warps read the
-// accumulators -- but B holds the whole query group: N = 4 * HI * QPS rows, row
-// (q, blk, h) = query q's head-h codes inside 32-code block blk and zeros elsewhere, so the
-// four K = 32 MMAs of a tile leave every block's exact partial dot product in its own column
-// (multiples of 1/4 below 2^11, exact in fp32) and one query's 4*HI columns are adjacent: one
-// 16-column tensor-memory load serves one query at HI = 4.  Block scales and head weights are
-// applied afterwards in fp32.  The keys (order-preserving uint32 of the score) go to the
-// caller's [T][ld] buffer and into a per-query 2048-bin shared-memory histogram of key >> 21
-// that the top-k selection starts from.
+// plus their block scales through cp.async, one thread issues the MMAs -- but B holds the whole
+// query group: N = 4 * HI * QPS rows, row (q, h, blk) = query q's head-h codes inside 32-code
+// block blk and zeros elsewhere, so the four K = 32 MMAs of a tile leave every block's exact
+// partial dot product in its own column (multiples of 1/4 below 2^11, exact in fp32), one
+// query's 4*HI columns adjacent and the four blocks of a head adjacent.  Sixteen epilogue warps
+// (four per TMEM lane quadrant, each a quarter of the group's queries) read a tile's columns,
+// hand the accumulator back at once, and apply block scales and head weights in fp32, two
+// blocks per packed f32x2 instruction.  The keys (order-preserving uint32 of the score) go to
+// the caller's [T][ld] buffer and into a per-query 2048-bin shared-memory histogram of
+// key >> 21 that the top-k selection starts from.
 #include "kernels.cuh"
 #include "sm100.cuh"
 
@@ -32,7 +33,7 @@ constexpr int kMaxPages = 1024;      // block-table entries one run may span
 constexpr int kRowBytes = 128;       // shared-memory bytes of one entry's 128 codes (16U4 in 16 B)
 constexpr int kPackedRowBytes = 64;  // global bytes of the same codes
 constexpr int kATileBytes = kTile * kRowBytes;
-constexpr int kEpiWarps = 8;         // two per TMEM lane quadrant, alternating tiles
+constexpr int kEpiWarps = 16;        // four per TMEM lane quadrant, a quarter of the queries each
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kProdWarps = 2;
 constexpr int kScaleSlots = 2 * kStages;
@@ -46,7 +47,7 @@ struct PfSmem {
   static constexpr int kA = 0;                                  // kStages x 16 KB, 1024-aligned
   static constexpr int kB = kA + kStages * kATileBytes;         // N x 128 B
   static constexpr int kScale = kB + N * kRowBytes;             // kScaleSlots x 128 x 4 B
-  static constexpr int kQw = kScale + kScaleSlots * kTile * 4;  // f32 [QPS][4][HI] qscale * w
+  static constexpr int kQw = kScale + kScaleSlots * kTile * 4;  // f32 [QPS][HI][4] qscale * w
   static constexpr int kQs = kQw + QPS * 4 * HI * 4;            // f32 [QPS][HI][4] qscale
   static constexpr int kHw = kQs + QPS * HI * 4 * 4;            // f32 [QPS][HI] w
   static constexpr int kPages = kHw + QPS * HI * 4;             // int [kMaxPages]
@@ -60,8 +61,30 @@ struct PfSmem {
 
 }  // namespace
 
+// packed pairs of fp32 (two IEEE operations per instruction)
+__device__ __forceinline__ unsigned long long f2_pack(float lo, float hi) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float f2_sum(unsigned long long v) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return lo + hi;
+}
+__device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsigned long long b, unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ unsigned long long f2_mul(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 template <int HI, int QPS>
-__global__ void __launch_bounds__(kThreads) index_tc_pf_kernel(const __grid_constant__ CUtensorMap tmap_k,
+__global__ void __launch_bounds__(kThreads, 1) index_tc_pf_kernel(const __grid_constant__ CUtensorMap tmap_k,
                                                               IndexParams p, int tiles_per_cta) {
   using L = PfSmem<HI, QPS>;
   constexpr int N = L::N;
@@ -110,7 +133,7 @@ __global__ void __launch_bounds__(kThreads) index_tc_pf_kernel(const __grid_cons
     }
     for (int i = 0; i < kAcc; ++i) {
       mbar_init(bar_accf + 8 * i, 1);
-      mbar_init(bar_acce + 8 * i, 4);
+      mbar_init(bar_acce + 8 * i, kEpiWarps);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -130,10 +153,10 @@ __global__ void __launch_bounds__(kThreads) index_tc_pf_kernel(const __grid_cons
       pages_s[i] = phys;
     }
   } else if (warp < kEpiWarps) {
-    // ---- B operand: row n = qi*V + blk*HI + h; codes of block blk sit in 16-byte chunks 2blk, 2blk+1
+    // ---- B operand: row n = qi*V + h*4 + blk; codes of block blk sit in 16-byte chunks 2blk, 2blk+1
     for (int idx = tid; idx < N * 8; idx += kEpiThreads) {
       const int n = idx >> 3, ch = idx & 7;
-      const int qi = n / V, blk = (n % V) / HI, h = n % HI;
+      const int qi = n / V, h = (n % V) >> 2, blk = n & 3;
       uint2 v = make_uint2(0u, 0u);
       if ((ch >> 1) == blk && qi < qn) {
         const long long qrow = (q0 + qi) * HI + h;
@@ -149,7 +172,7 @@ __global__ void __launch_bounds__(kThreads) index_tc_pf_kernel(const __grid_cons
       const float qsc = qi < qn ? ue8m0_to_f32(p.q_scale[qrow * 4 + blk]) : 0.0f;
       const float w = qi < qn ? (p.head_w ? p.head_w[qrow] : 1.0f) : 0.0f;
       qs_s[idx] = qsc;
-      qw_s[(qi * 4 + blk) * HI + h] = qsc * w;   // a power of two times the head weight: exact
+      qw_s[idx] = qsc * w;   // a power of two times the head weight: exact
       if (blk == 0) hw_s[qi * HI + h] = w;
     }
     if (with_hist)
@@ -205,13 +228,19 @@ __global__ void __launch_bounds__(kThreads) index_tc_pf_kernel(const __grid_cons
     }
     __syncwarp();
   } else {
-    // ---- epilogue: warp w reads TMEM lanes 32*(w%4).. of the tiles i with i % 2 == w / 4,
-    //      64 columns (64 / V queries) at a time
-    const int quad = warp & 3, par = warp >> 2;
+    // ---- epilogue: warp w reads TMEM lanes 32*(w%4).. (its entries) and the columns of
+    //      queries QPW*(w/4) .. QPW*(w/4)+QPW-1 of every tile
+    constexpr int QPW = QPS / 4;                    // queries per warp
+    constexpr int CW = QPW * V;                     // their columns
+    constexpr int kPhases = CW > 32 ? 2 : 1;        // column loads of at most 32 registers
+    constexpr int CWP = CW / kPhases;
+    static_assert(CWP % 16 == 0 && CWP <= 32 && QPW % kPhases == 0, "columns per warp");
+    const int quad = warp & 3, qb = (warp >> 2) * QPW;
     const int row = quad * 32 + lane;
-    constexpr int QC = 64 / V > 0 ? 64 / V : 1;    // queries per 64-column chunk
-    constexpr int CW = QC * V;                      // columns per chunk
-    for (int i = par; i < nt; i += 2) {
+    const int nq_first = (n0 + qb + 1) >> mshift;   // visible entries of the warp's first query
+    uint32_t* keys_row = p.keys_out != nullptr ? p.keys_out + (q0 + qb) * p.ld : nullptr;
+    float* scores_row = p.scores_out != nullptr ? p.scores_out + (q0 + qb) * p.ld : nullptr;
+    for (int i = 0; i < nt; ++i) {
       const int a = i % kAcc;
       bool ok = mbar_wait(bar_accf + 8 * a, (i / kAcc) & 1, p.status, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
@@ -223,45 +252,51 @@ __global__ void __launch_bounds__(kThreads) index_tc_pf_kernel(const __grid_cons
       ksc[1] = __uint_as_float(max((sc << 15) & 0x7F800000u, 0x00400000u));
       ksc[2] = __uint_as_float(max((sc << 7) & 0x7F800000u, 0x00400000u));
       ksc[3] = __uint_as_float(max((sc >> 1) & 0x7F800000u, 0x00400000u));
-      const int j = (t_begin + i) * kTile + row;
-      const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + a * N;
-#pragma unroll 1
-      for (int c0 = 0; c0 < N; c0 += CW) {
-        uint32_t d[CW];
+      const unsigned long long k01 = f2_pack(ksc[0], ksc[1]), k23 = f2_pack(ksc[2], ksc[3]);
+      const int e0 = (t_begin + i) * kTile;
+      const int j = e0 + row;
+      const bool full = e0 + kTile <= nq_first;     // every query of the warp sees the whole tile
 #pragma unroll
-        for (int c16 = 0; c16 < CW / 16; ++c16)
-          tmem_ld16(taddr + c0 + c16 * 16, *reinterpret_cast<uint32_t(*)[16]>(&d[c16 * 16]));
+      for (int ph = 0; ph < kPhases; ++ph) {
+        // this phase's columns into registers; the accumulator goes back after the last phase's load
+        uint32_t d[CWP];
+#pragma unroll
+        for (int c16 = 0; c16 < CWP / 16; ++c16)
+          tmem_ld16(tmem + ((uint32_t)(quad * 32) << 16) + a * N + qb * V + ph * CWP + c16 * 16,
+                    *reinterpret_cast<uint32_t(*)[16]>(&d[c16 * 16]));
         tmem_ld_wait();
-        if (c0 + CW == N) {
-          // every column of this accumulator is in registers: hand it back to the MMA warp
+        if (ph == kPhases - 1) {
           tc_fence_before_sync();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar_acce + 8 * a);
         }
 #pragma unroll
-        for (int qq = 0; qq < QC; ++qq) {
-          const int qi = c0 / V + qq;
+        for (int qp = 0; qp < QPW / kPhases; ++qp) {
+          const int qq = ph * (QPW / kPhases) + qp;
+          const int qi = qb + qq;
           float score;
           if (!p.relu) {
-            // phi = identity: sum over heads inside each block first (every term exact)
-            float tb[4];
+            // phi = identity: per block, the heads' weighted sum, then the block scales (every
+            // term exact); blocks (0, 1) and (2, 3) in packed pairs
+            unsigned long long t01 = 0ull, t23 = 0ull;
 #pragma unroll
-            for (int blk = 0; blk < 4; ++blk) {
-              const float* w = qw_s + (qi * 4 + blk) * HI;
-              float t = 0.0f;
-#pragma unroll
-              for (int h = 0; h < HI; ++h) t = fmaf(__uint_as_float(d[qq * V + blk * HI + h]), w[h], t);
-              tb[blk] = t;
+            for (int h = 0; h < HI; ++h) {
+              const float4 w = *reinterpret_cast<const float4*>(qw_s + (qi * HI + h) * 4);
+              const uint32_t* dh = d + qp * V + h * 4;
+              t01 = f2_fma(f2_pack(__uint_as_float(dh[0]), __uint_as_float(dh[1])), f2_pack(w.x, w.y), t01);
+              t23 = f2_fma(f2_pack(__uint_as_float(dh[2]), __uint_as_float(dh[3])), f2_pack(w.z, w.w), t23);
             }
-            score = fmaf(tb[3], ksc[3], fmaf(tb[2], ksc[2], fmaf(tb[1], ksc[1], tb[0] * ksc[0])));
+            score = f2_sum(f2_fma(t23, k23, f2_mul(t01, k01)));
           } else {
             float sh[HI];
 #pragma unroll
             for (int h = 0; h < HI; ++h) {
-              const float* qs = qs_s + (qi * HI + h) * 4;
-              float acc = 0.0f;
-#pragma unroll
-              for (int blk = 0; blk < 4; ++blk) acc = fmaf(__uint_as_float(d[qq * V + blk * HI + h]), ksc[blk] * qs[blk], acc);
+              const float4 qs = *reinterpret_cast<const float4*>(qs_s + (qi * HI + h) * 4);
+              const uint32_t* dh = d + qp * V + h * 4;
+              float acc = __uint_as_float(dh[0]) * (ksc[0] * qs.x);
+              acc = fmaf(__uint_as_float(dh[1]), ksc[1] * qs.y, acc);
+              acc = fmaf(__uint_as_float(dh[2]), ksc[2] * qs.z, acc);
+              acc = fmaf(__uint_as_float(dh[3]), ksc[3] * qs.w, acc);
               sh[h] = fmaxf(acc, 0.0f) * hw_s[qi * HI + h];
             }
 #pragma unroll
@@ -270,13 +305,12 @@ __global__ void __launch_bounds__(kThreads) index_tc_pf_kernel(const __grid_cons
               for (int h = 0; h < HI; h += 2 * w) sh[h] = sh[h] + sh[h + w];
             score = sh[0];
           }
-          if (qi < qn && j < ((n0 + qi + 1) >> mshift)) {
-            const long long o = (q0 + qi) * p.ld + j;
-            if (p.scores_out != nullptr) {
-              p.scores_out[o] = score;
+          if (qi < qn && (full || j < ((n0 + qi + 1) >> mshift))) {
+            if (scores_row != nullptr) {
+              scores_row[(long long)qq * p.ld + j] = score;
             } else {
               const uint32_t key = score_key(score);
-              p.keys_out[o] = key;
+              keys_row[(long long)qq * p.ld + j] = key;
               if (with_hist) atomicAdd(&hist_s[qi * kTopkHistBins + (key >> 21)], 1u);
             }
           }
