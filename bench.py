@@ -606,37 +606,69 @@ def run_gpu_prefill(args, rank, world, local, wl):
 
 def run_e2e(torch, layer, batch, graph, raw_in, q_in, iq_in, iqs_in, hw_in, out, seq_len, raw_steps, q_steps,
             iq_steps, iqs_steps, hw_steps, args, L, S, flush):
-    """Same step with its inputs coming from pinned host memory and the output read back."""
+    """Same step with its inputs copied from pinned host memory and the output read back, all
+    inside one CUDA graph: the small inputs (new KV rows, indexer queries, lengths) first on the
+    step's stream; the attention queries on a copy stream that only the attention waits for, so
+    that the largest copy runs next to compression and the indexer; the output copied back at
+    the end.  Before each replay the host writes that step's inputs into the pinned staging
+    buffers the graph copies from (outside the timed region, as a producer of the inputs would)."""
+    import long_context_sparse_24_b300 as lcsa
     n = min(args.steps, 8)
-    host_in = [t[:n].cpu().pin_memory() for t in (raw_steps, q_steps, iq_steps, iqs_steps, hw_steps)]
-    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = sum(t[0].numel() * t.element_size() for t in host_in) + seq_len.numel() * 4
-    d2h = out.numel() * out.element_size()
+    host_in = [t[:n].cpu() for t in (raw_steps, q_steps, iq_steps, iqs_steps, hw_steps)]
+    stage = [torch.empty(t.shape[1:], dtype=t.dtype).pin_memory() for t in host_in]
     seq_host = torch.empty(seq_len.shape, dtype=torch.int32).pin_memory()
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in stage) + seq_host.numel() * 4
+    d2h = out.numel() * out.element_size()
+    main = torch.cuda.Stream()
+    copy = torch.cuda.Stream()
+    q_ready = torch.cuda.Event()
+
+    def body():
+        # host -> device through lcs_stage_copy (kernels reading the pinned pages; the copy engine
+        # moves MB-sized host inputs several times slower); device -> host by the copy engine
+        copy.wait_stream(main)
+        lcsa.lcs_stage_copy([(q_in, stage[1])], stream=copy)
+        q_ready.record(copy)
+        lcsa.lcs_stage_copy([(raw_in, stage[0]), (iq_in, stage[2]), (iqs_in, stage[3]), (hw_in, stage[4]),
+                             (seq_len, seq_host)], stream=main)
+        layer.step(batch, raw_in, q_in, out, idx_q_fp4=iq_in, idx_q_scale=iqs_in, head_w=hw_in, stream=main,
+                   q_ready=q_ready)
+        host_out.copy_(out, non_blocking=True)
+        main.wait_stream(copy)
+
     # rewind the state positions: re-run decode positions L+warmup+steps .. (new tokens, same shapes)
     base = L + args.warmup + args.steps + 5
+    seq_host.fill_(base)
+    for k_, t in enumerate(host_in):
+        stage[k_].copy_(t[0])
+    torch.cuda.synchronize()
+    main.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(main):
+        body()                          # eager once (the copy stream and events warm up)
+    main.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=main):
+        body()
     times = []
-    st = torch.cuda.current_stream()
     for s in range(n):
+        for k_, t in enumerate(host_in):
+            stage[k_].copy_(t[s])
         seq_host.fill_(base + s + 1)
         flush.zero_()
+        torch.cuda.synchronize()
         e0 = torch.cuda.Event(enable_timing=True); e1 = torch.cuda.Event(enable_timing=True)
-        e0.record()
-        raw_in.copy_(host_in[0][s], non_blocking=True)
-        q_in.copy_(host_in[1][s], non_blocking=True)
-        iq_in.copy_(host_in[2][s], non_blocking=True)
-        iqs_in.copy_(host_in[3][s], non_blocking=True)
-        hw_in.copy_(host_in[4][s], non_blocking=True)
-        seq_len.copy_(seq_host, non_blocking=True)
-        graph.replay()
-        host_out.copy_(out, non_blocking=True)
-        e1.record()
-        st.synchronize()
+        with torch.cuda.stream(main):
+            e0.record(main)
+            g.replay()
+            e1.record(main)
+        main.synchronize()
         times.append(e0.elapsed_time(e1))
     ms = statistics.mean(times)
     return {"value": round(S / (ms * 1e-3), 1), "unit": UNIT, "ms_per_step": round(ms, 4),
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": n,
-            "api": "layer.step body (csa_compress, csa_index_topk, csa_attend, lcs_window_commit) as one CUDA graph"}
+            "api": "Layer.step (csa_compress, csa_attend_window | csa_index_topk, csa_attend_topk) with the "
+                   "host copies, one CUDA graph per step"}
 
 
 # ---------------------------------------------------------------------------------------------

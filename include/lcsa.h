@@ -252,6 +252,17 @@ lcs_status hca_attend(const lcs_batch* batch, const void* q, int32_t heads, int3
                       float softmax_scale, void* out, float* out_lse, void* workspace,
                       size_t workspace_bytes, int32_t* dev_status, void* stream);
 
+/* --- staging copies (serving input/output; not a step of the method) --------------------------
+ * Copies n <= 8 buffers, bytes[i] bytes from src[i] to dst[i], with one kernel on `stream` whose
+ * threads load and store the bytes themselves.  Each pointer may be device memory or pinned host
+ * memory (cudaHostAlloc / cudaHostRegister; it is used through its device alias), so a step's
+ * inputs can be read straight from pinned host pages: for MB-sized inputs this is several times
+ * faster than the copy engine on B300.  Buffers must not overlap.  16-byte aligned pairs move in
+ * 16-byte pieces.  Errors: LCS_ERR_UNSUPPORTED for n > 8, LCS_ERR_INVALID_ARG for a NULL or
+ * pageable pointer of a non-empty copy; nothing is launched then.  Capturable in a CUDA graph
+ * (the pointer lookups happen on the host at call time). */
+lcs_status lcs_stage_copy(int32_t n, void* const* dst, const void* const* src, const size_t* bytes, void* stream);
+
 /* --- library information -------------------------------------------------------------------- */
 int32_t lcs_abi_version(void);
 const char* lcs_status_string(int32_t status);

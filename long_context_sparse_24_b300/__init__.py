@@ -70,6 +70,7 @@ class lcs_index_keys(ctypes.Structure):
 P = ctypes.POINTER
 _SIGS = {
     "lcs_abi_version": (c_i32, []),
+    "lcs_stage_copy": (c_i32, [c_i32, c_vp, c_vp, c_vp, c_vp]),
     "lcs_status_string": (ctypes.c_char_p, [c_i32]),
     "lcs_device_check": (c_i32, []),
     "csa_compress": (c_i32, [P(lcs_batch), c_vp, P(lcs_compressor), P(lcs_state), P(lcs_rows), P(lcs_paging),
@@ -226,6 +227,21 @@ def hca_compress(batch: Batch, raw, comp: Compressor, state: State, entries: Row
     b, c, s, e, p = batch.c(), comp.c(), state.c(), entries.c(), paging.c()
     _check(_lib.hca_compress(ctypes.byref(b), _ptr(raw), ctypes.byref(c), ctypes.byref(s), ctypes.byref(e),
                              ctypes.byref(p), _ptr(dev_status), _stream(stream)), "hca_compress")
+
+
+def lcs_stage_copy(pairs, stream=None) -> None:
+    """Copy each (dst, src) tensor pair (device or pinned host, same byte size) with one kernel."""
+    n = len(pairs)
+    dst = (c_vp * max(n, 1))(*[_ptr(d) for d, _ in pairs])
+    src = (c_vp * max(n, 1))(*[_ptr(s_) for _, s_ in pairs])
+    nbytes = []
+    for d, s_ in pairs:
+        nb = s_.numel() * s_.element_size()
+        if d.numel() * d.element_size() != nb:
+            raise ValueError("lcs_stage_copy: destination and source sizes differ")
+        nbytes.append(nb)
+    sizes = (c_sz * max(n, 1))(*nbytes)
+    _check(_lib.lcs_stage_copy(n, dst, src, sizes, _stream(stream)), "lcs_stage_copy")
 
 
 def lcs_window_commit(batch: Batch, state: State, dev_status=None, stream=None) -> None:

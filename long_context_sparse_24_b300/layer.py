@@ -99,14 +99,19 @@ class Layer:
             lcs_window_commit(batch, self.cache.state, self.status, stream)
 
     def step(self, batch: Batch, raw_new: torch.Tensor, q: torch.Tensor, out: torch.Tensor,
-             lse: Optional[torch.Tensor] = None, idx_q_fp4=None, idx_q_scale=None, head_w=None, stream=None) -> None:
+             lse: Optional[torch.Tensor] = None, idx_q_fp4=None, idx_q_scale=None, head_w=None, stream=None,
+             q_ready: Optional[torch.cuda.Event] = None) -> None:
         """One pass of the hot path for the batch's new tokens.  CSA: compression and then the
         window part of attention (side stream) run next to the indexer top-k; the top-k part of
-        attention, with the merge, waits for both."""
+        attention, with the merge, waits for both.  q_ready: an event the attention waits for
+        before reading q (q still arriving, e.g. copied from the host on another stream), so
+        that compression and the indexer need not wait for it."""
         main = stream if stream is not None else torch.cuda.current_stream()
         if self.kind == "csa":
             self.side.wait_stream(main)
             self.compress(batch, raw_new, self.side)
+            if q_ready is not None:
+                self.side.wait_event(q_ready)
             csa_attend_window(batch, q, self.heads, self.top_k, self.m, self.cache.entries, self.cache.paging,
                               self.cache.state, self.scale, self.attend_ws, self.attend_ws_bytes, self.status,
                               self.side)
@@ -117,5 +122,7 @@ class Layer:
                             self.attend_ws_bytes, self.status, main)
         else:
             self.compress(batch, raw_new, main)
+            if q_ready is not None:
+                main.wait_event(q_ready)
             self.attend(batch, q, out, lse, main)
         self.commit(batch, main)

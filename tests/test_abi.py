@@ -81,6 +81,18 @@ def test_host_validation_without_gpu():
                         0x3000, None, None, 0, None, None) == 1
 
 
+def test_stage_copy_host_validation():
+    import long_context_sparse_24_b300 as lcsa
+    L = lcsa._lib
+    vp, sz = ctypes.c_void_p, ctypes.c_size_t
+    nine = (vp * 9)(*([0x1000] * 9))
+    assert L.lcs_stage_copy(9, nine, nine, (sz * 9)(*([16] * 9)), None) == 4      # more than 8 copies
+    assert L.lcs_stage_copy(0, None, None, None, None) == 0                      # nothing to copy
+    assert L.lcs_stage_copy(1, None, None, None, None) == 1                      # missing lists
+    assert L.lcs_stage_copy(1, (vp * 1)(None), (vp * 1)(0x1000), (sz * 1)(16), None) == 1   # NULL destination
+    lcsa.lcs_stage_copy([], stream=0)                                             # binding: empty list
+
+
 def test_workspace_sizes():
     import long_context_sparse_24_b300 as lcsa
     b = lcsa.lcs_batch(32, 0x1000, 0x2000, 32, 1, 131072)

@@ -355,3 +355,27 @@ def test_attend_matches_oracle(kind, lengths, new, heads, dim, fmt, m, k):
 ])
 def test_attend_window_then_topk_equals_one_call(lengths, new, heads, dim, fmt, k):
     _attend_case("csa", lengths, new, heads, dim, fmt, 4, k, split=True)
+
+
+# ---------------------------------------------------------------------------------------- staging
+
+def test_stage_copy_pinned_and_device():
+    """lcs_stage_copy: pinned host -> device, device -> pinned host and device -> device in one
+    launch, aligned and unaligned buffers, odd sizes; bytes equal."""
+    g = torch.Generator().manual_seed(5)
+    sizes = [2 * 1024 * 1024, 1000003, 17, 4096]
+    host = [torch.randint(0, 256, (n,), dtype=torch.uint8, generator=g).pin_memory() for n in sizes]
+    dev = [torch.zeros(n + 1, dtype=torch.uint8, device=DEV) for n in sizes]
+    pairs = [(dev[0][:sizes[0]], host[0]), (dev[1][1:], host[1]), (dev[2][:17], host[2]), (dev[3][:4096], host[3])]
+    lcsa.lcs_stage_copy(pairs)
+    torch.cuda.synchronize()
+    for (d, h) in pairs:
+        assert torch.equal(d.cpu(), h)
+    back = [torch.zeros(n, dtype=torch.uint8).pin_memory() for n in sizes[:2]]
+    other = torch.zeros(sizes[2], dtype=torch.uint8, device=DEV)
+    lcsa.lcs_stage_copy([(back[0], dev[0][:sizes[0]]), (back[1], dev[1][1:]), (other, dev[2][:17])])
+    torch.cuda.synchronize()
+    assert torch.equal(back[0], host[0]) and torch.equal(back[1], host[1])
+    assert torch.equal(other.cpu(), host[2])
+    with pytest.raises(lcsa.LcsError):
+        lcsa.lcs_stage_copy([(dev[2][:17], torch.zeros(17, dtype=torch.uint8))])   # pageable host memory
