@@ -66,7 +66,9 @@ typedef enum {
 } lcs_status;
 
 enum { LCS_ROW_BF16 = 0, LCS_ROW_FP8_SPLIT = 1 };
-enum { LCS_INDEX_RELU = 1 }; /* flags of csa_index_topk: phi = ReLU instead of identity     */
+/* flags of csa_index_topk: phi = ReLU instead of identity; run only the scoring or only the
+ * selection phase (see csa_index_topk) */
+enum { LCS_INDEX_RELU = 1, LCS_INDEX_SCORE_ONLY = 2, LCS_INDEX_SELECT_ONLY = 4 };
 
 /* A batch: num_seqs sequences that each receive new tokens in this call (a prefill chunk,
  * one decode token, or several speculative tokens).  Sequence b holds seq_len[b] raw tokens
@@ -172,7 +174,14 @@ lcs_status lcs_window_commit(const lcs_batch* batch, const lcs_state* state, int
  *   q_fp4   device uint8[total_new][heads][rank/2]    q_scale device uint8[total_new][heads][rank/32]
  *   head_w  device f32[total_new][heads] or NULL (all 1)
  *   heads in {1, 2, 4, 8}; rank in {64, 128}; 1 <= k <= 4096.
- * Workspace: device, >= lcs_index_topk_workspace(batch, m, k) bytes, 256-byte aligned. */
+ * Workspace: device, >= lcs_index_topk_workspace(batch, m, k) bytes, 256-byte aligned.
+ * Phases: a call runs the scoring phase (score keys and per-query histograms into the workspace)
+ * and then the selection phase (out_idx, out_cnt).  With LCS_INDEX_SCORE_ONLY it runs only the
+ * first, with LCS_INDEX_SELECT_ONLY only the second, which reads what an earlier scoring call
+ * with the same batch, m and workspace left there (it must be ordered after it: same stream or an
+ * event); the pair gives exactly the result of one call.  Both flags at once: LCS_ERR_INVALID_ARG.
+ * The split lets other work (e.g. the window part of attention) run next to the selection, which
+ * occupies one CTA per query. */
 size_t lcs_index_topk_workspace(const lcs_batch* batch, int32_t m, int32_t k);
 lcs_status csa_index_topk(const lcs_batch* batch, const uint8_t* q_fp4, const uint8_t* q_scale,
                           const float* head_w, int32_t heads, const lcs_index_keys* keys,

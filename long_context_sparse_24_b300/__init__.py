@@ -18,6 +18,8 @@ LIB_PATH = os.path.join(_HERE, "liblcsa.so")
 LCS_ROW_BF16 = 0
 LCS_ROW_FP8_SPLIT = 1
 LCS_INDEX_RELU = 1
+LCS_INDEX_SCORE_ONLY = 2
+LCS_INDEX_SELECT_ONLY = 4
 WINDOW = 128
 ROPE_DIMS = 64
 BLOCK_TOKENS = 128

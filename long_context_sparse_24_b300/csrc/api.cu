@@ -365,8 +365,10 @@ lcs_status csa_index_topk(const lcs_batch* batch, const uint8_t* q_fp4, const ui
   lcs_status s = index_common(batch, q_fp4, q_scale, heads, keys, paging, m, p);
   if (s != LCS_OK) return s;
   if (k < 1 || k > 4096) return LCS_ERR_UNSUPPORTED;
-  if ((flags & ~LCS_INDEX_RELU) != 0) return LCS_ERR_INVALID_ARG;
-  if (out_idx == nullptr || out_cnt == nullptr) return LCS_ERR_INVALID_ARG;
+  if ((flags & ~(LCS_INDEX_RELU | LCS_INDEX_SCORE_ONLY | LCS_INDEX_SELECT_ONLY)) != 0) return LCS_ERR_INVALID_ARG;
+  const bool score_only = (flags & LCS_INDEX_SCORE_ONLY) != 0, select_only = (flags & LCS_INDEX_SELECT_ONLY) != 0;
+  if (score_only && select_only) return LCS_ERR_INVALID_ARG;
+  if (!score_only && (out_idx == nullptr || out_cnt == nullptr)) return LCS_ERR_INVALID_ARG;
   const size_t need = lcs_index_topk_workspace(batch, m, k);
   if (workspace == nullptr || workspace_bytes < need) return LCS_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return LCS_ERR_ALIGNMENT;
@@ -380,11 +382,14 @@ lcs_status csa_index_topk(const lcs_batch* batch, const uint8_t* q_fp4, const ui
   p.status = dev_status;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int max_entries = batch->max_seq_len / m;
-  // the per-query histograms accumulate with atomics: clear them first
-  cudaError_t e = cudaMemsetAsync(ws + w.hist, 0, w.total - 256 - w.hist, st);
-  if (e != cudaSuccess) return LCS_ERR_CUDA;
-  e = launch_index(p, keys->rank, batch->max_new, max_entries, st);
-  if (e != cudaSuccess) return LCS_ERR_CUDA;
+  cudaError_t e = cudaSuccess;
+  if (!select_only) {
+    // the per-query histograms accumulate with atomics: clear them first
+    e = cudaMemsetAsync(ws + w.hist, 0, w.total - 256 - w.hist, st);
+    if (e != cudaSuccess) return LCS_ERR_CUDA;
+    e = launch_index(p, keys->rank, batch->max_new, max_entries, st);
+    if (e != cudaSuccess || score_only) return from_cuda(e);
+  }
   e = launch_topk_select(p.keys_out, p.hist, p.ld, batch->cu_new, batch->seq_len, batch->num_seqs, batch->max_new,
                          m, k, out_idx, out_cnt, st);
   return from_cuda(e);

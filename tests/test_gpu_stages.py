@@ -210,6 +210,17 @@ def test_index_scores_exact_and_topk_sets(heads, rank, relu, scaled, new, length
             assert np.array_equal(oi[qi, :len(sel)], sel), f"top-k seq {b} query {i}"
             assert np.all(oi[qi, len(sel):] == -1)
             qi += 1
+    # the scoring and selection phases as two calls give the same bits
+    idx2 = torch.full((T, k), -9, dtype=torch.int32, device=DEV)
+    cnt2 = torch.full((T,), -9, dtype=torch.int32, device=DEV)
+    ws2 = workspace(wsb)
+    lcsa.csa_index_topk(batch, q_fp4, q_sc, hw, heads, cache.keys, cache.paging, m, k,
+                        flags | lcsa.LCS_INDEX_SCORE_ONLY, None, None, ws2, wsb, st)
+    lcsa.csa_index_topk(batch, q_fp4, q_sc, hw, heads, cache.keys, cache.paging, m, k,
+                        flags | lcsa.LCS_INDEX_SELECT_ONLY, idx2, cnt2, ws2, wsb, st)
+    torch.cuda.synchronize()
+    assert_status_ok(st)
+    assert np.array_equal(idx2.cpu().numpy(), oi) and np.array_equal(cnt2.cpu().numpy(), oc)
 
 
 def test_topk_ties_take_lowest_index():
