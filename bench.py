@@ -29,11 +29,14 @@ import synth  # noqa: E402
 
 WL = synth.CONFIGS["csa_decode"]
 METRIC = "CSA/HCA attention queries/s at 128K-1M ctx"
-# DRAM bytes (read + write) per step of the two attention launches and of the indexer (scorer +
-# select), from one ncu capture of this workload (dram__bytes_read.sum + dram__bytes_write.sum) on
-# the current kernels; set to None whenever those kernels change until they are measured again.
-ATTEND_DRAM_BYTES = int(14.503e6 + 0.000256e6 + 4.550e6)
-INDEX_DRAM_BYTES = int(71.510e6 + 1.821e6 + 4.500e6)
+# DRAM bytes (read + write) per step of the attention (window launch + top-k launch + merge) and of
+# the indexer (scorer + select), from one ncu capture of this workload (dram__bytes_read.sum +
+# dram__bytes_write.sum; profiles/csa_decode_32x128k_launch_list.md) on the current kernels; set
+# to None whenever those kernels change until they are measured again.  ncu flushes L2 before each
+# captured kernel, so the merge's 10.58 MB are partials re-read from DRAM that the timed step
+# finds in L2.
+ATTEND_DRAM_BYTES = 4545024 + 14503424 + 10579968
+INDEX_DRAM_BYTES = 71511808 + 76800 + 4501760
 UNIT = "queries/s"
 
 
@@ -46,8 +49,13 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="csa_decode",
                     choices=["csa_decode", "hca_decode", "mixed_decode", "csa_prefill"],
-                    help="csa_decode is the headline line; the others measure the HCA decode and the mixed "
-                         "ragged multi-layer workloads with the same timing rules")
+                    help="csa_decode is the headline line; the others measure the HCA decode, the mixed "
+                         "ragged multi-layer and the CSA prefill workloads with the same timing rules")
+    ap.add_argument("--ctx-len", type=int, default=None,
+                    help="csa_prefill only: cached tokens instead of the workload's 1,048,576 (a smaller case of "
+                         "the same kernels, for profiler captures; the line then names the changed workload)")
+    ap.add_argument("--new-tokens", type=int, default=None,
+                    help="csa_prefill only: new tokens (queries) instead of the workload's 16,384")
     return ap.parse_args()
 
 
@@ -780,7 +788,14 @@ def main():
     assert args.warmup >= 3, "at least 3 warm-up steps"
     if args.workload != "csa_decode":
         runner = run_gpu_prefill if args.workload == "csa_prefill" else run_gpu_stack
-        res = runner(args, rank, world, local, synth.CONFIGS[args.workload])
+        wl = synth.CONFIGS[args.workload]
+        if args.workload == "csa_prefill" and (args.ctx_len is not None or args.new_tokens is not None):
+            import dataclasses
+            ctx = args.ctx_len if args.ctx_len is not None else wl.ctx_len
+            new_ = args.new_tokens if args.new_tokens is not None else wl.new_tokens
+            wl = dataclasses.replace(wl, name=f"csa_prefill_{ctx}_plus_{new_}_h{wl.heads}_d{wl.dim}", ctx_len=ctx,
+                                     new_tokens=new_)
+        res = runner(args, rank, world, local, wl)
         if rank == 0:
             value = res["per_rank_queries"] * world / (res["ms"] * 1e-3)
             print(json.dumps({"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
