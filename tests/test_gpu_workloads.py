@@ -246,16 +246,16 @@ def _fill_context(lay, seed, li, lengths, dim, chunk=16384):
     del raw_chunk
 
 
-def _check_csa_query(lay, seed, s_, t, row, q_np, qc, qs, hw, w, b, out_row, label):
+def _check_csa_query(lay, seed, s_, t, row, q_np, qc, qs, hw, w, b, out_row, label, li=0):
     m, k, D = lay.m, lay.top_k, lay.dim
     n = oracle.visible_entries(t, m)
-    kc, ks = _keys_np(seed, 0, s_, n, lay.index_rank)
+    kc, ks = _keys_np(seed, li, s_, n, lay.index_rank)
     sel = oracle.topk_select(oracle.index_scores(qc, qs, hw, kc, ks)[0, :n], k)
     assert int(lay.topk_cnt[row].item()) == len(sel), label
     assert np.array_equal(lay.topk_idx[row, :len(sel)].cpu().numpy(), sel), label
-    ent = oracle.quantize_rows(_entries_from_spans(seed, 0, s_, sel, m, True, w, b, D), "fp8_split")["deq"]
+    ent = oracle.quantize_rows(_entries_from_spans(seed, li, s_, sel, m, True, w, b, D), "fp8_split")["deq"]
     lo = max(0, t - 127)
-    win = oracle.quantize_rows(_raw_f64(seed, 0, s_, lo, t + 1 - lo, D), "fp8_split")["deq"]
+    win = oracle.quantize_rows(_raw_f64(seed, li, s_, lo, t + 1 - lo, D), "fp8_split")["deq"]
     o, _ = oracle.attend(bits_to_f64(q_np), np.concatenate([ent, win]), lay.scale)
     check_outputs(out_row, o, label)
 
@@ -354,23 +354,86 @@ def test_hca_decode_64x1m_full_size_sampled():
     assert int(lay.status.item()) == 0
     o = out.float().cpu().numpy().astype(np.float64)
     w64, b64 = w.astype(np.float64), b.astype(np.float64)
-    t = L
-    n = oracle.visible_entries(t, m)
-    chunk = 65536
-    raw_dev = torch.empty((chunk, D), dtype=torch.bfloat16, device=DEV)
     for s_ in (0, S - 1):
-        # the sequence's raw rows from the device-side generator, spot-checked against numpy
-        ent = np.empty((n, D))
-        for c0 in range(0, n * m, chunk):
-            sg.normal_bf16(raw_dev, seed, synth.tensor_id(synth.RAW, 0, s_), c0 * D)
-            bits = raw_dev.view(torch.int16).cpu().numpy().view(np.uint16)
-            if c0 in (0, 7 * chunk):
-                ref_bits = synth.normal_bf16(seed, synth.tensor_id(synth.RAW, 0, s_), c0 * D, 4096).reshape(8, D)
-                assert np.array_equal(bits[:8], ref_bits)
-            ent[c0 // m:(c0 + chunk) // m] = oracle.compress_blocked(bits_to_f64(bits), w64, b64, m, False)
-        ent_q = oracle.quantize_rows(ent, "fp8_split")["deq"]
-        win = oracle.quantize_rows(_raw_f64(seed, 0, s_, t - 127, 128, D), "fp8_split")["deq"]
-        ref, _ = oracle.attend(bits_to_f64(qs_np[s_]), np.concatenate([ent_q, win]), lay.scale)
+        ref = _hca_dense_ref(seed, 0, s_, L, m, D, w64, b64, bits_to_f64(qs_np[s_]), lay.scale)
         check_outputs(o[s_], ref, f"seq {s_}")
-    del lay, out, raw_dev
+    del lay, out
+    torch.cuda.empty_cache()
+
+
+def _hca_dense_ref(seed, li, s_, t, m, D, w64, b64, q64, scale, chunk=65536):
+    """Oracle HCA output of the query at position t: every entry compressed from the sequence's
+    raw rows (drawn by the device-side generator in chunks, spot-checked against numpy), then
+    the window rows."""
+    n = oracle.visible_entries(t, m)
+    ent = np.empty((n, D))
+    raw_dev = torch.empty((chunk, D), dtype=torch.bfloat16, device=DEV)
+    for c0 in range(0, n * m, chunk):
+        sg.normal_bf16(raw_dev, seed, synth.tensor_id(synth.RAW, li, s_), c0 * D)
+        bits = raw_dev.view(torch.int16).cpu().numpy().view(np.uint16)
+        if c0 in (0, 7 * chunk):
+            ref_bits = synth.normal_bf16(seed, synth.tensor_id(synth.RAW, li, s_), c0 * D, 8 * D).reshape(8, D)
+            assert np.array_equal(bits[:8], ref_bits)
+        rows = min(chunk, n * m - c0)
+        ent[c0 // m:(c0 + rows) // m] = oracle.compress_blocked(bits_to_f64(bits[:rows]), w64, b64, m, False)
+    ent_q = oracle.quantize_rows(ent, "fp8_split")["deq"]
+    lo = max(0, t - 127)
+    win = oracle.quantize_rows(_raw_f64(seed, li, s_, lo, t + 1 - lo, D), "fp8_split")["deq"]
+    ref, _ = oracle.attend(q64, np.concatenate([ent_q, win]), scale)
+    return ref
+
+
+def test_mixed_decode_16x8_layers_full_size_sampled():
+    """16 sequences of log-uniform lengths in [4096, 1M), 8 layers alternating CSA (k = 1024) and
+    HCA on one shared block table, one decode step through HybridStack; the longest and the
+    shortest sequence checked on layer 0 (CSA: top-k bit-exact, output) and layer 1 (HCA)."""
+    from long_context_sparse_24_b300.model import HybridStack
+    wl = synth.CONFIGS["mixed_decode"]
+    seed, S, H, D, k, hi, r = wl.seed, wl.num_seqs, wl.heads, wl.dim, wl.top_k, wl.index_heads, wl.index_rank
+    lengths = [int(x) for x in synth.mixed_lengths(seed, S)]
+    cap = max(lengths) + 256
+    stack = HybridStack(wl.layers, S, cap, H, D, lcsa.LCS_ROW_FP8_SPLIT, top_k=k, index_heads=hi, index_rank=r,
+                        device=DEV)
+    params = []
+    for li, lay in enumerate(stack.layers):
+        w, b = _comp_params(seed, li, D, lay.m, lay.overlap)
+        lay.set_compressor(torch.from_numpy(w).to(DEV), torch.from_numpy(b).to(DEV))
+        params.append((w.astype(np.float64), b.astype(np.float64)))
+        _fill_context(lay, seed, li, lengths, D, chunk=8192)
+        if lay.kind == "csa":
+            for s_ in range(S):
+                _fill_keys(lay, seed, li, s_, (lengths[s_] + 1) // 4, r)
+    raw_new, q_in, outs, iq, iqs, ihw, ins = [], [], [], [], [], [], []
+    for li, lay in enumerate(stack.layers):
+        rn = torch.empty((S, D), dtype=torch.bfloat16, device=DEV)
+        for s_ in range(S):
+            sg.normal_bf16(rn[s_], seed, synth.tensor_id(synth.RAW, li, s_), lengths[s_] * D)
+        raw_new.append(rn)
+        x = [_query_inputs(seed, li, s_, lengths[s_], 1, H, D, hi, r) for s_ in range(S)]
+        ins.append(x)
+        q_in.append(to_dev_bf16_bits(np.concatenate([v[0] for v in x])))
+        outs.append(torch.empty((S, H, D), dtype=torch.bfloat16, device=DEV))
+        if lay.kind == "csa":
+            iq.append(_dev_u8(synth.pack_e2m1(np.concatenate([v[1] for v in x]))))
+            iqs.append(_dev_u8(np.concatenate([v[2] for v in x])))
+            ihw.append(torch.from_numpy(np.concatenate([v[3] for v in x])).to(DEV))
+        else:
+            iq.append(None); iqs.append(None); ihw.append(None)
+    stack.step(stack.batch([L + 1 for L in lengths], [1] * S), raw_new, q_in, outs, iq, iqs, ihw)
+    torch.cuda.synchronize()
+    assert stack.status == [0] * wl.layers
+    picks = (int(np.argmax(lengths)), int(np.argmin(lengths)))
+    for li in (0, 1):
+        lay = stack.layers[li]
+        o = outs[li].float().cpu().numpy().astype(np.float64)
+        w64, b64 = params[li]
+        for s_ in picks:
+            q, qc, qs, hw = ins[li][s_]
+            if lay.kind == "csa":
+                _check_csa_query(lay, seed, s_, lengths[s_], s_, q[0], qc, qs, hw, w64, b64, o[s_],
+                                 f"layer {li} seq {s_}", li=li)
+            else:
+                ref = _hca_dense_ref(seed, li, s_, lengths[s_], lay.m, D, w64, b64, bits_to_f64(q[0]), lay.scale)
+                check_outputs(o[s_], ref, f"layer {li} seq {s_}")
+    del stack, outs
     torch.cuda.empty_cache()
