@@ -66,6 +66,37 @@ def dist_env():
     return rank, world, local
 
 
+# ---- multi-rank logic: every rank serves its own sequences (weak scaling, no data-path
+#      collective); the ranks meet only at a barrier before the timed steps and to take the
+#      slowest rank's step time
+
+def rank_seed(seed: int, rank: int) -> int:
+    """Seed of a rank's own sequences (independent problems per rank)."""
+    return seed + 1000 * rank
+
+
+def barrier(world: int) -> None:
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(ms: float, world: int, device=None) -> float:
+    """The slowest rank's step time (every rank gets it)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(per_rank_units: float, world: int, ms: float) -> float:
+    """Whole-job throughput: the units all ranks processed per step over the slowest step time."""
+    return per_rank_units * world / (ms * 1e-3)
+
+
 def workload_config(extra=None):
     cfg = {"workload": WL.name, "num_seqs": WL.num_seqs, "ctx_len": WL.ctx_len, "new_tokens_per_seq": 1,
            "heads": WL.heads, "kv_dim": WL.dim, "row_format": "fp8_e4m3(448)+bf16_rope(64)+f32_scale",
@@ -164,7 +195,7 @@ def run_gpu(args, rank, world, local):
     n_stage = 5                              # extra replays of an instrumented graph (stage times)
     steps_total = args.warmup + args.steps + n_stage
     cap = L + 128 * math.ceil((steps_total + 1) / 128) + 256
-    seed = WL.seed + 1000 * rank            # each rank serves its own sequences
+    seed = rank_seed(WL.seed, rank)         # each rank serves its own sequences
     layer = Layer("csa", S, cap, H, D, lcsa.LCS_ROW_FP8_SPLIT, m, top_k=k, index_heads=Hi, index_rank=r,
                   max_new=1, device=dev)
     # compressor parameters (w ~ N(0,1)/16, bias ~ N(0,1)/2)
@@ -264,9 +295,7 @@ def run_gpu(args, rank, world, local):
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps_total)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps_total)]
     stage_ms = []
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
+    barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         for s in range(1, timed_end):
@@ -288,11 +317,7 @@ def run_gpu(args, rank, world, local):
         status_ok = False
     per_step = [starts[s].elapsed_time(ends[s]) for s in range(args.warmup, timed_end)]
     ms = statistics.mean(per_step)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, dev)
     stages = ([statistics.mean(x[i] for x in stage_ms) for i in range(len(STAGES))] if stage_ms
               else [float("nan")] * len(STAGES))
     stage = dict(zip(STAGES, stages))
@@ -352,7 +377,7 @@ def run_gpu_stack(args, rank, world, local, wl):
         raise SystemExit("liblcsa needs a compute-capability 10.3 GPU")
     S, H, D = wl.num_seqs, wl.heads, wl.dim
     Hi, r, k = wl.index_heads, wl.index_rank, wl.top_k
-    seed = wl.seed + 1000 * rank
+    seed = rank_seed(wl.seed, rank)
     if wl.kind == "mixed":
         lengths = [int(x) for x in synth.mixed_lengths(seed, S)]
         n_layers, first = wl.layers, "csa"
@@ -436,9 +461,7 @@ def run_gpu_stack(args, rank, world, local, wl):
         step_body()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps_total)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps_total)]
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
+    barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         for st in range(1, steps_total):
@@ -450,11 +473,7 @@ def run_gpu_stack(args, rank, world, local, wl):
         torch.cuda.synchronize()
     status_ok = all(v == 0 for v in stack.status)
     ms = statistics.mean(starts[st].elapsed_time(ends[st]) for st in range(args.warmup, steps_total))
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, dev)
     # ---- whole-step algorithmic bytes (every layer is HBM-bound): CSA: 68 B per visible entry
     #      (indexer) + (k + 128) rows of 580 B; HCA: (visible entries + 128) rows of 580 B; both:
     #      query and output H x D BF16 per sequence
@@ -506,7 +525,7 @@ def run_gpu_prefill(args, rank, world, local, wl):
         raise SystemExit("liblcsa needs a compute-capability 10.3 GPU")
     L, T, H, D = wl.ctx_len, wl.new_tokens, wl.heads, wl.dim
     Hi, r, k, m = wl.index_heads, wl.index_rank, wl.top_k, wl.m
-    seed = wl.seed + 1000 * rank
+    seed = rank_seed(wl.seed, rank)
     cap = L + T + 256
     layer = Layer("csa", 1, cap, H, D, lcsa.LCS_ROW_FP8_SPLIT, m, top_k=k, index_heads=Hi, index_rank=r,
                   max_new=T, device=dev)
@@ -549,6 +568,7 @@ def run_gpu_prefill(args, rank, world, local, wl):
     n_tot = args.warmup + args.steps
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(n_tot)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(n_tot)]
+    barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         for st in range(n_tot):
@@ -558,11 +578,7 @@ def run_gpu_prefill(args, rank, world, local, wl):
             ends[st].record()
         torch.cuda.synchronize()
     ms = statistics.mean(starts[st].elapsed_time(ends[st]) for st in range(args.warmup, n_tot))
-    if world > 1:
-        import torch.distributed as dist
-        t_ = torch.tensor([ms], device=dev)
-        dist.all_reduce(t_, op=dist.ReduceOp.MAX)
-        ms = float(t_.item())
+    ms = max_over_ranks(ms, world, dev)
     # ---- per-stage device time: the step's calls one after another on one stream, untimed above
     cur = torch.cuda.current_stream()
     names = ["compress", "index_topk", "attend", "window_commit"]
@@ -797,7 +813,7 @@ def main():
                                      new_tokens=new_)
         res = runner(args, rank, world, local, wl)
         if rank == 0:
-            value = res["per_rank_queries"] * world / (res["ms"] * 1e-3)
+            value = job_value(res["per_rank_queries"], world, res["ms"])
             print(json.dumps({"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
                               "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(res["ms"], 5),
                               "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -808,8 +824,7 @@ def main():
         return
     res = run_gpu(args, rank, world, local)
     if rank == 0:
-        S_all = res["per_rank_queries"] * world
-        value = S_all / (res["ms"] * 1e-3)
+        value = job_value(res["per_rank_queries"], world, res["ms"])
         line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": round(res["ms"], 5), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "fp8/fp4 storage, bf16/f16 MMA, fp32 accumulate",
