@@ -244,9 +244,10 @@ lcs_status csa_attend(const lcs_batch* batch, const void* q, int32_t heads, cons
  * Arguments as for csa_attend (the window call needs no top-k list).  Both calls must get the same
  * batch, heads, k, m, row sets and workspace, and the window call must complete before the top-k
  * call's merge starts (same stream, or an event).  csa_attend_window + csa_attend_topk give
- * exactly the bits of csa_attend.  When the library does not compute the window part apart (see
- * lcs_attend_workspace: shapes outside the tensor-core plan), csa_attend_window launches nothing
- * and csa_attend_topk computes everything. */
+ * exactly the bits of csa_attend.  The library computes the window part apart only for D = 512
+ * FP8-split rows, up to 128 heads, k <= 2048 and at most half as many (query, 64-head group)
+ * pairs as the GPU has SMs; otherwise (other shapes, or runs of queries that fill the GPU by
+ * themselves) csa_attend_window launches nothing and csa_attend_topk computes everything. */
 lcs_status csa_attend_window(const lcs_batch* batch, const void* q, int32_t heads, int32_t k, int32_t m,
                              const lcs_rows* entries, const lcs_paging* paging, const lcs_state* state,
                              float softmax_scale, void* workspace, size_t workspace_bytes, int32_t* dev_status,
