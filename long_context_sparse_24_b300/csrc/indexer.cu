@@ -354,6 +354,9 @@ __global__ void __launch_bounds__(kSelThreads, 2) topk_select_kernel(const uint3
   bool overflow = false;
   for (int c0 = 0; c0 < N; c0 += kChunkKeys) {
     const int j0 = c0 + tid * kKPT;
+    // the next chunk toward L2 while this one is scanned (long prefill rows are not L2-resident)
+    if (j0 + kChunkKeys + kKPT <= N)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(src + j0 + kChunkKeys) : "memory");
     uint32_t u[kKPT];
     if (j0 + kKPT <= N) {
       const uint4* v = reinterpret_cast<const uint4*>(src + j0);
