@@ -82,9 +82,12 @@ SplitPlan plan_splits(const lcs_batch* b, int heads, int dim, int max_rows, bool
       const int tps = (tiles + es - 1) / es;
       return SplitPlan{(tiles + tps - 1) / tps + 1, 128 * tps, 1, (tiles + tps - 1) / tps, 1};
     }
+    // one list per query: cut it into runs of tps tiles so that all (query, head group) runs
+    // together come to about one tile load per SM (the last run of a query may be shorter;
+    // CTAs start in split order, so the short runs fill the SMs the long ones leave)
     const int tiles = std::max(1, (max_rows + 127) / 128);
-    const int sp = std::min(tiles, per_query);
-    const int tps = (tiles + sp - 1) / sp;
+    const long long units = ctas * tiles;
+    const int tps = (int)std::min<long long>(tiles, std::max<long long>(1, (units + num_sms() - 1) / num_sms()));
     const int splits = (tiles + tps - 1) / tps;
     return SplitPlan{splits, 128 * tps, 1, splits, 0};
   }
