@@ -35,8 +35,8 @@ METRIC = "CSA/HCA attention queries/s at 128K-1M ctx"
 # to None whenever those kernels change until they are measured again.  ncu flushes L2 before each
 # captured kernel, so the merge's 10.58 MB are partials re-read from DRAM that the timed step
 # finds in L2.
-ATTEND_DRAM_BYTES = 4545024 + 14503424 + 10579968
-INDEX_DRAM_BYTES = 71511808 + 76800 + 4501760
+ATTEND_DRAM_BYTES = 4546304 + 14500096 + 10579968
+INDEX_DRAM_BYTES = 71507968 + 35584 + 4502272
 UNIT = "queries/s"
 
 
