@@ -48,7 +48,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="csa_decode",
-                    choices=["csa_decode", "hca_decode", "mixed_decode", "csa_prefill"],
+                    choices=["csa_decode", "hca_decode", "mixed_decode", "csa_prefill", "index_key_quantize"],
                     help="csa_decode is the headline line; the others measure the HCA decode, the mixed "
                          "ragged multi-layer and the CSA prefill workloads with the same timing rules")
     ap.add_argument("--ctx-len", type=int, default=None,
@@ -628,6 +628,55 @@ def run_gpu_prefill(args, rank, world, local, wl):
             "per_rank_queries": T, "config": cfg, "launches": 2 + 2 + 1 + 1}
 
 
+# ---------------------------------------------------------------------------------------------
+# GPU arm, indexer key production: block-scaled FP4 of the keys of a 1M-token CSA context
+# ---------------------------------------------------------------------------------------------
+
+def run_gpu_quantize(args, rank, world, local):
+    """lcs_quantize_e2m1 over 4 x 266,240 BF16 rows of rank 128 (the indexer keys of a 1M-token
+    CSA context in four layers: more than L2), timed per launch after an L2 flush."""
+    import torch
+    import synth.gpu as sg
+    import long_context_sparse_24_b300 as lcsa
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if lcsa.lcs_device_check() != 0:
+        raise SystemExit("liblcsa needs a compute-capability 10.3 GPU")
+    rows, r = 4 * 266240, 128
+    x = torch.empty((rows, r), dtype=torch.bfloat16, device=dev)
+    sg.normal_bf16(x, rank_seed(5, rank), synth.tensor_id(synth.IDX_K), 0)
+    codes = torch.empty((rows, r // 2), dtype=torch.uint8, device=dev)
+    scales = torch.empty((rows, r // 32), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    n_tot = args.warmup + args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(n_tot)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(n_tot)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for st in range(n_tot):
+            flush.zero_()
+            starts[st].record()
+            lcsa.lcs_quantize_e2m1(x, codes, scales)
+            ends[st].record()
+        torch.cuda.synchronize()
+    ms = statistics.mean(starts[st].elapsed_time(ends[st]) for st in range(args.warmup, n_tot))
+    ms = max_over_ranks(ms, world, dev)
+    hbm, peak_kind = measured_peaks()
+    alg = rows * (r * 2 + r // 2 + r // 32)
+    achieved = alg / (ms * 1e-3) / 1e9
+    roofline = {"kernel": "quantize_e2m1_kernel (lcs_quantize_e2m1)", "bound": "hbm", "achieved": round(achieved, 1),
+                "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)", "algorithmic_bytes_per_launch": alg,
+                "traffic": None}
+    cfg = {"workload": "index_keys_fp4_4x266240_r128", "rows": rows, "rank": r, "input": "bf16 rows",
+           "output": "fp4_e2m1 codes + ue8m0 per 32", "l2": "flushed between timed launches (256 MB write); "
+           "input 273 MB > L2", "data": "synthetic"}
+    return {"ms": ms, "clocks": clk.summary(), "roofline": roofline, "status_ok": True, "per_rank_queries": rows,
+            "config": cfg, "launches": 1}
+
+
 def run_e2e(torch, layer, batch, graph, raw_in, q_in, iq_in, iqs_in, hw_in, out, seq_len, raw_steps, q_steps,
             iq_steps, iqs_steps, hw_steps, args, L, S, flush):
     """Same step with its inputs copied from pinned host memory and the output read back, all
@@ -803,6 +852,17 @@ def main():
         return
     assert args.warmup >= 3, "at least 3 warm-up steps"
     if args.workload != "csa_decode":
+        if args.workload == "index_key_quantize":
+            res = run_gpu_quantize(args, rank, world, local)
+            if rank == 0:
+                print(json.dumps({"metric": "indexer key rows quantised to block-scaled FP4 per second",
+                                  "value": round(job_value(res["per_rank_queries"], world, res["ms"]), 1),
+                                  "unit": "rows/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                                  "ms_per_step": round(res["ms"], 5), "higher_is_better": True, "scaling": "weak",
+                                  "vs_baseline": None, "dtype": "bf16 in, fp4 e2m1 + ue8m0 out", "data": "synthetic",
+                                  "config": res["config"], "roofline": res["roofline"], "clocks": res["clocks"],
+                                  "e2e": None, "gpu_launches": res["launches"] * args.steps, "device_status_ok": True}))
+            return
         runner = run_gpu_prefill if args.workload == "csa_prefill" else run_gpu_stack
         wl = synth.CONFIGS[args.workload]
         if args.workload == "csa_prefill" and (args.ctx_len is not None or args.new_tokens is not None):

@@ -262,6 +262,18 @@ lcs_status hca_attend(const lcs_batch* batch, const void* q, int32_t heads, int3
                       float softmax_scale, void* out, float* out_lse, void* workspace,
                       size_t workspace_bytes, int32_t* dev_status, void* stream);
 
+/* --- indexer key / query production: block-scaled FP4 (x-techcon section 4) -------------------
+ * Quantises BF16 rows x[rows][r] (r a multiple of 32, at most 4096) to E2M1 codes
+ * codes[rows][r/2] (two per byte, even element in the low nibble) and UE8M0 scale bytes
+ * scales[rows][r/32], the layout csa_index_topk reads for keys and queries.  Per 32-element
+ * block: the scale is the smallest power of two 2^e with amax <= 6 * 2^e (so nothing saturates),
+ * e clamped to [-127, 127] (all-zero blocks: e = -127, byte 0); each element is x / 2^e rounded to
+ * the nearest E2M1 value, ties to the code with mantissa bit 0, zero stored as +0.  (The pages fix
+ * the format, not the scale choice: this is the reading taken.)  x: device, 16-byte aligned;
+ * codes: device, 8-byte aligned; scales: device.  NaN / infinite inputs are not supported.  Errors: LCS_ERR_UNSUPPORTED
+ * for r outside the range, LCS_ERR_INVALID_ARG for NULL buffers; nothing is launched then. */
+lcs_status lcs_quantize_e2m1(const void* x, int64_t rows, int32_t r, uint8_t* codes, uint8_t* scales, void* stream);
+
 /* --- staging copies (serving input/output; not a step of the method) --------------------------
  * Copies n <= 8 buffers, bytes[i] bytes from src[i] to dst[i], with one kernel on `stream` whose
  * threads load and store the bytes themselves.  Each pointer may be device memory or pinned host

@@ -73,6 +73,7 @@ P = ctypes.POINTER
 _SIGS = {
     "lcs_abi_version": (c_i32, []),
     "lcs_stage_copy": (c_i32, [c_i32, c_vp, c_vp, c_vp, c_vp]),
+    "lcs_quantize_e2m1": (c_i32, [c_vp, c_i64, c_i32, c_vp, c_vp, c_vp]),
     "lcs_status_string": (ctypes.c_char_p, [c_i32]),
     "lcs_device_check": (c_i32, []),
     "csa_compress": (c_i32, [P(lcs_batch), c_vp, P(lcs_compressor), P(lcs_state), P(lcs_rows), P(lcs_paging),
@@ -229,6 +230,12 @@ def hca_compress(batch: Batch, raw, comp: Compressor, state: State, entries: Row
     b, c, s, e, p = batch.c(), comp.c(), state.c(), entries.c(), paging.c()
     _check(_lib.hca_compress(ctypes.byref(b), _ptr(raw), ctypes.byref(c), ctypes.byref(s), ctypes.byref(e),
                              ctypes.byref(p), _ptr(dev_status), _stream(stream)), "hca_compress")
+
+
+def lcs_quantize_e2m1(x, codes, scales, stream=None) -> None:
+    """Block-scaled FP4 of BF16 rows x [rows, r]: codes [rows, r/2] uint8, scales [rows, r/32] uint8."""
+    rows, r = int(x.shape[0]), int(x.shape[-1])
+    _check(_lib.lcs_quantize_e2m1(_ptr(x), rows, r, _ptr(codes), _ptr(scales), _stream(stream)), "lcs_quantize_e2m1")
 
 
 def lcs_stage_copy(pairs, stream=None) -> None:

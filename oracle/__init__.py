@@ -123,6 +123,42 @@ def e4m3_decode(b: np.ndarray) -> np.ndarray:
     return sign * mag
 
 
+E2M1_MAX = 6.0       # largest E2M1 magnitude (chenxutan section 6.2)
+
+
+def e2m1_block_quantize(x: np.ndarray, block: int = 32) -> tuple[np.ndarray, np.ndarray]:
+    """Block-scaled FP4 of x [..., r] (r a multiple of ``block``): E2M1 codes [..., r] and UE8M0
+    scale bytes [..., r/block].
+
+    The pages fix the format (E2M1 values with a power-of-two scale per 32 elements, x-techcon
+    section 4; latetalk: "blockwise scale") but not how the scale is chosen.  Reading taken:
+    the smallest power of two 2**e with amax <= 6 * 2**e, so that no element saturates, with e
+    clamped to the UE8M0 range [-127, 127] (all-zero blocks get e = -127); each element is
+    x / 2**e rounded to the nearest E2M1 value, ties to the even code (the one whose mantissa
+    bit is 0); a zero result is stored as +0 (code 0).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    shp = x.shape
+    blocks = x.reshape(shp[:-1] + (shp[-1] // block, block))
+    amax = np.abs(blocks).max(axis=-1)
+    # smallest e with 6 * 2**e >= amax: start from frexp and correct by one step either way
+    with np.errstate(divide="ignore"):
+        e = np.where(amax > 0, np.ceil(np.log2(np.where(amax > 0, amax, 1.0) / E2M1_MAX)), -127.0)
+    e = e.astype(np.int64)
+    e = np.where(np.ldexp(E2M1_MAX, e - 1) >= amax, e - 1, e)
+    e = np.where(np.ldexp(E2M1_MAX, e) < amax, e + 1, e)
+    e = np.clip(e, -127, 127)
+    v = blocks / np.ldexp(1.0, e)[..., None]
+    r = np.clip(_round_to_grid(v, 1, 0), -E2M1_MAX, E2M1_MAX)
+    mag = np.abs(r)
+    table = {0.0: 0, 0.5: 1, 1.0: 2, 1.5: 3, 2.0: 4, 3.0: 5, 4.0: 6, 6.0: 7}
+    codes = np.zeros(mag.shape, dtype=np.int64)
+    for val, code in table.items():
+        codes[mag == val] = code
+    codes = np.where((r < 0) & (codes != 0), codes | 8, codes)
+    return codes.reshape(shp).astype(np.uint8), (e + 127).astype(np.uint8)
+
+
 def bf16_bits(v: np.ndarray) -> np.ndarray:
     """Bit pattern of values already on the bf16 grid."""
     return (np.asarray(v, dtype=np.float64).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)

@@ -390,3 +390,30 @@ def test_stage_copy_pinned_and_device():
     assert torch.equal(other.cpu(), host[2])
     with pytest.raises(lcsa.LcsError):
         lcsa.lcs_stage_copy([(dev[2][:17], torch.zeros(17, dtype=torch.uint8))])   # pageable host memory
+
+
+# ---------------------------------------------------------------------------------------- FP4 keys
+
+@pytest.mark.parametrize("r", [128, 64, 160])
+def test_quantize_e2m1_matches_oracle(r):
+    """lcs_quantize_e2m1 against the oracle's block-scaled FP4: codes and scale bytes bit-exact,
+    including exact ties, all-zero blocks, subnormal and near-maximum BF16 inputs."""
+    rng = np.random.default_rng(21 + r)
+    rows = 1500
+    x = rng.standard_normal((rows, r)) * np.ldexp(1.0, rng.integers(-30, 30, size=(rows, 1)))
+    x[0, :32] = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 6.0] * 2 + [-0.25, -0.75, -1.25, -1.75,
+                                                                      -2.5, -3.5, -5.0, -6.0] * 2
+    x[1, :32] = 0.0
+    x[2, :32] = rng.standard_normal(32) * 1e-39          # BF16 subnormals
+    x[3, :32] = np.clip(rng.standard_normal(32), -3.0, 3.0) * 1e38   # near the BF16 maximum
+    x[4, :] = rng.integers(-7, 8, size=r) * 0.5          # values already on the E2M1 grid
+    bits = synth.f32_to_bf16_bits(x.astype(np.float32))
+    xv = synth.bf16_bits_to_f32(bits).astype(np.float64)
+    codes, scales = oracle.e2m1_block_quantize(xv)
+    xd = torch.from_numpy(bits.view(np.int16)).to(DEV).view(torch.bfloat16)
+    cd = torch.full((rows, r // 2), 0xAB, dtype=torch.uint8, device=DEV)
+    sd = torch.full((rows, r // 32), 0xAB, dtype=torch.uint8, device=DEV)
+    lcsa.lcs_quantize_e2m1(xd, cd, sd)
+    torch.cuda.synchronize()
+    assert np.array_equal(sd.cpu().numpy(), scales)
+    assert np.array_equal(cd.cpu().numpy(), synth.pack_e2m1(codes))

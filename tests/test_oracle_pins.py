@@ -408,3 +408,67 @@ def test_layer_full_topk_equals_dense_over_visible():
         rows = np.concatenate([ent[:oracle.visible_entries(int(t), 4)], win[oracle.window_positions(int(t))]])
         ref = oracle.attend(kw["q"][i], rows, kw["softmax_scale"])[0]
         assert np.allclose(out["o"][i], ref, rtol=1e-13, atol=1e-13)
+
+
+# ------------------------------------------------------------------------------------------------
+# Block-scaled FP4 quantisation (the indexer's key / query production, x-techcon section 4)
+# ------------------------------------------------------------------------------------------------
+
+def _e2m1_table():
+    codes = np.arange(16, dtype=np.uint8)
+    return codes, oracle.e2m1_value(codes)
+
+
+def test_e2m1_block_quantize_round_trips_representable_blocks():
+    """Blocks of E2M1 values times 2^e whose largest magnitude is 4 or 6 come back as the same
+    codes and scale exponent e (zero stored as +0)."""
+    rng = np.random.default_rng(11)
+    nb = 200
+    mags = rng.integers(0, 8, size=(nb, 32))
+    mags[np.arange(nb), rng.integers(0, 32, size=nb)] = rng.choice([6, 7], size=nb)   # 4.0 or 6.0
+    signs = rng.integers(0, 2, size=(nb, 32))
+    codes = (mags | (signs << 3)).astype(np.uint8)
+    codes[mags == 0] = 0
+    e = rng.integers(-40, 40, size=nb)
+    x = oracle.e2m1_value(codes) * np.ldexp(1.0, e)[:, None]
+    got_c, got_s = oracle.e2m1_block_quantize(x.reshape(1, -1))
+    assert np.array_equal(got_c.reshape(nb, 32), codes)
+    assert np.array_equal(got_s.reshape(nb).astype(np.int64) - 127, e)
+
+
+def test_e2m1_block_quantize_nearest_value_ties_to_even_brute_force():
+    """Every element's stored value is a nearest one among all 15 E2M1 values times the block
+    scale (checked by exhaustive search); on a tie the code's mantissa bit is 0; the scale is the
+    smallest power of two with amax <= 6 * scale."""
+    rng = np.random.default_rng(12)
+    x = rng.standard_normal((64, 128)) * np.ldexp(1.0, rng.integers(-10, 10, size=(64, 1)))
+    # exact ties: block 0 of row 0 holds the midpoints between neighbouring E2M1 values (scale 1)
+    x[0, :8] = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 6.0]
+    x[0, 8:32] = -np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0] * 3 + [0.0] * 3)
+    codes, scales = oracle.e2m1_block_quantize(x)
+    tc, tv = _e2m1_table()
+    for i in range(x.shape[0]):
+        for blk in range(4):
+            sc = oracle.ue8m0_value(scales[i, blk])
+            xb = x[i, blk * 32:(blk + 1) * 32]
+            amax = np.abs(xb).max()
+            assert 6.0 * sc >= amax and (amax == 0 or 6.0 * sc / 2 < amax)
+            for j in range(32):
+                c = codes[i, blk * 32 + j]
+                err = np.abs(xb[j] - tv * sc)
+                best = err.min()
+                assert abs(xb[j] - oracle.e2m1_value(c) * sc) == best
+                if np.count_nonzero(np.isclose(err, best, rtol=0, atol=0)) > 1 and best > 0:
+                    assert (c & 1) == 0
+    assert list(codes[0, :8]) == [0, 2, 2, 4, 4, 6, 6, 7]
+
+
+def test_e2m1_block_quantize_zero_and_extremes():
+    codes, scales = oracle.e2m1_block_quantize(np.zeros((2, 64)))
+    assert not codes.any() and np.all(scales == 0)                 # 2^-127, all +0
+    big = np.full((1, 32), 3.0e38)
+    c, s = oracle.e2m1_block_quantize(big)
+    assert s[0, 0] == 127 + 126 and np.all(c == 6)                # 3e38 = 4 * 2^126 (rounded)
+    tiny = np.full((1, 32), 1e-40)
+    c, s = oracle.e2m1_block_quantize(tiny)
+    assert s[0, 0] == 0                                            # clamped at 2^-127
