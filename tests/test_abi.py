@@ -93,6 +93,17 @@ def test_stage_copy_host_validation():
     lcsa.lcs_stage_copy([], stream=0)                                             # binding: empty list
 
 
+def test_quantize_e2m1_host_validation():
+    import long_context_sparse_24_b300 as lcsa
+    L = lcsa._lib
+    assert L.lcs_quantize_e2m1(0x1000, 4, 48, 0x2000, 0x3000, None) == 4        # r not a multiple of 32
+    assert L.lcs_quantize_e2m1(0x1000, 4, 8192, 0x2000, 0x3000, None) == 4      # r too large
+    assert L.lcs_quantize_e2m1(0x1000, 0, 128, 0x2000, 0x3000, None) == 0       # no rows: nothing to do
+    assert L.lcs_quantize_e2m1(None, 4, 128, 0x2000, 0x3000, None) == 1         # missing input
+    assert L.lcs_quantize_e2m1(0x1008, 4, 128, 0x2000, 0x3000, None) == 3       # input not 16-byte aligned
+    assert L.lcs_quantize_e2m1(0x1000, 4, 128, 0x2004, 0x3000, None) == 3       # codes not 8-byte aligned
+
+
 def test_workspace_sizes():
     import long_context_sparse_24_b300 as lcsa
     b = lcsa.lcs_batch(32, 0x1000, 0x2000, 32, 1, 131072)
