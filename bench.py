@@ -48,7 +48,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="csa_decode",
-                    choices=["csa_decode", "hca_decode", "mixed_decode", "csa_prefill", "index_key_quantize"],
+                    choices=["csa_decode", "hca_decode", "mixed_decode", "csa_prefill", "index_key_quantize",
+                             "attention_sink"],
                     help="csa_decode is the headline line; the others measure the HCA decode, the mixed "
                          "ragged multi-layer and the CSA prefill workloads with the same timing rules")
     ap.add_argument("--ctx-len", type=int, default=None,
@@ -632,6 +633,50 @@ def run_gpu_prefill(args, rank, world, local, wl):
 # GPU arm, indexer key production: block-scaled FP4 of the keys of a 1M-token CSA context
 # ---------------------------------------------------------------------------------------------
 
+def run_gpu_sink(args, rank, world, local):
+    """lcs_attention_sink over the attention outputs of the CSA prefill chunk (16,384 queries x 128
+    heads x 512 dims BF16, 2.1 GB: far beyond L2), timed per launch after an L2 flush."""
+    import torch
+    import synth.gpu as sg
+    import long_context_sparse_24_b300 as lcsa
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if lcsa.lcs_device_check() != 0:
+        raise SystemExit("liblcsa needs a compute-capability 10.3 GPU")
+    T, H, D = 16384, 128, 512
+    out = torch.empty((T, H, D), dtype=torch.bfloat16, device=dev)
+    sg.normal_bf16(out, rank_seed(6, rank), synth.tensor_id(synth.QUERY), 0)
+    lse = torch.full((T, H), 3.0, dtype=torch.float32, device=dev)
+    sink = torch.linspace(-2.0, 2.0, H, dtype=torch.float32, device=dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    n_tot = args.warmup + args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(n_tot)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(n_tot)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for st in range(n_tot):
+            flush.zero_()
+            starts[st].record()
+            lcsa.lcs_attention_sink(out, lse, sink)
+            ends[st].record()
+        torch.cuda.synchronize()
+    ms = statistics.mean(starts[st].elapsed_time(ends[st]) for st in range(args.warmup, n_tot))
+    ms = max_over_ranks(ms, world, dev)
+    hbm, peak_kind = measured_peaks()
+    alg = T * H * (2 * D * 2 + 8)
+    achieved = alg / (ms * 1e-3) / 1e9
+    roofline = {"kernel": "attention_sink_kernel (lcs_attention_sink)", "bound": "hbm", "achieved": round(achieved, 1),
+                "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)", "algorithmic_bytes_per_launch": alg,
+                "traffic": None}
+    cfg = {"workload": "attention_sink_16384q_h128_d512", "queries": T, "heads": H, "dim": D,
+           "l2": "flushed between timed launches (256 MB write); outputs 2.1 GB > L2", "data": "synthetic"}
+    return {"ms": ms, "clocks": clk.summary(), "roofline": roofline, "per_rank_queries": T, "config": cfg,
+            "launches": 1}
+
+
 def run_gpu_quantize(args, rank, world, local):
     """lcs_quantize_e2m1 over 4 x 266,240 BF16 rows of rank 128 (the indexer keys of a 1M-token
     CSA context in four layers: more than L2), timed per launch after an L2 flush."""
@@ -852,6 +897,16 @@ def main():
         return
     assert args.warmup >= 3, "at least 3 warm-up steps"
     if args.workload != "csa_decode":
+        if args.workload == "attention_sink":
+            res = run_gpu_sink(args, rank, world, local)
+            if rank == 0:
+                print(json.dumps({"metric": METRIC, "value": round(job_value(res["per_rank_queries"], world, res["ms"]), 1),
+                                  "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                                  "ms_per_step": round(res["ms"], 5), "higher_is_better": True, "scaling": "weak",
+                                  "vs_baseline": None, "dtype": "bf16 outputs, fp32 lse", "data": "synthetic",
+                                  "config": res["config"], "roofline": res["roofline"], "clocks": res["clocks"],
+                                  "e2e": None, "gpu_launches": res["launches"] * args.steps, "device_status_ok": True}))
+            return
         if args.workload == "index_key_quantize":
             res = run_gpu_quantize(args, rank, world, local)
             if rank == 0:

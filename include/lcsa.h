@@ -274,6 +274,18 @@ lcs_status hca_attend(const lcs_batch* batch, const void* q, int32_t heads, int3
  * for r outside the range, LCS_ERR_INVALID_ARG for NULL buffers; nothing is launched then. */
 lcs_status lcs_quantize_e2m1(const void* x, int64_t rows, int32_t r, uint8_t* codes, uint8_t* scales, void* stream);
 
+/* --- attention sink (a per-head logit in every softmax denominator, carrying no value) ----------
+ * Applied after csa_attend / csa_attend_topk / hca_attend from their outputs and log-sum-exp:
+ *   out[i,h,:] *= 1 / (1 + exp(sink[h] - lse[i,h])),  lse[i,h] = log(exp(lse[i,h]) + exp(sink[h])),
+ * which equals attention whose softmax has one more term exp(sink[h]) per head.  (The pages name
+ * an attention sink without defining it; this is the common learned-sink definition.)
+ *   out device bf16[total_new][heads][dim] (16-byte aligned, updated in place),
+ *   out_lse device f32[total_new][heads] (natural log, updated in place), sink device f32[heads]
+ *   in the logits' units (softmax_scale * q . row).  dim a multiple of 8.
+ * Errors: LCS_ERR_UNSUPPORTED for sizes out of range, LCS_ERR_INVALID_ARG for NULL buffers. */
+lcs_status lcs_attention_sink(void* out, float* out_lse, const float* sink, int64_t total_new, int32_t heads,
+                              int32_t dim, void* stream);
+
 /* --- staging copies (serving input/output; not a step of the method) --------------------------
  * Copies n <= 8 buffers, bytes[i] bytes from src[i] to dst[i], with one kernel on `stream` whose
  * threads load and store the bytes themselves.  Each pointer may be device memory or pinned host

@@ -74,6 +74,7 @@ _SIGS = {
     "lcs_abi_version": (c_i32, []),
     "lcs_stage_copy": (c_i32, [c_i32, c_vp, c_vp, c_vp, c_vp]),
     "lcs_quantize_e2m1": (c_i32, [c_vp, c_i64, c_i32, c_vp, c_vp, c_vp]),
+    "lcs_attention_sink": (c_i32, [c_vp, c_vp, c_vp, c_i64, c_i32, c_i32, c_vp]),
     "lcs_status_string": (ctypes.c_char_p, [c_i32]),
     "lcs_device_check": (c_i32, []),
     "csa_compress": (c_i32, [P(lcs_batch), c_vp, P(lcs_compressor), P(lcs_state), P(lcs_rows), P(lcs_paging),
@@ -236,6 +237,13 @@ def lcs_quantize_e2m1(x, codes, scales, stream=None) -> None:
     """Block-scaled FP4 of BF16 rows x [rows, r]: codes [rows, r/2] uint8, scales [rows, r/32] uint8."""
     rows, r = int(x.shape[0]), int(x.shape[-1])
     _check(_lib.lcs_quantize_e2m1(_ptr(x), rows, r, _ptr(codes), _ptr(scales), _stream(stream)), "lcs_quantize_e2m1")
+
+
+def lcs_attention_sink(out, out_lse, sink, stream=None) -> None:
+    """Per-head sink logits sink [heads] applied to attention outputs out [T, heads, D] and lse [T, heads]."""
+    T, H, D = int(out.shape[0]), int(out.shape[1]), int(out.shape[2])
+    _check(_lib.lcs_attention_sink(_ptr(out), _ptr(out_lse), _ptr(sink), T, H, D, _stream(stream)),
+           "lcs_attention_sink")
 
 
 def lcs_stage_copy(pairs, stream=None) -> None:

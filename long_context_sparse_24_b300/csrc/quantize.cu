@@ -90,3 +90,60 @@ extern "C" lcs_status lcs_quantize_e2m1(const void* x, int64_t rows, int32_t r, 
       static_cast<const uint4*>(x), n16, reinterpret_cast<uint2*>(codes), scales);
   return cudaGetLastError() == cudaSuccess ? LCS_OK : LCS_ERR_CUDA;
 }
+
+// ----------------------------------------------------------------------------------------------
+// Attention sink: a per-head logit that joins every softmax denominator and carries no value
+// (the csdn attention-details table names an attention sink without defining it; this is the
+// common learned-sink definition).  Applied after the attention call from its outputs and their
+// log-sum-exp: o' = o / (1 + exp(sink_h - lse)), lse' = log(exp(lse) + exp(sink_h)).
+// ----------------------------------------------------------------------------------------------
+
+namespace lcsa {
+namespace {
+
+constexpr int kSinkWarps = 4;
+
+__global__ void __launch_bounds__(kSinkWarps * 32) attention_sink_kernel(__nv_bfloat16* __restrict__ out,
+                                                                         float* __restrict__ lse,
+                                                                         const float* __restrict__ sink,
+                                                                         long long pairs, int heads, int dim) {
+  const long long pr = (long long)blockIdx.x * kSinkWarps + (threadIdx.x >> 5);   // (query, head)
+  if (pr >= pairs) return;                                                      // warp-uniform
+  const int lane = threadIdx.x & 31;
+  const int h = (int)(pr % heads);
+  const float l = lse[pr], s = sink[h];
+  const float d = s - l;
+  // 1 / (1 + e^d) without overflow, and log(e^l + e^s) = max + log1p(e^-|l - s|)
+  const float f = d > 0.0f ? expf(-d) / (1.0f + expf(-d)) : 1.0f / (1.0f + expf(d));
+  uint4* row = reinterpret_cast<uint4*>(out + pr * dim);
+  for (int i = lane; i < dim / 8; i += 32) {
+    uint4 v = row[i];
+    uint32_t* w = &v.x;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[j]));
+      const __nv_bfloat162 b = __floats2bfloat162_rn(a.x * f, a.y * f);
+      w[j] = *reinterpret_cast<const uint32_t*>(&b);
+    }
+    row[i] = v;
+  }
+  if (lane == 0) lse[pr] = fmaxf(l, s) + log1pf(expf(-fabsf(l - s)));
+}
+
+}  // namespace
+}  // namespace lcsa
+
+extern "C" lcs_status lcs_attention_sink(void* out, float* out_lse, const float* sink, int64_t total_new,
+                                         int32_t heads, int32_t dim, void* stream) {
+  using namespace lcsa;
+  if (total_new < 0 || heads <= 0 || dim <= 0 || (dim & 7) != 0) return LCS_ERR_UNSUPPORTED;
+  if (total_new == 0) return LCS_OK;
+  if (out == nullptr || out_lse == nullptr || sink == nullptr) return LCS_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(out) & 15u) return LCS_ERR_ALIGNMENT;
+  const long long pairs = total_new * (long long)heads;
+  const long long ctas = (pairs + kSinkWarps - 1) / kSinkWarps;
+  if (ctas > 0x7fffffffll) return LCS_ERR_UNSUPPORTED;
+  attention_sink_kernel<<<(unsigned)ctas, kSinkWarps * 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<__nv_bfloat16*>(out), out_lse, sink, pairs, heads, dim);
+  return cudaGetLastError() == cudaSuccess ? LCS_OK : LCS_ERR_CUDA;
+}

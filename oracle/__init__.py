@@ -347,6 +347,23 @@ def attend(q: np.ndarray, keys: np.ndarray, softmax_scale: float, values: np.nda
     return o, (mx + np.log(l))[:, 0]
 
 
+def attend_with_sink(q: np.ndarray, keys: np.ndarray, softmax_scale: float, sink: np.ndarray,
+                     values: np.ndarray | None = None):
+    """``attend`` with a per-head sink logit sink[H]: one more softmax term per head that takes
+    probability mass but carries no value (o = sum_r p_r v_r / (sum_r p_r + exp(sink))).
+
+    The csdn attention-details table names an attention sink without defining it; this is the
+    common definition of a learned per-head sink logit (a reading from outside the pages)."""
+    values = keys if values is None else values
+    logits = softmax_scale * (np.asarray(q, np.float64) @ np.asarray(keys, np.float64).T)
+    sink = np.asarray(sink, np.float64)[:, None]
+    mx = np.maximum(logits.max(axis=1, keepdims=True), sink)
+    p = np.exp(logits - mx)
+    l = p.sum(axis=1, keepdims=True) + np.exp(sink - mx)
+    o = (p @ np.asarray(values, np.float64)) / l
+    return o, (mx + np.log(l))[:, 0]
+
+
 def csa_query_rows(t: int, selected: np.ndarray, entries: np.ndarray, window_rows: np.ndarray,
                    window: int = WINDOW):
     """Rows one CSA query attends to: the selected entries, then its window rows.

@@ -104,6 +104,15 @@ def test_quantize_e2m1_host_validation():
     assert L.lcs_quantize_e2m1(0x1000, 4, 128, 0x2004, 0x3000, None) == 3       # codes not 8-byte aligned
 
 
+def test_attention_sink_host_validation():
+    import long_context_sparse_24_b300 as lcsa
+    L = lcsa._lib
+    assert L.lcs_attention_sink(0x1000, 0x2000, 0x3000, 4, 64, 100, None) == 4   # dim not a multiple of 8
+    assert L.lcs_attention_sink(0x1000, 0x2000, 0x3000, 0, 64, 512, None) == 0   # nothing to do
+    assert L.lcs_attention_sink(None, 0x2000, 0x3000, 4, 64, 512, None) == 1     # missing output
+    assert L.lcs_attention_sink(0x1008, 0x2000, 0x3000, 4, 64, 512, None) == 3   # output not 16-byte aligned
+
+
 def test_workspace_sizes():
     import long_context_sparse_24_b300 as lcsa
     b = lcsa.lcs_batch(32, 0x1000, 0x2000, 32, 1, 131072)

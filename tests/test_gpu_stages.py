@@ -238,7 +238,7 @@ def test_topk_ties_take_lowest_index():
 
 # ---------------------------------------------------------------------------------------- attention
 
-def _attend_case(kind, lengths, new, heads, dim, fmt, m, k, seed=41, scale=None, split=False):
+def _attend_case(kind, lengths, new, heads, dim, fmt, m, k, seed=41, scale=None, split=False, sink=None):
     """Fill an entry cache / window ring / new rows with oracle-quantised rows and run one call."""
     S = len(lengths)
     fmtc = buffers.row_format_code(fmt)
@@ -319,6 +319,8 @@ def _attend_case(kind, lengths, new, heads, dim, fmt, m, k, seed=41, scale=None,
         wsb = lcsa.lcs_attend_workspace(batch, heads, dim, cap // m + 128)
         lcsa.hca_attend(batch, q, heads, m, cache.entries, cache.paging, cache.state, scale, out, lse,
                         workspace(wsb), wsb, st)
+    if sink is not None:
+        lcsa.lcs_attention_sink(out, lse, torch.from_numpy(sink.astype(np.float32)).to(DEV))
     torch.cuda.synchronize()
     assert_status_ok(st)
     o = bf16_tensor_to_f64(out); l = lse.cpu().numpy()
@@ -332,7 +334,10 @@ def _attend_case(kind, lengths, new, heads, dim, fmt, m, k, seed=41, scale=None,
                 rows = oracle.csa_query_rows(t, sels[qi], ent_deq[b], win_deq[b])
             else:
                 rows = oracle.hca_query_rows(t, m, ent_deq[b], win_deq[b])
-            ro, rl = oracle.attend(qf[qi], rows, scale)
+            if sink is None:
+                ro, rl = oracle.attend(qf[qi], rows, scale)
+            else:
+                ro, rl = oracle.attend_with_sink(qf[qi], rows, scale, sink.astype(np.float32).astype(np.float64))
             check_outputs(o[qi], ro, f"{kind} seq {b} query {i}")
             assert np.allclose(l[qi], rl, atol=2e-3, rtol=1e-4), f"lse seq {b} query {i}"
             qi += 1
@@ -356,6 +361,19 @@ def _attend_case(kind, lengths, new, heads, dim, fmt, m, k, seed=41, scale=None,
 ])
 def test_attend_matches_oracle(kind, lengths, new, heads, dim, fmt, m, k):
     _attend_case(kind, lengths, new, heads, dim, fmt, m, k)
+
+
+@pytest.mark.parametrize("kind,lengths,new,heads,dim,fmt,m,k", [
+    ("csa", [2000, 4100, 300], [1, 1, 1], 64, 512, "fp8_split", 4, 512),
+    ("csa", [900, 2200], [40, 9], 64, 512, "fp8_split", 4, 64),
+    ("hca", [3000], [17], 64, 512, "fp8_split", 128, 0),
+    ("csa", [50, 700], [50, 20], 8, 128, "bf16", 4, 64),
+])
+def test_attention_sink_matches_oracle(kind, lengths, new, heads, dim, fmt, m, k):
+    """Attention, then lcs_attention_sink with per-head sink logits around the logits' range,
+    against the oracle's softmax with the sink term (outputs and lse)."""
+    sink = np.random.default_rng(7).standard_normal(heads) * 2.0
+    _attend_case(kind, lengths, new, heads, dim, fmt, m, k, sink=sink)
 
 
 @pytest.mark.parametrize("lengths,new,heads,dim,fmt,k", [

@@ -472,3 +472,35 @@ def test_e2m1_block_quantize_zero_and_extremes():
     tiny = np.full((1, 32), 1e-40)
     c, s = oracle.e2m1_block_quantize(tiny)
     assert s[0, 0] == 0                                            # clamped at 2^-127
+
+
+# ------------------------------------------------------------------------------------------------
+# Attention sink (NEXT-2 reading)
+# ------------------------------------------------------------------------------------------------
+
+def test_attend_with_sink_is_softmax_with_a_zero_value_row():
+    """A sink logit s is one more row whose logit is s (whatever q) and whose value is zero:
+    checked against torch's scaled_dot_product_attention over the rows plus such a row, and
+    against the limits s -> -inf (plain attention) and s -> +inf (output 0)."""
+    rng = np.random.default_rng(31)
+    H, D, R = 8, 64, 50
+    q = rng.standard_normal((H, D))
+    rows = rng.standard_normal((R, D))
+    sink = rng.standard_normal(H) * 3
+    scale = 1 / math.sqrt(D)
+    o, lse = oracle.attend_with_sink(q, rows, scale, sink)
+    # per head, the sink row: key chosen so that scale * q_h . key = sink_h, value 0
+    for h in range(H):
+        key = q[h] * (sink[h] / (scale * (q[h] @ q[h])))
+        k_all = torch.from_numpy(np.vstack([rows, key]))[None]
+        v_all = torch.from_numpy(np.vstack([rows, np.zeros(D)]))[None]
+        ref = torch.nn.functional.scaled_dot_product_attention(torch.from_numpy(q[h:h + 1])[None], k_all, v_all,
+                                                               scale=scale)[0, 0].numpy()
+        assert np.allclose(o[h], ref, rtol=1e-12, atol=1e-12)
+        logits = np.append(scale * rows @ q[h], sink[h])
+        assert np.isclose(lse[h], scipy.special.logsumexp(logits), rtol=1e-13)
+    o0, lse0 = oracle.attend(q, rows, scale)
+    o1, _ = oracle.attend_with_sink(q, rows, scale, np.full(H, -1e300))
+    assert np.allclose(o1, o0, rtol=0, atol=1e-15)
+    o2, _ = oracle.attend_with_sink(q, rows, scale, np.full(H, 1e4))
+    assert np.all(np.abs(o2) < 1e-300)
