@@ -29,14 +29,11 @@ import synth  # noqa: E402
 
 WL = synth.CONFIGS["csa_decode"]
 METRIC = "CSA/HCA attention queries/s at 128K-1M ctx"
-# DRAM bytes (read + write) per step of the attention (window launch + top-k launch + merge) and of
-# the indexer (scorer + select), from one ncu capture of this workload (dram__bytes_read.sum +
-# dram__bytes_write.sum; profiles/csa_decode_32x128k_launch_list.md) on the current kernels; set
-# to None whenever those kernels change until they are measured again.  ncu flushes L2 before each
-# captured kernel, so the merge's 10.58 MB are partials re-read from DRAM that the timed step
-# finds in L2.
-ATTEND_DRAM_BYTES = 4546304 + 14500096 + 10579968
-INDEX_DRAM_BYTES = 71507968 + 35584 + 4502272
+# DRAM bytes (read + write) per step of the attention and of the indexer on the csa_decode
+# workload, from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum), together with
+# the hash of the kernel sources they were taken on: when the sources differ from that hash the
+# counters no longer describe the kernels that run and `traffic` is reported as null.
+TRAFFIC = {"source_sha1": None, "attend": None, "index": None}
 UNIT = "queries/s"
 
 
@@ -48,10 +45,11 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="csa_decode",
-                    choices=["csa_decode", "hca_decode", "mixed_decode", "csa_prefill", "index_key_quantize",
-                             "attention_sink"],
-                    help="csa_decode is the headline line; the others measure the HCA decode, the mixed "
-                         "ragged multi-layer and the CSA prefill workloads with the same timing rules")
+                    choices=["csa_decode", "csa_decode_1m", "hca_decode", "mixed_decode", "csa_prefill",
+                             "compress_1m", "index_key_quantize", "attention_sink"],
+                    help="csa_decode is the headline line; the others measure the 1M-context CSA decode, the "
+                         "HCA decode, the mixed ragged multi-layer and the CSA prefill workloads, and the "
+                         "compression of a 1M-token context, with the same timing rules")
     ap.add_argument("--ctx-len", type=int, default=None,
                     help="csa_prefill only: cached tokens instead of the workload's 1,048,576 (a smaller case of "
                          "the same kernels, for profiler captures; the line then names the changed workload)")
@@ -98,11 +96,12 @@ def job_value(per_rank_units: float, world: int, ms: float) -> float:
     return per_rank_units * world / (ms * 1e-3)
 
 
-def workload_config(extra=None):
-    cfg = {"workload": WL.name, "num_seqs": WL.num_seqs, "ctx_len": WL.ctx_len, "new_tokens_per_seq": 1,
-           "heads": WL.heads, "kv_dim": WL.dim, "row_format": "fp8_e4m3(448)+bf16_rope(64)+f32_scale",
-           "m": WL.m, "overlap": True, "index_heads": WL.index_heads, "index_rank": WL.index_rank,
-           "index_format": "fp4_e2m1+ue8m0/32", "top_k": WL.top_k, "window": WL.window, "seed": WL.seed,
+def workload_config(extra=None, wl=None):
+    wl = wl or WL
+    cfg = {"workload": wl.name, "num_seqs": wl.num_seqs, "ctx_len": wl.ctx_len, "new_tokens_per_seq": 1,
+           "heads": wl.heads, "kv_dim": wl.dim, "row_format": "fp8_e4m3(448)+bf16_rope(64)+f32_scale",
+           "m": wl.m, "overlap": True, "index_heads": wl.index_heads, "index_rank": wl.index_rank,
+           "index_format": "fp4_e2m1+ue8m0/32", "top_k": wl.top_k, "window": wl.window, "seed": wl.seed,
            "l2": "flushed between timed steps (256 MB write)", "data": "synthetic"}
     if extra:
         cfg.update(extra)
@@ -169,6 +168,26 @@ class ClockSampler:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
+def kernel_source_sha1() -> str:
+    """sha1 over the library's kernel sources (file names and contents, sorted by name)."""
+    import hashlib
+    h = hashlib.sha1()
+    d = os.path.join(ROOT, "long_context_sparse_24_b300", "csrc")
+    for name in sorted(os.listdir(d)):
+        if name.endswith((".cu", ".cuh")):
+            h.update(name.encode())
+            with open(os.path.join(d, name), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()
+
+
+def traffic_of(part: str):
+    """ncu DRAM bytes of `part` if they were captured on the kernel sources that run, else None."""
+    if TRAFFIC.get("source_sha1") and TRAFFIC["source_sha1"] == kernel_source_sha1():
+        return TRAFFIC.get(part)
+    return None
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -181,7 +200,8 @@ def measured_peaks():
 # GPU arm
 # ---------------------------------------------------------------------------------------------
 
-def run_gpu(args, rank, world, local):
+def run_gpu(args, rank, world, local, wl=None):
+    wl = wl or WL
     import torch
     import synth.gpu as sg
     import long_context_sparse_24_b300 as lcsa
@@ -191,12 +211,12 @@ def run_gpu(args, rank, world, local):
     dev = torch.device("cuda", local)
     if lcsa.lcs_device_check() != 0:
         raise SystemExit("liblcsa needs a compute-capability 10.3 GPU")
-    S, L, H, D = WL.num_seqs, WL.ctx_len, WL.heads, WL.dim
-    Hi, r, k, m = WL.index_heads, WL.index_rank, WL.top_k, WL.m
+    S, L, H, D = wl.num_seqs, wl.ctx_len, wl.heads, wl.dim
+    Hi, r, k, m = wl.index_heads, wl.index_rank, wl.top_k, wl.m
     n_stage = 5                              # extra replays of an instrumented graph (stage times)
     steps_total = args.warmup + args.steps + n_stage
     cap = L + 128 * math.ceil((steps_total + 1) / 128) + 256
-    seed = rank_seed(WL.seed, rank)         # each rank serves its own sequences
+    seed = rank_seed(wl.seed, rank)         # each rank serves its own sequences
     layer = Layer("csa", S, cap, H, D, lcsa.LCS_ROW_FP8_SPLIT, m, top_k=k, index_heads=Hi, index_rank=r,
                   max_new=1, device=dev)
     # compressor parameters (w ~ N(0,1)/16, bias ~ N(0,1)/2)
@@ -331,33 +351,41 @@ def run_gpu(args, rank, world, local):
     hbm, peak_kind = measured_peaks()
     peak_src = f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback"
     n_vis = [(L + s + 1) // m for s in range(timed_end, steps_total)]
-    # ---- roofline of the dominant kernel: attend_tc1_kernel (window launch + top-k launch + merge).
-    #      Algorithmic bytes per query: (k + window) rows of 580 B, the query and the output (H x D
-    #      BF16 each); 4*H*D FLOP per row, i.e. about 167 FLOP/B, below the BF16/F16 tensor balance
-    #      point (~270 FLOP/B on this part), so HBM is the roof.
+    # ---- algorithmic bytes per step.  Attention: (k + window) rows of 580 B per query, the query and
+    #      the output (H x D BF16 each); 4*H*D FLOP per row (about 167 FLOP/B, below the F16 tensor
+    #      balance point of ~270 FLOP/B on this part, so HBM is the roof).  Indexer: 68 B of key per
+    #      visible entry per query, the query codes, scales and head weights, and the selection.
     att_bytes = S * ((k + 128) * (D - 64 + 128 + 4) + 2 * H * D * 2)
     att_ms = stage["attend_window"] + stage["attend_topk"]
-    att_achieved = att_bytes / (att_ms * 1e-3) / 1e9
-    roofline = {"kernel": "attend_tc1_kernel (csa_attend_window + csa_attend_topk incl. attend_combine_kernel)",
-                "bound": "hbm", "achieved": round(att_achieved, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(att_achieved / hbm, 4), "peak_source": peak_src,
-                "algorithmic_bytes_per_launch": int(att_bytes), "flop_per_step": int(S * 4 * H * D * (k + 128)),
-                "traffic": ATTEND_DRAM_BYTES,
-                "timing": "CUDA events around the two calls in the serialised copy of the step"}
-    # ---- the indexer (score scan + top-k select): 68 B per visible entry per query, plus queries and
-    #      the selection
     key_bytes = r // 2 + r // 32
     idx_bytes = statistics.mean(S * (n * key_bytes + Hi * key_bytes + Hi * 4 + k * 4 + 4) for n in n_vis)
-    idx_achieved = idx_bytes / (stage["index_topk"] * 1e-3) / 1e9
-    roofline_index = {"kernel": "csa_index_topk (index_tc_kernel + topk_select_kernel)", "bound": "hbm",
-                      "achieved": round(idx_achieved, 1), "peak": hbm, "unit": "GB/s",
-                      "frac": round(idx_achieved / hbm, 4), "peak_source": peak_src,
-                      "algorithmic_bytes_per_launch": int(idx_bytes), "traffic": INDEX_DRAM_BYTES}
+    idx_ms = stage["index_topk"]
+    comp_bytes = S * (D * 2 + (D - 64 + 128 + 4))     # one raw row in, one window row out per sequence
+    step_bytes = att_bytes + idx_bytes + comp_bytes
+
+    def roof(kernel, nbytes, t_ms, traffic, timing):
+        ach = nbytes / (t_ms * 1e-3) / 1e9
+        return {"kernel": kernel, "bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(ach / hbm, 4), "peak_source": peak_src, "algorithmic_bytes_per_launch": int(nbytes),
+                "traffic": traffic, "timing": timing}
+
+    timing = "CUDA events around the call(s) in a serialised copy of the step (event nodes in a CUDA graph)"
+    roofline_att = roof("csa_attend_window + csa_attend_topk (attention kernels incl. any merge)", att_bytes,
+                        att_ms, traffic_of("attend"), timing)
+    roofline_att["flop_per_step"] = int(S * 4 * H * D * (k + 128))
+    roofline_idx = roof("csa_index_topk (scorer and selection)", idx_bytes, idx_ms, traffic_of("index"), timing)
+    roofline_step = roof("whole step (compression, indexer, attention)", step_bytes, ms, None,
+                         "CUDA events around each timed step (the graph as it runs)")
+    # the dominant stage by device time is the line's roofline; the other stage and the whole step beside it
+    if att_ms >= idx_ms:
+        roofline, roofline_other = roofline_att, roofline_idx
+    else:
+        roofline, roofline_other = roofline_idx, roofline_att
     # ---- end to end through the public API with host buffers (pinned), copies in the timed region
     e2e = run_e2e(torch, layer, batch, graph, raw_in, q_in, iq_in, iqs_in, hw_in, out, seq_len, raw_steps,
                   q_steps, iq_steps, iqs_steps, hw_steps, args, L, S, flush)
     return {"ms": ms, "stages": stage, "clocks": clk.summary(), "roofline": roofline,
-            "roofline_index": roofline_index, "e2e": e2e,
+            "roofline_other": roofline_other, "roofline_step": roofline_step, "e2e": e2e,
             "launches": launches_per_step * args.steps, "status_ok": status_ok,
             "per_rank_queries": S}
 
@@ -633,6 +661,62 @@ def run_gpu_prefill(args, rank, world, local, wl):
 # GPU arm, indexer key production: block-scaled FP4 of the keys of a 1M-token CSA context
 # ---------------------------------------------------------------------------------------------
 
+def run_gpu_compress(args, rank, world, local):
+    """csa_compress of a whole 1,048,576-token context of one sequence in one call (BF16 rows of
+    D = 512 in, 262,144 entries of 580 B out, the window ring and pending rows updated), timed per
+    call after an L2 flush.  Algorithmic bytes: the raw rows read once (1 GiB) and the entries
+    written (152 MB); the overlapping windows re-read each block from L2/L1, not from HBM."""
+    import torch
+    import synth.gpu as sg
+    import long_context_sparse_24_b300 as lcsa
+    from long_context_sparse_24_b300.layer import Layer
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if lcsa.lcs_device_check() != 0:
+        raise SystemExit("liblcsa needs a compute-capability 10.3 GPU")
+    L, D, m = 1048576, 512, 4
+    seed = rank_seed(7, rank)
+    layer = Layer("csa", 1, L + 256, 64, D, lcsa.LCS_ROW_FP8_SPLIT, m, top_k=512, max_new=1, device=dev)
+    w = synth.bf16_bits_to_f32(synth.normal_bf16(seed, synth.tensor_id(synth.COMP_W), 0, D)) / 16
+    bias = synth.bf16_bits_to_f32(synth.normal_bf16(seed, synth.tensor_id(synth.COMP_B), 0, 2 * m)) / 2
+    layer.set_compressor(torch.from_numpy(w.astype(np.float32)).to(dev),
+                         torch.from_numpy(bias.astype(np.float32)).to(dev))
+    raw = torch.empty((L, D), dtype=torch.bfloat16, device=dev)
+    sg.normal_bf16(raw, seed, synth.tensor_id(synth.RAW, 0, 0), 0)
+    batch = layer.batch([L], [L])
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    layer.fill(batch, raw)
+    torch.cuda.synchronize()
+    n_tot = args.warmup + args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(n_tot)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(n_tot)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for st in range(n_tot):
+            flush.zero_()
+            starts[st].record()
+            layer.fill(batch, raw)       # the same context again: identical work and output
+            ends[st].record()
+        torch.cuda.synchronize()
+    ms = statistics.mean(starts[st].elapsed_time(ends[st]) for st in range(args.warmup, n_tot))
+    ms = max_over_ranks(ms, world, dev)
+    hbm, peak_kind = measured_peaks()
+    n_ent = L // m
+    alg = L * D * 2 + n_ent * (D - 64 + 128 + 4)
+    achieved = alg / (ms * 1e-3) / 1e9
+    roofline = {"kernel": "compress_entries_kernel<512,1> + compress_state_kernel<512> (csa_compress)",
+                "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved / hbm, 4), "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
+                "algorithmic_bytes_per_launch": int(alg), "traffic": None}
+    cfg = {"workload": "csa_compress_1m_d512_m4", "tokens": L, "dim": D, "m": m, "overlap": True,
+           "entries": n_ent, "row_format": "fp8_e4m3(448)+bf16_rope(64)+f32_scale",
+           "l2": "flushed between timed calls (256 MB write); input 1 GiB > L2", "data": "synthetic"}
+    return {"ms": ms, "clocks": clk.summary(), "roofline": roofline, "per_rank_queries": L, "config": cfg,
+            "launches": 2, "status_ok": int(layer.status.item()) == 0}
+
+
 def run_gpu_sink(args, rank, world, local):
     """lcs_attention_sink over the attention outputs of the CSA prefill chunk (16,384 queries x 128
     heads x 512 dims BF16, 2.1 GB: far beyond L2), timed per launch after an L2 flush."""
@@ -768,7 +852,7 @@ def run_e2e(torch, layer, batch, graph, raw_in, q_in, iq_in, iqs_in, hw_in, out,
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=main):
         body()
-    times = []
+    times, host_times = [], []
     for s in range(n):
         for k_, t in enumerate(host_in):
             stage[k_].copy_(t[s])
@@ -777,13 +861,18 @@ def run_e2e(torch, layer, batch, graph, raw_in, q_in, iq_in, iqs_in, hw_in, out,
         torch.cuda.synchronize()
         e0 = torch.cuda.Event(enable_timing=True); e1 = torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(main):
+            h0 = time.perf_counter()
             e0.record(main)
             g.replay()
             e1.record(main)
         main.synchronize()
+        host_times.append((time.perf_counter() - h0) * 1e3)
         times.append(e0.elapsed_time(e1))
     ms = statistics.mean(times)
+    host_ms = statistics.mean(host_times)
     return {"value": round(S / (ms * 1e-3), 1), "unit": UNIT, "ms_per_step": round(ms, 4),
+            "host_clock": {"value": round(S / (host_ms * 1e-3), 1), "ms_per_step": round(host_ms, 4),
+                           "timing": "host perf_counter from before the replay to after the stream synchronise"},
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": n,
             "api": "Layer.step (csa_compress, csa_attend_window | csa_index_topk, csa_attend_topk) with the "
                    "host copies, one CUDA graph per step"}
@@ -896,7 +985,19 @@ def main():
             print(json.dumps(line))
         return
     assert args.warmup >= 3, "at least 3 warm-up steps"
-    if args.workload != "csa_decode":
+    if args.workload == "compress_1m":
+        res = run_gpu_compress(args, rank, world, local)
+        if rank == 0:
+            print(json.dumps({"metric": "raw KV tokens compressed per second (CSA, m = 4, overlapping)",
+                              "value": round(job_value(res["per_rank_queries"], world, res["ms"]), 1),
+                              "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                              "ms_per_step": round(res["ms"], 5), "higher_is_better": True, "scaling": "weak",
+                              "vs_baseline": None, "dtype": "bf16 in, fp8 e4m3 + bf16 rope + f32 scale out, fp32 math",
+                              "data": "synthetic", "config": res["config"], "roofline": res["roofline"],
+                              "clocks": res["clocks"], "e2e": None, "gpu_launches": res["launches"] * args.steps,
+                              "device_status_ok": res["status_ok"]}))
+        return
+    if args.workload not in ("csa_decode", "csa_decode_1m"):
         if args.workload == "attention_sink":
             res = run_gpu_sink(args, rank, world, local)
             if rank == 0:
@@ -937,20 +1038,22 @@ def main():
                               "e2e": None, "gpu_launches": res["launches"] * args.steps,
                               "device_status_ok": res["status_ok"]}))
         return
-    res = run_gpu(args, rank, world, local)
+    wl = synth.CONFIGS[args.workload]
+    res = run_gpu(args, rank, world, local, wl)
     if rank == 0:
         value = job_value(res["per_rank_queries"], world, res["ms"])
         line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": round(res["ms"], 5), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "fp8/fp4 storage, bf16/f16 MMA, fp32 accumulate",
                 "data": "synthetic",
-                "config": workload_config({"parallelism": f"replicas x{world} (independent sequences per GPU)",
+                "config": workload_config(wl=wl, extra={"parallelism": f"replicas x{world} (independent sequences per GPU)",
                                            "stage_ms_source": "separate replays of a serialised copy of the step with event nodes between calls (the timed step runs compress and attend_window next to index_topk)",
                                            "stage_ms": {k_: round(v, 5) for k_, v in res["stages"].items()}}),
-                "roofline": res["roofline"], "roofline_index": res["roofline_index"], "clocks": res["clocks"],
+                "roofline": res["roofline"], "roofline_other": res["roofline_other"],
+                "roofline_step": res["roofline_step"], "clocks": res["clocks"],
                 "e2e": res["e2e"],
                 "gpu_launches": res["launches"], "device_status_ok": res["status_ok"]}
-        if not args.no_cpu_baseline and world == 1:
+        if not args.no_cpu_baseline and world == 1 and wl is WL:
             line["cpu_baseline"] = cpu_baseline()
         print(json.dumps(line))
 

@@ -180,6 +180,8 @@ lcs_status compress_common(const lcs_batch* batch, const void* raw, const lcs_co
   p.new_rows = make_rows(state->new_rows);
   if (!have_new) p.new_rows.nope = nullptr;
   p.window = make_rows(state->window);
+  // pending rows reach back at most 2m - 1 tokens (overlap) and the ring 128 tokens
+  p.state_tail = std::max(LCSA_WINDOW, slots);
   p.status = dev_status;
   return from_cuda(launch_compress(p, entries->dim, batch->max_new, static_cast<cudaStream_t>(stream)));
 }

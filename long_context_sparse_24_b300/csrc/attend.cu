@@ -531,12 +531,11 @@ __global__ void __launch_bounds__(D / 4) attend_combine_kernel(AttendParams p) {
 template <int D, int FMT, int MT>
 static cudaError_t launch_attend_t(const AttendParams& p, int total_new, cudaStream_t st) {
   using L = AttendSmem<D, FMT, MT>;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(attend_kernel<D, FMT, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static PerDeviceOnce attr;
+  cudaError_t ea = once_per_device(attr, [] {
+    return cudaFuncSetAttribute(attend_kernel<D, FMT, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+  });
+  if (ea != cudaSuccess) return ea;
   const int hgroups = (p.heads + L::HG - 1) / L::HG;
   dim3 grid(total_new, hgroups, p.splits);
   attend_kernel<D, FMT, MT><<<grid, 256, L::kBytes, st>>>(p);

@@ -538,12 +538,11 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
 
 cudaError_t launch_attend_tc(const AttendParams& p, int total_new, cudaStream_t st) {
   if (p.rows_per_split == kTileRows) return launch_attend_tc1(p, total_new, st);   // one tile per CTA
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(attend_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TcAttSmem::kBytes);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static PerDeviceOnce attr;
+  cudaError_t ea = once_per_device(attr, [] {
+    return cudaFuncSetAttribute(attend_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TcAttSmem::kBytes);
+  });
+  if (ea != cudaSuccess) return ea;
   const int z = p.part == 1 ? 1 : (p.part == 2 ? p.entry_splits : p.splits);
   dim3 grid(total_new, (p.heads + kHeads - 1) / kHeads, z);
   attend_tc_kernel<<<grid, kThreads, TcAttSmem::kBytes, st>>>(p);

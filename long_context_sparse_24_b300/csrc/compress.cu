@@ -271,12 +271,15 @@ __global__ void __launch_bounds__(256) compress_state_kernel(CompressParams p) {
   const int b = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const SeqSpan sp = seq_span(p.cu_new, p.seq_len, b);
-  const int i = blockIdx.x * 8 + warp;
+  // without new_rows only the last state_tail tokens can matter (pending rows, window ring)
+  const int first = (p.new_rows.nope == nullptr && p.state_tail > 0) ? max(0, sp.qn - p.state_tail) : 0;
+  const int i = first + blockIdx.x * 8 + warp;
   if (i >= sp.qn) return;
   const int t = sp.n0() + i;
   const int m = p.m;
   const int full = sp.n1 / m;
   const int keep_lo = p.overlap ? (full - 1) * m : full * m;
+  if (t < keep_lo && p.new_rows.nope == nullptr && t < sp.n1 - kWindow) return;   // neither kept nor stored
   const __nv_bfloat16* src = p.raw + (long long)(sp.q0 + i) * D;
   float v[PL][8];
   load_row<D>(src, lane, v);
@@ -357,7 +360,10 @@ cudaError_t launch_compress(const CompressParams& p, int D, int max_new, cudaStr
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || max_new == 0) return e;
-  dim3 g2((max_new + 7) / 8, p.num_seqs);
+  // without new_rows only the last state_tail tokens of each sequence go to the pending ring or
+  // the window ring: launch warps for those alone
+  const int warps = (p.new_rows.nope == nullptr && p.state_tail > 0 && p.state_tail < max_new) ? p.state_tail : max_new;
+  dim3 g2((warps + 7) / 8, p.num_seqs);
   if (D == 512) compress_state_kernel<512><<<g2, 256, 0, st>>>(p);
   else compress_state_kernel<128><<<g2, 256, 0, st>>>(p);
   return cudaGetLastError();

@@ -327,14 +327,13 @@ namespace {
 template <int HI, int QH>
 cudaError_t launch_tc_t(const CUtensorMap& tmap, const IndexParams& p, int max_entries, int sms, cudaStream_t st) {
   using L = TcSmem<QH, QH / HI>;
-  static bool attr = false;
-  if (!attr) {
+  static PerDeviceOnce attr;
+  cudaError_t ea = once_per_device(attr, [] {
     cudaError_t e = cudaFuncSetAttribute(index_tc_kernel<HI, QH>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(index_tc_kernel<HI, QH>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(index_tc_kernel<HI, QH>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    return e;
+  });
+  if (ea != cudaSuccess) return ea;
   // resident CTAs per SM: shared memory (228 KB per SM, 1 KB reserved per CTA) and tensor memory
   int occ = (228 * 1024) / (L::kBytes + 1024);
   const int occ_tmem = 512 / (int)tmem_cols_for(L::N);

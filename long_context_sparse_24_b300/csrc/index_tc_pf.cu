@@ -337,15 +337,15 @@ template <int HI, int QPS>
 cudaError_t launch_pf_t(const CUtensorMap& tmap, const IndexParams& p, int max_new, int max_entries,
                         cudaStream_t st) {
   using L = PfSmem<HI, QPS>;
-  static bool attr = false;
-  if (!attr) {
+  static PerDeviceOnce attr;
+  cudaError_t ea = once_per_device(attr, [] {
     cudaError_t e = cudaFuncSetAttribute(index_tc_pf_kernel<HI, QPS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          L::kBytes);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(index_tc_pf_kernel<HI, QPS>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(index_tc_pf_kernel<HI, QPS>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    return e;
+  });
+  if (ea != cudaSuccess) return ea;
   const int tiles = (max_entries + kTile - 1) / kTile;
   if (tiles == 0) return cudaSuccess;
   const int tpc_cap = kMaxPages * p.paging.epb / kTile;   // a run spans at most kMaxPages pages

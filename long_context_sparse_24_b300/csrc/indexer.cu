@@ -423,18 +423,16 @@ cudaError_t launch_index_scores(const IndexParams& p, int rank, int max_new, int
   dim3 grid((max_entries + CHUNK - 1) / CHUNK, (max_new + QG - 1) / QG, p.num_seqs);
   if (grid.x == 0 || grid.y == 0) return cudaSuccess;
   const size_t smem = p.hist ? (size_t)QG * kTopkHistBins * 4 : 0;
-  static bool attr = false;
-  if (!attr) {
+  static PerDeviceOnce attr;
+  cudaError_t ea = once_per_device(attr, [] {
     const int mx = 8 * kTopkHistBins * 4;
-    cudaFuncSetAttribute(index_score_kernel<4, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
-    cudaFuncSetAttribute(index_score_kernel<2, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
-    cudaFuncSetAttribute(index_score_kernel<1, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
-    cudaFuncSetAttribute(index_score_kernel<4, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
-    cudaFuncSetAttribute(index_score_kernel<2, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
-    cudaError_t e = cudaFuncSetAttribute(index_score_kernel<1, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+    cudaError_t e = cudaSuccess;
+    for (auto fn : {index_score_kernel<4, 4>, index_score_kernel<2, 4>, index_score_kernel<1, 4>,
+                    index_score_kernel<4, 2>, index_score_kernel<2, 2>, index_score_kernel<1, 2>})
+      if (e == cudaSuccess) e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+    return e;
+  });
+  if (ea != cudaSuccess) return ea;
   if (rank == 128) {
     if (NT == 4) index_score_kernel<4, 4><<<grid, 256, smem, st>>>(p);
     else if (NT == 2) index_score_kernel<2, 4><<<grid, 256, smem, st>>>(p);
@@ -451,15 +449,14 @@ cudaError_t launch_topk_select(const uint32_t* keys, const uint32_t* hist, long 
                                const int32_t* seq_len, int num_seqs, int max_new, int m, int k, int32_t* out_idx,
                                int32_t* out_cnt, cudaStream_t st) {
   const size_t smem = sizeof(SelectShared);
-  static bool attr_set = false;
-  if (!attr_set) {
+  static PerDeviceOnce attr;
+  cudaError_t ea = once_per_device(attr, [smem] {
     cudaError_t e = cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
     // two CTAs per SM for long query runs (prefill): ask for the whole carveout as shared memory
-    e = cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    return e;
+  });
+  if (ea != cudaSuccess) return ea;
   dim3 grid(max_new, num_seqs);
   if (grid.x == 0) return cudaSuccess;
   topk_select_kernel<<<grid, kSelThreads, smem, st>>>(keys, hist, ld, cu_new, seq_len, m, k, out_idx, out_cnt);

@@ -1,9 +1,34 @@
 // Kernel parameter blocks and launchers shared by the C ABI layer and the kernel files.
 #pragma once
 
+#include <atomic>
+#include <mutex>
+
 #include "common.cuh"
 
 namespace lcsa {
+
+// Kernel attributes (maximum dynamic shared memory, shared-memory carveout) belong to one device
+// context, so every launcher sets them once per device ordinal, under a lock (launchers may be
+// called from several host threads).
+constexpr int kMaxDevices = 64;
+struct PerDeviceOnce {
+  std::mutex mu;
+  std::atomic<bool> done[kMaxDevices];
+};
+template <typename F>
+cudaError_t once_per_device(PerDeviceOnce& once, F&& set) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (once.done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  std::lock_guard<std::mutex> lock(once.mu);
+  if (once.done[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+  e = set();
+  if (e == cudaSuccess) once.done[dev].store(true, std::memory_order_release);
+  return e;
+}
 
 struct CompressParams {
   const int32_t* cu_new;
@@ -21,6 +46,7 @@ struct CompressParams {
   Paging paging;
   Rows new_rows;   // nope == nullptr: write the window ring instead
   Rows window;
+  int state_tail;  // > 0: without new_rows, only the last state_tail new tokens reach the state
   int32_t* status;
 };
 

@@ -166,6 +166,10 @@ CONFIGS = {
     "csa_decode": Workload("csa_decode_32x128k_h64_d512", seed=1, kind="csa", num_seqs=32, ctx_len=131072,
                            new_tokens=1, heads=64, dim=512, row_format="fp8_split", m=4, overlap=True,
                            index_heads=4, index_rank=128, top_k=512),
+    # the decode batch at a 1M-token context with the larger top-k (k = 1024 for the Pro model)
+    "csa_decode_1m": Workload("csa_decode_32x1m_h64_d512_k1024", seed=1, kind="csa", num_seqs=32,
+                              ctx_len=1048576, new_tokens=1, heads=64, dim=512, row_format="fp8_split", m=4,
+                              overlap=True, index_heads=4, index_rank=128, top_k=1024),
     "csa_prefill": Workload("csa_prefill_1m_plus_16k_h128_d512", seed=2, kind="csa", num_seqs=1,
                             ctx_len=1048576, new_tokens=16384, heads=128, dim=512, row_format="fp8_split",
                             m=4, overlap=True, index_heads=4, index_rank=128, top_k=1024),

@@ -238,8 +238,13 @@ def test_topk_ties_take_lowest_index():
 
 # ---------------------------------------------------------------------------------------- attention
 
-def _attend_case(kind, lengths, new, heads, dim, fmt, m, k, seed=41, scale=None, split=False, sink=None):
-    """Fill an entry cache / window ring / new rows with oracle-quantised rows and run one call."""
+def _attend_case(kind, lengths, new, heads, dim, fmt, m, k, seed=41, scale=None, split=False, sink=None,
+                 corrupt_seq=None, rows_hook=None):
+    """Fill an entry cache / window ring / new rows with oracle-quantised rows and run one call.
+    corrupt_seq: unmap that sequence's first cache block before the call (host-side corruption of
+    the block table); the call must then report LCS_ERR_DEVICE_GUARD and every other sequence must
+    still match the oracle.  rows_hook(b, entry_rows): may change a sequence's entry rows (fp64)
+    before they are quantised."""
     S = len(lengths)
     fmtc = buffers.row_format_code(fmt)
     cap = max(lengths) + 128
@@ -253,7 +258,10 @@ def _attend_case(kind, lengths, new, heads, dim, fmt, m, k, seed=41, scale=None,
         L, q_n = lengths[b], new[b]
         n0 = L - q_n
         ne = L // m
-        ent = oracle.quantize_rows(rng.standard_normal((max(ne, 1), dim)), fmt)
+        ent_f = rng.standard_normal((max(ne, 1), dim))
+        if rows_hook is not None:
+            ent_f = rows_hook(b, ent_f)
+        ent = oracle.quantize_rows(ent_f, fmt)
         if ne:
             sub = {kk: v[:ne] for kk, v in ent.items() if kk != "format"}
             sub["format"] = ent["format"]
@@ -284,6 +292,8 @@ def _attend_case(kind, lengths, new, heads, dim, fmt, m, k, seed=41, scale=None,
         qs.append(queries_np(seed, 0, b, n0, q_n, heads, dim))
     q_bits = np.concatenate(qs)
     q = to_dev_bf16_bits(q_bits)
+    if corrupt_seq is not None:
+        cache.paging.block_table[corrupt_seq, 0] = -1
     out = torch.empty((T, heads, dim), dtype=torch.bfloat16, device=DEV)
     lse = torch.empty((T, heads), dtype=torch.float32, device=DEV)
     scale = scale if scale is not None else 1 / math.sqrt(dim)
@@ -322,12 +332,18 @@ def _attend_case(kind, lengths, new, heads, dim, fmt, m, k, seed=41, scale=None,
     if sink is not None:
         lcsa.lcs_attention_sink(out, lse, torch.from_numpy(sink.astype(np.float32)).to(DEV))
     torch.cuda.synchronize()
-    assert_status_ok(st)
+    if corrupt_seq is None:
+        assert_status_ok(st)
+    else:
+        assert int(st.item()) == 6, f"device status {int(st.item())}, expected LCS_ERR_DEVICE_GUARD"
     o = bf16_tensor_to_f64(out); l = lse.cpu().numpy()
     qf = bits_to_f64(q_bits)
     qi = 0
     for b in range(S):
         n0 = lengths[b] - new[b]
+        if b == corrupt_seq:
+            qi += new[b]
+            continue
         for i in range(new[b]):
             t = n0 + i
             if kind == "csa":
@@ -363,17 +379,21 @@ def test_attend_matches_oracle(kind, lengths, new, heads, dim, fmt, m, k):
     _attend_case(kind, lengths, new, heads, dim, fmt, m, k)
 
 
-@pytest.mark.parametrize("kind,lengths,new,heads,dim,fmt,m,k", [
-    ("csa", [2000, 4100, 300], [1, 1, 1], 64, 512, "fp8_split", 4, 512),
-    ("csa", [900, 2200], [40, 9], 64, 512, "fp8_split", 4, 64),
-    ("hca", [3000], [17], 64, 512, "fp8_split", 128, 0),
-    ("csa", [50, 700], [50, 20], 8, 128, "bf16", 4, 64),
+@pytest.mark.parametrize("kind,lengths,new,heads,dim,fmt,m,k,split", [
+    ("csa", [2000, 4100, 300], [1, 1, 1], 64, 512, "fp8_split", 4, 512, False),
+    ("csa", [2000, 4100, 300], [1, 1, 1], 64, 512, "fp8_split", 4, 512, True),   # window part apart
+    ("csa", [900, 2200], [40, 9], 64, 512, "fp8_split", 4, 64, False),
+    ("hca", [3000], [17], 64, 512, "fp8_split", 128, 0, False),
+    ("csa", [50, 700], [50, 20], 8, 128, "bf16", 4, 64, False),
+    # several tiles per CTA: lse from the online softmax across tiles
+    ("hca", [40000 - 700 * i for i in range(40)], [1] * 40, 64, 512, "fp8_split", 128, 0, False),
+    ("csa", [3000 + 37 * i for i in range(120)], [1] * 120, 64, 512, "fp8_split", 4, 1024, False),
 ])
-def test_attention_sink_matches_oracle(kind, lengths, new, heads, dim, fmt, m, k):
+def test_attention_sink_matches_oracle(kind, lengths, new, heads, dim, fmt, m, k, split):
     """Attention, then lcs_attention_sink with per-head sink logits around the logits' range,
     against the oracle's softmax with the sink term (outputs and lse)."""
     sink = np.random.default_rng(7).standard_normal(heads) * 2.0
-    _attend_case(kind, lengths, new, heads, dim, fmt, m, k, sink=sink)
+    _attend_case(kind, lengths, new, heads, dim, fmt, m, k, sink=sink, split=split)
 
 
 @pytest.mark.parametrize("lengths,new,heads,dim,fmt,k", [

@@ -410,6 +410,64 @@ def test_layer_full_topk_equals_dense_over_visible():
         assert np.allclose(out["o"][i], ref, rtol=1e-13, atol=1e-13)
 
 
+def _brute_rows(t, selected, entries, window_rows, window=128):
+    """The rows a CSA query attends, gathered one by one: the listed entries in list order, then
+    the window tokens from max(0, t - window + 1) up to t itself."""
+    rows = []
+    for j in selected:
+        rows.append(entries[int(j)])
+    p = max(0, t - window + 1)
+    while p <= t:
+        rows.append(window_rows[p])
+        p += 1
+    return np.array(rows)
+
+
+def _softmax_attend_loops(q, rows, scale):
+    """One head at a time, one row at a time: max, exponentials, weighted sum (plain loops)."""
+    h_n, d = q.shape
+    out = np.zeros((h_n, rows.shape[1]))
+    for h in range(h_n):
+        logits = [scale * float(np.dot(q[h], r)) for r in rows]
+        mx = max(logits)
+        w = [math.exp(z - mx) for z in logits]
+        tot = sum(w)
+        for wi, r in zip(w, rows):
+            out[h] += (wi / tot) * r
+    return out
+
+
+def test_csa_query_rows_gathers_the_selected_entries():
+    # k < N(t): only the listed entries join the window rows, in list order, whatever their positions
+    ent = RNG.standard_normal((300, 16))
+    win = RNG.standard_normal((1300, 16))
+    for t, sel in [(1199, np.array([0, 7, 8, 150, 299])), (1199, np.array([299, 3])), (40, np.array([5])),
+                   (1000, np.sort(RNG.choice(250, size=37, replace=False))), (7, np.zeros(0, np.int64))]:
+        got = oracle.csa_query_rows(t, sel, ent, win)
+        ref = _brute_rows(t, sel, ent, win)
+        assert got.shape == ref.shape and np.array_equal(got, ref), (t, sel[:4])
+
+
+def test_csa_layer_top_k_smaller_than_visible_entries_by_loops():
+    # the whole layer with k < N(t): the top-k of explicitly computed scores (a full sort per query),
+    # the rows gathered one by one and a loop softmax give the oracle's outputs
+    raw, kw = _small_layer(13, 240, k=5)
+    out = oracle.csa_layer(raw, **kw)
+    ent = out["entries"]["deq"]; win = out["window"]["deq"]
+    qv = oracle.blockscaled_values(kw["idx_q_codes"], kw["idx_q_scales"])
+    kv = oracle.blockscaled_values(kw["idx_k_codes"], kw["idx_k_scales"])
+    for i, t in enumerate(kw["q_pos"]):
+        n = oracle.visible_entries(int(t), 4)
+        assert n > kw["top_k"]
+        sc = [sum(kw["head_w"][i, h] * float(np.dot(qv[i, h], kv[j])) for h in range(qv.shape[1]))
+              for j in range(n)]
+        order = sorted(range(n), key=lambda j: (-sc[j], j))
+        sel = sorted(order[:kw["top_k"]])
+        assert list(out["topk"][i]) == sel
+        ref = _softmax_attend_loops(kw["q"][i], _brute_rows(int(t), sel, ent, win), kw["softmax_scale"])
+        assert np.allclose(out["o"][i], ref, rtol=1e-12, atol=1e-12)
+
+
 # ------------------------------------------------------------------------------------------------
 # Block-scaled FP4 quantisation (the indexer's key / query production, x-techcon section 4)
 # ------------------------------------------------------------------------------------------------

@@ -41,7 +41,7 @@ def _case(seed, lengths, new, m=4, heads=4, rank=128):
             to_dev_f32(np.concatenate(hw)))
 
 
-def _call_c_abi_noalloc(batch, q_fp4, q_sc, hw, heads, cache, m, k, out_idx, out_cnt, st):
+def _call_c_abi_noalloc(batch, q_fp4, q_sc, hw, heads, cache, m, k, out_idx, out_cnt, st, flags=0):
     """Call the exported C symbol directly (the C ABI, no Python wrapper logic)."""
     lib = ctypes.CDLL(lcsa.LIB_PATH)
     fn = lib.csa_index_topk_noalloc
@@ -51,7 +51,8 @@ def _call_c_abi_noalloc(batch, q_fp4, q_sc, hw, heads, cache, m, k, out_idx, out
                    vp, vp, vp, vp]
     b, kk, pg = batch.c(), cache.keys.c(), cache.paging.c()
     return fn(ctypes.byref(b), q_fp4.data_ptr(), q_sc.data_ptr(), hw.data_ptr(), heads, ctypes.byref(kk),
-              ctypes.byref(pg), m, k, 0, out_idx.data_ptr(), out_cnt.data_ptr(), st.data_ptr(),
+              ctypes.byref(pg), m, k, flags, out_idx.data_ptr() if out_idx is not None else None,
+              out_cnt.data_ptr() if out_cnt is not None else None, st.data_ptr(),
               torch.cuda.current_stream().cuda_stream)
 
 
@@ -77,6 +78,33 @@ def test_noalloc_topk_equals_workspace_entry_point_twice(first, second):
         assert_status_ok(st)
         assert torch.equal(got_idx, ref_idx)
         assert torch.equal(got_cnt, ref_cnt)
+
+
+def test_noalloc_score_then_select_phases_share_the_scratch():
+    """A scoring-only call leaves its results in the shared scratch; the selection-only call that
+    follows on the same stream reads them.  Together they equal one call with a caller-provided
+    workspace (same batch, m and k)."""
+    seed, lengths, new, k, m, heads = 63, [7000, 300, 12000], [1, 2, 1], 256, 4, 4
+    cache, batch, q_fp4, q_sc, hw = _case(seed, lengths, new)
+    T = batch.total_new
+    ref_idx = torch.full((T, k), -5, dtype=torch.int32, device=DEV)
+    ref_cnt = torch.full((T,), -5, dtype=torch.int32, device=DEV)
+    wsb = lcsa.lcs_index_topk_workspace(batch, m, k)
+    lcsa.csa_index_topk(batch, q_fp4, q_sc, hw, heads, cache.keys, cache.paging, m, k, 0, ref_idx, ref_cnt,
+                        workspace(wsb), wsb)
+    got_idx = torch.full((T, k), -9, dtype=torch.int32, device=DEV)
+    got_cnt = torch.full((T,), -9, dtype=torch.int32, device=DEV)
+    st = dev_status()
+    rc = _call_c_abi_noalloc(batch, q_fp4, q_sc, hw, heads, cache, m, k, None, None, st,
+                             flags=lcsa.LCS_INDEX_SCORE_ONLY)
+    assert rc == 0, lcsa.lcs_status_string(rc)
+    rc = _call_c_abi_noalloc(batch, q_fp4, q_sc, hw, heads, cache, m, k, got_idx, got_cnt, st,
+                             flags=lcsa.LCS_INDEX_SELECT_ONLY)
+    assert rc == 0, lcsa.lcs_status_string(rc)
+    torch.cuda.synchronize()
+    assert_status_ok(st)
+    assert torch.equal(got_idx, ref_idx)
+    assert torch.equal(got_cnt, ref_cnt)
 
 
 def test_noalloc_rejects_requests_beyond_its_scratch():
