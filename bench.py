@@ -46,7 +46,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="csa_decode",
                     choices=["csa_decode", "csa_decode_1m", "hca_decode", "mixed_decode", "csa_prefill",
-                             "compress_1m", "index_key_quantize", "attention_sink"],
+                             "compress_1m", "index_key_quantize", "attention_sink", "tensor_peak"],
                     help="csa_decode is the headline line; the others measure the 1M-context CSA decode, the "
                          "HCA decode, the mixed ragged multi-layer and the CSA prefill workloads, and the "
                          "compression of a 1M-token context, with the same timing rules")
@@ -661,6 +661,40 @@ def run_gpu_prefill(args, rank, world, local, wl):
 # GPU arm, indexer key production: block-scaled FP4 of the keys of a 1M-token CSA context
 # ---------------------------------------------------------------------------------------------
 
+def run_gpu_tensor_peak(args, rank, world, local):
+    """The tensor-pipe rates the roofline fractions of the tensor-bound kernels are taken against:
+    lcs_mma_probe, one CTA per SM issuing back-to-back tcgen05 MMAs of M = 128, N = 256 (kind 0:
+    kind::f8f6f4 with E2M1 operands, the indexer's MMA; kind 1: kind::f16, the attention's MMA),
+    timed with CUDA events, best of the timed launches."""
+    import torch
+    import long_context_sparse_24_b300 as lcsa
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if lcsa.lcs_device_check() != 0:
+        raise SystemExit("liblcsa needs a compute-capability 10.3 GPU")
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    mmas = 16384
+    out = {}
+    with ClockSampler(local) as clk:
+        for kind, kstep, name in ((0, 32, "f8f6f4_e2m1"), (1, 16, "f16")):
+            flop = 2.0 * 128 * 256 * kstep * mmas * sms
+            times = []
+            for it in range(args.warmup + args.steps):
+                e0 = torch.cuda.Event(enable_timing=True); e1 = torch.cuda.Event(enable_timing=True)
+                e0.record()
+                lcsa.lcs_mma_probe(kind, mmas, sms, st)
+                e1.record()
+                torch.cuda.synchronize()
+                if it >= args.warmup:
+                    times.append(e0.elapsed_time(e1))
+            out[name] = {"tflops": round(flop / (min(times) * 1e-3) / 1e12, 1),
+                         "ms": round(min(times), 4), "flop_per_launch": flop}
+    status_ok = int(st.item()) == 0
+    return {"rates": out, "clocks": clk.summary(), "status_ok": status_ok, "sms": sms, "mmas": mmas}
+
+
 def run_gpu_compress(args, rank, world, local):
     """csa_compress of a whole 1,048,576-token context of one sequence in one call (BF16 rows of
     D = 512 in, 262,144 entries of 580 B out, the window ring and pending rows updated), timed per
@@ -985,6 +1019,19 @@ def main():
             print(json.dumps(line))
         return
     assert args.warmup >= 3, "at least 3 warm-up steps"
+    if args.workload == "tensor_peak":
+        res = run_gpu_tensor_peak(args, rank, world, local)
+        if rank == 0:
+            r = res["rates"]
+            print(json.dumps({"metric": "tcgen05 tensor-pipe rate (probe)", "value": r["f8f6f4_e2m1"]["tflops"],
+                              "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                              "ms_per_step": r["f8f6f4_e2m1"]["ms"], "higher_is_better": True, "scaling": "weak",
+                              "vs_baseline": None, "dtype": "e2m1 x e2m1 -> f32 (kind::f8f6f4)", "data": "synthetic",
+                              "config": {"workload": "tcgen05_mma_probe_m128_n256", "ctas": res["sms"],
+                                         "mmas_per_cta": res["mmas"], "timing": "best of the timed launches"},
+                              "rates": r, "clocks": res["clocks"], "e2e": None,
+                              "gpu_launches": 2 * args.steps, "device_status_ok": res["status_ok"]}))
+        return
     if args.workload == "compress_1m":
         res = run_gpu_compress(args, rank, world, local)
         if rank == 0:

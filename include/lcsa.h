@@ -19,7 +19,8 @@
  * Conventions for every entry point
  *  - Pointers marked "device" are CUDA device pointers; "host" are host pointers.  Every
  *    buffer is owned by the caller.  The library allocates nothing, frees nothing, never
- *    synchronises and keeps no pointer after a call returns.  It is stateless and reentrant.
+ *    synchronises and keeps no pointer after a call returns.  It is reentrant and keeps no state
+ *    between calls apart from the bound of its device waits (lcs_set_wait_polls).
  *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).  Calls
  *    enqueue kernels and return; results are ready once the stream reaches them.
  *  - Argument errors are reported synchronously by the return value (nothing is launched).
@@ -48,10 +49,11 @@
 extern "C" {
 #endif
 
-#define LCSA_ABI_VERSION 1
+#define LCSA_ABI_VERSION 2
 #define LCSA_WINDOW 128      /* sliding-window rows (x-techcon section 2, CSA step 3)      */
 #define LCSA_ROPE_DIMS 64    /* BF16 RoPE slice (chenxutan.com/d/4230, section 4.5)         */
 #define LCSA_BLOCK_TOKENS 128 /* raw tokens per cache block, LCM(4,128) (x-techcon sec. 4) */
+#define LCSA_DEFAULT_WAIT_POLLS (1u << 20) /* polls of a bounded device wait (~1 us each)  */
 
 typedef enum {
   LCS_OK = 0,
@@ -123,16 +125,27 @@ typedef struct {
   void* pending;
   int32_t pending_slots;
   lcs_rows new_rows;
+  void* pending_scores;      /* per-channel compressors only: bf16[num_seqs][pending_slots][D], the
+                                score rows of the pending tokens (same ring as `pending`); else NULL */
 } lcs_state;
 
-/* Compressor parameters: z_t = w . k_t + bias[o], o = offset of token t in the entry's window
- * (0 .. 2m-1 with overlap, 0 .. m-1 without).  Entry j uses tokens [(j-1)m, (j+1)m) with
- * overlap, [jm, (j+1)m) without; tokens before 0 are left out of the softmax. */
+/* Compressor parameters.  Entry j uses tokens [(j-1)m, (j+1)m) with overlap, [jm, (j+1)m)
+ * without; o = offset of token t in the entry's window (0 .. 2m-1 with overlap, 0 .. m-1
+ * without); tokens before 0 are left out of the softmax.
+ *  scalar weights (scores NULL; x-techcon section 2, CSA step 1):
+ *    z_t = w . k_t + bias[o]; alpha = softmax over the window's rows; c = sum_t alpha_t k_t.
+ *  per-channel weights (scores set; the compressor sketch of chenxutan.com/d/4230, section 4.2,
+ *  with a per-offset bias): every raw token t comes with a score row s_t (D values, the output of
+ *  the compressor's own score projection, computed by the caller like the raw KV rows);
+ *    z[t,d] = s_t[d] + bias[o][d]; alpha[.,d] = softmax over the window's rows, channel by
+ *    channel; c[d] = sum_t alpha[t,d] k_t[d].  Requires m <= 4 and state->pending_scores. */
 typedef struct {
-  const float* w;            /* device f32[D]                                                */
-  const float* bias;         /* device f32[2m] (overlap) or f32[m]                            */
+  const float* w;            /* device f32[D] (scalar weights; unused with scores)           */
+  const float* bias;         /* device f32[2m] or f32[m]; with scores f32[2m][D] or f32[m][D] */
   int32_t m;                 /* ratio; a power of two dividing 128                            */
   int32_t overlap;           /* 1: overlapping windows of 2m rows                             */
+  const void* scores;        /* device bf16[total_new][D]: score rows of this call's new tokens
+                                (row = global token index), or NULL for scalar weights          */
 } lcs_compressor;
 
 /* Indexer keys: one per compressed entry, paged like the entries. */
@@ -174,15 +187,27 @@ lcs_status lcs_window_commit(const lcs_batch* batch, const lcs_state* state, int
  *   q_fp4   device uint8[total_new][heads][rank/2]    q_scale device uint8[total_new][heads][rank/32]
  *   head_w  device f32[total_new][heads] or NULL (all 1)
  *   heads in {1, 2, 4, 8}; rank in {64, 128}; 1 <= k <= 4096.
- * Workspace: device, >= lcs_index_topk_workspace(batch, m, k) bytes, 256-byte aligned.
- * Phases: a call runs the scoring phase (score keys and per-query histograms into the workspace)
- * and then the selection phase (out_idx, out_cnt).  With LCS_INDEX_SCORE_ONLY it runs only the
- * first, with LCS_INDEX_SELECT_ONLY only the second, which reads what an earlier scoring call
- * with the same batch, m and workspace left there (it must be ordered after it: same stream or an
- * event); the pair gives exactly the result of one call.  Both flags at once: LCS_ERR_INVALID_ARG.
- * The split lets other work (e.g. the window part of attention) run next to the selection, which
- * occupies one CTA per query. */
-size_t lcs_index_topk_workspace(const lcs_batch* batch, int32_t m, int32_t k);
+ * Workspace: device, >= lcs_index_topk_workspace(batch, heads, keys, paging, m, k) bytes (the
+ * same arguments as the call), 256-byte aligned.  Its first lcs_index_topk_workspace_zeroed()
+ * bytes must hold zeros before the first call on it (e.g. cudaMemset once after allocation): they
+ * are per-sequence counters that every completed call leaves at zero again.  After a call whose
+ * device status is LCS_ERR_TIMEOUT, zero them again before reusing the workspace.
+ * How the work is split: at rank 128 with 1, 2, 4 or 8 heads and 2k + 256 <= 4096, the scoring
+ * runs on the tensor cores with the top-k fused into it -- a CTA scores a run of the cache for a
+ * group of up to 4 queries of a sequence and keeps each query's k best entries, and the group's
+ * last CTA merges the runs' lists -- and the workspace holds only those lists (about 8 k bytes per
+ * query and run); otherwise every score's order-preserving key is written to the workspace (4
+ * bytes per query and visible entry) and a selection pass reads them back.
+ * Phases: a call runs the scoring phase and the selection phase.  With LCS_INDEX_SCORE_ONLY it
+ * runs only the first (the scores, or the runs' lists, into the workspace), with
+ * LCS_INDEX_SELECT_ONLY only the second (the selection from the workspace into out_idx,
+ * out_cnt), which reads what an earlier scoring call with the same batch, heads, keys, paging, m,
+ * k and workspace left there (it must be ordered after it: same stream or an event); the pair gives
+ * exactly the result of one call.  Both flags at once: LCS_ERR_INVALID_ARG. */
+size_t lcs_index_topk_workspace(const lcs_batch* batch, int32_t heads, const lcs_index_keys* keys,
+                                const lcs_paging* paging, int32_t m, int32_t k);
+/* Leading bytes of that workspace that must be zero before its first use (see above). */
+size_t lcs_index_topk_workspace_zeroed(const lcs_batch* batch);
 lcs_status csa_index_topk(const lcs_batch* batch, const uint8_t* q_fp4, const uint8_t* q_scale,
                           const float* head_w, int32_t heads, const lcs_index_keys* keys,
                           const lcs_paging* paging, int32_t m, int32_t k, int32_t flags,
@@ -200,8 +225,14 @@ lcs_status csa_index_scores(const lcs_batch* batch, const uint8_t* q_fp4, const 
  * memory from its own pool at start-up): no workspace argument; the scratch is a fixed array of
  * LCSA_NOALLOC_SCRATCH_BYTES in the library's device image, reserved on every GPU that loads the
  * library until the process exits.  Not a step of the method: the pages have no counterpart.
- *  - Requests needing more scratch than that (lcs_index_topk_workspace(batch, m, k) >
- *    LCSA_NOALLOC_SCRATCH_BYTES) return LCS_ERR_WORKSPACE and launch nothing.
+ *  - Requests needing more scratch than that (lcs_index_topk_workspace(batch, heads, keys, paging,
+ *    m, k) > LCSA_NOALLOC_SCRATCH_BYTES) return LCS_ERR_WORKSPACE and launch nothing.
+ *  - The array starts as zeros when the library is loaded and every completed call leaves its
+ *    leading counters at zero (see csa_index_topk); a call whose device status is LCS_ERR_TIMEOUT
+ *    may leave them non-zero, and later calls then report LCS_ERR_DEVICE_GUARD.
+ *  - A call with LCS_INDEX_SELECT_ONLY reads what the last LCS_INDEX_SCORE_ONLY call left in the
+ *    array: same batch, heads, keys, paging, m and k, ordered after it, with no other call to this
+ *    entry point in between.
  *  - Runs on the current device.  Its first call on a device looks up the array's device
  *    address (cudaGetSymbolAddress); make that first call before any stream capture.
  *  - Calls no allocator.  All calls share the array: calls whose kernels overlap on the GPU
@@ -225,8 +256,10 @@ lcs_status csa_index_topk_noalloc(const lcs_batch* batch, const uint8_t* q_fp4, 
  *   q       device bf16[total_new][heads][D]    out device bf16[total_new][heads][D]
  *   out_lse device f32[total_new][heads] (natural log of the softmax denominator) or NULL
  *   heads in {8, 16, 64, 128} (multiples of 16 up to 128, or 8); D in {128, 512}.
- * FP8-split rows: query values of the FP8 dims must lie within the f16 range, and row scales
- * must stay below 256 (|x| < 114688 before quantisation).
+ * FP8-split rows: query values of the FP8 dims must lie within the f16 range; a row's scale s_r
+ * must stay below 256 (|x| < 114688 before quantisation) and, at D = 512, its RoPE values within
+ * 65504 * s_r (the kernels compute in f16 on the rows divided by s_r).  A row outside these bounds
+ * is left out of the softmax and LCS_ERR_DEVICE_GUARD is reported.
  * Workspace: device, >= lcs_attend_workspace(batch, heads, D, max_rows) bytes, where max_rows
  * bounds the rows of one query (CSA: k + 128; HCA: floor(max_seq_len/m) + 128). */
 size_t lcs_attend_workspace(const lcs_batch* batch, int32_t heads, int32_t dim, int32_t max_rows);
@@ -296,6 +329,23 @@ lcs_status lcs_attention_sink(void* out, float* out_lse, const float* sink, int6
  * pageable pointer of a non-empty copy; nothing is launched then.  Capturable in a CUDA graph
  * (the pointer lookups happen on the host at call time). */
 lcs_status lcs_stage_copy(int32_t n, void* const* dst, const void* const* src, const size_t* bytes, void* stream);
+
+/* --- bounded waits --------------------------------------------------------------------------
+ * Every wait of a kernel on one of its own pipeline stages (tensor-core completion, TMA arrival)
+ * gives up after a bounded number of polls of up to about a microsecond each, records
+ * LCS_ERR_TIMEOUT in the call's device status word and lets the kernel finish without its
+ * results (it waits for its own copies still in flight first).  The bound applies to the calls
+ * made after this one on any host thread; default LCSA_DEFAULT_WAIT_POLLS (about a second).  0 makes
+ * every such wait give up at once: for testing the error path only.  Returns the previous bound. */
+uint32_t lcs_set_wait_polls(uint32_t polls);
+
+/* --- tensor-pipe throughput probe (measurement; not a step of the method) ---------------------
+ * Launches `ctas` CTAs (one per SM is the intended use) that each issue mmas_per_cta tcgen05 MMAs of
+ * M = 128, N = 256 back to back from shared memory into tensor memory: kind 0 = kind::f8f6f4 with
+ * E2M1 operands, K = 32 (the indexer's MMA); kind 1 = kind::f16 with F16 operands, K = 16 (the
+ * attention's MMA).  The caller times the launch and divides 2 * 128 * 256 * K * mmas_per_cta * ctas
+ * by the time.  mmas_per_cta >= 64.  Errors: LCS_ERR_UNSUPPORTED for other kinds or sizes. */
+lcs_status lcs_mma_probe(int32_t kind, int32_t mmas_per_cta, int32_t ctas, int32_t* dev_status, void* stream);
 
 /* --- library information -------------------------------------------------------------------- */
 int32_t lcs_abi_version(void);

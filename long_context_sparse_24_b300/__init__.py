@@ -58,11 +58,12 @@ class lcs_paging(ctypes.Structure):
 
 
 class lcs_state(ctypes.Structure):
-    _fields_ = [("window", lcs_rows), ("pending", c_vp), ("pending_slots", c_i32), ("new_rows", lcs_rows)]
+    _fields_ = [("window", lcs_rows), ("pending", c_vp), ("pending_slots", c_i32), ("new_rows", lcs_rows),
+                ("pending_scores", c_vp)]
 
 
 class lcs_compressor(ctypes.Structure):
-    _fields_ = [("w", c_vp), ("bias", c_vp), ("m", c_i32), ("overlap", c_i32)]
+    _fields_ = [("w", c_vp), ("bias", c_vp), ("m", c_i32), ("overlap", c_i32), ("scores", c_vp)]
 
 
 class lcs_index_keys(ctypes.Structure):
@@ -82,7 +83,10 @@ _SIGS = {
     "hca_compress": (c_i32, [P(lcs_batch), c_vp, P(lcs_compressor), P(lcs_state), P(lcs_rows), P(lcs_paging),
                              c_vp, c_vp]),
     "lcs_window_commit": (c_i32, [P(lcs_batch), P(lcs_state), c_vp, c_vp]),
-    "lcs_index_topk_workspace": (c_sz, [P(lcs_batch), c_i32, c_i32]),
+    "lcs_index_topk_workspace": (c_sz, [P(lcs_batch), c_i32, P(lcs_index_keys), P(lcs_paging), c_i32, c_i32]),
+    "lcs_index_topk_workspace_zeroed": (c_sz, [P(lcs_batch)]),
+    "lcs_set_wait_polls": (ctypes.c_uint32, [ctypes.c_uint32]),
+    "lcs_mma_probe": (c_i32, [c_i32, c_i32, c_i32, c_vp, c_vp]),
     "csa_index_topk": (c_i32, [P(lcs_batch), c_vp, c_vp, c_vp, c_i32, P(lcs_index_keys), P(lcs_paging), c_i32,
                                c_i32, c_i32, c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
     "csa_index_scores": (c_i32, [P(lcs_batch), c_vp, c_vp, c_vp, c_i32, P(lcs_index_keys), P(lcs_paging), c_i32,
@@ -174,22 +178,23 @@ class State:
     pending: object
     pending_slots: int
     new_rows: Optional[RowSet] = None
+    pending_scores: object = None   # per-channel compressors: bf16 [num_seqs, pending_slots, D]
 
     def c(self) -> lcs_state:
         nr = self.new_rows.c() if self.new_rows is not None else lcs_rows(self.window.format, self.window.dim, 0,
                                                                             None, None, None)
-        return lcs_state(self.window.c(), _ptr(self.pending), self.pending_slots, nr)
+        return lcs_state(self.window.c(), _ptr(self.pending), self.pending_slots, nr, _ptr(self.pending_scores))
 
 
 @dataclasses.dataclass
 class Compressor:
-    w: object                 # device f32 [D]
-    bias: object              # device f32 [2m] or [m]
+    w: object                 # device f32 [D] (scalar weights)
+    bias: object              # device f32 [2m] or [m]; per-channel: [2m, D] or [m, D]
     m: int
     overlap: bool
 
-    def c(self) -> lcs_compressor:
-        return lcs_compressor(_ptr(self.w), _ptr(self.bias), self.m, 1 if self.overlap else 0)
+    def c(self, scores=None) -> lcs_compressor:
+        return lcs_compressor(_ptr(self.w), _ptr(self.bias), self.m, 1 if self.overlap else 0, _ptr(scores))
 
 
 @dataclasses.dataclass
@@ -220,8 +225,10 @@ def lcs_device_check() -> int:
 
 
 def csa_compress(batch: Batch, raw, comp: Compressor, state: State, entries: RowSet, paging: Paging,
-                 dev_status=None, stream=None) -> None:
-    b, c, s, e, p = batch.c(), comp.c(), state.c(), entries.c(), paging.c()
+                 dev_status=None, stream=None, scores=None) -> None:
+    """scores: per-channel score rows of the new tokens (bf16 [total_new, D]) for a per-channel
+    compressor, else None."""
+    b, c, s, e, p = batch.c(), comp.c(scores), state.c(), entries.c(), paging.c()
     _check(_lib.csa_compress(ctypes.byref(b), _ptr(raw), ctypes.byref(c), ctypes.byref(s), ctypes.byref(e),
                              ctypes.byref(p), _ptr(dev_status), _stream(stream)), "csa_compress")
 
@@ -267,9 +274,22 @@ def lcs_window_commit(batch: Batch, state: State, dev_status=None, stream=None) 
            "lcs_window_commit")
 
 
-def lcs_index_topk_workspace(batch: Batch, m: int, k: int) -> int:
+def lcs_index_topk_workspace(batch: Batch, heads: int, keys: IndexKeys, paging: Paging, m: int, k: int) -> int:
+    b, kk, p = batch.c(), keys.c(), paging.c()
+    return _lib.lcs_index_topk_workspace(ctypes.byref(b), heads, ctypes.byref(kk), ctypes.byref(p), m, k)
+
+
+def lcs_index_topk_workspace_zeroed(batch: Batch) -> int:
     b = batch.c()
-    return _lib.lcs_index_topk_workspace(ctypes.byref(b), m, k)
+    return _lib.lcs_index_topk_workspace_zeroed(ctypes.byref(b))
+
+
+def lcs_set_wait_polls(polls: int) -> int:
+    return int(_lib.lcs_set_wait_polls(polls))
+
+
+def lcs_mma_probe(kind: int, mmas_per_cta: int, ctas: int, dev_status=None, stream=None) -> None:
+    _check(_lib.lcs_mma_probe(kind, mmas_per_cta, ctas, _ptr(dev_status), _stream(stream)), "lcs_mma_probe")
 
 
 def csa_index_topk(batch: Batch, q_fp4, q_scale, head_w, heads: int, keys: IndexKeys, paging: Paging, m: int,

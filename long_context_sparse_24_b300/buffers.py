@@ -62,8 +62,10 @@ class LayerCache:
 
 
 def alloc_layer(num_seqs: int, capacity: int, dim: int, fmt: int, m: int, overlap: bool, new_rows_cap: int,
-                device, index_rank: int = 0, block_order: Optional[Sequence[int]] = None) -> LayerCache:
-    """``block_order`` optionally permutes the physical blocks (to exercise the block table)."""
+                device, index_rank: int = 0, block_order: Optional[Sequence[int]] = None,
+                per_channel: bool = False) -> LayerCache:
+    """``block_order`` optionally permutes the physical blocks (to exercise the block table);
+    ``per_channel`` adds the pending score rows of a per-channel compressor."""
     bps = math.ceil(capacity / BLOCK_TOKENS)
     epb = BLOCK_TOKENS // m
     nblocks = num_seqs * bps
@@ -76,7 +78,9 @@ def alloc_layer(num_seqs: int, capacity: int, dim: int, fmt: int, m: int, overla
     pending = torch.zeros((num_seqs, slots, dim), dtype=torch.bfloat16, device=device)
     window = alloc_rows(fmt, dim, num_seqs * WINDOW, device)
     new_rows = alloc_rows(fmt, dim, new_rows_cap, device) if new_rows_cap > 0 else None
-    state = State(window, pending, slots, new_rows)
+    pending_scores = (torch.zeros((num_seqs, slots, dim), dtype=torch.bfloat16, device=device)
+                      if per_channel else None)
+    state = State(window, pending, slots, new_rows, pending_scores)
     keys = None
     if index_rank:
         keys = IndexKeys(torch.zeros((nblocks * epb, index_rank // 2), dtype=torch.uint8, device=device),

@@ -9,7 +9,7 @@ from concurrent.futures import ThreadPoolExecutor
 HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
-SOURCES = ["api.cu", "compress.cu", "indexer.cu", "index_tc.cu", "index_tc_pf.cu", "attend.cu", "attend_tc.cu", "attend_tc1.cu", "noalloc.cu", "stage.cu", "quantize.cu"]
+SOURCES = ["api.cu", "compress.cu", "indexer.cu", "index_tc.cu", "index_tc_pf.cu", "attend.cu", "attend_tc.cu", "attend_tc1.cu", "noalloc.cu", "stage.cu", "quantize.cu", "probe.cu"]
 LIB = os.path.join(HERE, "liblcsa.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

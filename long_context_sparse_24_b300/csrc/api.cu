@@ -1,5 +1,6 @@
 // C ABI entry points: argument validation, workspace layout and kernel launches.
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 
 #include "kernels.cuh"
@@ -62,6 +63,7 @@ struct SplitPlan {
   int tc;
   int entry_splits;   // tensor-core plan: 128-row tiles of entries; one more split for the window
   int window_apart;   // tensor-core plan: the window rows form their own split (CSA, few queries)
+  int hg;             // tensor-core plan: query heads per CTA
 };
 
 // The tensor-core attention takes FP8-split rows of D = 512 (the only D = 512 format), heads in
@@ -74,13 +76,26 @@ bool attend_tc_applies(int heads, int dim) { return dim == 512 && heads <= 128; 
 
 SplitPlan plan_splits(const lcs_batch* b, int heads, int dim, int max_rows, bool window_split) {
   if (attend_tc_applies(heads, dim)) {
+    const int sms = num_sms();
     const long long ctas = std::max<long long>(1, (long long)b->total_new * ((heads + 63) / 64));
-    const int per_query = (int)std::max<long long>(1, num_sms() / ctas);   // CTAs per (query, head group)
+    // CSA with few queries (64-head groups would leave most SMs idle): 16 heads per CTA, every CTA
+    // one query's whole row list (entries then window) for its heads -- the four head groups of a
+    // query read the same rows, from L2 after the first -- cut into runs of tiles only when the
+    // groups alone still leave SMs idle
+    if (window_split && heads % 16 == 0 && max_rows <= kAttendTcMaxRows && ctas * 2 <= sms) {
+      const long long ctas16 = (long long)b->total_new * (heads / 16);
+      const int tiles = std::max(1, (max_rows + 127) / 128);
+      const int want = (int)std::max<long long>(1, std::min<long long>(tiles, sms / std::max<long long>(1, ctas16)));
+      const int tps = (tiles + want - 1) / want;
+      const int splits = (tiles + tps - 1) / tps;
+      return SplitPlan{splits, 128 * tps, 1, splits, 0, 16};
+    }
+    const int per_query = (int)std::max<long long>(1, sms / ctas);   // CTAs per (query, head group)
     if (window_split && per_query > 1 && max_rows <= kAttendTcMaxRows) {
       const int tiles = std::max(1, (max_rows - LCSA_WINDOW + 127) / 128);
       const int es = std::min(tiles, per_query);
       const int tps = (tiles + es - 1) / es;
-      return SplitPlan{(tiles + tps - 1) / tps + 1, 128 * tps, 1, (tiles + tps - 1) / tps, 1};
+      return SplitPlan{(tiles + tps - 1) / tps + 1, 128 * tps, 1, (tiles + tps - 1) / tps, 1, 64};
     }
     // one list per query: cut it into runs of tps tiles so that all (query, head group) runs
     // together come to about one tile load per SM (the last run of a query may be shorter;
@@ -89,11 +104,11 @@ SplitPlan plan_splits(const lcs_batch* b, int heads, int dim, int max_rows, bool
     const long long units = ctas * tiles;
     const int tps = (int)std::min<long long>(tiles, std::max<long long>(1, (units + num_sms() - 1) / num_sms()));
     const int splits = (tiles + tps - 1) / tps;
-    return SplitPlan{splits, 128 * tps, 1, splits, 0};
+    return SplitPlan{splits, 128 * tps, 1, splits, 0, 64};
   }
   const int hg = heads <= 16 ? 1 : (heads + 63) / 64;
   const long long base = (long long)b->total_new * hg;
-  SplitPlan s{1, max_rows > 0 ? max_rows : 1, 0, 0, 0};
+  SplitPlan s{1, max_rows > 0 ? max_rows : 1, 0, 0, 0, 0};
   const int sms = num_sms();
   if (base <= 0 || base >= sms || max_rows <= 64) return s;
   int want = (int)(sms / base);
@@ -115,26 +130,56 @@ size_t attend_ws_bytes(const lcs_batch* b, int heads, int dim, const SplitPlan& 
   return per * dim * (s.tc ? 2 : 4) + per * 2 * 4 + 256;
 }
 
-// Workspace of csa_index_topk, in order: keys u32[T][ld], histograms u32[T][2048].
+std::atomic<uint32_t> g_wait_polls{LCSA_DEFAULT_WAIT_POLLS};
+
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+// Workspace of csa_index_topk.  Both layouts start with the ticket counters (one per sequence and
+// query group, at most int32[num_seqs][max_new]; zero between calls).  Fused top-k: run counts
+// int32[T][runs], run keys u64[T][runs][k].  Otherwise: score keys u32[T][ld], histograms
+// u32[T][2048].
 struct TopkWs {
-  size_t keys, hist, total;
+  bool fused;
+  IndexTcPlan plan;
+  size_t ticket, cnt, keys, hist, total;
 };
 
-// Indexer scores: the tcgen05 scorer for a few queries per sequence, the tcgen05 prefill scorer
-// for query runs, the warp-MMA scorer for what neither takes (rank 64, other page sizes).
-cudaError_t launch_index(const IndexParams& p, int rank, int max_new, int max_entries, cudaStream_t st) {
-  if (index_tc_qh(p, rank, max_new) > 0) return launch_index_tc(p, rank, max_new, max_entries, num_sms(), st);
-  if (index_tc_pf_applies(p, rank, max_new)) return launch_index_tc_pf(p, rank, max_new, max_entries, st);
-  return launch_index_scores(p, rank, max_new, max_entries, st);
+TopkWs topk_ws_layout(const lcs_batch* b, const IndexParams& p, int rank, int m, int k) {
+  TopkWs w{};
+  const size_t T = (size_t)b->total_new;
+  w.ticket = 0;
+  const size_t body = lcs_index_topk_workspace_zeroed(b);
+  w.plan = plan_index_tc(p, rank, b->max_new, b->max_seq_len / m, b->num_seqs, num_sms(), k);
+  w.fused = w.plan.applies != 0;
+  if (w.fused) {
+    w.cnt = body;
+    w.keys = w.cnt + round256(T * w.plan.runs * 4);
+    w.hist = w.keys;
+    w.total = w.keys + T * w.plan.runs * (size_t)k * 8 + 256;
+  } else {
+    w.keys = body;
+    w.hist = w.keys + round256(T * (size_t)index_ld(b, m) * 4);
+    w.total = w.hist + T * kTopkHistBins * 4 + 256;
+  }
+  return w;
 }
 
-TopkWs topk_ws_layout(const lcs_batch* b, int m) {
-  const size_t T = (size_t)b->total_new, ld = (size_t)index_ld(b, m);
-  TopkWs w;
-  w.keys = 0;
-  w.hist = w.keys + T * ld * 4;
-  w.total = w.hist + T * kTopkHistBins * 4 + 256;
-  return w;
+// Indexer scores on their own (csa_index_scores): the tcgen05 scorer for a few queries per
+// sequence, the tcgen05 prefill scorer for query runs, the warp-MMA scorer for what neither
+// takes (rank 64, other page sizes).
+cudaError_t launch_scores(const IndexParams& p, const lcs_batch* b, int rank, int m, cudaStream_t st) {
+  const int max_entries = b->max_seq_len / m;
+  const IndexTcPlan plan = plan_index_tc(p, rank, b->max_new, max_entries, b->num_seqs, num_sms(), 0);
+  if (plan.applies) return launch_index_tc(p, plan, st);
+  if (index_tc_pf_applies(p, rank, b->max_new)) return launch_index_tc_pf(p, rank, b->max_new, max_entries, st);
+  return launch_index_scores(p, rank, b->max_new, max_entries, st);
+}
+
+// Score keys and histograms of every (query, visible entry) for the selection pass: the tcgen05
+// prefill scorer for query runs, the warp-MMA scorer otherwise.
+cudaError_t launch_score_keys(const IndexParams& p, int rank, int max_new, int max_entries, cudaStream_t st) {
+  if (index_tc_pf_applies(p, rank, max_new)) return launch_index_tc_pf(p, rank, max_new, max_entries, st);
+  return launch_index_scores(p, rank, max_new, max_entries, st);
 }
 
 lcs_status compress_common(const lcs_batch* batch, const void* raw, const lcs_compressor* comp,
@@ -142,7 +187,9 @@ lcs_status compress_common(const lcs_batch* batch, const void* raw, const lcs_co
                            int32_t* dev_status, void* stream, bool hca) {
   lcs_status s = check_batch(batch);
   if (s != LCS_OK) return s;
-  if (comp == nullptr || state == nullptr || comp->w == nullptr || comp->bias == nullptr) return LCS_ERR_INVALID_ARG;
+  if (comp == nullptr || state == nullptr || comp->bias == nullptr) return LCS_ERR_INVALID_ARG;
+  const bool per_channel = comp->scores != nullptr;
+  if (!per_channel && comp->w == nullptr) return LCS_ERR_INVALID_ARG;
   if (raw == nullptr && batch->total_new > 0) return LCS_ERR_INVALID_ARG;
   if (!aligned16(raw) || !aligned16(state->pending)) return LCS_ERR_ALIGNMENT;
   const int m = comp->m;
@@ -150,6 +197,11 @@ lcs_status compress_common(const lcs_batch* batch, const void* raw, const lcs_co
   if (hca && comp->overlap) return LCS_ERR_UNSUPPORTED;
   const int slots = comp->overlap ? 2 * m : m;
   if (state->pending == nullptr || state->pending_slots != slots) return LCS_ERR_SHAPE;
+  if (per_channel) {   // the streaming compressor (ratios up to 4) takes per-channel weights
+    if (m > 4) return LCS_ERR_UNSUPPORTED;
+    if (state->pending_scores == nullptr) return LCS_ERR_INVALID_ARG;
+    if (!aligned16(comp->scores) || !aligned16(state->pending_scores)) return LCS_ERR_ALIGNMENT;
+  }
   if ((s = check_rows(entries)) != LCS_OK) return s;
   if ((s = check_paging(paging)) != LCS_OK) return s;
   const bool have_new = state->new_rows.nope != nullptr;
@@ -175,6 +227,8 @@ lcs_status compress_common(const lcs_batch* batch, const void* raw, const lcs_co
   p.pending = static_cast<const __nv_bfloat16*>(state->pending);
   p.pending_out = static_cast<__nv_bfloat16*>(state->pending);
   p.pending_slots = slots;
+  p.scores = static_cast<const __nv_bfloat16*>(comp->scores);
+  p.pending_scores = per_channel ? static_cast<__nv_bfloat16*>(state->pending_scores) : nullptr;
   p.entries = make_rows(*entries);
   p.paging = make_paging(*paging);
   p.new_rows = make_rows(state->new_rows);
@@ -211,6 +265,7 @@ lcs_status index_common(const lcs_batch* batch, const uint8_t* q_fp4, const uint
   p.k_rows = keys->num_rows;
   p.paging = make_paging(*paging);
   p.m = m;
+  p.wait_polls = g_wait_polls.load(std::memory_order_relaxed);
   return LCS_OK;
 }
 
@@ -264,6 +319,8 @@ lcs_status attend_common(const lcs_batch* batch, const void* q, int32_t heads, c
   p.tc = plan.tc;
   p.entry_splits = plan.entry_splits;
   p.window_split = plan.window_apart;
+  p.hg = plan.hg;
+  p.wait_polls = g_wait_polls.load(std::memory_order_relaxed);
   if (plan.splits > 1) {
     const size_t per = (size_t)batch->total_new * heads * plan.splits;
     const size_t ob = per * entries->dim * (plan.tc ? 2 : 4);
@@ -306,11 +363,24 @@ lcs_status csa_attend_part(const lcs_batch* batch, const void* q, int32_t heads,
 
 extern "C" {
 
-size_t lcs_index_topk_workspace(const lcs_batch* batch, int32_t m, int32_t k) {
-  (void)k;
-  if (batch == nullptr || m <= 0) return 0;
-  return topk_ws_layout(batch, m).total;
+size_t lcs_index_topk_workspace(const lcs_batch* batch, int32_t heads, const lcs_index_keys* keys,
+                                const lcs_paging* paging, int32_t m, int32_t k) {
+  if (batch == nullptr || keys == nullptr || paging == nullptr || m <= 0 || k < 1) return 0;
+  IndexParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.heads = heads;
+  p.k_fp4 = keys->fp4;
+  p.k_scale = keys->scale;
+  p.k_rows = keys->num_rows;
+  p.paging = make_paging(*paging);
+  return topk_ws_layout(batch, p, keys->rank, m, k).total;
 }
+
+size_t lcs_index_topk_workspace_zeroed(const lcs_batch* batch) {
+  return batch == nullptr ? 0 : round256((size_t)batch->num_seqs * std::max(1, batch->max_new) * 4);
+}
+
+uint32_t lcs_set_wait_polls(uint32_t polls) { return g_wait_polls.exchange(polls); }
 
 int32_t lcs_abi_version(void) { return LCSA_ABI_VERSION; }
 
@@ -374,25 +444,39 @@ lcs_status csa_index_topk(const lcs_batch* batch, const uint8_t* q_fp4, const ui
   const bool score_only = (flags & LCS_INDEX_SCORE_ONLY) != 0, select_only = (flags & LCS_INDEX_SELECT_ONLY) != 0;
   if (score_only && select_only) return LCS_ERR_INVALID_ARG;
   if (!score_only && (out_idx == nullptr || out_cnt == nullptr)) return LCS_ERR_INVALID_ARG;
-  const size_t need = lcs_index_topk_workspace(batch, m, k);
-  if (workspace == nullptr || workspace_bytes < need) return LCS_ERR_WORKSPACE;
+  const TopkWs w = topk_ws_layout(batch, p, keys->rank, m, k);
+  if (workspace == nullptr || workspace_bytes < w.total) return LCS_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return LCS_ERR_ALIGNMENT;
   p.head_w = head_w;
   p.relu = (flags & LCS_INDEX_RELU) ? 1 : 0;
   p.ld = index_ld(batch, m);
-  const TopkWs w = topk_ws_layout(batch, m);
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  p.keys_out = reinterpret_cast<uint32_t*>(ws + w.keys);
-  p.hist = reinterpret_cast<uint32_t*>(ws + w.hist);
   p.status = dev_status;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int max_entries = batch->max_seq_len / m;
   cudaError_t e = cudaSuccess;
+  if (w.fused) {
+    p.top_k = k;
+    p.cand_cap = w.plan.cap;
+    p.runs.runs = w.plan.runs;
+    p.runs.ticket = reinterpret_cast<int*>(ws + w.ticket);
+    p.runs.cnt = reinterpret_cast<int*>(ws + w.cnt);
+    p.runs.keys = reinterpret_cast<uint64_t*>(ws + w.keys);
+    p.out_idx = out_idx;
+    p.out_cnt = out_cnt;
+    if (select_only) return from_cuda(launch_topk_merge(p, w.plan, batch->max_new, st));
+    p.merge_inline = (!score_only && w.plan.merge_inline) ? 1 : 0;
+    e = launch_index_tc(p, w.plan, st);
+    if (e != cudaSuccess || score_only || p.merge_inline) return from_cuda(e);
+    return from_cuda(launch_topk_merge(p, w.plan, batch->max_new, st));
+  }
+  p.keys_out = reinterpret_cast<uint32_t*>(ws + w.keys);
+  p.hist = reinterpret_cast<uint32_t*>(ws + w.hist);
   if (!select_only) {
     // the per-query histograms accumulate with atomics: clear them first
-    e = cudaMemsetAsync(ws + w.hist, 0, w.total - 256 - w.hist, st);
+    e = cudaMemsetAsync(ws + w.hist, 0, (size_t)batch->total_new * kTopkHistBins * 4, st);
     if (e != cudaSuccess) return LCS_ERR_CUDA;
-    e = launch_index(p, keys->rank, batch->max_new, max_entries, st);
+    e = launch_score_keys(p, keys->rank, batch->max_new, max_entries, st);
     if (e != cudaSuccess || score_only) return from_cuda(e);
   }
   e = launch_topk_select(p.keys_out, p.hist, p.ld, batch->cu_new, batch->seq_len, batch->num_seqs, batch->max_new,
@@ -413,9 +497,7 @@ lcs_status csa_index_scores(const lcs_batch* batch, const uint8_t* q_fp4, const 
   p.ld = ld;
   p.scores_out = out_scores;
   p.status = dev_status;
-  const int max_entries = batch->max_seq_len / m;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  return from_cuda(launch_index(p, keys->rank, batch->max_new, max_entries, st));
+  return from_cuda(launch_scores(p, batch, keys->rank, m, static_cast<cudaStream_t>(stream)));
 }
 
 size_t lcs_attend_workspace(const lcs_batch* batch, int32_t heads, int32_t dim, int32_t max_rows) {

@@ -291,7 +291,12 @@ __global__ void __launch_bounds__(256, 1) attend_kernel(AttendParams p) {
     const int* valid = reinterpret_cast<const int*>(st + SL::kValidOff);
     if (tid < kRT) {
       const bool ok = valid[tid] != 0 && tile_begin + tid < r_end;
-      rscale[tid] = ok ? (kSplitFmt ? reinterpret_cast<const float*>(st + SL::kScaleOff)[tid] : 1.0f) : -1.0f;
+      float sc = ok ? (kSplitFmt ? reinterpret_cast<const float*>(st + SL::kScaleOff)[tid] : 1.0f) : -1.0f;
+      if (ok && kSplitFmt && !(sc < kMaxRowScale)) {   // P * s * 2^8 would leave the f16 range
+        report(p.status, LCS_ERR_DEVICE_GUARD);
+        sc = -1.0f;
+      }
+      rscale[tid] = sc;
     }
     __syncthreads();
 

@@ -41,41 +41,49 @@ namespace lcsa {
 namespace {
 
 constexpr int kTileRows = 128;
-constexpr int kHeads = 64;                // N of both products
 constexpr int kD = 512;
 constexpr int kNopeBytes = kD - kRope;    // 448 FP8 codes per row
 constexpr int kChunk = 16384;             // [128 rows][64 dims] BF16
-constexpr int kQChunk = 8192;             // [64 heads][64 dims] BF16
 constexpr int kThreads = 256;
 
+// HG query heads per CTA (the N of both products): 64, or 16 when a batch has too few queries to
+// fill the GPU with 64-head groups (CSA decode).
+template <int HG>
 struct TcAttSmem {
-  static constexpr int kQ = 0;                              // 8 x 8 KB; the epilogue transposes after the last tile
+  static constexpr int kQChunk = HG * 128;                  // [HG heads][64 dims] BF16
+  static constexpr int kQ = 0;                              // 8 chunks; the epilogue transposes after the last tile
   static constexpr int kT = kQ + 8 * kQChunk;               // 8 x 16 KB row tile (chunk 0: RoPE)
-  static constexpr int kP = kT + 8 * kChunk;                // 2 x 8 KB ([64 heads][64 rows])
+  static constexpr int kP = kT + 8 * kChunk;                // 2 chunks ([HG heads][64 rows])
   static constexpr int kScale = kP + 2 * kQChunk;           // f32 [2][128]   (tile parity)
   static constexpr int kRinv = kScale + 2 * kTileRows * 4;  // f32 [2][128]   1 / s_r
-  static constexpr int kDesc = kRinv + 2 * kTileRows * 4;   // long long [3][128] (tiles t, t+1, t+2)
-  static constexpr int kRed = kDesc + 3 * kTileRows * 8;    // f32 [4 warps][64] per-head partials
-  static constexpr int kM = kRed + 4 * kHeads * 4;          // f32 [64] running max (base 2)
-  static constexpr int kL = kM + kHeads * 4;                // f32 [64] running sum
-  static constexpr int kMn = kL + kHeads * 4;               // f32 [64] the tile's new max
-  static constexpr int kAlpha = kMn + kHeads * 4;           // f32 [64] rescale factor of O and l
-  static constexpr int kInv = kAlpha + kHeads * 4;          // f32 [64] output factor per head
-  static constexpr int kBar = kInv + kHeads * 4;            // u64 s, pv
-  static constexpr int kMisc = kBar + 16;                   // tmem base, rescale flag
+  // row descriptors: 64 heads, a ring of three tiles (t, t+1, t+2) resolved two tiles ahead; 16
+  // heads (shared memory to spare), every tile of the CTA's rows resolved up front
+  static constexpr int kDescTiles = HG == 16 ? (kAttendTcMaxRows + kTileRows - 1) / kTileRows : 3;
+  static constexpr int kDesc = kRinv + 2 * kTileRows * 4;   // long long [kDescTiles][128]
+  static constexpr int kRed = kDesc + kDescTiles * kTileRows * 8;   // f32 [4 warps][HG] per-head partials
+  static constexpr int kM = kRed + 4 * HG * 4;              // f32 [HG] running max (base 2)
+  static constexpr int kL = kM + HG * 4;                    // f32 [HG] running sum
+  static constexpr int kMn = kL + HG * 4;                   // f32 [HG] the tile's new max
+  static constexpr int kAlpha = kMn + HG * 4;               // f32 [HG] rescale factor of O and l
+  static constexpr int kInv = kAlpha + HG * 4;              // f32 [HG] output factor per head
+  static constexpr int kBar = kInv + HG * 4;                // u64 s, pv, drain
+  static constexpr int kMisc = kBar + 24;                   // tmem base, rescale flag
   static constexpr int kBytes = kMisc + 16 + 1024;
+  static constexpr uint32_t kTmemCols = HG == 64 ? 512 : 128;   // S^T (HG) + O^T (4 x HG)
+  static_assert(kBytes <= 227 * 1024, "shared memory");
+  static_assert(kQ % 1024 == 0 && kT % 1024 == 0 && kP % 1024 == 0, "operand chunks on 1024-byte swizzle atoms");
+  static_assert(8 * kQChunk >= 8 * HG * 32 * 4, "epilogue transposes fit the query buffer");
 };
-static_assert(TcAttSmem::kBytes <= 227 * 1024, "shared memory");
-static_assert(TcAttSmem::kQ % 1024 == 0 && TcAttSmem::kT % 1024 == 0 && TcAttSmem::kP % 1024 == 0,
-              "operand chunks on 1024-byte swizzle atoms");
 
-// Reduce-scatter of 64 per-lane values over the 32 lanes of a warp: afterwards v[0], v[1] hold
-// the reduction of heads hb, hb + 1 with hb = 32 b4 + 16 b3 + 8 b2 + 4 b1 + 2 b0 (b = lane bits).
-template <bool kMax>
-__device__ __forceinline__ void reduce_scatter64(float (&v)[64], int lane) {
+// Reduce-scatter of V per-lane values over the 32 lanes of a warp.  Halving rounds (lanes 16, 8,
+// ... apart) while a lane holds more than one value, then plain butterfly rounds: afterwards
+// v[0 .. max(1, V/32)) hold the reductions of heads scatter_head<V>(lane) + i.
+template <int V, bool kMax>
+__device__ __forceinline__ void reduce_scatter(float (&v)[V], int lane) {
+  constexpr int kHalving = V >= 64 ? 5 : (V == 32 ? 5 : (V == 16 ? 4 : (V == 8 ? 3 : 2)));
 #pragma unroll
-  for (int r = 0; r < 5; ++r) {
-    const int off = 16 >> r, n = 32 >> r;   // lanes apart, pairs kept
+  for (int r = 0; r < kHalving; ++r) {
+    const int off = 16 >> r, n = V >> (r + 1);   // lanes apart, values kept
     const bool hi = (lane & off) != 0;
 #pragma unroll
     for (int i = 0; i < n; ++i) {
@@ -85,10 +93,31 @@ __device__ __forceinline__ void reduce_scatter64(float (&v)[64], int lane) {
       v[i] = kMax ? fmaxf(keep, o) : keep + o;
     }
   }
+#pragma unroll
+  for (int off = 16 >> kHalving; off > 0; off >>= 1) {
+    const float o = __shfl_xor_sync(0xffffffffu, v[0], off);
+    v[0] = kMax ? fmaxf(v[0], o) : v[0] + o;
+  }
 }
 
+// First head of a lane's values after reduce_scatter<V> (lane bit 4 selects the upper half of the
+// values in the first round, bit 3 in the second, ...).
+template <int V>
 __device__ __forceinline__ int scatter_head(int lane) {
-  return ((lane >> 4) & 1) * 32 + ((lane >> 3) & 1) * 16 + ((lane >> 2) & 1) * 8 + ((lane >> 1) & 1) * 4 + (lane & 1) * 2;
+  constexpr int kHalving = V >= 64 ? 5 : (V == 32 ? 5 : (V == 16 ? 4 : (V == 8 ? 3 : 2)));
+  int h = 0;
+#pragma unroll
+  for (int r = 0; r < kHalving; ++r)
+    if (lane & (16 >> r)) h += V >> (r + 1);
+  return h;
+}
+
+// Whether a lane writes its reduced values (lanes that differ only in the butterfly bits hold
+// copies).
+template <int V>
+__device__ __forceinline__ bool scatter_writer(int lane) {
+  constexpr int kHalving = V >= 64 ? 5 : (V == 32 ? 5 : (V == 16 ? 4 : (V == 8 ? 3 : 2)));
+  return (lane & ((16 >> kHalving) * 2 - 1)) == 0 || kHalving == 5;
 }
 
 __device__ __forceinline__ uint64_t desc_mn_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
@@ -135,26 +164,26 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v, float m) {
 
 // grid: (total_new, head groups, splits); splits 0 .. entry_splits-1 take 128-row tiles of the
 // entries, split entry_splits the window rows (part 1: that split alone, part 2: the entry splits).
+template <int HG>
 __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) {
-  using L = TcAttSmem;
+  using L = TcAttSmem<HG>;
+  constexpr int kQChunk = L::kQChunk;
+  constexpr int kVals = HG >= 32 ? HG / 32 : 1;   // per-lane values after a reduce-scatter
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int q = blockIdx.x, hg = blockIdx.y;
   const int H = p.heads;
-  const int h0 = hg * kHeads;
-  // sequence of query q (cu_new non-decreasing)
-  int b = 0;
-  {
-    int lo = 0, hi = p.num_seqs - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (p.cu_new[mid] <= q) lo = mid; else hi = mid - 1;
-    }
-    b = lo;
-  }
+  const int h0 = hg * HG;
+  // sequence of query q (the row tile's space is free until the rows arrive)
+  const int b = find_seq_block(p.cu_new, p.num_seqs, q, reinterpret_cast<int*>(smem + L::kT), 8 * kChunk / 4 - 1);
   const SeqSpan sp = seq_span(p.cu_new, p.seq_len, b);
+  // the top-k list and the sequence's block-table row head for L2 while the count is read
+  if (p.topk_idx != nullptr && p.part != 1)
+    for (int i = tid * 32; i < p.k; i += kThreads * 32) prefetch_l2(p.topk_idx + (long long)q * p.k + i);
+  for (int i = tid * 32; i < p.paging.max_blocks; i += kThreads * 32)
+    prefetch_l2(p.paging.table + (long long)b * p.paging.max_blocks + i);
   const int n0 = sp.n0();
   const int t = n0 + (q - sp.q0);
   const int32_t* sel = p.topk_idx != nullptr ? p.topk_idx + (long long)q * p.k : nullptr;
@@ -185,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
   }
   if (r_begin >= r_end) {
     if (p.splits > 1)
-      for (int h = tid; h < kHeads; h += kThreads)
+      for (int h = tid; h < HG; h += kThreads)
         if (h0 + h < H) {
           float* ml = p.ws_ml + (((long long)q * H + h0 + h) * p.splits + split) * 2;
           ml[0] = -INFINITY;
@@ -194,6 +223,10 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
     return;
   }
   const int ntiles = (r_end - r_begin + kTileRows - 1) / kTileRows;
+  if (ntiles > L::kDescTiles && HG == 16) {   // more rows than the plan allows for (cannot happen)
+    if (tid == 0) report(p.status, LCS_ERR_DEVICE_GUARD);
+    return;
+  }
 
   long long* desc = reinterpret_cast<long long*>(smem + L::kDesc);
   float* sscale = reinterpret_cast<float*>(smem + L::kScale);
@@ -209,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
   volatile int* rescale_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
 
   // ---- the query first (independent of the rows): cp.async into eight K-major chunks
-  for (int idx = tid; idx < kHeads * 64; idx += kThreads) {
+  for (int idx = tid; idx < HG * 64; idx += kThreads) {
     const int h = idx >> 6, c = (idx >> 3) & 7, j = idx & 7;   // head, 64-dim chunk, 16-byte piece
     const bool okq = h0 + h < H;
     const __nv_bfloat16* g = p.q + ((long long)q * H + (okq ? h0 + h : 0)) * kD + c * 64 + j * 8;
@@ -251,9 +284,10 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
   uint4 cv[kNP];
   uint4 rv[kRP];
   float sc = 0.0f;                                   // threads 0-127: the scale of row tid
-  // issue the loads of tile tt (descriptors in desc[tt % 3]) into registers
+  auto dslot = [&](int tt) { return HG == 16 ? tt : tt % 3; };
+  // issue the loads of tile tt (descriptors in desc[dslot(tt)]) into registers
   auto load_tile = [&](int tt) {
-    const long long* dd = desc + (tt % 3) * kTileRows;
+    const long long* dd = desc + dslot(tt) * kTileRows;
     sc = 0.0f;
     if (tid < kTileRows && dd[tid] >= 0) {
       const long long d = dd[tid];
@@ -287,42 +321,54 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
     }
   };
 
-  if (tid < kTileRows) desc[tid] = make_desc(0, tid);
-  else if (ntiles > 1) desc[tid] = make_desc(1, tid - kTileRows);   // tile 1 in desc[1]
-  if (tid < kHeads) {
+  if (HG == 16) {
+    for (int i = tid; i < ntiles * kTileRows; i += kThreads) desc[i] = make_desc(i >> 7, i & 127);
+  } else if (tid < kTileRows) {
+    desc[tid] = make_desc(0, tid);
+  } else if (ntiles > 1) {
+    desc[tid] = make_desc(1, tid - kTileRows);   // tile 1 in desc[1]
+  }
+  if (tid < HG) {
     mrow[tid] = -INFINITY;
     lrow[tid] = 0.0f;
   }
   if (tid == 0) {
     mbar_init(bar_s, 1);
     mbar_init(bar_pv, 1);
+    mbar_init(bar_pv + 8, 1);   // drain
     fence_mbar_init();
   }
-  if (warp == 0) tmem_alloc(sbase + L::kMisc, 512);
+  if (warp == 0) tmem_alloc(sbase + L::kMisc, L::kTmemCols);
   __syncthreads();
   load_tile(0);
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tm_s = tmem;             // S'^T: columns 0..63
-  const uint32_t tm_o = tmem + 64;        // O^T block mb: columns 64 + 64*mb
+  const uint32_t tm_s = tmem;             // S'^T: columns 0 .. HG-1
+  const uint32_t tm_o = tmem + HG;        // O^T block mb: columns HG + HG*mb
 
-  constexpr uint32_t kIdS = idesc_f16(0, 128, kHeads);                 // F16, K-major A and B
-  constexpr uint32_t kIdO = idesc_f16(0, 128, kHeads) | (1u << 15);    // A (rows^T) MN-major
+  constexpr uint32_t kIdS = idesc_f16(0, 128, HG);                 // F16, K-major A and B
+  constexpr uint32_t kIdO = idesc_f16(0, 128, HG) | (1u << 15);    // A (rows^T) MN-major
   bool ok = true;
 
   for (int tt = 0; tt < ntiles; ++tt) {
     const int bp = tt & 1;
     const int trows = min(kTileRows, r_end - r_begin - tt * kTileRows);
     // ---- 1. the previous tile's PV MMAs have read the tile buffer and P
-    if (tt > 0) ok = mbar_wait(bar_pv, (tt - 1) & 1, p.status) && ok;
+    if (tt > 0) ok = mbar_wait(bar_pv, (tt - 1) & 1, p.status, nullptr, p.wait_polls) && ok;
     ok = __syncthreads_and(ok);
     if (!ok) break;
     // ---- 2. this tile's scales, then its rows widened into the tile buffer
     if (tid < kTileRows) {
-      sscale[bp * kTileRows + tid] = sc;
-      rinv[bp * kTileRows + tid] = sc > 0.0f ? __frcp_rn(sc) : 0.0f;
+      float s_r = sc;
+      if (desc[dslot(tt) * kTileRows + tid] >= 0 && !(s_r < kMaxRowScale)) {   // p * s_r * 2^8 leaves f16
+        report(p.status, LCS_ERR_DEVICE_GUARD);
+        desc[dslot(tt) * kTileRows + tid] = -1;
+        s_r = 0.0f;
+      }
+      sscale[bp * kTileRows + tid] = s_r;
+      rinv[bp * kTileRows + tid] = s_r > 0.0f ? __frcp_rn(s_r) : 0.0f;
     }
     __syncthreads();
 #pragma unroll
@@ -337,15 +383,20 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
 #pragma unroll
     for (int it = 0; it < kRP; ++it) {
       const int idx = it * kThreads + tid, r = idx >> 3, j = idx & 7;
-      *reinterpret_cast<uint4*>(smem + L::kT + r * 128 + ((j ^ (r & 7)) << 4)) =
-          bf16x8_to_f16x8(rv[it], rinv[bp * kTileRows + r]);
+      uint4 h = bf16x8_to_f16x8(rv[it], rinv[bp * kTileRows + r]);
+      if (f16x8_nonfinite(h)) {   // |rope| / s_r beyond the f16 range: the row is left out
+        report(p.status, LCS_ERR_DEVICE_GUARD);
+        desc[dslot(tt) * kTileRows + r] = -1;
+        h = make_uint4(0u, 0u, 0u, 0u);
+      }
+      *reinterpret_cast<uint4*>(smem + L::kT + r * 128 + ((j ^ (r & 7)) << 4)) = h;
     }
     // the next tile's rows go out now and fly while this tile computes
     if (tt + 1 < ntiles) load_tile(tt + 1);
     if (tt == 0) {
       cp_async_wait<0>();
       __syncthreads();
-      for (int idx = tid; idx < kHeads * 64; idx += kThreads) {   // query -> F16 in place
+      for (int idx = tid; idx < HG * 64; idx += kThreads) {   // query -> F16 in place
         uint4* pc = reinterpret_cast<uint4*>(smem + L::kQ + idx * 16);
         *pc = bf16x8_to_f16x8(*pc, 1.0f);
       }
@@ -365,28 +416,30 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
     }
     // ---- 4. warps 4-7: descriptors of tile tt + 2; warps 0-3: logits and the tile max per head
     const int r = warp * 32 + lane;           // warps 0-3: tile row
-    const int hb = scatter_head(lane);
-    const bool rvalid = warp < 4 && r < trows && desc[(tt % 3) * kTileRows + (r & 127)] >= 0;
+    const int hb = scatter_head<HG>(lane);
+    const bool hw_lane = scatter_writer<HG>(lane);
+    const bool rvalid = warp < 4 && r < trows && desc[dslot(tt) * kTileRows + (r & 127)] >= 0;
     if (warp >= 4) {
-      if (tt + 2 < ntiles) desc[((tt + 2) % 3) * kTileRows + tid - 128] = make_desc(tt + 2, tid - 128);
+      if (HG != 16 && tt + 2 < ntiles) desc[((tt + 2) % 3) * kTileRows + tid - 128] = make_desc(tt + 2, tid - 128);
     } else {
-      ok = mbar_wait(bar_s, tt & 1, p.status) && ok;
+      ok = mbar_wait(bar_s, tt & 1, p.status, nullptr, p.wait_polls) && ok;
       ok = __all_sync(0xffffffffu, ok);
       tc_fence_after_sync();
       if (ok) {
         const float lsc = sscale[bp * kTileRows + r] * p.scale_log2;   // logit = s_r * S', base 2
-        float w[64];
+        float w[HG];
 #pragma unroll
-        for (int c16 = 0; c16 < kHeads / 16; ++c16) {
+        for (int c16 = 0; c16 < HG / 16; ++c16) {
           uint32_t u[16];
           tmem_ld16(tm_s + ((uint32_t)(warp * 32) << 16) + c16 * 16, u);
           tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 16; ++j) w[c16 * 16 + j] = rvalid ? __uint_as_float(u[j]) * lsc : -INFINITY;
         }
-        reduce_scatter64<true>(w, lane);
-        red[warp * kHeads + hb] = w[0];
-        red[warp * kHeads + hb + 1] = w[1];
+        reduce_scatter<HG, true>(w, lane);
+        if (hw_lane)
+#pragma unroll
+          for (int i = 0; i < kVals; ++i) red[warp * HG + hb + i] = w[i];
       }
     }
     ok = __syncthreads_and(ok);
@@ -394,8 +447,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
     // ---- 5. new running max and rescale factors per head
     if (tid == 0) *rescale_flag = 0;
     __syncthreads();
-    if (tid < kHeads) {
-      const float mt = fmaxf(fmaxf(red[tid], red[kHeads + tid]), fmaxf(red[2 * kHeads + tid], red[3 * kHeads + tid]));
+    if (tid < HG) {
+      const float mt = fmaxf(fmaxf(red[tid], red[HG + tid]), fmaxf(red[2 * HG + tid], red[3 * HG + tid]));
       const float mo = mrow[tid];
       const float mn = fmaxf(mo, mt);
       const float al = (mo == -INFINITY || mn == -INFINITY) ? 0.0f : exp2f(mo - mn);
@@ -406,12 +459,12 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
     __syncthreads();
     // ---- 6. warps 0-3: P' and the tile sum per head; warps 4-7: rescale O^T where the max grew
     if (warp < 4) {
-      float w[64];
+      float w[HG];
       const float srow = sscale[bp * kTileRows + r] * kP2Scale;
       const float lsc = sscale[bp * kTileRows + r] * p.scale_log2;
       tc_fence_after_sync();
 #pragma unroll
-      for (int c16 = 0; c16 < kHeads / 16; ++c16) {   // the logits again, from tensor memory
+      for (int c16 = 0; c16 < HG / 16; ++c16) {   // the logits again, from tensor memory
         uint32_t u[16];
         tmem_ld16(tm_s + ((uint32_t)(warp * 32) << 16) + c16 * 16, u);
         tmem_ld_wait();
@@ -419,7 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
         for (int j = 0; j < 16; ++j) w[c16 * 16 + j] = rvalid ? __uint_as_float(u[j]) * lsc : -INFINITY;
       }
 #pragma unroll
-      for (int h = 0; h < 64; h += 2) {
+      for (int h = 0; h < HG; h += 2) {
         const float m0 = mnew[h], m1 = mnew[h + 1];
         const float a0 = m0 == -INFINITY ? 0.0f : exp2f(w[h] - m0);
         const float a1 = m1 == -INFINITY ? 0.0f : exp2f(w[h + 1] - m1);
@@ -432,16 +485,17 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
         *reinterpret_cast<__half*>(smem + L::kP + pc * kQChunk + (h + 1) * 128 + ((pj ^ ((h + 1) & 7)) << 4) + pe * 2) =
             __float2half_rn(a1 * srow);
       }
-      reduce_scatter64<false>(w, lane);
-      red[warp * kHeads + hb] = w[0];
-      red[warp * kHeads + hb + 1] = w[1];
+      reduce_scatter<HG, false>(w, lane);
+      if (hw_lane)
+#pragma unroll
+        for (int i = 0; i < kVals; ++i) red[warp * HG + hb + i] = w[i];
     } else if (*rescale_flag) {
       const int quad = warp & 3;
 #pragma unroll 1
       for (int mb = 0; mb < 4; ++mb)
 #pragma unroll 1
-        for (int c16 = 0; c16 < kHeads / 16; ++c16) {
-          const uint32_t ta = tm_o + 64 * mb + ((uint32_t)(quad * 32) << 16) + c16 * 16;
+        for (int c16 = 0; c16 < HG / 16; ++c16) {
+          const uint32_t ta = tm_o + HG * mb + ((uint32_t)(quad * 32) << 16) + c16 * 16;
           uint32_t u[16];
           tmem_ld16(ta, u);
           tmem_ld_wait();
@@ -456,49 +510,49 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
     __syncthreads();
     tc_fence_after_sync();
     // ---- 7. running statistics; O^T += R'^T . P'^T
-    if (tid < kHeads) {
-      lrow[tid] = lrow[tid] * alpha_s[tid] + (red[tid] + red[kHeads + tid]) + (red[2 * kHeads + tid] + red[3 * kHeads + tid]);
+    if (tid < HG) {
+      lrow[tid] = lrow[tid] * alpha_s[tid] + (red[tid] + red[HG + tid]) + (red[2 * HG + tid] + red[3 * HG + tid]);
       mrow[tid] = mnew[tid];
     }
     if (tid == 0) {
       for (int mb = 0; mb < 4; ++mb)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)   // 16 rows per step: two 8-row groups
-          tc_mma_f16(tm_o + 64 * mb, desc_mn_sw128(sbase + L::kT + 2 * mb * kChunk + kk * 2048, kChunk, 1024),
+          tc_mma_f16(tm_o + HG * mb, desc_mn_sw128(sbase + L::kT + 2 * mb * kChunk + kk * 2048, kChunk, 1024),
                      smem_desc_sw128(sbase + L::kP + (kk >> 2) * kQChunk) + 2 * (kk & 3), kIdO,
                      (tt > 0 || kk > 0) ? 1u : 0u);
       tc_commit(bar_pv);
     }
   }
-  if (ok) ok = mbar_wait(bar_pv, (ntiles - 1) & 1, p.status);
+  if (ok) ok = mbar_wait(bar_pv, (ntiles - 1) & 1, p.status, nullptr, p.wait_polls);
   ok = __syncthreads_and(ok);
   tc_fence_after_sync();
 
   // ---- epilogue: warp w reads lanes 32*(w%4) (dims) of blocks 2*(w/4), 2*(w/4)+1, transposes
   //      them through its own 8 KB of the query buffer and writes 16-byte pieces
   float* inv_s = reinterpret_cast<float*>(smem + L::kInv);
-  for (int h = tid; h < kHeads; h += kThreads) {
+  for (int h = tid; h < HG; h += kThreads) {
     const float l = lrow[h];
     inv_s[h] = p.splits == 1 ? (l > 0.0f ? 1.0f / (l * kP2Scale) : 0.0f) : 1.0f / kP2Scale;
   }
   __syncthreads();
   if (ok) {
     const int quad = warp & 3;
-    float* tb = reinterpret_cast<float*>(smem + L::kQ) + warp * (kHeads * 32);   // [64 heads][32 dims]
+    float* tb = reinterpret_cast<float*>(smem + L::kQ) + warp * (HG * 32);   // [HG heads][32 dims]
     for (int bi = 0; bi < 2; ++bi) {
       const int mb = 2 * (warp >> 2) + bi;
       const int dim0 = mb * 128 + quad * 32;
 #pragma unroll
-      for (int c16 = 0; c16 < kHeads / 16; ++c16) {
+      for (int c16 = 0; c16 < HG / 16; ++c16) {
         uint32_t v[16];
-        tmem_ld16(tm_o + 64 * mb + ((uint32_t)(quad * 32) << 16) + c16 * 16, v);
+        tmem_ld16(tm_o + HG * mb + ((uint32_t)(quad * 32) << 16) + c16 * 16, v);
         tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < 16; ++j) tb[(c16 * 16 + j) * 32 + lane] = __uint_as_float(v[j]) * inv_s[c16 * 16 + j];
       }
       __syncwarp();
 #pragma unroll 4
-      for (int i = 0; i < kHeads / 4; ++i) {
+      for (int i = 0; i < HG / 4; ++i) {
         const int h = i * 4 + (lane >> 3), d4 = (lane & 7) * 4;
         if (h0 + h < H) {
           const float4 o = *reinterpret_cast<const float4*>(tb + h * 32 + d4);
@@ -515,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
       }
       __syncwarp();
     }
-    for (int h = tid; h < kHeads; h += kThreads) {
+    for (int h = tid; h < HG; h += kThreads) {
       if (h0 + h >= H) continue;
       const float l = lrow[h], mm = mrow[h];
       if (p.splits == 1) {
@@ -528,27 +582,43 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
       }
     }
   }
+  // after a wait gave up, the MMAs still in flight complete before tensor memory is released
+  if (tid == 0 && !ok) {
+    tc_commit(bar_pv + 8);
+    mbar_wait(bar_pv + 8, 0, nullptr, nullptr, kWaitPolls);
+  }
   tc_fence_before_sync();
   __syncthreads();
   if (warp == 0) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, L::kTmemCols);
   }
 }
 
-cudaError_t launch_attend_tc(const AttendParams& p, int total_new, cudaStream_t st) {
-  if (p.rows_per_split == kTileRows) return launch_attend_tc1(p, total_new, st);   // one tile per CTA
+namespace {
+
+template <int HG>
+cudaError_t launch_attend_tc_t(const AttendParams& p, int total_new, cudaStream_t st) {
   static PerDeviceOnce attr;
   cudaError_t ea = once_per_device(attr, [] {
-    return cudaFuncSetAttribute(attend_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TcAttSmem::kBytes);
+    return cudaFuncSetAttribute(attend_tc_kernel<HG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                TcAttSmem<HG>::kBytes);
   });
   if (ea != cudaSuccess) return ea;
   const int z = p.part == 1 ? 1 : (p.part == 2 ? p.entry_splits : p.splits);
-  dim3 grid(total_new, (p.heads + kHeads - 1) / kHeads, z);
-  attend_tc_kernel<<<grid, kThreads, TcAttSmem::kBytes, st>>>(p);
+  dim3 grid(total_new, (p.heads + HG - 1) / HG, z);
+  attend_tc_kernel<HG><<<grid, kThreads, TcAttSmem<HG>::kBytes, st>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || p.splits == 1 || p.part == 1) return e;
   return launch_attend_combine(p, total_new, kD, st);
+}
+
+}  // namespace
+
+cudaError_t launch_attend_tc(const AttendParams& p, int total_new, cudaStream_t st) {
+  if (p.hg == 16) return launch_attend_tc_t<16>(p, total_new, st);
+  if (p.rows_per_split == kTileRows) return launch_attend_tc1(p, total_new, st);   // one tile per CTA
+  return launch_attend_tc_t<64>(p, total_new, st);
 }
 
 }  // namespace lcsa

@@ -56,8 +56,8 @@ struct TcAttSmem {
   static constexpr int kM = kDesc + kTileRows * 8;          // f32 [64]
   static constexpr int kL = kM + kHeads * 4;                // f32 [64]
   static constexpr int kInv = kL + kHeads * 4;              // f32 [64] output factor per head
-  static constexpr int kBar = kInv + kHeads * 4;            // u64 s, pv
-  static constexpr int kMisc = kBar + 16;                   // tmem base
+  static constexpr int kBar = kInv + kHeads * 4;            // u64 s, pv, drain
+  static constexpr int kMisc = kBar + 24;                   // tmem base
   static constexpr int kBytes = kMisc + 16 + 1024;
 };
 static_assert(TcAttSmem::kBytes <= 227 * 1024, "shared memory");
@@ -119,17 +119,14 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc1_kernel(AttendParams p)
   const int q = blockIdx.x, hg = blockIdx.y;
   const int H = p.heads;
   const int h0 = hg * kHeads;
-  // sequence of query q (cu_new non-decreasing)
-  int b = 0;
-  {
-    int lo = 0, hi = p.num_seqs - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (p.cu_new[mid] <= q) lo = mid; else hi = mid - 1;
-    }
-    b = lo;
-  }
+  // sequence of query q (the row tile's space is free until the rows arrive)
+  const int b = find_seq_block(p.cu_new, p.num_seqs, q, reinterpret_cast<int*>(smem + L::kT), 8 * kChunk / 4 - 1);
   const SeqSpan sp = seq_span(p.cu_new, p.seq_len, b);
+  // the top-k list and the sequence's block-table row head for L2 while the count is read
+  if (p.topk_idx != nullptr && p.part != 1)
+    for (int i = tid * 32; i < p.k; i += kThreads * 32) prefetch_l2(p.topk_idx + (long long)q * p.k + i);
+  for (int i = tid * 32; i < p.paging.max_blocks; i += kThreads * 32)
+    prefetch_l2(p.paging.table + (long long)b * p.paging.max_blocks + i);
   const int n0 = sp.n0();
   const int t = n0 + (q - sp.q0);
   const int32_t* sel = p.topk_idx != nullptr ? p.topk_idx + (long long)q * p.k : nullptr;
@@ -218,6 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc1_kernel(AttendParams p)
   if (tid == 0) {
     mbar_init(bar_s, 1);
     mbar_init(bar_pv, 1);
+    mbar_init(bar_pv + 8, 1);   // drain
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(sbase + L::kMisc, 512);
@@ -262,8 +260,14 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc1_kernel(AttendParams p)
       }
     }
     if (tid < kTileRows) {
-      sscale[tid] = sc;
-      rinv[tid] = sc > 0.0f ? __frcp_rn(sc) : 0.0f;
+      float s_r = sc;
+      if (desc[tid] >= 0 && !(s_r < kMaxRowScale)) {   // p * s_r * 2^8 would leave the f16 range
+        report(p.status, LCS_ERR_DEVICE_GUARD);
+        desc[tid] = -1;
+        s_r = 0.0f;
+      }
+      sscale[tid] = s_r;
+      rinv[tid] = s_r > 0.0f ? __frcp_rn(s_r) : 0.0f;
     }
     __syncthreads();
 #pragma unroll
@@ -278,7 +282,13 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc1_kernel(AttendParams p)
 #pragma unroll
     for (int it = 0; it < kRP; ++it) {
       const int idx = it * kThreads + tid, r = idx >> 3, j = idx & 7;
-      *reinterpret_cast<uint4*>(smem + L::kT + r * 128 + ((j ^ (r & 7)) << 4)) = bf16x8_to_f16x8(rv[it], rinv[r]);
+      uint4 h = bf16x8_to_f16x8(rv[it], rinv[r]);
+      if (f16x8_nonfinite(h)) {   // |rope| / s_r beyond the f16 range: the row is left out
+        report(p.status, LCS_ERR_DEVICE_GUARD);
+        desc[r] = -1;
+        h = make_uint4(0u, 0u, 0u, 0u);
+      }
+      *reinterpret_cast<uint4*>(smem + L::kT + r * 128 + ((j ^ (r & 7)) << 4)) = h;
     }
   }
   cp_async_wait<0>();
@@ -308,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc1_kernel(AttendParams p)
                    smem_desc_sw128(sbase + L::kQ + c * kQChunk) + 2 * kk, kIdS, (c > 0 || kk > 0) ? 1u : 0u);
     tc_commit(bar_s);
   }
-  bool ok = mbar_wait(bar_s, 0, p.status);
+  bool ok = mbar_wait(bar_s, 0, p.status, nullptr, p.wait_polls);
   ok = __syncthreads_and(ok);
   tc_fence_after_sync();
 
@@ -372,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc1_kernel(AttendParams p)
                    smem_desc_sw128(sbase + L::kP + (kk >> 2) * kQChunk) + 2 * (kk & 3), kIdO, kk > 0 ? 1u : 0u);
     tc_commit(bar_pv);
   }
-  if (ok) ok = mbar_wait(bar_pv, 0, p.status);
+  if (ok) ok = mbar_wait(bar_pv, 0, p.status, nullptr, p.wait_polls);
   ok = __syncthreads_and(ok);
   tc_fence_after_sync();
 
@@ -429,6 +439,11 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc1_kernel(AttendParams p)
         ml[1] = l;
       }
     }
+  }
+  // after a wait gave up, the MMAs still in flight complete before tensor memory is released
+  if (tid == 0 && !ok) {
+    tc_commit(bar_pv + 8);
+    mbar_wait(bar_pv + 8, 0, nullptr, nullptr, kWaitPolls);
   }
   tc_fence_before_sync();
   __syncthreads();

@@ -35,6 +35,33 @@ __device__ __forceinline__ SeqSpan seq_span(const int32_t* cu_new, const int32_t
   return s;
 }
 
+// Sequence of global query q (cu_new non-decreasing), found by the whole CTA: cu_new is staged in
+// shared memory with one parallel load when the batch has at most `cap` sequences (a binary search
+// over global memory costs a dependent load per step), else searched in global memory.  Every
+// thread of the CTA calls it; scratch: cap + 1 ints of shared memory, free again on return.
+__device__ __forceinline__ int find_seq_block(const int32_t* cu_new, int num_seqs, int q, int* scratch, int cap) {
+  int lo = 0, hi = num_seqs - 1;
+  if (num_seqs + 1 <= cap) {
+    for (int i = threadIdx.x; i <= num_seqs; i += blockDim.x) scratch[i] = cu_new[i];
+    __syncthreads();
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (scratch[mid] <= q) lo = mid; else hi = mid - 1;
+    }
+    __syncthreads();
+    return lo;
+  }
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (cu_new[mid] <= q) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // Row set view (mirrors lcs_rows).
 struct Rows {
   int format;
@@ -83,6 +110,20 @@ __device__ __forceinline__ long long entry_row(const Paging& pg, int b, int j, l
 // ---------------------------------------------------------------------------------------------
 // Number formats
 // ---------------------------------------------------------------------------------------------
+
+// The attention kernels multiply probabilities by a row's FP8 scale s_r and by 2^8 in f16
+// (p * s_r * 2^8 <= 65504 needs s_r < 256), and the tensor-core kernels divide the RoPE dims by
+// s_r in f16 (|rope| / s_r <= 65504).  Rows outside these ranges are left out of the softmax and
+// reported as LCS_ERR_DEVICE_GUARD.
+constexpr float kMaxRowScale = 256.0f;
+
+// True when one of the f16 values is infinite or NaN (exponent bits all set).
+__device__ __forceinline__ bool f16x2_nonfinite(uint32_t w) {
+  return (w & 0x7C00u) == 0x7C00u || (w & 0x7C000000u) == 0x7C000000u;
+}
+__device__ __forceinline__ bool f16x8_nonfinite(uint4 v) {
+  return f16x2_nonfinite(v.x) || f16x2_nonfinite(v.y) || f16x2_nonfinite(v.z) || f16x2_nonfinite(v.w);
+}
 
 // fp32 pair -> two E4M3 codes (round to nearest even, saturate to +-448), packed low = a.
 __device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float a, float b) {
@@ -162,17 +203,18 @@ __device__ __forceinline__ void mma_e4m3_zero(float* d, uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
 }
 
-// cp.async 16 / 4 bytes global -> shared (L2-only for 16-byte copies).
+// cp.async 16 / 4 bytes global -> shared (L2-only for 16-byte copies).  The memory clobbers keep
+// the compiler from moving shared-memory reads across a copy's issue or its wait.
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem)), "l"(gmem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem)), "l"(gmem) : "memory");
 }
 __device__ __forceinline__ void cp_async4(void* smem, const void* gmem) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(smem)), "l"(gmem));
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(smem)), "l"(gmem) : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;"); }
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N));
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 __device__ __forceinline__ float warp_sum(float v) {

@@ -262,6 +262,198 @@ __global__ void __launch_bounds__(256) compress_entries_kernel(CompressParams p)
   store_row<D>(p.entries, row, lane, acc);
 }
 
+// Score row of raw token t (per-channel weights): this call's score rows or the pending ring.
+__device__ __forceinline__ const __nv_bfloat16* score_row(const CompressParams& p, int b, const SeqSpan& sp, int t,
+                                                          int D) {
+  if (t >= sp.n0()) return p.scores + (long long)(sp.q0 + t - sp.n0()) * D;
+  return p.pending_scores + ((long long)b * p.pending_slots + (t % p.pending_slots)) * D;
+}
+
+// Compression for ratios up to 4 (CSA): a warp takes a run of kRollEntries consecutive entries of
+// one sequence and streams their blocks of M rows through a three-slot ring of its own in shared
+// memory (cp.async, 16 bytes per lane, each lane reading back only the pieces it copied), so that
+// every raw row is read from memory once: block j-1 stays for entry j (overlapping windows) and
+// block j+1 is in flight while entry j is formed.  The arithmetic of an entry is the same whichever
+// warp or call forms it.  Scalar weights: z_t = (w . k_t as a warp sum) + bias[offset], the
+// softmax over the rows that exist in row order, the weighted sum in row order.  Per-channel
+// weights (PC): a slot also holds the block's score rows; per channel, z = score + bias[offset][c],
+// the maximum over the rows, then the exponentials' sum and the exponential-weighted sum of the
+// rows in row order, divided by that sum.
+constexpr int kRollEntries = 16;
+constexpr int kRollSlots = 3;
+
+template <int D, int M, bool PC>
+__global__ void __launch_bounds__(PC ? 128 : 256) compress_roll_kernel(CompressParams p) {
+  constexpr int kWarps = PC ? 4 : 8;
+  constexpr int PL = RowChunks<D>::kPerLane;
+  constexpr int C = RowChunks<D>::kChunks;
+  constexpr int kBlockBytes = (PC ? 2 : 1) * M * D * 2;
+  extern __shared__ __align__(16) uint8_t roll_smem[];
+  const int b = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const SeqSpan sp = seq_span(p.cu_new, p.seq_len, b);
+  const int j_first = sp.n0() / M, j_end = sp.n1 / M;
+  const int ja = j_first + (blockIdx.x * kWarps + warp) * kRollEntries;
+  const int jb = min(j_end, ja + kRollEntries);
+  if (ja >= jb) return;
+  const bool ov = p.overlap != 0;
+  uint8_t* ring = roll_smem + warp * (kRollSlots * kBlockBytes);
+  float wv[PL][8];
+#pragma unroll
+  for (int i = 0; i < PL; ++i) {
+    const int c = lane + 32 * i;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) wv[i][k] = (!PC && c < C) ? p.w[c * 8 + k] : 0.0f;
+  }
+  // block jj -> slot (jj + 1) % 3 (rows 0..M-1 the raw rows, M..2M-1 the score rows); this lane
+  // copies its own chunks (a group per block, empty for blocks outside [0, jb))
+  auto issue = [&](int jj) {
+    if (jj >= 0 && jj < jb) {
+      uint8_t* slot = ring + ((jj + 1) % kRollSlots) * kBlockBytes;
+#pragma unroll
+      for (int r = 0; r < (PC ? 2 * M : M); ++r) {
+        const __nv_bfloat16* src = r < M ? token_row(p, b, sp, jj * M + r, D) : score_row(p, b, sp, jj * M + r - M, D);
+#pragma unroll
+        for (int i = 0; i < PL; ++i) {
+          const int c = lane + 32 * i;
+          if (c < C) cp_async16(slot + r * D * 2 + c * 16, src + c * 8);
+        }
+      }
+    }
+    cp_async_commit();
+  };
+  // row r of block jj (r >= M: its score rows) as fp32, this lane's chunks
+  auto row_vals = [&](int jj, int r, float (&v)[PL][8]) {
+    const uint8_t* slot = ring + ((jj + 1) % kRollSlots) * kBlockBytes;
+#pragma unroll
+    for (int i = 0; i < PL; ++i) {
+      const int c = lane + 32 * i;
+      const uint4 u = c < C ? *reinterpret_cast<const uint4*>(slot + r * D * 2 + c * 16) : make_uint4(0, 0, 0, 0);
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 f = __bfloat1622float2(h[k]);
+        v[i][2 * k] = f.x;
+        v[i][2 * k + 1] = f.y;
+      }
+    }
+  };
+  auto block_z = [&](int jj, float (&z)[M]) {
+#pragma unroll
+    for (int r = 0; r < M; ++r) {
+      float v[PL][8];
+      row_vals(jj, r, v);
+      float acc = 0.0f;
+#pragma unroll
+      for (int i = 0; i < PL; ++i)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) acc = fmaf(wv[i][k], v[i][k], acc);
+      z[r] = warp_sum(acc);
+    }
+  };
+  issue(ov ? ja - 1 : -1);
+  issue(ja);
+  issue(ja + 1);
+  float zp[M], zc[M];
+  if (!PC && ov && ja >= 1) {
+    cp_async_wait<2>();
+    block_z(ja - 1, zp);
+  }
+  for (int j = ja; j < jb; ++j) {
+    cp_async_wait<1>();   // blocks j-1 and j have landed (block j+1 may still be in flight)
+    constexpr int R2 = 2 * M;
+    const bool prev = ov && j >= 1;   // rows of block j-1 exist and belong to the window
+    float acc[PL][8];
+#pragma unroll
+    for (int i = 0; i < PL; ++i)
+#pragma unroll
+      for (int k = 0; k < 8; ++k) acc[i][k] = 0.0f;
+    if constexpr (!PC) {
+      block_z(j, zc);
+      // softmax over the window rows that exist: block j-1 (offsets 0..M-1) then block j
+      float z[R2];
+      bool ex[R2];
+#pragma unroll
+      for (int r = 0; r < M; ++r) {
+        ex[r] = prev;
+        z[r] = ex[r] ? zp[r] + p.bias[r] : -INFINITY;
+        ex[M + r] = true;
+        z[M + r] = zc[r] + p.bias[ov ? M + r : r];
+      }
+      float zmax = -INFINITY;
+#pragma unroll
+      for (int r = 0; r < R2; ++r) zmax = fmaxf(zmax, z[r]);
+      float zsum = 0.0f;
+#pragma unroll
+      for (int r = 0; r < R2; ++r) zsum += ex[r] ? expf(z[r] - zmax) : 0.0f;
+      const float inv = 1.0f / zsum;
+#pragma unroll
+      for (int r = 0; r < R2; ++r) {
+        if (!ex[r]) continue;
+        const float a = expf(z[r] - zmax) * inv;
+        float v[PL][8];
+        row_vals(r < M ? j - 1 : j, r % M, v);
+#pragma unroll
+        for (int i = 0; i < PL; ++i)
+#pragma unroll
+          for (int k = 0; k < 8; ++k) acc[i][k] = fmaf(a, v[i][k], acc[i][k]);
+      }
+#pragma unroll
+      for (int r = 0; r < M; ++r) zp[r] = zc[r];
+    } else {
+      // per channel: z = score + bias[offset][channel] over the rows that exist
+      float zmax[PL][8], zsum[PL][8];
+#pragma unroll
+      for (int i = 0; i < PL; ++i)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          zmax[i][k] = -INFINITY;
+          zsum[i][k] = 0.0f;
+        }
+#pragma unroll
+      for (int pass = 0; pass < 2; ++pass) {
+#pragma unroll
+        for (int r = 0; r < R2; ++r) {
+          if (r < M && !prev) continue;
+          const int o = ov ? r : r - M;   // offset in the window (non-overlapping: block j only)
+          if (o < 0) continue;
+          float sv[PL][8];
+          row_vals(r < M ? j - 1 : j, M + (r % M), sv);
+          float v[PL][8];
+          if (pass == 1) row_vals(r < M ? j - 1 : j, r % M, v);
+#pragma unroll
+          for (int i = 0; i < PL; ++i) {
+            const int c = lane + 32 * i;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const float z = sv[i][k] + (c < C ? p.bias[o * D + c * 8 + k] : 0.0f);
+              if (pass == 0) {
+                zmax[i][k] = fmaxf(zmax[i][k], z);
+              } else {
+                const float e = expf(z - zmax[i][k]);
+                zsum[i][k] += e;
+                acc[i][k] = fmaf(e, v[i][k], acc[i][k]);
+              }
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < PL; ++i)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) acc[i][k] = zsum[i][k] > 0.0f ? acc[i][k] / zsum[i][k] : 0.0f;
+    }
+    const long long row = entry_row(p.paging, b, j, p.entries.num_rows);
+    if (row < 0) {
+      if (lane == 0) report(p.status, LCS_ERR_DEVICE_GUARD);
+    } else {
+      store_row<D>(p.entries, row, lane, acc);
+    }
+    issue(j + 2);   // into the slot of block j-1, whose last reader was entry j
+  }
+  cp_async_wait<0>();
+}
+
 // One warp per new token: keep it in the pending ring if a future entry needs it, and write
 // its quantised row to new_rows (or to the window ring when new_rows is absent).
 // grid: (ceil(max_new / 8), num_seqs), block 256.
@@ -290,6 +482,16 @@ __global__ void __launch_bounds__(256) compress_state_kernel(CompressParams p) {
       int c = lane + 32 * k;
       if (c < RowChunks<D>::kChunks)
         *reinterpret_cast<uint4*>(dst + c * 8) = *reinterpret_cast<const uint4*>(src + c * 8);
+    }
+    if (p.pending_scores != nullptr) {   // per-channel weights: the token's score row too
+      const __nv_bfloat16* ssrc = p.scores + (long long)(sp.q0 + i) * D;
+      __nv_bfloat16* sdst = p.pending_scores + ((long long)b * p.pending_slots + (t % p.pending_slots)) * D;
+#pragma unroll
+      for (int k = 0; k < PL; ++k) {
+        int c = lane + 32 * k;
+        if (c < RowChunks<D>::kChunks)
+          *reinterpret_cast<uint4*>(sdst + c * 8) = *reinterpret_cast<const uint4*>(ssrc + c * 8);
+      }
     }
   }
   if (p.new_rows.nope != nullptr) {
@@ -345,20 +547,49 @@ __global__ void __launch_bounds__(256) window_commit_kernel(const int32_t* cu_ne
 // launchers
 // ----------------------------------------------------------------------------------------------
 
+template <int D, int M, bool PC>
+cudaError_t launch_roll(const CompressParams& p, int max_entries, cudaStream_t st) {
+  constexpr int kWarps = PC ? 4 : 8;
+  constexpr size_t smem = (size_t)kWarps * kRollSlots * (PC ? 2 : 1) * M * D * 2;
+  static PerDeviceOnce attr;
+  cudaError_t e = once_per_device(attr, [] {
+    return cudaFuncSetAttribute(compress_roll_kernel<D, M, PC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)smem);
+  });
+  if (e != cudaSuccess) return e;
+  dim3 grid((max_entries + kWarps * kRollEntries - 1) / (kWarps * kRollEntries), p.num_seqs);
+  compress_roll_kernel<D, M, PC><<<grid, kWarps * 32, smem, st>>>(p);
+  return cudaGetLastError();
+}
+
+template <int D, bool PC>
+cudaError_t launch_roll_m(const CompressParams& p, int max_entries, cudaStream_t st) {
+  if (p.m == 4) return launch_roll<D, 4, PC>(p, max_entries, st);
+  if (p.m == 2) return launch_roll<D, 2, PC>(p, max_entries, st);
+  return launch_roll<D, 1, PC>(p, max_entries, st);
+}
+
 cudaError_t launch_compress(const CompressParams& p, int D, int max_new, cudaStream_t st) {
   const int R = p.overlap ? 2 * p.m : p.m;
   const int max_entries = max_new / p.m + 1;
-  const bool cta_per_entry = R > 16;
-  const int epc = cta_per_entry ? 1 : 8;
-  dim3 grid((max_entries + epc - 1) / epc, p.num_seqs);
-  if (D == 512) {
-    if (cta_per_entry) compress_entries_kernel<512, 8><<<grid, 256, 0, st>>>(p);
-    else compress_entries_kernel<512, 1><<<grid, 256, 0, st>>>(p);
+  cudaError_t e;
+  if (p.m == 4 || p.m == 2 || p.m == 1) {
+    const bool pc = p.scores != nullptr;
+    if (D == 512) e = pc ? launch_roll_m<512, true>(p, max_entries, st) : launch_roll_m<512, false>(p, max_entries, st);
+    else e = pc ? launch_roll_m<128, true>(p, max_entries, st) : launch_roll_m<128, false>(p, max_entries, st);
   } else {
-    if (cta_per_entry) compress_entries_kernel<128, 8><<<grid, 256, 0, st>>>(p);
-    else compress_entries_kernel<128, 1><<<grid, 256, 0, st>>>(p);
+    const bool cta_per_entry = R > 16;
+    const int epc = cta_per_entry ? 1 : 8;
+    dim3 grid((max_entries + epc - 1) / epc, p.num_seqs);
+    if (D == 512) {
+      if (cta_per_entry) compress_entries_kernel<512, 8><<<grid, 256, 0, st>>>(p);
+      else compress_entries_kernel<512, 1><<<grid, 256, 0, st>>>(p);
+    } else {
+      if (cta_per_entry) compress_entries_kernel<128, 8><<<grid, 256, 0, st>>>(p);
+      else compress_entries_kernel<128, 1><<<grid, 256, 0, st>>>(p);
+    }
+    e = cudaGetLastError();
   }
-  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || max_new == 0) return e;
   // without new_rows only the last state_tail tokens of each sequence go to the pending ring or
   // the window ring: launch warps for those alone

@@ -1,5 +1,5 @@
-// Lightning-indexer scores on the tcgen05 tensor cores for batches with a few
-// queries per sequence (decode, short speculative runs).
+// Lightning-indexer scores and top-k on the tcgen05 tensor cores for batches with a few queries
+// per sequence (decode, short speculative runs).
 //
 // Defined by: m.x-techcon.com/article/133366, section 2, CSA step 2 (a low-rank indexer scores
 // every compressed entry, each query keeps its top-k) and section 4 "FP4量化感知训练" (the
@@ -9,18 +9,17 @@
 // Layout of the work.  A persistent, warp-specialised CTA scans a contiguous run of 128-entry
 // tiles of one sequence for all of that sequence's queries (QPS <= 4), through a ring of
 // shared-memory stages:
-//   warps 8-9 (producers, alternating tiles) look the run's pages up in the block table once, then streams tiles:
-//                      one lane per page issues a TMA copy of the page's codes in the tensor
-//                      map's "16 x U4 in 16 bytes" form with the 128-byte swizzle -- each
-//                      entry's 128 E2M1 codes occupy one 128-byte shared-memory row, the K-major
-//                      operand form of the kind::f8f6f4 MMA with E2M1 inputs -- and every lane
-//                      copies 16 bytes of block scales with cp.async (tiny bulk copies issue too
-//                      slowly from one thread to keep a paged scan at memory speed);
-//   warp 10 (MMA)       issues four K = 32 MMAs per tile into one of kAcc tensor-memory
+//   warps 8-9 (producers, alternating tiles) look the run's pages up in the block table once,
+//                      then stream tiles: one lane per page issues a TMA copy of the page's codes
+//                      in the tensor map's "16 x U4 in 16 bytes" form with the 128-byte swizzle --
+//                      each entry's 128 E2M1 codes occupy one 128-byte shared-memory row, the
+//                      K-major operand form of the kind::f8f6f4 MMA with E2M1 inputs -- and every
+//                      lane copies 16 bytes of block scales with cp.async;
+//   warp 10 (MMA)      issues four K = 32 MMAs per tile into one of kAcc tensor-memory
 //                      accumulators and commits them to that accumulator's barrier;
-//   warps 0-7          (one thread per entry = per TMEM lane, two warps per lane quadrant
-//                      taking alternate tiles) read the accumulator and release it, form the scores, write the order-preserving keys and
-//                      count them into the per-query key histogram used by the top-k selection.
+//   warps 0-7          (one thread per entry = per TMEM lane, two warps per lane quadrant taking
+//                      the two tiles of a tile pair) read the accumulator, release it and form
+//                      the scores.
 // The grid is one wave: about (SMs x resident CTAs) / sequences CTAs per sequence.
 //
 // The MMA: A = 128 entries x 128 codes, B = N rows built from the queries, where row
@@ -29,7 +28,22 @@
 // is zero outside its block, column (blk, q, h) of D is exactly that block's partial dot product
 // (a sum of 32 products of E2M1 values: multiples of 1/4 below 2^11, exact in fp32).  Block
 // scales and head weights are applied afterwards in fp32, as in the warp-MMA scorer.
+//
+// Top-k, fused into the epilogue (FUSED = true).  Each query's candidates are 64-bit keys
+// (score key << 32 | ~j) in a shared-memory buffer of cap = 2k + 256: a score enters when its key
+// beats the query's threshold, the k-th largest key the buffer held at its last compaction (a key
+// below it cannot be among the k largest of the run, nor of the sequence).  After every tile pair
+// the epilogue warps meet at a named barrier; a buffer past cap - 256 is cut to its k largest keys
+// (exact radix selection) and the threshold rises.  At the end of its run a CTA writes its k
+// largest keys and their count to the workspace; the sequence's last CTA to finish (a ticket
+// counter, left at zero again) merges the runs' lists: the k-th largest key of the sequence by
+// the same radix selection, then a bitmap of the selected entries read out in ascending j.  A
+// separate merge kernel does the same when the scoring phase runs alone or the bitmap does not fit
+// the CTA's shared memory.  FUSED = false writes the fp32 scores themselves (csa_index_scores).
+#include <algorithm>
+
 #include "kernels.cuh"
+#include "select.cuh"
 #include "sm100.cuh"
 
 namespace lcsa {
@@ -37,20 +51,20 @@ namespace lcsa {
 namespace {
 
 constexpr int kTile = 128;          // entries per MMA tile (M)
-#ifndef LCSA_INDEX_STAGES
-#define LCSA_INDEX_STAGES 5
-#endif
-constexpr int kStages = LCSA_INDEX_STAGES;  // shared-memory ring depth (tiles in flight per CTA)
-constexpr int kAcc = 4;             // tensor-memory accumulators
-constexpr int kMaxPages = 256;      // block-table entries a CTA's run may span
+constexpr int kStages = 5;          // shared-memory ring depth (tiles in flight per CTA)
+constexpr int kAcc = 8;             // tensor-memory accumulators (the MMA runs up to 8 tiles ahead)
+constexpr int kMaxPages = 8192;     // block-table entries a CTA's run may span
 constexpr int kRowBytes = 128;      // shared-memory bytes of one entry's 128 codes (16U4 in 16 B)
 constexpr int kPackedRowBytes = 64; // global bytes of the same codes
 constexpr int kATileBytes = kTile * kRowBytes;
-constexpr int kEpiWarps = 8;        // two per TMEM lane quadrant, alternating tiles
+constexpr int kEpiWarps = 8;        // two per TMEM lane quadrant, the two tiles of a pair
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kProdWarps = 2;       // producer warps, alternating tiles
 constexpr int kScaleSlots = 2 * kStages;  // block-scale ring (read by the epilogue, outlives a stage)
 constexpr int kThreads = kEpiThreads + 32 * kProdWarps + 32;
+constexpr int kCandPerThread = 16;  // candidate buffer per query <= kEpiThreads * kCandPerThread
+constexpr int kEpiBarrier = 1;      // named barrier of the epilogue warps
+constexpr int kMaxRuns = 256;       // CTAs per sequence (run lists a merge reads)
 
 template <int QH, int QPS>
 struct TcSmem {
@@ -60,11 +74,24 @@ struct TcSmem {
   static constexpr int kScale = kB + N * kRowBytes;           // kScaleSlots x 128 x 4 B
   static constexpr int kQs = kScale + kScaleSlots * kTile * 4;  // f32 [QH][4] q block scales
   static constexpr int kHw = kQs + QH * 4 * 4;                // f32 [QH] head weights
-  static constexpr int kPages = kHw + QH * 4;                 // int [kMaxPages]
-  static constexpr int kBar = kPages + kMaxPages * 4;         // u64 full/empty[kStages], accf/acce[kAcc]
-  static constexpr int kMisc = kBar + (2 * kStages + 2 * kAcc) * 8;  // tmem base, abort flag
-  static constexpr int kHist = kMisc + 16;                    // u32 [QPS][2048]
-  static constexpr int kBytes = kHist + QPS * kTopkHistBins * 4 + 1024;
+  static constexpr int kBar = (kHw + QH * 4 + 7) / 8 * 8;     // u64 full/empty[kStages], accf/acce[kAcc], drain
+  static constexpr int kArmed = kBar + (2 * kStages + 2 * kAcc + 1) * 8;   // int [kStages] last tile armed
+  static constexpr int kMisc = kArmed + kStages * 4 + 4;      // tmem base, abort flag, last-CTA flag
+  // (16-byte aligned from here on: the selection scratch holds 8-byte fields)
+  static constexpr int kThr = (kMisc + 16 + 15) / 16 * 16;    // u64 [QPS] thresholds
+  static constexpr int kCnt = kThr + QPS * 8;                 // int [QPS] candidate counts
+  static constexpr int kSelEpi = (kCnt + QPS * 4 + 15) / 16 * 16;   // SelScratch<kEpiThreads>
+  static_assert(alignof(SelScratch<kThreads>) <= 16 && alignof(SelScratch<kEpiThreads>) <= 16, "scratch alignment");
+  // after the scan the ring is idle: its tail holds the whole CTA's selection scratch and the merge's
+  // run offsets, its head the run bitmap (final selection) or the staged run lists (merge)
+  static constexpr int kRingEnd = kA + kStages * kATileBytes;
+  static constexpr int kRunOff = (kRingEnd - 4 * (kMaxRuns + 4)) / 16 * 16;              // int [runs + 1]
+  static constexpr int kSelAll = (kRunOff - (int)sizeof(SelScratch<kThreads>)) / 16 * 16;  // SelScratch<kThreads>
+  static constexpr int kCand = (kSelEpi + (int)sizeof(SelScratch<kEpiThreads>) + 15) / 16 * 16;   // u64 [QPS][cap], then
+  // the run's page table: int [pages]
+  static size_t bytes(bool fused, int cap, int pages) {
+    return (size_t)kCand + (fused ? (size_t)QPS * cap * 8 : 0) + (size_t)pages * 4 + 1024;
+  }
 };
 
 __host__ __device__ constexpr uint32_t tmem_cols_for(int n) {
@@ -74,10 +101,171 @@ __host__ __device__ constexpr uint32_t tmem_cols_for(int n) {
 
 }  // namespace
 
-// grid: (runs per sequence, num_seqs); block kThreads.  CTA (x, b) scans tiles
-// [x*tiles_per_cta, (x+1)*tiles_per_cta) of sequence b (clipped to its visible entries).
-template <int HI, int QH>
-__global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, IndexParams p,
+// The run's selected keys (those >= tau of buf[0..n)), written to dst in ascending entry index:
+// a bitmap over the run's entries [j0, j0 + 32*words) gives every key its rank by position
+// (keys of the run lie in that range).  Group of NT threads; bitmap: `words` words and prefix:
+// `words` ints of shared memory.  Returns the number written.
+template <int NT, int ID>
+__device__ int write_run_sorted(const uint64_t* buf, int n, uint64_t tau, int j0, int words, uint32_t* bitmap,
+                                int* prefix, uint64_t* dst, SelScratch<NT>& sc) {
+  const int tid = threadIdx.x;
+  for (int w = tid; w < words; w += NT) bitmap[w] = 0u;
+  group_sync<NT, ID>();
+  for (int x = tid; x < n; x += NT) {
+    const uint64_t u = buf[x];
+    if (u >= tau) {
+      const uint32_t rj = ~(uint32_t)u - (uint32_t)j0;
+      atomicOr(&bitmap[rj >> 5], 1u << (rj & 31u));
+    }
+  }
+  group_sync<NT, ID>();
+  // exclusive prefix of the words' bit counts: thread t sums words [t*wpt, (t+1)*wpt)
+  const int wpt = (words + NT - 1) / NT;
+  const int w0 = min(words, tid * wpt), w1 = min(words, w0 + wpt);
+  int mine = 0;
+  for (int w = w0; w < w1; ++w) mine += __popc(bitmap[w]);
+  int tot;
+  int run = group_scan_incl<NT, ID>(mine, sc.warp_tot, &tot) - mine;
+  for (int w = w0; w < w1; ++w) {
+    prefix[w] = run;
+    run += __popc(bitmap[w]);
+  }
+  group_sync<NT, ID>();
+  for (int x = tid; x < n; x += NT) {
+    const uint64_t u = buf[x];
+    if (u >= tau) {
+      const uint32_t rj = ~(uint32_t)u - (uint32_t)j0;
+      const int w = (int)(rj >> 5);
+      dst[prefix[w] + __popc(bitmap[w] & ((1u << (rj & 31u)) - 1u))] = u;
+    }
+  }
+  group_sync<NT, ID>();
+  return tot;
+}
+
+// The merge of one query's run lists into its top-k (the scorer's last CTA of a query group, or
+// the merge kernel).  Group of NT threads (ID 0: the whole CTA).  Every run list is sorted by entry
+// index and the runs cover increasing index ranges, so the lists read one after the other are
+// sorted too: they are staged in shared memory (stage: room for runs * k keys), the k-th largest
+// key is selected there, and the keys at or above it are read out in that order.  N: visible
+// entries of the query; run_off: runs + 1 ints of shared memory.
+template <int NT, int ID>
+__device__ void merge_query_topk(const TopkRuns& tr, long long q, int N, int k, uint64_t* stage, int stage_cap,
+                                 int* run_off, int32_t* out_idx, int32_t* out_cnt, SelScratch<NT>& sc) {
+  const int tid = threadIdx.x;
+  int32_t* out = out_idx + q * k;
+  if (N <= k) {   // every visible entry
+    for (int j = tid; j < k; j += NT) out[j] = j < N ? j : -1;
+    if (tid == 0) out_cnt[q] = N;
+    return;
+  }
+  const int* cnts = tr.cnt + q * tr.runs;
+  const uint64_t* keys = tr.keys + q * (long long)tr.runs * k;
+  // list offsets in the stage
+  {
+    const int c = tid < tr.runs ? min(__ldcg(cnts + tid), k) : 0;   // runs <= 256 <= NT
+    int tot;
+    const int incl = group_scan_incl<NT, ID>(c, sc.warp_tot, &tot);
+    if (tid < tr.runs) run_off[tid] = incl - c;
+    if (tid == 0) run_off[tr.runs] = tot;
+  }
+  group_sync<NT, ID>();
+  const int total = run_off[tr.runs];
+  // stage the lists: eight independent loads in flight per thread; a full run's smallest key is
+  // its k-th largest, and the largest of those bounds the sequence's k-th largest from below
+  if (tid == 0) sc.span[0] = 0ull;
+  group_sync<NT, ID>();
+  for (int x0 = tid; x0 < total; x0 += 8 * NT) {
+    uint64_t v[8];
+    int at[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int x = x0 + u * NT;
+      at[u] = -1;
+      v[u] = 0ull;
+      if (x < total) {
+        int lo = 0, hi = tr.runs - 1;   // the run holding stage position x
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (run_off[mid] <= x) lo = mid; else hi = mid - 1;
+        }
+        at[u] = x;
+        v[u] = __ldcg(reinterpret_cast<const unsigned long long*>(keys) + (long long)lo * k + (x - run_off[lo]));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      if (at[u] >= 0) stage[at[u]] = v[u];
+  }
+  group_sync<NT, ID>();
+  uint64_t tau;
+  if (total <= k) {
+    tau = 0ull;   // (fewer than k candidates only when the scoring gave up on a bounded wait: take them all)
+  } else {
+    // bound: the largest minimum over the runs that kept k keys (each such run has k keys >= it)
+    for (int r = 0; r < tr.runs; ++r) {
+      if (run_off[r + 1] - run_off[r] != k) continue;
+      unsigned long long mn = ~0ull;
+      for (int x = run_off[r] + tid; x < run_off[r + 1]; x += NT) mn = stage[x] < mn ? stage[x] : mn;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long y = __shfl_xor_sync(0xffffffffu, mn, o);
+        mn = y < mn ? y : mn;
+      }
+      if ((tid & 31) == 0 && mn != ~0ull) atomicMax(&sc.span[0], mn);
+    }
+    group_sync<NT, ID>();
+    const uint64_t bound = sc.span[0];
+    // the keys at or above the bound (at least k of them) gathered behind the staged lists when
+    // they fit, and the k-th largest selected among them only; else among all staged keys
+    uint64_t* cand = stage + total;
+    const int room = stage_cap - total;
+    if (tid == 0) sc.count = 0;
+    group_sync<NT, ID>();
+    for (int x0 = 0; x0 < total; x0 += NT) {
+      const int x = x0 + tid;
+      const uint64_t u = x < total ? stage[x] : 0ull;
+      const bool take = x < total && u >= bound;
+      const unsigned m = __ballot_sync(0xffffffffu, take);
+      if (m != 0u) {
+        const int leader = __ffs(m) - 1;
+        int base = 0;
+        if ((tid & 31) == leader) base = atomicAdd(&sc.count, __popc(m));
+        base = __shfl_sync(0xffffffffu, base, leader);
+        const int at = base + __popc(m & ((1u << (tid & 31)) - 1u));
+        if (take && at < room) cand[at] = u;
+      }
+    }
+    group_sync<NT, ID>();
+    const int nc = sc.count;
+    group_sync<NT, ID>();
+    tau = nc <= room ? kth_largest_key<NT, ID>(k, SmemKeys{cand, nc}, sc)
+                     : kth_largest_key<NT, ID>(k, SmemKeys{stage, total}, sc);
+  }
+  // ascending read-out: thread t takes stage positions [t*ppt, (t+1)*ppt)
+  const int ppt = (total + NT - 1) / NT;
+  const int x0 = min(total, tid * ppt), x1 = min(total, x0 + ppt);
+  int mine = 0;
+  for (int x = x0; x < x1; ++x) mine += stage[x] >= tau ? 1 : 0;
+  int tot;
+  int pos = group_scan_incl<NT, ID>(mine, sc.warp_tot, &tot) - mine;
+  for (int x = x0; x < x1; ++x) {
+    const uint64_t u = stage[x];
+    if (u >= tau) {
+      if (pos < k) out[pos] = (int32_t)~(uint32_t)u;
+      ++pos;
+    }
+  }
+  for (int j = tot + tid; j < k; j += NT) out[j] = -1;   // (tot == k for exact selections)
+  if (tid == 0) out_cnt[q] = min(tot, k);
+  group_sync<NT, ID>();
+}
+
+// grid: (runs, query groups, num_seqs); block kThreads.  CTA (x, g, b) scans tiles
+// [x*tiles_per_cta, (x+1)*tiles_per_cta) of sequence b (clipped to its visible entries) for the
+// sequence's queries g*QPS .. g*QPS + QPS - 1.
+template <int HI, int QH, bool FUSED>
+__global__ void __launch_bounds__(kThreads, QH >= 16 ? 1 : 2) index_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, IndexParams p,
                                                            int tiles_per_cta) {
   constexpr int QPS = QH / HI;
   using L = TcSmem<QH, QPS>;
@@ -88,234 +276,348 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int b = blockIdx.y;
+  const int b = blockIdx.z;
   const SeqSpan sp = seq_span(p.cu_new, p.seq_len, b);
-  const int qn = min(sp.qn, QPS);
-  if (qn <= 0) return;
-  const int n0 = sp.n0();
+  const int qg0 = blockIdx.y * QPS;                // the group's first query within the sequence
+  const int qn = min(sp.qn - qg0, QPS);
+  if (qn <= 0) return;   // (every CTA of the query group returns here: no ticket is taken)
+  const long long qrow0 = (long long)sp.q0 + qg0;  // its row in the batch
+  const int n0 = sp.n0() + qg0;                    // its position
   const int mshift = 31 - __clz(p.m);
   const int nmax = (n0 + qn) >> mshift;          // visible entries of the sequence's last query
   const int t_begin = blockIdx.x * tiles_per_cta;
   const int t_end = min((nmax + kTile - 1) / kTile, t_begin + tiles_per_cta);
-  if (t_begin >= t_end) return;
-  const int nt = t_end - t_begin;
-  const bool with_hist = p.hist != nullptr;
+  const int nt = max(0, t_end - t_begin);
+  const int k = p.top_k;
+  const int cap = p.cand_cap;
+  SelScratch<kThreads>& sel_all = *reinterpret_cast<SelScratch<kThreads>*>(smem + L::kSelAll);
+  uint64_t* thr_s = reinterpret_cast<uint64_t*>(smem + L::kThr);
+  int* cnt_s = reinterpret_cast<int*>(smem + L::kCnt);
+  uint64_t* cand_s = reinterpret_cast<uint64_t*>(smem + L::kCand);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 8);
+  if (nt == 0) {
+    if constexpr (FUSED) {
+      // no tiles in this run (ragged batch): an empty candidate list, and the ticket still counts it
+      for (int qi = tid; qi < qn; qi += kThreads) p.runs.cnt[(qrow0 + qi) * p.runs.runs + blockIdx.x] = 0;
+    } else {
+      return;
+    }
+  }
   const int epb = p.paging.epb;
   const int eshift = 31 - __clz(epb);
   const int page0 = (t_begin * kTile) >> eshift;
-  const int npages = ((min(nmax, t_end * kTile) - 1) >> eshift) - page0 + 1;  // <= kMaxPages (host)
+  const int npages = nt > 0 ? ((min(nmax, t_end * kTile) - 1) >> eshift) - page0 + 1 : 0;  // <= kMaxPages (host)
 
-  uint32_t* hist_s = reinterpret_cast<uint32_t*>(smem + L::kHist);
   float* qs_s = reinterpret_cast<float*>(smem + L::kQs);
   float* hw_s = reinterpret_cast<float*>(smem + L::kHw);
-  int* pages_s = reinterpret_cast<int*>(smem + L::kPages);
+  int* pages_s = reinterpret_cast<int*>(smem + L::kCand + (FUSED ? QPS * cap * 8 : 0));
+  int* armed_s = reinterpret_cast<int*>(smem + L::kArmed);
   const uint32_t bar_full = sbase + L::kBar;
   const uint32_t bar_empty = bar_full + kStages * 8;
   const uint32_t bar_accf = bar_empty + kStages * 8;
   const uint32_t bar_acce = bar_accf + kAcc * 8;
+  const uint32_t bar_drain = bar_acce + kAcc * 8;
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+  const uint32_t polls = p.wait_polls;
 
-  if (tid == kEpiThreads) {
-    for (int i = 0; i < kStages; ++i) {
-      mbar_init(bar_full + 8 * i, 33);   // the expect-tx arrival + one per producer lane
-      mbar_init(bar_empty + 8 * i, 1);   // the MMA commit
+  if (nt > 0) {
+    if (tid == kEpiThreads) {
+      for (int i = 0; i < kStages; ++i) {
+        mbar_init(bar_full + 8 * i, 33);   // the expect-tx arrival + one per producer lane
+        mbar_init(bar_empty + 8 * i, 1);   // the MMA commit
+        armed_s[i] = -1;
+      }
+      for (int i = 0; i < kAcc; ++i) {
+        mbar_init(bar_accf + 8 * i, 1);
+        mbar_init(bar_acce + 8 * i, 4);
+      }
+      mbar_init(bar_drain, 1);
+      *abort_flag = 0;
+      fence_mbar_init();
+      tma_prefetch_desc(&tmap_k);
     }
-    for (int i = 0; i < kAcc; ++i) {
-      mbar_init(bar_accf + 8 * i, 1);
-      mbar_init(bar_acce + 8 * i, 4);
+    if (FUSED && tid < QPS) {
+      thr_s[tid] = 0ull;
+      cnt_s[tid] = 0;
     }
-    *abort_flag = 0;
-    fence_mbar_init();
-    tma_prefetch_desc(&tmap_k);
-  }
-  __syncthreads();
+    __syncthreads();
 
-  if (warp == kEpiWarps) {
-    tmem_alloc(sbase + L::kMisc, kCols);
-    // physical block of every page the run touches (-1: unmapped or outside the key rows)
-    for (int i = lane; i < npages; i += 32) {
-      const int blk = page0 + i;
-      int phys = blk < p.paging.max_blocks ? p.paging.table[(long long)b * p.paging.max_blocks + blk] : -1;
-      if (phys < 0 || (long long)(phys + 1) * epb > p.k_rows) {
-        report(p.status, LCS_ERR_DEVICE_GUARD);
-        phys = -1;
-      }
-      pages_s[i] = phys;
-    }
-  } else if (warp < kEpiWarps) {
-    // ---- B operand: row n = blk*QH + c, c = qi*HI + h; codes of block blk in chunks 2blk, 2blk+1
-    for (int idx = tid; idx < N * 8; idx += kEpiThreads) {
-      const int n = idx >> 3, ch = idx & 7;
-      const int blk = n / QH, c = n % QH;
-      const int qi = c / HI, h = c % HI;
-      uint2 v = make_uint2(0u, 0u);
-      if ((ch >> 1) == blk && qi < qn) {
-        const long long qrow = (long long)(sp.q0 + qi) * HI + h;
-        const uint32_t* src = reinterpret_cast<const uint32_t*>(p.q_fp4 + qrow * 64 + ch * 8);
-        v = make_uint2(src[0], src[1]);
-      }
-      const int phys_ch = ch ^ (n & 7);
-      *reinterpret_cast<uint4*>(smem + L::kB + n * kRowBytes + phys_ch * 16) = make_uint4(v.x, v.y, 0u, 0u);
-    }
-    for (int idx = tid; idx < QH * 4; idx += kEpiThreads) {
-      const int c = idx >> 2, blk = idx & 3;
-      const int qi = c / HI, h = c % HI;
-      qs_s[idx] = qi < qn ? ue8m0_to_f32(p.q_scale[((long long)(sp.q0 + qi) * HI + h) * 4 + blk]) : 0.0f;
-    }
-    for (int c = tid; c < QH; c += kEpiThreads) {
-      const int qi = c / HI, h = c % HI;
-      hw_s[c] = qi < qn ? (p.head_w ? p.head_w[(long long)(sp.q0 + qi) * HI + h] : 1.0f) : 0.0f;
-    }
-    if (with_hist)
-      for (int i = tid; i < qn * kTopkHistBins; i += kEpiThreads) hist_s[i] = 0u;
-    fence_proxy_async_smem();
-  }
-  tc_fence_before_sync();
-  __syncthreads();
-  tc_fence_after_sync();
-  const uint32_t tmem = *tmem_slot;
-
-  if (warp >= kEpiWarps && warp < kEpiWarps + kProdWarps) {
-    // ---- producer warps (tile i by producer warp i % kProdWarps): stage i % kStages receives
-    //      tile t_begin + i.  Lane p issues page p's
-    //      tensor copy of the codes (the TMA unpacks them into the MMA operand form); every lane
-    //      copies 16 bytes of block scales with cp.async.  The stage's barrier expects the code
-    //      bytes from the copies plus one arrival per lane when its scale copy lands.
-    for (int i = warp - kEpiWarps; i < nt; i += kProdWarps) {
-      const int s = i % kStages;
-      bool ok = true;
-      if (lane == 0) ok = mbar_wait(bar_empty + 8 * s, ((i / kStages) & 1) ^ 1, p.status, abort_flag);
-      if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) == 0) break;
-      const int e0 = (t_begin + i) * kTile;
-      const int rows = min(kTile, ((min(nmax, e0 + kTile) - e0 + epb - 1) >> eshift) << eshift);  // whole pages
-      const uint32_t bar = bar_full + 8 * s;
-      const uint32_t a_dst = sbase + L::kA + s * kATileBytes;
-      const uint32_t s_dst = sbase + L::kScale + (i % kScaleSlots) * kTile * 4;
-      const int npg = rows >> eshift;
-      const int phys = lane < npg ? pages_s[((e0 >> eshift) - page0) + lane] : -1;
-      const uint32_t valid = __ballot_sync(0xffffffffu, phys >= 0);
-      if (lane == 0) mbar_arrive_expect_tx(bar, __popc(valid) * epb * kPackedRowBytes);
-      __syncwarp();
-      if (phys >= 0) tma_load_2d(a_dst + (lane << eshift) * kRowBytes, &tmap_k, 0, phys * epb, bar);
-      const int r = lane * 4;   // this lane's four scale words
-      const int ph = __shfl_sync(0xffffffffu, phys, (r >> eshift) & 31);
-      if (r < rows && ph >= 0) cp_async16_s(s_dst + r * 4, p.k_scale + ((long long)ph * epb + (r & (epb - 1))) * 4);
-      cp_async_arrive_noinc(bar);
-    }
-    cp_async_wait<0>();
-  } else if (warp == kEpiWarps + kProdWarps) {
-    if (lane == 0) {
-      // ---- MMA issuer: tile i -> accumulator i % kAcc
-      const uint64_t bdesc = smem_desc_sw128(sbase + L::kB);
-      for (int i = 0; i < nt; ++i) {
-        const int s = i % kStages, a = i % kAcc;
-        if (!mbar_wait(bar_full + 8 * s, (i / kStages) & 1, p.status, abort_flag)) break;
-        if (!mbar_wait(bar_acce + 8 * a, ((i / kAcc) & 1) ^ 1, p.status, abort_flag)) break;
-        tc_fence_after_sync();
-        const uint64_t adesc = smem_desc_sw128(sbase + L::kA + s * kATileBytes);
-#pragma unroll
-        for (int kb = 0; kb < 4; ++kb)   // K = 32 codes per MMA: 32 shared-memory bytes per step
-          tc_mma_f8f6f4(tmem + a * N, adesc + 2 * kb, bdesc + 2 * kb, kIdesc, kb > 0 ? 1u : 0u);
-        tc_commit(bar_accf + 8 * a);
-        tc_commit(bar_empty + 8 * s);   // the stage is free once these MMAs have read it
-      }
-    }
-    __syncwarp();
-  } else {
-    // ---- epilogue: warp w reads TMEM lanes 32*(w%4).. of the tiles i with i % 2 == w / 4
-    const int quad = warp & 3, par = warp >> 2;
-    float qsc[QH][4], hw[QH], qw[QH][4];
-#pragma unroll
-    for (int c = 0; c < QH; ++c) {
-      hw[c] = hw_s[c];
-#pragma unroll
-      for (int blk = 0; blk < 4; ++blk) {
-        qsc[c][blk] = qs_s[c * 4 + blk];
-        qw[c][blk] = qsc[c][blk] * hw[c];   // powers of two times the head weight: exact
-      }
-    }
-    int nq[QPS];
-#pragma unroll
-    for (int qi = 0; qi < QPS; ++qi) nq[qi] = qi < qn ? (n0 + qi + 1) >> mshift : 0;
-    const int row = quad * 32 + lane;
-    for (int i = par; i < nt; i += 2) {
-      const int a = i % kAcc;
-      bool ok = mbar_wait(bar_accf + 8 * a, (i / kAcc) & 1, p.status, abort_flag);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after_sync();
-      uint32_t d[N];
-#pragma unroll
-      for (int c16 = 0; c16 < N / 16; ++c16)
-        tmem_ld16(tmem + ((uint32_t)(quad * 32) << 16) + a * N + c16 * 16,
-                  *reinterpret_cast<uint32_t(*)[16]>(&d[c16 * 16]));
-      tmem_ld_wait();
-      const uint32_t sc = *reinterpret_cast<const uint32_t*>(smem + L::kScale + ((i % kScaleSlots) * kTile + row) * 4);
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_acce + 8 * a);
-      // 2^(e-127) for the four UE8M0 bytes (e = 0 gives the subnormal 2^-127)
-      float ksc[4];
-      ksc[0] = __uint_as_float(max((sc << 23) & 0x7F800000u, 0x00400000u));
-      ksc[1] = __uint_as_float(max((sc << 15) & 0x7F800000u, 0x00400000u));
-      ksc[2] = __uint_as_float(max((sc << 7) & 0x7F800000u, 0x00400000u));
-      ksc[3] = __uint_as_float(max((sc >> 1) & 0x7F800000u, 0x00400000u));
-      const int j = (t_begin + i) * kTile + row;
-#pragma unroll
-      for (int qi = 0; qi < QPS; ++qi) {
-        float score;
-        if (!p.relu) {
-          // phi = identity: sum over heads inside each block first (every term exact)
-          float tb[4];
-#pragma unroll
-          for (int blk = 0; blk < 4; ++blk) {
-            float t = 0.0f;
-#pragma unroll
-            for (int h = 0; h < HI; ++h) t = fmaf(__uint_as_float(d[blk * QH + qi * HI + h]), qw[qi * HI + h][blk], t);
-            tb[blk] = t;
-          }
-          score = fmaf(tb[3], ksc[3], fmaf(tb[2], ksc[2], fmaf(tb[1], ksc[1], tb[0] * ksc[0])));
-        } else {
-          float sh[HI];
-#pragma unroll
-          for (int h = 0; h < HI; ++h) {
-            const int c = qi * HI + h;
-            float acc = 0.0f;
-#pragma unroll
-            for (int blk = 0; blk < 4; ++blk) acc = fmaf(__uint_as_float(d[blk * QH + c]), ksc[blk] * qsc[c][blk], acc);
-            sh[h] = fmaxf(acc, 0.0f) * hw[c];
-          }
-#pragma unroll
-          for (int w = 1; w < HI; w <<= 1)
-#pragma unroll
-            for (int h = 0; h < HI; h += 2 * w) sh[h] = sh[h] + sh[h + w];
-          score = sh[0];
+    if (warp == kEpiWarps) {
+      tmem_alloc(sbase + L::kMisc, kCols);
+      // physical block of every page the run touches (-1: unmapped or outside the key rows)
+      for (int i = lane; i < npages; i += 32) {
+        const int blk = page0 + i;
+        int phys = blk < p.paging.max_blocks ? p.paging.table[(long long)b * p.paging.max_blocks + blk] : -1;
+        if (phys < 0 || (long long)(phys + 1) * epb > p.k_rows) {
+          report(p.status, LCS_ERR_DEVICE_GUARD);
+          phys = -1;
         }
-        if (j < nq[qi]) {
-          const long long o = (long long)(sp.q0 + qi) * p.ld + j;
-          if (p.scores_out != nullptr) {
-            p.scores_out[o] = score;
-          } else {
-            const uint32_t key = score_key(score);
-            p.keys_out[o] = key;
-            if (with_hist) atomicAdd(&hist_s[qi * kTopkHistBins + (key >> 21)], 1u);
-          }
-        }
+        pages_s[i] = phys;
       }
+    } else if (warp < kEpiWarps) {
+      // ---- B operand: row n = blk*QH + c, c = qi*HI + h; codes of block blk in chunks 2blk, 2blk+1
+      for (int idx = tid; idx < N * 8; idx += kEpiThreads) {
+        const int n = idx >> 3, ch = idx & 7;
+        const int blk = n / QH, c = n % QH;
+        const int qi = c / HI, h = c % HI;
+        uint2 v = make_uint2(0u, 0u);
+        if ((ch >> 1) == blk && qi < qn) {
+          const long long qrow = (qrow0 + qi) * HI + h;
+          const uint32_t* src = reinterpret_cast<const uint32_t*>(p.q_fp4 + qrow * 64 + ch * 8);
+          v = make_uint2(src[0], src[1]);
+        }
+        const int phys_ch = ch ^ (n & 7);
+        *reinterpret_cast<uint4*>(smem + L::kB + n * kRowBytes + phys_ch * 16) = make_uint4(v.x, v.y, 0u, 0u);
+      }
+      for (int idx = tid; idx < QH * 4; idx += kEpiThreads) {
+        const int c = idx >> 2, blk = idx & 3;
+        const int qi = c / HI, h = c % HI;
+        qs_s[idx] = qi < qn ? ue8m0_to_f32(p.q_scale[((qrow0 + qi) * HI + h) * 4 + blk]) : 0.0f;
+      }
+      for (int c = tid; c < QH; c += kEpiThreads) {
+        const int qi = c / HI, h = c % HI;
+        hw_s[c] = qi < qn ? (p.head_w ? p.head_w[(qrow0 + qi) * HI + h] : 1.0f) : 0.0f;
+      }
+      fence_proxy_async_smem();
     }
-  }
-  tc_fence_before_sync();
-  __syncthreads();
-  if (warp == kEpiWarps) {
+    tc_fence_before_sync();
+    __syncthreads();
     tc_fence_after_sync();
-    tmem_dealloc(tmem, kCols);
-  } else if (warp < kEpiWarps && with_hist) {
-    for (int i = tid; i < qn * kTopkHistBins; i += kEpiThreads) {
-      const uint32_t c = hist_s[i];
-      if (c) atomicAdd(&p.hist[(long long)(sp.q0 + i / kTopkHistBins) * kTopkHistBins + i % kTopkHistBins], c);
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp >= kEpiWarps && warp < kEpiWarps + kProdWarps) {
+      // ---- producer warps (tile i by producer warp i % kProdWarps): stage i % kStages receives
+      //      tile t_begin + i.  Lane p issues page p's tensor copy of the codes (the TMA unpacks
+      //      them into the MMA operand form); every lane copies 16 bytes of block scales with
+      //      cp.async.  The stage's barrier expects the code bytes from the copies plus one
+      //      arrival per lane when its scale copy lands.
+      for (int i = warp - kEpiWarps; i < nt; i += kProdWarps) {
+        const int s = i % kStages;
+        bool ok = true;
+        if (lane == 0) ok = mbar_wait(bar_empty + 8 * s, ((i / kStages) & 1) ^ 1, p.status, abort_flag, polls);
+        if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) == 0) break;
+        const int e0 = (t_begin + i) * kTile;
+        const int rows = min(kTile, ((min(nmax, e0 + kTile) - e0 + epb - 1) >> eshift) << eshift);  // whole pages
+        const uint32_t bar = bar_full + 8 * s;
+        const uint32_t a_dst = sbase + L::kA + s * kATileBytes;
+        const uint32_t s_dst = sbase + L::kScale + (i % kScaleSlots) * kTile * 4;
+        const int npg = rows >> eshift;
+        const int phys = lane < npg ? pages_s[((e0 >> eshift) - page0) + lane] : -1;
+        const uint32_t valid = __ballot_sync(0xffffffffu, phys >= 0);
+        if (lane == 0) {
+          armed_s[s] = i;
+          mbar_arrive_expect_tx(bar, __popc(valid) * epb * kPackedRowBytes);
+        }
+        __syncwarp();
+        if (phys >= 0) tma_load_2d(a_dst + (lane << eshift) * kRowBytes, &tmap_k, 0, phys * epb, bar);
+        const int r = lane * 4;   // this lane's four scale words
+        const int ph = __shfl_sync(0xffffffffu, phys, (r >> eshift) & 31);
+        if (r < rows && ph >= 0) cp_async16_s(s_dst + r * 4, p.k_scale + ((long long)ph * epb + (r & (epb - 1))) * 4);
+        cp_async_arrive_noinc(bar);
+      }
+      cp_async_wait<0>();
+    } else if (warp == kEpiWarps + kProdWarps) {
+      if (lane == 0) {
+        // ---- MMA issuer: tile i -> accumulator i % kAcc
+        const uint64_t bdesc = smem_desc_sw128(sbase + L::kB);
+        bool issued = false;
+        for (int i = 0; i < nt; ++i) {
+          const int s = i % kStages, a = i % kAcc;
+          if (!mbar_wait(bar_full + 8 * s, (i / kStages) & 1, p.status, abort_flag, polls)) break;
+          if (!mbar_wait(bar_acce + 8 * a, ((i / kAcc) & 1) ^ 1, p.status, abort_flag, polls)) break;
+          tc_fence_after_sync();
+          const uint64_t adesc = smem_desc_sw128(sbase + L::kA + s * kATileBytes);
+#pragma unroll
+          for (int kb = 0; kb < 4; ++kb)   // K = 32 codes per MMA: 32 shared-memory bytes per step
+            tc_mma_f8f6f4(tmem + a * N, adesc + 2 * kb, bdesc + 2 * kb, kIdesc, kb > 0 ? 1u : 0u);
+          tc_commit(bar_accf + 8 * a);
+          tc_commit(bar_empty + 8 * s);   // the stage is free once these MMAs have read it
+          issued = true;
+        }
+        // every MMA issued here has completed before the CTA releases tensor memory
+        if (issued && *abort_flag) {
+          tc_commit(bar_drain);
+          mbar_wait(bar_drain, 0, nullptr, nullptr, kWaitPolls);
+        }
+      }
+      __syncwarp();
+    } else {
+      // ---- epilogue: tile pair ip = tiles 2ip (warps 0-3) and 2ip+1 (warps 4-7); warp w reads
+      //      TMEM lanes 32*(w%4).. (its entries)
+      const int quad = warp & 3, par = warp >> 2;
+      float qsc[QH][4], hw[QH], qw[QH][4];
+#pragma unroll
+      for (int c = 0; c < QH; ++c) {
+        hw[c] = hw_s[c];
+#pragma unroll
+        for (int blk = 0; blk < 4; ++blk) {
+          qsc[c][blk] = qs_s[c * 4 + blk];
+          qw[c][blk] = qsc[c][blk] * hw[c];   // powers of two times the head weight: exact
+        }
+      }
+      int nq[QPS];
+#pragma unroll
+      for (int qi = 0; qi < QPS; ++qi) nq[qi] = qi < qn ? (n0 + qi + 1) >> mshift : 0;
+      const int row = quad * 32 + lane;
+      SelScratch<kEpiThreads>& sel = *reinterpret_cast<SelScratch<kEpiThreads>*>(smem + L::kSelEpi);
+      bool alive = true;
+      for (int i0 = 0; i0 < nt; i0 += 2) {
+        const int i = i0 + par;
+        if (i < nt && alive) {
+          const int a = i % kAcc;
+          bool ok = mbar_wait(bar_accf + 8 * a, (i / kAcc) & 1, p.status, abort_flag, polls);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) {
+            alive = false;
+          } else {
+            tc_fence_after_sync();
+            uint32_t d[N];
+#pragma unroll
+            for (int c16 = 0; c16 < N / 16; ++c16)
+              tmem_ld16(tmem + ((uint32_t)(quad * 32) << 16) + a * N + c16 * 16,
+                        *reinterpret_cast<uint32_t(*)[16]>(&d[c16 * 16]));
+            tmem_ld_wait();
+            const uint32_t sc =
+                *reinterpret_cast<const uint32_t*>(smem + L::kScale + ((i % kScaleSlots) * kTile + row) * 4);
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_acce + 8 * a);
+            // 2^(e-127) for the four UE8M0 bytes (e = 0 gives the subnormal 2^-127)
+            float ksc[4];
+            ksc[0] = __uint_as_float(max((sc << 23) & 0x7F800000u, 0x00400000u));
+            ksc[1] = __uint_as_float(max((sc << 15) & 0x7F800000u, 0x00400000u));
+            ksc[2] = __uint_as_float(max((sc << 7) & 0x7F800000u, 0x00400000u));
+            ksc[3] = __uint_as_float(max((sc >> 1) & 0x7F800000u, 0x00400000u));
+            const int j = (t_begin + i) * kTile + row;
+#pragma unroll
+            for (int qi = 0; qi < QPS; ++qi) {
+              float score;
+              if (!p.relu) {
+                // phi = identity: sum over heads inside each block first (every term exact)
+                float tb[4];
+#pragma unroll
+                for (int blk = 0; blk < 4; ++blk) {
+                  float t = 0.0f;
+#pragma unroll
+                  for (int h = 0; h < HI; ++h)
+                    t = fmaf(__uint_as_float(d[blk * QH + qi * HI + h]), qw[qi * HI + h][blk], t);
+                  tb[blk] = t;
+                }
+                score = fmaf(tb[3], ksc[3], fmaf(tb[2], ksc[2], fmaf(tb[1], ksc[1], tb[0] * ksc[0])));
+              } else {
+                float sh[HI];
+#pragma unroll
+                for (int h = 0; h < HI; ++h) {
+                  const int c = qi * HI + h;
+                  float acc = 0.0f;
+#pragma unroll
+                  for (int blk = 0; blk < 4; ++blk)
+                    acc = fmaf(__uint_as_float(d[blk * QH + c]), ksc[blk] * qsc[c][blk], acc);
+                  sh[h] = fmaxf(acc, 0.0f) * hw[c];
+                }
+#pragma unroll
+                for (int w = 1; w < HI; w <<= 1)
+#pragma unroll
+                  for (int h = 0; h < HI; h += 2 * w) sh[h] = sh[h] + sh[h + w];
+                score = sh[0];
+              }
+              const bool vis = j < nq[qi];
+              if constexpr (FUSED) {
+                const uint64_t key = ((uint64_t)score_key(score) << 32) | (uint64_t)(~(uint32_t)j);
+                warp_append(vis && key > thr_s[qi], key, cand_s + qi * cap, cnt_s + qi);
+              } else {
+                if (vis) p.scores_out[(qrow0 + qi) * p.ld + j] = score;
+              }
+            }
+          }
+        }
+        if constexpr (FUSED) {
+          // both tiles of the pair are in: cut buffers that could not take another pair
+          group_sync<kEpiThreads, kEpiBarrier>();
+#pragma unroll 1
+          for (int qi = 0; qi < qn; ++qi) {
+            const int n = cnt_s[qi];
+            if (n <= cap - 2 * kTile) continue;        // uniform: read after the barrier
+            uint64_t* buf = cand_s + qi * cap;
+            const uint64_t tau = kth_largest_key<kEpiThreads, kEpiBarrier>(k, SmemKeys{buf, n}, sel);
+            const int kept = compact_keys_ge<kEpiThreads, kEpiBarrier, kCandPerThread>(buf, n, tau, sel);
+            if (tid == 0) {
+              // exactly k keys >= tau remain; a later key can join the k largest only above tau
+              cnt_s[qi] = kept;
+              thr_s[qi] = tau;
+            }
+            group_sync<kEpiThreads, kEpiBarrier>();
+          }
+        }
+      }
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == kEpiWarps) {
+      tc_fence_after_sync();
+      tmem_dealloc(tmem, kCols);
+    } else if (tid == kEpiThreads + 32 && *abort_flag) {
+      // TMA copies still in flight after an abort land before the CTA leaves
+      for (int s = 0; s < kStages; ++s)
+        if (armed_s[s] >= 0) mbar_wait(bar_full + 8 * s, (armed_s[s] / kStages) & 1, nullptr, nullptr, kWaitPolls);
+    }
+    if constexpr (!FUSED) return;
+    // ---- the run's k largest keys -> workspace, in ascending entry index (the ring is idle now:
+    //      it holds the bitmap of the run's entries and its word prefixes)
+    __syncthreads();
+    const int words = nt * (kTile / 32);
+    uint32_t* run_bits = reinterpret_cast<uint32_t*>(smem + L::kA);
+    int* run_prefix = reinterpret_cast<int*>(smem + L::kA + words * 4);
+#pragma unroll 1
+    for (int qi = 0; qi < qn; ++qi) {
+      const int n = cnt_s[qi];
+      const uint64_t* buf = cand_s + qi * cap;
+      const uint64_t tau = n > k ? kth_largest_key<kThreads, 0>(k, SmemKeys{buf, n}, sel_all) : 0ull;
+      const long long q = qrow0 + qi;
+      uint64_t* dst = p.runs.keys + (q * p.runs.runs + blockIdx.x) * (long long)k;
+      const int w = write_run_sorted<kThreads, 0>(buf, n, tau, t_begin * kTile, words, run_bits, run_prefix, dst,
+                                                   sel_all);
+      if (tid == 0) p.runs.cnt[q * p.runs.runs + blockIdx.x] = w;
     }
   }
+  if constexpr (FUSED) {
+    if (!p.merge_inline) return;
+    // ---- the query group's last CTA to finish merges its runs
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+      const int old = atomicAdd(p.runs.ticket + (long long)b * gridDim.y + blockIdx.y, 1);
+      *last_flag = old == (int)gridDim.x - 1 ? 1 : (old >= (int)gridDim.x ? -1 : 0);
+    }
+    __syncthreads();
+    const int lf = *last_flag;
+    if (lf < 0 && tid == 0) report(p.status, LCS_ERR_DEVICE_GUARD);   // ticket not zero at the start
+    if (lf != 1) return;
+    __threadfence();
+    uint64_t* stage = reinterpret_cast<uint64_t*>(smem + L::kA);   // the ring is idle now
+    int* run_off = reinterpret_cast<int*>(smem + L::kRunOff);
+#pragma unroll 1
+    for (int qi = 0; qi < qn; ++qi)
+      merge_query_topk<kThreads, 0>(p.runs, qrow0 + qi, (n0 + qi + 1) >> mshift, k, stage,
+                                    (L::kSelAll - L::kA) / 8, run_off, p.out_idx, p.out_cnt, sel_all);
+    if (tid == 0) p.runs.ticket[(long long)b * gridDim.y + blockIdx.y] = 0;   // left at zero for the next call
+  }
+}
+
+// One CTA per query: the merge of the query's run lists (the selection phase on its own, or run
+// lists too long for the scorer's shared memory).  grid: (max_new, num_seqs), block 256.
+__global__ void __launch_bounds__(256) topk_merge_kernel(IndexParams p) {
+  extern __shared__ __align__(16) uint8_t merge_smem[];
+  const int b = blockIdx.y, i = blockIdx.x;
+  const SeqSpan sp = seq_span(p.cu_new, p.seq_len, b);
+  if (i >= sp.qn) return;
+  SelScratch<256>& sc = *reinterpret_cast<SelScratch<256>*>(merge_smem);
+  int* run_off = reinterpret_cast<int*>(merge_smem + sizeof(SelScratch<256>));
+  uint64_t* stage = reinterpret_cast<uint64_t*>(merge_smem + sizeof(SelScratch<256>) + (kMaxRuns + 4) * 4);
+  const int t = sp.n0() + i;
+  merge_query_topk<256, 0>(p.runs, sp.q0 + i, (t + 1) / p.m, p.top_k, stage, 2 * p.runs.runs * p.top_k, run_off,
+                           p.out_idx, p.out_cnt, sc);
 }
 
 // ----------------------------------------------------------------------------------------------
@@ -325,74 +627,155 @@ __global__ void __launch_bounds__(kThreads) index_tc_kernel(const __grid_constan
 namespace {
 
 template <int HI, int QH>
-cudaError_t launch_tc_t(const CUtensorMap& tmap, const IndexParams& p, int max_entries, int sms, cudaStream_t st) {
-  using L = TcSmem<QH, QH / HI>;
+size_t tc_smem_bytes(bool fused, int cap, int pages) {
+  return TcSmem<QH, QH / HI>::bytes(fused, cap, pages);
+}
+
+size_t tc_smem_for(int heads, int qh, bool fused, int cap, int pages) {
+  switch (heads * 100 + qh) {
+    case 104: return tc_smem_bytes<1, 4>(fused, cap, pages);
+    case 204: return tc_smem_bytes<2, 4>(fused, cap, pages);
+    case 208: return tc_smem_bytes<2, 8>(fused, cap, pages);
+    case 404: return tc_smem_bytes<4, 4>(fused, cap, pages);
+    case 408: return tc_smem_bytes<4, 8>(fused, cap, pages);
+    case 416: return tc_smem_bytes<4, 16>(fused, cap, pages);
+    case 808: return tc_smem_bytes<8, 8>(fused, cap, pages);
+    case 816: return tc_smem_bytes<8, 16>(fused, cap, pages);
+    default: return 0;
+  }
+}
+
+template <int HI, int QH, bool FUSED>
+cudaError_t launch_tc_t(const CUtensorMap& tmap, const IndexParams& p, const IndexTcPlan& plan, cudaStream_t st) {
   static PerDeviceOnce attr;
   cudaError_t ea = once_per_device(attr, [] {
-    cudaError_t e = cudaFuncSetAttribute(index_tc_kernel<HI, QH>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(index_tc_kernel<HI, QH>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    cudaError_t e = cudaFuncSetAttribute(index_tc_kernel<HI, QH, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         227 * 1024);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(index_tc_kernel<HI, QH, FUSED>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     return e;
   });
   if (ea != cudaSuccess) return ea;
-  // resident CTAs per SM: shared memory (228 KB per SM, 1 KB reserved per CTA) and tensor memory
-  int occ = (228 * 1024) / (L::kBytes + 1024);
-  const int occ_tmem = 512 / (int)tmem_cols_for(L::N);
-  if (occ > occ_tmem) occ = occ_tmem;
-  if (occ < 1) occ = 1;
-  const int tiles = (max_entries + kTile - 1) / kTile;
-  if (tiles == 0) return cudaSuccess;
-  int runs = (sms * occ) / p.num_seqs;             // one wave of CTAs
-  if (runs < 1) runs = 1;
-  int tpc = (tiles + runs - 1) / runs;
-  const int tpc_cap = kMaxPages * p.paging.epb / kTile;   // a run spans at most kMaxPages pages
-  if (tpc > tpc_cap) tpc = tpc_cap;
-  dim3 grid((tiles + tpc - 1) / tpc, p.num_seqs);
-  index_tc_kernel<HI, QH><<<grid, kThreads, L::kBytes, st>>>(tmap, p, tpc);
+  dim3 grid(plan.runs, plan.groups, p.num_seqs);
+  index_tc_kernel<HI, QH, FUSED><<<grid, kThreads, plan.smem, st>>>(tmap, p, plan.tpc);
   return cudaGetLastError();
+}
+
+template <bool FUSED>
+cudaError_t launch_tc_switch(int heads, int qh, const CUtensorMap& tmap, const IndexParams& p, const IndexTcPlan& plan,
+                             cudaStream_t st) {
+  switch (heads * 100 + qh) {
+    case 104: return launch_tc_t<1, 4, FUSED>(tmap, p, plan, st);
+    case 204: return launch_tc_t<2, 4, FUSED>(tmap, p, plan, st);
+    case 208: return launch_tc_t<2, 8, FUSED>(tmap, p, plan, st);
+    case 404: return launch_tc_t<4, 4, FUSED>(tmap, p, plan, st);
+    case 408: return launch_tc_t<4, 8, FUSED>(tmap, p, plan, st);
+    case 416: return launch_tc_t<4, 16, FUSED>(tmap, p, plan, st);
+    case 808: return launch_tc_t<8, 8, FUSED>(tmap, p, plan, st);
+    case 816: return launch_tc_t<8, 16, FUSED>(tmap, p, plan, st);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace
 
-// Columns (query-heads) per 32-code block the tensor-core scorer needs, or 0 when it does not
-// apply (rank other than 128, pages outside 8..128 entries, more than 4 queries per sequence,
-// key codes not 32-byte or scales not 16-byte aligned).
-int index_tc_qh(const IndexParams& p, int rank, int max_new) {
+// Columns (query-heads) per 32-code block the tensor-core scorer uses, or 0 when it does not
+// apply (rank other than 128, pages outside 8..128 entries, key codes not 32-byte or scales not
+// 16-byte aligned).  Up to 4 queries per sequence: all of them in one CTA; longer query runs (k >
+// 0, the fused top-k of a prefill chunk): groups of min(4, 16 / heads) queries.
+int index_tc_qh(const IndexParams& p, int rank, int max_new, bool groups) {
   if (rank != 128 || p.paging.epb < 8 || p.paging.epb > 128 || (p.paging.epb & (p.paging.epb - 1))) return 0;
   if ((reinterpret_cast<uintptr_t>(p.k_fp4) & 31u) || (reinterpret_cast<uintptr_t>(p.k_scale) & 15u)) return 0;
   if (p.k_rows < p.paging.epb || p.k_rows > (1ll << 31)) return 0;
-  if (max_new < 1 || max_new > 4) return 0;
+  if (p.heads != 1 && p.heads != 2 && p.heads != 4 && p.heads != 8) return 0;
+  if (max_new < 1) return 0;
+  if (max_new > 4) return groups ? std::min(4, 16 / p.heads) * p.heads : 0;
   const int need = max_new * p.heads;
   const int qh = need <= 4 ? 4 : (need <= 8 ? 8 : (need <= 16 ? 16 : 0));
   if (qh == 0 || qh / p.heads < max_new) return 0;
   return qh;
 }
 
-cudaError_t launch_index_tc(const IndexParams& p, int rank, int max_new, int max_entries, int sms, cudaStream_t st) {
-  const int qh = index_tc_qh(p, rank, max_new);
-  if (qh == 0) return cudaErrorInvalidValue;
+// The scorer's grid and shared memory; with k > 0 the fused top-k (applies = 0 when the
+// candidate buffers or the merge bitmap do not fit).
+IndexTcPlan plan_index_tc(const IndexParams& p, int rank, int max_new, int max_entries, int num_seqs, int sms, int k) {
+  IndexTcPlan plan{};
+  const bool fused = k > 0;
+  plan.qh = index_tc_qh(p, rank, max_new, fused);
+  if (plan.qh == 0) return plan;
+  const int qps = plan.qh / p.heads;
+  plan.groups = (max_new + qps - 1) / qps;
+  if (plan.groups > 65535) return plan;
+  const int tiles = std::max(1, (max_entries + kTile - 1) / kTile);
+  const int epb = p.paging.epb;
+  int tpc_cap = kMaxPages * epb / kTile;                       // a run spans at most kMaxPages pages
+  tpc_cap = std::max(tpc_cap, (tiles + kMaxRuns - 1) / kMaxRuns);   // and a sequence at most kMaxRuns runs
+  if (tpc_cap * kTile / epb > 4 * kMaxPages) return plan;
+  // resident CTAs per SM: tensor memory and registers (16 query-head columns take 168 registers a
+  // thread: one CTA), then shared memory below
+  const int occ_tmem = std::min(512 / (int)tmem_cols_for(4 * plan.qh), plan.qh >= 16 ? 1 : 2);
+  const int cap_min = fused ? 2 * k + 2 * kTile : 0;           // a compaction frees k slots or more
+  if (fused && cap_min > kEpiThreads * kCandPerThread) return plan;
+  // two resident CTAs per SM when their shared memory allows it, else one
+  for (int occ = std::min(2, occ_tmem); occ >= 1; --occ) {
+    int runs = std::max(1, (sms * occ) / std::max(1, num_seqs * plan.groups));   // about one wave
+    int tpc = std::min(tpc_cap, (tiles + runs - 1) / runs);
+    runs = (tiles + tpc - 1) / tpc;
+    const int pages = tpc * kTile / epb + 1;
+    const long long budget = (long long)(228 * 1024 / occ) - 1024;
+    const long long base = (long long)tc_smem_for(p.heads, plan.qh, fused, 0, pages);
+    if (base + 8ll * qps * cap_min > std::min<long long>(budget, 227 * 1024)) continue;
+    int cap = cap_min;
+    if (fused) {   // more candidate room while it fits: fewer compactions
+      const int fit = (int)((std::min<long long>(budget, 227 * 1024) - base) / (8ll * qps)) / (2 * kTile) * (2 * kTile);
+      cap = std::max(cap_min, std::min({fit, 4 * k + 2 * kTile, kEpiThreads * kCandPerThread}));
+    }
+    plan.runs = runs;
+    plan.tpc = tpc;
+    plan.cap = cap;
+    plan.smem = tc_smem_for(p.heads, plan.qh, fused, cap, pages);
+    plan.applies = 1;
+    break;
+  }
+  if (!plan.applies) return plan;
+  // the last CTA merges in place when the runs' lists fit its idle ring; a run's bitmap and word
+  // prefixes fit it in any case (tpc * 128 entries: at most 8 bits of ring per entry)
+  const size_t stage_bytes = (size_t)(TcSmem<16, 4>::kSelAll - TcSmem<16, 4>::kA);   // the same for every variant
+  plan.merge_inline = fused && (size_t)plan.runs * k * 8 <= stage_bytes;
+  plan.merge_smem = sizeof(SelScratch<256>) + (size_t)(kMaxRuns + 4) * 4 + (size_t)plan.runs * k * 16;
+  if (fused && (size_t)plan.tpc * kTile / 32 * 8 > stage_bytes) plan.applies = 0;
+  if (fused && !plan.merge_inline && plan.merge_smem > 227 * 1024) plan.applies = 0;
+  return plan;
+}
+
+cudaError_t launch_index_tc(const IndexParams& p, const IndexTcPlan& plan, cudaStream_t st) {
+  if (!plan.applies) return cudaErrorInvalidValue;
   auto enc = tensor_map_encoder();
   if (enc == nullptr) return cudaErrorNotSupported;
   // codes as [rows][128] 4-bit values; a box of one page is unpacked to 16 codes per 16 bytes
   CUtensorMap tmap;
-  const cuuint64_t gdim[2] = {(cuuint64_t)rank, (cuuint64_t)p.k_rows};
-  const cuuint64_t gstride[1] = {(cuuint64_t)(rank / 2)};
+  const cuuint64_t gdim[2] = {128u, (cuuint64_t)p.k_rows};
+  const cuuint64_t gstride[1] = {64u};
   const cuuint32_t box[2] = {128u, (cuuint32_t)p.paging.epb};
   const cuuint32_t estr[2] = {1u, 1u};
   CUresult r = enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<uint8_t*>(p.k_fp4), gdim, gstride, box,
                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-  switch (p.heads * 100 + qh) {
-    case 104: return launch_tc_t<1, 4>(tmap, p, max_entries, sms, st);
-    case 204: return launch_tc_t<2, 4>(tmap, p, max_entries, sms, st);
-    case 208: return launch_tc_t<2, 8>(tmap, p, max_entries, sms, st);
-    case 404: return launch_tc_t<4, 4>(tmap, p, max_entries, sms, st);
-    case 408: return launch_tc_t<4, 8>(tmap, p, max_entries, sms, st);
-    case 416: return launch_tc_t<4, 16>(tmap, p, max_entries, sms, st);
-    case 808: return launch_tc_t<8, 8>(tmap, p, max_entries, sms, st);
-    case 816: return launch_tc_t<8, 16>(tmap, p, max_entries, sms, st);
-    default: return cudaErrorInvalidValue;
-  }
+  if (p.scores_out != nullptr) return launch_tc_switch<false>(p.heads, plan.qh, tmap, p, plan, st);
+  return launch_tc_switch<true>(p.heads, plan.qh, tmap, p, plan, st);
+}
+
+cudaError_t launch_topk_merge(const IndexParams& p, const IndexTcPlan& plan, int max_new, cudaStream_t st) {
+  static PerDeviceOnce attr;
+  cudaError_t ea = once_per_device(attr, [] {
+    return cudaFuncSetAttribute(topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  });
+  if (ea != cudaSuccess) return ea;
+  dim3 grid(max_new, p.num_seqs);
+  if (grid.x == 0) return cudaSuccess;
+  topk_merge_kernel<<<grid, 256, plan.merge_smem, st>>>(p);
+  return cudaGetLastError();
 }
 
 }  // namespace lcsa

@@ -42,12 +42,24 @@ struct CompressParams {
   const __nv_bfloat16* pending;
   __nv_bfloat16* pending_out;
   int pending_slots;
+  const __nv_bfloat16* scores;         // per-channel weights: score rows of the new tokens, else null
+  __nv_bfloat16* pending_scores;       // and of the pending tokens (same ring as pending)
   Rows entries;
   Paging paging;
   Rows new_rows;   // nope == nullptr: write the window ring instead
   Rows window;
   int state_tail;  // > 0: without new_rows, only the last state_tail new tokens reach the state
   int32_t* status;
+};
+
+// Per-run top-k lists of the fused decode indexer (workspace): run r of query q keeps up to k
+// keys (score key << 32 | ~j) at keys[(q*runs + r)*k ..] and their count at cnt[q*runs + r];
+// ticket[b] counts the sequence's finished runs (zero between calls).
+struct TopkRuns {
+  int runs;
+  int* cnt;
+  uint64_t* keys;
+  int* ticket;
 };
 
 struct IndexParams {
@@ -68,6 +80,14 @@ struct IndexParams {
   float* scores_out;        // [T][ld] fp32 scores
   uint32_t* hist;           // [T][2048] histogram of key >> 21 (with keys_out), zeroed by the caller
   long long ld;
+  // fused top-k (tensor-core decode scorer)
+  int top_k;
+  int cand_cap;             // candidate buffer per query (2k + 256)
+  int merge_inline;         // 1: the sequence's last CTA merges the run lists
+  TopkRuns runs;
+  int32_t* out_idx;         // [T][k]
+  int32_t* out_cnt;         // [T]
+  uint32_t wait_polls;      // bound of every mbarrier wait (polls of up to ~1 us)
   int32_t* status;
 };
 
@@ -97,6 +117,8 @@ struct AttendParams {
   int entry_splits;          // tensor-core kernel: splits over the entries; split entry_splits = window
   int part;                  // tensor-core kernel: 0 every split, 1 the window split only, 2 the entry splits
   int window_split;          // tensor-core kernel: 1 the window rows form split entry_splits (CSA)
+  int hg;                    // tensor-core kernel: query heads per CTA (16 or 64)
+  uint32_t wait_polls;       // bound of every mbarrier wait (polls of up to ~1 us)
   int32_t* status;
 };
 
@@ -109,8 +131,21 @@ cudaError_t launch_topk_select(const uint32_t* keys, const uint32_t* hist, long 
                                const int32_t* seq_len, int num_seqs, int max_new, int m, int k, int32_t* out_idx,
                                int32_t* out_cnt, cudaStream_t st);
 // tcgen05 scorer for a few queries per sequence: query-head columns it would use (0 = not applicable)
-int index_tc_qh(const IndexParams& p, int rank, int max_new);
-cudaError_t launch_index_tc(const IndexParams& p, int rank, int max_new, int max_entries, int sms, cudaStream_t st);
+struct IndexTcPlan {
+  int applies;        // 0: the scorer (with k > 0: the fused top-k) does not take this batch
+  int qh;             // query-head columns per 32-code block
+  int groups;         // query groups per sequence (qh / heads queries each)
+  int runs;           // CTAs per query group
+  int tpc;            // 128-entry tiles per CTA
+  int cap;            // candidate buffer per query (fused)
+  int merge_inline;   // the sequence's last CTA merges (else the merge kernel)
+  size_t smem;        // dynamic shared memory of the scorer
+  size_t merge_smem;  // dynamic shared memory of the merge kernel
+};
+// k > 0: plan of the fused top-k; k = 0: of the scores (csa_index_scores)
+IndexTcPlan plan_index_tc(const IndexParams& p, int rank, int max_new, int max_entries, int num_seqs, int sms, int k);
+cudaError_t launch_index_tc(const IndexParams& p, const IndexTcPlan& plan, cudaStream_t st);
+cudaError_t launch_topk_merge(const IndexParams& p, const IndexTcPlan& plan, int max_new, cudaStream_t st);
 // tcgen05 scorer for long runs of queries per sequence (prefill chunks)
 bool index_tc_pf_applies(const IndexParams& p, int rank, int max_new);
 cudaError_t launch_index_tc_pf(const IndexParams& p, int rank, int max_new, int max_entries, cudaStream_t st);

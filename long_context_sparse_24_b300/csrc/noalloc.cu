@@ -14,10 +14,14 @@
 // current, and then cached.  The first call on a device does that lookup; make that first
 // call before any stream capture starts.
 //
-// All calls share the one array, which keeps whatever the previous call left in it.  The
-// indexer path writes every scratch value before it reads it, so no clearing is needed.  Two
-// calls whose kernels overlap on the GPU (different streams, or different host threads on the
-// same device without ordering) race on the array and give wrong results: order them.
+// All calls share the one array, which keeps whatever the previous call left in it.  Its leading
+// per-sequence counters must be zero when a call starts: the array is zero when the library's
+// module is loaded, and every call that completes leaves them at zero again (on the path that
+// writes every score instead, the histograms are cleared by a memset of this array, which is not
+// an allocation).  A call with LCS_INDEX_SELECT_ONLY reads what the last LCS_INDEX_SCORE_ONLY call
+// left in the array.  Two calls whose kernels overlap on the GPU (different streams, or different
+// host threads on the same device without ordering) race on the array and give wrong results:
+// order them.
 #include <mutex>
 
 #include "kernels.cuh"
@@ -52,9 +56,10 @@ extern "C" lcs_status csa_index_topk_noalloc(const lcs_batch* batch, const uint8
                                              const lcs_paging* paging, int32_t m, int32_t k, int32_t flags,
                                              int32_t* out_idx, int32_t* out_cnt, int32_t* dev_status,
                                              void* stream) {
-  if (batch == nullptr) return LCS_ERR_INVALID_ARG;
-  if (m <= 0) return LCS_ERR_UNSUPPORTED;
-  if (lcs_index_topk_workspace(batch, m, k) > (size_t)LCSA_NOALLOC_SCRATCH_BYTES) return LCS_ERR_WORKSPACE;
+  if (batch == nullptr || keys == nullptr || paging == nullptr) return LCS_ERR_INVALID_ARG;
+  if (m <= 0 || k < 1) return LCS_ERR_UNSUPPORTED;
+  if (lcs_index_topk_workspace(batch, heads, keys, paging, m, k) > (size_t)LCSA_NOALLOC_SCRATCH_BYTES)
+    return LCS_ERR_WORKSPACE;
   void* scratch = nullptr;
   lcs_status s = scratch_on_current_device(&scratch);
   if (s != LCS_OK) return s;

@@ -50,13 +50,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-constexpr uint32_t kWaitPolls = 1u << 20;  // polls of up to ~1 us each: about a second in all
+constexpr uint32_t kWaitPolls = LCSA_DEFAULT_WAIT_POLLS;  // polls of up to ~1 us each: about a second
 
-// Waits for phase `parity` of the barrier; false (and LCS_ERR_TIMEOUT recorded) after the bound
-// or as soon as *abort becomes non-zero.
+// Waits for phase `parity` of the barrier; false (and LCS_ERR_TIMEOUT recorded) after `polls`
+// polls (0: at once, without looking) or as soon as *abort becomes non-zero.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t* status,
-                                          volatile int* abort = nullptr) {
-  for (uint32_t i = 0; i < kWaitPolls; ++i) {
+                                          volatile int* abort = nullptr, uint32_t polls = kWaitPolls) {
+  for (uint32_t i = 0; i < polls; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if (abort != nullptr && *abort) return false;
   }

@@ -2,8 +2,8 @@
 
 Owns the caller-side buffers (entry cache, indexer keys, state cache, workspaces) and issues the
 library calls of one step in order:
-  CSA: csa_compress || csa_index_topk (scoring), then csa_attend_window || csa_index_topk
-       (selection), then csa_attend_topk [-> lcs_window_commit]
+  CSA: (csa_compress -> csa_attend_window) || csa_index_topk, then csa_attend_topk
+       [-> lcs_window_commit]
   HCA: hca_compress -> hca_attend [-> lcs_window_commit]
 (lcs_window_commit only for multi-token steps; single-token steps keep the window in the ring.)
 No arithmetic of the method happens here.
@@ -15,9 +15,9 @@ from typing import Optional, Sequence
 
 import torch
 
-from . import (LCS_INDEX_RELU, LCS_INDEX_SCORE_ONLY, LCS_INDEX_SELECT_ONLY, WINDOW, Batch, Compressor, csa_attend, csa_attend_topk, csa_attend_window,
-               csa_compress, csa_index_topk, hca_attend,
-               hca_compress, lcs_attend_workspace, lcs_index_topk_workspace, lcs_window_commit)
+from . import (LCS_INDEX_RELU, WINDOW, Batch, Compressor, csa_attend, csa_attend_topk, csa_attend_window, csa_compress,
+               csa_index_topk, hca_attend, hca_compress, lcs_attend_workspace, lcs_index_topk_workspace,
+               lcs_window_commit)
 from . import buffers
 
 
@@ -43,22 +43,24 @@ class Layer:
                                          0 if self.ring_only else num_seqs * max_new,
                                          device, index_rank=index_rank if kind == "csa" else 0,
                                          block_order=block_order)
-        # compression does not feed the indexer: it runs on a side stream next to it, and so does
-        # the window part of attention once the indexer's scoring phase has left the SMs
+        # compression and the window part of attention do not feed the indexer: they run on a side
+        # stream next to it
         self.side = torch.cuda.Stream(device=device) if kind == "csa" else None
-        self.scored = torch.cuda.Event() if kind == "csa" else None
         self.comp: Optional[Compressor] = None
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
         # workspaces sized for the largest step this layer will run
         T = num_seqs * max_new
         probe = Batch(0, 0, num_seqs, T, max_new, capacity)
-        self.topk_ws_bytes = lcs_index_topk_workspace(probe, self.m, top_k) if kind == "csa" else 0
+        self.topk_ws_bytes = (lcs_index_topk_workspace(probe, index_heads, self.cache.keys, self.cache.paging, self.m,
+                                                       top_k) if kind == "csa" else 0)
         rows = (top_k + WINDOW) if kind == "csa" else (capacity // self.m + WINDOW)
         self.attend_rows = rows
         # the split plan (and so the workspace) depends on the step's token count: take the largest
         self.attend_ws_bytes = max(lcs_attend_workspace(Batch(0, 0, num_seqs, n, max_new, capacity), heads, dim, rows)
                                    for n in sorted({*range(1, min(T, 160) + 1), T}))
-        self.topk_ws = torch.empty(max(self.topk_ws_bytes, 256), dtype=torch.uint8, device=device)
+        # the index workspace starts with counters that must be zero before the first call (every
+        # call leaves them zero)
+        self.topk_ws = torch.zeros(max(self.topk_ws_bytes, 256), dtype=torch.uint8, device=device)
         self.attend_ws = torch.empty(max(self.attend_ws_bytes, 256), dtype=torch.uint8, device=device)
         self.topk_idx = torch.empty((T, max(top_k, 1)), dtype=torch.int32, device=device)
         self.topk_cnt = torch.empty((T,), dtype=torch.int32, device=device)
@@ -78,7 +80,8 @@ class Layer:
 
     def fill(self, batch: Batch, raw: torch.Tensor, stream=None) -> None:
         """Compress a chunk whose tokens are not attended in this call (cache building)."""
-        st = buffers.State(self.cache.state.window, self.cache.state.pending, self.cache.state.pending_slots, None)
+        st = buffers.State(self.cache.state.window, self.cache.state.pending, self.cache.state.pending_slots, None,
+                           self.cache.state.pending_scores)
         fn = csa_compress if self.kind == "csa" else hca_compress
         fn(batch, raw, self.comp, st, self.cache.entries, self.cache.paging, self.status, stream)
 
@@ -105,25 +108,21 @@ class Layer:
     def step(self, batch: Batch, raw_new: torch.Tensor, q: torch.Tensor, out: torch.Tensor,
              lse: Optional[torch.Tensor] = None, idx_q_fp4=None, idx_q_scale=None, head_w=None, stream=None,
              q_ready: Optional[torch.cuda.Event] = None) -> None:
-        """One pass of the hot path for the batch's new tokens.  CSA: compression (side stream)
-        runs next to the indexer's scoring phase; the window part of attention (side stream) next
-        to its selection phase, which occupies one CTA per query and leaves the other SMs free;
-        the top-k part of attention, with the merge, waits for both.  q_ready: an event the
-        attention waits for before reading q (q still arriving, e.g. copied from the host on
-        another stream), so that compression and the indexer need not wait for it."""
+        """One pass of the hot path for the batch's new tokens.  CSA: compression, then the window
+        part of attention (side stream) run next to the indexer (scoring with the top-k fused in);
+        the top-k part of attention, with the merge of the two parts, waits for both.  q_ready:
+        an event the attention waits for before reading q (q still arriving, e.g. copied from the
+        host on another stream), so that compression and the indexer need not wait for it."""
         main = stream if stream is not None else torch.cuda.current_stream()
         if self.kind == "csa":
             self.side.wait_stream(main)
             self.compress(batch, raw_new, self.side)
-            self.select(batch, idx_q_fp4, idx_q_scale, head_w, main, LCS_INDEX_SCORE_ONLY)
-            self.scored.record(main)
-            self.side.wait_event(self.scored)
             if q_ready is not None:
                 self.side.wait_event(q_ready)
             csa_attend_window(batch, q, self.heads, self.top_k, self.m, self.cache.entries, self.cache.paging,
                               self.cache.state, self.scale, self.attend_ws, self.attend_ws_bytes, self.status,
                               self.side)
-            self.select(batch, idx_q_fp4, idx_q_scale, head_w, main, LCS_INDEX_SELECT_ONLY)
+            self.select(batch, idx_q_fp4, idx_q_scale, head_w, main)
             main.wait_stream(self.side)
             csa_attend_topk(batch, q, self.heads, self.topk_idx, self.topk_cnt, self.top_k, self.m, self.cache.entries,
                             self.cache.paging, self.cache.state, self.scale, out, lse, self.attend_ws,

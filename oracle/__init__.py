@@ -253,6 +253,40 @@ def compress(raw: np.ndarray, w: np.ndarray, bias: np.ndarray, m: int, overlap: 
     return (out, weights) if return_weights else out
 
 
+def compress_per_channel(raw: np.ndarray, scores: np.ndarray, bias: np.ndarray, m: int, overlap: bool,
+                         first: int = 0, count: int | None = None, return_weights: bool = False):
+    """Entries ``first .. first+count-1`` with per-channel weights (the variant reading).
+
+    chenxutan section 4.2 sketches the compressor with a score vector per raw token (one score per
+    channel, from its own projection), a softmax over the window's tokens taken channel by
+    channel, and a channel-by-channel weighted sum; x-techcon section 2 adds a positional bias,
+    here one per window offset and channel.  For entry j with window rows t in [lo, hi) clipped at
+    0: z[t, d] = scores[t, d] + bias[t - lo, d]; alpha[:, d] = softmax over the existing rows of
+    z[:, d]; c[d] = sum_t alpha[t, d] raw[t, d].  ``scores`` [n, D] are the already projected score
+    rows; ``bias`` is [2m, D] (overlapping windows) or [m, D].
+    """
+    raw = np.asarray(raw, dtype=np.float64)
+    scores = np.asarray(scores, dtype=np.float64)
+    n = raw.shape[0]
+    total = num_entries(n, m)
+    if count is None:
+        count = total - first
+    assert 0 <= first and first + count <= total and scores.shape == raw.shape
+    assert bias.shape == ((2 * m if overlap else m), raw.shape[1])
+    out = np.empty((count, raw.shape[1]), dtype=np.float64)
+    weights = []
+    for i, j in enumerate(range(first, first + count)):
+        lo, hi = entry_span(j, m, overlap)
+        t = np.arange(max(lo, 0), hi)
+        z = scores[t] + bias[t - lo]                       # [rows, D]
+        a = np.exp(z - z.max(axis=0, keepdims=True))
+        a = a / a.sum(axis=0, keepdims=True)               # softmax over the rows, per channel
+        out[i] = (a * raw[t]).sum(axis=0)
+        if return_weights:
+            weights.append(a)
+    return (out, weights) if return_weights else out
+
+
 def compress_blocked(raw: np.ndarray, w: np.ndarray, bias: np.ndarray, m: int, overlap: bool,
                      first: int = 0, count: int | None = None) -> np.ndarray:
     """The same entries as ``compress``, evaluated a block of m rows at a time (for long

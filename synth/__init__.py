@@ -40,7 +40,7 @@ INV_SQRT128_BITS = 0x3DB504F3             # fp32(1/sqrt(128))
 E2M1_DRAW_CODES = np.array([0, 1, 2, 3, 4, 5, 6, 7, 9, 10, 11, 12, 13, 14, 15], dtype=np.uint8)
 
 # tensor kinds (the high byte of a tensor id)
-RAW, QUERY, IDX_Q, IDX_QS, IDX_K, IDX_KS, HEAD_W, COMP_W, COMP_B, LENGTHS = range(1, 11)
+RAW, QUERY, IDX_Q, IDX_QS, IDX_K, IDX_KS, HEAD_W, COMP_W, COMP_B, LENGTHS, COMP_SCORES = range(1, 12)
 
 
 def tensor_id(kind: int, layer: int = 0, seq: int = 0) -> int:

@@ -147,7 +147,8 @@ def bf16_tensor_to_f64(t: torch.Tensor) -> np.ndarray:
 
 
 def workspace(nbytes: int) -> torch.Tensor:
-    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=DEV)
+    # zeros: the index workspace's leading counters must start at zero
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=DEV)
 
 
 def dev_status() -> torch.Tensor:

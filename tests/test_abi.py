@@ -12,7 +12,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 def header_functions():
     text = open(os.path.join(ROOT, "include", "lcsa.h")).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:lcs_status|size_t|int32_t|const char\*)\s+(\w+)\s*\(", text, flags=re.M)))
+    return sorted(set(re.findall(r"^\s*(?:lcs_status|size_t|int32_t|uint32_t|const char\*)\s+(\w+)\s*\(", text, flags=re.M)))
 
 
 def test_header_declares_the_five_operations():
@@ -31,7 +31,7 @@ def test_library_exports_every_declared_symbol():
 
 def test_abi_version_and_status_strings():
     import long_context_sparse_24_b300 as lcsa
-    assert lcsa.lcs_abi_version() == 1
+    assert lcsa.lcs_abi_version() == 2
     assert lcsa.lcs_status_string(0) == "ok"
     assert "workspace" in lcsa.lcs_status_string(8)
 
@@ -115,6 +115,20 @@ def test_attention_sink_host_validation():
 
 def test_workspace_sizes():
     import long_context_sparse_24_b300 as lcsa
+    keys = lcsa.lcs_index_keys(0x10000, 0x20000, 128, 32 * 32768)
+    pg = lcsa.lcs_paging(32, 1024, 0x3000)
+    # decode (one query per sequence, rank 128): the top-k runs inside the scorer and the workspace
+    # holds per-run lists of k keys, far less than a key per (query, entry)
     b = lcsa.lcs_batch(32, 0x1000, 0x2000, 32, 1, 131072)
-    n = lcsa._lib.lcs_index_topk_workspace(ctypes.byref(b), 4, 512)
-    assert n >= 32 * (131072 // 4) * 4
+    n = lcsa._lib.lcs_index_topk_workspace(ctypes.byref(b), 4, ctypes.byref(keys), ctypes.byref(pg), 4, 512)
+    assert 32 * 512 * 8 <= n < 32 * (131072 // 4) * 4
+    assert lcsa._lib.lcs_index_topk_workspace_zeroed(ctypes.byref(b)) == 256
+    # a prefill chunk at rank 128: query groups, still lists of k keys per query and run
+    b = lcsa.lcs_batch(1, 0x1000, 0x2000, 2048, 2048, 131072)
+    n = lcsa._lib.lcs_index_topk_workspace(ctypes.byref(b), 4, ctypes.byref(keys), ctypes.byref(pg), 4, 512)
+    assert 2048 * 512 * 8 <= n < 2048 * (131072 // 4) * 4
+    assert lcsa._lib.lcs_index_topk_workspace_zeroed(ctypes.byref(b)) == 2048 * 4
+    # rank 64: every score key of every (query, visible entry) pair
+    keys64 = lcsa.lcs_index_keys(0x10000, 0x20000, 64, 32 * 32768)
+    n = lcsa._lib.lcs_index_topk_workspace(ctypes.byref(b), 4, ctypes.byref(keys64), ctypes.byref(pg), 4, 512)
+    assert n >= 2048 * (131072 // 4) * 4

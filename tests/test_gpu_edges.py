@@ -24,7 +24,7 @@ def _topk(batch, cache, q_fp4, q_sc, hw, heads, m, k, st=None):
     T = batch.total_new
     out_idx = torch.full((T, k), -7, dtype=torch.int32, device=DEV)
     out_cnt = torch.full((T,), -7, dtype=torch.int32, device=DEV)
-    wsb = lcsa.lcs_index_topk_workspace(batch, m, k)
+    wsb = lcsa.lcs_index_topk_workspace(batch, heads, cache.keys, cache.paging, m, k)
     lcsa.csa_index_topk(batch, q_fp4, q_sc, hw, heads, cache.keys, cache.paging, m, k, 0, out_idx, out_cnt,
                         workspace(wsb), wsb, st)
     torch.cuda.synchronize()
@@ -101,3 +101,49 @@ def test_unmapped_page_reports_guard_indexer():
 ])
 def test_unmapped_page_reports_guard_attention(kind, lengths, new, m, k):
     _attend_case(kind, lengths, new, 64, 512, "fp8_split", m, k, corrupt_seq=1)
+
+
+def _nope_tiny_rows(b, rows):
+    """Every 9th entry row of sequence 0: RoPE dims +-2 and FP8 dims with amax = 2/400, so that
+    |rope| / s_r = 448 * 400 exceeds the f16 range of the kernels' widened rows."""
+    if b == 0:
+        rows = rows.copy()
+        sel = rows[::9]
+        sel[:, :64] = np.where(sel[:, :64] < 0, -2.0, 2.0)
+        sel[:, 64:] *= (2.0 / 400.0) / np.abs(sel[:, 64:]).max(axis=1, keepdims=True)
+        rows[::9] = sel
+    return rows
+
+
+def test_rope_beyond_f16_range_reports_guard():
+    """Rows whose RoPE dims exceed 65504 times the row's FP8 scale cannot be widened to f16: the
+    call reports LCS_ERR_DEVICE_GUARD; the sequences without such rows still match the oracle."""
+    _attend_case("csa", [2000, 4100, 300], [1, 1, 1], 64, 512, "fp8_split", 4, 512,
+                 rows_hook=_nope_tiny_rows, skip_seq=0, expect_status=6)
+
+
+def test_bounded_waits_report_timeout_then_recover():
+    """With the wait bound at 0 every pipeline wait of the tensor-core kernels gives up at once: the
+    calls complete, the device status reads LCS_ERR_TIMEOUT and the context stays usable -- the
+    same calls under the default bound then give the oracle's results."""
+    m, k, heads, rank = 4, 64, 4, 128
+    lengths, new = [3000, 5000], [1, 1]
+    cache, batch, kcs, kss, qcs, qss, hws, q_fp4, q_sc, hw = _index_case(lengths, new, m, k, heads, rank, False,
+                                                                       True)
+    prev = lcsa.lcs_set_wait_polls(0)
+    try:
+        st = dev_status()
+        _topk(batch, cache, q_fp4, q_sc, hw, heads, m, k, st)
+        assert int(st.item()) == 7, f"indexer: device status {int(st.item())}, expected LCS_ERR_TIMEOUT"
+        for kind, lens, mm, kk in (("csa", [2000, 4100, 300], 4, 512), ("hca", [20000, 1500], 128, 0)):
+            _attend_case(kind, lens, [1] * len(lens), 64, 512, "fp8_split", mm, kk, expect_status=7)
+    finally:
+        assert lcsa.lcs_set_wait_polls(prev) == 0
+    st = dev_status()
+    oi, oc = _topk(batch, cache, q_fp4, q_sc, hw, heads, m, k, st)
+    assert_status_ok(st)
+    for b, L in enumerate(lengths):
+        ref = oracle.index_scores(qcs[b], qss[b], hws[b], kcs[b], kss[b])
+        sel = oracle.topk_select(ref[0, :oracle.visible_entries(L - 1, m)], k)
+        assert oc[b] == len(sel) and np.array_equal(oi[b, :len(sel)], sel), f"seq {b}"
+    _attend_case("csa", [2000, 4100, 300], [1, 1, 1], 64, 512, "fp8_split", 4, 512)

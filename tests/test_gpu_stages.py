@@ -41,8 +41,19 @@ def test_gpu_generator_matches_numpy():
 
 # ---------------------------------------------------------------------------------------- compression
 
-def _compress_run(lengths, chunk_plan, m, overlap, dim, fmt, seed=21, block_order_seed=None):
-    """Compress len(lengths) sequences fed in calls: chunk_plan[c][b] new tokens of seq b in call c."""
+def _score_rows_np(seed, seq, n, dim):
+    """Per-channel score rows of a sequence's raw tokens (bf16 bit patterns [n, dim], N(0,1))."""
+    return synth.normal_bf16(seed, synth.tensor_id(synth.COMP_SCORES, 0, seq), 0, n * dim, None).reshape(n, dim)
+
+
+def _per_channel_bias(seed, dim, m, overlap):
+    nb = 2 * m if overlap else m
+    return bits_to_f64(synth.normal_bf16(seed, synth.tensor_id(synth.COMP_B, 1), 0, nb * dim)).reshape(nb, dim) * 0.5
+
+
+def _compress_run(lengths, chunk_plan, m, overlap, dim, fmt, seed=21, block_order_seed=None, per_channel=False):
+    """Compress len(lengths) sequences fed in calls: chunk_plan[c][b] new tokens of seq b in call c.
+    per_channel: score rows per token (a per-channel compressor) instead of the scalar weights."""
     S = len(lengths)
     fmtc = buffers.row_format_code(fmt)
     cap = max(lengths) + 256
@@ -51,10 +62,14 @@ def _compress_run(lengths, chunk_plan, m, overlap, dim, fmt, seed=21, block_orde
     if block_order_seed is not None:
         order = np.random.default_rng(block_order_seed).permutation(S * bps).tolist()
     new_cap = max(sum(c) for c in chunk_plan)
-    cache = buffers.alloc_layer(S, cap, dim, fmtc, m, overlap, new_cap, DEV, block_order=order)
+    cache = buffers.alloc_layer(S, cap, dim, fmtc, m, overlap, new_cap, DEV, block_order=order,
+                                per_channel=per_channel)
     w, bias = compressor_params(seed, 0, dim, m, overlap)
+    if per_channel:
+        bias = _per_channel_bias(seed, dim, m, overlap)
     comp = lcsa.Compressor(to_dev_f32(w), to_dev_f32(bias), m, overlap)
     raws = [raw_rows_gpu(seed, 0, b, lengths[b], dim) for b in range(S)]
+    scs = [to_dev_bf16_bits(_score_rows_np(seed, b, lengths[b], dim)) for b in range(S)] if per_channel else None
     st = dev_status()
     pos = [0] * S
     for call in chunk_plan:
@@ -62,8 +77,13 @@ def _compress_run(lengths, chunk_plan, m, overlap, dim, fmt, seed=21, block_orde
         batch = buffers.make_batch(after, call, DEV, max_seq_len=cap)
         parts = [raws[b][pos[b]:after[b]] for b in range(S)]
         raw = torch.cat(parts).contiguous() if batch.total_new else torch.empty((1, dim), dtype=torch.bfloat16, device=DEV)
-        fn = lcsa.csa_compress if overlap or m < 128 else lcsa.hca_compress
-        fn(batch, raw, comp, cache.state, cache.entries, cache.paging, st)
+        if per_channel:
+            sc = (torch.cat([scs[b][pos[b]:after[b]] for b in range(S)]).contiguous() if batch.total_new
+                  else torch.empty((1, dim), dtype=torch.bfloat16, device=DEV))
+            lcsa.csa_compress(batch, raw, comp, cache.state, cache.entries, cache.paging, st, scores=sc)
+        else:
+            fn = lcsa.csa_compress if overlap or m < 128 else lcsa.hca_compress
+            fn(batch, raw, comp, cache.state, cache.entries, cache.paging, st)
         lcsa.lcs_window_commit(batch, cache.state, st)
         pos = after
     torch.cuda.synchronize()
@@ -125,6 +145,45 @@ def test_compress_incremental_equals_one_shot(m, overlap):
             assert np.array_equal(a[key], c[key]), (b, key)
     for key in ("nope", "rope", "scale"):
         assert torch.equal(getattr(one.state.window, key), getattr(inc.state.window, key))
+
+
+@pytest.mark.parametrize("m,overlap,dim,fmt", [(4, True, 512, "fp8_split"), (4, True, 128, "bf16"),
+                                               (2, False, 512, "fp8_split"), (1, False, 128, "fp8_split")])
+def test_compress_per_channel_matches_oracle(m, overlap, dim, fmt):
+    """The per-channel reading (a score row per token, softmax per channel) against the oracle."""
+    lengths = [1, 3, 300, 517]
+    cache, _, _ = _compress_run(lengths, [lengths], m, overlap, dim, fmt, block_order_seed=4, per_channel=True)
+    bias = _per_channel_bias(21, dim, m, overlap)
+    for b, L in enumerate(lengths):
+        nf = L // m
+        if not nf:
+            continue
+        raw = bits_to_f64(raw_rows_np(21, 0, b, L, dim))
+        sc = bits_to_f64(_score_rows_np(21, b, L, dim))
+        orc = oracle.quantize_rows(oracle.compress_per_channel(raw, sc, bias, m, overlap), fmt)
+        gpu = read_rows(cache.entries, entry_rows_of(cache, b, range(nf)))
+        compare_quantized(gpu, orc, f"per-channel entries seq {b}")
+
+
+def test_compress_per_channel_incremental_equals_one_shot():
+    # the pending score rows carry the overlapping block across calls: same bits as one call
+    lengths = [263, 517, 130]
+    rng = np.random.default_rng(6)
+    plan, left = [], list(lengths)
+    while any(left):
+        call = []
+        for b in range(3):
+            c = min(left[b], int(rng.choice([0, 1, 1, 1, 3, 17, 64])))
+            call.append(c)
+            left[b] -= c
+        plan.append(call)
+    one, _, _ = _compress_run(lengths, [lengths], 4, True, 512, "fp8_split", per_channel=True)
+    inc, _, _ = _compress_run(lengths, plan, 4, True, 512, "fp8_split", per_channel=True)
+    for b, L in enumerate(lengths):
+        rows = entry_rows_of(one, b, range(L // 4))
+        a, c = read_rows(one.entries, rows), read_rows(inc.entries, rows)
+        for key in ("nope", "rope", "scale"):
+            assert np.array_equal(a[key], c[key]), (b, key)
 
 
 # ---------------------------------------------------------------------------------------- indexer
@@ -191,7 +250,7 @@ def test_index_scores_exact_and_topk_sets(heads, rank, relu, scaled, new, length
     lcsa.csa_index_scores(batch, q_fp4, q_sc, hw, heads, cache.keys, cache.paging, m, flags, scores, ld, st)
     out_idx = torch.full((T, k), -7, dtype=torch.int32, device=DEV)
     out_cnt = torch.full((T,), -7, dtype=torch.int32, device=DEV)
-    wsb = lcsa.lcs_index_topk_workspace(batch, m, k)
+    wsb = lcsa.lcs_index_topk_workspace(batch, heads, cache.keys, cache.paging, m, k)
     ws = workspace(wsb)
     lcsa.csa_index_topk(batch, q_fp4, q_sc, hw, heads, cache.keys, cache.paging, m, k, flags, out_idx, out_cnt,
                         ws, wsb, st)
@@ -229,7 +288,7 @@ def test_topk_ties_take_lowest_index():
     cache, batch, *_, q_fp4, q_sc, hw = _index_case(lengths, new, m, k, 4, 128, False, True, ties=True)
     out_idx = torch.empty((batch.total_new, k), dtype=torch.int32, device=DEV)
     out_cnt = torch.empty((batch.total_new,), dtype=torch.int32, device=DEV)
-    wsb = lcsa.lcs_index_topk_workspace(batch, m, k)
+    wsb = lcsa.lcs_index_topk_workspace(batch, 4, cache.keys, cache.paging, m, k)
     lcsa.csa_index_topk(batch, q_fp4, q_sc, hw, 4, cache.keys, cache.paging, m, k, 0, out_idx, out_cnt,
                         workspace(wsb), wsb)
     torch.cuda.synchronize()
@@ -239,12 +298,14 @@ def test_topk_ties_take_lowest_index():
 # ---------------------------------------------------------------------------------------- attention
 
 def _attend_case(kind, lengths, new, heads, dim, fmt, m, k, seed=41, scale=None, split=False, sink=None,
-                 corrupt_seq=None, rows_hook=None):
+                 corrupt_seq=None, rows_hook=None, skip_seq=None, expect_status=None):
     """Fill an entry cache / window ring / new rows with oracle-quantised rows and run one call.
     corrupt_seq: unmap that sequence's first cache block before the call (host-side corruption of
     the block table); the call must then report LCS_ERR_DEVICE_GUARD and every other sequence must
     still match the oracle.  rows_hook(b, entry_rows): may change a sequence's entry rows (fp64)
-    before they are quantised."""
+    before they are quantised.  expect_status: the device status the call must report (outputs
+    are not checked when it is LCS_ERR_TIMEOUT); skip_seq: a sequence whose outputs are not
+    checked."""
     S = len(lengths)
     fmtc = buffers.row_format_code(fmt)
     cap = max(lengths) + 128
@@ -332,16 +393,19 @@ def _attend_case(kind, lengths, new, heads, dim, fmt, m, k, seed=41, scale=None,
     if sink is not None:
         lcsa.lcs_attention_sink(out, lse, torch.from_numpy(sink.astype(np.float32)).to(DEV))
     torch.cuda.synchronize()
-    if corrupt_seq is None:
-        assert_status_ok(st)
-    else:
-        assert int(st.item()) == 6, f"device status {int(st.item())}, expected LCS_ERR_DEVICE_GUARD"
+    want = expect_status if expect_status is not None else (6 if corrupt_seq is not None else 0)
+    got = int(st.item())
+    assert got == want, f"device status {got} ({lcsa.STATUS_NAMES.get(got)}), expected {lcsa.STATUS_NAMES[want]}"
+    if want == 7:
+        return
+    if corrupt_seq is not None:
+        skip_seq = corrupt_seq
     o = bf16_tensor_to_f64(out); l = lse.cpu().numpy()
     qf = bits_to_f64(q_bits)
     qi = 0
     for b in range(S):
         n0 = lengths[b] - new[b]
-        if b == corrupt_seq:
+        if b == skip_seq:
             qi += new[b]
             continue
         for i in range(new[b]):

@@ -410,6 +410,60 @@ def test_layer_full_topk_equals_dense_over_visible():
         assert np.allclose(out["o"][i], ref, rtol=1e-13, atol=1e-13)
 
 
+# ------------------------------------------------------------------------------------------------
+# Per-channel compression weights (the variant reading: chenxutan section 4.2 sketch)
+# ------------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("m,overlap", [(4, True), (4, False), (2, True), (1, False)])
+def test_per_channel_weights_are_a_softmax_per_channel(m, overlap):
+    n, d = 37, 24
+    raw = RNG.standard_normal((n, d)); sc = RNG.standard_normal((n, d)) * 2
+    bias = RNG.standard_normal(((2 * m if overlap else m), d))
+    out, ws = oracle.compress_per_channel(raw, sc, bias, m, overlap, return_weights=True)
+    for j, a in enumerate(ws):
+        lo, hi = oracle.entry_span(j, m, overlap)
+        t = np.arange(max(lo, 0), hi)
+        assert np.allclose(a.sum(axis=0), 1.0, atol=1e-15)
+        assert np.allclose(a, scipy.special.softmax(sc[t] + bias[t - lo], axis=0), rtol=1e-13, atol=1e-15)
+        assert np.allclose(out[j], np.einsum("td,td->d", a, raw[t]), rtol=1e-13, atol=1e-13)
+
+
+def test_per_channel_with_equal_channels_is_the_scalar_reading():
+    # every channel scored by the scalar w . k_t and one bias per offset: the per-channel softmax is
+    # the same in every channel, and the entries are those of the scalar compressor
+    n, d, m = 41, 16, 4
+    raw = RNG.standard_normal((n, d)); w = RNG.standard_normal(d); b = RNG.standard_normal(2 * m)
+    sc = np.repeat((raw @ w)[:, None], d, axis=1)
+    per = oracle.compress_per_channel(raw, sc, np.repeat(b[:, None], d, axis=1), m, True)
+    assert np.allclose(per, oracle.compress(raw, w, b, m, True), rtol=1e-13, atol=1e-13)
+
+
+def test_per_channel_channels_are_independent_and_local():
+    n, d, m = 40, 12, 4
+    raw = RNG.standard_normal((n, d)); sc = RNG.standard_normal((n, d))
+    bias = RNG.standard_normal((2 * m, d))
+    a = oracle.compress_per_channel(raw, sc, bias, m, True)
+    raw2, sc2 = raw.copy(), sc.copy()
+    raw2[:, 5] += 3.0; sc2[:, 5] -= 2.0                   # channel 5 only
+    b = oracle.compress_per_channel(raw2, sc2, bias, m, True)
+    keep = [c for c in range(d) if c != 5]
+    assert np.array_equal(a[:, keep], b[:, keep]) and not np.allclose(a[:, 5], b[:, 5])
+    raw3 = raw.copy(); raw3[20] += 5.0                    # token 20 (block 5) reaches entries 5 and 6 only
+    c = oracle.compress_per_channel(raw3, sc, bias, m, True)
+    changed = [j for j in range(n // m) if not np.array_equal(a[j], c[j])]
+    assert changed == [5, 6]
+
+
+def test_per_channel_constant_window_and_ratio_one():
+    n, d = 24, 8
+    row = RNG.standard_normal(d)
+    raw = np.tile(row, (n, 1)); sc = RNG.standard_normal((n, d))
+    out = oracle.compress_per_channel(raw, sc, RNG.standard_normal((8, d)), 4, True)
+    assert np.allclose(out, np.tile(row, (n // 4, 1)), rtol=1e-14, atol=1e-14)
+    raw = RNG.standard_normal((n, d))
+    assert np.array_equal(oracle.compress_per_channel(raw, sc, np.zeros((1, d)), 1, False), raw)
+
+
 def _brute_rows(t, selected, entries, window_rows, window=128):
     """The rows a CSA query attends, gathered one by one: the listed entries in list order, then
     the window tokens from max(0, t - window + 1) up to t itself."""

@@ -66,7 +66,7 @@ def test_noalloc_topk_equals_workspace_entry_point_twice(first, second):
         T = batch.total_new
         ref_idx = torch.full((T, k), -5, dtype=torch.int32, device=DEV)
         ref_cnt = torch.full((T,), -5, dtype=torch.int32, device=DEV)
-        wsb = lcsa.lcs_index_topk_workspace(batch, m, k)
+        wsb = lcsa.lcs_index_topk_workspace(batch, heads, cache.keys, cache.paging, m, k)
         lcsa.csa_index_topk(batch, q_fp4, q_sc, hw, heads, cache.keys, cache.paging, m, k, 0, ref_idx, ref_cnt,
                             workspace(wsb), wsb)
         got_idx = torch.full((T, k), -9, dtype=torch.int32, device=DEV)
@@ -89,7 +89,7 @@ def test_noalloc_score_then_select_phases_share_the_scratch():
     T = batch.total_new
     ref_idx = torch.full((T, k), -5, dtype=torch.int32, device=DEV)
     ref_cnt = torch.full((T,), -5, dtype=torch.int32, device=DEV)
-    wsb = lcsa.lcs_index_topk_workspace(batch, m, k)
+    wsb = lcsa.lcs_index_topk_workspace(batch, heads, cache.keys, cache.paging, m, k)
     lcsa.csa_index_topk(batch, q_fp4, q_sc, hw, heads, cache.keys, cache.paging, m, k, 0, ref_idx, ref_cnt,
                         workspace(wsb), wsb)
     got_idx = torch.full((T, k), -9, dtype=torch.int32, device=DEV)
@@ -108,13 +108,14 @@ def test_noalloc_score_then_select_phases_share_the_scratch():
 
 
 def test_noalloc_rejects_requests_beyond_its_scratch():
-    # 64 queries over 131072-entry sequences need 32 MiB of scratch: refused, nothing launched
+    # a chunk of 300 queries over a 131072-entry sequence at rank 64 keeps every score key: 157 MB of
+    # scratch, refused, nothing launched
     cap = 4 * 131072 + 128
-    batch = buffers.make_batch([cap - 128] * 64, [1] * 64, DEV, max_seq_len=cap)
-    assert lcsa.lcs_index_topk_workspace(batch, 4, 512) > lcsa.NOALLOC_SCRATCH_BYTES
+    batch = buffers.make_batch([cap - 128], [300], DEV, max_seq_len=cap)
     z = torch.zeros(16, dtype=torch.int32, device=DEV)
-    keys = lcsa.IndexKeys(z, z, 128, 1)
+    keys = lcsa.IndexKeys(z, z, 64, 1)
     pg = lcsa.Paging(z, 32, 1)
+    assert lcsa.lcs_index_topk_workspace(batch, 4, keys, pg, 4, 512) > lcsa.NOALLOC_SCRATCH_BYTES
     with pytest.raises(lcsa.LcsError) as e:
         lcsa.csa_index_topk_noalloc(batch, z, z, None, 4, keys, pg, 4, 512, 0, z, z)
     assert e.value.status == 8
