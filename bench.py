@@ -188,6 +188,25 @@ def traffic_of(part: str):
     return None
 
 
+def graph_kernel_count(graph):
+    """Kernel nodes of a captured CUDA graph (the step's launches of this library's kernels), read
+    back through the CUDA runtime; None when the graph cannot be inspected."""
+    try:
+        from cuda.bindings import runtime as cr
+        g = cr.cudaGraph_t(init_value=int(graph.raw_cuda_graph()))
+        err, _, n = cr.cudaGraphGetNodes(g, 0)
+        if err != cr.cudaError_t.cudaSuccess:
+            return None
+        err, nodes, n = cr.cudaGraphGetNodes(g, n)
+        if err != cr.cudaError_t.cudaSuccess:
+            return None
+        kinds = [cr.cudaGraphNodeGetType(nd) for nd in nodes[:n]]
+        return sum(1 for e, t in kinds if e == cr.cudaError_t.cudaSuccess and
+                   t == cr.cudaGraphNodeType.cudaGraphNodeTypeKernel)
+    except Exception:
+        return None
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -306,9 +325,11 @@ def run_gpu(args, rank, world, local, wl=None):
     load_step(0)
     step_body(with_events=False)
     torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()             # the timed step: kernels only
+    graph = torch.cuda.CUDAGraph(keep_graph=True)   # the timed step: kernels only
     with torch.cuda.graph(graph):
         step_body(with_events=False)
+    graph.instantiate()
+    graph_kernels = graph_kernel_count(graph)
     graph_ev = torch.cuda.CUDAGraph()          # the same step with event nodes between the calls
     with torch.cuda.graph(graph_ev):
         step_body(with_events=True)
@@ -347,7 +368,9 @@ def run_gpu(args, rank, world, local, wl=None):
     # top-k part, merge; otherwise one kernel, plus a merge when split) + window commit
     tc_plan = D == 512 and H <= 64 and k <= 2048
     attend_launches = 3 if tc_plan else (2 if splits_used else 1)
-    launches_per_step = 2 + 2 + attend_launches + (0 if layer.ring_only else 1)
+    launches_per_step = 2 + 1 + attend_launches + (0 if layer.ring_only else 1)
+    if graph_kernels is not None:   # counted from the captured step itself
+        launches_per_step = graph_kernels
     hbm, peak_kind = measured_peaks()
     peak_src = f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback"
     n_vis = [(L + s + 1) // m for s in range(timed_end, steps_total)]
@@ -485,9 +508,11 @@ def run_gpu_stack(args, rank, world, local, wl):
     load_step(0)
     step_body()
     torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
+    graph = torch.cuda.CUDAGraph(keep_graph=True)
     with torch.cuda.graph(graph):
         step_body()
+    graph.instantiate()
+    graph_kernels = graph_kernel_count(graph)
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps_total)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps_total)]
     barrier(world)
@@ -527,7 +552,9 @@ def run_gpu_stack(args, rank, world, local, wl):
     n_hca = n_layers - n_csa
     # CSA layer: compress (2) + indexer (2) + attention window part, top-k part, merge (3);
     # HCA layer: compress (2) + attention + merge (2)
-    launches = n_csa * (2 + 2 + 3) + n_hca * (2 + 2)
+    launches = n_csa * (2 + 1 + 3) + n_hca * (2 + 2)
+    if graph_kernels is not None:   # counted from the captured step itself
+        launches = graph_kernels
     cfg = {"workload": wl.name, "num_seqs": S, "layers": n_layers, "layer_kinds": stack.kinds,
            "ctx_len": lengths if wl.kind == "mixed" else wl.ctx_len, "new_tokens_per_seq": 1, "heads": H,
            "kv_dim": D, "row_format": "fp8_e4m3(448)+bf16_rope(64)+f32_scale", "csa_m": 4, "hca_m": 128,
@@ -591,9 +618,11 @@ def run_gpu_prefill(args, rank, world, local, wl):
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     step_body()
     torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
+    graph = torch.cuda.CUDAGraph(keep_graph=True)
     with torch.cuda.graph(graph):
         step_body()
+    graph.instantiate()
+    graph_kernels = graph_kernel_count(graph)
     n_tot = args.warmup + args.steps
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(n_tot)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(n_tot)]
@@ -654,7 +683,8 @@ def run_gpu_prefill(args, rank, world, local, wl):
            "step": "the same chunk of new tokens re-run every step (identical work)",
            "l2": "flushed between timed steps (256 MB write)", "data": "synthetic"}
     return {"ms": ms, "clocks": clk.summary(), "roofline": roofline, "status_ok": int(layer.status.item()) == 0,
-            "per_rank_queries": T, "config": cfg, "launches": 2 + 2 + 1 + 1}
+            "per_rank_queries": T, "config": cfg,
+            "launches": graph_kernels if graph_kernels is not None else 2 + 2 + 1 + 1}
 
 
 # ---------------------------------------------------------------------------------------------

@@ -190,14 +190,17 @@ lcs_status lcs_window_commit(const lcs_batch* batch, const lcs_state* state, int
  * Workspace: device, >= lcs_index_topk_workspace(batch, heads, keys, paging, m, k) bytes (the
  * same arguments as the call), 256-byte aligned.  Its first lcs_index_topk_workspace_zeroed()
  * bytes must hold zeros before the first call on it (e.g. cudaMemset once after allocation): they
- * are per-sequence counters that every completed call leaves at zero again.  After a call whose
- * device status is LCS_ERR_TIMEOUT, zero them again before reusing the workspace.
- * How the work is split: at rank 128 with 1, 2, 4 or 8 heads and 2k + 256 <= 4096, the scoring
- * runs on the tensor cores with the top-k fused into it -- a CTA scores a run of the cache for a
- * group of up to 4 queries of a sequence and keeps each query's k best entries, and the group's
- * last CTA merges the runs' lists -- and the workspace holds only those lists (about 8 k bytes per
- * query and run); otherwise every score's order-preserving key is written to the workspace (4
- * bytes per query and visible entry) and a selection pass reads them back.
+ * are per-sequence counters and per-query thresholds that every completed call leaves at zero
+ * again.  After a call whose device status is LCS_ERR_TIMEOUT, zero them again before reusing the
+ * workspace.
+ * How the work is split: at rank 128 with 1, 2, 4 or 8 heads, 2k + 256 <= 4096 and up to 16
+ * queries per sequence, the scoring runs on the tensor cores with the top-k fused into it -- a CTA
+ * scores a run of the cache for a group of up to 4 queries of a sequence and keeps each query's
+ * best entries, the runs of a query share the best threshold any of them has reached, and the
+ * group's last CTA merges the runs' lists -- and the workspace holds only those lists (at most
+ * about 8 k bytes per query and run); otherwise (longer query runs, rank 64) every score's
+ * order-preserving key is written to the workspace (4 bytes per query and visible entry) and a
+ * selection pass reads them back.
  * Phases: a call runs the scoring phase and the selection phase.  With LCS_INDEX_SCORE_ONLY it
  * runs only the first (the scores, or the runs' lists, into the workspace), with
  * LCS_INDEX_SELECT_ONLY only the second (the selection from the workspace into out_idx,

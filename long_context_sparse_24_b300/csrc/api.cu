@@ -16,6 +16,7 @@ lcs_status check_batch(const lcs_batch* b) {
   if (b->num_seqs <= 0 || b->num_seqs > 65535) return LCS_ERR_UNSUPPORTED;
   if (b->total_new < 0 || b->max_new < 0 || b->max_seq_len < 0) return LCS_ERR_INVALID_ARG;
   if (b->max_new > b->max_seq_len) return LCS_ERR_SHAPE;
+  if ((long long)b->total_new > (long long)b->num_seqs * b->max_new) return LCS_ERR_SHAPE;   // no sequence has more
   return LCS_OK;
 }
 
@@ -134,26 +135,39 @@ std::atomic<uint32_t> g_wait_polls{LCSA_DEFAULT_WAIT_POLLS};
 
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
-// Workspace of csa_index_topk.  Both layouts start with the ticket counters (one per sequence and
-// query group, at most int32[num_seqs][max_new]; zero between calls).  Fused top-k: run counts
-// int32[T][runs], run keys u64[T][runs][k].  Otherwise: score keys u32[T][ld], histograms
-// u32[T][2048].
+constexpr int kFusedMaxQueries = 16;   // queries per sequence up to which the top-k is fused
+
+// Workspace of csa_index_topk.  Both layouts start with the part that is zero between calls: the
+// ticket counters (one per sequence and query group, at most int32[num_seqs][max_new]), then the
+// queries' shared thresholds (u64[num_seqs][max_new], at least one per batch row).  Fused top-k: run counts
+// int32[T][runs], run thresholds u64[T][runs], run keys u64[T][runs][k].  Otherwise: score keys
+// u32[T][ld], histograms u32[T][2048].
 struct TopkWs {
   bool fused;
   IndexTcPlan plan;
-  size_t ticket, cnt, keys, hist, total;
+  size_t ticket, gthr, cnt, tau, keys, hist, total;
 };
+
+size_t zeroed_tickets_bytes(const lcs_batch* b) {
+  return round256((size_t)b->num_seqs * std::max(1, b->max_new) * 4);
+}
 
 TopkWs topk_ws_layout(const lcs_batch* b, const IndexParams& p, int rank, int m, int k) {
   TopkWs w{};
   const size_t T = (size_t)b->total_new;
   w.ticket = 0;
+  w.gthr = zeroed_tickets_bytes(b);
   const size_t body = lcs_index_topk_workspace_zeroed(b);
-  w.plan = plan_index_tc(p, rank, b->max_new, b->max_seq_len / m, b->num_seqs, num_sms(), k);
+  // the top-k fused into the scorer serves up to 16 queries per sequence (groups of at most 4 per
+  // CTA); longer query runs take the prefill scorer, whose CTAs score 16 queries per key tile (a
+  // quarter of the key reads) and write every score key for the select kernel
+  const bool long_runs = b->max_new > kFusedMaxQueries && index_tc_pf_applies(p, rank, b->max_new);
+  if (!long_runs) w.plan = plan_index_tc(p, rank, b->max_new, b->max_seq_len / m, b->num_seqs, num_sms(), k);
   w.fused = w.plan.applies != 0;
   if (w.fused) {
     w.cnt = body;
-    w.keys = w.cnt + round256(T * w.plan.runs * 4);
+    w.tau = w.cnt + round256(T * w.plan.runs * 4);
+    w.keys = w.tau + round256(T * w.plan.runs * 8);
     w.hist = w.keys;
     w.total = w.keys + T * w.plan.runs * (size_t)k * 8 + 256;
   } else {
@@ -377,7 +391,8 @@ size_t lcs_index_topk_workspace(const lcs_batch* batch, int32_t heads, const lcs
 }
 
 size_t lcs_index_topk_workspace_zeroed(const lcs_batch* batch) {
-  return batch == nullptr ? 0 : round256((size_t)batch->num_seqs * std::max(1, batch->max_new) * 4);
+  if (batch == nullptr) return 0;
+  return zeroed_tickets_bytes(batch) + round256((size_t)batch->num_seqs * std::max(1, batch->max_new) * 8);
 }
 
 uint32_t lcs_set_wait_polls(uint32_t polls) { return g_wait_polls.exchange(polls); }
@@ -461,6 +476,9 @@ lcs_status csa_index_topk(const lcs_batch* batch, const uint8_t* q_fp4, const ui
     p.runs.runs = w.plan.runs;
     p.runs.ticket = reinterpret_cast<int*>(ws + w.ticket);
     p.runs.cnt = reinterpret_cast<int*>(ws + w.cnt);
+    p.runs.tau = reinterpret_cast<uint64_t*>(ws + w.tau);
+    // (a scoring call on its own shares no threshold: the counters stay zero without a merge)
+    p.runs.gthr = score_only || select_only ? nullptr : reinterpret_cast<uint64_t*>(ws + w.gthr);
     p.runs.keys = reinterpret_cast<uint64_t*>(ws + w.keys);
     p.out_idx = out_idx;
     p.out_cnt = out_cnt;

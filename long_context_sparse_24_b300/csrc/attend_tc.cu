@@ -391,8 +391,26 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
       }
       *reinterpret_cast<uint4*>(smem + L::kT + r * 128 + ((j ^ (r & 7)) << 4)) = h;
     }
-    // the next tile's rows go out now and fly while this tile computes
+    // the next tile's rows go out now and fly while this tile computes; with every descriptor
+    // resolved up front (16 heads) the tile after it is fetched into L2 meanwhile
     if (tt + 1 < ntiles) load_tile(tt + 1);
+    if (HG == 16 && tt + 2 < ntiles) {
+      // 128 rows x (448 code bytes + 128 RoPE bytes): 3.5 + 1 lines of 128 bytes a row
+      for (int x = tid; x < kTileRows * 5; x += kThreads) {
+        const int r = x / 5, part = x % 5;
+        const long long d = desc[(tt + 2) * kTileRows + r];
+        if (d < 0) continue;
+        const int kind = (int)(d >> 60);
+        const long long rw = d & ((1ll << 60) - 1);
+        if (part < 4) {
+          const uint8_t* src = (kind == 1 ? p.new_rows.nope : (kind == 2 ? p.window.nope : p.entries.nope));
+          prefetch_l2(src + rw * kNopeBytes + part * 128);
+        } else {
+          const __nv_bfloat16* src = (kind == 1 ? p.new_rows.rope : (kind == 2 ? p.window.rope : p.entries.rope));
+          prefetch_l2(src + rw * kRope);
+        }
+      }
+    }
     if (tt == 0) {
       cp_async_wait<0>();
       __syncthreads();

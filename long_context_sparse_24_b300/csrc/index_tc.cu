@@ -60,7 +60,10 @@ constexpr int kATileBytes = kTile * kRowBytes;
 constexpr int kEpiWarps = 8;        // two per TMEM lane quadrant, the two tiles of a pair
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kProdWarps = 2;       // producer warps, alternating tiles
-constexpr int kScaleSlots = 2 * kStages;  // block-scale ring (read by the epilogue, outlives a stage)
+// block-scale ring: tile i's scales are copied once stage i % kStages is free (the MMA of tile
+// i - kStages is done, so the epilogue has read tile i - kStages - kAcc); they are read by the
+// epilogue of tile i, so kStages + kAcc tiles' scales can be live at once
+constexpr int kScaleSlots = kStages + kAcc;
 constexpr int kThreads = kEpiThreads + 32 * kProdWarps + 32;
 constexpr int kCandPerThread = 16;  // candidate buffer per query <= kEpiThreads * kCandPerThread
 constexpr int kEpiBarrier = 1;      // named barrier of the epilogue warps
@@ -87,6 +90,7 @@ struct TcSmem {
   static constexpr int kRingEnd = kA + kStages * kATileBytes;
   static constexpr int kRunOff = (kRingEnd - 4 * (kMaxRuns + 4)) / 16 * 16;              // int [runs + 1]
   static constexpr int kSelAll = (kRunOff - (int)sizeof(SelScratch<kThreads>)) / 16 * 16;  // SelScratch<kThreads>
+  static constexpr int kHist = kSelAll - 2048 * 4;                                       // u32 [2048]
   static constexpr int kCand = (kSelEpi + (int)sizeof(SelScratch<kEpiThreads>) + 15) / 16 * 16;   // u64 [QPS][cap], then
   // the run's page table: int [pages]
   static size_t bytes(bool fused, int cap, int pages) {
@@ -146,13 +150,17 @@ __device__ int write_run_sorted(const uint64_t* buf, int n, uint64_t tau, int j0
 // The merge of one query's run lists into its top-k (the scorer's last CTA of a query group, or
 // the merge kernel).  Group of NT threads (ID 0: the whole CTA).  Every run list is sorted by entry
 // index and the runs cover increasing index ranges, so the lists read one after the other are
-// sorted too: they are staged in shared memory (stage: room for runs * k keys), the k-th largest
-// key is selected there, and the keys at or above it are read out in that order.  N: visible
-// entries of the query; run_off: runs + 1 ints of shared memory.
-template <int NT, int ID>
+// sorted too: they are staged in shared memory (stage: room for stage_cap keys), the k-th largest
+// key is selected there, and the keys at or above it are read out in that order.  A run whose list
+// is full recorded the threshold of its own k keys; the largest of those bounds the query's k-th
+// largest key from below, so the selection looks only at the staged keys at or above it.  N:
+// visible entries of the query; run_off: runs + 1 ints of shared memory; hist: 1 << BITS counters
+// of shared memory.
+template <int NT, int ID, int BITS>
 __device__ void merge_query_topk(const TopkRuns& tr, long long q, int N, int k, uint64_t* stage, int stage_cap,
-                                 int* run_off, int32_t* out_idx, int32_t* out_cnt, SelScratch<NT>& sc) {
-  const int tid = threadIdx.x;
+                                 int* run_off, uint32_t* hist, int32_t* out_idx, int32_t* out_cnt,
+                                 SelScratch<NT>& sc) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int32_t* out = out_idx + q * k;
   if (N <= k) {   // every visible entry
     for (int j = tid; j < k; j += NT) out[j] = j < N ? j : -1;
@@ -161,27 +169,35 @@ __device__ void merge_query_topk(const TopkRuns& tr, long long q, int N, int k, 
   }
   const int* cnts = tr.cnt + q * tr.runs;
   const uint64_t* keys = tr.keys + q * (long long)tr.runs * k;
-  // list offsets in the stage
+  // list offsets in the stage, and the bound: the largest threshold of the runs (runs <= 256 <= NT)
+  uint64_t bound;
   {
-    const int c = tid < tr.runs ? min(__ldcg(cnts + tid), k) : 0;   // runs <= 256 <= NT
+    const int c = tid < tr.runs ? min(__ldcg(cnts + tid), k) : 0;
+    unsigned long long t = tid < tr.runs ? __ldcg(reinterpret_cast<const unsigned long long*>(tr.tau) + q * tr.runs + tid)
+                                         : 0ull;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const unsigned long long y = __shfl_xor_sync(0xffffffffu, t, o);
+      t = y > t ? y : t;
+    }
+    if (lane == 0) sc.span[warp] = t;
     int tot;
-    const int incl = group_scan_incl<NT, ID>(c, sc.warp_tot, &tot);
+    const int incl = group_scan_incl<NT, ID>(c, sc.warp_tot, &tot);   // (its barriers publish span)
     if (tid < tr.runs) run_off[tid] = incl - c;
     if (tid == 0) run_off[tr.runs] = tot;
+    unsigned long long bmax = 0ull;
+#pragma unroll
+    for (int w = 0; w < NT / 32; ++w) bmax = sc.span[w] > bmax ? sc.span[w] : bmax;
+    bound = bmax;
   }
   group_sync<NT, ID>();
-  const int total = run_off[tr.runs];
-  // stage the lists: eight independent loads in flight per thread; a full run's smallest key is
-  // its k-th largest, and the largest of those bounds the sequence's k-th largest from below
-  if (tid == 0) sc.span[0] = 0ull;
-  group_sync<NT, ID>();
+  const int total = min(run_off[tr.runs], stage_cap);   // (the host sizes the stage for every list)
+  // stage the lists: eight independent loads in flight per thread
   for (int x0 = tid; x0 < total; x0 += 8 * NT) {
     uint64_t v[8];
-    int at[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int x = x0 + u * NT;
-      at[u] = -1;
       v[u] = 0ull;
       if (x < total) {
         int lo = 0, hi = tr.runs - 1;   // the run holding stage position x
@@ -189,59 +205,16 @@ __device__ void merge_query_topk(const TopkRuns& tr, long long q, int N, int k, 
           const int mid = (lo + hi + 1) >> 1;
           if (run_off[mid] <= x) lo = mid; else hi = mid - 1;
         }
-        at[u] = x;
         v[u] = __ldcg(reinterpret_cast<const unsigned long long*>(keys) + (long long)lo * k + (x - run_off[lo]));
       }
     }
 #pragma unroll
     for (int u = 0; u < 8; ++u)
-      if (at[u] >= 0) stage[at[u]] = v[u];
+      if (x0 + u * NT < total) stage[x0 + u * NT] = v[u];
   }
   group_sync<NT, ID>();
-  uint64_t tau;
-  if (total <= k) {
-    tau = 0ull;   // (fewer than k candidates only when the scoring gave up on a bounded wait: take them all)
-  } else {
-    // bound: the largest minimum over the runs that kept k keys (each such run has k keys >= it)
-    for (int r = 0; r < tr.runs; ++r) {
-      if (run_off[r + 1] - run_off[r] != k) continue;
-      unsigned long long mn = ~0ull;
-      for (int x = run_off[r] + tid; x < run_off[r + 1]; x += NT) mn = stage[x] < mn ? stage[x] : mn;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const unsigned long long y = __shfl_xor_sync(0xffffffffu, mn, o);
-        mn = y < mn ? y : mn;
-      }
-      if ((tid & 31) == 0 && mn != ~0ull) atomicMax(&sc.span[0], mn);
-    }
-    group_sync<NT, ID>();
-    const uint64_t bound = sc.span[0];
-    // the keys at or above the bound (at least k of them) gathered behind the staged lists when
-    // they fit, and the k-th largest selected among them only; else among all staged keys
-    uint64_t* cand = stage + total;
-    const int room = stage_cap - total;
-    if (tid == 0) sc.count = 0;
-    group_sync<NT, ID>();
-    for (int x0 = 0; x0 < total; x0 += NT) {
-      const int x = x0 + tid;
-      const uint64_t u = x < total ? stage[x] : 0ull;
-      const bool take = x < total && u >= bound;
-      const unsigned m = __ballot_sync(0xffffffffu, take);
-      if (m != 0u) {
-        const int leader = __ffs(m) - 1;
-        int base = 0;
-        if ((tid & 31) == leader) base = atomicAdd(&sc.count, __popc(m));
-        base = __shfl_sync(0xffffffffu, base, leader);
-        const int at = base + __popc(m & ((1u << (tid & 31)) - 1u));
-        if (take && at < room) cand[at] = u;
-      }
-    }
-    group_sync<NT, ID>();
-    const int nc = sc.count;
-    group_sync<NT, ID>();
-    tau = nc <= room ? kth_largest_key<NT, ID>(k, SmemKeys{cand, nc}, sc)
-                     : kth_largest_key<NT, ID>(k, SmemKeys{stage, total}, sc);
-  }
+  // (fewer than k keys only when the scoring gave up on a bounded wait: take them all)
+  const uint64_t tau = total <= k ? 0ull : kth_largest_key<NT, ID, BITS>(stage, total, k, sc, hist, bound);
   // ascending read-out: thread t takes stage positions [t*ppt, (t+1)*ppt)
   const int ppt = (total + NT - 1) / NT;
   const int x0 = min(total, tid * ppt), x1 = min(total, x0 + ppt);
@@ -298,7 +271,10 @@ __global__ void __launch_bounds__(kThreads, QH >= 16 ? 1 : 2) index_tc_kernel(co
   if (nt == 0) {
     if constexpr (FUSED) {
       // no tiles in this run (ragged batch): an empty candidate list, and the ticket still counts it
-      for (int qi = tid; qi < qn; qi += kThreads) p.runs.cnt[(qrow0 + qi) * p.runs.runs + blockIdx.x] = 0;
+      for (int qi = tid; qi < qn; qi += kThreads) {
+        p.runs.cnt[(qrow0 + qi) * p.runs.runs + blockIdx.x] = 0;
+        p.runs.tau[(qrow0 + qi) * p.runs.runs + blockIdx.x] = 0ull;
+      }
     } else {
       return;
     }
@@ -341,20 +317,20 @@ __global__ void __launch_bounds__(kThreads, QH >= 16 ? 1 : 2) index_tc_kernel(co
       thr_s[tid] = 0ull;
       cnt_s[tid] = 0;
     }
+    // the physical block of every page the run touches, copied by every thread at once (the
+    // producer lane that reads an entry checks it)
+    for (int i = tid; i < npages; i += kThreads) {
+      const int blk = page0 + i;
+      if (blk < p.paging.max_blocks)
+        cp_async4(pages_s + i, p.paging.table + (long long)b * p.paging.max_blocks + blk);
+      else
+        pages_s[i] = -1;
+    }
+    cp_async_commit();
     __syncthreads();
 
     if (warp == kEpiWarps) {
       tmem_alloc(sbase + L::kMisc, kCols);
-      // physical block of every page the run touches (-1: unmapped or outside the key rows)
-      for (int i = lane; i < npages; i += 32) {
-        const int blk = page0 + i;
-        int phys = blk < p.paging.max_blocks ? p.paging.table[(long long)b * p.paging.max_blocks + blk] : -1;
-        if (phys < 0 || (long long)(phys + 1) * epb > p.k_rows) {
-          report(p.status, LCS_ERR_DEVICE_GUARD);
-          phys = -1;
-        }
-        pages_s[i] = phys;
-      }
     } else if (warp < kEpiWarps) {
       // ---- B operand: row n = blk*QH + c, c = qi*HI + h; codes of block blk in chunks 2blk, 2blk+1
       for (int idx = tid; idx < N * 8; idx += kEpiThreads) {
@@ -381,6 +357,7 @@ __global__ void __launch_bounds__(kThreads, QH >= 16 ? 1 : 2) index_tc_kernel(co
       }
       fence_proxy_async_smem();
     }
+    cp_async_wait<0>();
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
@@ -403,7 +380,11 @@ __global__ void __launch_bounds__(kThreads, QH >= 16 ? 1 : 2) index_tc_kernel(co
         const uint32_t a_dst = sbase + L::kA + s * kATileBytes;
         const uint32_t s_dst = sbase + L::kScale + (i % kScaleSlots) * kTile * 4;
         const int npg = rows >> eshift;
-        const int phys = lane < npg ? pages_s[((e0 >> eshift) - page0) + lane] : -1;
+        int phys = lane < npg ? pages_s[((e0 >> eshift) - page0) + lane] : -1;
+        if (lane < npg && (phys < 0 || (long long)(phys + 1) * epb > p.k_rows)) {
+          report(p.status, LCS_ERR_DEVICE_GUARD);   // unmapped, or outside the key rows
+          phys = -1;
+        }
         const uint32_t valid = __ballot_sync(0xffffffffu, phys >= 0);
         if (lane == 0) {
           armed_s[s] = i;
@@ -462,8 +443,12 @@ __global__ void __launch_bounds__(kThreads, QH >= 16 ? 1 : 2) index_tc_kernel(co
       const int row = quad * 32 + lane;
       SelScratch<kEpiThreads>& sel = *reinterpret_cast<SelScratch<kEpiThreads>*>(smem + L::kSelEpi);
       bool alive = true;
+      const bool share = FUSED && p.runs.gthr != nullptr;
       for (int i0 = 0; i0 < nt; i0 += 2) {
         const int i = i0 + par;
+        // the threshold the query's other runs have reached (read now, taken at the pair's end)
+        uint64_t gnext = 0ull;
+        if (share && tid < qn) gnext = __ldcg(reinterpret_cast<const unsigned long long*>(p.runs.gthr) + qrow0 + tid);
         if (i < nt && alive) {
           const int a = i % kAcc;
           bool ok = mbar_wait(bar_accf + 8 * a, (i / kAcc) & 1, p.status, abort_flag, polls);
@@ -533,6 +518,9 @@ __global__ void __launch_bounds__(kThreads, QH >= 16 ? 1 : 2) index_tc_kernel(co
           }
         }
         if constexpr (FUSED) {
+          // any run's threshold is at most the query's k-th largest key: a larger one from another
+          // run filters this run's later keys too
+          if (share && tid < qn && gnext > thr_s[tid]) thr_s[tid] = gnext;
           // both tiles of the pair are in: cut buffers that could not take another pair
           group_sync<kEpiThreads, kEpiBarrier>();
 #pragma unroll 1
@@ -540,12 +528,23 @@ __global__ void __launch_bounds__(kThreads, QH >= 16 ? 1 : 2) index_tc_kernel(co
             const int n = cnt_s[qi];
             if (n <= cap - 2 * kTile) continue;        // uniform: read after the barrier
             uint64_t* buf = cand_s + qi * cap;
-            const uint64_t tau = kth_largest_key<kEpiThreads, kEpiBarrier>(k, SmemKeys{buf, n}, sel);
+            // a threshold with k to k + k/8 of the buffer's keys at or above it (no more than the
+            // buffer can keep while taking another pair), or the current one when fewer than k
+            // keys pass that: every later key below it has k larger ones.  Published to the
+            // query's other runs.
+            const uint64_t lo = thr_s[qi];
+            const SelResult r = select_top<kEpiThreads, kEpiBarrier, 8>(buf, n, k, k >> 3, sel, sel.hist, lo);
+            const uint64_t tau = r.tau > lo ? r.tau : lo;
             const int kept = compact_keys_ge<kEpiThreads, kEpiBarrier, kCandPerThread>(buf, n, tau, sel);
             if (tid == 0) {
-              // exactly k keys >= tau remain; a later key can join the k largest only above tau
               cnt_s[qi] = kept;
-              thr_s[qi] = tau;
+              uint64_t t = tau;
+              if (share) {
+                const unsigned long long o =
+                    atomicMax(reinterpret_cast<unsigned long long*>(p.runs.gthr) + qrow0 + qi, (unsigned long long)t);
+                t = o > t ? o : t;
+              }
+              thr_s[qi] = t;
             }
             group_sync<kEpiThreads, kEpiBarrier>();
           }
@@ -569,16 +568,27 @@ __global__ void __launch_bounds__(kThreads, QH >= 16 ? 1 : 2) index_tc_kernel(co
     const int words = nt * (kTile / 32);
     uint32_t* run_bits = reinterpret_cast<uint32_t*>(smem + L::kA);
     int* run_prefix = reinterpret_cast<int*>(smem + L::kA + words * 4);
+    uint32_t* hist = reinterpret_cast<uint32_t*>(smem + L::kHist);
 #pragma unroll 1
     for (int qi = 0; qi < qn; ++qi) {
       const int n = cnt_s[qi];
       const uint64_t* buf = cand_s + qi * cap;
-      const uint64_t tau = n > k ? kth_largest_key<kThreads, 0>(k, SmemKeys{buf, n}, sel_all) : 0ull;
+      // the run's list: its k largest keys, or all of them at or above the current threshold when
+      // fewer pass it (the buffer holds every key of the run at or above that threshold)
+      const uint64_t lo = thr_s[qi];
+      uint64_t tau = lo;
+      if (n > 0) {
+        const SelResult r = select_top<kThreads, 0, 11>(buf, n, k, 0, sel_all, hist, lo);
+        tau = r.tau > lo ? r.tau : lo;
+      }
       const long long q = qrow0 + qi;
       uint64_t* dst = p.runs.keys + (q * p.runs.runs + blockIdx.x) * (long long)k;
       const int w = write_run_sorted<kThreads, 0>(buf, n, tau, t_begin * kTile, words, run_bits, run_prefix, dst,
                                                    sel_all);
-      if (tid == 0) p.runs.cnt[q * p.runs.runs + blockIdx.x] = w;
+      if (tid == 0) {
+        p.runs.cnt[q * p.runs.runs + blockIdx.x] = w;
+        p.runs.tau[q * p.runs.runs + blockIdx.x] = tau;
+      }
     }
   }
   if constexpr (FUSED) {
@@ -599,11 +609,28 @@ __global__ void __launch_bounds__(kThreads, QH >= 16 ? 1 : 2) index_tc_kernel(co
     int* run_off = reinterpret_cast<int*>(smem + L::kRunOff);
 #pragma unroll 1
     for (int qi = 0; qi < qn; ++qi)
-      merge_query_topk<kThreads, 0>(p.runs, qrow0 + qi, (n0 + qi + 1) >> mshift, k, stage,
-                                    (L::kSelAll - L::kA) / 8, run_off, p.out_idx, p.out_cnt, sel_all);
-    if (tid == 0) p.runs.ticket[(long long)b * gridDim.y + blockIdx.y] = 0;   // left at zero for the next call
+      // (the candidate buffers are idle now: with room for them, the selection's histogram has
+      // 2048 bins there, else 256 in the scratch)
+      if (QPS * cap * 8 >= 2048 * 4)
+        merge_query_topk<kThreads, 0, 11>(p.runs, qrow0 + qi, (n0 + qi + 1) >> mshift, k, stage,
+                                          (L::kSelAll - L::kA) / 8, run_off, reinterpret_cast<uint32_t*>(cand_s),
+                                          p.out_idx, p.out_cnt, sel_all);
+      else
+        merge_query_topk<kThreads, 0, 8>(p.runs, qrow0 + qi, (n0 + qi + 1) >> mshift, k, stage,
+                                         (L::kSelAll - L::kA) / 8, run_off, sel_all.hist, p.out_idx, p.out_cnt,
+                                         sel_all);
+    if (tid == 0) {   // left at zero for the next call
+      p.runs.ticket[(long long)b * gridDim.y + blockIdx.y] = 0;
+      if (p.runs.gthr != nullptr)
+        for (int qi = 0; qi < qn; ++qi) p.runs.gthr[qrow0 + qi] = 0ull;
+    }
   }
 }
+
+// the merge kernel's shared memory: scratch, histogram, run offsets, then room for the lists
+constexpr int kMergeHist = ((int)sizeof(SelScratch<256>) + 15) / 16 * 16;
+constexpr int kMergeRunOff = kMergeHist + 2048 * 4;
+constexpr int kMergeStage = kMergeRunOff + (kMaxRuns + 4) * 4;
 
 // One CTA per query: the merge of the query's run lists (the selection phase on its own, or run
 // lists too long for the scorer's shared memory).  grid: (max_new, num_seqs), block 256.
@@ -613,11 +640,13 @@ __global__ void __launch_bounds__(256) topk_merge_kernel(IndexParams p) {
   const SeqSpan sp = seq_span(p.cu_new, p.seq_len, b);
   if (i >= sp.qn) return;
   SelScratch<256>& sc = *reinterpret_cast<SelScratch<256>*>(merge_smem);
-  int* run_off = reinterpret_cast<int*>(merge_smem + sizeof(SelScratch<256>));
-  uint64_t* stage = reinterpret_cast<uint64_t*>(merge_smem + sizeof(SelScratch<256>) + (kMaxRuns + 4) * 4);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(merge_smem + kMergeHist);
+  int* run_off = reinterpret_cast<int*>(merge_smem + kMergeRunOff);
+  uint64_t* stage = reinterpret_cast<uint64_t*>(merge_smem + kMergeStage);
   const int t = sp.n0() + i;
-  merge_query_topk<256, 0>(p.runs, sp.q0 + i, (t + 1) / p.m, p.top_k, stage, 2 * p.runs.runs * p.top_k, run_off,
-                           p.out_idx, p.out_cnt, sc);
+  merge_query_topk<256, 0, 11>(p.runs, sp.q0 + i, (t + 1) / p.m, p.top_k, stage, p.runs.runs * p.top_k, run_off,
+                               hist, p.out_idx, p.out_cnt, sc);
+  if (threadIdx.x == 0 && p.runs.gthr != nullptr) p.runs.gthr[sp.q0 + i] = 0ull;   // left at zero
 }
 
 // ----------------------------------------------------------------------------------------------
@@ -742,8 +771,8 @@ IndexTcPlan plan_index_tc(const IndexParams& p, int rank, int max_new, int max_e
   // prefixes fit it in any case (tpc * 128 entries: at most 8 bits of ring per entry)
   const size_t stage_bytes = (size_t)(TcSmem<16, 4>::kSelAll - TcSmem<16, 4>::kA);   // the same for every variant
   plan.merge_inline = fused && (size_t)plan.runs * k * 8 <= stage_bytes;
-  plan.merge_smem = sizeof(SelScratch<256>) + (size_t)(kMaxRuns + 4) * 4 + (size_t)plan.runs * k * 16;
-  if (fused && (size_t)plan.tpc * kTile / 32 * 8 > stage_bytes) plan.applies = 0;
+  plan.merge_smem = (size_t)kMergeStage + (size_t)plan.runs * k * 8;
+  if (fused && (size_t)plan.tpc * kTile / 32 * 8 > (size_t)(TcSmem<16, 4>::kHist - TcSmem<16, 4>::kA)) plan.applies = 0;
   if (fused && !plan.merge_inline && plan.merge_smem > 227 * 1024) plan.applies = 0;
   return plan;
 }

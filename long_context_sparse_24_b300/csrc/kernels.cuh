@@ -57,9 +57,11 @@ struct CompressParams {
 // ticket[b] counts the sequence's finished runs (zero between calls).
 struct TopkRuns {
   int runs;
-  int* cnt;
-  uint64_t* keys;
+  int* cnt;         // [T][runs] keys in each run's list
+  uint64_t* tau;    // [T][runs] the run's selection threshold (0 when it kept every candidate)
+  uint64_t* keys;   // [T][runs][k] each run's list, ascending entry index
   int* ticket;
+  uint64_t* gthr;   // [T] the query's threshold shared by its runs (zero between calls), or null
 };
 
 struct IndexParams {

@@ -15,7 +15,7 @@
 // call before any stream capture starts.
 //
 // All calls share the one array, which keeps whatever the previous call left in it.  Its leading
-// per-sequence counters must be zero when a call starts: the array is zero when the library's
+// per-sequence counters and per-query thresholds must be zero when a call starts: the array is zero when the library's
 // module is loaded, and every call that completes leaves them at zero again (on the path that
 // writes every score instead, the histograms are cleared by a memset of this array, which is not
 // an allocation).  A call with LCS_INDEX_SELECT_ONLY reads what the last LCS_INDEX_SCORE_ONLY call

@@ -57,55 +57,35 @@ struct SelScratch {
   unsigned long long span[2 * (NT / 32)];   // per-warp max / min of the keys
 };
 
-// Adds one to hist[bin] for every lane that passes `take`, one shared atomic per distinct bin of
-// the warp (keys of a selection often share their leading digits: per-lane atomics on one address
-// would serialise).  The whole warp must call.
-__device__ __forceinline__ void warp_hist_add(bool take, uint32_t bin, uint32_t* hist) {
-  const unsigned act = __ballot_sync(0xffffffffu, take);
-  if (!take) return;
-  const unsigned same = __match_any_sync(act, bin);
-  if ((threadIdx.x & 31) == (unsigned)(__ffs(same) - 1)) atomicAdd(&hist[bin], (uint32_t)__popc(same));
-}
-
-// Key sources for the selection: groups of keys, count(g) keys in group g.
-struct SmemKeys {            // one array
-  const uint64_t* buf;
-  int n;
-  __device__ __forceinline__ int groups() const { return 1; }
-  __device__ __forceinline__ int count(int) const { return n; }
-  __device__ __forceinline__ uint64_t key(int, int i) const { return buf[i]; }
-};
-struct RunLists {            // lists of up to `stride` keys each, counts in shared memory
-  const uint64_t* keys;      // global, written by other CTAs of the grid: read through L2
-  const int* cnt;
-  int lists;
-  int stride;
-  __device__ __forceinline__ int groups() const { return lists; }
-  __device__ __forceinline__ int count(int g) const { return cnt[g]; }
-  __device__ __forceinline__ uint64_t key(int g, int i) const {
-    return __ldcg(reinterpret_cast<const unsigned long long*>(keys) + (long long)g * stride + i);
-  }
+// The outcome of a selection: the keys at or above tau are taken, `count` of them.
+struct SelResult {
+  uint64_t tau;
+  int count;
 };
 
-// The threshold tau with exactly k of the source's keys >= tau (k <= number of keys; keys
-// unique).  Most-significant-digit radix selection, 8 bits per pass, stopping as soon as the digit
-// bin that holds the k-th key is taken whole (with unique keys that happens at the last digit at
-// the latest).
-template <int NT, int ID, typename Src>
-__device__ uint64_t kth_largest_key(int k, const Src& src, SelScratch<NT>& sc) {
-  static_assert(NT >= 256, "one bin per thread");
+// Most-significant-digit radix selection over the keys of buf[0..n) at or above lo (shared memory,
+// unique keys; with fewer than k of them at or above lo, all of those: {lo, their count}):
+// BITS-bit digits, the first one ending at the highest bit in which the largest and the smallest
+// key differ (the leading bits every key shares need no pass).  A level counts the keys under the
+// current prefix per digit value, finds the digit bin that holds the k-th largest key and stops
+// once the keys at or above that bin's lower edge number at most k + slack; else the bin becomes
+// the prefix of the next level.  slack = 0 gives the exact selection (count == k); with unique
+// keys the last level's bins hold one key each, so the loop ends there at the latest.  hist: 1 <<
+// BITS counters of shared memory, left at zero.
+template <int NT, int ID, int BITS>
+__device__ SelResult select_top(const uint64_t* buf, int n, int k, int slack, SelScratch<NT>& sc, uint32_t* hist,
+                                uint64_t lo = 0ull) {
+  constexpr int B = 1 << BITS;
+  constexpr int PER = (B + NT - 1) / NT;   // bins a thread scans, in descending order
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // the leading bits all keys share need no pass: start at the byte of the highest bit in which
-  // the largest and the smallest key differ
   unsigned long long kmax = 0ull, kmin = ~0ull;
-  for (int g = 0; g < src.groups(); ++g) {
-    const int n = src.count(g);
-    for (int i = tid; i < n; i += NT) {
-      const unsigned long long u = src.key(g, i);
-      kmax = u > kmax ? u : kmax;
-      kmin = u < kmin ? u : kmin;
-    }
+  for (int i = tid; i < n; i += NT) {
+    const unsigned long long u = buf[i];
+    if (u < lo) continue;
+    kmax = u > kmax ? u : kmax;
+    kmin = u < kmin ? u : kmin;
   }
+  for (int i = tid; i < B; i += NT) hist[i] = 0u;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     const unsigned long long a = __shfl_xor_sync(0xffffffffu, kmax, o), b = __shfl_xor_sync(0xffffffffu, kmin, o);
@@ -122,38 +102,68 @@ __device__ uint64_t kth_largest_key(int k, const Src& src, SelScratch<NT>& sc) {
     kmax = sc.span[2 * w] > kmax ? sc.span[2 * w] : kmax;
     kmin = sc.span[2 * w + 1] < kmin ? sc.span[2 * w + 1] : kmin;
   }
-  if (kmax == kmin) return kmax;   // one key (k == 1)
-  int shift = (63 - __clzll((long long)(kmax ^ kmin))) & ~7;
-  uint64_t prefix = shift >= 56 ? 0ull : (kmax & (~0ull << (shift + 8)));
-  int remaining = k;
-  for (;; shift -= 8) {
-    const uint64_t hi = shift >= 56 ? 0ull : (~0ull << (shift + 8));
-    if (tid < 256) sc.hist[tid] = 0u;
+  group_sync<NT, ID>();   // (span is free again for the caller)
+  if (kmax < kmin) return SelResult{lo, 0};      // no key at or above lo
+  if (kmax == kmin) return SelResult{kmax, 1};   // one key
+  const int hb = 63 - __clzll((long long)(kmax ^ kmin));   // the highest bit in which keys differ
+  int width = hb + 1 < BITS ? hb + 1 : BITS;
+  int shift = hb + 1 - width;
+  uint64_t prefix = hb >= 63 ? 0ull : (kmax & (~0ull << (hb + 1)));
+  int above0 = 0;   // keys above the current prefix's range
+  for (;;) {
+    const uint64_t hi_mask = shift + width >= 64 ? 0ull : (~0ull << (shift + width));
+    const uint32_t dmask = (1u << width) - 1u;
+    for (int i = tid; i < n; i += NT) {
+      const uint64_t u = buf[i];
+      if (u >= lo && (u & hi_mask) == prefix) atomicAdd(&hist[(uint32_t)(u >> shift) & dmask], 1u);
+    }
     group_sync<NT, ID>();
-    for (int g = 0; g < src.groups(); ++g) {
-      const int n = src.count(g);
-      for (int i0 = 0; i0 < n; i0 += NT) {   // warp-uniform trip count: the whole warp adds
-        const int i = i0 + tid;
-        const uint64_t u = i < n ? src.key(g, i) : 0ull;
-        warp_hist_add(i < n && (u & hi) == prefix, (uint32_t)(u >> shift) & 255u, sc.hist);
+    // thread t scans bins B-1-t*PER down to B-(t+1)*PER
+    int c = 0;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      const int pos = tid * PER + j;
+      c += pos < B ? (int)hist[B - 1 - pos] : 0;
+    }
+    int tot;
+    const int incl = group_scan_incl<NT, ID>(c, sc.warp_tot, &tot);
+    if (above0 + tot < k) {   // (first level only: every key at or above lo is taken)
+      for (int i = tid; i < B; i += NT) hist[i] = 0u;
+      group_sync<NT, ID>();
+      return SelResult{lo, above0 + tot};
+    }
+    if (incl - c + above0 < k && incl + above0 >= k) {
+      int cum = above0 + incl - c;
+      for (int j = 0; j < PER; ++j) {
+        const int pos = tid * PER + j;
+        const int h = pos < B ? (int)hist[B - 1 - pos] : 0;
+        if (cum + h >= k) {
+          sc.found[0] = B - 1 - pos;
+          sc.found[1] = cum;
+          sc.found[2] = h;
+          break;
+        }
+        cum += h;
       }
     }
     group_sync<NT, ID>();
-    const int c = tid < 256 ? (int)sc.hist[255 - tid] : 0;   // bins in descending order
-    int tot;
-    const int incl = group_scan_incl<NT, ID>(c, sc.warp_tot, &tot);
-    if (tid < 256 && incl - c < remaining && incl >= remaining) {
-      sc.found[0] = 255 - tid;
-      sc.found[1] = incl - c;
-      sc.found[2] = c;
-    }
-    group_sync<NT, ID>();
     const int d = sc.found[0], above = sc.found[1], in_bin = sc.found[2];
+    for (int i = tid; i < B; i += NT) hist[i] = 0u;
     group_sync<NT, ID>();
     prefix |= (uint64_t)d << shift;
-    remaining -= above;
-    if (in_bin == remaining || shift == 0) return prefix;
+    if (above + in_bin <= k + slack || shift == 0) return SelResult{prefix, above + in_bin};
+    above0 = above;
+    width = shift < BITS ? shift : BITS;
+    shift -= width;
   }
+}
+
+// The threshold tau with exactly k of buf[0..n)'s keys >= tau (k <= n; keys unique); keys below
+// lo are left out (at least k keys at or above it).
+template <int NT, int ID, int BITS>
+__device__ __forceinline__ uint64_t kth_largest_key(const uint64_t* buf, int n, int k, SelScratch<NT>& sc,
+                                                    uint32_t* hist, uint64_t lo = 0ull) {
+  return select_top<NT, ID, BITS>(buf, n, k, 0, sc, hist, lo).tau;
 }
 
 // Appends `key` (where `take`) to buf at positions handed out by sc.count, one shared atomic per

@@ -122,12 +122,18 @@ def test_workspace_sizes():
     b = lcsa.lcs_batch(32, 0x1000, 0x2000, 32, 1, 131072)
     n = lcsa._lib.lcs_index_topk_workspace(ctypes.byref(b), 4, ctypes.byref(keys), ctypes.byref(pg), 4, 512)
     assert 32 * 512 * 8 <= n < 32 * (131072 // 4) * 4
-    assert lcsa._lib.lcs_index_topk_workspace_zeroed(ctypes.byref(b)) == 256
-    # a prefill chunk at rank 128: query groups, still lists of k keys per query and run
+    # zero between calls: a ticket (int32) and a shared threshold (u64) per sequence and query
+    assert lcsa._lib.lcs_index_topk_workspace_zeroed(ctypes.byref(b)) == 256 + 256
+    # up to 16 queries per sequence at rank 128: query groups, still lists of k keys per query and run
+    b = lcsa.lcs_batch(64, 0x1000, 0x2000, 1024, 16, 131072)
+    n = lcsa._lib.lcs_index_topk_workspace(ctypes.byref(b), 4, ctypes.byref(keys), ctypes.byref(pg), 4, 512)
+    assert 1024 * 512 * 8 <= n < 1024 * (131072 // 4) * 4
+    assert lcsa._lib.lcs_index_topk_workspace_zeroed(ctypes.byref(b)) == 1024 * 4 + 1024 * 8
+    # a prefill chunk: the prefill scorer writes every score key (4 bytes per query and visible entry)
     b = lcsa.lcs_batch(1, 0x1000, 0x2000, 2048, 2048, 131072)
     n = lcsa._lib.lcs_index_topk_workspace(ctypes.byref(b), 4, ctypes.byref(keys), ctypes.byref(pg), 4, 512)
-    assert 2048 * 512 * 8 <= n < 2048 * (131072 // 4) * 4
-    assert lcsa._lib.lcs_index_topk_workspace_zeroed(ctypes.byref(b)) == 2048 * 4
+    assert n >= 2048 * (131072 // 4) * 4
+    assert lcsa._lib.lcs_index_topk_workspace_zeroed(ctypes.byref(b)) == 2048 * 4 + 2048 * 8
     # rank 64: every score key of every (query, visible entry) pair
     keys64 = lcsa.lcs_index_keys(0x10000, 0x20000, 64, 32 * 32768)
     n = lcsa._lib.lcs_index_topk_workspace(ctypes.byref(b), 4, ctypes.byref(keys64), ctypes.byref(pg), 4, 512)

@@ -225,8 +225,9 @@ def _index_case(lengths, new, m, k, heads, rank, relu, scaled, seed=31, ties=Fal
     (2, 128, True, True, [3, 4, 1], [37, 600, 2100]),
     (8, 128, False, True, [1, 1, 1], [37, 600, 2100]),
     (8, 128, False, True, [2, 1, 2], [300, 4600, 2100]),
-    # longer runs of queries at rank 128: tensor-core prefill scorer (groups of 16 queries, 8 at
-    # Hi = 8; ragged last groups; causal limits inside a tile; runs of 256 tiles)
+    # longer runs of queries at rank 128: up to 16 per sequence, the fused scorer in groups of up
+    # to 4 queries; beyond, the tensor-core prefill scorer (groups of 16 queries, 8 at Hi = 8;
+    # ragged last groups; causal limits inside a tile; runs of 256 tiles) and the select kernel
     (4, 128, False, True, [1, 5, 40], [37, 600, 2100]),
     (2, 128, True, True, [2, 1, 9], [37, 600, 2100]),
     (4, 128, False, True, [17, 40, 33], [600, 2100, 5000]),
@@ -235,6 +236,11 @@ def _index_case(lengths, new, m, k, heads, rank, relu, scaled, seed=31, ties=Fal
     (8, 128, False, True, [9, 20, 5], [37, 600, 2100]),
     (8, 128, True, True, [3, 24, 7], [37, 600, 2100]),
     (4, 128, False, True, [5, 21], [600, 140000]),
+    (4, 128, False, True, [5, 12], [600, 140000]),
+    # long sequences: 14 to 27 tiles per CTA, so that the stage, block-scale and accumulator rings
+    # all wrap several times under random scores
+    (4, 128, False, True, [1, 3], [600000, 1000000]),
+    (2, 128, True, True, [1, 1], [1000000, 300000]),
     # rank 64: warp-MMA scorer
     (1, 64, False, False, [1, 7, 33], [37, 600, 2100]),
     (8, 64, False, True, [1, 3, 17], [37, 600, 2100]),
