@@ -37,6 +37,47 @@ TRAFFIC = {"source_sha1": None, "attend": None, "index": None}
 UNIT = "queries/s"
 
 
+# measured after the headline by default: the other configurations and the tensor-pipe probe
+OTHER_WORKLOADS = ("csa_decode_1m", "hca_decode", "mixed_decode", "csa_prefill", "compress_1m", "tensor_peak")
+
+
+def run_others(args):
+    """The other workloads, each as `bench.py --workload W` in a child process on this GPU (no
+    torchrun variables: a plain one-GPU run), their JSON lines condensed for the headline line."""
+    import subprocess
+    names = OTHER_WORKLOADS if args.others == "auto" else tuple(w for w in args.others.split(",") if w)
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "LOCAL_WORLD_SIZE", "MASTER_ADDR", "MASTER_PORT",
+                        "GROUP_RANK", "ROLE_RANK", "TORCHELASTIC_RUN_ID")}
+    out = {}
+    for w in names:
+        cmd = [sys.executable, os.path.abspath(__file__), "--workload", w, "--steps", str(min(args.steps, 10)),
+               "--warmup", str(max(3, min(args.warmup, 5))), "--no-cpu-baseline", "--others", "none"]
+        try:
+            r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=600)
+            lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+            if r.returncode != 0 or not lines:
+                out[w] = {"error": f"exit {r.returncode}: {(r.stderr or '').strip().splitlines()[-1:]}"}
+                continue
+            d = json.loads(lines[-1])
+            keep = {k: d.get(k) for k in ("metric", "value", "unit", "ms_per_step", "steps", "warmup", "dtype",
+                                          "gpu_launches", "device_status_ok")}
+            keep["workload"] = (d.get("config") or {}).get("workload")
+            rf = d.get("roofline") or {}
+            keep["roofline"] = {k: rf.get(k) for k in ("kernel", "bound", "achieved", "peak", "unit", "frac")}
+            if d.get("roofline_step"):
+                rs = d["roofline_step"]
+                keep["roofline_step"] = {k: rs.get(k) for k in ("achieved", "peak", "unit", "frac")}
+            if d.get("rates"):
+                keep["rates"] = d["rates"]
+            ck = d.get("clocks") or {}
+            keep["clocks"] = {k: ck.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons")}
+            out[w] = keep
+        except Exception as e:   # a failed extra line never costs the headline
+            out[w] = {"error": repr(e)[:200]}
+    return out
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -55,6 +96,10 @@ def parse():
                          "the same kernels, for profiler captures; the line then names the changed workload)")
     ap.add_argument("--new-tokens", type=int, default=None,
                     help="csa_prefill only: new tokens (queries) instead of the workload's 16,384")
+    ap.add_argument("--others", default="auto",
+                    help="comma-separated workloads measured after the headline (csa_decode, one GPU only), each "
+                         "in a process of its own, and summarised in the headline line under 'other_workloads'; "
+                         "'auto': " + ",".join(OTHER_WORKLOADS) + "; 'none': the headline alone")
     return ap.parse_args()
 
 
@@ -1132,6 +1177,8 @@ def main():
                 "gpu_launches": res["launches"], "device_status_ok": res["status_ok"]}
         if not args.no_cpu_baseline and world == 1 and wl is WL:
             line["cpu_baseline"] = cpu_baseline()
+        if world == 1 and wl is WL and args.others != "none":
+            line["other_workloads"] = run_others(args)
         print(json.dumps(line))
 
 

@@ -344,10 +344,12 @@ uint32_t lcs_set_wait_polls(uint32_t polls);
 
 /* --- tensor-pipe throughput probe (measurement; not a step of the method) ---------------------
  * Launches `ctas` CTAs (one per SM is the intended use) that each issue mmas_per_cta tcgen05 MMAs of
- * M = 128, N = 256 back to back from shared memory into tensor memory: kind 0 = kind::f8f6f4 with
- * E2M1 operands, K = 32 (the indexer's MMA); kind 1 = kind::f16 with F16 operands, K = 16 (the
- * attention's MMA).  The caller times the launch and divides 2 * 128 * 256 * K * mmas_per_cta * ctas
- * by the time.  mmas_per_cta >= 64.  Errors: LCS_ERR_UNSUPPORTED for other kinds or sizes. */
+ * M = 128 back to back from shared memory into tensor memory: kind 0 = kind::f8f6f4 with E2M1
+ * operands, N = 256, K = 32 (the indexer's MMA); kind 1 = kind::f16 with F16 operands, N = 256,
+ * K = 16 (the attention's MMA); kind 2 = kind::mxf4, block-scaled E2M1 operands packed two codes a
+ * byte with a UE8M0 scale per 32 codes, N = 240, K = 64.  The caller times the launch and divides
+ * 2 * 128 * N * K * mmas_per_cta * ctas by the time.  mmas_per_cta >= 64.  Errors:
+ * LCS_ERR_UNSUPPORTED for other kinds or sizes. */
 lcs_status lcs_mma_probe(int32_t kind, int32_t mmas_per_cta, int32_t ctas, int32_t* dev_status, void* stream);
 
 /* --- library information -------------------------------------------------------------------- */

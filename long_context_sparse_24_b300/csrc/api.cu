@@ -64,7 +64,6 @@ struct SplitPlan {
   int tc;
   int entry_splits;   // tensor-core plan: 128-row tiles of entries; one more split for the window
   int window_apart;   // tensor-core plan: the window rows form their own split (CSA, few queries)
-  int hg;             // tensor-core plan: query heads per CTA
 };
 
 // The tensor-core attention takes FP8-split rows of D = 512 (the only D = 512 format), heads in
@@ -79,24 +78,12 @@ SplitPlan plan_splits(const lcs_batch* b, int heads, int dim, int max_rows, bool
   if (attend_tc_applies(heads, dim)) {
     const int sms = num_sms();
     const long long ctas = std::max<long long>(1, (long long)b->total_new * ((heads + 63) / 64));
-    // CSA with few queries (64-head groups would leave most SMs idle): 16 heads per CTA, every CTA
-    // one query's whole row list (entries then window) for its heads -- the four head groups of a
-    // query read the same rows, from L2 after the first -- cut into runs of tiles only when the
-    // groups alone still leave SMs idle
-    if (window_split && heads % 16 == 0 && max_rows <= kAttendTcMaxRows && ctas * 2 <= sms) {
-      const long long ctas16 = (long long)b->total_new * (heads / 16);
-      const int tiles = std::max(1, (max_rows + 127) / 128);
-      const int want = (int)std::max<long long>(1, std::min<long long>(tiles, sms / std::max<long long>(1, ctas16)));
-      const int tps = (tiles + want - 1) / want;
-      const int splits = (tiles + tps - 1) / tps;
-      return SplitPlan{splits, 128 * tps, 1, splits, 0, 16};
-    }
     const int per_query = (int)std::max<long long>(1, sms / ctas);   // CTAs per (query, head group)
     if (window_split && per_query > 1 && max_rows <= kAttendTcMaxRows) {
       const int tiles = std::max(1, (max_rows - LCSA_WINDOW + 127) / 128);
       const int es = std::min(tiles, per_query);
       const int tps = (tiles + es - 1) / es;
-      return SplitPlan{(tiles + tps - 1) / tps + 1, 128 * tps, 1, (tiles + tps - 1) / tps, 1, 64};
+      return SplitPlan{(tiles + tps - 1) / tps + 1, 128 * tps, 1, (tiles + tps - 1) / tps, 1};
     }
     // one list per query: cut it into runs of tps tiles so that all (query, head group) runs
     // together come to about one tile load per SM (the last run of a query may be shorter;
@@ -105,11 +92,11 @@ SplitPlan plan_splits(const lcs_batch* b, int heads, int dim, int max_rows, bool
     const long long units = ctas * tiles;
     const int tps = (int)std::min<long long>(tiles, std::max<long long>(1, (units + num_sms() - 1) / num_sms()));
     const int splits = (tiles + tps - 1) / tps;
-    return SplitPlan{splits, 128 * tps, 1, splits, 0, 64};
+    return SplitPlan{splits, 128 * tps, 1, splits, 0};
   }
   const int hg = heads <= 16 ? 1 : (heads + 63) / 64;
   const long long base = (long long)b->total_new * hg;
-  SplitPlan s{1, max_rows > 0 ? max_rows : 1, 0, 0, 0, 0};
+  SplitPlan s{1, max_rows > 0 ? max_rows : 1, 0, 0, 0};
   const int sms = num_sms();
   if (base <= 0 || base >= sms || max_rows <= 64) return s;
   int want = (int)(sms / base);
@@ -333,7 +320,6 @@ lcs_status attend_common(const lcs_batch* batch, const void* q, int32_t heads, c
   p.tc = plan.tc;
   p.entry_splits = plan.entry_splits;
   p.window_split = plan.window_apart;
-  p.hg = plan.hg;
   p.wait_polls = g_wait_polls.load(std::memory_order_relaxed);
   if (plan.splits > 1) {
     const size_t per = (size_t)batch->total_new * heads * plan.splits;

@@ -58,7 +58,7 @@ struct TcAttSmem {
   static constexpr int kRinv = kScale + 2 * kTileRows * 4;  // f32 [2][128]   1 / s_r
   // row descriptors: 64 heads, a ring of three tiles (t, t+1, t+2) resolved two tiles ahead; 16
   // heads (shared memory to spare), every tile of the CTA's rows resolved up front
-  static constexpr int kDescTiles = HG == 16 ? (kAttendTcMaxRows + kTileRows - 1) / kTileRows : 3;
+  static constexpr int kDescTiles = 3;                       // ring of three tiles' descriptors
   static constexpr int kDesc = kRinv + 2 * kTileRows * 4;   // long long [kDescTiles][128]
   static constexpr int kRed = kDesc + kDescTiles * kTileRows * 8;   // f32 [4 warps][HG] per-head partials
   static constexpr int kM = kRed + 4 * HG * 4;              // f32 [HG] running max (base 2)
@@ -223,10 +223,6 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
     return;
   }
   const int ntiles = (r_end - r_begin + kTileRows - 1) / kTileRows;
-  if (ntiles > L::kDescTiles && HG == 16) {   // more rows than the plan allows for (cannot happen)
-    if (tid == 0) report(p.status, LCS_ERR_DEVICE_GUARD);
-    return;
-  }
 
   long long* desc = reinterpret_cast<long long*>(smem + L::kDesc);
   float* sscale = reinterpret_cast<float*>(smem + L::kScale);
@@ -284,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
   uint4 cv[kNP];
   uint4 rv[kRP];
   float sc = 0.0f;                                   // threads 0-127: the scale of row tid
-  auto dslot = [&](int tt) { return HG == 16 ? tt : tt % 3; };
+  auto dslot = [&](int tt) { return tt % 3; };
   // issue the loads of tile tt (descriptors in desc[dslot(tt)]) into registers
   auto load_tile = [&](int tt) {
     const long long* dd = desc + dslot(tt) * kTileRows;
@@ -321,9 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
     }
   };
 
-  if (HG == 16) {
-    for (int i = tid; i < ntiles * kTileRows; i += kThreads) desc[i] = make_desc(i >> 7, i & 127);
-  } else if (tid < kTileRows) {
+  if (tid < kTileRows) {
     desc[tid] = make_desc(0, tid);
   } else if (ntiles > 1) {
     desc[tid] = make_desc(1, tid - kTileRows);   // tile 1 in desc[1]
@@ -391,26 +385,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
       }
       *reinterpret_cast<uint4*>(smem + L::kT + r * 128 + ((j ^ (r & 7)) << 4)) = h;
     }
-    // the next tile's rows go out now and fly while this tile computes; with every descriptor
-    // resolved up front (16 heads) the tile after it is fetched into L2 meanwhile
+    // the next tile's rows go out now and fly while this tile computes
     if (tt + 1 < ntiles) load_tile(tt + 1);
-    if (HG == 16 && tt + 2 < ntiles) {
-      // 128 rows x (448 code bytes + 128 RoPE bytes): 3.5 + 1 lines of 128 bytes a row
-      for (int x = tid; x < kTileRows * 5; x += kThreads) {
-        const int r = x / 5, part = x % 5;
-        const long long d = desc[(tt + 2) * kTileRows + r];
-        if (d < 0) continue;
-        const int kind = (int)(d >> 60);
-        const long long rw = d & ((1ll << 60) - 1);
-        if (part < 4) {
-          const uint8_t* src = (kind == 1 ? p.new_rows.nope : (kind == 2 ? p.window.nope : p.entries.nope));
-          prefetch_l2(src + rw * kNopeBytes + part * 128);
-        } else {
-          const __nv_bfloat16* src = (kind == 1 ? p.new_rows.rope : (kind == 2 ? p.window.rope : p.entries.rope));
-          prefetch_l2(src + rw * kRope);
-        }
-      }
-    }
     if (tt == 0) {
       cp_async_wait<0>();
       __syncthreads();
@@ -438,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
     const bool hw_lane = scatter_writer<HG>(lane);
     const bool rvalid = warp < 4 && r < trows && desc[dslot(tt) * kTileRows + (r & 127)] >= 0;
     if (warp >= 4) {
-      if (HG != 16 && tt + 2 < ntiles) desc[((tt + 2) % 3) * kTileRows + tid - 128] = make_desc(tt + 2, tid - 128);
+      if (tt + 2 < ntiles) desc[((tt + 2) % 3) * kTileRows + tid - 128] = make_desc(tt + 2, tid - 128);
     } else {
       ok = mbar_wait(bar_s, tt & 1, p.status, nullptr, p.wait_polls) && ok;
       ok = __all_sync(0xffffffffu, ok);
@@ -634,7 +610,6 @@ cudaError_t launch_attend_tc_t(const AttendParams& p, int total_new, cudaStream_
 }  // namespace
 
 cudaError_t launch_attend_tc(const AttendParams& p, int total_new, cudaStream_t st) {
-  if (p.hg == 16) return launch_attend_tc_t<16>(p, total_new, st);
   if (p.rows_per_split == kTileRows) return launch_attend_tc1(p, total_new, st);   // one tile per CTA
   return launch_attend_tc_t<64>(p, total_new, st);
 }

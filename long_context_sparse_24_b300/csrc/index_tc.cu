@@ -151,15 +151,16 @@ __device__ int write_run_sorted(const uint64_t* buf, int n, uint64_t tau, int j0
 // the merge kernel).  Group of NT threads (ID 0: the whole CTA).  Every run list is sorted by entry
 // index and the runs cover increasing index ranges, so the lists read one after the other are
 // sorted too: they are staged in shared memory (stage: room for stage_cap keys), the k-th largest
-// key is selected there, and the keys at or above it are read out in that order.  A run whose list
-// is full recorded the threshold of its own k keys; the largest of those bounds the query's k-th
-// largest key from below, so the selection looks only at the staged keys at or above it.  N:
-// visible entries of the query; run_off: runs + 1 ints of shared memory; hist: 1 << BITS counters
-// of shared memory.
+// key is selected, and the staged keys at or above it are read out in that order.  Every run
+// recorded a threshold at most the query's k-th largest key, with all of its keys at or above it
+// in its list; the largest of those bounds the selection from below, so the keys at or above it
+// are gathered as candidates while staging (cand: room for cand_cap keys; when more pass, the
+// selection runs over the stage).  N: visible entries of the query; run_off: runs + 1 ints of
+// shared memory; hist: 1 << BITS counters of shared memory.
 template <int NT, int ID, int BITS>
 __device__ void merge_query_topk(const TopkRuns& tr, long long q, int N, int k, uint64_t* stage, int stage_cap,
-                                 int* run_off, uint32_t* hist, int32_t* out_idx, int32_t* out_cnt,
-                                 SelScratch<NT>& sc) {
+                                 uint64_t* cand, int cand_cap, int* run_off, uint32_t* hist, int32_t* out_idx,
+                                 int32_t* out_cnt, SelScratch<NT>& sc) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int32_t* out = out_idx + q * k;
   if (N <= k) {   // every visible entry
@@ -168,7 +169,7 @@ __device__ void merge_query_topk(const TopkRuns& tr, long long q, int N, int k, 
     return;
   }
   const int* cnts = tr.cnt + q * tr.runs;
-  const uint64_t* keys = tr.keys + q * (long long)tr.runs * k;
+  const unsigned long long* keys = reinterpret_cast<const unsigned long long*>(tr.keys) + q * (long long)tr.runs * k;
   // list offsets in the stage, and the bound: the largest threshold of the runs (runs <= 256 <= NT)
   uint64_t bound;
   {
@@ -184,7 +185,10 @@ __device__ void merge_query_topk(const TopkRuns& tr, long long q, int N, int k, 
     int tot;
     const int incl = group_scan_incl<NT, ID>(c, sc.warp_tot, &tot);   // (its barriers publish span)
     if (tid < tr.runs) run_off[tid] = incl - c;
-    if (tid == 0) run_off[tr.runs] = tot;
+    if (tid == 0) {
+      run_off[tr.runs] = tot;
+      sc.count = 0;
+    }
     unsigned long long bmax = 0ull;
 #pragma unroll
     for (int w = 0; w < NT / 32; ++w) bmax = sc.span[w] > bmax ? sc.span[w] : bmax;
@@ -192,29 +196,44 @@ __device__ void merge_query_topk(const TopkRuns& tr, long long q, int N, int k, 
   }
   group_sync<NT, ID>();
   const int total = min(run_off[tr.runs], stage_cap);   // (the host sizes the stage for every list)
-  // stage the lists: eight independent loads in flight per thread
-  for (int x0 = tid; x0 < total; x0 += 8 * NT) {
-    uint64_t v[8];
+  // stage the lists, a warp per run (16 loads in flight per lane), and gather the candidates
+  constexpr int kU = 16;
+  for (int r = warp; r < tr.runs; r += NT / 32) {
+    const int o = run_off[r];
+    const int c = min(run_off[r + 1], total) - o;
+    const unsigned long long* src = keys + (long long)r * k;
+    for (int x0 = 0; x0 < c; x0 += 32 * kU) {
+      uint64_t v[kU];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int x = x0 + u * NT;
-      v[u] = 0ull;
-      if (x < total) {
-        int lo = 0, hi = tr.runs - 1;   // the run holding stage position x
-        while (lo < hi) {
-          const int mid = (lo + hi + 1) >> 1;
-          if (run_off[mid] <= x) lo = mid; else hi = mid - 1;
+      for (int u = 0; u < kU; ++u) {
+        const int x = x0 + u * 32 + lane;
+        v[u] = x < c ? __ldcg(src + x) : 0ull;
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int x = x0 + u * 32 + lane;
+        if (x < c) stage[o + x] = v[u];
+        const bool take = x < c && v[u] >= bound;
+        const unsigned m = __ballot_sync(0xffffffffu, take);
+        if (m != 0u) {
+          const int leader = __ffs(m) - 1;
+          int base = 0;
+          if (lane == leader) base = atomicAdd(&sc.count, __popc(m));
+          base = __shfl_sync(0xffffffffu, base, leader);
+          const int at = base + __popc(m & ((1u << lane) - 1u));
+          if (take && at < cand_cap) cand[at] = v[u];
         }
-        v[u] = __ldcg(reinterpret_cast<const unsigned long long*>(keys) + (long long)lo * k + (x - run_off[lo]));
       }
     }
-#pragma unroll
-    for (int u = 0; u < 8; ++u)
-      if (x0 + u * NT < total) stage[x0 + u * NT] = v[u];
   }
   group_sync<NT, ID>();
+  const int nc = sc.count;
+  group_sync<NT, ID>();
   // (fewer than k keys only when the scoring gave up on a bounded wait: take them all)
-  const uint64_t tau = total <= k ? 0ull : kth_largest_key<NT, ID, BITS>(stage, total, k, sc, hist, bound);
+  uint64_t tau = 0ull;
+  if (total > k)
+    tau = nc <= cand_cap ? kth_largest_key<NT, ID, BITS>(cand, nc, k, sc, hist)
+                         : kth_largest_key<NT, ID, BITS>(stage, total, k, sc, hist, bound);
   // ascending read-out: thread t takes stage positions [t*ppt, (t+1)*ppt)
   const int ppt = (total + NT - 1) / NT;
   const int x0 = min(total, tid * ppt), x1 = min(total, x0 + ppt);
@@ -607,18 +626,22 @@ __global__ void __launch_bounds__(kThreads, QH >= 16 ? 1 : 2) index_tc_kernel(co
     __threadfence();
     uint64_t* stage = reinterpret_cast<uint64_t*>(smem + L::kA);   // the ring is idle now
     int* run_off = reinterpret_cast<int*>(smem + L::kRunOff);
+    // (the candidate buffers are idle now: they hold the selection's histogram, 2048 bins when
+    // there is room for them beside the gathered candidates, else 256 in the scratch)
+    constexpr int kHistBytes = 2048 * 4;
+    const int region = QPS * cap * 8;
 #pragma unroll 1
-    for (int qi = 0; qi < qn; ++qi)
-      // (the candidate buffers are idle now: with room for them, the selection's histogram has
-      // 2048 bins there, else 256 in the scratch)
-      if (QPS * cap * 8 >= 2048 * 4)
+    for (int qi = 0; qi < qn; ++qi) {
+      if (region >= kHistBytes + 8 * 1024)
         merge_query_topk<kThreads, 0, 11>(p.runs, qrow0 + qi, (n0 + qi + 1) >> mshift, k, stage,
-                                          (L::kSelAll - L::kA) / 8, run_off, reinterpret_cast<uint32_t*>(cand_s),
+                                          (L::kSelAll - L::kA) / 8, cand_s + kHistBytes / 8,
+                                          (region - kHistBytes) / 8, run_off, reinterpret_cast<uint32_t*>(cand_s),
                                           p.out_idx, p.out_cnt, sel_all);
       else
         merge_query_topk<kThreads, 0, 8>(p.runs, qrow0 + qi, (n0 + qi + 1) >> mshift, k, stage,
-                                         (L::kSelAll - L::kA) / 8, run_off, sel_all.hist, p.out_idx, p.out_cnt,
-                                         sel_all);
+                                         (L::kSelAll - L::kA) / 8, cand_s, region / 8, run_off, sel_all.hist,
+                                         p.out_idx, p.out_cnt, sel_all);
+    }
     if (tid == 0) {   // left at zero for the next call
       p.runs.ticket[(long long)b * gridDim.y + blockIdx.y] = 0;
       if (p.runs.gthr != nullptr)
@@ -627,7 +650,8 @@ __global__ void __launch_bounds__(kThreads, QH >= 16 ? 1 : 2) index_tc_kernel(co
   }
 }
 
-// the merge kernel's shared memory: scratch, histogram, run offsets, then room for the lists
+// the merge kernel's shared memory: scratch, histogram, run offsets, then room for the lists and
+// as many candidates
 constexpr int kMergeHist = ((int)sizeof(SelScratch<256>) + 15) / 16 * 16;
 constexpr int kMergeRunOff = kMergeHist + 2048 * 4;
 constexpr int kMergeStage = kMergeRunOff + (kMaxRuns + 4) * 4;
@@ -644,8 +668,9 @@ __global__ void __launch_bounds__(256) topk_merge_kernel(IndexParams p) {
   int* run_off = reinterpret_cast<int*>(merge_smem + kMergeRunOff);
   uint64_t* stage = reinterpret_cast<uint64_t*>(merge_smem + kMergeStage);
   const int t = sp.n0() + i;
-  merge_query_topk<256, 0, 11>(p.runs, sp.q0 + i, (t + 1) / p.m, p.top_k, stage, p.runs.runs * p.top_k, run_off,
-                               hist, p.out_idx, p.out_cnt, sc);
+  const int lists = p.runs.runs * p.top_k;
+  merge_query_topk<256, 0, 11>(p.runs, sp.q0 + i, (t + 1) / p.m, p.top_k, stage, lists, stage + lists, lists,
+                               run_off, hist, p.out_idx, p.out_cnt, sc);
   if (threadIdx.x == 0 && p.runs.gthr != nullptr) p.runs.gthr[sp.q0 + i] = 0ull;   // left at zero
 }
 
@@ -771,7 +796,7 @@ IndexTcPlan plan_index_tc(const IndexParams& p, int rank, int max_new, int max_e
   // prefixes fit it in any case (tpc * 128 entries: at most 8 bits of ring per entry)
   const size_t stage_bytes = (size_t)(TcSmem<16, 4>::kSelAll - TcSmem<16, 4>::kA);   // the same for every variant
   plan.merge_inline = fused && (size_t)plan.runs * k * 8 <= stage_bytes;
-  plan.merge_smem = (size_t)kMergeStage + (size_t)plan.runs * k * 8;
+  plan.merge_smem = (size_t)kMergeStage + (size_t)plan.runs * k * 16;
   if (fused && (size_t)plan.tpc * kTile / 32 * 8 > (size_t)(TcSmem<16, 4>::kHist - TcSmem<16, 4>::kA)) plan.applies = 0;
   if (fused && !plan.merge_inline && plan.merge_smem > 227 * 1024) plan.applies = 0;
   return plan;

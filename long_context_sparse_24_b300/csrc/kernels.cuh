@@ -119,7 +119,6 @@ struct AttendParams {
   int entry_splits;          // tensor-core kernel: splits over the entries; split entry_splits = window
   int part;                  // tensor-core kernel: 0 every split, 1 the window split only, 2 the entry splits
   int window_split;          // tensor-core kernel: 1 the window rows form split entry_splits (CSA)
-  int hg;                    // tensor-core kernel: query heads per CTA (16 or 64)
   uint32_t wait_polls;       // bound of every mbarrier wait (polls of up to ~1 us)
   int32_t* status;
 };

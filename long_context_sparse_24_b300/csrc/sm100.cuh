@@ -150,6 +150,25 @@ __host__ __device__ constexpr uint32_t idesc_f8f6f4(uint32_t fmt_a, uint32_t fmt
   return (1u << 4) | (fmt_a << 7) | (fmt_b << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
+// Shared-memory matrix descriptor, K-major operand with the 64-byte swizzle: rows of 64 bytes
+// (128 packed FP4 codes), groups of 8 rows 512 bytes apart, atoms 512-byte aligned.
+__device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);         // start address
+  d |= (uint64_t)1u << 16;                         // leading byte offset (unused for swizzled K-major)
+  d |= (uint64_t)(512u >> 4) << 32;                // stride byte offset: 8 rows x 64 B
+  d |= (uint64_t)1u << 46;                         // descriptor version (sm_100 family)
+  d |= (uint64_t)4u << 61;                         // layout: 64-byte swizzle
+  return d;
+}
+
+// Instruction descriptor of kind::mxf4 (block-scaled: E2M1 x E2M1 with a UE8M0 scale per 32
+// codes, fp32 accumulation, K = 64 per instruction), both operands K-major, scale-factor data
+// IDs 0.
+__host__ __device__ constexpr uint32_t idesc_mxf4(uint32_t M, uint32_t N) {
+  return (1u << 7) | (1u << 10) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24);
+}
+
 // Instruction descriptor of kind::f16 with fp32 accumulation: fmt 0 F16, 1 BF16.
 __host__ __device__ constexpr uint32_t idesc_f16(uint32_t fmt, uint32_t M, uint32_t N) {
   return (1u << 4) | (fmt << 7) | (fmt << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
@@ -174,6 +193,24 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uin
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// Block-scaled D[tmem] (+)= (A . SFA)[smem] * (B . SFB)[smem]^T, scale factors in tensor memory
+// (two per row and instruction: one per 32 codes), issued by one thread.
+__device__ __forceinline__ void tc_mma_mxf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+      : "memory");
+}
+
+// Writes 4 consecutive 32-bit TMEM columns of this thread's lane, every column the same word.
+__device__ __forceinline__ void tmem_st4_fill(uint32_t taddr, uint32_t w) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%1,%1,%1};" ::"r"(taddr), "r"(w) : "memory");
 }
 
 // The barrier's next phase completes once every tcgen05 operation this thread issued before has.
