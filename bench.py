@@ -738,8 +738,9 @@ def run_gpu_prefill(args, rank, world, local, wl):
 
 def run_gpu_tensor_peak(args, rank, world, local):
     """The tensor-pipe rates the roofline fractions of the tensor-bound kernels are taken against:
-    lcs_mma_probe, one CTA per SM issuing back-to-back tcgen05 MMAs of M = 128, N = 256 (kind 0:
-    kind::f8f6f4 with E2M1 operands, the indexer's MMA; kind 1: kind::f16, the attention's MMA),
+    lcs_mma_probe, one CTA per SM issuing back-to-back tcgen05 MMAs of M = 128 (kind 0:
+    kind::f8f6f4 with E2M1 operands, N = 256; kind 1: kind::f16, N = 256, the attention's MMA;
+    kind 2: block-scaled kind::mxf4 with packed E2M1 operands, N = 240, the decode indexer's MMA),
     timed with CUDA events, best of the timed launches."""
     import torch
     import long_context_sparse_24_b300 as lcsa
@@ -753,8 +754,8 @@ def run_gpu_tensor_peak(args, rank, world, local):
     mmas = 16384
     out = {}
     with ClockSampler(local) as clk:
-        for kind, kstep, name in ((0, 32, "f8f6f4_e2m1"), (1, 16, "f16")):
-            flop = 2.0 * 128 * 256 * kstep * mmas * sms
+        for kind, n_, kstep, name in ((0, 256, 32, "f8f6f4_e2m1"), (1, 256, 16, "f16"), (2, 240, 64, "mxf4_e2m1")):
+            flop = 2.0 * 128 * n_ * kstep * mmas * sms
             times = []
             for it in range(args.warmup + args.steps):
                 e0 = torch.cuda.Event(enable_timing=True); e1 = torch.cuda.Event(enable_timing=True)
@@ -1098,14 +1099,15 @@ def main():
         res = run_gpu_tensor_peak(args, rank, world, local)
         if rank == 0:
             r = res["rates"]
-            print(json.dumps({"metric": "tcgen05 tensor-pipe rate (probe)", "value": r["f8f6f4_e2m1"]["tflops"],
+            print(json.dumps({"metric": "tcgen05 tensor-pipe rate (probe): block-scaled FP4", "value": r["mxf4_e2m1"]["tflops"],
                               "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-                              "ms_per_step": r["f8f6f4_e2m1"]["ms"], "higher_is_better": True, "scaling": "weak",
-                              "vs_baseline": None, "dtype": "e2m1 x e2m1 -> f32 (kind::f8f6f4)", "data": "synthetic",
-                              "config": {"workload": "tcgen05_mma_probe_m128_n256", "ctas": res["sms"],
+                              "ms_per_step": r["mxf4_e2m1"]["ms"], "higher_is_better": True, "scaling": "weak",
+                              "vs_baseline": None, "dtype": "e2m1 x e2m1 (ue8m0 per 32) -> f32 (kind::mxf4)",
+                              "data": "synthetic",
+                              "config": {"workload": "tcgen05_mma_probe_m128", "ctas": res["sms"],
                                          "mmas_per_cta": res["mmas"], "timing": "best of the timed launches"},
                               "rates": r, "clocks": res["clocks"], "e2e": None,
-                              "gpu_launches": 2 * args.steps, "device_status_ok": res["status_ok"]}))
+                              "gpu_launches": 3 * (args.warmup + args.steps), "device_status_ok": res["status_ok"]}))
         return
     if args.workload == "compress_1m":
         res = run_gpu_compress(args, rank, world, local)

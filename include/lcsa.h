@@ -193,7 +193,7 @@ lcs_status lcs_window_commit(const lcs_batch* batch, const lcs_state* state, int
  * are per-sequence counters and per-query thresholds that every completed call leaves at zero
  * again.  After a call whose device status is LCS_ERR_TIMEOUT, zero them again before reusing the
  * workspace.
- * How the work is split: at rank 128 with 1, 2, 4 or 8 heads, 2k + 256 <= 4096 and up to 16
+ * How the work is split: at rank 128 with 1, 2, 4 or 8 heads, 9k/8 + 256 <= 4096 and up to 16
  * queries per sequence, the scoring runs on the tensor cores with the top-k fused into it -- a CTA
  * scores a run of the cache for a group of up to 4 queries of a sequence and keeps each query's
  * best entries, the runs of a query share the best threshold any of them has reached, and the

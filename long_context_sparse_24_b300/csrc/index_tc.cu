@@ -9,37 +9,42 @@
 // Layout of the work.  A persistent, warp-specialised CTA scans a contiguous run of 128-entry
 // tiles of one sequence for all of that sequence's queries (QPS <= 4), through a ring of
 // shared-memory stages:
-//   warps 8-9 (producers, alternating tiles) look the run's pages up in the block table once,
-//                      then stream tiles: one lane per page issues a TMA copy of the page's codes
-//                      in the tensor map's "16 x U4 in 16 bytes" form with the 128-byte swizzle --
-//                      each entry's 128 E2M1 codes occupy one 128-byte shared-memory row, the
-//                      K-major operand form of the kind::f8f6f4 MMA with E2M1 inputs -- and every
-//                      lane copies 16 bytes of block scales with cp.async;
-//   warp 10 (MMA)      issues four K = 32 MMAs per tile into one of kAcc tensor-memory
-//                      accumulators and commits them to that accumulator's barrier;
+//   warps 8-9 (producers, alternating tiles) stream tiles: one lane per page issues a TMA copy
+//                      of the page's codes as they are stored, two E2M1 codes a byte, with the
+//                      64-byte swizzle -- each entry's 128 codes occupy one 64-byte shared-memory
+//                      row, the K-major operand form of the block-scaled kind::mxf4 MMA -- and
+//                      every lane copies 16 bytes of block scales with cp.async;
+//   warp 10 (MMA)      issues two K = 64 MMAs per tile into one of the tensor-memory accumulators
+//                      and commits them to that accumulator's barrier;
 //   warps 0-7          (one thread per entry = per TMEM lane, two warps per lane quadrant taking
 //                      the two tiles of a tile pair) read the accumulator, release it and form
 //                      the scores.
 // The grid is one wave: about (SMs x resident CTAs) / sequences CTAs per sequence.
 //
 // The MMA: A = 128 entries x 128 codes, B = N rows built from the queries, where row
-// (blk, q, h) holds query q's head-h codes inside block blk and zeros elsewhere.  Four MMAs of
-// K = 32 (one per block) accumulate into D = 128 x N fp32 in tensor memory; because every B row
-// is zero outside its block, column (blk, q, h) of D is exactly that block's partial dot product
-// (a sum of 32 products of E2M1 values: multiples of 1/4 below 2^11, exact in fp32).  Block
-// scales and head weights are applied afterwards in fp32, as in the warp-MMA scorer.
+// (blk, q, h) holds query q's head-h codes inside block blk and zeros elsewhere.  Two
+// kind::mxf4 MMAs of K = 64 accumulate into D = 128 x N fp32 in tensor memory with every scale
+// factor 2^0 (UE8M0 127, eight tensor-memory columns written once); because every B row is zero
+// outside its block, column (blk, q, h) of D is exactly that block's partial dot product (a sum of
+// 32 products of E2M1 values: multiples of 1/4 below 2^11, exact in fp32).  Block scales and head
+// weights are applied afterwards in fp32, as in the warp-MMA scorer, so that every score is the
+// same fp32 arithmetic whatever the scales (the packed operand halves the shared memory a tile
+// needs, which doubles the tiles in flight).
 //
 // Top-k, fused into the epilogue (FUSED = true).  Each query's candidates are 64-bit keys
-// (score key << 32 | ~j) in a shared-memory buffer of cap = 2k + 256: a score enters when its key
-// beats the query's threshold, the k-th largest key the buffer held at its last compaction (a key
-// below it cannot be among the k largest of the run, nor of the sequence).  After every tile pair
-// the epilogue warps meet at a named barrier; a buffer past cap - 256 is cut to its k largest keys
-// (exact radix selection) and the threshold rises.  At the end of its run a CTA writes its k
-// largest keys and their count to the workspace; the sequence's last CTA to finish (a ticket
-// counter, left at zero again) merges the runs' lists: the k-th largest key of the sequence by
-// the same radix selection, then a bitmap of the selected entries read out in ascending j.  A
-// separate merge kernel does the same when the scoring phase runs alone or the bitmap does not fit
-// the CTA's shared memory.  FUSED = false writes the fp32 scores themselves (csa_index_scores).
+// (score key << 32 | ~j) in a shared-memory buffer of cap >= k + k/8 + 256 keys: a score enters
+// when its key beats the query's threshold (no key below it can be among the k largest of the
+// run, nor of the sequence).  After every tile pair the epilogue warps meet at a named barrier; a
+// buffer past cap - 256 is cut by a radix selection that stops at a digit bin leaving k to
+// k + k/8 keys, whose lower edge becomes the threshold -- published to the query's other runs,
+// whose thresholds are just as valid (each is at most the query's k-th largest key).  At the end
+// of its run a CTA writes its k largest keys (exact selection), ascending in j, their count and
+// its threshold to the workspace; the sequence's last CTA to finish (a ticket counter, left at
+// zero again) merges the runs' lists: the largest of the runs' thresholds bounds the selection
+// from below, the k-th largest key comes from the same radix selection, and the staged lists are
+// read out in ascending j.  A separate merge kernel does the same when the scoring phase runs
+// alone or the lists do not fit the CTA's shared memory.  FUSED = false writes the fp32 scores
+// themselves (csa_index_scores).
 #include <algorithm>
 
 #include "kernels.cuh"
@@ -51,18 +56,19 @@ namespace lcsa {
 namespace {
 
 constexpr int kTile = 128;          // entries per MMA tile (M)
-constexpr int kStages = 5;          // shared-memory ring depth (tiles in flight per CTA)
-constexpr int kAcc = 8;             // tensor-memory accumulators (the MMA runs up to 8 tiles ahead)
+constexpr int kStages = 10;         // shared-memory ring depth (tiles in flight per CTA)
+constexpr int kAcc = 8;             // tensor-memory accumulators at most (the MMA runs up to 8 tiles ahead)
+constexpr int kSfCols = 8;          // tensor-memory columns of the (unit) scale factors
 constexpr int kMaxPages = 8192;     // block-table entries a CTA's run may span
-constexpr int kRowBytes = 128;      // shared-memory bytes of one entry's 128 codes (16U4 in 16 B)
+constexpr int kRowBytes = 64;       // shared-memory bytes of one entry's 128 codes (packed)
 constexpr int kPackedRowBytes = 64; // global bytes of the same codes
 constexpr int kATileBytes = kTile * kRowBytes;
 constexpr int kEpiWarps = 8;        // two per TMEM lane quadrant, the two tiles of a pair
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kProdWarps = 2;       // producer warps, alternating tiles
 // block-scale ring: tile i's scales are copied once stage i % kStages is free (the MMA of tile
-// i - kStages is done, so the epilogue has read tile i - kStages - kAcc); they are read by the
-// epilogue of tile i, so kStages + kAcc tiles' scales can be live at once
+// i - kStages is done, so the epilogue has read tile i - kStages - accumulators); they are read
+// by the epilogue of tile i, so kStages + kAcc tiles' scales can be live at once
 constexpr int kScaleSlots = kStages + kAcc;
 constexpr int kThreads = kEpiThreads + 32 * kProdWarps + 32;
 constexpr int kCandPerThread = 16;  // candidate buffer per query <= kEpiThreads * kCandPerThread
@@ -72,8 +78,8 @@ constexpr int kMaxRuns = 256;       // CTAs per sequence (run lists a merge read
 template <int QH, int QPS>
 struct TcSmem {
   static constexpr int N = 4 * QH;                            // MMA N: (block, query-head) columns
-  static constexpr int kA = 0;                                // kStages x 16 KB, 1024-aligned
-  static constexpr int kB = kA + kStages * kATileBytes;       // N x 128 B
+  static constexpr int kA = 0;                                // kStages x 8 KB, 1024-aligned
+  static constexpr int kB = kA + kStages * kATileBytes;       // N x 64 B
   static constexpr int kScale = kB + N * kRowBytes;           // kScaleSlots x 128 x 4 B
   static constexpr int kQs = kScale + kScaleSlots * kTile * 4;  // f32 [QH][4] q block scales
   static constexpr int kHw = kQs + QH * 4 * 4;                // f32 [QH] head weights
@@ -98,8 +104,12 @@ struct TcSmem {
   }
 };
 
+// accumulators of N columns: 8 while they and the scale factors fit 256 columns, else 7 (which
+// keeps 32 query-head columns at two CTAs an SM and 64 within the 512 columns)
+__host__ __device__ constexpr int acc_for(int n) { return 8 * n + kSfCols <= 256 ? 8 : 7; }
+
 __host__ __device__ constexpr uint32_t tmem_cols_for(int n) {
-  const int c = kAcc * n;
+  const int c = acc_for(n) * n + kSfCols;
   return c <= 32 ? 32 : (c <= 64 ? 64 : (c <= 128 ? 128 : (c <= 256 ? 256 : 512)));
 }
 
@@ -257,13 +267,15 @@ __device__ void merge_query_topk(const TopkRuns& tr, long long q, int N, int k, 
 // [x*tiles_per_cta, (x+1)*tiles_per_cta) of sequence b (clipped to its visible entries) for the
 // sequence's queries g*QPS .. g*QPS + QPS - 1.
 template <int HI, int QH, bool FUSED>
-__global__ void __launch_bounds__(kThreads, QH >= 16 ? 1 : 2) index_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, IndexParams p,
+__global__ void __launch_bounds__(kThreads, QH >= 16 ? 1 : 2) index_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                                                           const __grid_constant__ CUtensorMap tmap_t, IndexParams p,
                                                            int tiles_per_cta) {
   constexpr int QPS = QH / HI;
   using L = TcSmem<QH, QPS>;
   constexpr int N = L::N;
   constexpr uint32_t kCols = tmem_cols_for(N);
-  constexpr uint32_t kIdesc = idesc_f8f6f4(5, 5, kTile, N);  // E2M1 x E2M1 -> f32, M = 128
+  constexpr int kAccN = acc_for(N);
+  constexpr uint32_t kIdesc = idesc_mxf4(kTile, N);  // E2M1 x E2M1 (unit block scales) -> f32, M = 128
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -331,6 +343,7 @@ __global__ void __launch_bounds__(kThreads, QH >= 16 ? 1 : 2) index_tc_kernel(co
       *abort_flag = 0;
       fence_mbar_init();
       tma_prefetch_desc(&tmap_k);
+      tma_prefetch_desc(&tmap_t);
     }
     if (FUSED && tid < QPS) {
       thr_s[tid] = 0ull;
@@ -351,19 +364,20 @@ __global__ void __launch_bounds__(kThreads, QH >= 16 ? 1 : 2) index_tc_kernel(co
     if (warp == kEpiWarps) {
       tmem_alloc(sbase + L::kMisc, kCols);
     } else if (warp < kEpiWarps) {
-      // ---- B operand: row n = blk*QH + c, c = qi*HI + h; codes of block blk in chunks 2blk, 2blk+1
-      for (int idx = tid; idx < N * 8; idx += kEpiThreads) {
-        const int n = idx >> 3, ch = idx & 7;
+      // ---- B operand: row n = blk*QH + c, c = qi*HI + h; the 16-byte chunk blk of its 64 bytes
+      //      holds block blk's 32 packed codes (64-byte swizzle: chunk ch of row n at ch ^ (n/2 % 4))
+      for (int idx = tid; idx < N * 4; idx += kEpiThreads) {
+        const int n = idx >> 2, ch = idx & 3;
         const int blk = n / QH, c = n % QH;
         const int qi = c / HI, h = c % HI;
-        uint2 v = make_uint2(0u, 0u);
-        if ((ch >> 1) == blk && qi < qn) {
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (ch == blk && qi < qn) {
           const long long qrow = (qrow0 + qi) * HI + h;
-          const uint32_t* src = reinterpret_cast<const uint32_t*>(p.q_fp4 + qrow * 64 + ch * 8);
-          v = make_uint2(src[0], src[1]);
+          const uint32_t* src = reinterpret_cast<const uint32_t*>(p.q_fp4 + qrow * 64 + ch * 16);
+          v = make_uint4(src[0], src[1], src[2], src[3]);
         }
-        const int phys_ch = ch ^ (n & 7);
-        *reinterpret_cast<uint4*>(smem + L::kB + n * kRowBytes + phys_ch * 16) = make_uint4(v.x, v.y, 0u, 0u);
+        const int phys_ch = ch ^ ((n >> 1) & 3);
+        *reinterpret_cast<uint4*>(smem + L::kB + n * kRowBytes + phys_ch * 16) = v;
       }
       for (int idx = tid; idx < QH * 4; idx += kEpiThreads) {
         const int c = idx >> 2, blk = idx & 3;
@@ -381,11 +395,21 @@ __global__ void __launch_bounds__(kThreads, QH >= 16 ? 1 : 2) index_tc_kernel(co
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
+    // the scale factors of every MMA, 2^0: written once by warps 0-3 (their tensor-memory lanes)
+    if (warp < 4) {
+      const uint32_t tm_sf = tmem + kAccN * N + ((uint32_t)(warp * 32) << 16);
+      tmem_st4_fill(tm_sf, 0x7F7F7F7Fu);
+      tmem_st4_fill(tm_sf + 4, 0x7F7F7F7Fu);
+      tmem_st_wait();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
 
     if (warp >= kEpiWarps && warp < kEpiWarps + kProdWarps) {
       // ---- producer warps (tile i by producer warp i % kProdWarps): stage i % kStages receives
-      //      tile t_begin + i.  Lane p issues page p's tensor copy of the codes (the TMA unpacks
-      //      them into the MMA operand form); every lane copies 16 bytes of block scales with
+      //      tile t_begin + i.  Lane p issues page p's tensor copy of the codes (the TMA lays
+      //      them out in the MMA operand form); every lane copies 16 bytes of block scales with
       //      cp.async.  The stage's barrier expects the code bytes from the copies plus one
       //      arrival per lane when its scale copy lands.
       for (int i = warp - kEpiWarps; i < nt; i += kProdWarps) {
@@ -405,12 +429,20 @@ __global__ void __launch_bounds__(kThreads, QH >= 16 ? 1 : 2) index_tc_kernel(co
           phys = -1;
         }
         const uint32_t valid = __ballot_sync(0xffffffffu, phys >= 0);
+        // a tile whose pages are consecutive blocks of the cache is one copy of 128 rows (8 KB),
+        // otherwise one copy per page
+        const int p0 = __shfl_sync(0xffffffffu, phys, 0);
+        const bool whole = rows == kTile && p0 >= 0 && __all_sync(0xffffffffu, lane >= npg || phys == p0 + lane);
         if (lane == 0) {
           armed_s[s] = i;
           mbar_arrive_expect_tx(bar, __popc(valid) * epb * kPackedRowBytes);
         }
         __syncwarp();
-        if (phys >= 0) tma_load_2d(a_dst + (lane << eshift) * kRowBytes, &tmap_k, 0, phys * epb, bar);
+        if (whole) {
+          if (lane == 0) tma_load_2d(a_dst, &tmap_t, 0, p0 * epb, bar);
+        } else if (phys >= 0) {
+          tma_load_2d(a_dst + (lane << eshift) * kRowBytes, &tmap_k, 0, phys * epb, bar);
+        }
         const int r = lane * 4;   // this lane's four scale words
         const int ph = __shfl_sync(0xffffffffu, phys, (r >> eshift) & 31);
         if (r < rows && ph >= 0) cp_async16_s(s_dst + r * 4, p.k_scale + ((long long)ph * epb + (r & (epb - 1))) * 4);
@@ -419,18 +451,19 @@ __global__ void __launch_bounds__(kThreads, QH >= 16 ? 1 : 2) index_tc_kernel(co
       cp_async_wait<0>();
     } else if (warp == kEpiWarps + kProdWarps) {
       if (lane == 0) {
-        // ---- MMA issuer: tile i -> accumulator i % kAcc
-        const uint64_t bdesc = smem_desc_sw128(sbase + L::kB);
+        // ---- MMA issuer: tile i -> accumulator i % kAccN
+        const uint64_t bdesc = smem_desc_sw64(sbase + L::kB);
+        const uint32_t tm_sf = tmem + kAccN * N;
         bool issued = false;
         for (int i = 0; i < nt; ++i) {
-          const int s = i % kStages, a = i % kAcc;
+          const int s = i % kStages, a = i % kAccN;
           if (!mbar_wait(bar_full + 8 * s, (i / kStages) & 1, p.status, abort_flag, polls)) break;
-          if (!mbar_wait(bar_acce + 8 * a, ((i / kAcc) & 1) ^ 1, p.status, abort_flag, polls)) break;
+          if (!mbar_wait(bar_acce + 8 * a, ((i / kAccN) & 1) ^ 1, p.status, abort_flag, polls)) break;
           tc_fence_after_sync();
-          const uint64_t adesc = smem_desc_sw128(sbase + L::kA + s * kATileBytes);
+          const uint64_t adesc = smem_desc_sw64(sbase + L::kA + s * kATileBytes);
 #pragma unroll
-          for (int kb = 0; kb < 4; ++kb)   // K = 32 codes per MMA: 32 shared-memory bytes per step
-            tc_mma_f8f6f4(tmem + a * N, adesc + 2 * kb, bdesc + 2 * kb, kIdesc, kb > 0 ? 1u : 0u);
+          for (int kb = 0; kb < 2; ++kb)   // K = 64 codes per MMA: 32 shared-memory bytes per step
+            tc_mma_mxf4(tmem + a * N, adesc + 2 * kb, bdesc + 2 * kb, kIdesc, tm_sf, tm_sf + 4, kb > 0 ? 1u : 0u);
           tc_commit(bar_accf + 8 * a);
           tc_commit(bar_empty + 8 * s);   // the stage is free once these MMAs have read it
           issued = true;
@@ -469,8 +502,8 @@ __global__ void __launch_bounds__(kThreads, QH >= 16 ? 1 : 2) index_tc_kernel(co
         uint64_t gnext = 0ull;
         if (share && tid < qn) gnext = __ldcg(reinterpret_cast<const unsigned long long*>(p.runs.gthr) + qrow0 + tid);
         if (i < nt && alive) {
-          const int a = i % kAcc;
-          bool ok = mbar_wait(bar_accf + 8 * a, (i / kAcc) & 1, p.status, abort_flag, polls);
+          const int a = i % kAccN;
+          bool ok = mbar_wait(bar_accf + 8 * a, (i / kAccN) & 1, p.status, abort_flag, polls);
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) {
             alive = false;
@@ -700,7 +733,8 @@ size_t tc_smem_for(int heads, int qh, bool fused, int cap, int pages) {
 }
 
 template <int HI, int QH, bool FUSED>
-cudaError_t launch_tc_t(const CUtensorMap& tmap, const IndexParams& p, const IndexTcPlan& plan, cudaStream_t st) {
+cudaError_t launch_tc_t(const CUtensorMap& tmap, const CUtensorMap& tmap_t, const IndexParams& p,
+                        const IndexTcPlan& plan, cudaStream_t st) {
   static PerDeviceOnce attr;
   cudaError_t ea = once_per_device(attr, [] {
     cudaError_t e = cudaFuncSetAttribute(index_tc_kernel<HI, QH, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -711,22 +745,23 @@ cudaError_t launch_tc_t(const CUtensorMap& tmap, const IndexParams& p, const Ind
   });
   if (ea != cudaSuccess) return ea;
   dim3 grid(plan.runs, plan.groups, p.num_seqs);
-  index_tc_kernel<HI, QH, FUSED><<<grid, kThreads, plan.smem, st>>>(tmap, p, plan.tpc);
+  index_tc_kernel<HI, QH, FUSED><<<grid, kThreads, plan.smem, st>>>(tmap, tmap_t, p, plan.tpc);
   return cudaGetLastError();
 }
 
 template <bool FUSED>
-cudaError_t launch_tc_switch(int heads, int qh, const CUtensorMap& tmap, const IndexParams& p, const IndexTcPlan& plan,
+cudaError_t launch_tc_switch(int heads, int qh, const CUtensorMap& tmap, const CUtensorMap& tmap_t, const IndexParams& p,
+                             const IndexTcPlan& plan,
                              cudaStream_t st) {
   switch (heads * 100 + qh) {
-    case 104: return launch_tc_t<1, 4, FUSED>(tmap, p, plan, st);
-    case 204: return launch_tc_t<2, 4, FUSED>(tmap, p, plan, st);
-    case 208: return launch_tc_t<2, 8, FUSED>(tmap, p, plan, st);
-    case 404: return launch_tc_t<4, 4, FUSED>(tmap, p, plan, st);
-    case 408: return launch_tc_t<4, 8, FUSED>(tmap, p, plan, st);
-    case 416: return launch_tc_t<4, 16, FUSED>(tmap, p, plan, st);
-    case 808: return launch_tc_t<8, 8, FUSED>(tmap, p, plan, st);
-    case 816: return launch_tc_t<8, 16, FUSED>(tmap, p, plan, st);
+    case 104: return launch_tc_t<1, 4, FUSED>(tmap, tmap_t, p, plan, st);
+    case 204: return launch_tc_t<2, 4, FUSED>(tmap, tmap_t, p, plan, st);
+    case 208: return launch_tc_t<2, 8, FUSED>(tmap, tmap_t, p, plan, st);
+    case 404: return launch_tc_t<4, 4, FUSED>(tmap, tmap_t, p, plan, st);
+    case 408: return launch_tc_t<4, 8, FUSED>(tmap, tmap_t, p, plan, st);
+    case 416: return launch_tc_t<4, 16, FUSED>(tmap, tmap_t, p, plan, st);
+    case 808: return launch_tc_t<8, 8, FUSED>(tmap, tmap_t, p, plan, st);
+    case 816: return launch_tc_t<8, 16, FUSED>(tmap, tmap_t, p, plan, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -768,7 +803,8 @@ IndexTcPlan plan_index_tc(const IndexParams& p, int rank, int max_new, int max_e
   // resident CTAs per SM: tensor memory and registers (16 query-head columns take 168 registers a
   // thread: one CTA), then shared memory below
   const int occ_tmem = std::min(512 / (int)tmem_cols_for(4 * plan.qh), plan.qh >= 16 ? 1 : 2);
-  const int cap_min = fused ? 2 * k + 2 * kTile : 0;           // a compaction frees k slots or more
+  // a compaction keeps at most k + k/8 keys and leaves room for the next pair of tiles
+  const int cap_min = fused ? (k + (k >> 3) + 2 * kTile + 15) / 16 * 16 : 0;
   if (fused && cap_min > kEpiThreads * kCandPerThread) return plan;
   // two resident CTAs per SM when their shared memory allows it, else one
   for (int occ = std::min(2, occ_tmem); occ >= 1; --occ) {
@@ -806,18 +842,28 @@ cudaError_t launch_index_tc(const IndexParams& p, const IndexTcPlan& plan, cudaS
   if (!plan.applies) return cudaErrorInvalidValue;
   auto enc = tensor_map_encoder();
   if (enc == nullptr) return cudaErrorNotSupported;
-  // codes as [rows][128] 4-bit values; a box of one page is unpacked to 16 codes per 16 bytes
+  // codes as [rows][64] bytes (two 4-bit codes each); a box of one page lands as rows of 64 bytes
+  // with the 64-byte swizzle, the packed operand form of kind::mxf4
   CUtensorMap tmap;
-  const cuuint64_t gdim[2] = {128u, (cuuint64_t)p.k_rows};
+  const cuuint64_t gdim[2] = {64u, (cuuint64_t)p.k_rows};
   const cuuint64_t gstride[1] = {64u};
-  const cuuint32_t box[2] = {128u, (cuuint32_t)p.paging.epb};
+  const cuuint32_t box[2] = {64u, (cuuint32_t)p.paging.epb};
   const cuuint32_t estr[2] = {1u, 1u};
-  CUresult r = enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<uint8_t*>(p.k_fp4), gdim, gstride, box,
-                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  CUresult r = enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(p.k_fp4), gdim, gstride, box,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-  if (p.scores_out != nullptr) return launch_tc_switch<false>(p.heads, plan.qh, tmap, p, plan, st);
-  return launch_tc_switch<true>(p.heads, plan.qh, tmap, p, plan, st);
+  // the same codes in boxes of a whole tile (128 rows), for tiles whose pages are consecutive
+  CUtensorMap tmap_t = tmap;
+  if (p.k_rows >= kTile) {
+    const cuuint32_t box_t[2] = {64u, (cuuint32_t)kTile};
+    r = enc(&tmap_t, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(p.k_fp4), gdim, gstride, box_t, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
+  if (p.scores_out != nullptr) return launch_tc_switch<false>(p.heads, plan.qh, tmap, tmap_t, p, plan, st);
+  return launch_tc_switch<true>(p.heads, plan.qh, tmap, tmap_t, p, plan, st);
 }
 
 cudaError_t launch_topk_merge(const IndexParams& p, const IndexTcPlan& plan, int max_new, cudaStream_t st) {
