@@ -96,6 +96,10 @@ def parse():
                          "the same kernels, for profiler captures; the line then names the changed workload)")
     ap.add_argument("--new-tokens", type=int, default=None,
                     help="csa_prefill only: new tokens (queries) instead of the workload's 16,384")
+    ap.add_argument("--num-seqs", type=int, default=None,
+                    help="csa_decode / csa_decode_1m only: sequences instead of the workload's 32 (a smaller case "
+                         "of the same kernels, for profiler captures; the line then names the changed workload and "
+                         "measures no other workloads)")
     ap.add_argument("--others", default="auto",
                     help="comma-separated workloads measured after the headline (csa_decode, one GPU only), each "
                          "in a process of its own, and summarised in the headline line under 'other_workloads'; "
@@ -343,8 +347,8 @@ def run_gpu(args, rank, world, local, wl=None):
 
     def step_body(with_events=True):
         if not with_events:
-            # the timed step: compression and the window part of attention next to the indexer
-            # (side stream), then the top-k part of attention with the merge
+            # the timed step: compression and the window part of attention (side stream) next to
+            # the indexer, which leaves them SMs; then the top-k part of attention with the merge
             layer.step(batch, raw_in, q_in, out, idx_q_fp4=iq_in, idx_q_scale=iqs_in, head_w=hw_in)
             return
         # the same calls, serialised on one stream with an event node after each
@@ -352,7 +356,7 @@ def run_gpu(args, rank, world, local, wl=None):
         calls = [lambda: layer.compress(batch, raw_in),
                  lambda: csa_attend_window(batch, q_in, H, k, m, c.entries, c.paging, c.state, layer.scale,
                                            layer.attend_ws, layer.attend_ws_bytes, layer.status),
-                 lambda: layer.select(batch, iq_in, iqs_in, hw_in),
+                 lambda: layer.select(batch, iq_in, iqs_in, hw_in, spare_sms=layer.window_ctas(batch)),
                  lambda: csa_attend_topk(batch, q_in, H, layer.topk_idx, layer.topk_cnt, k, m, c.entries, c.paging,
                                          c.state, layer.scale, out, None, layer.attend_ws, layer.attend_ws_bytes,
                                          layer.status),
@@ -438,7 +442,7 @@ def run_gpu(args, rank, world, local, wl=None):
                 "traffic": traffic, "timing": timing}
 
     timing = "CUDA events around the call(s) in a serialised copy of the step (event nodes in a CUDA graph)"
-    roofline_att = roof("csa_attend_window + csa_attend_topk (attention kernels incl. any merge)", att_bytes,
+    roofline_att = roof("csa_attend_window + csa_attend_topk (attention kernels incl. the merge)", att_bytes,
                         att_ms, traffic_of("attend"), timing)
     roofline_att["flop_per_step"] = int(S * 4 * H * D * (k + 128))
     roofline_idx = roof("csa_index_topk (scorer and selection)", idx_bytes, idx_ms, traffic_of("index"), timing)
@@ -1163,6 +1167,10 @@ def main():
                               "device_status_ok": res["status_ok"]}))
         return
     wl = synth.CONFIGS[args.workload]
+    if args.num_seqs is not None:
+        import dataclasses
+        wl = dataclasses.replace(wl, name=wl.name.replace(f"{wl.num_seqs}x", f"{args.num_seqs}x", 1),
+                                 num_seqs=args.num_seqs)
     res = run_gpu(args, rank, world, local, wl)
     if rank == 0:
         value = job_value(res["per_rank_queries"], world, res["ms"])

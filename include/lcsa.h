@@ -69,8 +69,10 @@ typedef enum {
 
 enum { LCS_ROW_BF16 = 0, LCS_ROW_FP8_SPLIT = 1 };
 /* flags of csa_index_topk: phi = ReLU instead of identity; run only the scoring or only the
- * selection phase (see csa_index_topk) */
+ * selection phase; leave n SMs (0..255) free for work the caller runs next to the call (see
+ * csa_index_topk) */
 enum { LCS_INDEX_RELU = 1, LCS_INDEX_SCORE_ONLY = 2, LCS_INDEX_SELECT_ONLY = 4 };
+#define LCS_INDEX_SPARE_SMS(n) ((int32_t)(((n) & 0xFF) << 8))
 
 /* A batch: num_seqs sequences that each receive new tokens in this call (a prefill chunk,
  * one decode token, or several speculative tokens).  Sequence b holds seq_len[b] raw tokens
@@ -206,7 +208,12 @@ lcs_status lcs_window_commit(const lcs_batch* batch, const lcs_state* state, int
  * LCS_INDEX_SELECT_ONLY only the second (the selection from the workspace into out_idx,
  * out_cnt), which reads what an earlier scoring call with the same batch, heads, keys, paging, m,
  * k and workspace left there (it must be ordered after it: same stream or an event); the pair gives
- * exactly the result of one call.  Both flags at once: LCS_ERR_INVALID_ARG. */
+ * exactly the result of one call.  Both flags at once: LCS_ERR_INVALID_ARG.
+ * Sharing the GPU: with LCS_INDEX_SPARE_SMS(n) the scoring kernel sizes its grid for n SMs fewer
+ * than the GPU has (at least 16 remain), so that kernels the caller runs next to it on another
+ * stream -- e.g. the window part of attention, one CTA of about 208 KB of shared memory per query
+ * and 64-head group -- find whole SMs free instead of waiting for the scorer's CTAs to drain.  The
+ * result is the same; the workspace size above covers every n. */
 size_t lcs_index_topk_workspace(const lcs_batch* batch, int32_t heads, const lcs_index_keys* keys,
                                 const lcs_paging* paging, int32_t m, int32_t k);
 /* Leading bytes of that workspace that must be zero before its first use (see above). */

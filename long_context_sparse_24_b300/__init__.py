@@ -20,6 +20,11 @@ LCS_ROW_FP8_SPLIT = 1
 LCS_INDEX_RELU = 1
 LCS_INDEX_SCORE_ONLY = 2
 LCS_INDEX_SELECT_ONLY = 4
+
+
+def LCS_INDEX_SPARE_SMS(n: int) -> int:
+    """csa_index_topk flag: leave n SMs (0..255) free for work run next to the call."""
+    return (int(n) & 0xFF) << 8
 WINDOW = 128
 ROPE_DIMS = 64
 BLOCK_TOKENS = 128

@@ -87,10 +87,13 @@ SplitPlan plan_splits(const lcs_batch* b, int heads, int dim, int max_rows, bool
     }
     // one list per query: cut it into runs of tps tiles so that all (query, head group) runs
     // together come to about one tile load per SM (the last run of a query may be shorter;
-    // CTAs start in split order, so the short runs fill the SMs the long ones leave)
+    // CTAs start in split order, so the short runs fill the SMs the long ones leave); with few
+    // queries and short lists (CSA top-k plus window in one call), the shortest runs that keep
+    // every run in one wave of CTAs
     const int tiles = std::max(1, (max_rows + 127) / 128);
     const long long units = ctas * tiles;
-    const int tps = (int)std::min<long long>(tiles, std::max<long long>(1, (units + num_sms() - 1) / num_sms()));
+    int tps = (int)std::min<long long>(tiles, std::max<long long>(1, (units + num_sms() - 1) / num_sms()));
+    if (ctas * 2 <= sms && tiles <= 32) tps = (tiles + (int)(sms / ctas) - 1) / (int)(sms / ctas);
     const int splits = (tiles + tps - 1) / tps;
     return SplitPlan{splits, 128 * tps, 1, splits, 0};
   }
@@ -139,7 +142,7 @@ size_t zeroed_tickets_bytes(const lcs_batch* b) {
   return round256((size_t)b->num_seqs * std::max(1, b->max_new) * 4);
 }
 
-TopkWs topk_ws_layout(const lcs_batch* b, const IndexParams& p, int rank, int m, int k) {
+TopkWs topk_ws_layout(const lcs_batch* b, const IndexParams& p, int rank, int m, int k, int sms) {
   TopkWs w{};
   const size_t T = (size_t)b->total_new;
   w.ticket = 0;
@@ -149,7 +152,7 @@ TopkWs topk_ws_layout(const lcs_batch* b, const IndexParams& p, int rank, int m,
   // CTA); longer query runs take the prefill scorer, whose CTAs score 16 queries per key tile (a
   // quarter of the key reads) and write every score key for the select kernel
   const bool long_runs = b->max_new > kFusedMaxQueries && index_tc_pf_applies(p, rank, b->max_new);
-  if (!long_runs) w.plan = plan_index_tc(p, rank, b->max_new, b->max_seq_len / m, b->num_seqs, num_sms(), k);
+  if (!long_runs) w.plan = plan_index_tc(p, rank, b->max_new, b->max_seq_len / m, b->num_seqs, sms, k);
   w.fused = w.plan.applies != 0;
   if (w.fused) {
     w.cnt = body;
@@ -339,8 +342,10 @@ lcs_status csa_attend_part(const lcs_batch* batch, const void* q, int32_t heads,
   if (topk_idx == nullptr && part != 1) return LCS_ERR_INVALID_ARG;
   if (k < 1 || k > 4096 || m <= 0 || m > 128) return LCS_ERR_UNSUPPORTED;
   AttendParams p;
+  // the window rows form a split of their own only for the two-part calls (the window part runs
+  // next to the indexer); one call plans the query's entries and window rows as one list
   lcs_status s = attend_common(batch, q, heads, entries, paging, state, part == 1 ? nullptr : out, workspace,
-                               workspace_bytes, k + LCSA_WINDOW, p, true, part == 1);
+                               workspace_bytes, k + LCSA_WINDOW, p, part != 0, part == 1);
   if (s != LCS_OK) return s;
   if (part != 0 && !p.window_split) {
     // only the tensor-core plan for few queries computes the window split apart: otherwise the
@@ -373,7 +378,8 @@ size_t lcs_index_topk_workspace(const lcs_batch* batch, int32_t heads, const lcs
   p.k_scale = keys->scale;
   p.k_rows = keys->num_rows;
   p.paging = make_paging(*paging);
-  return topk_ws_layout(batch, p, keys->rank, m, k).total;
+  // (the grid, and so the number of run lists, is largest with every SM: this covers any spare)
+  return topk_ws_layout(batch, p, keys->rank, m, k, num_sms()).total;
 }
 
 size_t lcs_index_topk_workspace_zeroed(const lcs_batch* batch) {
@@ -441,11 +447,13 @@ lcs_status csa_index_topk(const lcs_batch* batch, const uint8_t* q_fp4, const ui
   lcs_status s = index_common(batch, q_fp4, q_scale, heads, keys, paging, m, p);
   if (s != LCS_OK) return s;
   if (k < 1 || k > 4096) return LCS_ERR_UNSUPPORTED;
-  if ((flags & ~(LCS_INDEX_RELU | LCS_INDEX_SCORE_ONLY | LCS_INDEX_SELECT_ONLY)) != 0) return LCS_ERR_INVALID_ARG;
+  if ((flags & ~(LCS_INDEX_RELU | LCS_INDEX_SCORE_ONLY | LCS_INDEX_SELECT_ONLY | LCS_INDEX_SPARE_SMS(0xFF))) != 0)
+    return LCS_ERR_INVALID_ARG;
+  const int sms = std::max(std::min(16, num_sms()), num_sms() - ((flags >> 8) & 0xFF));
   const bool score_only = (flags & LCS_INDEX_SCORE_ONLY) != 0, select_only = (flags & LCS_INDEX_SELECT_ONLY) != 0;
   if (score_only && select_only) return LCS_ERR_INVALID_ARG;
   if (!score_only && (out_idx == nullptr || out_cnt == nullptr)) return LCS_ERR_INVALID_ARG;
-  const TopkWs w = topk_ws_layout(batch, p, keys->rank, m, k);
+  const TopkWs w = topk_ws_layout(batch, p, keys->rank, m, k, sms);
   if (workspace == nullptr || workspace_bytes < w.total) return LCS_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return LCS_ERR_ALIGNMENT;
   p.head_w = head_w;

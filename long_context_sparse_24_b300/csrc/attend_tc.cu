@@ -176,9 +176,18 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
   const int q = blockIdx.x, hg = blockIdx.y;
   const int H = p.heads;
   const int h0 = hg * HG;
+  // this CTA's split, and (before the sequence is known) the query's top-k count and the entry
+  // indices of the rows of its first tiles, read with the batch's offsets
+  const int split = p.part == 1 ? p.entry_splits : blockIdx.z;
+  const int32_t* sel = p.topk_idx != nullptr ? p.topk_idx + (long long)q * p.k : nullptr;
+  const int spec_r = p.window_split ? (split < p.entry_splits ? split * p.rows_per_split + tid : -1)
+                                    : split * p.rows_per_split + tid;   // this thread's row of the first tiles
+  int spec_j = -1;
+  if (sel != nullptr && p.part != 1 && spec_r >= 0 && spec_r < p.k && tid < 2 * kTileRows) spec_j = __ldg(sel + spec_r);
+  const int cnt_g = (sel != nullptr && p.part != 1 && p.topk_cnt != nullptr) ? __ldg(p.topk_cnt + q) : 0;
   // sequence of query q (the row tile's space is free until the rows arrive)
-  const int b = find_seq_block(p.cu_new, p.num_seqs, q, reinterpret_cast<int*>(smem + L::kT), 8 * kChunk / 4 - 1);
-  const SeqSpan sp = seq_span(p.cu_new, p.seq_len, b);
+  int b;
+  const SeqSpan sp = find_seq_span(p.cu_new, p.seq_len, p.num_seqs, q, reinterpret_cast<int*>(smem + L::kT), 8 * kChunk / 4 - 1, &b);
   // the top-k list and the sequence's block-table row head for L2 while the count is read
   if (p.topk_idx != nullptr && p.part != 1)
     for (int i = tid * 32; i < p.k; i += kThreads * 32) prefetch_l2(p.topk_idx + (long long)q * p.k + i);
@@ -186,14 +195,13 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
     prefetch_l2(p.paging.table + (long long)b * p.paging.max_blocks + i);
   const int n0 = sp.n0();
   const int t = n0 + (q - sp.q0);
-  const int32_t* sel = p.topk_idx != nullptr ? p.topk_idx + (long long)q * p.k : nullptr;
   int cnt;
   if (p.part == 1) {
     cnt = 0;                         // window split alone: the entry list is not needed
   } else if (sel == nullptr) {
     cnt = (t + 1) / p.m;             // HCA: every visible entry
   } else if (p.topk_cnt != nullptr) {
-    cnt = min(p.topk_cnt[q], p.k);
+    cnt = min(cnt_g, p.k);
   } else {
     cnt = 0;
     while (cnt < p.k && sel[cnt] >= 0) ++cnt;
@@ -203,7 +211,6 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
   const int R = cnt + W;
   // this CTA's rows: CSA (window apart): splits 0 .. entry_splits-1 cover the entries, split
   // entry_splits the window; HCA: one list of entries then window, rows_per_split each
-  const int split = p.part == 1 ? p.entry_splits : blockIdx.z;
   int r_begin, r_end;
   if (p.window_split) {
     r_begin = split < p.entry_splits ? split * p.rows_per_split : cnt;
@@ -255,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
     long long d = -1;
     if (r < r_end) {
       if (r < cnt) {
-        const int j = sel != nullptr ? sel[r] : r;
+        const int j = sel != nullptr ? (r == spec_r ? spec_j : sel[r]) : r;
         long long row = -1;
         if (j >= 0 && j < nvis) row = entry_row(p.paging, b, j, p.entries.num_rows);
         if (row < 0) report(p.status, LCS_ERR_DEVICE_GUARD);

@@ -58,6 +58,33 @@ __device__ __forceinline__ int find_seq_block(const int32_t* cu_new, int num_seq
   return lo;
 }
 
+// The sequence b of global query q and its span, found by the whole CTA with cu_new and seq_len
+// staged in shared memory by one parallel load (scratch: 2 * num_seqs + 1 ints when that is at
+// most `cap`; otherwise read from global memory).
+__device__ __forceinline__ SeqSpan find_seq_span(const int32_t* cu_new, const int32_t* seq_len, int num_seqs, int q,
+                                                 int* scratch, int cap, int* b_out) {
+  if (2 * num_seqs + 1 > cap) {
+    const int b = find_seq_block(cu_new, num_seqs, q, scratch, 0);
+    *b_out = b;
+    return seq_span(cu_new, seq_len, b);
+  }
+  for (int i = threadIdx.x; i <= num_seqs; i += blockDim.x) scratch[i] = cu_new[i];
+  for (int i = threadIdx.x; i < num_seqs; i += blockDim.x) scratch[num_seqs + 1 + i] = seq_len[i];
+  __syncthreads();
+  int lo = 0, hi = num_seqs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (scratch[mid] <= q) lo = mid; else hi = mid - 1;
+  }
+  SeqSpan s;
+  s.q0 = scratch[lo];
+  s.qn = scratch[lo + 1] - s.q0;
+  s.n1 = scratch[num_seqs + 1 + lo];
+  __syncthreads();
+  *b_out = lo;
+  return s;
+}
+
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }

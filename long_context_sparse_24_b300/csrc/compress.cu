@@ -196,11 +196,20 @@ __global__ void __launch_bounds__(256) compress_entries_kernel(CompressParams p)
   for (int rr = lane; rr < R; rr += 32) zmax = fmaxf(zmax, zbuf[e_local][rr]);
   zmax = warp_max(zmax);
   float zsum = 0.0f;
-  for (int rr = lane; rr < R; rr += 32) {
-    float z = zbuf[e_local][rr];
-    zsum += (z == -INFINITY) ? 0.0f : expf(z - zmax);
+  if (R <= 16) {
+    // every lane sums in row order: the streaming kernel's order, so that an entry has the same
+    // bits whichever kernel forms it
+    for (int rr = 0; rr < R; ++rr) {
+      const float z = zbuf[e_local][rr];
+      zsum += (z == -INFINITY) ? 0.0f : expf(z - zmax);
+    }
+  } else {
+    for (int rr = lane; rr < R; rr += 32) {
+      const float z = zbuf[e_local][rr];
+      zsum += (z == -INFINITY) ? 0.0f : expf(z - zmax);
+    }
+    zsum = warp_sum(zsum);
   }
-  zsum = warp_sum(zsum);
   const float inv = 1.0f / zsum;
 
   float acc[PL][8];
@@ -569,12 +578,17 @@ cudaError_t launch_roll_m(const CompressParams& p, int max_entries, cudaStream_t
   return launch_roll<D, 1, PC>(p, max_entries, st);
 }
 
+constexpr int kFewTokens = 16;
+
 cudaError_t launch_compress(const CompressParams& p, int D, int max_new, cudaStream_t st) {
   const int R = p.overlap ? 2 * p.m : p.m;
   const int max_entries = max_new / p.m + 1;
   cudaError_t e;
-  if (p.m == 4 || p.m == 2 || p.m == 1) {
-    const bool pc = p.scores != nullptr;
+  // the streaming kernel (a shared-memory ring per warp) for chunks and for per-channel weights;
+  // a few new tokens per sequence (decode: at most one entry completes) with scalar weights take
+  // a warp per entry and no shared memory, so that their CTAs fit on SMs next to the indexer's
+  const bool pc = p.scores != nullptr;
+  if ((p.m == 4 || p.m == 2 || p.m == 1) && (max_new > kFewTokens || pc)) {
     if (D == 512) e = pc ? launch_roll_m<512, true>(p, max_entries, st) : launch_roll_m<512, false>(p, max_entries, st);
     else e = pc ? launch_roll_m<128, true>(p, max_entries, st) : launch_roll_m<128, false>(p, max_entries, st);
   } else {

@@ -683,8 +683,7 @@ __global__ void __launch_bounds__(kThreads, QH >= 16 ? 1 : 2) index_tc_kernel(co
   }
 }
 
-// the merge kernel's shared memory: scratch, histogram, run offsets, then room for the lists and
-// as many candidates
+// the merge kernel's shared memory: scratch, histogram, run offsets, then room for the lists
 constexpr int kMergeHist = ((int)sizeof(SelScratch<256>) + 15) / 16 * 16;
 constexpr int kMergeRunOff = kMergeHist + 2048 * 4;
 constexpr int kMergeStage = kMergeRunOff + (kMaxRuns + 4) * 4;
@@ -701,8 +700,8 @@ __global__ void __launch_bounds__(256) topk_merge_kernel(IndexParams p) {
   int* run_off = reinterpret_cast<int*>(merge_smem + kMergeRunOff);
   uint64_t* stage = reinterpret_cast<uint64_t*>(merge_smem + kMergeStage);
   const int t = sp.n0() + i;
-  const int lists = p.runs.runs * p.top_k;
-  merge_query_topk<256, 0, 11>(p.runs, sp.q0 + i, (t + 1) / p.m, p.top_k, stage, lists, stage + lists, lists,
+  // (the stage holds the lists; the selection reads them with the lower bound, no candidate array)
+  merge_query_topk<256, 0, 11>(p.runs, sp.q0 + i, (t + 1) / p.m, p.top_k, stage, p.runs.runs * p.top_k, nullptr, 0,
                                run_off, hist, p.out_idx, p.out_cnt, sc);
   if (threadIdx.x == 0 && p.runs.gthr != nullptr) p.runs.gthr[sp.q0 + i] = 0ull;   // left at zero
 }
@@ -798,7 +797,10 @@ IndexTcPlan plan_index_tc(const IndexParams& p, int rank, int max_new, int max_e
   const int tiles = std::max(1, (max_entries + kTile - 1) / kTile);
   const int epb = p.paging.epb;
   int tpc_cap = kMaxPages * epb / kTile;                       // a run spans at most kMaxPages pages
-  tpc_cap = std::max(tpc_cap, (tiles + kMaxRuns - 1) / kMaxRuns);   // and a sequence at most kMaxRuns runs
+  // a sequence has at most kMaxRuns runs, and no more than the merge kernel can stage the lists of
+  const int runs_max = fused ? std::max(1, std::min(kMaxRuns, (227 * 1024 - kMergeStage) / (8 * k))) : kMaxRuns;
+  const int tpc_min = (tiles + runs_max - 1) / runs_max;   // fewer runs: longer ones
+  tpc_cap = std::max(tpc_cap, tpc_min);
   if (tpc_cap * kTile / epb > 4 * kMaxPages) return plan;
   // resident CTAs per SM: tensor memory and registers (16 query-head columns take 168 registers a
   // thread: one CTA), then shared memory below
@@ -809,7 +811,7 @@ IndexTcPlan plan_index_tc(const IndexParams& p, int rank, int max_new, int max_e
   // two resident CTAs per SM when their shared memory allows it, else one
   for (int occ = std::min(2, occ_tmem); occ >= 1; --occ) {
     int runs = std::max(1, (sms * occ) / std::max(1, num_seqs * plan.groups));   // about one wave
-    int tpc = std::min(tpc_cap, (tiles + runs - 1) / runs);
+    int tpc = std::max(tpc_min, std::min(tpc_cap, (tiles + runs - 1) / runs));
     runs = (tiles + tpc - 1) / tpc;
     const int pages = tpc * kTile / epb + 1;
     const long long budget = (long long)(228 * 1024 / occ) - 1024;
@@ -832,7 +834,7 @@ IndexTcPlan plan_index_tc(const IndexParams& p, int rank, int max_new, int max_e
   // prefixes fit it in any case (tpc * 128 entries: at most 8 bits of ring per entry)
   const size_t stage_bytes = (size_t)(TcSmem<16, 4>::kSelAll - TcSmem<16, 4>::kA);   // the same for every variant
   plan.merge_inline = fused && (size_t)plan.runs * k * 8 <= stage_bytes;
-  plan.merge_smem = (size_t)kMergeStage + (size_t)plan.runs * k * 16;
+  plan.merge_smem = (size_t)kMergeStage + (size_t)plan.runs * k * 8;
   if (fused && (size_t)plan.tpc * kTile / 32 * 8 > (size_t)(TcSmem<16, 4>::kHist - TcSmem<16, 4>::kA)) plan.applies = 0;
   if (fused && !plan.merge_inline && plan.merge_smem > 227 * 1024) plan.applies = 0;
   return plan;

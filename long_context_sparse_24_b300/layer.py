@@ -15,9 +15,9 @@ from typing import Optional, Sequence
 
 import torch
 
-from . import (LCS_INDEX_RELU, WINDOW, Batch, Compressor, csa_attend, csa_attend_topk, csa_attend_window, csa_compress,
-               csa_index_topk, hca_attend, hca_compress, lcs_attend_workspace, lcs_index_topk_workspace,
-               lcs_window_commit)
+from . import (LCS_INDEX_RELU, LCS_INDEX_SPARE_SMS, WINDOW, Batch, Compressor, csa_attend, csa_attend_topk,
+               csa_attend_window, csa_compress, csa_index_topk, hca_attend, hca_compress, lcs_attend_workspace,
+               lcs_index_topk_workspace, lcs_window_commit)
 from . import buffers
 
 
@@ -48,6 +48,7 @@ class Layer:
         self.side = torch.cuda.Stream(device=device) if kind == "csa" else None
         self.comp: Optional[Compressor] = None
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.sms = torch.cuda.get_device_properties(device).multi_processor_count
         # workspaces sized for the largest step this layer will run
         T = num_seqs * max_new
         probe = Batch(0, 0, num_seqs, T, max_new, capacity)
@@ -85,11 +86,21 @@ class Layer:
         fn = csa_compress if self.kind == "csa" else hca_compress
         fn(batch, raw, self.comp, st, self.cache.entries, self.cache.paging, self.status, stream)
 
-    def select(self, batch: Batch, q_fp4, q_scale, head_w, stream=None, phase: int = 0) -> None:
-        """Indexer top-k; phase: 0 both phases, LCS_INDEX_SCORE_ONLY or LCS_INDEX_SELECT_ONLY."""
+    def select(self, batch: Batch, q_fp4, q_scale, head_w, stream=None, phase: int = 0, spare_sms: int = 0) -> None:
+        """Indexer top-k; phase: 0 both phases, LCS_INDEX_SCORE_ONLY or LCS_INDEX_SELECT_ONLY;
+        spare_sms: SMs the scorer leaves free for work running next to it."""
         csa_index_topk(batch, q_fp4, q_scale, head_w, self.index_heads, self.cache.keys, self.cache.paging, self.m,
-                       self.top_k, (LCS_INDEX_RELU if self.relu else 0) | phase, self.topk_idx, self.topk_cnt,
-                       self.topk_ws, self.topk_ws_bytes, self.status, stream)
+                       self.top_k, (LCS_INDEX_RELU if self.relu else 0) | phase | LCS_INDEX_SPARE_SMS(spare_sms),
+                       self.topk_idx, self.topk_cnt, self.topk_ws, self.topk_ws_bytes, self.status, stream)
+
+    def window_ctas(self, batch: Batch) -> int:
+        """SMs the indexer leaves to the window part of attention: one per query and 64-head group
+        when they are few, and the indexer's scan is short enough (up to 65,536 entries a
+        sequence) that the window part would otherwise lengthen the step; at longer contexts the
+        scan dominates the step and keeps every SM (measured: 32 x 128K step 117.6 -> 109.7 us
+        with the SMs left free, 32 x 1M 252 -> 284 us)."""
+        n = batch.total_new * ((self.heads + 63) // 64)
+        return n if n * 4 <= self.sms and batch.max_seq_len // self.m <= 65536 else 0
 
     def attend(self, batch: Batch, q: torch.Tensor, out: torch.Tensor, lse: Optional[torch.Tensor] = None,
                stream=None) -> None:
@@ -109,10 +120,12 @@ class Layer:
              lse: Optional[torch.Tensor] = None, idx_q_fp4=None, idx_q_scale=None, head_w=None, stream=None,
              q_ready: Optional[torch.cuda.Event] = None) -> None:
         """One pass of the hot path for the batch's new tokens.  CSA: compression, then the window
-        part of attention (side stream) run next to the indexer (scoring with the top-k fused in);
-        the top-k part of attention, with the merge of the two parts, waits for both.  q_ready:
-        an event the attention waits for before reading q (q still arriving, e.g. copied from the
-        host on another stream), so that compression and the indexer need not wait for it."""
+        part of attention (side stream), run next to the indexer (scoring with the top-k fused
+        in), which leaves SMs free for the window part's CTAs (about 208 KB of shared memory
+        each: they could not start beside the indexer's CTAs otherwise); the top-k part of
+        attention, with the merge of the two parts, waits for both.  q_ready: an event the
+        attention waits for before reading q (q still arriving, e.g. copied from the host on
+        another stream), so that compression and the indexer need not wait for it."""
         main = stream if stream is not None else torch.cuda.current_stream()
         if self.kind == "csa":
             self.side.wait_stream(main)
@@ -122,7 +135,7 @@ class Layer:
             csa_attend_window(batch, q, self.heads, self.top_k, self.m, self.cache.entries, self.cache.paging,
                               self.cache.state, self.scale, self.attend_ws, self.attend_ws_bytes, self.status,
                               self.side)
-            self.select(batch, idx_q_fp4, idx_q_scale, head_w, main)
+            self.select(batch, idx_q_fp4, idx_q_scale, head_w, main, spare_sms=self.window_ctas(batch))
             main.wait_stream(self.side)
             csa_attend_topk(batch, q, self.heads, self.topk_idx, self.topk_cnt, self.top_k, self.m, self.cache.entries,
                             self.cache.paging, self.cache.state, self.scale, out, lse, self.attend_ws,

@@ -74,6 +74,10 @@ def test_host_validation_without_gpu():
     assert L.csa_index_topk(*args(4, 0, 0x8000, 1 << 20)) == 4
     assert L.csa_index_topk(*args(4, 16, None, 0)) == 8
     assert L.csa_index_topk(*args(4, 16, 0x8000, 1)) == 8
+    # flags beyond ReLU, the two phases and the spare-SM count
+    assert L.csa_index_topk(by(_batch(lcsa)), 0x1000, 0x2000, None, 4, by(keys), by(pag), 4, 16, 1 << 16, 0x3000,
+                            0x4000, 0x8000, 1 << 20, None, None) == 1
+    assert lcsa.LCS_INDEX_SPARE_SMS(32) == 32 << 8 and lcsa.LCS_INDEX_SPARE_SMS(300) == (300 & 0xFF) << 8
     # attention: heads 24 unsupported; topk list missing
     assert L.csa_attend(by(_batch(lcsa)), 0x1000, 24, 0x2000, None, 16, 4, by(rows), by(pag), by(st), 1.0,
                         0x3000, None, None, 0, None, None) == 4

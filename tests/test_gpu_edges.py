@@ -20,12 +20,12 @@ lcsa = pytest.importorskip("long_context_sparse_24_b300")
 pytestmark = pytest.mark.gpu
 
 
-def _topk(batch, cache, q_fp4, q_sc, hw, heads, m, k, st=None):
+def _topk(batch, cache, q_fp4, q_sc, hw, heads, m, k, st=None, flags=0):
     T = batch.total_new
     out_idx = torch.full((T, k), -7, dtype=torch.int32, device=DEV)
     out_cnt = torch.full((T,), -7, dtype=torch.int32, device=DEV)
     wsb = lcsa.lcs_index_topk_workspace(batch, heads, cache.keys, cache.paging, m, k)
-    lcsa.csa_index_topk(batch, q_fp4, q_sc, hw, heads, cache.keys, cache.paging, m, k, 0, out_idx, out_cnt,
+    lcsa.csa_index_topk(batch, q_fp4, q_sc, hw, heads, cache.keys, cache.paging, m, k, flags, out_idx, out_cnt,
                         workspace(wsb), wsb, st)
     torch.cuda.synchronize()
     return out_idx.cpu().numpy(), out_cnt.cpu().numpy()
@@ -147,3 +147,37 @@ def test_bounded_waits_report_timeout_then_recover():
         sel = oracle.topk_select(ref[0, :oracle.visible_entries(L - 1, m)], k)
         assert oc[b] == len(sel) and np.array_equal(oi[b, :len(sel)], sel), f"seq {b}"
     _attend_case("csa", [2000, 4100, 300], [1, 1, 1], 64, 512, "fp8_split", 4, 512)
+
+
+@pytest.mark.parametrize("spare", [32, 100, 140])
+def test_topk_with_spare_sms_matches_oracle(spare):
+    """The scorer sized for fewer SMs (longer runs, fewer run lists; at least 16 SMs remain) gives
+    the oracle's top-k, as with every SM."""
+    m, k, heads, rank = 4, 512, 4, 128
+    lengths, new = [40000, 130000, 9000], [1, 1, 1]
+    cache, batch, kcs, kss, qcs, qss, hws, q_fp4, q_sc, hw = _index_case(lengths, new, m, k, heads, rank, False,
+                                                                       True)
+    st = dev_status()
+    oi, oc = _topk(batch, cache, q_fp4, q_sc, hw, heads, m, k, st, flags=lcsa.LCS_INDEX_SPARE_SMS(spare))
+    assert_status_ok(st)
+    for b, L in enumerate(lengths):
+        ref = oracle.index_scores(qcs[b], qss[b], hws[b], kcs[b], kss[b])
+        sel = oracle.topk_select(ref[0, :oracle.visible_entries(L - 1, m)], k)
+        assert oc[b] == len(sel) and np.array_equal(oi[b, :len(sel)], sel), f"seq {b}"
+
+
+def test_topk_few_long_sequences_merge_kernel():
+    """Two sequences of about a million tokens at k = 1024: more runs than the scorer's ring can
+    stage, so the runs are capped to what the merge kernel stages and the merge kernel selects;
+    the top-k equals the oracle's."""
+    m, k, heads, rank = 4, 1024, 4, 128
+    lengths, new = [1000000, 700001], [1, 1]
+    cache, batch, kcs, kss, qcs, qss, hws, q_fp4, q_sc, hw = _index_case(lengths, new, m, k, heads, rank, False,
+                                                                       True)
+    st = dev_status()
+    oi, oc = _topk(batch, cache, q_fp4, q_sc, hw, heads, m, k, st)
+    assert_status_ok(st)
+    for b, L in enumerate(lengths):
+        ref = oracle.index_scores(qcs[b], qss[b], hws[b], kcs[b], kss[b])
+        sel = oracle.topk_select(ref[0, :oracle.visible_entries(L - 1, m)], k)
+        assert oc[b] == len(sel) and np.array_equal(oi[b, :len(sel)], sel), f"seq {b}"

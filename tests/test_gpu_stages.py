@@ -382,13 +382,12 @@ def _attend_case(kind, lengths, new, heads, dim, fmt, m, k, seed=41, scale=None,
             torch.cuda.current_stream().wait_stream(side)
             lcsa.csa_attend_topk(batch, q, heads, idx_t, cnt_t, k, m, cache.entries, cache.paging, cache.state,
                                  scale, out, lse, ws, wsb, st)
+            # the one call plans the window rows into the entries' list (other splits, so other
+            # rounding): it is checked against the oracle as well
             one_out = torch.empty_like(out)
             one_lse = torch.empty_like(lse)
             lcsa.csa_attend(batch, q, heads, idx_t, cnt_t, k, m, cache.entries, cache.paging, cache.state, scale,
                             one_out, one_lse, workspace(wsb), wsb, st)
-            torch.cuda.synchronize()
-            assert torch.equal(out.view(torch.int16), one_out.view(torch.int16)), "split != one call (outputs)"
-            assert torch.equal(lse, one_lse), "split != one call (lse)"
         else:
             lcsa.csa_attend(batch, q, heads, idx_t, cnt_t, k, m, cache.entries, cache.paging, cache.state, scale, out,
                             lse, workspace(wsb), wsb, st)
@@ -398,6 +397,8 @@ def _attend_case(kind, lengths, new, heads, dim, fmt, m, k, seed=41, scale=None,
                         workspace(wsb), wsb, st)
     if sink is not None:
         lcsa.lcs_attention_sink(out, lse, torch.from_numpy(sink.astype(np.float32)).to(DEV))
+        if kind == "csa" and split:
+            lcsa.lcs_attention_sink(one_out, one_lse, torch.from_numpy(sink.astype(np.float32)).to(DEV))
     torch.cuda.synchronize()
     want = expect_status if expect_status is not None else (6 if corrupt_seq is not None else 0)
     got = int(st.item())
@@ -406,27 +407,29 @@ def _attend_case(kind, lengths, new, heads, dim, fmt, m, k, seed=41, scale=None,
         return
     if corrupt_seq is not None:
         skip_seq = corrupt_seq
-    o = bf16_tensor_to_f64(out); l = lse.cpu().numpy()
+    results = [(out, lse, "")] + ([(one_out, one_lse, " (one call)")] if kind == "csa" and split else [])
     qf = bits_to_f64(q_bits)
-    qi = 0
-    for b in range(S):
-        n0 = lengths[b] - new[b]
-        if b == skip_seq:
-            qi += new[b]
-            continue
-        for i in range(new[b]):
-            t = n0 + i
-            if kind == "csa":
-                rows = oracle.csa_query_rows(t, sels[qi], ent_deq[b], win_deq[b])
-            else:
-                rows = oracle.hca_query_rows(t, m, ent_deq[b], win_deq[b])
-            if sink is None:
-                ro, rl = oracle.attend(qf[qi], rows, scale)
-            else:
-                ro, rl = oracle.attend_with_sink(qf[qi], rows, scale, sink.astype(np.float32).astype(np.float64))
-            check_outputs(o[qi], ro, f"{kind} seq {b} query {i}")
-            assert np.allclose(l[qi], rl, atol=2e-3, rtol=1e-4), f"lse seq {b} query {i}"
-            qi += 1
+    for res_out, res_lse, tag in results:
+        o = bf16_tensor_to_f64(res_out); l = res_lse.cpu().numpy()
+        qi = 0
+        for b in range(S):
+            n0 = lengths[b] - new[b]
+            if b == skip_seq:
+                qi += new[b]
+                continue
+            for i in range(new[b]):
+                t = n0 + i
+                if kind == "csa":
+                    rows = oracle.csa_query_rows(t, sels[qi], ent_deq[b], win_deq[b])
+                else:
+                    rows = oracle.hca_query_rows(t, m, ent_deq[b], win_deq[b])
+                if sink is None:
+                    ro, rl = oracle.attend(qf[qi], rows, scale)
+                else:
+                    ro, rl = oracle.attend_with_sink(qf[qi], rows, scale, sink.astype(np.float32).astype(np.float64))
+                check_outputs(o[qi], ro, f"{kind} seq {b} query {i}{tag}")
+                assert np.allclose(l[qi], rl, atol=2e-3, rtol=1e-4), f"lse seq {b} query {i}{tag}"
+                qi += 1
 
 
 @pytest.mark.parametrize("kind,lengths,new,heads,dim,fmt,m,k", [
@@ -472,7 +475,7 @@ def test_attention_sink_matches_oracle(kind, lengths, new, heads, dim, fmt, m, k
     ([130, 7], [1, 7], 16, 512, "fp8_split", 32),                  # short sequences, N(t) < k
     ([50, 700], [50, 20], 8, 128, "bf16", 64),                     # no separate window part: all in the top-k call
 ])
-def test_attend_window_then_topk_equals_one_call(lengths, new, heads, dim, fmt, k):
+def test_attend_window_then_topk_and_one_call(lengths, new, heads, dim, fmt, k):
     _attend_case("csa", lengths, new, heads, dim, fmt, 4, k, split=True)
 
 
