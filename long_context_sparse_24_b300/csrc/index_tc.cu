@@ -331,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, QH >= 16 ? 1 : 2) index_tc_kernel(co
   if (nt > 0) {
     if (tid == kEpiThreads) {
       for (int i = 0; i < kStages; ++i) {
-        mbar_init(bar_full + 8 * i, 33);   // the expect-tx arrival + one per producer lane
+        mbar_init(bar_full + 8 * i, 1);    // the expect-tx arrival (codes and scales: transaction bytes)
         mbar_init(bar_empty + 8 * i, 1);   // the MMA commit
         armed_s[i] = -1;
       }
@@ -395,6 +395,12 @@ __global__ void __launch_bounds__(kThreads, QH >= 16 ? 1 : 2) index_tc_kernel(co
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
+    // do the run's pages follow one another in the cache (every one mapped and inside the key rows)?
+    bool contig_mine = true;
+    for (int i = tid; i < npages; i += kThreads) {
+      const int ph = pages_s[i];
+      contig_mine = contig_mine && ph >= 0 && ph == pages_s[0] + i && (long long)(ph + 1) * epb <= p.k_rows;
+    }
     // the scale factors of every MMA, 2^0: written once by warps 0-3 (their tensor-memory lanes)
     if (warp < 4) {
       const uint32_t tm_sf = tmem + kAccN * N + ((uint32_t)(warp * 32) << 16);
@@ -403,15 +409,16 @@ __global__ void __launch_bounds__(kThreads, QH >= 16 ? 1 : 2) index_tc_kernel(co
       tmem_st_wait();
     }
     tc_fence_before_sync();
-    __syncthreads();
+    const bool run_contig = __syncthreads_and(contig_mine ? 1 : 0) != 0;
     tc_fence_after_sync();
 
     if (warp >= kEpiWarps && warp < kEpiWarps + kProdWarps) {
       // ---- producer warps (tile i by producer warp i % kProdWarps): stage i % kStages receives
-      //      tile t_begin + i.  Lane p issues page p's tensor copy of the codes (the TMA lays
-      //      them out in the MMA operand form); every lane copies 16 bytes of block scales with
-      //      cp.async.  The stage's barrier expects the code bytes from the copies plus one
-      //      arrival per lane when its scale copy lands.
+      //      tile t_begin + i: the codes by tensor copies (the TMA lays them out in the MMA operand
+      //      form) and the block scales by bulk copies, all counted in the stage barrier's
+      //      transaction bytes.  A run whose pages are consecutive blocks of the cache (checked
+      //      once) takes one thread a tile: one copy of 128 rows and one of their scales; otherwise
+      //      lane p copies page p.
       for (int i = warp - kEpiWarps; i < nt; i += kProdWarps) {
         const int s = i % kStages;
         bool ok = true;
@@ -423,32 +430,36 @@ __global__ void __launch_bounds__(kThreads, QH >= 16 ? 1 : 2) index_tc_kernel(co
         const uint32_t a_dst = sbase + L::kA + s * kATileBytes;
         const uint32_t s_dst = sbase + L::kScale + (i % kScaleSlots) * kTile * 4;
         const int npg = rows >> eshift;
-        int phys = lane < npg ? pages_s[((e0 >> eshift) - page0) + lane] : -1;
-        if (lane < npg && (phys < 0 || (long long)(phys + 1) * epb > p.k_rows)) {
-          report(p.status, LCS_ERR_DEVICE_GUARD);   // unmapped, or outside the key rows
-          phys = -1;
+        if (run_contig) {
+          if (lane == 0) {
+            const int p0 = pages_s[(e0 >> eshift) - page0];
+            armed_s[s] = i;
+            mbar_arrive_expect_tx(bar, rows * (kPackedRowBytes + 4));
+            if (rows == kTile) {
+              tma_load_2d(a_dst, &tmap_t, 0, p0 * epb, bar);
+            } else {
+              for (int pg = 0; pg < npg; ++pg) tma_load_2d(a_dst + (pg << eshift) * kRowBytes, &tmap_k, 0, (p0 + pg) * epb, bar);
+            }
+            bulk_load(s_dst, p.k_scale + (long long)p0 * epb * 4, rows * 4, bar);
+          }
+        } else {
+          int phys = lane < npg ? pages_s[((e0 >> eshift) - page0) + lane] : -1;
+          if (lane < npg && (phys < 0 || (long long)(phys + 1) * epb > p.k_rows)) {
+            report(p.status, LCS_ERR_DEVICE_GUARD);   // unmapped, or outside the key rows
+            phys = -1;
+          }
+          const uint32_t valid = __ballot_sync(0xffffffffu, phys >= 0);
+          if (lane == 0) {
+            armed_s[s] = i;
+            mbar_arrive_expect_tx(bar, __popc(valid) * epb * (kPackedRowBytes + 4));
+          }
+          __syncwarp();
+          if (phys >= 0) {
+            tma_load_2d(a_dst + (lane << eshift) * kRowBytes, &tmap_k, 0, phys * epb, bar);
+            bulk_load(s_dst + (lane << eshift) * 4, p.k_scale + (long long)phys * epb * 4, epb * 4, bar);
+          }
         }
-        const uint32_t valid = __ballot_sync(0xffffffffu, phys >= 0);
-        // a tile whose pages are consecutive blocks of the cache is one copy of 128 rows (8 KB),
-        // otherwise one copy per page
-        const int p0 = __shfl_sync(0xffffffffu, phys, 0);
-        const bool whole = rows == kTile && p0 >= 0 && __all_sync(0xffffffffu, lane >= npg || phys == p0 + lane);
-        if (lane == 0) {
-          armed_s[s] = i;
-          mbar_arrive_expect_tx(bar, __popc(valid) * epb * kPackedRowBytes);
-        }
-        __syncwarp();
-        if (whole) {
-          if (lane == 0) tma_load_2d(a_dst, &tmap_t, 0, p0 * epb, bar);
-        } else if (phys >= 0) {
-          tma_load_2d(a_dst + (lane << eshift) * kRowBytes, &tmap_k, 0, phys * epb, bar);
-        }
-        const int r = lane * 4;   // this lane's four scale words
-        const int ph = __shfl_sync(0xffffffffu, phys, (r >> eshift) & 31);
-        if (r < rows && ph >= 0) cp_async16_s(s_dst + r * 4, p.k_scale + ((long long)ph * epb + (r & (epb - 1))) * 4);
-        cp_async_arrive_noinc(bar);
       }
-      cp_async_wait<0>();
     } else if (warp == kEpiWarps + kProdWarps) {
       if (lane == 0) {
         // ---- MMA issuer: tile i -> accumulator i % kAccN
@@ -582,15 +593,14 @@ __global__ void __launch_bounds__(kThreads, QH >= 16 ? 1 : 2) index_tc_kernel(co
             uint64_t* buf = cand_s + qi * cap;
             // a threshold with k to k + k/8 of the buffer's keys at or above it (no more than the
             // buffer can keep while taking another pair), or the current one when fewer than k
-            // keys pass that: every later key below it has k larger ones.  Published to the
-            // query's other runs.
+            // keys pass that: every later key below it has k larger ones
             const uint64_t lo = thr_s[qi];
             const SelResult r = select_top<kEpiThreads, kEpiBarrier, 8>(buf, n, k, k >> 3, sel, sel.hist, lo);
             const uint64_t tau = r.tau > lo ? r.tau : lo;
             const int kept = compact_keys_ge<kEpiThreads, kEpiBarrier, kCandPerThread>(buf, n, tau, sel);
             if (tid == 0) {
               cnt_s[qi] = kept;
-              uint64_t t = tau;
+              uint64_t t = tau;   // (published to the query's other runs)
               if (share) {
                 const unsigned long long o =
                     atomicMax(reinterpret_cast<unsigned long long*>(p.runs.gthr) + qrow0 + qi, (unsigned long long)t);
