@@ -33,7 +33,9 @@ METRIC = "CSA/HCA attention queries/s at 128K-1M ctx"
 # workload, from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum), together with
 # the hash of the kernel sources they were taken on: when the sources differ from that hash the
 # counters no longer describe the kernels that run and `traffic` is reported as null.
-TRAFFIC = {"source_sha1": None, "attend": None, "index": None}
+TRAFFIC = {"source_sha1": "0b7a5bb7af6d427e997e5bb5830014e355dd741e",
+           "attend": 29761376,    # attend_tc1_kernel (top-k part 14.50 MB + window part 4.68 MB) + combine 10.58 MB
+           "index": 72943360}     # index_tc_kernel<4, 4, 1>: 71.57 MB read + 1.37 MB written
 UNIT = "queries/s"
 
 

@@ -83,7 +83,8 @@ struct TcSmem {
   static constexpr int kScale = kB + N * kRowBytes;           // kScaleSlots x 128 x 4 B
   static constexpr int kQs = kScale + kScaleSlots * kTile * 4;  // f32 [QH][4] q block scales
   static constexpr int kHw = kQs + QH * 4 * 4;                // f32 [QH] head weights
-  static constexpr int kBar = (kHw + QH * 4 + 7) / 8 * 8;     // u64 full/empty[kStages], accf/acce[kAcc], drain
+  static constexpr int kQw = kHw + QH * 4;                    // f32 [QH][4] q block scale x head weight
+  static constexpr int kBar = (kQw + QH * 4 * 4 + 7) / 8 * 8;  // u64 full/empty[kStages], accf/acce[kAcc], drain
   static constexpr int kArmed = kBar + (2 * kStages + 2 * kAcc + 1) * 8;   // int [kStages] last tile armed
   static constexpr int kMisc = kArmed + kStages * 4 + 4;      // tmem base, abort flag, last-CTA flag
   // (16-byte aligned from here on: the selection scratch holds 8-byte fields)
@@ -317,6 +318,7 @@ __global__ void __launch_bounds__(kThreads, QH >= 16 ? 1 : 2) index_tc_kernel(co
 
   float* qs_s = reinterpret_cast<float*>(smem + L::kQs);
   float* hw_s = reinterpret_cast<float*>(smem + L::kHw);
+  float* qw_s = reinterpret_cast<float*>(smem + L::kQw);
   int* pages_s = reinterpret_cast<int*>(smem + L::kCand + (FUSED ? QPS * cap * 8 : 0));
   int* armed_s = reinterpret_cast<int*>(smem + L::kArmed);
   const uint32_t bar_full = sbase + L::kBar;
@@ -382,7 +384,10 @@ __global__ void __launch_bounds__(kThreads, QH >= 16 ? 1 : 2) index_tc_kernel(co
       for (int idx = tid; idx < QH * 4; idx += kEpiThreads) {
         const int c = idx >> 2, blk = idx & 3;
         const int qi = c / HI, h = c % HI;
-        qs_s[idx] = qi < qn ? ue8m0_to_f32(p.q_scale[((qrow0 + qi) * HI + h) * 4 + blk]) : 0.0f;
+        const float qs = qi < qn ? ue8m0_to_f32(p.q_scale[((qrow0 + qi) * HI + h) * 4 + blk]) : 0.0f;
+        qs_s[idx] = qs;
+        // powers of two times the head weight: exact
+        qw_s[idx] = qi < qn ? qs * (p.head_w ? p.head_w[(qrow0 + qi) * HI + h] : 1.0f) : 0.0f;
       }
       for (int c = tid; c < QH; c += kEpiThreads) {
         const int qi = c / HI, h = c % HI;
@@ -490,16 +495,8 @@ __global__ void __launch_bounds__(kThreads, QH >= 16 ? 1 : 2) index_tc_kernel(co
       // ---- epilogue: tile pair ip = tiles 2ip (warps 0-3) and 2ip+1 (warps 4-7); warp w reads
       //      TMEM lanes 32*(w%4).. (its entries)
       const int quad = warp & 3, par = warp >> 2;
-      float qsc[QH][4], hw[QH], qw[QH][4];
-#pragma unroll
-      for (int c = 0; c < QH; ++c) {
-        hw[c] = hw_s[c];
-#pragma unroll
-        for (int blk = 0; blk < 4; ++blk) {
-          qsc[c][blk] = qs_s[c * 4 + blk];
-          qw[c][blk] = qsc[c][blk] * hw[c];   // powers of two times the head weight: exact
-        }
-      }
+      // (the query's block scales and head weights are read from shared memory where they are
+      // used: broadcast reads, registers kept for the accumulator columns)
       int nq[QPS];
 #pragma unroll
       for (int qi = 0; qi < QPS; ++qi) nq[qi] = qi < qn ? (n0 + qi + 1) >> mshift : 0;
@@ -507,89 +504,112 @@ __global__ void __launch_bounds__(kThreads, QH >= 16 ? 1 : 2) index_tc_kernel(co
       SelScratch<kEpiThreads>& sel = *reinterpret_cast<SelScratch<kEpiThreads>*>(smem + L::kSelEpi);
       bool alive = true;
       const bool share = FUSED && p.runs.gthr != nullptr;
-      for (int i0 = 0; i0 < nt; i0 += 2) {
-        const int i = i0 + par;
-        // the threshold the query's other runs have reached (read now, taken at the pair's end)
+      // a warp takes kPerWarp tiles an iteration (the two warp groups alternate) and the warps meet
+      // once an iteration (measured: two tiles a warp was no faster and needs more candidate room)
+      constexpr int kPerWarp = 1;
+      constexpr int kIter = 2 * kPerWarp;
+      // the scores of tile i (accumulator columns d, the entries' block-scale word sc)
+      auto score_tile = [&](const uint32_t (&d)[N], uint32_t sc, int i) {
+        // 2^(e-127) for the four UE8M0 bytes (e = 0 gives the subnormal 2^-127)
+        float ksc[4];
+        ksc[0] = __uint_as_float(max((sc << 23) & 0x7F800000u, 0x00400000u));
+        ksc[1] = __uint_as_float(max((sc << 15) & 0x7F800000u, 0x00400000u));
+        ksc[2] = __uint_as_float(max((sc << 7) & 0x7F800000u, 0x00400000u));
+        ksc[3] = __uint_as_float(max((sc >> 1) & 0x7F800000u, 0x00400000u));
+        const int j = (t_begin + i) * kTile + row;
+#pragma unroll
+        for (int qi = 0; qi < QPS; ++qi) {
+          float score;
+          if (!p.relu) {
+            // phi = identity: sum over heads inside each block first (every term exact)
+            float tb[4];
+#pragma unroll
+            for (int blk = 0; blk < 4; ++blk) {
+              float t = 0.0f;
+#pragma unroll
+              for (int h = 0; h < HI; ++h)
+                t = fmaf(__uint_as_float(d[blk * QH + qi * HI + h]), qw_s[(qi * HI + h) * 4 + blk], t);
+              tb[blk] = t;
+            }
+            score = fmaf(tb[3], ksc[3], fmaf(tb[2], ksc[2], fmaf(tb[1], ksc[1], tb[0] * ksc[0])));
+          } else {
+            float sh[HI];
+#pragma unroll
+            for (int h = 0; h < HI; ++h) {
+              const int c = qi * HI + h;
+              float acc = 0.0f;
+#pragma unroll
+              for (int blk = 0; blk < 4; ++blk)
+                acc = fmaf(__uint_as_float(d[blk * QH + c]), ksc[blk] * qs_s[c * 4 + blk], acc);
+              sh[h] = fmaxf(acc, 0.0f) * hw_s[c];
+            }
+#pragma unroll
+            for (int w = 1; w < HI; w <<= 1)
+#pragma unroll
+              for (int h = 0; h < HI; h += 2 * w) sh[h] = sh[h] + sh[h + w];
+            score = sh[0];
+          }
+          const bool vis = j < nq[qi];
+          if constexpr (FUSED) {
+            const uint64_t key = ((uint64_t)score_key(score) << 32) | (uint64_t)(~(uint32_t)j);
+            warp_append(vis && key > thr_s[qi], key, cand_s + qi * cap, cnt_s + qi);
+          } else {
+            if (vis) p.scores_out[(qrow0 + qi) * p.ld + j] = score;
+          }
+        }
+      };
+      for (int i0 = 0; i0 < nt; i0 += kIter) {
+        // the threshold the query's other runs have reached (read now, taken at the iteration's end)
         uint64_t gnext = 0ull;
         if (share && tid < qn) gnext = __ldcg(reinterpret_cast<const unsigned long long*>(p.runs.gthr) + qrow0 + tid);
-        if (i < nt && alive) {
-          const int a = i % kAccN;
-          bool ok = mbar_wait(bar_accf + 8 * a, (i / kAccN) & 1, p.status, abort_flag, polls);
-          ok = __all_sync(0xffffffffu, ok);
-          if (!ok) {
-            alive = false;
-          } else {
-            tc_fence_after_sync();
-            uint32_t d[N];
+        uint32_t d[kPerWarp][N];
+        bool have[kPerWarp];
 #pragma unroll
-            for (int c16 = 0; c16 < N / 16; ++c16)
-              tmem_ld16(tmem + ((uint32_t)(quad * 32) << 16) + a * N + c16 * 16,
-                        *reinterpret_cast<uint32_t(*)[16]>(&d[c16 * 16]));
-            tmem_ld_wait();
-            const uint32_t sc =
-                *reinterpret_cast<const uint32_t*>(smem + L::kScale + ((i % kScaleSlots) * kTile + row) * 4);
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_acce + 8 * a);
-            // 2^(e-127) for the four UE8M0 bytes (e = 0 gives the subnormal 2^-127)
-            float ksc[4];
-            ksc[0] = __uint_as_float(max((sc << 23) & 0x7F800000u, 0x00400000u));
-            ksc[1] = __uint_as_float(max((sc << 15) & 0x7F800000u, 0x00400000u));
-            ksc[2] = __uint_as_float(max((sc << 7) & 0x7F800000u, 0x00400000u));
-            ksc[3] = __uint_as_float(max((sc >> 1) & 0x7F800000u, 0x00400000u));
-            const int j = (t_begin + i) * kTile + row;
+        for (int u = 0; u < kPerWarp; ++u) {
+          const int i = i0 + par + 2 * u;
+          have[u] = i < nt && alive;
+          if (have[u]) {
+            const int a = i % kAccN;
+            bool ok = mbar_wait(bar_accf + 8 * a, (i / kAccN) & 1, p.status, abort_flag, polls);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) {
+              alive = false;
+              have[u] = false;
+            } else {
+              tc_fence_after_sync();
 #pragma unroll
-            for (int qi = 0; qi < QPS; ++qi) {
-              float score;
-              if (!p.relu) {
-                // phi = identity: sum over heads inside each block first (every term exact)
-                float tb[4];
-#pragma unroll
-                for (int blk = 0; blk < 4; ++blk) {
-                  float t = 0.0f;
-#pragma unroll
-                  for (int h = 0; h < HI; ++h)
-                    t = fmaf(__uint_as_float(d[blk * QH + qi * HI + h]), qw[qi * HI + h][blk], t);
-                  tb[blk] = t;
-                }
-                score = fmaf(tb[3], ksc[3], fmaf(tb[2], ksc[2], fmaf(tb[1], ksc[1], tb[0] * ksc[0])));
-              } else {
-                float sh[HI];
-#pragma unroll
-                for (int h = 0; h < HI; ++h) {
-                  const int c = qi * HI + h;
-                  float acc = 0.0f;
-#pragma unroll
-                  for (int blk = 0; blk < 4; ++blk)
-                    acc = fmaf(__uint_as_float(d[blk * QH + c]), ksc[blk] * qsc[c][blk], acc);
-                  sh[h] = fmaxf(acc, 0.0f) * hw[c];
-                }
-#pragma unroll
-                for (int w = 1; w < HI; w <<= 1)
-#pragma unroll
-                  for (int h = 0; h < HI; h += 2 * w) sh[h] = sh[h] + sh[h + w];
-                score = sh[0];
-              }
-              const bool vis = j < nq[qi];
-              if constexpr (FUSED) {
-                const uint64_t key = ((uint64_t)score_key(score) << 32) | (uint64_t)(~(uint32_t)j);
-                warp_append(vis && key > thr_s[qi], key, cand_s + qi * cap, cnt_s + qi);
-              } else {
-                if (vis) p.scores_out[(qrow0 + qi) * p.ld + j] = score;
-              }
+              for (int c16 = 0; c16 < N / 16; ++c16)
+                tmem_ld16(tmem + ((uint32_t)(quad * 32) << 16) + a * N + c16 * 16,
+                          *reinterpret_cast<uint32_t(*)[16]>(&d[u][c16 * 16]));
             }
           }
         }
+        tmem_ld_wait();
+        uint32_t sc[kPerWarp];
+#pragma unroll
+        for (int u = 0; u < kPerWarp; ++u)
+          sc[u] = have[u] ? *reinterpret_cast<const uint32_t*>(
+                                smem + L::kScale + (((i0 + par + 2 * u) % kScaleSlots) * kTile + row) * 4)
+                          : 0u;
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0)
+#pragma unroll
+          for (int u = 0; u < kPerWarp; ++u)
+            if (have[u]) mbar_arrive(bar_acce + 8 * ((i0 + par + 2 * u) % kAccN));
+#pragma unroll
+        for (int u = 0; u < kPerWarp; ++u)
+          if (have[u]) score_tile(d[u], sc[u], i0 + par + 2 * u);
         if constexpr (FUSED) {
           // any run's threshold is at most the query's k-th largest key: a larger one from another
           // run filters this run's later keys too
           if (share && tid < qn && gnext > thr_s[tid]) thr_s[tid] = gnext;
-          // both tiles of the pair are in: cut buffers that could not take another pair
+          // the iteration's tiles are in: cut buffers that could not take another iteration
           group_sync<kEpiThreads, kEpiBarrier>();
 #pragma unroll 1
           for (int qi = 0; qi < qn; ++qi) {
             const int n = cnt_s[qi];
-            if (n <= cap - 2 * kTile) continue;        // uniform: read after the barrier
+            if (n <= cap - kIter * kTile) continue;    // uniform: read after the barrier
             uint64_t* buf = cand_s + qi * cap;
             // a threshold with k to k + k/8 of the buffer's keys at or above it (no more than the
             // buffer can keep while taking another pair), or the current one when fewer than k
@@ -815,7 +835,7 @@ IndexTcPlan plan_index_tc(const IndexParams& p, int rank, int max_new, int max_e
   // resident CTAs per SM: tensor memory and registers (16 query-head columns take 168 registers a
   // thread: one CTA), then shared memory below
   const int occ_tmem = std::min(512 / (int)tmem_cols_for(4 * plan.qh), plan.qh >= 16 ? 1 : 2);
-  // a compaction keeps at most k + k/8 keys and leaves room for the next pair of tiles
+  // a compaction keeps at most k + k/8 keys and leaves room for the epilogue's next two tiles
   const int cap_min = fused ? (k + (k >> 3) + 2 * kTile + 15) / 16 * 16 : 0;
   if (fused && cap_min > kEpiThreads * kCandPerThread) return plan;
   // two resident CTAs per SM when their shared memory allows it, else one
