@@ -49,7 +49,7 @@
 extern "C" {
 #endif
 
-#define LCSA_ABI_VERSION 2
+#define LCSA_ABI_VERSION 3
 #define LCSA_WINDOW 128      /* sliding-window rows (x-techcon section 2, CSA step 3)      */
 #define LCSA_ROPE_DIMS 64    /* BF16 RoPE slice (chenxutan.com/d/4230, section 4.5)         */
 #define LCSA_BLOCK_TOKENS 128 /* raw tokens per cache block, LCM(4,128) (x-techcon sec. 4) */
@@ -130,6 +130,19 @@ typedef struct {
   void* pending_scores;      /* per-channel compressors only: bf16[num_seqs][pending_slots][D], the
                                 score rows of the pending tokens (same ring as `pending`); else NULL */
 } lcs_state;
+
+/* Separate value rows (chenxutan.com/d/4230, section 4.5: the hybrid cache keeps K and V apart;
+ * the other pages describe shared-KV attention, where the row is key and value).  Each set holds
+ * the value row of the key row with the same number in its counterpart: entries <-> the entry
+ * cache (same paging), window <-> state->window (same ring), new_rows <-> state->new_rows.  Each
+ * set has its counterpart's format, dim and num_rows; new_rows.nope is NULL exactly when
+ * state->new_rows.nope is.  Value entries are produced like key entries (csa_compress /
+ * hca_compress over the raw value rows). */
+typedef struct {
+  lcs_rows entries;
+  lcs_rows window;
+  lcs_rows new_rows;
+} lcs_values;
 
 /* Compressor parameters.  Entry j uses tokens [(j-1)m, (j+1)m) with overlap, [jm, (j+1)m)
  * without; o = offset of token t in the entry's window (0 .. 2m-1 with overlap, 0 .. m-1
@@ -260,7 +273,11 @@ lcs_status csa_index_topk_noalloc(const lcs_batch* batch, const uint8_t* q_fp4, 
  *        then window tokens max(0,t-127) .. t;
  *   HCA: the entries 0 .. N(t)-1, N(t) = floor((t+1)/m), then the same window tokens;
  * logits = softmax_scale * q[i,h,:] . row, o[i,h,:] = sum p * row (shared KV: the row is key
- * and value).  Window token p is read from state->new_rows when p is one of this call's new
+ * and value), or, with `values` set, o[i,h,:] = sum p * value row (the row with the same number in
+ * the matching set of *values; values NULL = shared KV).  With values set the calls run the
+ * warp-MMA kernel (csa_attend_window then launches nothing and csa_attend_topk computes
+ * everything); value rows obey the row bounds below and a value row outside them is left out of
+ * the softmax with LCS_ERR_DEVICE_GUARD.  Window token p is read from state->new_rows when p is one of this call's new
  * tokens (p >= seq_len-q_b) and from the window ring otherwise; with new_rows.nope NULL every
  * window row comes from the ring, which requires batch->max_new <= 1 (LCS_ERR_SHAPE otherwise).
  *   q       device bf16[total_new][heads][D]    out device bf16[total_new][heads][D]
@@ -271,12 +288,15 @@ lcs_status csa_index_topk_noalloc(const lcs_batch* batch, const uint8_t* q_fp4, 
  * 65504 * s_r (the kernels compute in f16 on the rows divided by s_r).  A row outside these bounds
  * is left out of the softmax and LCS_ERR_DEVICE_GUARD is reported.
  * Workspace: device, >= lcs_attend_workspace(batch, heads, D, max_rows) bytes, where max_rows
- * bounds the rows of one query (CSA: k + 128; HCA: floor(max_seq_len/m) + 128). */
+ * bounds the rows of one query (CSA: k + 128; HCA: floor(max_seq_len/m) + 128); the size covers
+ * calls with and without values.
+ * Errors (nothing launched): LCS_ERR_SHAPE for value sets whose format, dim or num_rows differ
+ * from their key counterparts. */
 size_t lcs_attend_workspace(const lcs_batch* batch, int32_t heads, int32_t dim, int32_t max_rows);
 lcs_status csa_attend(const lcs_batch* batch, const void* q, int32_t heads, const int32_t* topk_idx,
                       const int32_t* topk_cnt, int32_t k, int32_t m, const lcs_rows* entries,
-                      const lcs_paging* paging, const lcs_state* state, float softmax_scale,
-                      void* out, float* out_lse, void* workspace, size_t workspace_bytes,
+                      const lcs_paging* paging, const lcs_state* state, const lcs_values* values,
+                      float softmax_scale, void* out, float* out_lse, void* workspace, size_t workspace_bytes,
                       int32_t* dev_status, void* stream);
 /* csa_attend in two calls, so that the sliding-window part, which does not depend on the top-k
  * selection, can run while the indexer does (CSA step 3 of x-techcon section 2 attends the window
@@ -290,19 +310,20 @@ lcs_status csa_attend(const lcs_batch* batch, const void* q, int32_t heads, cons
  * exactly the bits of csa_attend.  The library computes the window part apart only for D = 512
  * FP8-split rows, up to 128 heads, k <= 2048 and at most half as many (query, 64-head group)
  * pairs as the GPU has SMs; otherwise (other shapes, or runs of queries that fill the GPU by
- * themselves) csa_attend_window launches nothing and csa_attend_topk computes everything. */
+ * themselves, or calls with values) csa_attend_window launches nothing and csa_attend_topk
+ * computes everything. */
 lcs_status csa_attend_window(const lcs_batch* batch, const void* q, int32_t heads, int32_t k, int32_t m,
                              const lcs_rows* entries, const lcs_paging* paging, const lcs_state* state,
-                             float softmax_scale, void* workspace, size_t workspace_bytes, int32_t* dev_status,
-                             void* stream);
+                             const lcs_values* values, float softmax_scale, void* workspace,
+                             size_t workspace_bytes, int32_t* dev_status, void* stream);
 lcs_status csa_attend_topk(const lcs_batch* batch, const void* q, int32_t heads, const int32_t* topk_idx,
                            const int32_t* topk_cnt, int32_t k, int32_t m, const lcs_rows* entries,
-                           const lcs_paging* paging, const lcs_state* state, float softmax_scale, void* out,
-                           float* out_lse, void* workspace, size_t workspace_bytes, int32_t* dev_status,
-                           void* stream);
+                           const lcs_paging* paging, const lcs_state* state, const lcs_values* values,
+                           float softmax_scale, void* out, float* out_lse, void* workspace,
+                           size_t workspace_bytes, int32_t* dev_status, void* stream);
 lcs_status hca_attend(const lcs_batch* batch, const void* q, int32_t heads, int32_t m,
                       const lcs_rows* entries, const lcs_paging* paging, const lcs_state* state,
-                      float softmax_scale, void* out, float* out_lse, void* workspace,
+                      const lcs_values* values, float softmax_scale, void* out, float* out_lse, void* workspace,
                       size_t workspace_bytes, int32_t* dev_status, void* stream);
 
 /* --- indexer key / query production: block-scaled FP4 (x-techcon section 4) -------------------

@@ -67,6 +67,10 @@ class lcs_state(ctypes.Structure):
                 ("pending_scores", c_vp)]
 
 
+class lcs_values(ctypes.Structure):
+    _fields_ = [("entries", lcs_rows), ("window", lcs_rows), ("new_rows", lcs_rows)]
+
+
 class lcs_compressor(ctypes.Structure):
     _fields_ = [("w", c_vp), ("bias", c_vp), ("m", c_i32), ("overlap", c_i32), ("scores", c_vp)]
 
@@ -100,13 +104,13 @@ _SIGS = {
                                        c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp]),
     "lcs_attend_workspace": (c_sz, [P(lcs_batch), c_i32, c_i32, c_i32]),
     "csa_attend": (c_i32, [P(lcs_batch), c_vp, c_i32, c_vp, c_vp, c_i32, c_i32, P(lcs_rows), P(lcs_paging),
-                           P(lcs_state), ctypes.c_float, c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
+                           P(lcs_state), P(lcs_values), ctypes.c_float, c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
     "csa_attend_window": (c_i32, [P(lcs_batch), c_vp, c_i32, c_i32, c_i32, P(lcs_rows), P(lcs_paging), P(lcs_state),
-                                  ctypes.c_float, c_vp, c_sz, c_vp, c_vp]),
+                                  P(lcs_values), ctypes.c_float, c_vp, c_sz, c_vp, c_vp]),
     "csa_attend_topk": (c_i32, [P(lcs_batch), c_vp, c_i32, c_vp, c_vp, c_i32, c_i32, P(lcs_rows), P(lcs_paging),
-                                P(lcs_state), ctypes.c_float, c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
+                                P(lcs_state), P(lcs_values), ctypes.c_float, c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
     "hca_attend": (c_i32, [P(lcs_batch), c_vp, c_i32, c_i32, P(lcs_rows), P(lcs_paging), P(lcs_state),
-                           ctypes.c_float, c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
+                           P(lcs_values), ctypes.c_float, c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -189,6 +193,28 @@ class State:
         nr = self.new_rows.c() if self.new_rows is not None else lcs_rows(self.window.format, self.window.dim, 0,
                                                                             None, None, None)
         return lcs_state(self.window.c(), _ptr(self.pending), self.pending_slots, nr, _ptr(self.pending_scores))
+
+
+@dataclasses.dataclass
+class Values:
+    """Separate value rows: each set numbered like its key counterpart (entry cache, window ring,
+    new rows of the call)."""
+    entries: RowSet
+    window: RowSet
+    new_rows: Optional[RowSet] = None
+
+    def c(self) -> lcs_values:
+        nr = self.new_rows.c() if self.new_rows is not None else lcs_rows(self.window.format, self.window.dim, 0,
+                                                                            None, None, None)
+        return lcs_values(self.entries.c(), self.window.c(), nr)
+
+
+def _values_ref(values: Optional[Values]):
+    """(ctypes argument, keep-alive) for an optional Values."""
+    if values is None:
+        return None, None
+    v = values.c()
+    return ctypes.byref(v), v
 
 
 @dataclasses.dataclass
@@ -334,35 +360,40 @@ def lcs_attend_workspace(batch: Batch, heads: int, dim: int, max_rows: int) -> i
 
 def csa_attend(batch: Batch, q, heads: int, topk_idx, topk_cnt, k: int, m: int, entries: RowSet, paging: Paging,
                state: State, softmax_scale: float, out, out_lse, workspace, workspace_bytes: int, dev_status=None,
-               stream=None) -> None:
+               stream=None, values: Optional[Values] = None) -> None:
     b, e, p, s = batch.c(), entries.c(), paging.c(), state.c()
+    vr, _keep = _values_ref(values)
     _check(_lib.csa_attend(ctypes.byref(b), _ptr(q), heads, _ptr(topk_idx), _ptr(topk_cnt), k, m, ctypes.byref(e),
-                           ctypes.byref(p), ctypes.byref(s), softmax_scale, _ptr(out), _ptr(out_lse),
+                           ctypes.byref(p), ctypes.byref(s), vr, softmax_scale, _ptr(out), _ptr(out_lse),
                            _ptr(workspace), workspace_bytes, _ptr(dev_status), _stream(stream)), "csa_attend")
 
 
 def csa_attend_window(batch: Batch, q, heads: int, k: int, m: int, entries: RowSet, paging: Paging, state: State,
-                      softmax_scale: float, workspace, workspace_bytes: int, dev_status=None, stream=None) -> None:
+                      softmax_scale: float, workspace, workspace_bytes: int, dev_status=None, stream=None,
+                      values: Optional[Values] = None) -> None:
     b, e, p, s = batch.c(), entries.c(), paging.c(), state.c()
+    vr, _keep = _values_ref(values)
     _check(_lib.csa_attend_window(ctypes.byref(b), _ptr(q), heads, k, m, ctypes.byref(e), ctypes.byref(p),
-                                  ctypes.byref(s), softmax_scale, _ptr(workspace), workspace_bytes, _ptr(dev_status),
+                                  ctypes.byref(s), vr, softmax_scale, _ptr(workspace), workspace_bytes, _ptr(dev_status),
                                   _stream(stream)), "csa_attend_window")
 
 
 def csa_attend_topk(batch: Batch, q, heads: int, topk_idx, topk_cnt, k: int, m: int, entries: RowSet, paging: Paging,
                     state: State, softmax_scale: float, out, out_lse, workspace, workspace_bytes: int,
-                    dev_status=None, stream=None) -> None:
+                    dev_status=None, stream=None, values: Optional[Values] = None) -> None:
     b, e, p, s = batch.c(), entries.c(), paging.c(), state.c()
+    vr, _keep = _values_ref(values)
     _check(_lib.csa_attend_topk(ctypes.byref(b), _ptr(q), heads, _ptr(topk_idx), _ptr(topk_cnt), k, m,
-                                ctypes.byref(e), ctypes.byref(p), ctypes.byref(s), softmax_scale, _ptr(out),
+                                ctypes.byref(e), ctypes.byref(p), ctypes.byref(s), vr, softmax_scale, _ptr(out),
                                 _ptr(out_lse), _ptr(workspace), workspace_bytes, _ptr(dev_status), _stream(stream)),
            "csa_attend_topk")
 
 
 def hca_attend(batch: Batch, q, heads: int, m: int, entries: RowSet, paging: Paging, state: State,
                softmax_scale: float, out, out_lse, workspace, workspace_bytes: int, dev_status=None,
-               stream=None) -> None:
+               stream=None, values: Optional[Values] = None) -> None:
     b, e, p, s = batch.c(), entries.c(), paging.c(), state.c()
+    vr, _keep = _values_ref(values)
     _check(_lib.hca_attend(ctypes.byref(b), _ptr(q), heads, m, ctypes.byref(e), ctypes.byref(p), ctypes.byref(s),
-                           softmax_scale, _ptr(out), _ptr(out_lse), _ptr(workspace), workspace_bytes,
+                           vr, softmax_scale, _ptr(out), _ptr(out_lse), _ptr(workspace), workspace_bytes,
                            _ptr(dev_status), _stream(stream)), "hca_attend")

@@ -74,8 +74,8 @@ struct SplitPlan {
 // entries then window rows, cut into about one wave of CTAs.
 bool attend_tc_applies(int heads, int dim) { return dim == 512 && heads <= 128; }
 
-SplitPlan plan_splits(const lcs_batch* b, int heads, int dim, int max_rows, bool window_split) {
-  if (attend_tc_applies(heads, dim)) {
+SplitPlan plan_splits(const lcs_batch* b, int heads, int dim, int max_rows, bool window_split, bool tc_ok = true) {
+  if (tc_ok && attend_tc_applies(heads, dim)) {
     const int sms = num_sms();
     const long long ctas = std::max<long long>(1, (long long)b->total_new * ((heads + 63) / 64));
     const int per_query = (int)std::max<long long>(1, sms / ctas);   // CTAs per (query, head group)
@@ -273,9 +273,27 @@ lcs_status index_common(const lcs_batch* batch, const uint8_t* q_fp4, const uint
   return LCS_OK;
 }
 
+// Value sets: each one's format, dim and row count equal its key counterpart's (the same row
+// numbers address both), and new value rows exist exactly when new key rows do.
+lcs_status check_values(const lcs_values* v, const lcs_rows* entries, const lcs_state* state) {
+  lcs_status s;
+  const lcs_rows* pairs[2][2] = {{&v->entries, entries}, {&v->window, &state->window}};
+  for (auto& pr : pairs) {
+    if ((s = check_rows(pr[0])) != LCS_OK) return s;
+    if (!same_layout(*pr[0], *pr[1]) || pr[0]->num_rows != pr[1]->num_rows) return LCS_ERR_SHAPE;
+  }
+  if ((v->new_rows.nope != nullptr) != (state->new_rows.nope != nullptr)) return LCS_ERR_SHAPE;
+  if (v->new_rows.nope != nullptr) {
+    if ((s = check_rows(&v->new_rows)) != LCS_OK) return s;
+    if (!same_layout(v->new_rows, state->new_rows) || v->new_rows.num_rows != state->new_rows.num_rows)
+      return LCS_ERR_SHAPE;
+  }
+  return LCS_OK;
+}
+
 lcs_status attend_common(const lcs_batch* batch, const void* q, int32_t heads, const lcs_rows* entries,
-                         const lcs_paging* paging, const lcs_state* state, void* out, void* workspace,
-                         size_t workspace_bytes, int max_rows, AttendParams& p, bool window_split,
+                         const lcs_paging* paging, const lcs_state* state, const lcs_values* values, void* out,
+                         void* workspace, size_t workspace_bytes, int max_rows, AttendParams& p, bool window_split,
                          bool no_out = false) {
   lcs_status s = check_batch(batch);
   if (s != LCS_OK) return s;
@@ -299,7 +317,8 @@ lcs_status attend_common(const lcs_batch* batch, const void* q, int32_t heads, c
   }
   if (entries->num_rows < 1) return LCS_ERR_SHAPE;
   if (entries->format == LCS_ROW_BF16 && entries->dim == 512) return LCS_ERR_UNSUPPORTED;
-  const SplitPlan plan = plan_splits(batch, heads, entries->dim, max_rows, window_split);
+  if (values != nullptr && (s = check_values(values, entries, state)) != LCS_OK) return s;
+  const SplitPlan plan = plan_splits(batch, heads, entries->dim, max_rows, window_split, values == nullptr);
   const size_t need = attend_ws_bytes(batch, heads, entries->dim, plan);
   if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return LCS_ERR_WORKSPACE;
   if (need > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return LCS_ERR_ALIGNMENT;
@@ -316,6 +335,12 @@ lcs_status attend_common(const lcs_batch* batch, const void* q, int32_t heads, c
   if (!have_new) {
     p.new_rows.nope = nullptr;
     p.new_rows.num_rows = 0;
+  }
+  if (values != nullptr) {
+    p.sv = 1;
+    p.v_entries = make_rows(values->entries);
+    p.v_window = make_rows(values->window);
+    p.v_new_rows = make_rows(values->new_rows);
   }
   p.out = static_cast<__nv_bfloat16*>(out);
   p.splits = plan.splits;
@@ -336,16 +361,16 @@ lcs_status attend_common(const lcs_batch* batch, const void* q, int32_t heads, c
 
 lcs_status csa_attend_part(const lcs_batch* batch, const void* q, int32_t heads, const int32_t* topk_idx,
                            const int32_t* topk_cnt, int32_t k, int32_t m, const lcs_rows* entries,
-                           const lcs_paging* paging, const lcs_state* state, float softmax_scale, void* out,
-                           float* out_lse, void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream,
-                           int part) {
+                           const lcs_paging* paging, const lcs_state* state, const lcs_values* values,
+                           float softmax_scale, void* out, float* out_lse, void* workspace, size_t workspace_bytes,
+                           int32_t* dev_status, void* stream, int part) {
   if (topk_idx == nullptr && part != 1) return LCS_ERR_INVALID_ARG;
   if (k < 1 || k > 4096 || m <= 0 || m > 128) return LCS_ERR_UNSUPPORTED;
   AttendParams p;
   // the window rows form a split of their own only for the two-part calls (the window part runs
   // next to the indexer); one call plans the query's entries and window rows as one list
-  lcs_status s = attend_common(batch, q, heads, entries, paging, state, part == 1 ? nullptr : out, workspace,
-                               workspace_bytes, k + LCSA_WINDOW, p, part != 0, part == 1);
+  lcs_status s = attend_common(batch, q, heads, entries, paging, state, values, part == 1 ? nullptr : out,
+                               workspace, workspace_bytes, k + LCSA_WINDOW, p, part != 0, part == 1);
   if (s != LCS_OK) return s;
   if (part != 0 && !p.window_split) {
     // only the tensor-core plan for few queries computes the window split apart: otherwise the
@@ -514,42 +539,45 @@ lcs_status csa_index_scores(const lcs_batch* batch, const uint8_t* q_fp4, const 
 
 size_t lcs_attend_workspace(const lcs_batch* batch, int32_t heads, int32_t dim, int32_t max_rows) {
   if (batch == nullptr) return 0;
-  // the same size serves a CSA call (window apart) and an HCA call (one list)
-  return std::max(attend_ws_bytes(batch, heads, dim, plan_splits(batch, heads, dim, max_rows, true)),
-                  attend_ws_bytes(batch, heads, dim, plan_splits(batch, heads, dim, max_rows, false)));
+  // the same size serves a CSA call (window apart), an HCA call (one list) and calls with values
+  // (warp-MMA plan)
+  return std::max({attend_ws_bytes(batch, heads, dim, plan_splits(batch, heads, dim, max_rows, true)),
+                   attend_ws_bytes(batch, heads, dim, plan_splits(batch, heads, dim, max_rows, false)),
+                   attend_ws_bytes(batch, heads, dim, plan_splits(batch, heads, dim, max_rows, false, false))});
 }
 
 lcs_status csa_attend(const lcs_batch* batch, const void* q, int32_t heads, const int32_t* topk_idx,
                       const int32_t* topk_cnt, int32_t k, int32_t m, const lcs_rows* entries, const lcs_paging* paging,
-                      const lcs_state* state, float softmax_scale, void* out, float* out_lse, void* workspace,
-                      size_t workspace_bytes, int32_t* dev_status, void* stream) {
-  return csa_attend_part(batch, q, heads, topk_idx, topk_cnt, k, m, entries, paging, state, softmax_scale, out,
-                         out_lse, workspace, workspace_bytes, dev_status, stream, 0);
+                      const lcs_state* state, const lcs_values* values, float softmax_scale, void* out,
+                      float* out_lse, void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  return csa_attend_part(batch, q, heads, topk_idx, topk_cnt, k, m, entries, paging, state, values, softmax_scale,
+                         out, out_lse, workspace, workspace_bytes, dev_status, stream, 0);
 }
 
 lcs_status csa_attend_window(const lcs_batch* batch, const void* q, int32_t heads, int32_t k, int32_t m,
                              const lcs_rows* entries, const lcs_paging* paging, const lcs_state* state,
-                             float softmax_scale, void* workspace, size_t workspace_bytes, int32_t* dev_status,
-                             void* stream) {
-  return csa_attend_part(batch, q, heads, nullptr, nullptr, k, m, entries, paging, state, softmax_scale, nullptr,
-                         nullptr, workspace, workspace_bytes, dev_status, stream, 1);
+                             const lcs_values* values, float softmax_scale, void* workspace, size_t workspace_bytes,
+                             int32_t* dev_status, void* stream) {
+  return csa_attend_part(batch, q, heads, nullptr, nullptr, k, m, entries, paging, state, values, softmax_scale,
+                         nullptr, nullptr, workspace, workspace_bytes, dev_status, stream, 1);
 }
 
 lcs_status csa_attend_topk(const lcs_batch* batch, const void* q, int32_t heads, const int32_t* topk_idx,
                            const int32_t* topk_cnt, int32_t k, int32_t m, const lcs_rows* entries,
-                           const lcs_paging* paging, const lcs_state* state, float softmax_scale, void* out,
-                           float* out_lse, void* workspace, size_t workspace_bytes, int32_t* dev_status,
-                           void* stream) {
-  return csa_attend_part(batch, q, heads, topk_idx, topk_cnt, k, m, entries, paging, state, softmax_scale, out,
-                         out_lse, workspace, workspace_bytes, dev_status, stream, 2);
+                           const lcs_paging* paging, const lcs_state* state, const lcs_values* values,
+                           float softmax_scale, void* out, float* out_lse, void* workspace, size_t workspace_bytes,
+                           int32_t* dev_status, void* stream) {
+  return csa_attend_part(batch, q, heads, topk_idx, topk_cnt, k, m, entries, paging, state, values, softmax_scale,
+                         out, out_lse, workspace, workspace_bytes, dev_status, stream, 2);
 }
 
 lcs_status hca_attend(const lcs_batch* batch, const void* q, int32_t heads, int32_t m, const lcs_rows* entries,
-                      const lcs_paging* paging, const lcs_state* state, float softmax_scale, void* out, float* out_lse,
-                      void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream) {
+                      const lcs_paging* paging, const lcs_state* state, const lcs_values* values, float softmax_scale,
+                      void* out, float* out_lse, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                      void* stream) {
   if (m <= 0 || m > 128) return LCS_ERR_UNSUPPORTED;
   AttendParams p;
-  lcs_status s = attend_common(batch, q, heads, entries, paging, state, out, workspace, workspace_bytes,
+  lcs_status s = attend_common(batch, q, heads, entries, paging, state, values, out, workspace, workspace_bytes,
                                batch ? batch->max_seq_len / m + LCSA_WINDOW : 0, p, false);
   if (s != LCS_OK) return s;
   p.m = m;

@@ -17,6 +17,8 @@
 //   softmax  online, in base 2, fp32; P (bf16) for the RoPE output dims and P*scale_row*2^8
 //            (f16) for the FP8 output dims;
 //   O += PV  every warp owns D/8 output columns for all heads of the CTA.
+// Separate values (SV): the stage holds the value rows' bytes next to the key rows'; once S is
+// computed the value rows are widened into the same tile and P2 takes the value row's scale.
 // Splits write (O, m, l) partials that a second kernel combines with the usual LSE rule.
 #include "kernels.cuh"
 
@@ -47,29 +49,34 @@ __device__ __forceinline__ int tile_off(int r, int c) {
 // Same for the [HG][RT] probability tiles (4 chunks per row).
 __device__ __forceinline__ int ptile_off(int r, int c) { return r * (kRT * 2) + ((c ^ ((r >> 1) & 3)) << 4); }
 
-template <int D, int FMT>
+// One stage: the key rows' stored bytes (codes / RoPE dims / scales), with SV the value rows' in
+// the same layout at kV, then the row-valid flags.
+template <int D, int FMT, bool SV>
 struct StageLayout {
   static constexpr int kNopeBytes = FMT == LCS_ROW_FP8_SPLIT ? (D - kRope) : D * 2;
   static constexpr int kRopeBytes = FMT == LCS_ROW_FP8_SPLIT ? kRope * 2 : 0;
   static constexpr int kNope = 0;
   static constexpr int kRopeOff = kRT * kNopeBytes;
   static constexpr int kScaleOff = kRopeOff + kRT * kRopeBytes;
-  static constexpr int kValidOff = kScaleOff + kRT * 4;
+  static constexpr int kPart = (kScaleOff + kRT * 4 + 127) / 128 * 128;
+  static constexpr int kV = kPart;
+  static constexpr int kValidOff = kPart * (SV ? 2 : 1);
   static constexpr int kBytes = ((kValidOff + kRT * 4) + 127) / 128 * 128;
 };
 
-template <int D, int FMT, int MT>
+template <int D, int FMT, int MT, bool SV = false>
 struct AttendSmem {
   static constexpr int HG = 16 * MT;
   static constexpr int kQ = 0;
   static constexpr int kR = kQ + HG * D * 2;
   static constexpr int kStage = kR + kRT * D * 2;
-  static constexpr int kS = kStage + kStages * StageLayout<D, FMT>::kBytes;
+  static constexpr int kS = kStage + kStages * StageLayout<D, FMT, SV>::kBytes;
   static constexpr int kSStride = kRT + 1;
   static constexpr int kP = kS + HG * kSStride * 4;
   static constexpr int kP2 = kP + HG * kRT * 2;
   static constexpr int kRowScale = kP2 + HG * kRT * 2;
-  static constexpr int kM = kRowScale + kRT * 4;
+  static constexpr int kVScale = kRowScale + kRT * 4;      // SV: the value rows' scales
+  static constexpr int kM = kVScale + (SV ? kRT * 4 : 0);
   static constexpr int kL = kM + HG * 4;
   static constexpr int kAlpha = kL + HG * 4;
   static constexpr int kDesc = kAlpha + HG * 4;              // long long [kDescRows]
@@ -86,10 +93,10 @@ __device__ __forceinline__ int find_seq(const int32_t* cu_new, int num_seqs, int
   return lo;
 }
 
-template <int D, int FMT, int MT>
+template <int D, int FMT, int MT, bool SV>
 __global__ void __launch_bounds__(256, 1) attend_kernel(AttendParams p) {
-  using L = AttendSmem<D, FMT, MT>;
-  using SL = StageLayout<D, FMT>;
+  using L = AttendSmem<D, FMT, MT, SV>;
+  using SL = StageLayout<D, FMT, SV>;
   constexpr int HG = L::HG;
   constexpr bool kSplitFmt = FMT == LCS_ROW_FP8_SPLIT;
   constexpr int kChunks = D / 8;
@@ -189,6 +196,17 @@ __global__ void __launch_bounds__(256, 1) attend_kernel(AttendParams p) {
       cp_async16_zfill(st + SL::kRopeOff + rr * SL::kRopeBytes + u * 16, src_rope + rw * SL::kRopeBytes + u * 16, nb);
       if (u == 0) cp_async4_zfill(st + SL::kScaleOff + rr * 4, src_scale + rw, ok ? 4 : 0);
     }
+    if (SV) {   // the value row with the same number in the matching value set
+      const Rows& vs = kind == 1 ? p.v_new_rows : (kind == 2 ? p.v_window : p.v_entries);
+      uint8_t* sv = st + SL::kV;
+      for (int c = u; c < SL::kNopeBytes / 16; c += 8)
+        cp_async16_zfill(sv + rr * SL::kNopeBytes + c * 16, vs.nope + rw * SL::kNopeBytes + c * 16, nb);
+      if (kSplitFmt) {
+        cp_async16_zfill(sv + SL::kRopeOff + rr * SL::kRopeBytes + u * 16,
+                         reinterpret_cast<const uint8_t*>(vs.rope) + rw * SL::kRopeBytes + u * 16, nb);
+        if (u == 0) cp_async4_zfill(sv + SL::kScaleOff + rr * 4, vs.scale + rw, ok ? 4 : 0);
+      }
+    }
     if (u == 0) reinterpret_cast<int*>(st + SL::kValidOff)[rr] = ok ? 1 : 0;
   };
 
@@ -270,24 +288,27 @@ __global__ void __launch_bounds__(256, 1) attend_kernel(AttendParams p) {
         *reinterpret_cast<uint4*>(w) = v;
       }
     }
-    // ---- widen the staged rows into the [RT][D] tile
+    // ---- widen the staged rows (key rows, then with SV the value rows) into the [RT][D] tile
     const uint8_t* st = smem + L::kStage + (ti % kStages) * SL::kBytes;
-    for (int idx = tid; idx < kRT * kChunks; idx += 256) {
-      const int r = idx / kChunks, c = idx % kChunks;
-      uint4 v;
-      if (!kSplitFmt) {
-        v = *reinterpret_cast<const uint4*>(st + r * SL::kNopeBytes + c * 16);
-      } else if (c < kRope / 8) {
-        v = *reinterpret_cast<const uint4*>(st + SL::kRopeOff + r * SL::kRopeBytes + c * 16);
-      } else {
-        const uint2 raw = *reinterpret_cast<const uint2*>(st + r * SL::kNopeBytes + (c - kRope / 8) * 8);
-        v.x = e4m3x2_to_f16x2(raw.x & 0xFFFF);
-        v.y = e4m3x2_to_f16x2(raw.x >> 16);
-        v.z = e4m3x2_to_f16x2(raw.y & 0xFFFF);
-        v.w = e4m3x2_to_f16x2(raw.y >> 16);
+    auto widen = [&](const uint8_t* src) {
+      for (int idx = tid; idx < kRT * kChunks; idx += 256) {
+        const int r = idx / kChunks, c = idx % kChunks;
+        uint4 v;
+        if (!kSplitFmt) {
+          v = *reinterpret_cast<const uint4*>(src + r * SL::kNopeBytes + c * 16);
+        } else if (c < kRope / 8) {
+          v = *reinterpret_cast<const uint4*>(src + SL::kRopeOff + r * SL::kRopeBytes + c * 16);
+        } else {
+          const uint2 raw = *reinterpret_cast<const uint2*>(src + r * SL::kNopeBytes + (c - kRope / 8) * 8);
+          v.x = e4m3x2_to_f16x2(raw.x & 0xFFFF);
+          v.y = e4m3x2_to_f16x2(raw.x >> 16);
+          v.z = e4m3x2_to_f16x2(raw.y & 0xFFFF);
+          v.w = e4m3x2_to_f16x2(raw.y >> 16);
+        }
+        *reinterpret_cast<uint4*>(Rs + tile_off<D>(r, c)) = v;
       }
-      *reinterpret_cast<uint4*>(Rs + tile_off<D>(r, c)) = v;
-    }
+    };
+    widen(st);
     const int* valid = reinterpret_cast<const int*>(st + SL::kValidOff);
     if (tid < kRT) {
       const bool ok = valid[tid] != 0 && tile_begin + tid < r_end;
@@ -295,6 +316,15 @@ __global__ void __launch_bounds__(256, 1) attend_kernel(AttendParams p) {
       if (ok && kSplitFmt && !(sc < kMaxRowScale)) {   // P * s * 2^8 would leave the f16 range
         report(p.status, LCS_ERR_DEVICE_GUARD);
         sc = -1.0f;
+      }
+      if (SV) {
+        // the value row's scale weights P2; a value row outside the bound leaves the row out
+        float vsc = ok ? (kSplitFmt ? reinterpret_cast<const float*>(st + SL::kV + SL::kScaleOff)[tid] : 1.0f) : -1.0f;
+        if (ok && kSplitFmt && !(vsc < kMaxRowScale)) {
+          report(p.status, LCS_ERR_DEVICE_GUARD);
+          sc = -1.0f;
+        }
+        reinterpret_cast<float*>(smem + L::kVScale)[tid] = vsc;
       }
       rscale[tid] = sc;
     }
@@ -353,6 +383,10 @@ __global__ void __launch_bounds__(256, 1) attend_kernel(AttendParams p) {
     }
     __syncthreads();
 
+    // the S MMAs have read the key rows: the value rows take their place (the softmax below
+    // touches neither)
+    if (SV) widen(st + SL::kV);
+
     // ---- online softmax over this tile
     {
       constexpr int TPH = 256 / HG;      // threads per head row
@@ -379,8 +413,8 @@ __global__ void __launch_bounds__(256, 1) attend_kernel(AttendParams p) {
         sum += pv;
         const __nv_bfloat16 bb = __float2bfloat16_rn(pv);
         pb[c] = *reinterpret_cast<const uint16_t*>(&bb);
-        const float s = rscale[c0 + c];
-        const __half hh = __float2half_rn(pv * fmaxf(s, 0.0f) * kP2Scale);
+        const float s = SV ? reinterpret_cast<const float*>(smem + L::kVScale)[c0 + c] : rscale[c0 + c];
+        const __half hh = __float2half_rn(fminf(pv * fmaxf(s, 0.0f) * kP2Scale, 65504.0f));
         p2[c] = *reinterpret_cast<const uint16_t*>(&hh);
       }
 #pragma unroll
@@ -533,17 +567,18 @@ __global__ void __launch_bounds__(D / 4) attend_combine_kernel(AttendParams p) {
 // launch
 // ----------------------------------------------------------------------------------------------
 
-template <int D, int FMT, int MT>
+template <int D, int FMT, int MT, bool SV>
 static cudaError_t launch_attend_t(const AttendParams& p, int total_new, cudaStream_t st) {
-  using L = AttendSmem<D, FMT, MT>;
+  using L = AttendSmem<D, FMT, MT, SV>;
+  static_assert(L::kBytes <= 227 * 1024, "shared memory of one CTA");
   static PerDeviceOnce attr;
   cudaError_t ea = once_per_device(attr, [] {
-    return cudaFuncSetAttribute(attend_kernel<D, FMT, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+    return cudaFuncSetAttribute(attend_kernel<D, FMT, MT, SV>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
   });
   if (ea != cudaSuccess) return ea;
   const int hgroups = (p.heads + L::HG - 1) / L::HG;
   dim3 grid(total_new, hgroups, p.splits);
-  attend_kernel<D, FMT, MT><<<grid, 256, L::kBytes, st>>>(p);
+  attend_kernel<D, FMT, MT, SV><<<grid, 256, L::kBytes, st>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || p.splits == 1) return e;
   attend_combine_kernel<D><<<dim3(total_new, p.heads), D / 4, 0, st>>>(p);
@@ -563,20 +598,25 @@ size_t attend_smem_bytes(int D, int fmt, int heads) {
   return small ? AttendSmem<128, LCS_ROW_FP8_SPLIT, 1>::kBytes : AttendSmem<128, LCS_ROW_FP8_SPLIT, 4>::kBytes;
 }
 
+template <bool SV>
+static cudaError_t launch_attend_sv(const AttendParams& p, int D, int fmt, int total_new, cudaStream_t st) {
+  const bool small = p.heads <= 16;
+  if (D == 512) {
+    if (small) return launch_attend_t<512, LCS_ROW_FP8_SPLIT, 1, SV>(p, total_new, st);
+    return launch_attend_t<512, LCS_ROW_FP8_SPLIT, 4, SV>(p, total_new, st);
+  }
+  if (fmt == LCS_ROW_BF16) {
+    if (small) return launch_attend_t<128, LCS_ROW_BF16, 1, SV>(p, total_new, st);
+    return launch_attend_t<128, LCS_ROW_BF16, 4, SV>(p, total_new, st);
+  }
+  if (small) return launch_attend_t<128, LCS_ROW_FP8_SPLIT, 1, SV>(p, total_new, st);
+  return launch_attend_t<128, LCS_ROW_FP8_SPLIT, 4, SV>(p, total_new, st);
+}
+
 cudaError_t launch_attend(const AttendParams& p, int D, int fmt, int total_new, cudaStream_t st) {
   if (total_new == 0) return cudaSuccess;
   if (p.tc) return launch_attend_tc(p, total_new, st);
-  const bool small = p.heads <= 16;
-  if (D == 512) {
-    if (small) return launch_attend_t<512, LCS_ROW_FP8_SPLIT, 1>(p, total_new, st);
-    return launch_attend_t<512, LCS_ROW_FP8_SPLIT, 4>(p, total_new, st);
-  }
-  if (fmt == LCS_ROW_BF16) {
-    if (small) return launch_attend_t<128, LCS_ROW_BF16, 1>(p, total_new, st);
-    return launch_attend_t<128, LCS_ROW_BF16, 4>(p, total_new, st);
-  }
-  if (small) return launch_attend_t<128, LCS_ROW_FP8_SPLIT, 1>(p, total_new, st);
-  return launch_attend_t<128, LCS_ROW_FP8_SPLIT, 4>(p, total_new, st);
+  return p.sv ? launch_attend_sv<true>(p, D, fmt, total_new, st) : launch_attend_sv<false>(p, D, fmt, total_new, st);
 }
 
 }  // namespace lcsa

@@ -107,6 +107,10 @@ struct AttendParams {
   Paging paging;
   Rows window;
   Rows new_rows;
+  int sv;                    // 1: separate value rows (warp-MMA kernel only)
+  Rows v_entries;            // value rows numbered like entries / window / new_rows
+  Rows v_window;
+  Rows v_new_rows;
   float scale_log2;
   __nv_bfloat16* out;
   float* out_lse;

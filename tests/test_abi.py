@@ -31,7 +31,7 @@ def test_library_exports_every_declared_symbol():
 
 def test_abi_version_and_status_strings():
     import long_context_sparse_24_b300 as lcsa
-    assert lcsa.lcs_abi_version() == 2
+    assert lcsa.lcs_abi_version() == 3
     assert lcsa.lcs_status_string(0) == "ok"
     assert "workspace" in lcsa.lcs_status_string(8)
 
@@ -79,10 +79,44 @@ def test_host_validation_without_gpu():
                             0x4000, 0x8000, 1 << 20, None, None) == 1
     assert lcsa.LCS_INDEX_SPARE_SMS(32) == 32 << 8 and lcsa.LCS_INDEX_SPARE_SMS(300) == (300 & 0xFF) << 8
     # attention: heads 24 unsupported; topk list missing
-    assert L.csa_attend(by(_batch(lcsa)), 0x1000, 24, 0x2000, None, 16, 4, by(rows), by(pag), by(st), 1.0,
+    assert L.csa_attend(by(_batch(lcsa)), 0x1000, 24, 0x2000, None, 16, 4, by(rows), by(pag), by(st), None, 1.0,
                         0x3000, None, None, 0, None, None) == 4
-    assert L.csa_attend(by(_batch(lcsa)), 0x1000, 64, None, None, 16, 4, by(rows), by(pag), by(st), 1.0,
+    assert L.csa_attend(by(_batch(lcsa)), 0x1000, 64, None, None, 16, 4, by(rows), by(pag), by(st), None, 1.0,
                         0x3000, None, None, 0, None, None) == 1
+
+
+def test_separate_values_host_validation():
+    """Value sets must match their key counterparts' format, dim and row count, and come with new
+    rows exactly when the state has them; a matching set passes to the workspace check."""
+    import long_context_sparse_24_b300 as lcsa
+    L = lcsa._lib
+    by = ctypes.byref
+    fp8 = lambda n: lcsa.lcs_rows(lcsa.LCS_ROW_FP8_SPLIT, 512, n, 0x1000, 0x2000, 0x3000)
+    entries, ring, new = fp8(64), fp8(128), fp8(4)
+    pag = lcsa.lcs_paging(32, 2, 0x4000)
+    st = lcsa.lcs_state(ring, 0x5000, 8, new)
+    b = _batch(lcsa)
+    call = lambda v, heads=64: L.csa_attend(by(b), 0x1000, heads, 0x2000, None, 16, 4, by(entries), by(pag), by(st),
+                                            by(v) if v is not None else None, 1.0, 0x3000, None, None, 0, None, None)
+    hcall = lambda v: L.hca_attend(by(b), 0x1000, 64, 128, by(entries), by(pag), by(st), by(v), 1.0, 0x3000, None,
+                                   None, 0, None, None)
+    good = lcsa.lcs_values(fp8(64), fp8(128), fp8(4))
+    # one value set with fewer rows, another format, new rows missing
+    assert call(lcsa.lcs_values(fp8(63), fp8(128), fp8(4))) == 2
+    assert call(lcsa.lcs_values(fp8(64), fp8(129), fp8(4))) == 2
+    assert call(lcsa.lcs_values(fp8(64), fp8(128), fp8(5))) == 2
+    bf = lcsa.lcs_rows(lcsa.LCS_ROW_BF16, 512, 64, 0x1000, None, None)
+    assert call(lcsa.lcs_values(bf, fp8(128), fp8(4))) == 2
+    assert call(lcsa.lcs_values(fp8(64), fp8(128), lcsa.lcs_rows(lcsa.LCS_ROW_FP8_SPLIT, 512, 0, None, None, None))) == 2
+    # a value set without its scales, or misaligned
+    assert call(lcsa.lcs_values(lcsa.lcs_rows(lcsa.LCS_ROW_FP8_SPLIT, 512, 64, 0x1000, 0x2000, None), fp8(128),
+                                fp8(4))) == 1
+    assert call(lcsa.lcs_values(lcsa.lcs_rows(lcsa.LCS_ROW_FP8_SPLIT, 512, 64, 0x1008, 0x2000, 0x3000), fp8(128),
+                                fp8(4))) == 3
+    # matching sets get as far as the workspace check (none given), as do calls without values
+    assert call(good) == 8 and call(None) == 8
+    assert hcall(good) == 8
+    assert hcall(lcsa.lcs_values(fp8(64), fp8(100), fp8(4))) == 2
 
 
 def test_stage_copy_host_validation():

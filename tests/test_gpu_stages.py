@@ -304,12 +304,13 @@ def test_topk_ties_take_lowest_index():
 # ---------------------------------------------------------------------------------------- attention
 
 def _attend_case(kind, lengths, new, heads, dim, fmt, m, k, seed=41, scale=None, split=False, sink=None,
-                 corrupt_seq=None, rows_hook=None, skip_seq=None, expect_status=None):
+                 corrupt_seq=None, rows_hook=None, skip_seq=None, expect_status=None, separate_v=False):
     """Fill an entry cache / window ring / new rows with oracle-quantised rows and run one call.
     corrupt_seq: unmap that sequence's first cache block before the call (host-side corruption of
     the block table); the call must then report LCS_ERR_DEVICE_GUARD and every other sequence must
     still match the oracle.  rows_hook(b, entry_rows): may change a sequence's entry rows (fp64)
-    before they are quantised.  expect_status: the device status the call must report (outputs
+    before they are quantised.  separate_v: value rows of their own (entries, window ring and new
+    rows numbered like the key rows, drawn from other streams) passed as `values`.  expect_status: the device status the call must report (outputs
     are not checked when it is LCS_ERR_TIMEOUT); skip_seq: a sequence whose outputs are not
     checked."""
     S = len(lengths)
@@ -321,6 +322,13 @@ def _attend_case(kind, lengths, new, heads, dim, fmt, m, k, seed=41, scale=None,
     batch = buffers.make_batch(lengths, new, DEV, max_seq_len=cap)
     rng = np.random.default_rng(seed)
     ent_deq, win_deq, sels, qs = [], [], [], []
+    vals, vent_deq, vwin_deq = None, [], []
+    if separate_v:
+        vals = lcsa.Values(buffers.alloc_rows(fmtc, dim, cache.entries.num_rows, DEV),
+                           buffers.alloc_rows(fmtc, dim, cache.state.window.num_rows, DEV),
+                           buffers.alloc_rows(fmtc, dim, cache.state.new_rows.num_rows, DEV)
+                           if cache.state.new_rows is not None else None)
+        vrng = np.random.default_rng(seed + 1)
     for b in range(S):
         L, q_n = lengths[b], new[b]
         n0 = L - q_n
@@ -350,6 +358,25 @@ def _attend_case(kind, lengths, new, heads, dim, fmt, m, k, seed=41, scale=None,
         q0 = sum(new[:b])
         if q_n:
             write_rows(cache.state.new_rows, np.arange(q0, q0 + q_n), sub)
+        if separate_v:
+            # value rows with the key rows' numbers: entries, ring and new rows
+            vent = oracle.quantize_rows(vrng.standard_normal((max(ne, 1), dim)) * 3.0, fmt)
+            if ne:
+                sub = {kk: v[:ne] for kk, v in vent.items() if kk != "format"}
+                sub["format"] = vent["format"]
+                write_rows(vals.entries, entry_rows_of(cache, b, range(ne)), sub)
+            vent_deq.append(vent["deq"][:ne])
+            vq = oracle.quantize_rows(bits_to_f64(raw_rows_np(seed, 1, b, L - p_lo, dim, start=p_lo)), fmt)
+            vd = np.zeros((L, dim)); vd[p_lo:L] = vq["deq"]
+            vwin_deq.append(vd)
+            if ring_pos.size:
+                sub = {kk: v[:n0 - p_lo] for kk, v in vq.items() if kk not in ("format", "deq")}
+                sub["format"] = vq["format"]
+                write_rows(vals.window, b * 128 + ring_pos % 128, sub)
+            if q_n:
+                sub = {kk: v[n0 - p_lo:] for kk, v in vq.items() if kk not in ("format", "deq")}
+                sub["format"] = vq["format"]
+                write_rows(vals.new_rows, np.arange(q0, q0 + q_n), sub)
         for i in range(q_n):
             t = n0 + i
             n = oracle.visible_entries(t, m)
@@ -378,23 +405,23 @@ def _attend_case(kind, lengths, new, heads, dim, fmt, m, k, seed=41, scale=None,
             side = torch.cuda.Stream()
             side.wait_stream(torch.cuda.current_stream())
             lcsa.csa_attend_window(batch, q, heads, k, m, cache.entries, cache.paging, cache.state, scale, ws, wsb,
-                                   st, stream=side)
+                                   st, stream=side, values=vals)
             torch.cuda.current_stream().wait_stream(side)
             lcsa.csa_attend_topk(batch, q, heads, idx_t, cnt_t, k, m, cache.entries, cache.paging, cache.state,
-                                 scale, out, lse, ws, wsb, st)
+                                 scale, out, lse, ws, wsb, st, values=vals)
             # the one call plans the window rows into the entries' list (other splits, so other
             # rounding): it is checked against the oracle as well
             one_out = torch.empty_like(out)
             one_lse = torch.empty_like(lse)
             lcsa.csa_attend(batch, q, heads, idx_t, cnt_t, k, m, cache.entries, cache.paging, cache.state, scale,
-                            one_out, one_lse, workspace(wsb), wsb, st)
+                            one_out, one_lse, workspace(wsb), wsb, st, values=vals)
         else:
             lcsa.csa_attend(batch, q, heads, idx_t, cnt_t, k, m, cache.entries, cache.paging, cache.state, scale, out,
-                            lse, workspace(wsb), wsb, st)
+                            lse, workspace(wsb), wsb, st, values=vals)
     else:
         wsb = lcsa.lcs_attend_workspace(batch, heads, dim, cap // m + 128)
         lcsa.hca_attend(batch, q, heads, m, cache.entries, cache.paging, cache.state, scale, out, lse,
-                        workspace(wsb), wsb, st)
+                        workspace(wsb), wsb, st, values=vals)
     if sink is not None:
         lcsa.lcs_attention_sink(out, lse, torch.from_numpy(sink.astype(np.float32)).to(DEV))
         if kind == "csa" and split:
@@ -419,14 +446,20 @@ def _attend_case(kind, lengths, new, heads, dim, fmt, m, k, seed=41, scale=None,
                 continue
             for i in range(new[b]):
                 t = n0 + i
+                vrows = None
                 if kind == "csa":
                     rows = oracle.csa_query_rows(t, sels[qi], ent_deq[b], win_deq[b])
+                    if separate_v:
+                        vrows = oracle.csa_query_rows(t, sels[qi], vent_deq[b], vwin_deq[b])
                 else:
                     rows = oracle.hca_query_rows(t, m, ent_deq[b], win_deq[b])
+                    if separate_v:
+                        vrows = oracle.hca_query_rows(t, m, vent_deq[b], vwin_deq[b])
                 if sink is None:
-                    ro, rl = oracle.attend(qf[qi], rows, scale)
+                    ro, rl = oracle.attend(qf[qi], rows, scale, values=vrows)
                 else:
-                    ro, rl = oracle.attend_with_sink(qf[qi], rows, scale, sink.astype(np.float32).astype(np.float64))
+                    ro, rl = oracle.attend_with_sink(qf[qi], rows, scale, sink.astype(np.float32).astype(np.float64),
+                                                     values=vrows)
                 check_outputs(o[qi], ro, f"{kind} seq {b} query {i}{tag}")
                 assert np.allclose(l[qi], rl, atol=2e-3, rtol=1e-4), f"lse seq {b} query {i}{tag}"
                 qi += 1
@@ -450,6 +483,23 @@ def _attend_case(kind, lengths, new, heads, dim, fmt, m, k, seed=41, scale=None,
 ])
 def test_attend_matches_oracle(kind, lengths, new, heads, dim, fmt, m, k):
     _attend_case(kind, lengths, new, heads, dim, fmt, m, k)
+
+
+@pytest.mark.parametrize("kind,lengths,new,heads,dim,fmt,m,k,split", [
+    ("csa", [2000, 4100, 300], [1, 1, 1], 64, 512, "fp8_split", 4, 512, False),   # decode
+    ("csa", [2000, 4100, 300], [1, 1, 1], 64, 512, "fp8_split", 4, 512, True),    # two calls
+    ("csa", [900, 2200], [40, 9], 64, 512, "fp8_split", 4, 64, False),            # prefill chunk
+    ("csa", [3000], [3], 96, 512, "fp8_split", 4, 256, False),                    # partial head group
+    ("csa", [130, 7], [1, 7], 16, 512, "fp8_split", 4, 32, False),                # N(t) < k
+    ("hca", [20000, 1500, 128], [1, 1, 1], 64, 512, "fp8_split", 128, 0, False),
+    ("hca", [3000], [17], 128, 512, "fp8_split", 128, 0, False),
+    ("csa", [50, 700], [50, 20], 8, 128, "bf16", 4, 64, False),
+    ("csa", [600], [5], 8, 128, "fp8_split", 4, 64, False),
+])
+def test_attend_separate_values_matches_oracle(kind, lengths, new, heads, dim, fmt, m, k, split):
+    """Separate value rows (a value set numbered like each key set) against the oracle's attention
+    with values apart from keys."""
+    _attend_case(kind, lengths, new, heads, dim, fmt, m, k, split=split, separate_v=True)
 
 
 @pytest.mark.parametrize("kind,lengths,new,heads,dim,fmt,m,k,split", [
