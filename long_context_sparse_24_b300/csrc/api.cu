@@ -159,7 +159,7 @@ TopkWs topk_ws_layout(const lcs_batch* b, const IndexParams& p, int rank, int m,
     w.tau = w.cnt + round256(T * w.plan.runs * 4);
     w.keys = w.tau + round256(T * w.plan.runs * 8);
     w.hist = w.keys;
-    w.total = w.keys + T * w.plan.runs * (size_t)k * 8 + 256;
+    w.total = w.keys + T * w.plan.runs * (size_t)w.plan.list_cap * 8 + 256;
   } else {
     w.keys = body;
     w.hist = w.keys + round256(T * (size_t)index_ld(b, m) * 4);
@@ -499,6 +499,7 @@ lcs_status csa_index_topk(const lcs_batch* batch, const uint8_t* q_fp4, const ui
     // (a scoring call on its own shares no threshold: the counters stay zero without a merge)
     p.runs.gthr = score_only || select_only ? nullptr : reinterpret_cast<uint64_t*>(ws + w.gthr);
     p.runs.keys = reinterpret_cast<uint64_t*>(ws + w.keys);
+    p.runs.list_cap = w.plan.list_cap;
     p.out_idx = out_idx;
     p.out_cnt = out_cnt;
     if (select_only) return from_cuda(launch_topk_merge(p, w.plan, batch->max_new, st));

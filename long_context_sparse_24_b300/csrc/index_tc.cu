@@ -38,11 +38,12 @@
 // buffer past cap - 256 is cut by a radix selection that stops at a digit bin leaving k to
 // k + k/8 keys, whose lower edge becomes the threshold -- published to the query's other runs,
 // whose thresholds are just as valid (each is at most the query's k-th largest key).  At the end
-// of its run a CTA writes its k largest keys (exact selection), ascending in j, their count and
-// its threshold to the workspace; the sequence's last CTA to finish (a ticket counter, left at
-// zero again) merges the runs' lists: the largest of the runs' thresholds bounds the selection
-// from below, the k-th largest key comes from the same radix selection, and the staged lists are
-// read out in ascending j.  A separate merge kernel does the same when the scoring phase runs
+// of its run a CTA writes its keys at or above a threshold that k to k + k/4 of them reach (the
+// same radix selection, stopped at a digit bin), ascending in j, their count and that threshold
+// to the workspace; the sequence's last CTA to finish (a ticket counter, left at zero again)
+// merges the runs' lists: the largest of the runs' thresholds bounds the selection from below, the
+// k-th largest key comes from the exact radix selection, and the staged lists are read out in
+// ascending j.  A separate merge kernel does the same when the scoring phase runs
 // alone or the lists do not fit the CTA's shared memory.  FUSED = false writes the fp32 scores
 // themselves (csa_index_scores).
 #include <algorithm>
@@ -56,7 +57,11 @@ namespace lcsa {
 namespace {
 
 constexpr int kTile = 128;          // entries per MMA tile (M)
-constexpr int kStages = 10;         // shared-memory ring depth (tiles in flight per CTA)
+// shared-memory ring depth (tiles in flight per CTA): the shallow ring leaves room for candidate
+// buffers that take a whole run without a compaction; the deep one, for long runs with long lists,
+// lets the last CTA stage every run's list in the idle ring
+constexpr int kStagesShallow = 6;
+constexpr int kStagesDeep = 10;
 constexpr int kAcc = 8;             // tensor-memory accumulators at most (the MMA runs up to 8 tiles ahead)
 constexpr int kSfCols = 8;          // tensor-memory columns of the (unit) scale factors
 constexpr int kMaxPages = 8192;     // block-table entries a CTA's run may span
@@ -66,17 +71,18 @@ constexpr int kATileBytes = kTile * kRowBytes;
 constexpr int kEpiWarps = 8;        // two per TMEM lane quadrant, the two tiles of a pair
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kProdWarps = 2;       // producer warps, alternating tiles
-// block-scale ring: tile i's scales are copied once stage i % kStages is free (the MMA of tile
-// i - kStages is done, so the epilogue has read tile i - kStages - accumulators); they are read
-// by the epilogue of tile i, so kStages + kAcc tiles' scales can be live at once
-constexpr int kScaleSlots = kStages + kAcc;
 constexpr int kThreads = kEpiThreads + 32 * kProdWarps + 32;
-constexpr int kCandPerThread = 16;  // candidate buffer per query <= kEpiThreads * kCandPerThread
+constexpr int kCandPerThread = 16;  // keys a thread holds in registers in one block of a compaction
 constexpr int kEpiBarrier = 1;      // named barrier of the epilogue warps
 constexpr int kMaxRuns = 256;       // CTAs per sequence (run lists a merge reads)
 
-template <int QH, int QPS>
+// block-scale ring: tile i's scales are copied once stage i % kStages is free (the MMA of tile
+// i - kStages is done, so the epilogue has read tile i - kStages - accumulators); they are read
+// by the epilogue of tile i, so kStages + kAcc tiles' scales can be live at once
+template <int QH, int QPS, int ST>
 struct TcSmem {
+  static constexpr int kStages = ST;
+  static constexpr int kScaleSlots = ST + kAcc;
   static constexpr int N = 4 * QH;                            // MMA N: (block, query-head) columns
   static constexpr int kA = 0;                                // kStages x 8 KB, 1024-aligned
   static constexpr int kB = kA + kStages * kATileBytes;       // N x 64 B
@@ -163,8 +169,8 @@ __device__ int write_run_sorted(const uint64_t* buf, int n, uint64_t tau, int j0
 // index and the runs cover increasing index ranges, so the lists read one after the other are
 // sorted too: they are staged in shared memory (stage: room for stage_cap keys), the k-th largest
 // key is selected, and the staged keys at or above it are read out in that order.  Every run
-// recorded a threshold at most the query's k-th largest key, with all of its keys at or above it
-// in its list; the largest of those bounds the selection from below, so the keys at or above it
+// recorded a threshold at most the query's k-th largest key (at least k of the run's keys, or all
+// of them, are at or above it), with all of its keys at or above it in its list; the largest of those bounds the selection from below, so the keys at or above it
 // are gathered as candidates while staging (cand: room for cand_cap keys; when more pass, the
 // selection runs over the stage).  N: visible entries of the query; run_off: runs + 1 ints of
 // shared memory; hist: 1 << BITS counters of shared memory.
@@ -180,11 +186,12 @@ __device__ void merge_query_topk(const TopkRuns& tr, long long q, int N, int k, 
     return;
   }
   const int* cnts = tr.cnt + q * tr.runs;
-  const unsigned long long* keys = reinterpret_cast<const unsigned long long*>(tr.keys) + q * (long long)tr.runs * k;
+  const int lcap = tr.list_cap;
+  const unsigned long long* keys = reinterpret_cast<const unsigned long long*>(tr.keys) + q * (long long)tr.runs * lcap;
   // list offsets in the stage, and the bound: the largest threshold of the runs (runs <= 256 <= NT)
   uint64_t bound;
   {
-    const int c = tid < tr.runs ? min(__ldcg(cnts + tid), k) : 0;
+    const int c = tid < tr.runs ? min(__ldcg(cnts + tid), lcap) : 0;
     unsigned long long t = tid < tr.runs ? __ldcg(reinterpret_cast<const unsigned long long*>(tr.tau) + q * tr.runs + tid)
                                          : 0ull;
 #pragma unroll
@@ -212,7 +219,7 @@ __device__ void merge_query_topk(const TopkRuns& tr, long long q, int N, int k, 
   for (int r = warp; r < tr.runs; r += NT / 32) {
     const int o = run_off[r];
     const int c = min(run_off[r + 1], total) - o;
-    const unsigned long long* src = keys + (long long)r * k;
+    const unsigned long long* src = keys + (long long)r * lcap;
     for (int x0 = 0; x0 < c; x0 += 32 * kU) {
       uint64_t v[kU];
 #pragma unroll
@@ -267,12 +274,14 @@ __device__ void merge_query_topk(const TopkRuns& tr, long long q, int N, int k, 
 // grid: (runs, query groups, num_seqs); block kThreads.  CTA (x, g, b) scans tiles
 // [x*tiles_per_cta, (x+1)*tiles_per_cta) of sequence b (clipped to its visible entries) for the
 // sequence's queries g*QPS .. g*QPS + QPS - 1.
-template <int HI, int QH, bool FUSED>
+template <int HI, int QH, bool FUSED, int ST>
 __global__ void __launch_bounds__(kThreads, QH >= 16 ? 1 : 2) index_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                                                            const __grid_constant__ CUtensorMap tmap_t, IndexParams p,
                                                            int tiles_per_cta) {
   constexpr int QPS = QH / HI;
-  using L = TcSmem<QH, QPS>;
+  using L = TcSmem<QH, QPS, ST>;
+  constexpr int kStages = L::kStages;
+  constexpr int kScaleSlots = L::kScaleSlots;
   constexpr int N = L::N;
   constexpr uint32_t kCols = tmem_cols_for(N);
   constexpr int kAccN = acc_for(N);
@@ -655,16 +664,17 @@ __global__ void __launch_bounds__(kThreads, QH >= 16 ? 1 : 2) index_tc_kernel(co
     for (int qi = 0; qi < qn; ++qi) {
       const int n = cnt_s[qi];
       const uint64_t* buf = cand_s + qi * cap;
-      // the run's list: its k largest keys, or all of them at or above the current threshold when
-      // fewer pass it (the buffer holds every key of the run at or above that threshold)
+      // the run's list: its keys at or above a digit bin's lower edge with k to list_cap keys at or
+      // above it, or all of them at or above the current threshold when fewer pass it (the buffer
+      // holds every key of the run at or above that threshold); the merge selects exactly
       const uint64_t lo = thr_s[qi];
       uint64_t tau = lo;
       if (n > 0) {
-        const SelResult r = select_top<kThreads, 0, 11>(buf, n, k, 0, sel_all, hist, lo);
+        const SelResult r = select_top<kThreads, 0, 11>(buf, n, k, p.runs.list_cap - k, sel_all, hist, lo);
         tau = r.tau > lo ? r.tau : lo;
       }
       const long long q = qrow0 + qi;
-      uint64_t* dst = p.runs.keys + (q * p.runs.runs + blockIdx.x) * (long long)k;
+      uint64_t* dst = p.runs.keys + (q * p.runs.runs + blockIdx.x) * (long long)p.runs.list_cap;
       const int w = write_run_sorted<kThreads, 0>(buf, n, tau, t_begin * kTile, words, run_bits, run_prefix, dst,
                                                    sel_all);
       if (tid == 0) {
@@ -731,7 +741,7 @@ __global__ void __launch_bounds__(256) topk_merge_kernel(IndexParams p) {
   uint64_t* stage = reinterpret_cast<uint64_t*>(merge_smem + kMergeStage);
   const int t = sp.n0() + i;
   // (the stage holds the lists; the selection reads them with the lower bound, no candidate array)
-  merge_query_topk<256, 0, 11>(p.runs, sp.q0 + i, (t + 1) / p.m, p.top_k, stage, p.runs.runs * p.top_k, nullptr, 0,
+  merge_query_topk<256, 0, 11>(p.runs, sp.q0 + i, (t + 1) / p.m, p.top_k, stage, p.runs.runs * p.runs.list_cap, nullptr, 0,
                                run_off, hist, p.out_idx, p.out_cnt, sc);
   if (threadIdx.x == 0 && p.runs.gthr != nullptr) p.runs.gthr[sp.q0 + i] = 0ull;   // left at zero
 }
@@ -743,39 +753,51 @@ __global__ void __launch_bounds__(256) topk_merge_kernel(IndexParams p) {
 namespace {
 
 template <int HI, int QH>
-size_t tc_smem_bytes(bool fused, int cap, int pages) {
-  return TcSmem<QH, QH / HI>::bytes(fused, cap, pages);
+size_t tc_smem_bytes(bool fused, int cap, int pages, int stages) {
+  return stages == kStagesShallow ? TcSmem<QH, QH / HI, kStagesShallow>::bytes(fused, cap, pages)
+                                  : TcSmem<QH, QH / HI, kStagesDeep>::bytes(fused, cap, pages);
 }
 
-size_t tc_smem_for(int heads, int qh, bool fused, int cap, int pages) {
+size_t tc_smem_for(int heads, int qh, bool fused, int cap, int pages, int stages) {
   switch (heads * 100 + qh) {
-    case 104: return tc_smem_bytes<1, 4>(fused, cap, pages);
-    case 204: return tc_smem_bytes<2, 4>(fused, cap, pages);
-    case 208: return tc_smem_bytes<2, 8>(fused, cap, pages);
-    case 404: return tc_smem_bytes<4, 4>(fused, cap, pages);
-    case 408: return tc_smem_bytes<4, 8>(fused, cap, pages);
-    case 416: return tc_smem_bytes<4, 16>(fused, cap, pages);
-    case 808: return tc_smem_bytes<8, 8>(fused, cap, pages);
-    case 816: return tc_smem_bytes<8, 16>(fused, cap, pages);
+    case 104: return tc_smem_bytes<1, 4>(fused, cap, pages, stages);
+    case 204: return tc_smem_bytes<2, 4>(fused, cap, pages, stages);
+    case 208: return tc_smem_bytes<2, 8>(fused, cap, pages, stages);
+    case 404: return tc_smem_bytes<4, 4>(fused, cap, pages, stages);
+    case 408: return tc_smem_bytes<4, 8>(fused, cap, pages, stages);
+    case 416: return tc_smem_bytes<4, 16>(fused, cap, pages, stages);
+    case 808: return tc_smem_bytes<8, 8>(fused, cap, pages, stages);
+    case 816: return tc_smem_bytes<8, 16>(fused, cap, pages, stages);
     default: return 0;
   }
 }
 
-template <int HI, int QH, bool FUSED>
-cudaError_t launch_tc_t(const CUtensorMap& tmap, const CUtensorMap& tmap_t, const IndexParams& p,
-                        const IndexTcPlan& plan, cudaStream_t st) {
+template <int HI, int QH, bool FUSED, int ST>
+cudaError_t launch_tc_st(const CUtensorMap& tmap, const CUtensorMap& tmap_t, const IndexParams& p,
+                         const IndexTcPlan& plan, cudaStream_t st) {
   static PerDeviceOnce attr;
   cudaError_t ea = once_per_device(attr, [] {
-    cudaError_t e = cudaFuncSetAttribute(index_tc_kernel<HI, QH, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         227 * 1024);
+    cudaError_t e = cudaFuncSetAttribute(index_tc_kernel<HI, QH, FUSED, ST>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(index_tc_kernel<HI, QH, FUSED>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+      e = cudaFuncSetAttribute(index_tc_kernel<HI, QH, FUSED, ST>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               100);
     return e;
   });
   if (ea != cudaSuccess) return ea;
   dim3 grid(plan.runs, plan.groups, p.num_seqs);
-  index_tc_kernel<HI, QH, FUSED><<<grid, kThreads, plan.smem, st>>>(tmap, tmap_t, p, plan.tpc);
+  index_tc_kernel<HI, QH, FUSED, ST><<<grid, kThreads, plan.smem, st>>>(tmap, tmap_t, p, plan.tpc);
   return cudaGetLastError();
+}
+
+// the scores alone always take the deep ring (no candidate buffers to make room for)
+template <int HI, int QH, bool FUSED>
+cudaError_t launch_tc_t(const CUtensorMap& tmap, const CUtensorMap& tmap_t, const IndexParams& p,
+                        const IndexTcPlan& plan, cudaStream_t st) {
+  if constexpr (FUSED) {
+    if (plan.stages == kStagesShallow) return launch_tc_st<HI, QH, true, kStagesShallow>(tmap, tmap_t, p, plan, st);
+  }
+  return launch_tc_st<HI, QH, FUSED, kStagesDeep>(tmap, tmap_t, p, plan, st);
 }
 
 template <bool FUSED>
@@ -815,7 +837,9 @@ int index_tc_qh(const IndexParams& p, int rank, int max_new, bool groups) {
 }
 
 // The scorer's grid and shared memory; with k > 0 the fused top-k (applies = 0 when the
-// candidate buffers or the merge bitmap do not fit).
+// candidate buffers or the merge bitmap do not fit).  The fused top-k takes the shallow ring when
+// the last CTA can stage every run's list in it (its candidate buffers then have room for about
+// 4 KB more keys each), else the deep ring.
 IndexTcPlan plan_index_tc(const IndexParams& p, int rank, int max_new, int max_entries, int num_seqs, int sms, int k) {
   IndexTcPlan plan{};
   const bool fused = k > 0;
@@ -837,37 +861,52 @@ IndexTcPlan plan_index_tc(const IndexParams& p, int rank, int max_new, int max_e
   const int occ_tmem = std::min(512 / (int)tmem_cols_for(4 * plan.qh), plan.qh >= 16 ? 1 : 2);
   // a compaction keeps at most k + k/8 keys and leaves room for the epilogue's next two tiles
   const int cap_min = fused ? (k + (k >> 3) + 2 * kTile + 15) / 16 * 16 : 0;
-  if (fused && cap_min > kEpiThreads * kCandPerThread) return plan;
-  // two resident CTAs per SM when their shared memory allows it, else one
-  for (int occ = std::min(2, occ_tmem); occ >= 1; --occ) {
-    int runs = std::max(1, (sms * occ) / std::max(1, num_seqs * plan.groups));   // about one wave
-    int tpc = std::max(tpc_min, std::min(tpc_cap, (tiles + runs - 1) / runs));
-    runs = (tiles + tpc - 1) / tpc;
-    const int pages = tpc * kTile / epb + 1;
-    const long long budget = (long long)(228 * 1024 / occ) - 1024;
-    const long long base = (long long)tc_smem_for(p.heads, plan.qh, fused, 0, pages);
-    if (base + 8ll * qps * cap_min > std::min<long long>(budget, 227 * 1024)) continue;
-    int cap = cap_min;
-    if (fused) {   // more candidate room while it fits: fewer compactions
-      const int fit = (int)((std::min<long long>(budget, 227 * 1024) - base) / (8ll * qps)) / (2 * kTile) * (2 * kTile);
-      cap = std::max(cap_min, std::min({fit, 4 * k + 2 * kTile, kEpiThreads * kCandPerThread}));
+  auto attempt = [&](int stages) {
+    IndexTcPlan pl = plan;
+    pl.stages = stages;
+    // two resident CTAs per SM when their shared memory allows it, else one
+    for (int occ = std::min(2, occ_tmem); occ >= 1; --occ) {
+      int runs = std::max(1, (sms * occ) / std::max(1, num_seqs * pl.groups));   // about one wave
+      int tpc = std::max(tpc_min, std::min(tpc_cap, (tiles + runs - 1) / runs));
+      runs = (tiles + tpc - 1) / tpc;
+      const int pages = tpc * kTile / epb + 1;
+      const long long budget = std::min<long long>((long long)(228 * 1024 / occ) - 1024, 227 * 1024);
+      const long long base = (long long)tc_smem_for(p.heads, pl.qh, fused, 0, pages, stages);
+      if (base + 8ll * qps * cap_min > budget) continue;
+      int cap = cap_min;
+      if (fused) {   // more candidate room while it fits, up to a whole run's entries: fewer compactions
+        const int fit = (int)((budget - base) / (8ll * qps)) / (2 * kTile) * (2 * kTile);
+        cap = std::max(cap_min, std::min(fit, (tpc + 2) * kTile));
+      }
+      pl.runs = runs;
+      pl.tpc = tpc;
+      pl.cap = cap;
+      pl.smem = tc_smem_for(p.heads, pl.qh, fused, cap, pages, stages);
+      pl.applies = 1;
+      break;
     }
-    plan.runs = runs;
-    plan.tpc = tpc;
-    plan.cap = cap;
-    plan.smem = tc_smem_for(p.heads, plan.qh, fused, cap, pages);
-    plan.applies = 1;
-    break;
+    if (!pl.applies) return pl;
+    // the last CTA merges in place when the runs' lists fit its idle ring; a run's bitmap and word
+    // prefixes fit it in any case (tpc * 128 entries: at most 8 bits of ring per entry)
+    const size_t stage_bytes = stages == kStagesShallow
+                                   ? (size_t)(TcSmem<16, 4, kStagesShallow>::kSelAll - TcSmem<16, 4, kStagesShallow>::kA)
+                                   : (size_t)(TcSmem<16, 4, kStagesDeep>::kSelAll - TcSmem<16, 4, kStagesDeep>::kA);
+    const size_t bitmap_bytes = stages == kStagesShallow
+                                    ? (size_t)(TcSmem<16, 4, kStagesShallow>::kHist - TcSmem<16, 4, kStagesShallow>::kA)
+                                    : (size_t)(TcSmem<16, 4, kStagesDeep>::kHist - TcSmem<16, 4, kStagesDeep>::kA);
+    // lists with slack when they fit the ring, else exact ones
+    pl.list_cap = fused && (size_t)pl.runs * topk_list_cap(k) * 8 <= stage_bytes ? topk_list_cap(k) : k;
+    pl.merge_inline = fused && (size_t)pl.runs * pl.list_cap * 8 <= stage_bytes;
+    pl.merge_smem = (size_t)kMergeStage + (size_t)pl.runs * pl.list_cap * 8;
+    if (fused && (size_t)pl.tpc * kTile / 32 * 8 > bitmap_bytes) pl.applies = 0;
+    if (fused && !pl.merge_inline && pl.merge_smem > 227 * 1024) pl.applies = 0;
+    return pl;
+  };
+  if (fused) {
+    const IndexTcPlan shallow = attempt(kStagesShallow);
+    if (shallow.applies && shallow.merge_inline) return shallow;
   }
-  if (!plan.applies) return plan;
-  // the last CTA merges in place when the runs' lists fit its idle ring; a run's bitmap and word
-  // prefixes fit it in any case (tpc * 128 entries: at most 8 bits of ring per entry)
-  const size_t stage_bytes = (size_t)(TcSmem<16, 4>::kSelAll - TcSmem<16, 4>::kA);   // the same for every variant
-  plan.merge_inline = fused && (size_t)plan.runs * k * 8 <= stage_bytes;
-  plan.merge_smem = (size_t)kMergeStage + (size_t)plan.runs * k * 8;
-  if (fused && (size_t)plan.tpc * kTile / 32 * 8 > (size_t)(TcSmem<16, 4>::kHist - TcSmem<16, 4>::kA)) plan.applies = 0;
-  if (fused && !plan.merge_inline && plan.merge_smem > 227 * 1024) plan.applies = 0;
-  return plan;
+  return attempt(kStagesDeep);
 }
 
 cudaError_t launch_index_tc(const IndexParams& p, const IndexTcPlan& plan, cudaStream_t st) {

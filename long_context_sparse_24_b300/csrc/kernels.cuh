@@ -59,10 +59,16 @@ struct TopkRuns {
   int runs;
   int* cnt;         // [T][runs] keys in each run's list
   uint64_t* tau;    // [T][runs] the run's selection threshold (0 when it kept every candidate)
-  uint64_t* keys;   // [T][runs][k] each run's list, ascending entry index
+  uint64_t* keys;   // [T][runs][list_cap] each run's list, ascending entry index
+  int list_cap;     // keys a run's list holds at most (topk_list_cap(k), or k: exact lists)
   int* ticket;
   uint64_t* gthr;   // [T] the query's threshold shared by its runs (zero between calls), or null
 };
+
+// A run's list: its keys at or above a threshold with k to k + k/4 keys at or above it (all of
+// them when it has fewer than k), so that its selection may stop at a digit bin that leaves a few
+// more than k; or exactly its k largest (list capacity k).
+__host__ __device__ constexpr int topk_list_cap(int k) { return k + (k >> 2); }
 
 struct IndexParams {
   const int32_t* cu_new;
@@ -143,6 +149,9 @@ struct IndexTcPlan {
   int runs;           // CTAs per query group
   int tpc;            // 128-entry tiles per CTA
   int cap;            // candidate buffer per query (fused)
+  int stages;         // shared-memory ring depth
+  int list_cap;       // keys of a run's list: topk_list_cap(k) when the lists then still fit the
+                      // last CTA's ring, else k (exact per-run selection)
   int merge_inline;   // the sequence's last CTA merges (else the merge kernel)
   size_t smem;        // dynamic shared memory of the scorer
   size_t merge_smem;  // dynamic shared memory of the merge kernel

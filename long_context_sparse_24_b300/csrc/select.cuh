@@ -104,7 +104,7 @@ __device__ SelResult select_top(const uint64_t* buf, int n, int k, int slack, Se
   }
   group_sync<NT, ID>();   // (span is free again for the caller)
   if (kmax < kmin) return SelResult{lo, 0};      // no key at or above lo
-  if (kmax == kmin) return SelResult{kmax, 1};   // one key
+  if (kmax == kmin) return SelResult{k <= 1 ? kmax : lo, 1};   // one key: the k-th largest, or fewer than k
   const int hb = 63 - __clzll((long long)(kmax ^ kmin));   // the highest bit in which keys differ
   int width = hb + 1 < BITS ? hb + 1 : BITS;
   int shift = hb + 1 - width;
@@ -179,22 +179,27 @@ __device__ __forceinline__ void warp_append(bool take, uint64_t key, uint64_t* b
   if (take) buf[base + __popc(m & ((1u << lane) - 1u))] = key;
 }
 
-// Keeps the keys >= tau of buf[0..n) (order not kept); returns how many remain.  n <= NT * MAXPER.
+// Keeps the keys >= tau of buf[0..n) (order not kept); returns how many remain.  The keys go in
+// blocks of NT * MAXPER: a block is read into registers before any of its keys is written back,
+// and a kept key lands below the end of its own block (no more keys are kept than were read), so
+// it only overwrites keys already read.
 template <int NT, int ID, int MAXPER>
 __device__ int compact_keys_ge(uint64_t* buf, int n, uint64_t tau, SelScratch<NT>& sc) {
   const int tid = threadIdx.x;
-  uint64_t v[MAXPER];
-#pragma unroll
-  for (int s = 0; s < MAXPER; ++s) {
-    const int i = tid + s * NT;
-    v[s] = i < n ? buf[i] : 0ull;
-  }
   if (tid == 0) sc.count = 0;
-  group_sync<NT, ID>();
+  for (int b0 = 0; b0 < n; b0 += NT * MAXPER) {
+    uint64_t v[MAXPER];
 #pragma unroll
-  for (int s = 0; s < MAXPER; ++s) {
-    const int i = tid + s * NT;
-    warp_append(i < n && v[s] >= tau, v[s], buf, &sc.count);
+    for (int s = 0; s < MAXPER; ++s) {
+      const int i = b0 + tid + s * NT;
+      v[s] = i < n ? buf[i] : 0ull;
+    }
+    group_sync<NT, ID>();
+#pragma unroll
+    for (int s = 0; s < MAXPER; ++s) {
+      const int i = b0 + tid + s * NT;
+      warp_append(i < n && v[s] >= tau, v[s], buf, &sc.count);
+    }
   }
   group_sync<NT, ID>();
   const int r = sc.count;
