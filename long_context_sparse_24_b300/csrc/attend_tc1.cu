@@ -119,23 +119,33 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc1_kernel(AttendParams p)
   const int q = blockIdx.x, hg = blockIdx.y;
   const int H = p.heads;
   const int h0 = hg * kHeads;
-  // this CTA's split, and (before the sequence is known) the query's top-k count and the entry
-  // indices of the rows of its first tiles, read with the batch's offsets
   const int split = p.part == 1 ? p.entry_splits : blockIdx.z;
   const int32_t* sel = p.topk_idx != nullptr ? p.topk_idx + (long long)q * p.k : nullptr;
-  const int spec_r = p.window_split ? (split < p.entry_splits ? split * p.rows_per_split + tid : -1)
-                                    : split * p.rows_per_split + tid;   // this thread's row of the first tiles
-  int spec_j = -1;
-  if (sel != nullptr && p.part != 1 && spec_r >= 0 && spec_r < p.k && tid < 2 * kTileRows) spec_j = __ldg(sel + spec_r);
-  const int cnt_g = (sel != nullptr && p.part != 1 && p.topk_cnt != nullptr) ? __ldg(p.topk_cnt + q) : 0;
-  // sequence of query q (the row tile's space is free until the rows arrive)
+  // ---- what does not depend on the indexer first (launched as its programmatic dependent, this
+  //      part runs while the indexer's last CTAs merge): the query by cp.async into eight K-major
+  //      chunks, the sequence of query q (the row tile's space is free until the rows arrive), its
+  //      block-table row head into L2
+  for (int idx = tid; idx < kHeads * 64; idx += kThreads) {
+    const int h = idx >> 6, c = (idx >> 3) & 7, j = idx & 7;   // head, 64-dim chunk, 16-byte piece
+    const bool ok = h0 + h < H;
+    const __nv_bfloat16* g = p.q + ((long long)q * H + (ok ? h0 + h : 0)) * kD + c * 64 + j * 8;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(sbase + L::kQ + c * kQChunk + h * 128 +
+                                                                      ((j ^ (h & 7)) << 4)),
+                 "l"(g), "r"(ok ? 16 : 0) : "memory");
+  }
+  cp_async_commit();
   int b;
   const SeqSpan sp = find_seq_span(p.cu_new, p.seq_len, p.num_seqs, q, reinterpret_cast<int*>(smem + L::kT), 8 * kChunk / 4 - 1, &b);
-  // the top-k list and the sequence's block-table row head for L2 while the count is read
-  if (p.topk_idx != nullptr && p.part != 1)
-    for (int i = tid * 32; i < p.k; i += kThreads * 32) prefetch_l2(p.topk_idx + (long long)q * p.k + i);
   for (int i = tid * 32; i < p.paging.max_blocks; i += kThreads * 32)
     prefetch_l2(p.paging.table + (long long)b * p.paging.max_blocks + i);
+  // ---- the top-k count and the entry indices of this thread's row of the first tiles (written
+  //      by the indexer)
+  grid_dependency_wait();
+  const int spec_r = p.window_split ? (split < p.entry_splits ? split * p.rows_per_split + tid : -1)
+                                    : split * p.rows_per_split + tid;
+  int spec_j = -1;
+  if (sel != nullptr && p.part != 1 && spec_r >= 0 && spec_r < p.k && tid < 2 * kTileRows) spec_j = __ldcg(sel + spec_r);
+  const int cnt_g = (sel != nullptr && p.part != 1 && p.topk_cnt != nullptr) ? __ldcg(p.topk_cnt + q) : 0;
   const int n0 = sp.n0();
   const int t = n0 + (q - sp.q0);
   int cnt;
@@ -147,7 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc1_kernel(AttendParams p)
     cnt = min(cnt_g, p.k);
   } else {
     cnt = 0;
-    while (cnt < p.k && sel[cnt] >= 0) ++cnt;
+    while (cnt < p.k && __ldcg(sel + cnt) >= 0) ++cnt;
   }
   const int nvis = (t + 1) / p.m;
   const int W = min(t + 1, kWindow);
@@ -169,6 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc1_kernel(AttendParams p)
           ml[0] = -INFINITY;
           ml[1] = 0.0f;
         }
+    cp_async_wait<0>();   // the query's copies land before the CTA leaves
     return;
   }
   const int nrows = r_end - r_begin;
@@ -182,17 +193,6 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc1_kernel(AttendParams p)
   const uint32_t bar_pv = bar_s + 8;
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + L::kMisc);
 
-  // ---- the query first (independent of the rows): cp.async into eight K-major chunks
-  for (int idx = tid; idx < kHeads * 64; idx += kThreads) {
-    const int h = idx >> 6, c = (idx >> 3) & 7, j = idx & 7;   // head, 64-dim chunk, 16-byte piece
-    const bool ok = h0 + h < H;
-    const __nv_bfloat16* g = p.q + ((long long)q * H + (ok ? h0 + h : 0)) * kD + c * 64 + j * 8;
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(sbase + L::kQ + c * kQChunk + h * 128 +
-                                                                      ((j ^ (h & 7)) << 4)),
-                 "l"(g), "r"(ok ? 16 : 0) : "memory");
-  }
-  cp_async_commit();
-
   // ---- row descriptors and scales: bits 60..61 select the row set (0 entries, 1 new rows,
   //      2 ring), -1 = none
   if (tid < kTileRows) {
@@ -200,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc1_kernel(AttendParams p)
     long long d = -1;
     if (r < r_end) {
       if (r < cnt) {
-        const int j = sel != nullptr ? (r == spec_r ? spec_j : sel[r]) : r;
+        const int j = sel != nullptr ? (r == spec_r ? spec_j : __ldcg(sel + r)) : r;
         long long row = -1;
         if (j >= 0 && j < nvis) row = entry_row(p.paging, b, j, p.entries.num_rows);
         if (row < 0) report(p.status, LCS_ERR_DEVICE_GUARD);
@@ -467,9 +467,21 @@ cudaError_t launch_attend_tc1(const AttendParams& p, int total_new, cudaStream_t
   });
   if (ea != cudaSuccess) return ea;
   const int z = p.part == 1 ? 1 : (p.part == 2 ? p.entry_splits : p.splits);
-  dim3 grid(total_new, (p.heads + kHeads - 1) / kHeads, z);
-  attend_tc1_kernel<<<grid, kThreads, TcAttSmem::kBytes, st>>>(p);
-  cudaError_t e = cudaGetLastError();
+  // CSA calls start as programmatic dependents of the preceding kernel in the stream (the
+  // indexer lets them start once its scan is done): the kernel reads nothing that kernel writes
+  // before grid_dependency_wait()
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(total_new, (p.heads + kHeads - 1) / kHeads, z);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = TcAttSmem::kBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = pdl;
+  cfg.numAttrs = p.topk_idx != nullptr && p.part != 1 ? 1 : 0;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, attend_tc1_kernel, p);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess || p.splits == 1 || p.part == 1) return e;
   return launch_attend_combine(p, total_new, kD, st);
 }

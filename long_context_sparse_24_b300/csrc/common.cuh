@@ -89,6 +89,14 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
+// Programmatic dependent launch (PTX griddepcontrol).  A kernel launched as a programmatic
+// dependent of the preceding kernel in its stream may start before that kernel ends: it must not
+// read what that kernel writes before grid_dependency_wait(), which returns once the preceding
+// grid has completed and its writes are visible (at once for a kernel launched normally).
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the dependent grid start once every CTA of this grid has issued this or exited.
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Row set view (mirrors lcs_rows).
 struct Rows {
   int format;

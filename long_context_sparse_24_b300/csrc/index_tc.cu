@@ -567,10 +567,12 @@ __global__ void __launch_bounds__(kThreads, QH >= 16 ? 1 : 2) index_tc_kernel(co
           }
         }
       };
+      // the threshold the query's other runs have reached: read in one iteration and taken at the
+      // end of the next, so that no iteration waits for the load (an older value is as valid)
+      uint64_t gload = 0ull;
       for (int i0 = 0; i0 < nt; i0 += kIter) {
-        // the threshold the query's other runs have reached (read now, taken at the iteration's end)
-        uint64_t gnext = 0ull;
-        if (share && tid < qn) gnext = __ldcg(reinterpret_cast<const unsigned long long*>(p.runs.gthr) + qrow0 + tid);
+        const uint64_t gnext = gload;
+        if (share && tid < qn) gload = __ldcg(reinterpret_cast<const unsigned long long*>(p.runs.gthr) + qrow0 + tid);
         uint32_t d[kPerWarp][N];
         bool have[kPerWarp];
 #pragma unroll
@@ -644,6 +646,9 @@ __global__ void __launch_bounds__(kThreads, QH >= 16 ? 1 : 2) index_tc_kernel(co
     }
     tc_fence_before_sync();
     __syncthreads();
+    // the scan is done: a programmatic dependent (the attention over the selected entries) may
+    // start its own prologue on the SMs the scan leaves
+    grid_launch_dependents();
     if (warp == kEpiWarps) {
       tc_fence_after_sync();
       tmem_dealloc(tmem, kCols);
