@@ -429,14 +429,14 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
       if (ok) {
         const float lsc = sscale[bp * kTileRows + r] * p.scale_log2;   // logit = s_r * S', base 2
         float w[HG];
+        uint32_t u[HG / 16][16];   // every load in flight, one wait
 #pragma unroll
-        for (int c16 = 0; c16 < HG / 16; ++c16) {
-          uint32_t u[16];
-          tmem_ld16(tm_s + ((uint32_t)(warp * 32) << 16) + c16 * 16, u);
-          tmem_ld_wait();
+        for (int c16 = 0; c16 < HG / 16; ++c16) tmem_ld16(tm_s + ((uint32_t)(warp * 32) << 16) + c16 * 16, u[c16]);
+        tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 16; ++j) w[c16 * 16 + j] = rvalid ? __uint_as_float(u[j]) * lsc : -INFINITY;
-        }
+        for (int c16 = 0; c16 < HG / 16; ++c16)
+#pragma unroll
+          for (int j = 0; j < 16; ++j) w[c16 * 16 + j] = rvalid ? __uint_as_float(u[c16][j]) * lsc : -INFINITY;
         reduce_scatter<HG, true>(w, lane);
         if (hw_lane)
 #pragma unroll
@@ -464,13 +464,15 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
       const float srow = sscale[bp * kTileRows + r] * kP2Scale;
       const float lsc = sscale[bp * kTileRows + r] * p.scale_log2;
       tc_fence_after_sync();
+      {   // the logits again, from tensor memory (every load in flight, one wait)
+        uint32_t u[HG / 16][16];
 #pragma unroll
-      for (int c16 = 0; c16 < HG / 16; ++c16) {   // the logits again, from tensor memory
-        uint32_t u[16];
-        tmem_ld16(tm_s + ((uint32_t)(warp * 32) << 16) + c16 * 16, u);
+        for (int c16 = 0; c16 < HG / 16; ++c16) tmem_ld16(tm_s + ((uint32_t)(warp * 32) << 16) + c16 * 16, u[c16]);
         tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) w[c16 * 16 + j] = rvalid ? __uint_as_float(u[j]) * lsc : -INFINITY;
+        for (int c16 = 0; c16 < HG / 16; ++c16)
+#pragma unroll
+          for (int j = 0; j < 16; ++j) w[c16 * 16 + j] = rvalid ? __uint_as_float(u[c16][j]) * lsc : -INFINITY;
       }
 #pragma unroll
       for (int h = 0; h < HG; h += 2) {
@@ -543,14 +545,15 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
     for (int bi = 0; bi < 2; ++bi) {
       const int mb = 2 * (warp >> 2) + bi;
       const int dim0 = mb * 128 + quad * 32;
+      uint32_t v[HG / 16][16];   // every load in flight, one wait
 #pragma unroll
-      for (int c16 = 0; c16 < HG / 16; ++c16) {
-        uint32_t v[16];
-        tmem_ld16(tm_o + HG * mb + ((uint32_t)(quad * 32) << 16) + c16 * 16, v);
-        tmem_ld_wait();
+      for (int c16 = 0; c16 < HG / 16; ++c16)
+        tmem_ld16(tm_o + HG * mb + ((uint32_t)(quad * 32) << 16) + c16 * 16, v[c16]);
+      tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) tb[(c16 * 16 + j) * 32 + lane] = __uint_as_float(v[j]) * inv_s[c16 * 16 + j];
-      }
+      for (int c16 = 0; c16 < HG / 16; ++c16)
+#pragma unroll
+        for (int j = 0; j < 16; ++j) tb[(c16 * 16 + j) * 32 + lane] = __uint_as_float(v[c16][j]) * inv_s[c16 * 16 + j];
       __syncwarp();
 #pragma unroll 4
       for (int i = 0; i < HG / 4; ++i) {

@@ -335,14 +335,14 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc1_kernel(AttendParams p)
     const int r = warp * 32 + lane;
     const bool valid = r < nrows && desc[r] >= 0;
     const float lsc = sscale[r] * p.scale_log2;   // logit = s_r * S', in base 2
+    uint32_t v[kHeads / 16][16];   // the four loads in flight together, one wait
 #pragma unroll
-    for (int c16 = 0; c16 < kHeads / 16; ++c16) {
-      uint32_t v[16];
-      tmem_ld16(tm_s + ((uint32_t)(warp * 32) << 16) + c16 * 16, v);
-      tmem_ld_wait();
+    for (int c16 = 0; c16 < kHeads / 16; ++c16) tmem_ld16(tm_s + ((uint32_t)(warp * 32) << 16) + c16 * 16, v[c16]);
+    tmem_ld_wait();
 #pragma unroll
-      for (int j = 0; j < 16; ++j) st[r * 65 + c16 * 16 + j] = valid ? __uint_as_float(v[j]) * lsc : -INFINITY;
-    }
+    for (int c16 = 0; c16 < kHeads / 16; ++c16)
+#pragma unroll
+      for (int j = 0; j < 16; ++j) st[r * 65 + c16 * 16 + j] = valid ? __uint_as_float(v[c16][j]) * lsc : -INFINITY;
   }
   __syncthreads();
   {
@@ -407,14 +407,15 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc1_kernel(AttendParams p)
     for (int bi = 0; bi < 2; ++bi) {
       const int mb = 2 * (warp >> 2) + bi;
       const int dim0 = mb * 128 + quad * 32;
+      uint32_t v[kHeads / 16][16];   // the four loads in flight together, one wait
 #pragma unroll
-      for (int c16 = 0; c16 < kHeads / 16; ++c16) {
-        uint32_t v[16];
-        tmem_ld16(tm_o + 64 * mb + ((uint32_t)(quad * 32) << 16) + c16 * 16, v);
-        tmem_ld_wait();
+      for (int c16 = 0; c16 < kHeads / 16; ++c16)
+        tmem_ld16(tm_o + 64 * mb + ((uint32_t)(quad * 32) << 16) + c16 * 16, v[c16]);
+      tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) tb[(c16 * 16 + j) * 32 + lane] = __uint_as_float(v[j]) * inv_s[c16 * 16 + j];
-      }
+      for (int c16 = 0; c16 < kHeads / 16; ++c16)
+#pragma unroll
+        for (int j = 0; j < 16; ++j) tb[(c16 * 16 + j) * 32 + lane] = __uint_as_float(v[c16][j]) * inv_s[c16 * 16 + j];
       __syncwarp();
 #pragma unroll 4
       for (int i = 0; i < kHeads / 4; ++i) {
