@@ -277,7 +277,12 @@ lcs_status csa_index_topk_noalloc(const lcs_batch* batch, const uint8_t* q_fp4, 
  * the matching set of *values; values NULL = shared KV).  With values set the calls run the
  * warp-MMA kernel (csa_attend_window then launches nothing and csa_attend_topk computes
  * everything); value rows obey the row bounds below and a value row outside them is left out of
- * the softmax with LCS_ERR_DEVICE_GUARD.  Window token p is read from state->new_rows when p is one of this call's new
+ * the softmax with LCS_ERR_DEVICE_GUARD.
+ * sink: device f32[heads] or NULL: a per-head logit (natural log, not scaled by softmax_scale)
+ * that joins every softmax denominator and carries no value, o = sum_r p_r v_r / (sum_r p_r +
+ * e^sink), out_lse = log(sum_r e^logit_r + e^sink) (the csdn attention-details table names an
+ * attention sink; this is the common learned-sink reading); finite values; the same result as
+ * lcs_attention_sink applied to the call's outputs, rounded once.  csa_attend_window takes none.  Window token p is read from state->new_rows when p is one of this call's new
  * tokens (p >= seq_len-q_b) and from the window ring otherwise; with new_rows.nope NULL every
  * window row comes from the ring, which requires batch->max_new <= 1 (LCS_ERR_SHAPE otherwise).
  *   q       device bf16[total_new][heads][D]    out device bf16[total_new][heads][D]
@@ -296,8 +301,8 @@ size_t lcs_attend_workspace(const lcs_batch* batch, int32_t heads, int32_t dim, 
 lcs_status csa_attend(const lcs_batch* batch, const void* q, int32_t heads, const int32_t* topk_idx,
                       const int32_t* topk_cnt, int32_t k, int32_t m, const lcs_rows* entries,
                       const lcs_paging* paging, const lcs_state* state, const lcs_values* values,
-                      float softmax_scale, void* out, float* out_lse, void* workspace, size_t workspace_bytes,
-                      int32_t* dev_status, void* stream);
+                      const float* sink, float softmax_scale, void* out, float* out_lse, void* workspace,
+                      size_t workspace_bytes, int32_t* dev_status, void* stream);
 /* csa_attend in two calls, so that the sliding-window part, which does not depend on the top-k
  * selection, can run while the indexer does (CSA step 3 of x-techcon section 2 attends the window
  * rows and the selected entries in one softmax; splitting the rows and merging the per-part
@@ -319,12 +324,12 @@ lcs_status csa_attend_window(const lcs_batch* batch, const void* q, int32_t head
 lcs_status csa_attend_topk(const lcs_batch* batch, const void* q, int32_t heads, const int32_t* topk_idx,
                            const int32_t* topk_cnt, int32_t k, int32_t m, const lcs_rows* entries,
                            const lcs_paging* paging, const lcs_state* state, const lcs_values* values,
-                           float softmax_scale, void* out, float* out_lse, void* workspace,
+                           const float* sink, float softmax_scale, void* out, float* out_lse, void* workspace,
                            size_t workspace_bytes, int32_t* dev_status, void* stream);
 lcs_status hca_attend(const lcs_batch* batch, const void* q, int32_t heads, int32_t m,
                       const lcs_rows* entries, const lcs_paging* paging, const lcs_state* state,
-                      const lcs_values* values, float softmax_scale, void* out, float* out_lse, void* workspace,
-                      size_t workspace_bytes, int32_t* dev_status, void* stream);
+                      const lcs_values* values, const float* sink, float softmax_scale, void* out, float* out_lse,
+                      void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream);
 
 /* --- indexer key / query production: block-scaled FP4 (x-techcon section 4) -------------------
  * Quantises BF16 rows x[rows][r] (r a multiple of 32, at most 4096) to E2M1 codes
@@ -339,6 +344,8 @@ lcs_status hca_attend(const lcs_batch* batch, const void* q, int32_t heads, int3
 lcs_status lcs_quantize_e2m1(const void* x, int64_t rows, int32_t r, uint8_t* codes, uint8_t* scales, void* stream);
 
 /* --- attention sink (a per-head logit in every softmax denominator, carrying no value) ----------
+ * The standalone form, for outputs of calls made without `sink` (the attention calls fold the
+ * same term into their own normalisation).
  * Applied after csa_attend / csa_attend_topk / hca_attend from their outputs and log-sum-exp:
  *   out[i,h,:] *= 1 / (1 + exp(sink[h] - lse[i,h])),  lse[i,h] = log(exp(lse[i,h]) + exp(sink[h])),
  * which equals attention whose softmax has one more term exp(sink[h]) per head.  (The pages name

@@ -104,13 +104,13 @@ _SIGS = {
                                        c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp]),
     "lcs_attend_workspace": (c_sz, [P(lcs_batch), c_i32, c_i32, c_i32]),
     "csa_attend": (c_i32, [P(lcs_batch), c_vp, c_i32, c_vp, c_vp, c_i32, c_i32, P(lcs_rows), P(lcs_paging),
-                           P(lcs_state), P(lcs_values), ctypes.c_float, c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
+                           P(lcs_state), P(lcs_values), c_vp, ctypes.c_float, c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
     "csa_attend_window": (c_i32, [P(lcs_batch), c_vp, c_i32, c_i32, c_i32, P(lcs_rows), P(lcs_paging), P(lcs_state),
                                   P(lcs_values), ctypes.c_float, c_vp, c_sz, c_vp, c_vp]),
     "csa_attend_topk": (c_i32, [P(lcs_batch), c_vp, c_i32, c_vp, c_vp, c_i32, c_i32, P(lcs_rows), P(lcs_paging),
-                                P(lcs_state), P(lcs_values), ctypes.c_float, c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
+                                P(lcs_state), P(lcs_values), c_vp, ctypes.c_float, c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
     "hca_attend": (c_i32, [P(lcs_batch), c_vp, c_i32, c_i32, P(lcs_rows), P(lcs_paging), P(lcs_state),
-                           P(lcs_values), ctypes.c_float, c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
+                           P(lcs_values), c_vp, ctypes.c_float, c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -360,11 +360,11 @@ def lcs_attend_workspace(batch: Batch, heads: int, dim: int, max_rows: int) -> i
 
 def csa_attend(batch: Batch, q, heads: int, topk_idx, topk_cnt, k: int, m: int, entries: RowSet, paging: Paging,
                state: State, softmax_scale: float, out, out_lse, workspace, workspace_bytes: int, dev_status=None,
-               stream=None, values: Optional[Values] = None) -> None:
+               stream=None, values: Optional[Values] = None, sink=None) -> None:
     b, e, p, s = batch.c(), entries.c(), paging.c(), state.c()
     vr, _keep = _values_ref(values)
     _check(_lib.csa_attend(ctypes.byref(b), _ptr(q), heads, _ptr(topk_idx), _ptr(topk_cnt), k, m, ctypes.byref(e),
-                           ctypes.byref(p), ctypes.byref(s), vr, softmax_scale, _ptr(out), _ptr(out_lse),
+                           ctypes.byref(p), ctypes.byref(s), vr, _ptr(sink), softmax_scale, _ptr(out), _ptr(out_lse),
                            _ptr(workspace), workspace_bytes, _ptr(dev_status), _stream(stream)), "csa_attend")
 
 
@@ -380,20 +380,20 @@ def csa_attend_window(batch: Batch, q, heads: int, k: int, m: int, entries: RowS
 
 def csa_attend_topk(batch: Batch, q, heads: int, topk_idx, topk_cnt, k: int, m: int, entries: RowSet, paging: Paging,
                     state: State, softmax_scale: float, out, out_lse, workspace, workspace_bytes: int,
-                    dev_status=None, stream=None, values: Optional[Values] = None) -> None:
+                    dev_status=None, stream=None, values: Optional[Values] = None, sink=None) -> None:
     b, e, p, s = batch.c(), entries.c(), paging.c(), state.c()
     vr, _keep = _values_ref(values)
     _check(_lib.csa_attend_topk(ctypes.byref(b), _ptr(q), heads, _ptr(topk_idx), _ptr(topk_cnt), k, m,
-                                ctypes.byref(e), ctypes.byref(p), ctypes.byref(s), vr, softmax_scale, _ptr(out),
+                                ctypes.byref(e), ctypes.byref(p), ctypes.byref(s), vr, _ptr(sink), softmax_scale, _ptr(out),
                                 _ptr(out_lse), _ptr(workspace), workspace_bytes, _ptr(dev_status), _stream(stream)),
            "csa_attend_topk")
 
 
 def hca_attend(batch: Batch, q, heads: int, m: int, entries: RowSet, paging: Paging, state: State,
                softmax_scale: float, out, out_lse, workspace, workspace_bytes: int, dev_status=None,
-               stream=None, values: Optional[Values] = None) -> None:
+               stream=None, values: Optional[Values] = None, sink=None) -> None:
     b, e, p, s = batch.c(), entries.c(), paging.c(), state.c()
     vr, _keep = _values_ref(values)
     _check(_lib.hca_attend(ctypes.byref(b), _ptr(q), heads, m, ctypes.byref(e), ctypes.byref(p), ctypes.byref(s),
-                           vr, softmax_scale, _ptr(out), _ptr(out_lse), _ptr(workspace), workspace_bytes,
+                           vr, _ptr(sink), softmax_scale, _ptr(out), _ptr(out_lse), _ptr(workspace), workspace_bytes,
                            _ptr(dev_status), _stream(stream)), "hca_attend")

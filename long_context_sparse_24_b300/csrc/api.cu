@@ -362,9 +362,10 @@ lcs_status attend_common(const lcs_batch* batch, const void* q, int32_t heads, c
 lcs_status csa_attend_part(const lcs_batch* batch, const void* q, int32_t heads, const int32_t* topk_idx,
                            const int32_t* topk_cnt, int32_t k, int32_t m, const lcs_rows* entries,
                            const lcs_paging* paging, const lcs_state* state, const lcs_values* values,
-                           float softmax_scale, void* out, float* out_lse, void* workspace, size_t workspace_bytes,
-                           int32_t* dev_status, void* stream, int part) {
+                           const float* sink, float softmax_scale, void* out, float* out_lse, void* workspace,
+                           size_t workspace_bytes, int32_t* dev_status, void* stream, int part) {
   if (topk_idx == nullptr && part != 1) return LCS_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(sink) & 3u) return LCS_ERR_ALIGNMENT;
   if (k < 1 || k > 4096 || m <= 0 || m > 128) return LCS_ERR_UNSUPPORTED;
   AttendParams p;
   // the window rows form a split of their own only for the two-part calls (the window part runs
@@ -384,6 +385,7 @@ lcs_status csa_attend_part(const lcs_batch* batch, const void* q, int32_t heads,
   p.k = k;
   p.m = m;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  p.sink = part == 1 ? nullptr : sink;
   p.out_lse = out_lse;
   p.status = dev_status;
   return from_cuda(launch_attend(p, entries->dim, entries->format, batch->total_new, static_cast<cudaStream_t>(stream)));
@@ -549,40 +551,43 @@ size_t lcs_attend_workspace(const lcs_batch* batch, int32_t heads, int32_t dim, 
 
 lcs_status csa_attend(const lcs_batch* batch, const void* q, int32_t heads, const int32_t* topk_idx,
                       const int32_t* topk_cnt, int32_t k, int32_t m, const lcs_rows* entries, const lcs_paging* paging,
-                      const lcs_state* state, const lcs_values* values, float softmax_scale, void* out,
-                      float* out_lse, void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream) {
-  return csa_attend_part(batch, q, heads, topk_idx, topk_cnt, k, m, entries, paging, state, values, softmax_scale,
-                         out, out_lse, workspace, workspace_bytes, dev_status, stream, 0);
+                      const lcs_state* state, const lcs_values* values, const float* sink, float softmax_scale,
+                      void* out, float* out_lse, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                      void* stream) {
+  return csa_attend_part(batch, q, heads, topk_idx, topk_cnt, k, m, entries, paging, state, values, sink,
+                         softmax_scale, out, out_lse, workspace, workspace_bytes, dev_status, stream, 0);
 }
 
 lcs_status csa_attend_window(const lcs_batch* batch, const void* q, int32_t heads, int32_t k, int32_t m,
                              const lcs_rows* entries, const lcs_paging* paging, const lcs_state* state,
                              const lcs_values* values, float softmax_scale, void* workspace, size_t workspace_bytes,
                              int32_t* dev_status, void* stream) {
-  return csa_attend_part(batch, q, heads, nullptr, nullptr, k, m, entries, paging, state, values, softmax_scale,
-                         nullptr, nullptr, workspace, workspace_bytes, dev_status, stream, 1);
+  return csa_attend_part(batch, q, heads, nullptr, nullptr, k, m, entries, paging, state, values, nullptr,
+                         softmax_scale, nullptr, nullptr, workspace, workspace_bytes, dev_status, stream, 1);
 }
 
 lcs_status csa_attend_topk(const lcs_batch* batch, const void* q, int32_t heads, const int32_t* topk_idx,
                            const int32_t* topk_cnt, int32_t k, int32_t m, const lcs_rows* entries,
                            const lcs_paging* paging, const lcs_state* state, const lcs_values* values,
-                           float softmax_scale, void* out, float* out_lse, void* workspace, size_t workspace_bytes,
-                           int32_t* dev_status, void* stream) {
-  return csa_attend_part(batch, q, heads, topk_idx, topk_cnt, k, m, entries, paging, state, values, softmax_scale,
-                         out, out_lse, workspace, workspace_bytes, dev_status, stream, 2);
+                           const float* sink, float softmax_scale, void* out, float* out_lse, void* workspace,
+                           size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  return csa_attend_part(batch, q, heads, topk_idx, topk_cnt, k, m, entries, paging, state, values, sink,
+                         softmax_scale, out, out_lse, workspace, workspace_bytes, dev_status, stream, 2);
 }
 
 lcs_status hca_attend(const lcs_batch* batch, const void* q, int32_t heads, int32_t m, const lcs_rows* entries,
-                      const lcs_paging* paging, const lcs_state* state, const lcs_values* values, float softmax_scale,
-                      void* out, float* out_lse, void* workspace, size_t workspace_bytes, int32_t* dev_status,
-                      void* stream) {
+                      const lcs_paging* paging, const lcs_state* state, const lcs_values* values, const float* sink,
+                      float softmax_scale, void* out, float* out_lse, void* workspace, size_t workspace_bytes,
+                      int32_t* dev_status, void* stream) {
   if (m <= 0 || m > 128) return LCS_ERR_UNSUPPORTED;
+  if (reinterpret_cast<uintptr_t>(sink) & 3u) return LCS_ERR_ALIGNMENT;
   AttendParams p;
   lcs_status s = attend_common(batch, q, heads, entries, paging, state, values, out, workspace, workspace_bytes,
                                batch ? batch->max_seq_len / m + LCSA_WINDOW : 0, p, false);
   if (s != LCS_OK) return s;
   p.m = m;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  p.sink = sink;
   p.out_lse = out_lse;
   p.status = dev_status;
   return from_cuda(launch_attend(p, entries->dim, entries->format, batch->total_new, static_cast<cudaStream_t>(stream)));

@@ -498,7 +498,7 @@ __global__ void __launch_bounds__(256, 1) attend_kernel(AttendParams p) {
       if (h >= H) continue;
       const float l = lrow[hl], mm = mrow[hl];
       if (p.splits == 1) {
-        const float inv = l > 0.0f ? oscale / l : 0.0f;
+        const float inv = oscale * softmax_norm(mm, l, p.sink, h).f;
         __nv_bfloat16* o = p.out + ((long long)q * H + h) * D + dcol0;
 #pragma unroll
         for (int c = 0; c < NTD; ++c) {
@@ -506,7 +506,7 @@ __global__ void __launch_bounds__(256, 1) attend_kernel(AttendParams p) {
           *reinterpret_cast<__nv_bfloat162*>(o + c * 8 + 2 * t4) = v;
         }
         if (p.out_lse != nullptr && warp == 0 && t4 == 0)
-          p.out_lse[(long long)q * H + h] = l > 0.0f ? (mm + log2f(l)) * 0.69314718055994531f : -INFINITY;
+          p.out_lse[(long long)q * H + h] = softmax_norm(mm, l, p.sink, h).lse2 * 0.69314718055994531f;
       } else {
         float* o = p.ws_o + (((long long)q * H + h) * p.splits + split) * D + dcol0;
 #pragma unroll
@@ -555,12 +555,13 @@ __global__ void __launch_bounds__(D / 4) attend_combine_kernel(AttendParams p) {
     acc.z = fmaf(v.z, wgt, acc.z);
     acc.w = fmaf(v.w, wgt, acc.w);
   }
-  const float inv = Lsum > 0.0f ? 1.0f / Lsum : 0.0f;
+  const SoftmaxNorm nm = softmax_norm(M, Lsum, p.sink, h);
+  const float inv = nm.f;
   __nv_bfloat16* o = p.out + ((long long)q * H + h) * D + tid * 4;
   *reinterpret_cast<__nv_bfloat162*>(o) = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
   *reinterpret_cast<__nv_bfloat162*>(o + 2) = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
   if (tid == 0 && p.out_lse != nullptr)
-    p.out_lse[(long long)q * H + h] = Lsum > 0.0f ? (M + log2f(Lsum)) * 0.69314718055994531f : -INFINITY;
+    p.out_lse[(long long)q * H + h] = nm.lse2 * 0.69314718055994531f;
 }
 
 // ----------------------------------------------------------------------------------------------

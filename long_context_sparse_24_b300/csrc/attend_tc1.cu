@@ -396,10 +396,9 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc1_kernel(AttendParams p)
   // ---- epilogue: warp w reads lanes 32*(w%4) (dims) of blocks 2*(w/4), 2*(w/4)+1, transposes
   //      them through its own 8 KB of the query buffer and writes 16-byte pieces
   float* inv_s = reinterpret_cast<float*>(smem + L::kInv);
-  for (int h = tid; h < kHeads; h += kThreads) {
-    const float l = lrow[h];
-    inv_s[h] = p.splits == 1 ? (l > 0.0f ? 1.0f / (l * kP2Scale) : 0.0f) : 1.0f / kP2Scale;
-  }
+  for (int h = tid; h < kHeads; h += kThreads)
+    inv_s[h] = p.splits == 1 ? softmax_norm(mrow[h], lrow[h], h0 + h < H ? p.sink : nullptr, h0 + h).f / kP2Scale
+                             : 1.0f / kP2Scale;
   __syncthreads();
   if (ok) {
     const int quad = warp & 3;
@@ -440,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc1_kernel(AttendParams p)
       const float l = lrow[h], mm = mrow[h];
       if (p.splits == 1) {
         if (p.out_lse != nullptr)
-          p.out_lse[(long long)q * H + h0 + h] = l > 0.0f ? (mm + log2f(l)) * 0.69314718055994531f : -INFINITY;
+          p.out_lse[(long long)q * H + h0 + h] = softmax_norm(mm, l, p.sink, h0 + h).lse2 * 0.69314718055994531f;
       } else {
         float* ml = p.ws_ml + (((long long)q * H + h0 + h) * p.splits + split) * 2;
         ml[0] = mm;

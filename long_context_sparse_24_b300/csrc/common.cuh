@@ -89,6 +89,23 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
+// The end of a softmax over rows with a per-head sink logit folded in (one more term e^sink in the
+// denominator that carries no value; sink in natural-log units, NULL = none).  The rows give their
+// running max m and sum l of 2^(logit - m) (logits in base 2); f turns the rows' weighted sum
+// (relative to m) into the output and lse2 is the log-sum-exp in base 2.  Without a sink f = 1/l.
+struct SoftmaxNorm {
+  float f;
+  float lse2;
+};
+__device__ __forceinline__ SoftmaxNorm softmax_norm(float m, float l, const float* sink, int h) {
+  if (sink == nullptr) return SoftmaxNorm{l > 0.0f ? 1.0f / l : 0.0f, l > 0.0f ? m + log2f(l) : -INFINITY};
+  const float s2 = sink[h] * 1.4426950408889634f;
+  const float mx = l > 0.0f ? fmaxf(m, s2) : s2;
+  const float a = l > 0.0f ? exp2f(m - mx) : 0.0f;
+  const float lp = fmaf(l, a, exp2f(s2 - mx));
+  return SoftmaxNorm{a / lp, mx + log2f(lp)};
+}
+
 // Programmatic dependent launch (PTX griddepcontrol).  A kernel launched as a programmatic
 // dependent of the preceding kernel in its stream may start before that kernel ends: it must not
 // read what that kernel writes before grid_dependency_wait(), which returns once the preceding

@@ -118,6 +118,7 @@ struct AttendParams {
   Rows v_window;
   Rows v_new_rows;
   float scale_log2;
+  const float* sink;         // [heads] sink logits folded into the softmax (natural log), or null
   __nv_bfloat16* out;
   float* out_lse;
   float* ws_o;               // [T][H][splits][D] fp32 partials (warp-MMA kernel), or

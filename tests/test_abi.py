@@ -79,9 +79,9 @@ def test_host_validation_without_gpu():
                             0x4000, 0x8000, 1 << 20, None, None) == 1
     assert lcsa.LCS_INDEX_SPARE_SMS(32) == 32 << 8 and lcsa.LCS_INDEX_SPARE_SMS(300) == (300 & 0xFF) << 8
     # attention: heads 24 unsupported; topk list missing
-    assert L.csa_attend(by(_batch(lcsa)), 0x1000, 24, 0x2000, None, 16, 4, by(rows), by(pag), by(st), None, 1.0,
+    assert L.csa_attend(by(_batch(lcsa)), 0x1000, 24, 0x2000, None, 16, 4, by(rows), by(pag), by(st), None, None, 1.0,
                         0x3000, None, None, 0, None, None) == 4
-    assert L.csa_attend(by(_batch(lcsa)), 0x1000, 64, None, None, 16, 4, by(rows), by(pag), by(st), None, 1.0,
+    assert L.csa_attend(by(_batch(lcsa)), 0x1000, 64, None, None, 16, 4, by(rows), by(pag), by(st), None, None, 1.0,
                         0x3000, None, None, 0, None, None) == 1
 
 
@@ -97,9 +97,10 @@ def test_separate_values_host_validation():
     st = lcsa.lcs_state(ring, 0x5000, 8, new)
     b = _batch(lcsa)
     call = lambda v, heads=64: L.csa_attend(by(b), 0x1000, heads, 0x2000, None, 16, 4, by(entries), by(pag), by(st),
-                                            by(v) if v is not None else None, 1.0, 0x3000, None, None, 0, None, None)
-    hcall = lambda v: L.hca_attend(by(b), 0x1000, 64, 128, by(entries), by(pag), by(st), by(v), 1.0, 0x3000, None,
-                                   None, 0, None, None)
+                                            by(v) if v is not None else None, None, 1.0, 0x3000, None, None, 0, None,
+                                            None)
+    hcall = lambda v, sink=None: L.hca_attend(by(b), 0x1000, 64, 128, by(entries), by(pag), by(st), by(v), sink, 1.0,
+                                              0x3000, None, None, 0, None, None)
     good = lcsa.lcs_values(fp8(64), fp8(128), fp8(4))
     # one value set with fewer rows, another format, new rows missing
     assert call(lcsa.lcs_values(fp8(63), fp8(128), fp8(4))) == 2
@@ -117,6 +118,8 @@ def test_separate_values_host_validation():
     assert call(good) == 8 and call(None) == 8
     assert hcall(good) == 8
     assert hcall(lcsa.lcs_values(fp8(64), fp8(100), fp8(4))) == 2
+    # a sink pointer not 4-byte aligned
+    assert hcall(good, 0x5002) == 3 and hcall(good, 0x5004) == 8
 
 
 def test_stage_copy_host_validation():

@@ -304,13 +304,16 @@ def test_topk_ties_take_lowest_index():
 # ---------------------------------------------------------------------------------------- attention
 
 def _attend_case(kind, lengths, new, heads, dim, fmt, m, k, seed=41, scale=None, split=False, sink=None,
-                 corrupt_seq=None, rows_hook=None, skip_seq=None, expect_status=None, separate_v=False):
+                 corrupt_seq=None, rows_hook=None, skip_seq=None, expect_status=None, separate_v=False,
+                 sink_fused=False):
     """Fill an entry cache / window ring / new rows with oracle-quantised rows and run one call.
     corrupt_seq: unmap that sequence's first cache block before the call (host-side corruption of
     the block table); the call must then report LCS_ERR_DEVICE_GUARD and every other sequence must
     still match the oracle.  rows_hook(b, entry_rows): may change a sequence's entry rows (fp64)
     before they are quantised.  separate_v: value rows of their own (entries, window ring and new
-    rows numbered like the key rows, drawn from other streams) passed as `values`.  expect_status: the device status the call must report (outputs
+    rows numbered like the key rows, drawn from other streams) passed as `values`.  sink: per-head
+    sink logits, applied by lcs_attention_sink after the call, or with sink_fused by the attention
+    call itself.  expect_status: the device status the call must report (outputs
     are not checked when it is LCS_ERR_TIMEOUT); skip_seq: a sequence whose outputs are not
     checked."""
     S = len(lengths)
@@ -392,6 +395,8 @@ def _attend_case(kind, lengths, new, heads, dim, fmt, m, k, seed=41, scale=None,
     lse = torch.empty((T, heads), dtype=torch.float32, device=DEV)
     scale = scale if scale is not None else 1 / math.sqrt(dim)
     st = dev_status()
+    sink_dev = torch.from_numpy(sink.astype(np.float32)).to(DEV) if sink is not None else None
+    fsink = sink_dev if sink_fused else None
     if kind == "csa":
         idx = np.full((T, k), -1, np.int32)
         for i, s in enumerate(sels):
@@ -408,24 +413,24 @@ def _attend_case(kind, lengths, new, heads, dim, fmt, m, k, seed=41, scale=None,
                                    st, stream=side, values=vals)
             torch.cuda.current_stream().wait_stream(side)
             lcsa.csa_attend_topk(batch, q, heads, idx_t, cnt_t, k, m, cache.entries, cache.paging, cache.state,
-                                 scale, out, lse, ws, wsb, st, values=vals)
+                                 scale, out, lse, ws, wsb, st, values=vals, sink=fsink)
             # the one call plans the window rows into the entries' list (other splits, so other
             # rounding): it is checked against the oracle as well
             one_out = torch.empty_like(out)
             one_lse = torch.empty_like(lse)
             lcsa.csa_attend(batch, q, heads, idx_t, cnt_t, k, m, cache.entries, cache.paging, cache.state, scale,
-                            one_out, one_lse, workspace(wsb), wsb, st, values=vals)
+                            one_out, one_lse, workspace(wsb), wsb, st, values=vals, sink=fsink)
         else:
             lcsa.csa_attend(batch, q, heads, idx_t, cnt_t, k, m, cache.entries, cache.paging, cache.state, scale, out,
-                            lse, workspace(wsb), wsb, st, values=vals)
+                            lse, workspace(wsb), wsb, st, values=vals, sink=fsink)
     else:
         wsb = lcsa.lcs_attend_workspace(batch, heads, dim, cap // m + 128)
         lcsa.hca_attend(batch, q, heads, m, cache.entries, cache.paging, cache.state, scale, out, lse,
-                        workspace(wsb), wsb, st, values=vals)
-    if sink is not None:
-        lcsa.lcs_attention_sink(out, lse, torch.from_numpy(sink.astype(np.float32)).to(DEV))
+                        workspace(wsb), wsb, st, values=vals, sink=fsink)
+    if sink is not None and not sink_fused:
+        lcsa.lcs_attention_sink(out, lse, sink_dev)
         if kind == "csa" and split:
-            lcsa.lcs_attention_sink(one_out, one_lse, torch.from_numpy(sink.astype(np.float32)).to(DEV))
+            lcsa.lcs_attention_sink(one_out, one_lse, sink_dev)
     torch.cuda.synchronize()
     want = expect_status if expect_status is not None else (6 if corrupt_seq is not None else 0)
     got = int(st.item())
@@ -512,11 +517,24 @@ def test_attend_separate_values_matches_oracle(kind, lengths, new, heads, dim, f
     ("hca", [40000 - 700 * i for i in range(40)], [1] * 40, 64, 512, "fp8_split", 128, 0, False),
     ("csa", [3000 + 37 * i for i in range(120)], [1] * 120, 64, 512, "fp8_split", 4, 1024, False),
 ])
-def test_attention_sink_matches_oracle(kind, lengths, new, heads, dim, fmt, m, k, split):
-    """Attention, then lcs_attention_sink with per-head sink logits around the logits' range,
-    against the oracle's softmax with the sink term (outputs and lse)."""
+@pytest.mark.parametrize("fused", [False, True])
+def test_attention_sink_matches_oracle(kind, lengths, new, heads, dim, fmt, m, k, split, fused):
+    """Per-head sink logits around the logits' range, applied by lcs_attention_sink after the
+    attention or folded into the attention's own normalisation (single-split epilogues and the
+    combine), against the oracle's softmax with the sink term (outputs and lse)."""
     sink = np.random.default_rng(7).standard_normal(heads) * 2.0
-    _attend_case(kind, lengths, new, heads, dim, fmt, m, k, sink=sink, split=split)
+    _attend_case(kind, lengths, new, heads, dim, fmt, m, k, sink=sink, split=split, sink_fused=fused)
+
+
+@pytest.mark.parametrize("kind,lengths,new,heads,dim,fmt,m,k", [
+    ("csa", [2000, 4100, 300], [1, 1, 1], 64, 512, "fp8_split", 4, 512),
+    ("hca", [3000], [17], 64, 512, "fp8_split", 128, 0),
+    ("csa", [50, 700], [50, 20], 8, 128, "bf16", 4, 64),
+])
+def test_attention_sink_with_separate_values(kind, lengths, new, heads, dim, fmt, m, k):
+    """The folded sink together with separate value rows (warp-MMA kernel), against the oracle."""
+    sink = np.random.default_rng(8).standard_normal(heads) * 3.0
+    _attend_case(kind, lengths, new, heads, dim, fmt, m, k, sink=sink, sink_fused=True, separate_v=True)
 
 
 @pytest.mark.parametrize("lengths,new,heads,dim,fmt,k", [
