@@ -84,8 +84,8 @@ struct TcSmem {
   static constexpr int kStages = ST;
   static constexpr int kScaleSlots = ST + kAcc;
   static constexpr int N = 4 * QH;                            // MMA N: (block, query-head) columns
-  static constexpr int kA = 0;                                // kStages x 8 KB, 1024-aligned
-  static constexpr int kB = kA + kStages * kATileBytes;       // N x 64 B
+  // the fixed part first
+  static constexpr int kB = 0;                                // N x 64 B (1024-aligned)
   static constexpr int kScale = kB + N * kRowBytes;           // kScaleSlots x 128 x 4 B
   static constexpr int kQs = kScale + kScaleSlots * kTile * 4;  // f32 [QH][4] q block scales
   static constexpr int kHw = kQs + QH * 4 * 4;                // f32 [QH] head weights
@@ -98,17 +98,23 @@ struct TcSmem {
   static constexpr int kCnt = kThr + QPS * 8;                 // int [QPS] candidate counts
   static constexpr int kSelEpi = (kCnt + QPS * 4 + 15) / 16 * 16;   // SelScratch<kEpiThreads>
   static_assert(alignof(SelScratch<kThreads>) <= 16 && alignof(SelScratch<kEpiThreads>) <= 16, "scratch alignment");
-  // after the scan the ring is idle: its tail holds the whole CTA's selection scratch and the merge's
-  // run offsets, its head the run bitmap (final selection) or the staged run lists (merge)
-  static constexpr int kRingEnd = kA + kStages * kATileBytes;
-  static constexpr int kRunOff = (kRingEnd - 4 * (kMaxRuns + 4)) / 16 * 16;              // int [runs + 1]
-  static constexpr int kSelAll = (kRunOff - (int)sizeof(SelScratch<kThreads>)) / 16 * 16;  // SelScratch<kThreads>
-  static constexpr int kHist = kSelAll - 2048 * 4;                                       // u32 [2048]
-  static constexpr int kCand = (kSelEpi + (int)sizeof(SelScratch<kEpiThreads>) + 15) / 16 * 16;   // u64 [QPS][cap], then
-  // the run's page table: int [pages]
-  static size_t bytes(bool fused, int cap, int pages) {
-    return (size_t)kCand + (fused ? (size_t)QPS * cap * 8 : 0) + (size_t)pages * 4 + 1024;
+  static constexpr int kCand = (kSelEpi + (int)sizeof(SelScratch<kEpiThreads>) + 15) / 16 * 16;   // u64 [QPS][cap]
+  // then the ring of kStages x 8 KB (1024-aligned) right after the candidate buffers, then the
+  // run's page table: int [pages].  After the scan the ring is idle: its tail holds the whole CTA's
+  // selection scratch, the merge's run offsets and a 2048-bin histogram, its head the run bitmap
+  // (final selection); the merge stages the run lists from the (idle) candidate buffers on through
+  // the ring up to the histogram.
+  static constexpr int kRingBytes = kStages * kATileBytes;
+  static constexpr int kRunOffR = (kRingBytes - 4 * (kMaxRuns + 4)) / 16 * 16;              // int [runs + 1]
+  static constexpr int kSelAllR = (kRunOffR - (int)sizeof(SelScratch<kThreads>)) / 16 * 16;  // SelScratch<kThreads>
+  static constexpr int kHistR = kSelAllR - 2048 * 4;                                       // u32 [2048]
+  __host__ __device__ static constexpr int ring_off(bool fused, int cap) {
+    return (kCand + (fused ? QPS * cap * 8 : 0) + 1023) / 1024 * 1024;
   }
+  static size_t bytes(bool fused, int cap, int pages) {
+    return (size_t)ring_off(fused, cap) + kRingBytes + (size_t)pages * 4 + 1024;
+  }
+  static size_t stage_bytes(int cap) { return (size_t)(ring_off(true, cap) + kHistR - kCand); }
 };
 
 // accumulators of N columns: 8 while they and the scale factors fit 256 columns, else 7 (which
@@ -214,6 +220,11 @@ __device__ void merge_query_topk(const TopkRuns& tr, long long q, int N, int k, 
   }
   group_sync<NT, ID>();
   const int total = min(run_off[tr.runs], stage_cap);   // (the host sizes the stage for every list)
+  if (cand_cap < 0) {   // the candidates go right after the staged lists
+    const int at = (total + 1) & ~1;
+    cand = stage + at;
+    cand_cap = max(0, stage_cap - at);
+  }
   // stage the lists, a warp per run (16 loads in flight per lane), and gather the candidates
   constexpr int kU = 16;
   for (int r = warp; r < tr.runs; r += NT / 32) {
@@ -304,7 +315,8 @@ __global__ void __launch_bounds__(kThreads, QH >= 16 ? 1 : 2) index_tc_kernel(co
   const int nt = max(0, t_end - t_begin);
   const int k = p.top_k;
   const int cap = p.cand_cap;
-  SelScratch<kThreads>& sel_all = *reinterpret_cast<SelScratch<kThreads>*>(smem + L::kSelAll);
+  const int ring_off = L::ring_off(FUSED, cap);   // the ring after the candidate buffers
+  SelScratch<kThreads>& sel_all = *reinterpret_cast<SelScratch<kThreads>*>(smem + ring_off + L::kSelAllR);
   uint64_t* thr_s = reinterpret_cast<uint64_t*>(smem + L::kThr);
   int* cnt_s = reinterpret_cast<int*>(smem + L::kCnt);
   uint64_t* cand_s = reinterpret_cast<uint64_t*>(smem + L::kCand);
@@ -328,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, QH >= 16 ? 1 : 2) index_tc_kernel(co
   float* qs_s = reinterpret_cast<float*>(smem + L::kQs);
   float* hw_s = reinterpret_cast<float*>(smem + L::kHw);
   float* qw_s = reinterpret_cast<float*>(smem + L::kQw);
-  int* pages_s = reinterpret_cast<int*>(smem + L::kCand + (FUSED ? QPS * cap * 8 : 0));
+  int* pages_s = reinterpret_cast<int*>(smem + ring_off + L::kRingBytes);
   int* armed_s = reinterpret_cast<int*>(smem + L::kArmed);
   const uint32_t bar_full = sbase + L::kBar;
   const uint32_t bar_empty = bar_full + kStages * 8;
@@ -441,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, QH >= 16 ? 1 : 2) index_tc_kernel(co
         const int e0 = (t_begin + i) * kTile;
         const int rows = min(kTile, ((min(nmax, e0 + kTile) - e0 + epb - 1) >> eshift) << eshift);  // whole pages
         const uint32_t bar = bar_full + 8 * s;
-        const uint32_t a_dst = sbase + L::kA + s * kATileBytes;
+        const uint32_t a_dst = sbase + ring_off + s * kATileBytes;
         const uint32_t s_dst = sbase + L::kScale + (i % kScaleSlots) * kTile * 4;
         const int npg = rows >> eshift;
         if (run_contig) {
@@ -485,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, QH >= 16 ? 1 : 2) index_tc_kernel(co
           if (!mbar_wait(bar_full + 8 * s, (i / kStages) & 1, p.status, abort_flag, polls)) break;
           if (!mbar_wait(bar_acce + 8 * a, ((i / kAccN) & 1) ^ 1, p.status, abort_flag, polls)) break;
           tc_fence_after_sync();
-          const uint64_t adesc = smem_desc_sw64(sbase + L::kA + s * kATileBytes);
+          const uint64_t adesc = smem_desc_sw64(sbase + ring_off + s * kATileBytes);
 #pragma unroll
           for (int kb = 0; kb < 2; ++kb)   // K = 64 codes per MMA: 32 shared-memory bytes per step
             tc_mma_mxf4(tmem + a * N, adesc + 2 * kb, bdesc + 2 * kb, kIdesc, tm_sf, tm_sf + 4, kb > 0 ? 1u : 0u);
@@ -662,9 +674,9 @@ __global__ void __launch_bounds__(kThreads, QH >= 16 ? 1 : 2) index_tc_kernel(co
     //      it holds the bitmap of the run's entries and its word prefixes)
     __syncthreads();
     const int words = nt * (kTile / 32);
-    uint32_t* run_bits = reinterpret_cast<uint32_t*>(smem + L::kA);
-    int* run_prefix = reinterpret_cast<int*>(smem + L::kA + words * 4);
-    uint32_t* hist = reinterpret_cast<uint32_t*>(smem + L::kHist);
+    uint32_t* run_bits = reinterpret_cast<uint32_t*>(smem + ring_off);
+    int* run_prefix = reinterpret_cast<int*>(smem + ring_off + words * 4);
+    uint32_t* hist = reinterpret_cast<uint32_t*>(smem + ring_off + L::kHistR);
 #pragma unroll 1
     for (int qi = 0; qi < qn; ++qi) {
       const int n = cnt_s[qi];
@@ -702,24 +714,16 @@ __global__ void __launch_bounds__(kThreads, QH >= 16 ? 1 : 2) index_tc_kernel(co
     if (lf < 0 && tid == 0) report(p.status, LCS_ERR_DEVICE_GUARD);   // ticket not zero at the start
     if (lf != 1) return;
     __threadfence();
-    uint64_t* stage = reinterpret_cast<uint64_t*>(smem + L::kA);   // the ring is idle now
-    int* run_off = reinterpret_cast<int*>(smem + L::kRunOff);
-    // (the candidate buffers are idle now: they hold the selection's histogram, 2048 bins when
-    // there is room for them beside the gathered candidates, else 256 in the scratch)
-    constexpr int kHistBytes = 2048 * 4;
-    const int region = QPS * cap * 8;
+    // the candidate buffers and the ring are idle now: the lists are staged from the first on,
+    // the gathered candidates follow them
+    uint64_t* stage = cand_s;
+    int* run_off = reinterpret_cast<int*>(smem + ring_off + L::kRunOffR);
+    uint32_t* hist = reinterpret_cast<uint32_t*>(smem + ring_off + L::kHistR);
+    const int stage_cap = (ring_off + L::kHistR - L::kCand) / 8;
 #pragma unroll 1
-    for (int qi = 0; qi < qn; ++qi) {
-      if (region >= kHistBytes + 8 * 1024)
-        merge_query_topk<kThreads, 0, 11>(p.runs, qrow0 + qi, (n0 + qi + 1) >> mshift, k, stage,
-                                          (L::kSelAll - L::kA) / 8, cand_s + kHistBytes / 8,
-                                          (region - kHistBytes) / 8, run_off, reinterpret_cast<uint32_t*>(cand_s),
-                                          p.out_idx, p.out_cnt, sel_all);
-      else
-        merge_query_topk<kThreads, 0, 8>(p.runs, qrow0 + qi, (n0 + qi + 1) >> mshift, k, stage,
-                                         (L::kSelAll - L::kA) / 8, cand_s, region / 8, run_off, sel_all.hist,
-                                         p.out_idx, p.out_cnt, sel_all);
-    }
+    for (int qi = 0; qi < qn; ++qi)
+      merge_query_topk<kThreads, 0, 11>(p.runs, qrow0 + qi, (n0 + qi + 1) >> mshift, k, stage, stage_cap, nullptr,
+                                        -1, run_off, hist, p.out_idx, p.out_cnt, sel_all);
     if (tid == 0) {   // left at zero for the next call
       p.runs.ticket[(long long)b * gridDim.y + blockIdx.y] = 0;
       if (p.runs.gthr != nullptr)
@@ -773,6 +777,27 @@ size_t tc_smem_for(int heads, int qh, bool fused, int cap, int pages, int stages
     case 416: return tc_smem_bytes<4, 16>(fused, cap, pages, stages);
     case 808: return tc_smem_bytes<8, 8>(fused, cap, pages, stages);
     case 816: return tc_smem_bytes<8, 16>(fused, cap, pages, stages);
+    default: return 0;
+  }
+}
+
+template <int HI, int QH>
+size_t tc_stage_bytes(int cap, int stages) {
+  return stages == kStagesShallow ? TcSmem<QH, QH / HI, kStagesShallow>::stage_bytes(cap)
+                                  : TcSmem<QH, QH / HI, kStagesDeep>::stage_bytes(cap);
+}
+
+// bytes from the candidate buffers to the ring's histogram: the merge's staging room
+size_t tc_stage_bytes_for(int heads, int qh, int cap, int stages) {
+  switch (heads * 100 + qh) {
+    case 104: return tc_stage_bytes<1, 4>(cap, stages);
+    case 204: return tc_stage_bytes<2, 4>(cap, stages);
+    case 208: return tc_stage_bytes<2, 8>(cap, stages);
+    case 404: return tc_stage_bytes<4, 4>(cap, stages);
+    case 408: return tc_stage_bytes<4, 8>(cap, stages);
+    case 416: return tc_stage_bytes<4, 16>(cap, stages);
+    case 808: return tc_stage_bytes<8, 8>(cap, stages);
+    case 816: return tc_stage_bytes<8, 16>(cap, stages);
     default: return 0;
   }
 }
@@ -877,11 +902,14 @@ IndexTcPlan plan_index_tc(const IndexParams& p, int rank, int max_new, int max_e
       const int pages = tpc * kTile / epb + 1;
       const long long budget = std::min<long long>((long long)(228 * 1024 / occ) - 1024, 227 * 1024);
       const long long base = (long long)tc_smem_for(p.heads, pl.qh, fused, 0, pages, stages);
-      if (base + 8ll * qps * cap_min > budget) continue;
+      if ((long long)tc_smem_for(p.heads, pl.qh, fused, cap_min, pages, stages) > budget) continue;
       int cap = cap_min;
       if (fused) {   // more candidate room while it fits, up to a whole run's entries: fewer compactions
         const int fit = (int)((budget - base) / (8ll * qps)) / (2 * kTile) * (2 * kTile);
         cap = std::max(cap_min, std::min(fit, (tpc + 2) * kTile));
+        // (the ring after the buffers is 1024-aligned: give back room until the whole fits)
+        while (cap > cap_min && (long long)tc_smem_for(p.heads, pl.qh, fused, cap, pages, stages) > budget)
+          cap = std::max(cap_min, cap - 2 * kTile);
       }
       pl.runs = runs;
       pl.tpc = tpc;
@@ -893,12 +921,9 @@ IndexTcPlan plan_index_tc(const IndexParams& p, int rank, int max_new, int max_e
     if (!pl.applies) return pl;
     // the last CTA merges in place when the runs' lists fit its idle ring; a run's bitmap and word
     // prefixes fit it in any case (tpc * 128 entries: at most 8 bits of ring per entry)
-    const size_t stage_bytes = stages == kStagesShallow
-                                   ? (size_t)(TcSmem<16, 4, kStagesShallow>::kSelAll - TcSmem<16, 4, kStagesShallow>::kA)
-                                   : (size_t)(TcSmem<16, 4, kStagesDeep>::kSelAll - TcSmem<16, 4, kStagesDeep>::kA);
-    const size_t bitmap_bytes = stages == kStagesShallow
-                                    ? (size_t)(TcSmem<16, 4, kStagesShallow>::kHist - TcSmem<16, 4, kStagesShallow>::kA)
-                                    : (size_t)(TcSmem<16, 4, kStagesDeep>::kHist - TcSmem<16, 4, kStagesDeep>::kA);
+    const size_t stage_bytes = tc_stage_bytes_for(p.heads, pl.qh, pl.cap, stages);
+    const size_t bitmap_bytes = stages == kStagesShallow ? (size_t)TcSmem<16, 4, kStagesShallow>::kHistR
+                                                         : (size_t)TcSmem<16, 4, kStagesDeep>::kHistR;
     // lists with slack when they fit the ring, else exact ones
     pl.list_cap = fused && (size_t)pl.runs * topk_list_cap(k) * 8 <= stage_bytes ? topk_list_cap(k) : k;
     pl.merge_inline = fused && (size_t)pl.runs * pl.list_cap * 8 <= stage_bytes;
