@@ -924,8 +924,10 @@ IndexTcPlan plan_index_tc(const IndexParams& p, int rank, int max_new, int max_e
     const size_t stage_bytes = tc_stage_bytes_for(p.heads, pl.qh, pl.cap, stages);
     const size_t bitmap_bytes = stages == kStagesShallow ? (size_t)TcSmem<16, 4, kStagesShallow>::kHistR
                                                          : (size_t)TcSmem<16, 4, kStagesDeep>::kHistR;
-    // lists with slack when they fit the ring, else exact ones
-    pl.list_cap = fused && (size_t)pl.runs * topk_list_cap(k) * 8 <= stage_bytes ? topk_list_cap(k) : k;
+    // lists with slack (k/4, else k/8) when they fit the staging room, else exact ones
+    pl.list_cap = k;
+    for (const int lc : {topk_list_cap(k), k + (k >> 3)})
+      if (fused && pl.list_cap == k && (size_t)pl.runs * lc * 8 <= stage_bytes) pl.list_cap = lc;
     pl.merge_inline = fused && (size_t)pl.runs * pl.list_cap * 8 <= stage_bytes;
     pl.merge_smem = (size_t)kMergeStage + (size_t)pl.runs * pl.list_cap * 8;
     if (fused && (size_t)pl.tpc * kTile / 32 * 8 > bitmap_bytes) pl.applies = 0;

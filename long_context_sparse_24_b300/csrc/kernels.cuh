@@ -60,7 +60,7 @@ struct TopkRuns {
   int* cnt;         // [T][runs] keys in each run's list
   uint64_t* tau;    // [T][runs] the run's selection threshold (0 when it kept every candidate)
   uint64_t* keys;   // [T][runs][list_cap] each run's list, ascending entry index
-  int list_cap;     // keys a run's list holds at most (topk_list_cap(k), or k: exact lists)
+  int list_cap;     // keys a run's list holds at most (k + k/4, k + k/8, or k: exact lists)
   int* ticket;
   uint64_t* gthr;   // [T] the query's threshold shared by its runs (zero between calls), or null
 };
@@ -151,8 +151,8 @@ struct IndexTcPlan {
   int tpc;            // 128-entry tiles per CTA
   int cap;            // candidate buffer per query (fused)
   int stages;         // shared-memory ring depth
-  int list_cap;       // keys of a run's list: topk_list_cap(k) when the lists then still fit the
-                      // last CTA's ring, else k (exact per-run selection)
+  int list_cap;       // keys of a run's list: topk_list_cap(k), else k + k/8, when the lists then
+                      // still fit the last CTA's staging room, else k (exact per-run selection)
   int merge_inline;   // the sequence's last CTA merges (else the merge kernel)
   size_t smem;        // dynamic shared memory of the scorer
   size_t merge_smem;  // dynamic shared memory of the merge kernel
