@@ -225,34 +225,29 @@ __device__ void merge_query_topk(const TopkRuns& tr, long long q, int N, int k, 
     cand = stage + at;
     cand_cap = max(0, stage_cap - at);
   }
-  // stage the lists, a warp per run (16 loads in flight per lane), and gather the candidates
-  constexpr int kU = 16;
+  // stage the lists, a warp per run, by 8-byte asynchronous copies (every copy in flight at once,
+  // no registers held), then gather the candidates from the stage
   for (int r = warp; r < tr.runs; r += NT / 32) {
     const int o = run_off[r];
     const int c = min(run_off[r + 1], total) - o;
     const unsigned long long* src = keys + (long long)r * lcap;
-    for (int x0 = 0; x0 < c; x0 += 32 * kU) {
-      uint64_t v[kU];
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int x = x0 + u * 32 + lane;
-        v[u] = x < c ? __ldcg(src + x) : 0ull;
-      }
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int x = x0 + u * 32 + lane;
-        if (x < c) stage[o + x] = v[u];
-        const bool take = x < c && v[u] >= bound;
-        const unsigned m = __ballot_sync(0xffffffffu, take);
-        if (m != 0u) {
-          const int leader = __ffs(m) - 1;
-          int base = 0;
-          if (lane == leader) base = atomicAdd(&sc.count, __popc(m));
-          base = __shfl_sync(0xffffffffu, base, leader);
-          const int at = base + __popc(m & ((1u << lane) - 1u));
-          if (take && at < cand_cap) cand[at] = v[u];
-        }
-      }
+    for (int x = lane; x < c; x += 32)
+      asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(stage + o + x)), "l"(src + x) : "memory");
+  }
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  group_sync<NT, ID>();
+  for (int x0 = 0; x0 < total; x0 += NT) {   // (the same trip count on every thread)
+    const int x = x0 + tid;
+    const uint64_t u = x < total ? stage[x] : 0ull;
+    const bool take = x < total && u >= bound;
+    const unsigned m = __ballot_sync(0xffffffffu, take);
+    if (m != 0u) {
+      const int leader = __ffs(m) - 1;
+      int base = 0;
+      if (lane == leader) base = atomicAdd(&sc.count, __popc(m));
+      base = __shfl_sync(0xffffffffu, base, leader);
+      const int at = base + __popc(m & ((1u << lane) - 1u));
+      if (take && at < cand_cap) cand[at] = u;
     }
   }
   group_sync<NT, ID>();
