@@ -168,7 +168,9 @@ template <int HG>
 __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) {
   using L = TcAttSmem<HG>;
   constexpr int kQChunk = L::kQChunk;
-  constexpr int kVals = HG >= 32 ? HG / 32 : 1;   // per-lane values after a reduce-scatter
+  constexpr int HH = HG / 2;                       // heads a warp takes in the logit and P' passes
+  constexpr int kVals = HH >= 32 ? HH / 32 : 1;   // per-lane values after a reduce-scatter
+  static_assert(HH >= 8 && HH % 16 == 0, "two warps a TMEM lane quadrant, half the heads each");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -415,33 +417,33 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
                      smem_desc_sw128(sbase + L::kQ + c * kQChunk) + 2 * kk, kIdS, (c > 0 || kk > 0) ? 1u : 0u);
       tc_commit(bar_s);
     }
-    // ---- 4. warps 4-7: descriptors of tile tt + 2; warps 0-3: logits and the tile max per head
-    const int r = warp * 32 + lane;           // warps 0-3: tile row
-    const int hb = scatter_head<HG>(lane);
-    const bool hw_lane = scatter_writer<HG>(lane);
-    const bool rvalid = warp < 4 && r < trows && desc[dslot(tt) * kTileRows + (r & 127)] >= 0;
-    if (warp >= 4) {
-      if (tt + 2 < ntiles) desc[((tt + 2) % 3) * kTileRows + tid - 128] = make_desc(tt + 2, tid - 128);
-    } else {
-      ok = mbar_wait(bar_s, tt & 1, p.status, nullptr, p.wait_polls) && ok;
-      ok = __all_sync(0xffffffffu, ok);
-      tc_fence_after_sync();
-      if (ok) {
-        const float lsc = sscale[bp * kTileRows + r] * p.scale_log2;   // logit = s_r * S', base 2
-        float w[HG];
-        uint32_t u[HG / 16][16];   // every load in flight, one wait
+    // ---- 4. logits and the tile max per head: warp w takes the rows of TMEM lane quadrant w % 4
+    //      and half of the heads (w / 4); warps 4-7 also build the descriptors of tile tt + 2
+    const int quad = warp & 3, hhalf = warp >> 2;
+    const int r = quad * 32 + lane;           // tile row
+    const int hb = scatter_head<HH>(lane);
+    const bool hw_lane = scatter_writer<HH>(lane);
+    const bool rvalid = r < trows && desc[dslot(tt) * kTileRows + r] >= 0;
+    if (warp >= 4 && tt + 2 < ntiles) desc[((tt + 2) % 3) * kTileRows + tid - 128] = make_desc(tt + 2, tid - 128);
+    ok = mbar_wait(bar_s, tt & 1, p.status, nullptr, p.wait_polls) && ok;
+    ok = __all_sync(0xffffffffu, ok);
+    tc_fence_after_sync();
+    if (ok) {
+      const float lsc = sscale[bp * kTileRows + r] * p.scale_log2;   // logit = s_r * S', base 2
+      float w[HH];
+      uint32_t u[HH / 16][16];   // every load in flight, one wait
 #pragma unroll
-        for (int c16 = 0; c16 < HG / 16; ++c16) tmem_ld16(tm_s + ((uint32_t)(warp * 32) << 16) + c16 * 16, u[c16]);
-        tmem_ld_wait();
+      for (int c16 = 0; c16 < HH / 16; ++c16)
+        tmem_ld16(tm_s + ((uint32_t)(quad * 32) << 16) + hhalf * HH + c16 * 16, u[c16]);
+      tmem_ld_wait();
 #pragma unroll
-        for (int c16 = 0; c16 < HG / 16; ++c16)
+      for (int c16 = 0; c16 < HH / 16; ++c16)
 #pragma unroll
-          for (int j = 0; j < 16; ++j) w[c16 * 16 + j] = rvalid ? __uint_as_float(u[c16][j]) * lsc : -INFINITY;
-        reduce_scatter<HG, true>(w, lane);
-        if (hw_lane)
+        for (int j = 0; j < 16; ++j) w[c16 * 16 + j] = rvalid ? __uint_as_float(u[c16][j]) * lsc : -INFINITY;
+      reduce_scatter<HH, true>(w, lane);
+      if (hw_lane)
 #pragma unroll
-          for (int i = 0; i < kVals; ++i) red[warp * HG + hb + i] = w[i];
-      }
+        for (int i = 0; i < kVals; ++i) red[quad * HG + hhalf * HH + hb + i] = w[i];
     }
     ok = __syncthreads_and(ok);
     if (!ok) break;
@@ -458,29 +460,32 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
       if (tt > 0 && al < 1.0f) *rescale_flag = 1;
     }
     __syncthreads();
-    // ---- 6. warps 0-3: P' and the tile sum per head; warps 4-7: rescale O^T where the max grew
-    if (warp < 4) {
-      float w[HG];
+    // ---- 6. P' and the tile sum per head (warp w: its quadrant's rows, its half of the heads),
+    //      then, where the max grew, O^T rescaled (warp w: its quadrant's lanes, blocks of its half)
+    {
+      float w[HH];
       const float srow = sscale[bp * kTileRows + r] * kP2Scale;
       const float lsc = sscale[bp * kTileRows + r] * p.scale_log2;
       tc_fence_after_sync();
       {   // the logits again, from tensor memory (every load in flight, one wait)
-        uint32_t u[HG / 16][16];
+        uint32_t u[HH / 16][16];
 #pragma unroll
-        for (int c16 = 0; c16 < HG / 16; ++c16) tmem_ld16(tm_s + ((uint32_t)(warp * 32) << 16) + c16 * 16, u[c16]);
+        for (int c16 = 0; c16 < HH / 16; ++c16)
+          tmem_ld16(tm_s + ((uint32_t)(quad * 32) << 16) + hhalf * HH + c16 * 16, u[c16]);
         tmem_ld_wait();
 #pragma unroll
-        for (int c16 = 0; c16 < HG / 16; ++c16)
+        for (int c16 = 0; c16 < HH / 16; ++c16)
 #pragma unroll
           for (int j = 0; j < 16; ++j) w[c16 * 16 + j] = rvalid ? __uint_as_float(u[c16][j]) * lsc : -INFINITY;
       }
 #pragma unroll
-      for (int h = 0; h < HG; h += 2) {
+      for (int hl = 0; hl < HH; hl += 2) {
+        const int h = hhalf * HH + hl;
         const float m0 = mnew[h], m1 = mnew[h + 1];
-        const float a0 = m0 == -INFINITY ? 0.0f : exp2f(w[h] - m0);
-        const float a1 = m1 == -INFINITY ? 0.0f : exp2f(w[h + 1] - m1);
-        w[h] = a0;
-        w[h + 1] = a1;
+        const float a0 = m0 == -INFINITY ? 0.0f : exp2f(w[hl] - m0);
+        const float a1 = m1 == -INFINITY ? 0.0f : exp2f(w[hl + 1] - m1);
+        w[hl] = a0;
+        w[hl + 1] = a1;
         // P'[h][r], [h+1][r]: K-major, chunk r/64, piece (r%64)/8 of head row h, element r%8
         const int pc = r >> 6, pj = (r & 63) >> 3, pe = r & 7;
         *reinterpret_cast<__half*>(smem + L::kP + pc * kQChunk + h * 128 + ((pj ^ (h & 7)) << 4) + pe * 2) =
@@ -488,24 +493,26 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
         *reinterpret_cast<__half*>(smem + L::kP + pc * kQChunk + (h + 1) * 128 + ((pj ^ ((h + 1) & 7)) << 4) + pe * 2) =
             __float2half_rn(a1 * srow);
       }
-      reduce_scatter<HG, false>(w, lane);
+      reduce_scatter<HH, false>(w, lane);
       if (hw_lane)
 #pragma unroll
-        for (int i = 0; i < kVals; ++i) red[warp * HG + hb + i] = w[i];
-    } else if (*rescale_flag) {
-      const int quad = warp & 3;
+        for (int i = 0; i < kVals; ++i) red[quad * HG + hhalf * HH + hb + i] = w[i];
+    }
+    if (*rescale_flag) {
 #pragma unroll 1
-      for (int mb = 0; mb < 4; ++mb)
-#pragma unroll 1
-        for (int c16 = 0; c16 < HG / 16; ++c16) {
-          const uint32_t ta = tm_o + HG * mb + ((uint32_t)(quad * 32) << 16) + c16 * 16;
-          uint32_t u[16];
-          tmem_ld16(ta, u);
-          tmem_ld_wait();
+      for (int cc = 0; cc < 2 * (HG / 32); ++cc) {   // two 16-column chunks at a time, one wait
+        const int mb = 2 * hhalf + cc / (HG / 32), c0 = (cc % (HG / 32)) * 2;
+        uint32_t u[2][16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) u[j] = __float_as_uint(__uint_as_float(u[j]) * alpha_s[c16 * 16 + j]);
-          tmem_st16(ta, u);
+        for (int c = 0; c < 2; ++c) tmem_ld16(tm_o + HG * mb + ((uint32_t)(quad * 32) << 16) + (c0 + c) * 16, u[c]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) u[c][j] = __float_as_uint(__uint_as_float(u[c][j]) * alpha_s[(c0 + c) * 16 + j]);
+          tmem_st16(tm_o + HG * mb + ((uint32_t)(quad * 32) << 16) + (c0 + c) * 16, u[c]);
         }
+      }
       tmem_st_wait();
     }
     fence_proxy_async_smem();
