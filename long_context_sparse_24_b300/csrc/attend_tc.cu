@@ -410,11 +410,14 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
     tc_fence_after_sync();
     // ---- 3. S'^T = R' . Q^T
     if (tid == 0) {
+      // (descriptors: the base ones plus constant offsets of the start-address field)
+      const uint64_t da = smem_desc_sw128(sbase + L::kT), db = smem_desc_sw128(sbase + L::kQ);
+#pragma unroll
       for (int c = 0; c < 8; ++c)
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          tc_mma_f16(tm_s, smem_desc_sw128(sbase + L::kT + c * kChunk) + 2 * kk,
-                     smem_desc_sw128(sbase + L::kQ + c * kQChunk) + 2 * kk, kIdS, (c > 0 || kk > 0) ? 1u : 0u);
+          tc_mma_f16(tm_s, da + (uint64_t)((c * kChunk) >> 4) + 2 * kk, db + (uint64_t)((c * kQChunk) >> 4) + 2 * kk,
+                     kIdS, (c > 0 || kk > 0) ? 1u : 0u);
       tc_commit(bar_s);
     }
     // ---- 4. logits and the tile max per head: warp w takes the rows of TMEM lane quadrant w % 4
@@ -525,12 +528,13 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(AttendParams p) 
       mrow[tid] = mnew[tid];
     }
     if (tid == 0) {
+      const uint64_t da = desc_mn_sw128(sbase + L::kT, kChunk, 1024), db = smem_desc_sw128(sbase + L::kP);
+#pragma unroll
       for (int mb = 0; mb < 4; ++mb)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)   // 16 rows per step: two 8-row groups
-          tc_mma_f16(tm_o + HG * mb, desc_mn_sw128(sbase + L::kT + 2 * mb * kChunk + kk * 2048, kChunk, 1024),
-                     smem_desc_sw128(sbase + L::kP + (kk >> 2) * kQChunk) + 2 * (kk & 3), kIdO,
-                     (tt > 0 || kk > 0) ? 1u : 0u);
+          tc_mma_f16(tm_o + HG * mb, da + (uint64_t)((2 * mb * kChunk + kk * 2048) >> 4),
+                     db + (uint64_t)(((kk >> 2) * kQChunk) >> 4) + 2 * (kk & 3), kIdO, (tt > 0 || kk > 0) ? 1u : 0u);
       tc_commit(bar_pv);
     }
   }

@@ -318,11 +318,14 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc1_kernel(AttendParams p)
   // ---- S'^T = R' . Q^T: 8 chunks x 4 steps of 16 dims
   if (tid == 0) {
     tc_fence_after_sync();
+    // (descriptors: the base ones plus constant offsets of the start-address field)
+    const uint64_t da = smem_desc_sw128(sbase + L::kT), db = smem_desc_sw128(sbase + L::kQ);
+#pragma unroll
     for (int c = 0; c < 8; ++c)
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)
-        tc_mma_f16(tm_s, smem_desc_sw128(sbase + L::kT + c * kChunk) + 2 * kk,
-                   smem_desc_sw128(sbase + L::kQ + c * kQChunk) + 2 * kk, kIdS, (c > 0 || kk > 0) ? 1u : 0u);
+        tc_mma_f16(tm_s, da + (uint64_t)((c * kChunk) >> 4) + 2 * kk, db + (uint64_t)((c * kQChunk) >> 4) + 2 * kk,
+                   kIdS, (c > 0 || kk > 0) ? 1u : 0u);
     tc_commit(bar_s);
   }
   bool ok = mbar_wait(bar_s, 0, p.status, nullptr, p.wait_polls);
@@ -382,11 +385,13 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc1_kernel(AttendParams p)
   // ---- O^T = R'^T . P'^T: four 128-dim blocks x 8 steps of 16 rows
   if (tid == 0 && ok) {
     tc_fence_after_sync();
+    const uint64_t da = desc_mn_sw128(sbase + L::kT, kChunk, 1024), db = smem_desc_sw128(sbase + L::kP);
+#pragma unroll
     for (int mb = 0; mb < 4; ++mb)
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        tc_mma_f16(tm_o + 64 * mb, desc_mn_sw128(sbase + L::kT + 2 * mb * kChunk + kk * 2048, kChunk, 1024),
-                   smem_desc_sw128(sbase + L::kP + (kk >> 2) * kQChunk) + 2 * (kk & 3), kIdO, kk > 0 ? 1u : 0u);
+        tc_mma_f16(tm_o + 64 * mb, da + (uint64_t)((2 * mb * kChunk + kk * 2048) >> 4),
+                   db + (uint64_t)(((kk >> 2) * kQChunk) >> 4) + 2 * (kk & 3), kIdO, kk > 0 ? 1u : 0u);
     tc_commit(bar_pv);
   }
   if (ok) ok = mbar_wait(bar_pv, 0, p.status, nullptr, p.wait_polls);
