@@ -398,8 +398,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc1_kernel(AttendParams p)
   ok = __syncthreads_and(ok);
   tc_fence_after_sync();
 
-  // ---- epilogue: warp w reads lanes 32*(w%4) (dims) of blocks 2*(w/4), 2*(w/4)+1, transposes
-  //      them through its own 8 KB of the query buffer and writes 16-byte pieces
+  // ---- epilogue: warp w reads lanes 32*(w%4) (dims) of blocks 2*(w/4), 2*(w/4)+1 and writes each
+  //      head's 32 dims straight from the registers (64 contiguous bytes a warp and head)
   float* inv_s = reinterpret_cast<float*>(smem + L::kInv);
   for (int h = tid; h < kHeads; h += kThreads)
     inv_s[h] = p.splits == 1 ? softmax_norm(mrow[h], lrow[h], h0 + h < H ? p.sink : nullptr, h0 + h).f / kP2Scale
@@ -407,37 +407,28 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc1_kernel(AttendParams p)
   __syncthreads();
   if (ok) {
     const int quad = warp & 3;
-    float* tb = reinterpret_cast<float*>(smem + L::kQ) + warp * (kHeads * 32);   // [64 heads][32 dims]
+    __nv_bfloat16* base = p.splits == 1 ? p.out + (long long)q * H * kD : p.ws_ob + (long long)q * H * p.splits * kD;
+    const long long hstride = p.splits == 1 ? kD : (long long)p.splits * kD;   // between heads
+    const long long soff = p.splits == 1 ? 0 : (long long)split * kD;
+    const int hn = min(kHeads, H - h0);   // heads of this group that exist
     for (int bi = 0; bi < 2; ++bi) {
       const int mb = 2 * (warp >> 2) + bi;
-      const int dim0 = mb * 128 + quad * 32;
-      uint32_t v[kHeads / 16][16];   // the four loads in flight together, one wait
+      __nv_bfloat16* o = base + (long long)h0 * hstride + soff + mb * 128 + quad * 32 + lane;
+#pragma unroll 1
+      for (int c2 = 0; c2 < kHeads / 32; ++c2) {   // 32 heads: two loads in flight, one wait
+        uint32_t v[2][16];
 #pragma unroll
-      for (int c16 = 0; c16 < kHeads / 16; ++c16)
-        tmem_ld16(tm_o + 64 * mb + ((uint32_t)(quad * 32) << 16) + c16 * 16, v[c16]);
-      tmem_ld_wait();
+        for (int c = 0; c < 2; ++c)
+          tmem_ld16(tm_o + 64 * mb + ((uint32_t)(quad * 32) << 16) + (2 * c2 + c) * 16, v[c]);
+        tmem_ld_wait();
 #pragma unroll
-      for (int c16 = 0; c16 < kHeads / 16; ++c16)
+        for (int c = 0; c < 2; ++c)
 #pragma unroll
-        for (int j = 0; j < 16; ++j) tb[(c16 * 16 + j) * 32 + lane] = __uint_as_float(v[c16][j]) * inv_s[c16 * 16 + j];
-      __syncwarp();
-#pragma unroll 4
-      for (int i = 0; i < kHeads / 4; ++i) {
-        const int h = i * 4 + (lane >> 3), d4 = (lane & 7) * 4;
-        if (h0 + h < H) {
-          const float4 o = *reinterpret_cast<const float4*>(tb + h * 32 + d4);
-          if (p.splits == 1) {
-            __nv_bfloat162 lo = __floats2bfloat162_rn(o.x, o.y), hi = __floats2bfloat162_rn(o.z, o.w);
-            uint2 pk = make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
-            *reinterpret_cast<uint2*>(p.out + ((long long)q * H + h0 + h) * kD + dim0 + d4) = pk;
-          } else {
-            __nv_bfloat162 lo = __floats2bfloat162_rn(o.x, o.y), hi = __floats2bfloat162_rn(o.z, o.w);
-            uint2 pk = make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
-            *reinterpret_cast<uint2*>(p.ws_ob + (((long long)q * H + h0 + h) * p.splits + split) * kD + dim0 + d4) = pk;
+          for (int j = 0; j < 16; ++j) {
+            const int h = (2 * c2 + c) * 16 + j;
+            if (h < hn) o[h * hstride] = __float2bfloat16_rn(__uint_as_float(v[c][j]) * inv_s[h]);
           }
-        }
       }
-      __syncwarp();
     }
     for (int h = tid; h < kHeads; h += kThreads) {
       if (h0 + h >= H) continue;
