@@ -33,9 +33,9 @@ METRIC = "CSA/HCA attention queries/s at 128K-1M ctx"
 # workload, from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum), together with
 # the hash of the kernel sources they were taken on: when the sources differ from that hash the
 # counters no longer describe the kernels that run and `traffic` is reported as null.
-TRAFFIC = {"source_sha1": "d7b5be74e26c0ea32f9432cb4d5eaf2a47197a50",
-           "attend": 29757867,    # attend_tc1_kernel (top-k part 14.50 MB + window part 4.68 MB) + combine 10.58 MB
-           "index": 71708843}     # index_tc_kernel<4, 4, 1, 6>: 71.62 MB read + 0.09 MB written (mean of 3 launches)
+TRAFFIC = {"source_sha1": "5f6d294e3797af814dc9b4ca91cf0c83d9bd7add",
+           "attend": 29762731,    # attend_tc1_kernel (top-k part 14.50 MB + window part 4.68 MB) + combine 10.58 MB
+           "index": 71670272}     # index_tc_kernel<4, 4, 1, 6>: 71.62 MB read + 0.05 MB written (mean of 3 launches)
 UNIT = "queries/s"
 
 
