@@ -36,7 +36,17 @@ __global__ void __launch_bounds__(256) stage_copy_kernel(const __grid_constant__
     const unsigned long long n16 = n >> 4;
     const uint4* s4 = reinterpret_cast<const uint4*>(src);
     uint4* d4 = reinterpret_cast<uint4*>(dst);
-    for (unsigned long long k = tid; k < n16; k += stride) d4[k] = s4[k];
+    // four pieces a thread loaded before any is stored: their reads (host memory over the link,
+    // for pinned sources) are in flight together
+    for (unsigned long long k0 = tid; k0 < n16; k0 += 4 * stride) {
+      uint4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (k0 + u * stride < n16) v[u] = s4[k0 + u * stride];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (k0 + u * stride < n16) d4[k0 + u * stride] = v[u];
+    }
     for (unsigned long long k = (n16 << 4) + tid; k < n; k += stride) dst[k] = src[k];
   } else {
     for (unsigned long long k = tid; k < n; k += stride) dst[k] = src[k];
