@@ -33,9 +33,9 @@ METRIC = "CSA/HCA attention queries/s at 128K-1M ctx"
 # workload, from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum), together with
 # the hash of the kernel sources they were taken on: when the sources differ from that hash the
 # counters no longer describe the kernels that run and `traffic` is reported as null.
-TRAFFIC = {"source_sha1": "41a0418ef7c7f505a066903b121411237af40246",
-           "attend": 29763499,    # attend_tc1_kernel (top-k part 14.50 MB + window part 4.68 MB) + combine 10.58 MB
-           "index": 71680341}     # index_tc_kernel<4, 4, 1, 6>: 71.62 MB read + 0.06 MB written (mean of 3 launches)
+TRAFFIC = {"source_sha1": "ed92e68e5bf6e37899e63376ba67e52d88c4cbef",
+           "attend": 29762901,    # attend_tc1_kernel (top-k part 14.50 MB + window part 4.68 MB) + combine 10.58 MB
+           "index": 71652181}     # index_tc_kernel<4, 4, 1, 6>: 71.60 MB read + 0.05 MB written (mean of 3 launches)
 UNIT = "queries/s"
 
 

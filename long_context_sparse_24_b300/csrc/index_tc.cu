@@ -72,7 +72,7 @@ constexpr int kEpiWarps = 8;        // two per TMEM lane quadrant, the two tiles
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kProdWarps = 2;       // producer warps, alternating tiles
 constexpr int kThreads = kEpiThreads + 32 * kProdWarps + 32;
-constexpr int kCandPerThread = 16;  // keys a thread holds in registers in one block of a compaction
+constexpr int kCandPerThread = 8;  // keys a thread holds in registers in one block of a compaction
 constexpr int kEpiBarrier = 1;      // named barrier of the epilogue warps
 constexpr int kMaxRuns = 256;       // CTAs per sequence (run lists a merge reads)
 
@@ -176,13 +176,14 @@ __device__ int write_run_sorted(const uint64_t* buf, int n, uint64_t tau, int j0
 // sorted too: they are staged in shared memory (stage: room for stage_cap keys), the k-th largest
 // key is selected, and the staged keys at or above it are read out in that order.  Every run
 // recorded a threshold at most the query's k-th largest key (at least k of the run's keys, or all
-// of them, are at or above it), with all of its keys at or above it in its list; the largest of those bounds the selection from below, so the keys at or above it
-// are gathered as candidates while staging (cand: room for cand_cap keys; when more pass, the
-// selection runs over the stage).  N: visible entries of the query; run_off: runs + 1 ints of
-// shared memory; hist: 1 << BITS counters of shared memory.
+// of them, are at or above it), with all of its keys at or above it in its list; the largest of
+// those bounds the selection from below (the selection reads the stage and leaves out the keys
+// under the bound: with a few runs a query nearly all staged keys pass it, so gathering the
+// candidates first would cost a pass and save none).  N: visible entries of the query; run_off:
+// runs + 1 ints of shared memory; hist: 1 << BITS counters of shared memory.
 template <int NT, int ID, int BITS>
 __device__ void merge_query_topk(const TopkRuns& tr, long long q, int N, int k, uint64_t* stage, int stage_cap,
-                                 uint64_t* cand, int cand_cap, int* run_off, uint32_t* hist, int32_t* out_idx,
+                                 int* run_off, uint32_t* hist, int32_t* out_idx,
                                  int32_t* out_cnt, SelScratch<NT>& sc) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int32_t* out = out_idx + q * k;
@@ -209,10 +210,7 @@ __device__ void merge_query_topk(const TopkRuns& tr, long long q, int N, int k, 
     int tot;
     const int incl = group_scan_incl<NT, ID>(c, sc.warp_tot, &tot);   // (its barriers publish span)
     if (tid < tr.runs) run_off[tid] = incl - c;
-    if (tid == 0) {
-      run_off[tr.runs] = tot;
-      sc.count = 0;
-    }
+    if (tid == 0) run_off[tr.runs] = tot;
     unsigned long long bmax = 0ull;
 #pragma unroll
     for (int w = 0; w < NT / 32; ++w) bmax = sc.span[w] > bmax ? sc.span[w] : bmax;
@@ -220,13 +218,8 @@ __device__ void merge_query_topk(const TopkRuns& tr, long long q, int N, int k, 
   }
   group_sync<NT, ID>();
   const int total = min(run_off[tr.runs], stage_cap);   // (the host sizes the stage for every list)
-  if (cand_cap < 0) {   // the candidates go right after the staged lists
-    const int at = (total + 1) & ~1;
-    cand = stage + at;
-    cand_cap = max(0, stage_cap - at);
-  }
   // stage the lists, a warp per run, by 8-byte asynchronous copies (every copy in flight at once,
-  // no registers held), then gather the candidates from the stage
+  // no registers held)
   for (int r = warp; r < tr.runs; r += NT / 32) {
     const int o = run_off[r];
     const int c = min(run_off[r + 1], total) - o;
@@ -236,28 +229,8 @@ __device__ void merge_query_topk(const TopkRuns& tr, long long q, int N, int k, 
   }
   asm volatile("cp.async.wait_all;" ::: "memory");
   group_sync<NT, ID>();
-  for (int x0 = 0; x0 < total; x0 += NT) {   // (the same trip count on every thread)
-    const int x = x0 + tid;
-    const uint64_t u = x < total ? stage[x] : 0ull;
-    const bool take = x < total && u >= bound;
-    const unsigned m = __ballot_sync(0xffffffffu, take);
-    if (m != 0u) {
-      const int leader = __ffs(m) - 1;
-      int base = 0;
-      if (lane == leader) base = atomicAdd(&sc.count, __popc(m));
-      base = __shfl_sync(0xffffffffu, base, leader);
-      const int at = base + __popc(m & ((1u << lane) - 1u));
-      if (take && at < cand_cap) cand[at] = u;
-    }
-  }
-  group_sync<NT, ID>();
-  const int nc = sc.count;
-  group_sync<NT, ID>();
   // (fewer than k keys only when the scoring gave up on a bounded wait: take them all)
-  uint64_t tau = 0ull;
-  if (total > k)
-    tau = nc <= cand_cap ? kth_largest_key<NT, ID, BITS>(cand, nc, k, sc, hist)
-                         : kth_largest_key<NT, ID, BITS>(stage, total, k, sc, hist, bound);
+  const uint64_t tau = total > k ? kth_largest_key<NT, ID, BITS>(stage, total, k, sc, hist, bound) : 0ull;
   // ascending read-out: thread t takes stage positions [t*ppt, (t+1)*ppt)
   const int ppt = (total + NT - 1) / NT;
   const int x0 = min(total, tid * ppt), x1 = min(total, x0 + ppt);
@@ -265,12 +238,16 @@ __device__ void merge_query_topk(const TopkRuns& tr, long long q, int N, int k, 
   for (int x = x0; x < x1; ++x) mine += stage[x] >= tau ? 1 : 0;
   int tot;
   int pos = group_scan_incl<NT, ID>(mine, sc.warp_tot, &tot) - mine;
-  for (int x = x0; x < x1; ++x) {
-    const uint64_t u = stage[x];
-    if (u >= tau) {
-      if (pos < k) out[pos] = (int32_t)~(uint32_t)u;
-      ++pos;
-    }
+  for (int xb = x0; xb < x1; xb += 8) {   // (8 keys read before their stores: the loads overlap)
+    uint64_t v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) v[u] = xb + u < x1 ? stage[xb + u] : 0ull;
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      if (xb + u < x1 && v[u] >= tau) {
+        if (pos < k) out[pos] = (int32_t)~(uint32_t)v[u];
+        ++pos;
+      }
   }
   for (int j = tot + tid; j < k; j += NT) out[j] = -1;   // (tot == k for exact selections)
   if (tid == 0) out_cnt[q] = min(tot, k);
@@ -638,13 +615,10 @@ __global__ void __launch_bounds__(kThreads, QH >= 16 ? 1 : 2) index_tc_kernel(co
             const int kept = compact_keys_ge<kEpiThreads, kEpiBarrier, kCandPerThread>(buf, n, tau, sel);
             if (tid == 0) {
               cnt_s[qi] = kept;
-              uint64_t t = tau;   // (published to the query's other runs)
-              if (share) {
-                const unsigned long long o =
-                    atomicMax(reinterpret_cast<unsigned long long*>(p.runs.gthr) + qrow0 + qi, (unsigned long long)t);
-                t = o > t ? o : t;
-              }
-              thr_s[qi] = t;
+              thr_s[qi] = tau;
+              // published to the query's other runs (theirs reach this run through the shared
+              // threshold's read an iteration ahead: nothing waits for the atomic)
+              if (share) atomicMax(reinterpret_cast<unsigned long long*>(p.runs.gthr) + qrow0 + qi, (unsigned long long)tau);
             }
             group_sync<kEpiThreads, kEpiBarrier>();
           }
@@ -709,16 +683,15 @@ __global__ void __launch_bounds__(kThreads, QH >= 16 ? 1 : 2) index_tc_kernel(co
     if (lf < 0 && tid == 0) report(p.status, LCS_ERR_DEVICE_GUARD);   // ticket not zero at the start
     if (lf != 1) return;
     __threadfence();
-    // the candidate buffers and the ring are idle now: the lists are staged from the first on,
-    // the gathered candidates follow them
+    // the candidate buffers and the ring are idle now: the lists are staged from the first on
     uint64_t* stage = cand_s;
     int* run_off = reinterpret_cast<int*>(smem + ring_off + L::kRunOffR);
     uint32_t* hist = reinterpret_cast<uint32_t*>(smem + ring_off + L::kHistR);
     const int stage_cap = (ring_off + L::kHistR - L::kCand) / 8;
 #pragma unroll 1
     for (int qi = 0; qi < qn; ++qi)
-      merge_query_topk<kThreads, 0, 11>(p.runs, qrow0 + qi, (n0 + qi + 1) >> mshift, k, stage, stage_cap, nullptr,
-                                        -1, run_off, hist, p.out_idx, p.out_cnt, sel_all);
+      merge_query_topk<kThreads, 0, 11>(p.runs, qrow0 + qi, (n0 + qi + 1) >> mshift, k, stage, stage_cap, run_off,
+                                        hist, p.out_idx, p.out_cnt, sel_all);
     if (tid == 0) {   // left at zero for the next call
       p.runs.ticket[(long long)b * gridDim.y + blockIdx.y] = 0;
       if (p.runs.gthr != nullptr)
@@ -745,8 +718,8 @@ __global__ void __launch_bounds__(256) topk_merge_kernel(IndexParams p) {
   uint64_t* stage = reinterpret_cast<uint64_t*>(merge_smem + kMergeStage);
   const int t = sp.n0() + i;
   // (the stage holds the lists; the selection reads them with the lower bound, no candidate array)
-  merge_query_topk<256, 0, 11>(p.runs, sp.q0 + i, (t + 1) / p.m, p.top_k, stage, p.runs.runs * p.runs.list_cap, nullptr, 0,
-                               run_off, hist, p.out_idx, p.out_cnt, sc);
+  merge_query_topk<256, 0, 11>(p.runs, sp.q0 + i, (t + 1) / p.m, p.top_k, stage, p.runs.runs * p.runs.list_cap, run_off,
+                               hist, p.out_idx, p.out_cnt, sc);
   if (threadIdx.x == 0 && p.runs.gthr != nullptr) p.runs.gthr[sp.q0 + i] = 0ull;   // left at zero
 }
 

@@ -76,6 +76,7 @@ template <int NT, int ID, int BITS>
 __device__ SelResult select_top(const uint64_t* buf, int n, int k, int slack, SelScratch<NT>& sc, uint32_t* hist,
                                 uint64_t lo = 0ull) {
   constexpr int B = 1 << BITS;
+  constexpr int kBatch = 8;
   constexpr int PER = (B + NT - 1) / NT;   // bins a thread scans, in descending order
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   unsigned long long kmax = 0ull, kmin = ~0ull;
@@ -113,9 +114,16 @@ __device__ SelResult select_top(const uint64_t* buf, int n, int k, int slack, Se
   for (;;) {
     const uint64_t hi_mask = shift + width >= 64 ? 0ull : (~0ull << (shift + width));
     const uint32_t dmask = (1u << width) - 1u;
-    for (int i = tid; i < n; i += NT) {
-      const uint64_t u = buf[i];
-      if (u >= lo && (u & hi_mask) == prefix) atomicAdd(&hist[(uint32_t)(u >> shift) & dmask], 1u);
+    // a thread's keys are read kBatch at a time before any counter is touched, so that their
+    // loads overlap (a load of buf cannot be moved above an atomic on hist: both are shared memory)
+    for (int i0 = tid; i0 < n; i0 += NT * kBatch) {
+      uint64_t v[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) v[u] = i0 + u * NT < n ? buf[i0 + u * NT] : 0ull;
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u)
+        if (i0 + u * NT < n && v[u] >= lo && (v[u] & hi_mask) == prefix)
+          atomicAdd(&hist[(uint32_t)(v[u] >> shift) & dmask], 1u);
     }
     group_sync<NT, ID>();
     // thread t scans bins B-1-t*PER down to B-(t+1)*PER
@@ -180,31 +188,32 @@ __device__ __forceinline__ void warp_append(bool take, uint64_t key, uint64_t* b
 }
 
 // Keeps the keys >= tau of buf[0..n) (order not kept); returns how many remain.  The keys go in
-// blocks of NT * MAXPER: a block is read into registers before any of its keys is written back,
-// and a kept key lands below the end of its own block (no more keys are kept than were read), so
-// it only overwrites keys already read.
+// blocks of NT * MAXPER: a block is read into registers, a prefix sum over the group gives every
+// thread the place of its kept keys, and the writes start once the whole block has been read (the
+// scan's barriers); a kept key lands below the end of its own block (no more keys are kept than
+// were read), so it only overwrites keys already read.
 template <int NT, int ID, int MAXPER>
 __device__ int compact_keys_ge(uint64_t* buf, int n, uint64_t tau, SelScratch<NT>& sc) {
   const int tid = threadIdx.x;
-  if (tid == 0) sc.count = 0;
+  int kept = 0;   // (the same on every thread)
   for (int b0 = 0; b0 < n; b0 += NT * MAXPER) {
     uint64_t v[MAXPER];
+    int mine = 0;
 #pragma unroll
     for (int s = 0; s < MAXPER; ++s) {
       const int i = b0 + tid + s * NT;
       v[s] = i < n ? buf[i] : 0ull;
+      mine += i < n && v[s] >= tau ? 1 : 0;
     }
-    group_sync<NT, ID>();
+    int tot;
+    int pos = kept + group_scan_incl<NT, ID>(mine, sc.warp_tot, &tot) - mine;
 #pragma unroll
-    for (int s = 0; s < MAXPER; ++s) {
-      const int i = b0 + tid + s * NT;
-      warp_append(i < n && v[s] >= tau, v[s], buf, &sc.count);
-    }
+    for (int s = 0; s < MAXPER; ++s)
+      if (b0 + tid + s * NT < n && v[s] >= tau) buf[pos++] = v[s];
+    kept += tot;
   }
   group_sync<NT, ID>();
-  const int r = sc.count;
-  group_sync<NT, ID>();
-  return r;
+  return kept;
 }
 
 }  // namespace lcsa
