@@ -263,7 +263,20 @@ def _check_csa_query(lay, seed, s_, t, row, q_np, qc, qs, hw, w, b, out_row, lab
 def test_csa_decode_32x128k_full_size_sampled():
     """32 sequences x 131,072 cached tokens, 64 heads, D=512, k=512: one decode step; sequences
     0, 13 and 31 checked against the oracle (top-k bit-exact, outputs)."""
-    wl = synth.CONFIGS["csa_decode"]
+    _csa_decode_full_size_sampled("csa_decode", (0, 13, 31))
+
+
+def test_csa_decode_32x1m_full_size_sampled():
+    """32 sequences x 1,048,576 cached tokens, 64 heads, D=512, k=1024 (the 1M-context decode
+    workload): one decode step in the layer driver's launch configuration, where each of the fused
+    scorer's runs cuts its candidate buffer during the scan and the query's last CTA merges nine
+    run lists; sequences 0, 17 and 31 checked against the oracle (top-k over 262,144 entries
+    bit-exact, outputs)."""
+    _csa_decode_full_size_sampled("csa_decode_1m", (0, 17, 31))
+
+
+def _csa_decode_full_size_sampled(name, sampled):
+    wl = synth.CONFIGS[name]
     seed, S, L, H, D, m, k, hi, r = wl.seed, wl.num_seqs, wl.ctx_len, wl.heads, wl.dim, wl.m, wl.top_k, \
         wl.index_heads, wl.index_rank
     lay = Layer("csa", S, L + 256, H, D, lcsa.LCS_ROW_FP8_SPLIT, m, top_k=k, index_heads=hi, index_rank=r,
@@ -287,9 +300,9 @@ def test_csa_decode_32x128k_full_size_sampled():
     assert int(lay.status.item()) == 0
     o = out.float().cpu().numpy().astype(np.float64)
     w64, b64 = w.astype(np.float64), b.astype(np.float64)
-    for s_ in (0, 13, 31):
+    for s_ in sampled:
         q, qc, qs, hw = ins[s_]
-        _check_csa_query(lay, seed, s_, L, s_, q[0], qc, qs, hw, w64, b64, o[s_], f"seq {s_}")
+        _check_csa_query(lay, seed, s_, L, s_, q[0], qc, qs, hw, w64, b64, o[s_], f"{name} seq {s_}")
     del lay, out
     torch.cuda.empty_cache()
 
