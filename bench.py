@@ -232,9 +232,10 @@ def kernel_source_sha1() -> str:
     return h.hexdigest()
 
 
-def traffic_of(part: str):
-    """ncu DRAM bytes of `part` if they were captured on the kernel sources that run, else None."""
-    if TRAFFIC.get("source_sha1") and TRAFFIC["source_sha1"] == kernel_source_sha1():
+def traffic_of(part: str, workload: str):
+    """ncu DRAM bytes of `part` if they were captured on the kernel sources that run and on this
+    workload (the table holds the csa_decode step's), else None."""
+    if workload == WL.name and TRAFFIC.get("source_sha1") and TRAFFIC["source_sha1"] == kernel_source_sha1():
         return TRAFFIC.get(part)
     return None
 
@@ -445,9 +446,10 @@ def run_gpu(args, rank, world, local, wl=None):
 
     timing = "CUDA events around the call(s) in a serialised copy of the step (event nodes in a CUDA graph)"
     roofline_att = roof("csa_attend_window + csa_attend_topk (attention kernels incl. the merge)", att_bytes,
-                        att_ms, traffic_of("attend"), timing)
+                        att_ms, traffic_of("attend", wl.name), timing)
     roofline_att["flop_per_step"] = int(S * 4 * H * D * (k + 128))
-    roofline_idx = roof("csa_index_topk (scorer and selection)", idx_bytes, idx_ms, traffic_of("index"), timing)
+    roofline_idx = roof("csa_index_topk (scorer and selection)", idx_bytes, idx_ms, traffic_of("index", wl.name),
+                        timing)
     roofline_step = roof("whole step (compression, indexer, attention)", step_bytes, ms, None,
                          "CUDA events around each timed step (the graph as it runs)")
     # the dominant stage by device time is the line's roofline; the other stage and the whole step beside it
